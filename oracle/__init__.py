@@ -1,0 +1,315 @@
+"""CPU oracle for INT8-QK quantized attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  It shares no code with the CUDA
+library and never imports it; the only thing both sides share is the
+seeded input generator, which holds none of the method's arithmetic.
+
+The arithmetic lives in ``sage_oracle.c`` (plain C, fp32 quantisation
+decisions, exact integer dot products, fp64 softmax).  This module only
+marshals numpy arrays, performs the paged-cache gather (a pure index
+lookup) and runs independent (batch, head) problems on a thread pool.
+
+Sources, by page title and section:
+  [P1] "INT8 QK MMAC on gfx936 DCU: paged access, fragment mapping and GQA"
+  [P3] "SageAttention -- MetaX MXMACA port" README
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+from . import build as _build
+
+_LIB = None
+_vp = ctypes.c_void_p
+_i64 = ctypes.c_int64
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        lib = ctypes.CDLL(_build.build())
+        lib.oracle_quant_int8.argtypes = [_vp, _i64, _i64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp]
+        lib.oracle_quant_int8.restype = None
+        lib.oracle_token_mean.argtypes = [_vp, _i64, _i64, ctypes.c_int, _vp]
+        lib.oracle_token_mean.restype = None
+        lib.oracle_row_bias.argtypes = [_vp, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp]
+        lib.oracle_row_bias.restype = None
+        lib.oracle_qk_int32.argtypes = [_vp, _i64, _vp, _i64, ctypes.c_int, _vp]
+        lib.oracle_qk_int32.restype = _i64
+        lib.oracle_attend.argtypes = [_i64, ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp,
+                                      _vp, ctypes.c_int, _i64, ctypes.c_double, _vp, _vp]
+        lib.oracle_attend.restype = _i64
+        lib.oracle_splitk_combine.argtypes = [_vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp]
+        lib.oracle_splitk_combine.restype = None
+        _LIB = lib
+    return _LIB
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(_vp)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(np.asarray(a), dtype=dtype)
+
+
+def default_threads() -> int:
+    return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------------------
+# Quantisation ([P1] section 4; [P3] quant kernel table and advanced config)
+# --------------------------------------------------------------------------
+
+def token_mean(x):
+    """Per-(sequence, channel) mean over tokens, fp64 token-order sum -> fp32.
+
+    x: [..., S, D] float32.  Returns float32 [..., D].
+    """
+    x = _c(x, np.float32)
+    *lead, S, D = x.shape
+    BH = int(np.prod(lead)) if lead else 1
+    mu = np.empty((BH, D), np.float32)
+    _lib().oracle_token_mean(_p(x), BH, S, D, _p(mu))
+    return mu.reshape(*lead, D)
+
+
+def quant_int8(x, block_tokens: int = 1, smooth: bool = False, mu=None):
+    """Symmetric INT8 quantisation, s = amax/127, q = rne(x/s) in fp32.
+
+    x: float32 [..., S, D] (fp16/bf16 inputs converted exactly to fp32).
+    block_tokens: 1 = per token, else tokens per block (128 Q, 64 K).
+    smooth: subtract the token mean first (computed here unless ``mu``
+    is given, in which case that mean is used as is).
+    Returns (q int8 [..., S, D], scale fp32 [..., ceil(S/block)], mu or None).
+    """
+    x = _c(x, np.float32)
+    *lead, S, D = x.shape
+    BH = int(np.prod(lead)) if lead else 1
+    if smooth and mu is None:
+        mu = token_mean(x)
+    mu_c = None if (not smooth) else _c(mu, np.float32).reshape(BH, D)
+    G = (S + block_tokens - 1) // block_tokens
+    q = np.empty((BH, S, D), np.int8)
+    s = np.empty((BH, G), np.float32)
+    _lib().oracle_quant_int8(_p(x), BH, S, D, int(block_tokens), _p(mu_c), _p(q), _p(s))
+    mu_out = None if mu_c is None else mu_c.reshape(*lead, D)
+    return q.reshape(*lead, S, D), s.reshape(*lead, G), mu_out
+
+
+def row_bias(x, mu):
+    """b_i = sum_c x_ic mu_c in fp64.  x: [B,H,S,D]; mu: [B,Hmu,D] (GQA groups)."""
+    x = _c(x, np.float32)
+    mu = _c(mu, np.float32)
+    B, H, S, D = x.shape
+    Hmu = mu.shape[1]
+    out = np.empty((B, H, S), np.float64)
+    _lib().oracle_row_bias(_p(x), B, H, S, D, _p(mu), Hmu, _p(out))
+    return out
+
+
+def qk_int32(q, k):
+    """Raw INT32 scores of one head ([P1] 2.1): q [Sq,D] int8, k [Sk,D] int8."""
+    q = _c(q, np.int8)
+    k = _c(k, np.int8)
+    Sq, D = q.shape
+    Sk = k.shape[0]
+    acc = np.empty((Sq, Sk), np.int32)
+    bad = _lib().oracle_qk_int32(_p(q), Sq, _p(k), Sk, D, _p(acc))
+    if bad:
+        raise ValueError("raw score outside the INT32 bound D*127^2")
+    return acc
+
+
+def expand_scale(scale, n: int, block: int):
+    """Per-row scale of rows 0..n-1 from per-group scales ([..., G])."""
+    idx = np.arange(n) // block
+    return np.asarray(scale)[..., idx]
+
+
+# --------------------------------------------------------------------------
+# Paged cache lookup ([P1] section 3, steps 1-5)
+# cache layout [block, kv_head, head_dim/16, block_size=16, 16];
+# scale layout [block, kv_head, 16]
+# --------------------------------------------------------------------------
+
+PAGE = 16
+
+
+def gather_paged(cache, block_row, n_tokens: int, kv_head: int):
+    """Logical [n_tokens, D] int8 rows of one (sequence, kv head).
+
+    Token t lives in physical block block_row[t // 16], slot t % 16;
+    channel c in sub-block c // 16 at position c % 16.
+    """
+    cache = np.asarray(cache)
+    D = cache.shape[2] * 16
+    t = np.arange(n_tokens)
+    blk = np.asarray(block_row)[t // PAGE].astype(np.int64)
+    # advanced indices (blk, kv_head, slot) -> [n_tokens, D/16, 16]
+    rows = cache[blk, kv_head, :, t % PAGE, :]
+    return np.ascontiguousarray(rows.reshape(n_tokens, D))
+
+
+def gather_paged_scale(scale, block_row, n_tokens: int, kv_head: int):
+    """Per-token fp32 scale [n_tokens] of one (sequence, kv head)."""
+    t = np.arange(n_tokens)
+    blk = np.asarray(block_row)[t // PAGE].astype(np.int64)
+    return np.ascontiguousarray(np.asarray(scale)[blk, kv_head, t % PAGE], dtype=np.float32)
+
+
+# --------------------------------------------------------------------------
+# Attention ([P1] section 1; [P3] attention pipeline)
+# --------------------------------------------------------------------------
+
+def attend(q, sq, k, sk, v, *, sm_scale, causal=False, causal_offset=0, qpos=None,
+           qbias=None, smoothed=None):
+    """One query-row batch against one key set; returns (o fp64, lse fp64)."""
+    q = _c(q, np.int8)
+    sq = _c(sq, np.float32)
+    k = _c(k, np.int8)
+    sk = _c(sk, np.float32)
+    v = _c(v, np.float64)
+    nq, D = q.shape
+    nk = k.shape[0]
+    qb = None if qbias is None else _c(qbias, np.float64)
+    sm = None if smoothed is None else _c(smoothed, np.uint8)
+    qp = None
+    if causal:
+        qp = _c(np.arange(nq) if qpos is None else qpos, np.int64)
+    o = np.empty((nq, D), np.float64)
+    lse = np.empty((nq,), np.float64)
+    bad = _lib().oracle_attend(nq, D, _p(q), _p(sq), _p(qb), _p(qp), nk, _p(k), _p(sk), _p(sm),
+                               _p(v), int(bool(causal)), int(causal_offset), float(sm_scale),
+                               _p(o), _p(lse))
+    if bad:
+        raise ValueError("raw score outside the INT32 bound D*127^2")
+    return o, lse
+
+
+def _run(jobs, threads):
+    threads = threads or default_threads()
+    if threads <= 1 or len(jobs) <= 1:
+        return [j() for j in jobs]
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        return list(ex.map(lambda f: f(), jobs))
+
+
+def prefill(q_i8, q_scale, q_block, k_i8, k_scale, k_block, v, *, causal, sm_scale=None,
+            q_bias=None, prefix=None, rows=None, threads=None):
+    """Prefill attention, optionally over a paged INT8 prefix.
+
+    q_i8 [B,Hq,Sq,D] int8, q_scale [B,Hq,ceil(Sq/q_block)] fp32;
+    k_i8 [B,Hkv,Sc,D] int8 (the contiguous chunk), k_scale [B,Hkv,ceil(Sc/k_block)];
+    v [B,Hkv,Sc,D] float values (fp16/bf16 as given);
+    q_bias [B,Hq,Sq] fp64 or None: when given the chunk keys are smoothed
+    and their scores get q_bias back (the smooth_k correction);
+    prefix: None or dict(k_cache, v_cache [nblk,Hkv,D/16,16,16] int8,
+    k_scale, v_scale [nblk,Hkv,16] fp32, block_table [B,maxblk] int32,
+    lens [B]) -- prefix keys come first, then the chunk.
+    Causal alignment is bottom-right: key j is visible to query i iff
+    j <= i + (Sk - Sq), Sk = prefix + chunk length.
+    rows: optional query-row indices to evaluate (same for every b, h).
+    Returns (o fp64 [B,Hq,R,D], lse fp64 [B,Hq,R]).
+    """
+    q_i8 = np.asarray(q_i8)
+    B, Hq, Sq, D = q_i8.shape
+    Hkv, Sc = k_i8.shape[1], k_i8.shape[2]
+    group = Hq // Hkv
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    rows = np.arange(Sq) if rows is None else np.asarray(rows, np.int64)
+    R = len(rows)
+    o = np.zeros((B, Hq, R, D), np.float64)
+    lse = np.zeros((B, Hq, R), np.float64)
+    v = np.asarray(v, np.float64)
+    sq_full = expand_scale(q_scale, Sq, q_block)
+    sk_full = expand_scale(k_scale, Sc, k_block)
+    jobs = []
+    for b in range(B):
+        P = 0 if prefix is None else int(prefix["lens"][b])
+        for g in range(Hkv):
+            if P:
+                bt = prefix["block_table"][b]
+                kp = gather_paged(prefix["k_cache"], bt, P, g)
+                vp = gather_paged(prefix["v_cache"], bt, P, g).astype(np.float64)
+                skp = gather_paged_scale(prefix["k_scale"], bt, P, g)
+                svp = gather_paged_scale(prefix["v_scale"], bt, P, g).astype(np.float64)
+                vp = vp * svp[:, None]
+                keys = np.concatenate([kp, k_i8[b, g]], 0)
+                sks = np.concatenate([skp, sk_full[b, g]], 0)
+                vals = np.concatenate([vp, v[b, g]], 0)
+            else:
+                keys, sks, vals = np.asarray(k_i8[b, g]), sk_full[b, g], v[b, g]
+            smoothed = None
+            if q_bias is not None:
+                smoothed = np.concatenate([np.zeros(P, np.uint8), np.ones(Sc, np.uint8)])
+            for h in range(g * group, (g + 1) * group):
+                def job(b=b, h=h, keys=keys, sks=sks, vals=vals, smoothed=smoothed, P=P):
+                    qb = None if q_bias is None else np.asarray(q_bias)[b, h, rows]
+                    ob, lb = attend(q_i8[b, h, rows], sq_full[b, h, rows], keys, sks, vals,
+                                    sm_scale=sm_scale, causal=causal,
+                                    causal_offset=P + Sc - Sq, qpos=rows, qbias=qb,
+                                    smoothed=smoothed)
+                    o[b, h] = ob
+                    lse[b, h] = lb
+                jobs.append(job)
+    _run(jobs, threads)
+    return o, lse
+
+
+def decode_paged(q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
+                 context_lens, *, sm_scale=None, threads=None, pairs=None):
+    """Single-token decode over a paged INT8 K/V cache ([P1] sections 3-5).
+
+    q_i8 [B,Hq,D] int8, q_scale [B,Hq] fp32; caches [nblk,Hkv,D/16,16,16]
+    int8; scales [nblk,Hkv,16] fp32; block_table [B,maxblk] int32;
+    context_lens [B].  Query head h reads kv head h // (Hq/Hkv).
+    pairs: optional list of (b, kv_head) to evaluate (others stay zero).
+    Returns (o fp64 [B,Hq,D], lse fp64 [B,Hq]).
+    """
+    q_i8 = np.asarray(q_i8)
+    B, Hq, D = q_i8.shape
+    Hkv = k_cache.shape[1]
+    group = Hq // Hkv
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    o = np.zeros((B, Hq, D), np.float64)
+    lse = np.full((B, Hq), -np.inf, np.float64)
+    if pairs is None:
+        pairs = [(b, g) for b in range(B) for g in range(Hkv)]
+    jobs = []
+    for (b, g) in pairs:
+        def job(b=b, g=g):
+            n = int(context_lens[b])
+            bt = block_table[b]
+            keys = gather_paged(k_cache, bt, n, g)
+            sk = gather_paged_scale(k_scale, bt, n, g)
+            vals = gather_paged(v_cache, bt, n, g).astype(np.float64)
+            vals *= gather_paged_scale(v_scale, bt, n, g).astype(np.float64)[:, None]
+            hs = slice(g * group, (g + 1) * group)
+            ob, lb = attend(q_i8[b, hs], np.asarray(q_scale)[b, hs], keys, sk, vals,
+                            sm_scale=sm_scale)
+            o[b, hs] = ob
+            lse[b, hs] = lb
+        jobs.append(job)
+    _run(jobs, threads)
+    return o, lse
+
+
+def splitk_combine(o_part, lse_part):
+    """LSE-weighted combine of split-K partials: o_part [..., S, D], lse_part [..., S]."""
+    o_part = _c(o_part, np.float64)
+    lse_part = _c(lse_part, np.float64)
+    *lead, S, D = o_part.shape
+    R = int(np.prod(lead)) if lead else 1
+    o = np.empty((R, D), np.float64)
+    lse = np.empty((R,), np.float64)
+    _lib().oracle_splitk_combine(_p(o_part), _p(lse_part), R, S, D, _p(o), _p(lse))
+    return o.reshape(*lead, D), lse.reshape(*lead)

@@ -1,0 +1,391 @@
+"""Pins that tie the CPU oracle to what the pages and mathematics fix.
+
+None of these re-types the oracle's own formula: each checks it against a
+hand-derived value printed on (or derived from) the pages, a closed form,
+an invariant, a textbook routine written independently here (float64
+numpy attention), or brute force on tiny inputs.  The cases are chosen so
+that a plausible slip in the oracle (a dropped scale, a transposed
+operand, a wrong causal offset, a sign error in the smooth_k bias, a wrong
+LSE base, a wrong page index) fails at least one of them.
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def textbook_attention(q, k, v, sm_scale, causal=False, offset=0):
+    """Plain float64 softmax(q k^T * sm_scale) v with natural-log LSE."""
+    s = (q.astype(np.float64) @ k.astype(np.float64).T) * sm_scale
+    if causal:
+        i = np.arange(q.shape[0])[:, None]
+        j = np.arange(k.shape[0])[None, :]
+        s = np.where(j <= i + offset, s, -np.inf)
+    m = s.max(axis=1, keepdims=True)
+    p = np.exp(s - m)
+    l = p.sum(axis=1, keepdims=True)
+    return (p / l) @ v.astype(np.float64), (m + np.log(l))[:, 0]
+
+
+def integer_rows(rng, n, d, amax=127):
+    """Integer rows whose absolute maximum is exactly ``amax`` (so s = amax/127)."""
+    x = rng.integers(-amax, amax + 1, size=(n, d)).astype(np.float32)
+    cols = rng.integers(0, d, size=n)
+    sign = rng.choice([-1.0, 1.0], size=n)
+    x[np.arange(n), cols] = sign * amax
+    return x
+
+
+# --------------------------------------------------------------------------
+# quantisation
+# --------------------------------------------------------------------------
+
+def _read_ties():
+    rows = []
+    for line in open(os.path.join(GOLDEN, "quant_ties.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        amax, xs, qs = [part.split() for part in line.split("|")]
+        rows.append((float(amax[0]), np.array(xs, np.float32), np.array(qs, np.int64)))
+    return rows
+
+
+@pytest.mark.parametrize("case", range(4))
+def test_quant_golden_ties(case):
+    amax, xs, expect = _read_ties()[case]
+    # every value is fp16-representable: the fp16 -> fp32 path is exact
+    assert np.all(xs.astype(np.float16).astype(np.float32) == xs)
+    q, s, _ = oracle.quant_int8(xs[None, None, :])
+    assert s[0, 0] == np.float32(amax) / np.float32(127.0)
+    assert q[0, 0].tolist() == expect.tolist()
+
+
+def test_quant_bounds_and_error():
+    rng = np.random.default_rng(1)
+    x = rng.standard_normal((3, 37, 64)).astype(np.float16).astype(np.float32)
+    for block in (1, 8, 16, 64):
+        q, s, _ = oracle.quant_int8(x, block_tokens=block)
+        assert q.dtype == np.int8 and np.abs(q.astype(np.int32)).max() <= 127
+        G = (37 + block - 1) // block
+        assert s.shape == (3, G)
+        for b in range(3):
+            for g in range(G):
+                grp = x[b, g * block:(g + 1) * block]
+                amax = np.abs(grp).max()
+                assert s[b, g] == np.float32(amax) / np.float32(127)
+                qq = q[b, g * block:(g + 1) * block].astype(np.float64)
+                # reconstruction error at most half a step (plus fp32 slack)
+                err = np.abs(qq * s[b, g] - grp)
+                assert err.max() <= 0.5 * s[b, g] * (1 + 1e-5)
+                # the element that sets amax lands on +-127
+                idx = np.unravel_index(np.abs(grp).argmax(), grp.shape)
+                assert abs(int(q[b, g * block + idx[0], idx[1]])) == 127
+                # sign is preserved wherever the code is non-zero
+                nz = qq != 0
+                assert np.all(np.sign(qq[nz]) == np.sign(grp[nz]))
+
+
+def test_quant_zero_group():
+    x = np.zeros((1, 4, 16), np.float32)
+    x[0, 2:] = 1.0
+    q, s, _ = oracle.quant_int8(x, block_tokens=2)
+    assert s[0, 0] == 0.0 and np.all(q[0, :2] == 0)
+    assert s[0, 1] == np.float32(1) / np.float32(127) and np.all(q[0, 2:] == 127)
+
+
+def test_quant_integer_identity():
+    rng = np.random.default_rng(2)
+    x = integer_rows(rng, 50, 128)
+    q, s, _ = oracle.quant_int8(x[None])
+    assert np.all(s == 1.0)
+    assert np.array_equal(q[0].astype(np.float32), x)
+
+
+def test_token_mean_closed_forms():
+    S, D = 33, 16
+    t = np.arange(S, dtype=np.float32)[:, None] * np.ones((1, D), np.float32)
+    x = (t * 0.5 + np.arange(D, dtype=np.float32)[None, :])[None]
+    mu = oracle.token_mean(x)
+    # mean of 0.5*t + c over t = 0..S-1 is 0.25*(S-1) + c
+    expect = 0.25 * (S - 1) + np.arange(D, dtype=np.float64)
+    assert np.array_equal(mu[0], expect.astype(np.float32))
+    const = np.full((2, 7, 4), 3.25, np.float32)
+    assert np.all(oracle.token_mean(const) == 3.25)
+
+
+def test_smooth_subtracts_mean_before_quant():
+    # K rows = mu + I with I integer (amax 127) and symmetric (+I, -I pairs)
+    # so that the token mean is exactly mu and K - mu = I exactly.
+    rng = np.random.default_rng(3)
+    half = integer_rows(rng, 8, 32)
+    I = np.concatenate([half, -half], 0)
+    mu = (rng.integers(-64, 64, size=32) * 0.25).astype(np.float32)
+    k = (I + mu[None, :]).astype(np.float32)
+    q8, s, mu_o = oracle.quant_int8(k[None], smooth=True)
+    assert np.array_equal(mu_o[0], mu)
+    assert np.all(s == 1.0)
+    assert np.array_equal(q8[0].astype(np.float32), I)
+
+
+# --------------------------------------------------------------------------
+# raw INT32 scores
+# --------------------------------------------------------------------------
+
+def test_int32_bound_golden():
+    line = [l for l in open(os.path.join(GOLDEN, "int32_bound.txt")) if not l.startswith("#")][0]
+    D, bound = map(int, line.split())
+    ones = np.full((2, D), 127, np.int8)
+    neg = np.full((2, D), -127, np.int8)
+    assert oracle.qk_int32(ones, ones)[0, 0] == bound
+    assert oracle.qk_int32(ones, neg)[0, 0] == -bound
+    assert oracle.qk_int32(neg, neg)[1, 1] == bound
+
+
+def test_qk_brute_force():
+    rng = np.random.default_rng(4)
+    q = rng.integers(-127, 128, size=(5, 48)).astype(np.int8)
+    k = rng.integers(-127, 128, size=(7, 48)).astype(np.int8)
+    acc = oracle.qk_int32(q, k)
+    for i in range(5):
+        for j in range(7):
+            assert acc[i, j] == sum(int(q[i, c]) * int(k[j, c]) for c in range(48))
+
+
+# --------------------------------------------------------------------------
+# attention
+# --------------------------------------------------------------------------
+
+def test_reduces_to_textbook_attention_when_quant_is_identity():
+    rng = np.random.default_rng(5)
+    Sq, Sk, D = 24, 40, 64
+    q = integer_rows(rng, Sq, D)
+    k = integer_rows(rng, Sk, D)
+    v = rng.standard_normal((Sk, D))
+    qi, sq, _ = oracle.quant_int8(q[None])
+    ki, sk, _ = oracle.quant_int8(k[None])
+    sm = 1.0 / 4096.0
+    for causal in (False, True):
+        o, lse = oracle.attend(qi[0], sq[0], ki[0], sk[0], v, sm_scale=sm, causal=causal,
+                               causal_offset=Sk - Sq)
+        o_ref, lse_ref = textbook_attention(q, k, v, sm, causal, Sk - Sq)
+        np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_scales_are_row_and_column_scales():
+    # dequantised textbook: Qhat = q*sQ (per row), Khat = k*sK (per column);
+    # per-token K scales are distinct powers of two, so any swap of the
+    # row/column role or an off-by-one column shift changes the result.
+    rng = np.random.default_rng(6)
+    Sq, Sk, D = 9, 16, 32
+    qi = rng.integers(-127, 128, (Sq, D)).astype(np.int8)
+    ki = rng.integers(-127, 128, (Sk, D)).astype(np.int8)
+    sq = (2.0 ** -rng.integers(8, 14, Sq)).astype(np.float32)
+    sk = (2.0 ** -np.arange(6, 6 + Sk)).astype(np.float32)
+    v = rng.standard_normal((Sk, D))
+    o, lse = oracle.attend(qi, sq, ki, sk, v, sm_scale=0.125)
+    o_ref, lse_ref = textbook_attention(qi * sq[:, None].astype(np.float64),
+                                        ki * sk[:, None].astype(np.float64), v, 0.125)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_invariants_uniform_and_constant_values():
+    rng = np.random.default_rng(7)
+    Sq, Sk, D = 6, 33, 16
+    qi = rng.integers(-127, 128, (Sq, D)).astype(np.int8)
+    ki = rng.integers(-127, 128, (Sk, D)).astype(np.int8)
+    sq = rng.uniform(0.01, 0.02, Sq).astype(np.float32)
+    sk = rng.uniform(0.01, 0.02, Sk).astype(np.float32)
+    # V == 1 -> O == 1 (softmax rows sum to one)
+    o, _ = oracle.attend(qi, sq, ki, sk, np.ones((Sk, D)), sm_scale=0.3)
+    np.testing.assert_allclose(o, 1.0, rtol=0, atol=1e-14)
+    # K == 0 -> uniform weights: O = mean(V), LSE = ln(Sk)
+    v = rng.standard_normal((Sk, D))
+    o, lse = oracle.attend(qi, sq, np.zeros((Sk, D), np.int8), sk, v, sm_scale=0.3)
+    np.testing.assert_allclose(o, np.broadcast_to(v.mean(0), o.shape), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(Sk), rtol=0, atol=1e-14)
+
+
+def test_causal_equals_truncated_key_set():
+    rng = np.random.default_rng(8)
+    Sq, Sk, D = 12, 20, 32
+    qi = rng.integers(-127, 128, (Sq, D)).astype(np.int8)
+    ki = rng.integers(-127, 128, (Sk, D)).astype(np.int8)
+    sq = rng.uniform(0.005, 0.02, Sq).astype(np.float32)
+    sk = rng.uniform(0.005, 0.02, Sk).astype(np.float32)
+    v = rng.standard_normal((Sk, D))
+    off = Sk - Sq
+    o, lse = oracle.attend(qi, sq, ki, sk, v, sm_scale=0.2, causal=True, causal_offset=off)
+    for i in range(Sq):
+        n = i + off + 1
+        oi, li = oracle.attend(qi[i:i + 1], sq[i:i + 1], ki[:n], sk[:n], v[:n], sm_scale=0.2)
+        np.testing.assert_allclose(o[i], oi[0], rtol=1e-13, atol=1e-15)
+        np.testing.assert_allclose(lse[i], li[0], rtol=1e-13)
+    # a row with no visible key: zero output, -inf LSE
+    o2, l2 = oracle.attend(qi[:2], sq[:2], ki, sk, v, sm_scale=0.2, causal=True,
+                           causal_offset=-1)
+    assert np.all(o2[0] == 0) and l2[0] == -np.inf and np.isfinite(l2[1])
+
+
+def test_smooth_k_bias_restores_unsmoothed_scores():
+    # K = mu + I exactly (see test_smooth_subtracts_mean_before_quant), integer
+    # Q with amax 127: with the smooth_k bias the method equals textbook
+    # attention on the ORIGINAL K; without it the LSE is off by sm*(q.mu).
+    rng = np.random.default_rng(9)
+    D, Sq = 32, 10
+    half = integer_rows(rng, 12, D)
+    I = np.concatenate([half, -half], 0)
+    mu = (rng.integers(-64, 64, size=D) * 0.25).astype(np.float32)
+    k = (I + mu[None, :]).astype(np.float32)
+    q = integer_rows(rng, Sq, D)
+    v = rng.standard_normal((k.shape[0], D))
+    sm = 1.0 / 8192.0
+    ki, sk, mu_o = oracle.quant_int8(k[None, None], smooth=True)
+    qi, sq, _ = oracle.quant_int8(q[None, None])
+    bias = oracle.row_bias(q[None, None], mu_o)
+    np.testing.assert_allclose(bias[0, 0], q.astype(np.float64) @ mu.astype(np.float64),
+                               rtol=1e-15)
+    o, lse = oracle.attend(qi[0, 0], sq[0, 0], ki[0, 0], sk[0, 0], v, sm_scale=sm,
+                           qbias=bias[0, 0], smoothed=np.ones(k.shape[0], np.uint8))
+    o_ref, lse_ref = textbook_attention(q, k, v, sm)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-12, atol=1e-12)
+    o2, lse2 = oracle.attend(qi[0, 0], sq[0, 0], ki[0, 0], sk[0, 0], v, sm_scale=sm)
+    np.testing.assert_allclose(o2, o_ref, rtol=1e-11, atol=1e-12)  # row constant cancels in O
+    np.testing.assert_allclose(lse2 + sm * bias[0, 0], lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_gqa_mapping():
+    rng = np.random.default_rng(10)
+    B, Hq, Hkv, S, D = 1, 6, 2, 16, 32
+    q = rng.standard_normal((B, Hq, S, D)).astype(np.float32)
+    k = rng.standard_normal((B, Hkv, S, D)).astype(np.float32)
+    v = rng.standard_normal((B, Hkv, S, D))
+    qi, sq, _ = oracle.quant_int8(q)
+    ki, sk, _ = oracle.quant_int8(k)
+    o, _ = oracle.prefill(qi, sq, 1, ki, sk, 1, v, causal=False, sm_scale=0.2, threads=1)
+    for h in range(Hq):
+        g = h // (Hq // Hkv)
+        oh, _ = oracle.attend(qi[0, h], sq[0, h], ki[0, g], sk[0, g], v[0, g], sm_scale=0.2)
+        np.testing.assert_array_equal(o[0, h], oh)
+        other, _ = oracle.attend(qi[0, h], sq[0, h], ki[0, 1 - g], sk[0, 1 - g], v[0, 1 - g],
+                                 sm_scale=0.2)
+        assert np.abs(o[0, h] - other).max() > 1e-3
+
+
+# --------------------------------------------------------------------------
+# paged cache, decode, split-K combine
+# --------------------------------------------------------------------------
+
+def _scatter_to_pages(k_logical, s_logical, table, nblk):
+    """Write logical rows [Hkv][L][D] into pages of layout [blk][kvh][D/16][16][16]."""
+    Hkv, L, D = k_logical.shape
+    cache = np.zeros((nblk, Hkv, D // 16, 16, 16), np.int8)
+    sc = np.zeros((nblk, Hkv, 16), np.float32)
+    for g in range(Hkv):
+        for t in range(L):
+            blk = table[t // 16]
+            for c in range(D):
+                cache[blk, g, c // 16, t % 16, c % 16] = k_logical[g, t, c]
+            sc[blk, g, t % 16] = s_logical[g, t]
+    return cache, sc
+
+
+def test_paged_decode_equals_dense_attention():
+    rng = np.random.default_rng(11)
+    Hq, Hkv, D, L = 4, 2, 32, 45       # ragged last page
+    nblk = 7
+    table = rng.permutation(nblk)[:3].astype(np.int32)
+    kl = rng.integers(-127, 128, (Hkv, L, D)).astype(np.int8)
+    vl = rng.integers(-127, 128, (Hkv, L, D)).astype(np.int8)
+    ksl = rng.uniform(0.005, 0.02, (Hkv, L)).astype(np.float32)
+    vsl = rng.uniform(0.005, 0.02, (Hkv, L)).astype(np.float32)
+    kc, ks = _scatter_to_pages(kl, ksl, table, nblk)
+    vc, vs = _scatter_to_pages(vl, vsl, table, nblk)
+    qi = rng.integers(-127, 128, (1, Hq, D)).astype(np.int8)
+    sq = rng.uniform(0.005, 0.02, (1, Hq)).astype(np.float32)
+    o, lse = oracle.decode_paged(qi, sq, kc, vc, ks, vs, table[None], [L], sm_scale=0.25,
+                                 threads=1)
+    for h in range(Hq):
+        g = h // 2
+        vv = vl[g].astype(np.float64) * vsl[g][:, None].astype(np.float64)
+        o_ref, l_ref = textbook_attention(qi[0, h:h + 1] * np.float64(sq[0, h]),
+                                          kl[g] * ksl[g][:, None].astype(np.float64), vv, 0.25)
+        np.testing.assert_allclose(o[0, h], o_ref[0], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse[0, h], l_ref[0], rtol=1e-12)
+    # a different physical placement of the same logical pages gives the
+    # bitwise-same result
+    table2 = rng.permutation(nblk)[:3].astype(np.int32)
+    kc2, ks2 = _scatter_to_pages(kl, ksl, table2, nblk)
+    vc2, vs2 = _scatter_to_pages(vl, vsl, table2, nblk)
+    o2, lse2 = oracle.decode_paged(qi, sq, kc2, vc2, ks2, vs2, table2[None], [L], sm_scale=0.25,
+                                   threads=1)
+    assert np.array_equal(o, o2) and np.array_equal(lse, lse2)
+
+
+def test_splitk_combine_matches_unsplit():
+    rng = np.random.default_rng(12)
+    D, L = 16, 50
+    qi = rng.integers(-127, 128, (3, D)).astype(np.int8)
+    sq = rng.uniform(0.005, 0.02, 3).astype(np.float32)
+    ki = rng.integers(-127, 128, (L, D)).astype(np.int8)
+    sk = rng.uniform(0.005, 0.02, L).astype(np.float32)
+    v = rng.standard_normal((L, D))
+    o_full, l_full = oracle.attend(qi, sq, ki, sk, v, sm_scale=0.5)
+    bounds = [0, 7, 7, 30, 50, 50]   # includes empty segments
+    parts_o, parts_l = [], []
+    for a, b in zip(bounds[:-1], bounds[1:]):
+        if b > a:
+            o, l = oracle.attend(qi, sq, ki[a:b], sk[a:b], v[a:b], sm_scale=0.5)
+        else:
+            o, l = np.zeros((3, D)), np.full(3, -np.inf)
+        parts_o.append(o)
+        parts_l.append(l)
+    op = np.stack(parts_o, 1)   # [3, S, D]
+    lp = np.stack(parts_l, 1)   # [3, S]
+    o, l = oracle.splitk_combine(op, lp)
+    np.testing.assert_allclose(o, o_full, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(l, l_full, rtol=1e-13)
+    # one segment: identity
+    o1, l1 = oracle.splitk_combine(op[:, 3:4], lp[:, 3:4])
+    np.testing.assert_allclose(o1, op[:, 3], rtol=1e-15)
+    assert np.array_equal(l1, lp[:, 3])
+    # all segments empty
+    oe, le = oracle.splitk_combine(np.zeros((2, 3, D)), np.full((2, 3), -np.inf))
+    assert np.all(oe == 0) and np.all(le == -np.inf)
+
+
+def test_prefill_with_paged_prefix_equals_concatenated_keys():
+    rng = np.random.default_rng(13)
+    Hq, Hkv, D, P, Sc = 2, 1, 32, 37, 20
+    nblk = 5
+    table = rng.permutation(nblk)[:3].astype(np.int32)
+    kl = rng.integers(-127, 128, (Hkv, P, D)).astype(np.int8)
+    vl = rng.integers(-127, 128, (Hkv, P, D)).astype(np.int8)
+    ksl = rng.uniform(0.005, 0.02, (Hkv, P)).astype(np.float32)
+    vsl = rng.uniform(0.005, 0.02, (Hkv, P)).astype(np.float32)
+    kc, ks = _scatter_to_pages(kl, ksl, table, nblk)
+    vc, vs = _scatter_to_pages(vl, vsl, table, nblk)
+    qi = rng.integers(-127, 128, (1, Hq, Sc, D)).astype(np.int8)
+    sq = rng.uniform(0.005, 0.02, (1, Hq, Sc)).astype(np.float32)
+    kn = rng.integers(-127, 128, (1, Hkv, Sc, D)).astype(np.int8)
+    skn = rng.uniform(0.005, 0.02, (1, Hkv, Sc)).astype(np.float32)
+    vn = rng.standard_normal((1, Hkv, Sc, D))
+    prefix = dict(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs, block_table=table[None],
+                  lens=[P])
+    o, lse = oracle.prefill(qi, sq, 1, kn, skn, 1, vn, causal=True, sm_scale=0.3,
+                            prefix=prefix, threads=1)
+    for h in range(Hq):
+        kk = np.concatenate([kl[0] * ksl[0][:, None].astype(np.float64),
+                             kn[0, 0] * skn[0, 0][:, None].astype(np.float64)], 0)
+        vv = np.concatenate([vl[0] * vsl[0][:, None].astype(np.float64), vn[0, 0]], 0)
+        o_ref, l_ref = textbook_attention(qi[0, h] * sq[0, h][:, None].astype(np.float64), kk, vv,
+                                          0.3, causal=True, offset=P)
+        np.testing.assert_allclose(o[0, h], o_ref, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(lse[0, h], l_ref, rtol=1e-12)
