@@ -1,0 +1,254 @@
+/*
+ * sage_attn.h -- C ABI of libsageattn.so: INT8-QK quantized attention for
+ * GB300 (sm_103a).
+ *
+ * Sources (cited by page title and section):
+ *   [P1] "INT8 QK MMAC on gfx936 DCU: paged access, fragment mapping and
+ *        GQA" (forum.sourcefind.cn) -- quantisation rule (section 4), score
+ *        recovery (section 1), INT32 bound (section 2.1), paged K cache
+ *        layout and lookup (section 3), split-K decode and GQA (sections
+ *        4-5), reject-don't-guess applicability checks (section 7).
+ *   [P3] "SageAttention -- MetaX MXMACA port" README (gitlink.org.cn) --
+ *        per-block granularity CTA_Q=128 / CTA_K=64, smooth_k with LSE
+ *        correction, causal masking, base-2 online softmax, FP16 P.V with
+ *        FP32 accumulation, LSE return (feature matrix, attention kernel
+ *        pipeline, advanced configuration).
+ *
+ * Conventions shared by every entry point
+ *   - Every pointer argument is a DEVICE pointer owned by the caller unless
+ *     the comment says "host".  The library never allocates, frees or
+ *     keeps a pointer beyond the call.
+ *   - Work is enqueued on the caller's CUDA stream (`stream`, a
+ *     cudaStream_t passed as void*; NULL = legacy default stream).  No call
+ *     synchronises except sage_check_device_status().
+ *   - Tensors are dense row-major unless strides are given; "[B,H,S,D]"
+ *     lists dimensions outermost first.
+ *   - Every call returns a sage_status_t and never throws or aborts.  On
+ *     failure nothing has been enqueued (argument errors) or the launch
+ *     failed (SAGE_ERR_CUDA); sage_get_last_error_message() tells why.
+ *   - Kernels never trap.  Every wait inside a kernel is bounded; a wait
+ *     that runs out, a block-table entry outside [0, num_blocks) or a
+ *     context length outside [0, max_context_len] sets a per-device error
+ *     word that sage_check_device_status() reads; the offending page is
+ *     not read (its keys are masked) and the length is clamped.
+ */
+#ifndef SAGE_ATTN_H
+#define SAGE_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum sage_status {
+    SAGE_OK = 0,
+    SAGE_ERR_INVALID_ARG = 1,   /* null pointer, bad shape/stride/alignment, GQA mismatch */
+    SAGE_ERR_UNSUPPORTED = 2,   /* valid request outside what this build implements */
+    SAGE_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    SAGE_ERR_TIMEOUT = 4,       /* device error word: a bounded wait ran out */
+    SAGE_ERR_BAD_BLOCK = 5      /* device error word: block-table entry or length out of range */
+} sage_status_t;
+
+typedef enum sage_dtype {
+    SAGE_F16 = 0,
+    SAGE_BF16 = 1
+} sage_dtype_t;
+
+/* Message of the last failing call on the calling host thread. */
+const char *sage_get_last_error_message(void);
+
+/* Library ABI version (increments on any signature change). */
+int sage_version(void);
+
+/* --------------------------------------------------------------------------
+ * Quantisation  ([P1] section 4; [P3] quant kernel table, feature matrix)
+ *
+ * Symmetric dynamic INT8 quantisation of x [B,H,S,D]:
+ *   group = one token row (block_tokens == 1) or block_tokens consecutive
+ *   tokens of one (b, h) (per-block granularity, 128 for Q and 64 for K);
+ *   s = amax / 127 in fp32 (amax = max |x| over the group; s = 0 when
+ *   amax = 0);  q = round-to-nearest-even(fp32(x / s)) in [-127, 127].
+ * smooth != 0: first computes mu[b,h,c] = mean over the S tokens of
+ *   x[b,h,:,c] (exact sum, rounded once to fp32) and quantises x - mu
+ *   (smooth_k).
+ * mu_in != NULL: also writes the row bias bias[b,h,s] = sum_c x[b,h,s,c] *
+ *   mu_in[b, h / (H / mu_heads), c] (fp32), the term smooth_k removes from
+ *   the scores of Q against smoothed K.
+ *
+ * x        : f16/bf16, element strides (stride_b, stride_h, stride_s) with the
+ *            channel dimension contiguous; the base address and every row
+ *            must be 16-byte aligned (strides multiples of 8 elements).  HND
+ *            and NHD layouts are both expressed through the strides.
+ * D        : 64, 128 or 256.   block_tokens: 1..1024.
+ * x_int8   : int8 [B,H,S,D] dense (HND).
+ * scale    : fp32 [B,H,ceil(S/block_tokens)].
+ * mu_out   : fp32 [B,H,D], required iff smooth.
+ * bias_out : fp32 [B,H,S], required iff mu_in.
+ * ------------------------------------------------------------------------ */
+sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B, int H, int S, int D,
+                              int64_t stride_b, int64_t stride_h, int64_t stride_s,
+                              int block_tokens, int smooth, const float *mu_in, int mu_heads,
+                              int8_t *x_int8, float *scale, float *mu_out, float *bias_out,
+                              void *stream);
+
+/* --------------------------------------------------------------------------
+ * Paged INT8 K/V cache  ([P1] section 3)
+ *   k_cache, v_cache : int8 [num_blocks, Hkv, D/16, 16, 16]; token t of a
+ *                      sequence sits in physical block block_table[b][t/16],
+ *                      slot t % 16; channel c at [c/16][slot][c%16].
+ *   k_scale, v_scale : fp32 [num_blocks, Hkv, 16], per token and KV head.
+ *   block_table      : int32 [B, max_blocks].
+ * ------------------------------------------------------------------------ */
+
+/* --------------------------------------------------------------------------
+ * Split-K paged decode  ([P1] sections 1, 3, 4, 5)
+ *
+ * One new query token per sequence.  Query head h reads KV head
+ * h / (Hq / Hkv) (GQA).  For each (b, h):
+ *   acc_j = sum_c q[b,h,c] * k_j[c]                      (exact INT32)
+ *   t_j   = acc_j * q_scale[b,h] * k_scale_j * sm_scale   (per score)
+ *   o     = sum_j softmax(t)_j * v_scale_j * v_j          (FP32 accumulation)
+ *   lse   = ln sum_j exp(t_j)
+ * The context is cut into num_segments contiguous runs of pages; each is
+ * reduced on its own and the partials are merged by the LSE combine
+ * (sage_splitk_combine).
+ * ------------------------------------------------------------------------ */
+typedef struct sage_decode_args {
+    const int8_t *q;            /* [B, Hq, D] int8 (sage_quant_int8 output) */
+    const float *q_scale;       /* [B, Hq] fp32 */
+    const int8_t *k_cache;      /* paged layout above */
+    const int8_t *v_cache;
+    const float *k_scale;       /* [num_blocks, Hkv, 16] */
+    const float *v_scale;
+    const int32_t *block_table; /* [B, max_blocks] */
+    const int32_t *context_lens;/* [B], each in [0, max_context_len] */
+    int B, Hq, Hkv, D;          /* D = 64, 128 or 256; Hq % Hkv == 0 */
+    int num_blocks, max_blocks;
+    int max_context_len;        /* host-side bound on context_lens, <= 16 * max_blocks */
+    float sm_scale;             /* <= 0 selects 1/sqrt(D) */
+    int num_segments;           /* 0 selects sage_decode_num_segments() */
+    void *out;                  /* [B, Hq, D] */
+    sage_dtype_t out_dtype;
+    float *lse;                 /* optional [B, Hq] natural-log LSE (-inf for empty context) */
+} sage_decode_args_t;
+
+/* Segment count the library picks for num_segments == 0 (host only). */
+int sage_decode_num_segments(int B, int Hq, int Hkv, int max_context_len);
+
+/* Bytes of workspace sage_attn_decode_paged needs: fp32 partial outputs
+ * [B,Hq,S,D] plus fp32 partial LSEs [B,Hq,S] (0 when S == 1). */
+size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments);
+
+/* workspace: device buffer of at least sage_attn_decode_workspace_size()
+ * bytes, 16-byte aligned; may be NULL when the segment count is 1.  Its
+ * contents are scratch and are overwritten. */
+sage_status_t sage_attn_decode_paged(const sage_decode_args_t *args, void *workspace,
+                                     size_t workspace_bytes, void *stream);
+
+/* --------------------------------------------------------------------------
+ * Split-K LSE combine  ([P1] section 4 split-K; [P3] LSE returned "for
+ * concatenation").  For every row r:
+ *   M = max_s lse_part[r,s],  L = M + ln sum_s exp(lse_part[r,s] - M)
+ *   out[r] = sum_s exp(lse_part[r,s] - L) * o_part[r,s]
+ * Segments with lse = -inf are skipped; a row with no live segment gets
+ * out = 0 and lse = -inf.
+ * o_part : fp32 [R, S, D] (each segment's output, already normalised)
+ * lse_part: fp32 [R, S] natural log.  out: [R, D] of out_dtype.
+ * lse_out : optional fp32 [R].  D = 64, 128 or 256; 1 <= S <= 1024.
+ * ------------------------------------------------------------------------ */
+sage_status_t sage_splitk_combine(const float *o_part, const float *lse_part, int R, int S, int D,
+                                  void *out, sage_dtype_t out_dtype, float *lse_out,
+                                  void *stream);
+
+/* --------------------------------------------------------------------------
+ * Prefill  ([P3] attention kernel pipeline and advanced configuration;
+ * [P1] sections 5.2 and 7 for chunked prefill over a paged INT8 history)
+ *
+ * Queries [B,Hq,Sq,D] attend to Sp paged prefix keys (optional) followed by
+ * Sk contiguous chunk keys.  Query head h reads KV head h / (Hq/Hkv).
+ *   acc_ij = sum_c q_ic k_jc                         (exact INT32)
+ *   z_ij   = sm_scale * (acc_ij * sq_i * sk_j + [j in chunk and q_bias] * q_bias_i)
+ *   causal: key j (index over prefix + chunk) is visible to query i iff
+ *           j <= i + (Sp + Sk - Sq)  (bottom-right alignment)
+ *   o_i    = sum_j softmax(z)_ij v_j,  v_j = v_scale_j * v_int8_j (prefix) or
+ *            the f16/bf16 value (chunk);  P.V in 16-bit with FP32 accumulation
+ *   lse_i  = ln sum_j exp(z_ij)
+ * q_bias (from sage_quant_int8's bias_out with the K mean) restores the
+ * scores of smoothed chunk keys; with no prefix it only shifts the LSE
+ * ([P3]'s LSE correction).
+ * ------------------------------------------------------------------------ */
+typedef struct sage_prefill_args {
+    int B, Hq, Hkv, Sq, Sk, D;      /* D = 64, 128 or 256; Sk may be 0 with a prefix */
+    const int8_t *q;                /* [B, Hq, Sq, D] int8 */
+    const float *q_scale;           /* [B, Hq, ceil(Sq / q_block)] */
+    int q_block;                    /* 1 (per token) or a multiple of 128 */
+    const int8_t *k;                /* [B, Hkv, Sk, D] int8 (chunk keys) */
+    const float *k_scale;           /* [B, Hkv, ceil(Sk / k_block)] */
+    int k_block;                    /* 1 (per token) or a multiple of 64 */
+    const void *v;                  /* [B, Hkv, Sk, D] chunk values */
+    sage_dtype_t v_dtype;           /* P.V runs in this 16-bit type */
+    const float *q_bias;            /* optional [B, Hq, Sq]: chunk keys are smoothed */
+    /* optional paged INT8 prefix (all NULL / 0 when absent) */
+    const int8_t *k_cache, *v_cache;
+    const float *k_cache_scale, *v_cache_scale;
+    const int32_t *block_table;     /* [B, max_blocks] */
+    const int32_t *prefix_lens;     /* [B] device; each <= max_prefix_len */
+    int num_blocks, max_blocks, max_prefix_len;
+    int causal;
+    float sm_scale;                 /* <= 0 selects 1/sqrt(D) */
+    void *out;                      /* [B, Hq, Sq, D] */
+    sage_dtype_t out_dtype;
+    float *lse;                     /* optional [B, Hq, Sq] */
+} sage_prefill_args_t;
+
+sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *stream);
+
+/* --------------------------------------------------------------------------
+ * Test hooks: raw INT32 scores through the same device tile paths
+ * ([P1] section 7, layer 1: check the lane/fragment mapping of the raw
+ * accumulators).
+ * sage_debug_prefill_qk_int32: runs sage_attn_prefill and also writes
+ *   scores[b,h,i,j] = acc_ij for every visible (i, j); masked entries are
+ *   left untouched.  scores: int32 [B, Hq, Sq, max_prefix_len + Sk].
+ * sage_debug_decode_qk_int32: runs sage_attn_decode_paged and writes
+ *   scores[b,h,j] for j < context_lens[b]; scores: int32 [B, Hq, max_context_len].
+ * ------------------------------------------------------------------------ */
+sage_status_t sage_debug_prefill_qk_int32(const sage_prefill_args_t *args, int32_t *scores,
+                                          void *stream);
+sage_status_t sage_debug_decode_qk_int32(const sage_decode_args_t *args, void *workspace,
+                                         size_t workspace_bytes, int32_t *scores, void *stream);
+
+/* --------------------------------------------------------------------------
+ * Runtime-path evidence ([P1] section 7, layer 4: prove the target kernel
+ * ran).  Describes the last kernel launched by the calling host thread.
+ * ------------------------------------------------------------------------ */
+typedef struct sage_launch_info {
+    char kernel[64];
+    int grid[3];
+    int block[3];
+    int cluster[3];
+    int smem_bytes;
+    int num_segments;
+    int launches;               /* kernels enqueued by the last API call */
+} sage_launch_info_t;
+
+sage_status_t sage_last_launch_info(sage_launch_info_t *info /* host */);
+
+/* Synchronises `stream`, reads and clears the current device's error word.
+ * Returns SAGE_OK, SAGE_ERR_TIMEOUT or SAGE_ERR_BAD_BLOCK (or SAGE_ERR_CUDA).
+ * `detail` (host, optional) receives the raw word. */
+sage_status_t sage_check_device_status(void *stream, int *detail);
+
+/* Test hook for the bounded-wait path: launches a kernel that waits on an
+ * mbarrier nothing arrives on, with a limit of `timeout_us` microseconds
+ * (1..5,000,000); the kernel gives up, sets SAGE_ERR_TIMEOUT in the error
+ * word and returns.  Used to show the context stays usable. */
+sage_status_t sage_debug_timeout_probe(int timeout_us, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SAGE_ATTN_H */

@@ -1,0 +1,332 @@
+"""Thin ctypes binding of libsageattn.so (the C ABI in include/sage_attn.h).
+
+Argument marshalling only: torch tensors are checked for device, dtype and
+layout, outputs are allocated with torch, and raw device pointers plus the
+current CUDA stream are handed to the library.  Every step of the
+attention path runs in the library's kernels; there is no fallback: if the
+library is missing or the tensors are not on a CUDA device the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+SAGE_OK = 0
+SAGE_ERR_INVALID_ARG = 1
+SAGE_ERR_UNSUPPORTED = 2
+SAGE_ERR_CUDA = 3
+SAGE_ERR_TIMEOUT = 4
+SAGE_ERR_BAD_BLOCK = 5
+
+SAGE_F16 = 0
+SAGE_BF16 = 1
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_i64 = ctypes.c_int64
+_f = ctypes.c_float
+
+
+class SageError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("sage status %d: %s" % (status, message))
+        self.status = status
+
+
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [("q", _vp), ("q_scale", _vp), ("k_cache", _vp), ("v_cache", _vp),
+                ("k_scale", _vp), ("v_scale", _vp), ("block_table", _vp), ("context_lens", _vp),
+                ("B", _i), ("Hq", _i), ("Hkv", _i), ("D", _i), ("num_blocks", _i),
+                ("max_blocks", _i), ("max_context_len", _i), ("sm_scale", _f),
+                ("num_segments", _i), ("out", _vp), ("out_dtype", _i), ("lse", _vp)]
+
+
+class PrefillArgs(ctypes.Structure):
+    _fields_ = [("B", _i), ("Hq", _i), ("Hkv", _i), ("Sq", _i), ("Sk", _i), ("D", _i),
+                ("q", _vp), ("q_scale", _vp), ("q_block", _i),
+                ("k", _vp), ("k_scale", _vp), ("k_block", _i),
+                ("v", _vp), ("v_dtype", _i), ("q_bias", _vp),
+                ("k_cache", _vp), ("v_cache", _vp), ("k_cache_scale", _vp), ("v_cache_scale", _vp),
+                ("block_table", _vp), ("prefix_lens", _vp),
+                ("num_blocks", _i), ("max_blocks", _i), ("max_prefix_len", _i),
+                ("causal", _i), ("sm_scale", _f), ("out", _vp), ("out_dtype", _i), ("lse", _vp)]
+
+
+class LaunchInfo(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_char * 64), ("grid", _i * 3), ("block", _i * 3),
+                ("cluster", _i * 3), ("smem_bytes", _i), ("num_segments", _i), ("launches", _i)]
+
+
+_LIB = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def lib():
+    """Load libsageattn.so (built in-tree by build.py); raise if it is absent."""
+    global _LIB
+    if _LIB is None:
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError("libsageattn.so is not built (%s); run "
+                               "int8_quantized_attention_gb300.build.build()" % path)
+        L = ctypes.CDLL(path)
+        L.sage_get_last_error_message.restype = ctypes.c_char_p
+        L.sage_version.restype = _i
+        L.sage_quant_int8.argtypes = [_vp, _i, _i, _i, _i, _i, _i64, _i64, _i64, _i, _i, _vp, _i,
+                                      _vp, _vp, _vp, _vp, _vp]
+        L.sage_quant_int8.restype = _i
+        L.sage_decode_num_segments.argtypes = [_i, _i, _i, _i]
+        L.sage_decode_num_segments.restype = _i
+        L.sage_attn_decode_workspace_size.argtypes = [_i, _i, _i, _i]
+        L.sage_attn_decode_workspace_size.restype = ctypes.c_size_t
+        L.sage_attn_decode_paged.argtypes = [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t, _vp]
+        L.sage_attn_decode_paged.restype = _i
+        L.sage_debug_decode_qk_int32.argtypes = [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t,
+                                                 _vp, _vp]
+        L.sage_debug_decode_qk_int32.restype = _i
+        L.sage_splitk_combine.argtypes = [_vp, _vp, _i, _i, _i, _vp, _i, _vp, _vp]
+        L.sage_splitk_combine.restype = _i
+        L.sage_attn_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+        L.sage_attn_prefill.restype = _i
+        L.sage_debug_prefill_qk_int32.argtypes = [ctypes.POINTER(PrefillArgs), _vp, _vp]
+        L.sage_debug_prefill_qk_int32.restype = _i
+        L.sage_last_launch_info.argtypes = [ctypes.POINTER(LaunchInfo)]
+        L.sage_last_launch_info.restype = _i
+        L.sage_check_device_status.argtypes = [_vp, ctypes.POINTER(_i)]
+        L.sage_check_device_status.restype = _i
+        L.sage_debug_timeout_probe.argtypes = [_i, _vp]
+        L.sage_debug_timeout_probe.restype = _i
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int):
+    if status != SAGE_OK:
+        raise SageError(status, lib().sage_get_last_error_message().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must be on a CUDA device")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dt(dtype) -> int:
+    if dtype == torch.float16:
+        return SAGE_F16
+    if dtype == torch.bfloat16:
+        return SAGE_BF16
+    raise ValueError("dtype must be float16 or bfloat16, got %s" % dtype)
+
+
+def _need(t, dtype, name):
+    if t.dtype != dtype:
+        raise ValueError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+# --------------------------------------------------------------------------
+# Entry points
+# --------------------------------------------------------------------------
+
+def sage_quant_int8(x: torch.Tensor, block_tokens: int = 1, smooth: bool = False,
+                    mu_in: Optional[torch.Tensor] = None, layout: str = "HND", stream=None):
+    """Quantise x to INT8 (s = amax/127, round-to-nearest-even).
+
+    x: [B,H,S,D] (layout "HND") or [B,S,H,D] ("NHD"), f16/bf16, channel
+    dimension contiguous.  Returns (x_int8 [B,H,S,D], scale, mu, bias):
+    scale [B,H,ceil(S/block_tokens)]; mu [B,H,D] when smooth; bias [B,H,S]
+    (= x . mu_in, GQA-broadcast) when mu_in [B,Hmu,D] is given.
+    """
+    if layout == "HND":
+        B, H, S, D = x.shape
+        sb, sh, ss = x.stride(0), x.stride(1), x.stride(2)
+    elif layout == "NHD":
+        B, S, H, D = x.shape
+        sb, ss, sh = x.stride(0), x.stride(1), x.stride(2)
+    else:
+        raise ValueError("layout must be HND or NHD")
+    if x.stride(3) != 1:
+        raise ValueError("channel dimension must be contiguous")
+    dev = x.device
+    G = (S + block_tokens - 1) // block_tokens
+    q = torch.empty((B, H, S, D), dtype=torch.int8, device=dev)
+    scale = torch.empty((B, H, G), dtype=torch.float32, device=dev)
+    mu = torch.empty((B, H, D), dtype=torch.float32, device=dev) if smooth else None
+    bias = None
+    mu_heads = 0
+    if mu_in is not None:
+        _need(mu_in, torch.float32, "mu_in")
+        mu_heads = mu_in.shape[1]
+        bias = torch.empty((B, H, S), dtype=torch.float32, device=dev)
+    _check(lib().sage_quant_int8(_ptr(x), _dt(x.dtype), B, H, S, D, sb, sh, ss, block_tokens,
+                                 int(bool(smooth)), _ptr(mu_in), mu_heads, _ptr(q), _ptr(scale),
+                                 _ptr(mu), _ptr(bias), _stream(stream)))
+    return q, scale, mu, bias
+
+
+def decode_num_segments(B: int, Hq: int, Hkv: int, max_context_len: int) -> int:
+    return int(lib().sage_decode_num_segments(B, Hq, Hkv, max_context_len))
+
+
+def decode_workspace_size(B: int, Hq: int, D: int, num_segments: int) -> int:
+    return int(lib().sage_attn_decode_workspace_size(B, Hq, D, num_segments))
+
+
+def _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                 max_context_len, sm_scale, num_segments, out, lse):
+    _need(q_int8, torch.int8, "q_int8")
+    _need(q_scale, torch.float32, "q_scale")
+    _need(k_cache, torch.int8, "k_cache")
+    _need(v_cache, torch.int8, "v_cache")
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    _need(block_table, torch.int32, "block_table")
+    _need(context_lens, torch.int32, "context_lens")
+    B, Hq, D = q_int8.shape
+    a = DecodeArgs()
+    a.q, a.q_scale = _ptr(q_int8), _ptr(q_scale)
+    a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
+    a.k_scale, a.v_scale = _ptr(k_scale), _ptr(v_scale)
+    a.block_table, a.context_lens = _ptr(block_table), _ptr(context_lens)
+    a.B, a.Hq, a.Hkv, a.D = B, Hq, k_cache.shape[1], D
+    a.num_blocks, a.max_blocks = k_cache.shape[0], block_table.shape[1]
+    a.max_context_len = int(max_context_len)
+    a.sm_scale = float(sm_scale) if sm_scale else 0.0
+    a.num_segments = int(num_segments)
+    a.out, a.out_dtype = _ptr(out), _dt(out.dtype)
+    a.lse = _ptr(lse)
+    return a
+
+
+def sage_attn_decode_paged(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
+                           context_lens, max_context_len: int, *, sm_scale=None,
+                           num_segments: int = 0, out_dtype=torch.bfloat16,
+                           return_lse: bool = False, workspace: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None, debug_scores=None, stream=None):
+    """Split-K paged INT8 decode + LSE combine.  Returns out [B,Hq,D] (and lse)."""
+    B, Hq, D = q_int8.shape
+    Hkv = k_cache.shape[1]
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q_int8.device)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q_int8.device) if return_lse else None
+    S = num_segments or decode_num_segments(B, Hq, Hkv, max_context_len)
+    need = decode_workspace_size(B, Hq, D, S)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=q_int8.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a = _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
+                     context_lens, max_context_len, sm_scale, S, out, lse)
+    if debug_scores is not None:
+        _need(debug_scores, torch.int32, "debug_scores")
+        _check(lib().sage_debug_decode_qk_int32(ctypes.byref(a), _ptr(workspace), ws_bytes,
+                                                _ptr(debug_scores), _stream(stream)))
+    else:
+        _check(lib().sage_attn_decode_paged(ctypes.byref(a), _ptr(workspace), ws_bytes,
+                                            _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def sage_splitk_combine(o_part: torch.Tensor, lse_part: torch.Tensor, out_dtype=torch.bfloat16,
+                        return_lse: bool = False, stream=None):
+    """LSE combine of split-K partials: o_part [..., S, D] fp32, lse_part [..., S] fp32."""
+    _need(o_part, torch.float32, "o_part")
+    _need(lse_part, torch.float32, "lse_part")
+    *lead, S, D = o_part.shape
+    R = int(math.prod(lead)) if lead else 1
+    out = torch.empty((*lead, D), dtype=out_dtype, device=o_part.device)
+    lse = torch.empty(tuple(lead), dtype=torch.float32, device=o_part.device) if return_lse else None
+    _check(lib().sage_splitk_combine(_ptr(o_part), _ptr(lse_part), R, S, D, _ptr(out),
+                                     _dt(out_dtype), _ptr(lse), _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: int, v, *,
+                      causal: bool, sm_scale=None, q_bias=None, prefix: Optional[dict] = None,
+                      out_dtype=None, return_lse: bool = False, debug_scores=None, stream=None):
+    """INT8-QK prefill attention over an optional paged INT8 prefix + a chunk.
+
+    q_int8 [B,Hq,Sq,D]; q_scale [B,Hq,ceil(Sq/q_block)]; k_int8 [B,Hkv,Sk,D];
+    k_scale [B,Hkv,ceil(Sk/k_block)]; v [B,Hkv,Sk,D] f16/bf16; q_bias [B,Hq,Sq]
+    (smooth_k correction) or None; prefix = dict(k_cache, v_cache, k_scale,
+    v_scale, block_table, lens, max_len) or None.
+    """
+    B, Hq, Sq, D = q_int8.shape
+    Hkv, Sk = k_int8.shape[1], k_int8.shape[2]
+    _need(q_int8, torch.int8, "q_int8")
+    _need(k_int8, torch.int8, "k_int8")
+    _need(q_scale, torch.float32, "q_scale")
+    _need(k_scale, torch.float32, "k_scale")
+    if not v.is_contiguous():
+        raise ValueError("v must be contiguous")
+    out_dtype = out_dtype or v.dtype
+    out = torch.empty((B, Hq, Sq, D), dtype=out_dtype, device=q_int8.device)
+    lse = (torch.empty((B, Hq, Sq), dtype=torch.float32, device=q_int8.device)
+           if return_lse else None)
+    a = PrefillArgs()
+    a.B, a.Hq, a.Hkv, a.Sq, a.Sk, a.D = B, Hq, Hkv, Sq, Sk, D
+    a.q, a.q_scale, a.q_block = _ptr(q_int8), _ptr(q_scale), q_block
+    a.k, a.k_scale, a.k_block = _ptr(k_int8), _ptr(k_scale), k_block
+    a.v, a.v_dtype = _ptr(v), _dt(v.dtype)
+    if q_bias is not None:
+        _need(q_bias, torch.float32, "q_bias")
+    a.q_bias = _ptr(q_bias)
+    if prefix is not None:
+        for key in ("k_cache", "v_cache"):
+            _need(prefix[key], torch.int8, key)
+        for key in ("k_scale", "v_scale"):
+            _need(prefix[key], torch.float32, key)
+        _need(prefix["block_table"], torch.int32, "block_table")
+        _need(prefix["lens"], torch.int32, "lens")
+        a.k_cache, a.v_cache = _ptr(prefix["k_cache"]), _ptr(prefix["v_cache"])
+        a.k_cache_scale, a.v_cache_scale = _ptr(prefix["k_scale"]), _ptr(prefix["v_scale"])
+        a.block_table, a.prefix_lens = _ptr(prefix["block_table"]), _ptr(prefix["lens"])
+        a.num_blocks = prefix["k_cache"].shape[0]
+        a.max_blocks = prefix["block_table"].shape[1]
+        a.max_prefix_len = int(prefix["max_len"])
+    a.causal = int(bool(causal))
+    a.sm_scale = float(sm_scale) if sm_scale else 0.0
+    a.out, a.out_dtype, a.lse = _ptr(out), _dt(out_dtype), _ptr(lse)
+    if debug_scores is not None:
+        _need(debug_scores, torch.int32, "debug_scores")
+        _check(lib().sage_debug_prefill_qk_int32(ctypes.byref(a), _ptr(debug_scores),
+                                                 _stream(stream)))
+    else:
+        _check(lib().sage_attn_prefill(ctypes.byref(a), _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def last_launch_info() -> dict:
+    info = LaunchInfo()
+    _check(lib().sage_last_launch_info(ctypes.byref(info)))
+    return dict(kernel=info.kernel.decode(), grid=tuple(info.grid), block=tuple(info.block),
+                cluster=tuple(info.cluster), smem_bytes=info.smem_bytes,
+                num_segments=info.num_segments, launches=info.launches)
+
+
+def check_device_status(stream=None):
+    """Synchronise and read/clear the device error word: (status, raw word)."""
+    word = _i(0)
+    st = lib().sage_check_device_status(_stream(stream), ctypes.byref(word))
+    return st, word.value
+
+
+def debug_timeout_probe(timeout_us: int, stream=None):
+    _check(lib().sage_debug_timeout_probe(int(timeout_us), _stream(stream)))

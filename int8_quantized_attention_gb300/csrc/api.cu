@@ -1,0 +1,416 @@
+// C-ABI host layer of libsageattn.so: argument validation, launch
+// configuration, the per-device error word and the launch record.
+// Every entry point is declared (and documented) in include/sage_attn.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sage_attn.h"
+
+#define SAGE_API extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+thread_local std::string g_msg;
+thread_local sage::LaunchLog g_last;
+
+// Error word of the device (bit set of sage::kErrTimeout / kErrBadBlock).
+__device__ int g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int *g_err_ptr[kMaxDevices] = {};
+
+sage_status_t fail(sage_status_t s, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_msg = buf;
+    return s;
+}
+
+sage_status_t cuda_fail(cudaError_t e, const char *what) {
+    return fail(SAGE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device address of this device's error word (looked up once per device).
+sage_status_t error_word(int **out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(SAGE_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_error_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        g_err_ptr[dev] = static_cast<int *>(p);
+    }
+    *out = g_err_ptr[dev];
+    return SAGE_OK;
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        return 152;
+    return n;
+}
+
+int ilog2_exact(int x) {
+    int s = 0;
+    while ((1 << s) < x) ++s;
+    return (1 << s) == x ? s : -1;
+}
+
+__global__ void timeout_probe_kernel(long long limit_ns, int *err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        sage::mbar_init(sage::smem_u32(&bar), 1);
+        sage::fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x != 0) return;
+    // Nothing ever arrives on `bar`: the wait must give up on its own.
+    const unsigned long long t0 = sage::global_timer_ns();
+    while (!sage::mbar_try_wait(sage::smem_u32(&bar), 0)) {
+        if ((long long)(sage::global_timer_ns() - t0) > limit_ns) {
+            atomicOr(err, sage::kErrTimeout);
+            return;
+        }
+    }
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+
+SAGE_API const char *sage_get_last_error_message(void) { return g_msg.c_str(); }
+
+SAGE_API int sage_version(void) { return 1; }
+
+SAGE_API sage_status_t sage_last_launch_info(sage_launch_info_t *info) {
+    if (!info) return fail(SAGE_ERR_INVALID_ARG, "info is NULL");
+    memset(info, 0, sizeof(*info));
+    strncpy(info->kernel, g_last.kernel, sizeof(info->kernel) - 1);
+    info->grid[0] = g_last.grid.x, info->grid[1] = g_last.grid.y, info->grid[2] = g_last.grid.z;
+    info->block[0] = g_last.block.x, info->block[1] = g_last.block.y,
+    info->block[2] = g_last.block.z;
+    info->cluster[0] = g_last.cluster.x, info->cluster[1] = g_last.cluster.y,
+    info->cluster[2] = g_last.cluster.z;
+    info->smem_bytes = g_last.smem;
+    info->num_segments = g_last.segments;
+    info->launches = g_last.count;
+    return SAGE_OK;
+}
+
+SAGE_API sage_status_t sage_check_device_status(void *stream, int *detail) {
+    int *ew = nullptr;
+    sage_status_t s = error_word(&ew);
+    if (s != SAGE_OK) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int word = 0;
+    e = cudaMemcpy(&word, ew, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "read error word");
+    e = cudaMemset(ew, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+    if (detail) *detail = word;
+    if (word & sage::kErrBadBlock)
+        return fail(SAGE_ERR_BAD_BLOCK, "a block-table entry or context length was out of range");
+    if (word & sage::kErrTimeout) return fail(SAGE_ERR_TIMEOUT, "a bounded device wait ran out");
+    return SAGE_OK;
+}
+
+SAGE_API sage_status_t sage_debug_timeout_probe(int timeout_us, void *stream) {
+    if (timeout_us < 1 || timeout_us > 5000000)
+        return fail(SAGE_ERR_INVALID_ARG, "timeout_us must be in [1, 5e6]");
+    int *ew = nullptr;
+    sage_status_t s = error_word(&ew);
+    if (s != SAGE_OK) return s;
+    g_last = sage::LaunchLog();
+    timeout_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        (long long)timeout_us * 1000ll, ew);
+    g_last.add("timeout_probe_kernel", dim3(1), dim3(32), dim3(1, 1, 1), 0);
+    cudaError_t e = cudaGetLastError();
+    return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "timeout probe launch");
+}
+
+// ------------------------------------------------------------------ quant
+
+SAGE_API sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B, int H, int S,
+                                       int D, int64_t stride_b, int64_t stride_h,
+                                       int64_t stride_s, int block_tokens, int smooth,
+                                       const float *mu_in, int mu_heads, int8_t *x_int8,
+                                       float *scale, float *mu_out, float *bias_out,
+                                       void *stream) {
+    if (dtype != SAGE_F16 && dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "x dtype must be f16 or bf16");
+    if (!head_dim_ok(D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", D);
+    if (B < 0 || H < 0 || S < 0) return fail(SAGE_ERR_INVALID_ARG, "negative shape");
+    if (block_tokens < 1 || block_tokens > 1024)
+        return fail(SAGE_ERR_INVALID_ARG, "block_tokens %d outside [1, 1024]", block_tokens);
+    g_last = sage::LaunchLog();
+    if ((int64_t)B * H * S == 0) return SAGE_OK;
+    if (!x || !x_int8 || !scale) return fail(SAGE_ERR_INVALID_ARG, "x, x_int8 and scale are required");
+    if (!aligned(x, 16)) return fail(SAGE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    if (!aligned(x_int8, 8)) return fail(SAGE_ERR_INVALID_ARG, "x_int8 must be 8-byte aligned");
+    if (stride_b % 8 || stride_h % 8 || stride_s % 8)
+        return fail(SAGE_ERR_INVALID_ARG, "strides must be multiples of 8 elements");
+    if (smooth && !mu_out) return fail(SAGE_ERR_INVALID_ARG, "smooth needs mu_out");
+    if (smooth && (int64_t)B * H > 65535)
+        return fail(SAGE_ERR_UNSUPPORTED, "smooth supports at most 65535 (batch, head) pairs");
+    if (mu_in) {
+        if (!bias_out) return fail(SAGE_ERR_INVALID_ARG, "mu_in needs bias_out");
+        if (mu_heads < 1 || H % mu_heads)
+            return fail(SAGE_ERR_INVALID_ARG, "H (%d) must be a multiple of mu_heads (%d)", H,
+                        mu_heads);
+    }
+    sage::QuantParams p = {};
+    p.x = x;
+    p.bf16 = dtype == SAGE_BF16;
+    p.B = B, p.H = H, p.S = S, p.D = D;
+    p.sb = stride_b, p.sh = stride_h, p.ss = stride_s;
+    p.block = block_tokens;
+    p.smooth = smooth;
+    p.mu_bias = mu_in;
+    p.mu_heads = mu_in ? mu_heads : 1;
+    p.q = x_int8;
+    p.scale = scale;
+    p.mu_out = mu_out;
+    p.bias = mu_in ? bias_out : nullptr;
+    cudaError_t e = sage::launch_quant(p, static_cast<cudaStream_t>(stream), g_last);
+    return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "quant launch");
+}
+
+// ---------------------------------------------------------------- combine
+
+static sage_status_t check_combine(const float *o_part, const float *lse_part, int R, int S, int D,
+                                   const void *out, sage_dtype_t out_dtype) {
+    if (!head_dim_ok(D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", D);
+    if (out_dtype != SAGE_F16 && out_dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "out dtype must be f16 or bf16");
+    if (R < 0 || S < 1 || S > 1024) return fail(SAGE_ERR_INVALID_ARG, "need R >= 0, 1 <= S <= 1024");
+    if (R > 0 && (!o_part || !lse_part || !out))
+        return fail(SAGE_ERR_INVALID_ARG, "o_part, lse_part and out are required");
+    if (!aligned(o_part, 8)) return fail(SAGE_ERR_INVALID_ARG, "o_part must be 8-byte aligned");
+    return SAGE_OK;
+}
+
+SAGE_API sage_status_t sage_splitk_combine(const float *o_part, const float *lse_part, int R,
+                                           int S, int D, void *out, sage_dtype_t out_dtype,
+                                           float *lse_out, void *stream) {
+    sage_status_t s = check_combine(o_part, lse_part, R, S, D, out, out_dtype);
+    if (s != SAGE_OK) return s;
+    g_last = sage::LaunchLog();
+    sage::CombineParams p = {o_part, lse_part, R, S, D, out, out_dtype == SAGE_BF16, lse_out};
+    cudaError_t e = sage::launch_combine(p, static_cast<cudaStream_t>(stream), g_last);
+    return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "combine launch");
+}
+
+// ----------------------------------------------------------------- decode
+
+SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int max_context_len) {
+    if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || max_context_len <= 0) return 1;
+    const int group = Hq / Hkv;
+    const int64_t units = (int64_t)B * Hkv * ((group + 7) / 8);
+    const int64_t target = 2ll * sm_count();
+    const int pages = (max_context_len + 15) / 16;
+    int64_t S = (target + units - 1) / units;
+    // at least one page per consumer warp in every segment
+    const int64_t cap = pages / 4 > 1 ? pages / 4 : 1;
+    if (S > cap) S = cap;
+    if (S > 1024) S = 1024;
+    if (S < 1) S = 1;
+    const int64_t pps = (pages + S - 1) / S;
+    return (int)((pages + pps - 1) / pps);
+}
+
+SAGE_API size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments) {
+    if (num_segments <= 1 || B <= 0 || Hq <= 0 || D <= 0) return 0;
+    const size_t rows = (size_t)B * Hq * num_segments;
+    size_t o = rows * D * sizeof(float);
+    o = (o + 255) & ~(size_t)255;
+    return o + rows * sizeof(float);
+}
+
+static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
+                                size_t workspace_bytes, int32_t *dbg, void *stream) {
+    if (!a) return fail(SAGE_ERR_INVALID_ARG, "args is NULL");
+    if (!head_dim_ok(a->D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", a->D);
+    if (a->out_dtype != SAGE_F16 && a->out_dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "out dtype must be f16 or bf16");
+    if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->Hq % a->Hkv)
+        return fail(SAGE_ERR_INVALID_ARG, "need Hq a positive multiple of Hkv (Hq=%d Hkv=%d)",
+                    a->Hq, a->Hkv);
+    if (a->max_context_len < 0 || a->max_blocks < 0 ||
+        (int64_t)a->max_context_len > 16ll * a->max_blocks)
+        return fail(SAGE_ERR_INVALID_ARG, "max_context_len %d exceeds 16 * max_blocks (%d)",
+                    a->max_context_len, a->max_blocks);
+    if (a->num_segments < 0 || a->num_segments > 1024)
+        return fail(SAGE_ERR_INVALID_ARG, "num_segments outside [0, 1024]");
+    g_last = sage::LaunchLog();
+    if (a->B == 0) return SAGE_OK;
+    if (!a->q || !a->q_scale || !a->context_lens || !a->out)
+        return fail(SAGE_ERR_INVALID_ARG, "q, q_scale, context_lens and out are required");
+    if (a->max_context_len > 0) {
+        if (!a->k_cache || !a->v_cache || !a->k_scale || !a->v_scale || !a->block_table)
+            return fail(SAGE_ERR_INVALID_ARG, "cache, scales and block_table are required");
+        if (a->num_blocks < 1) return fail(SAGE_ERR_INVALID_ARG, "num_blocks must be >= 1");
+        if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) || !aligned(a->k_scale, 16) ||
+            !aligned(a->v_scale, 16))
+            return fail(SAGE_ERR_INVALID_ARG, "caches and scales must be 16-byte aligned");
+    }
+    if (!aligned(a->q, 4)) return fail(SAGE_ERR_INVALID_ARG, "q must be 4-byte aligned");
+    int S = a->num_segments ? a->num_segments
+                            : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->max_context_len);
+    const int pages = (a->max_context_len + 15) / 16;
+    int pps = pages > 0 ? (pages + S - 1) / S : 1;
+    if (pages > 0) S = (pages + pps - 1) / pps;
+    else S = 1;
+    int *ew = nullptr;
+    sage_status_t st = error_word(&ew);
+    if (st != SAGE_OK) return st;
+    sage::DecodeParams p = {};
+    p.q = a->q, p.q_scale = a->q_scale;
+    p.k_cache = a->k_cache, p.v_cache = a->v_cache, p.k_scale = a->k_scale, p.v_scale = a->v_scale;
+    p.block_table = a->block_table, p.context_lens = a->context_lens;
+    p.B = a->B, p.Hq = a->Hq, p.Hkv = a->Hkv, p.D = a->D, p.group = a->Hq / a->Hkv;
+    p.head_tiles = (p.group + 7) / 8;
+    p.num_blocks = a->num_blocks, p.max_blocks = a->max_blocks;
+    p.num_segments = S, p.pages_per_seg = pps;
+    p.max_ctx = a->max_context_len;
+    const float sm = a->sm_scale > 0.0f ? a->sm_scale : 1.0f / sqrtf((float)a->D);
+    p.qk_scale_log2 = sm * 1.4426950408889634f;
+    p.out = a->out, p.out_bf16 = a->out_dtype == SAGE_BF16, p.lse = a->lse;
+    p.dbg = dbg, p.dbg_stride = a->max_context_len;
+    p.err = ew;
+    if (S > 1) {
+        const size_t need = sage_attn_decode_workspace_size(a->B, a->Hq, a->D, S);
+        if (!workspace || workspace_bytes < need)
+            return fail(SAGE_ERR_INVALID_ARG, "workspace too small: need %zu bytes for %d segments",
+                        need, S);
+        if (!aligned(workspace, 16)) return fail(SAGE_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+        const size_t rows = (size_t)a->B * a->Hq * S;
+        p.o_part = static_cast<float *>(workspace);
+        p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
+                                               ((rows * a->D * sizeof(float) + 255) & ~(size_t)255));
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaError_t e = sage::launch_decode(p, cs, g_last);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    if (S > 1) {
+        sage::LaunchLog tmp = g_last;
+        sage::CombineParams c = {p.o_part, p.lse_part, a->B * a->Hq, S, a->D, a->out,
+                                 p.out_bf16, a->lse};
+        e = sage::launch_combine(c, cs, tmp);
+        if (e != cudaSuccess) return cuda_fail(e, "combine launch");
+        // keep the decode kernel as the recorded kernel; count both launches
+        g_last.count = tmp.count;
+    }
+    return SAGE_OK;
+}
+
+SAGE_API sage_status_t sage_attn_decode_paged(const sage_decode_args_t *args, void *workspace,
+                                              size_t workspace_bytes, void *stream) {
+    return run_decode(args, workspace, workspace_bytes, nullptr, stream);
+}
+
+SAGE_API sage_status_t sage_debug_decode_qk_int32(const sage_decode_args_t *args, void *workspace,
+                                                  size_t workspace_bytes, int32_t *scores,
+                                                  void *stream) {
+    if (!scores) return fail(SAGE_ERR_INVALID_ARG, "scores is NULL");
+    return run_decode(args, workspace, workspace_bytes, scores, stream);
+}
+
+// ---------------------------------------------------------------- prefill
+
+static sage_status_t run_prefill(const sage_prefill_args_t *a, int32_t *dbg, void *stream) {
+    if (!a) return fail(SAGE_ERR_INVALID_ARG, "args is NULL");
+    if (!head_dim_ok(a->D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", a->D);
+    if (a->out_dtype != SAGE_F16 && a->out_dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "out dtype must be f16 or bf16");
+    if (a->v_dtype != SAGE_F16 && a->v_dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "v dtype must be f16 or bf16");
+    if (a->B < 0 || a->Sq < 0 || a->Sk < 0 || a->Hq < 1 || a->Hkv < 1 || a->Hq % a->Hkv)
+        return fail(SAGE_ERR_INVALID_ARG, "bad shape (B=%d Hq=%d Hkv=%d Sq=%d Sk=%d)", a->B, a->Hq,
+                    a->Hkv, a->Sq, a->Sk);
+    const int qs = a->q_block == 1 ? 0 : ilog2_exact(a->q_block);
+    const int ks = a->k_block == 1 ? 0 : ilog2_exact(a->k_block);
+    if (qs < 0 || (a->q_block != 1 && a->q_block < 128))
+        return fail(SAGE_ERR_UNSUPPORTED, "q_block must be 1 or a power of two >= 128");
+    if (ks < 0 || (a->k_block != 1 && a->k_block < 64))
+        return fail(SAGE_ERR_UNSUPPORTED, "k_block must be 1 or a power of two >= 64");
+    const bool has_prefix = a->max_prefix_len > 0;
+    if (a->max_prefix_len < 0 ||
+        (has_prefix && (int64_t)a->max_prefix_len > 16ll * a->max_blocks))
+        return fail(SAGE_ERR_INVALID_ARG, "max_prefix_len exceeds 16 * max_blocks");
+    g_last = sage::LaunchLog();
+    if ((int64_t)a->B * a->Sq == 0) return SAGE_OK;
+    if (!a->q || !a->q_scale || !a->out) return fail(SAGE_ERR_INVALID_ARG, "q, q_scale, out required");
+    if (a->Sk > 0 && (!a->k || !a->k_scale || !a->v))
+        return fail(SAGE_ERR_INVALID_ARG, "k, k_scale and v are required when Sk > 0");
+    if (has_prefix) {
+        if (!a->k_cache || !a->v_cache || !a->k_cache_scale || !a->v_cache_scale ||
+            !a->block_table || !a->prefix_lens || a->num_blocks < 1)
+            return fail(SAGE_ERR_INVALID_ARG, "paged prefix needs caches, scales, table, lens");
+        if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) ||
+            !aligned(a->k_cache_scale, 16) || !aligned(a->v_cache_scale, 16))
+            return fail(SAGE_ERR_INVALID_ARG, "caches and scales must be 16-byte aligned");
+    }
+    if (a->Sk + a->max_prefix_len == 0) return fail(SAGE_ERR_INVALID_ARG, "no keys");
+    if (!aligned(a->q, 16) || (a->k && !aligned(a->k, 16)) || (a->v && !aligned(a->v, 16)) ||
+        !aligned(a->out, 16))
+        return fail(SAGE_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    int *ew = nullptr;
+    sage_status_t st = error_word(&ew);
+    if (st != SAGE_OK) return st;
+    sage::PrefillParams p = {};
+    p.B = a->B, p.Hq = a->Hq, p.Hkv = a->Hkv, p.Sq = a->Sq, p.Sk = a->Sk, p.D = a->D;
+    p.group = a->Hq / a->Hkv;
+    p.q = a->q, p.q_scale = a->q_scale, p.q_shift = qs;
+    p.q_groups = (a->Sq + a->q_block - 1) / a->q_block;
+    p.k = a->k, p.k_scale = a->k_scale, p.k_shift = ks;
+    p.k_groups = (a->Sk + a->k_block - 1) / a->k_block;
+    p.v = a->v, p.v_bf16 = a->v_dtype == SAGE_BF16;
+    p.q_bias = a->q_bias;
+    if (has_prefix) {
+        p.k_cache = a->k_cache, p.v_cache = a->v_cache;
+        p.k_cache_scale = a->k_cache_scale, p.v_cache_scale = a->v_cache_scale;
+        p.block_table = a->block_table, p.prefix_lens = a->prefix_lens;
+        p.num_blocks = a->num_blocks, p.max_blocks = a->max_blocks;
+        p.max_prefix_len = a->max_prefix_len;
+    }
+    p.causal = a->causal != 0;
+    const float sm = a->sm_scale > 0.0f ? a->sm_scale : 1.0f / sqrtf((float)a->D);
+    p.qk_scale_log2 = sm * 1.4426950408889634f;
+    p.out = a->out, p.out_bf16 = a->out_dtype == SAGE_BF16, p.lse = a->lse;
+    p.dbg = dbg;
+    p.err = ew;
+    cudaError_t e = sage::launch_prefill(p, static_cast<cudaStream_t>(stream), g_last);
+    if (e == cudaErrorNotSupported)
+        return fail(SAGE_ERR_UNSUPPORTED, "prefill configuration not supported by this build");
+    return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "prefill launch");
+}
+
+SAGE_API sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *stream) {
+    return run_prefill(args, nullptr, stream);
+}
+
+SAGE_API sage_status_t sage_debug_prefill_qk_int32(const sage_prefill_args_t *args,
+                                                   int32_t *scores, void *stream) {
+    if (!scores) return fail(SAGE_ERR_INVALID_ARG, "scores is NULL");
+    return run_prefill(args, scores, stream);
+}

@@ -1,0 +1,164 @@
+// Device primitives shared by the sm_103a kernels: bounded mbarrier waits,
+// bulk async copies, exact int8 -> f16 conversion, small math helpers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace sage {
+
+// Bits of the per-device error word (see sage_check_device_status).
+constexpr int kErrTimeout = 1;
+constexpr int kErrBadBlock = 2;
+
+// Upper bound on any single wait inside a kernel (nanoseconds).
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA / bulk copy) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete.  Gives up after kWaitLimitNs,
+// sets the timeout bit of *err and returns false; never spins forever.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------- bulk async copies
+// 1-D global -> shared copy completing on an mbarrier (transaction bytes).
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_evict_first(uint32_t dst, const void *src, uint32_t bytes,
+                                                     uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// ------------------------------------------------ exact int8 -> f16 / bf16
+// For a signed byte b, (b ^ 0x80) = b + 128 =: u in [0, 255].  The f16 with
+// bit pattern 0x6400 | u equals 1024 + u exactly, so subtracting 1152 gives
+// b exactly (all integers below 2048 are f16-representable).
+// Input: four int8 packed in a 32-bit word; output: two f16x2 words holding
+// bytes (0,1) and (2,3).
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    // __byte_perm: result byte k = byte (selector nibble k) of {u (0..3), 0x64646464 (4..7)}
+    uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);  // halves: 0x64|u0, 0x64|u1
+    uint32_t c = __byte_perm(u, 0x64646464u, 0x4342);  // halves: 0x64|u2, 0x64|u3
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    __half2 l = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
+    __half2 h = __hsub2(*reinterpret_cast<__half2 *>(&c), bias);
+    lo = *reinterpret_cast<uint32_t *>(&l);
+    hi = *reinterpret_cast<uint32_t *>(&h);
+}
+
+// bf16 variant: the fp32 with bits 0x4B000000 | u equals 2^23 + u exactly;
+// subtracting 2^23 + 128 gives b exactly, and every |b| <= 128 is exact in
+// bf16 (8 significand bits), so the final rounding is exact too.
+__device__ __forceinline__ void i8x4_to_bf16x4(uint32_t w, uint32_t &lo, uint32_t &hi) {
+    const uint32_t u = w ^ 0x80808080u;
+    const float k = 8388736.0f;  // 2^23 + 128
+    const float f0 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)) - k;
+    const float f1 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)) - k;
+    const float f2 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)) - k;
+    const float f3 = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)) - k;
+    __nv_bfloat162 l = __floats2bfloat162_rn(f0, f1);
+    __nv_bfloat162 h = __floats2bfloat162_rn(f2, f3);
+    lo = *reinterpret_cast<uint32_t *>(&l);
+    hi = *reinterpret_cast<uint32_t *>(&h);
+}
+
+// ------------------------------------------------------------------ misc
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <typename T>
+struct DT;
+template <>
+struct DT<__half> {
+    static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+    static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
+};
+template <>
+struct DT<__nv_bfloat16> {
+    static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ __nv_bfloat16 from_f(float x) {
+        return __float2bfloat16_rn(x);
+    }
+};
+
+}  // namespace sage

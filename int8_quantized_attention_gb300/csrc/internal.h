@@ -1,0 +1,111 @@
+// Internal (non-exported) interface between the C-ABI host layer and the
+// kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+namespace sage {
+
+// Record of the kernels one API call enqueued (runtime-path evidence).
+struct LaunchLog {
+    char kernel[64] = {0};
+    dim3 grid, block, cluster;
+    int smem = 0;
+    int segments = 0;
+    int count = 0;
+    void add(const char *name, dim3 g, dim3 b, dim3 c, int sm) {
+        strncpy(kernel, name, sizeof(kernel) - 1);
+        grid = g;
+        block = b;
+        cluster = c;
+        smem = sm;
+        ++count;
+    }
+};
+
+struct QuantParams {
+    const void *x;
+    int bf16;
+    int B, H, S, D;
+    int64_t sb, sh, ss;
+    int block;                // tokens per group (1 = per token)
+    int smooth;
+    const float *mu_sub;      // set internally to mu_out after the mean pass
+    const float *mu_bias;     // optional mean for the row bias
+    int mu_heads;
+    int8_t *q;
+    float *scale;
+    float *mu_out;
+    float *bias;
+};
+
+cudaError_t launch_quant(const QuantParams &p, cudaStream_t st, LaunchLog &log);
+
+struct CombineParams {
+    const float *o_part;      // [R, S, D]
+    const float *lse_part;    // [R, S]
+    int R, S, D;
+    void *out;
+    int out_bf16;
+    float *lse_out;
+};
+
+cudaError_t launch_combine(const CombineParams &p, cudaStream_t st, LaunchLog &log);
+
+struct DecodeParams {
+    const int8_t *q;
+    const float *q_scale;
+    const int8_t *k_cache, *v_cache;
+    const float *k_scale, *v_scale;
+    const int32_t *block_table, *context_lens;
+    int B, Hq, Hkv, D, group, head_tiles;
+    int num_blocks, max_blocks;
+    int num_segments, pages_per_seg;
+    int max_ctx;              // host bound on context_lens (<= 16 * max_blocks)
+    float qk_scale_log2;      // sm_scale * log2(e)
+    float *o_part;            // [B*Hq, S, D] when num_segments > 1
+    float *lse_part;          // [B*Hq, S]
+    void *out;                // [B*Hq, D] when num_segments == 1
+    int out_bf16;
+    float *lse;               // optional [B*Hq] when num_segments == 1
+    int32_t *dbg;             // optional raw score dump [B*Hq, dbg_stride]
+    int dbg_stride;
+    int *err;
+};
+
+int decode_ctas_per_sm(int D);
+cudaError_t launch_decode(const DecodeParams &p, cudaStream_t st, LaunchLog &log);
+
+struct PrefillParams {
+    int B, Hq, Hkv, Sq, Sk, D, group;
+    const int8_t *q;
+    const float *q_scale;
+    int q_shift;              // log2(q_block): 0 per token, 7 per 128-token block
+    int q_groups;             // ceil(Sq / q_block)
+    const int8_t *k;
+    const float *k_scale;
+    int k_shift;
+    int k_groups;
+    const void *v;
+    int v_bf16;
+    const float *q_bias;
+    const int8_t *k_cache, *v_cache;
+    const float *k_cache_scale, *v_cache_scale;
+    const int32_t *block_table, *prefix_lens;
+    int num_blocks, max_blocks, max_prefix_len;
+    int causal;
+    float qk_scale_log2;      // sm_scale * log2(e)
+    void *out;
+    int out_bf16;
+    float *lse;
+    int32_t *dbg;             // optional [B,Hq,Sq,max_prefix_len+Sk]
+    int *err;
+};
+
+cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
+
+cudaError_t launch_timeout_probe(int timeout_us, int *err, cudaStream_t st, LaunchLog &log);
+
+}  // namespace sage

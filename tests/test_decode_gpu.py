@@ -1,0 +1,200 @@
+"""GPU parity: split-K paged decode + LSE combine against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, f32, np_
+from int8_quantized_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _quant_query(sage, B, Hq, D, seed):
+    q = W.decode_query(B, Hq, D, seed=seed, device="cuda")
+    qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
+    return qi[:, :, 0].contiguous(), qs[:, :, 0].contiguous()
+
+
+def _run(sage, qi, qs, c, max_len, **kw):
+    return sage.sage_attn_decode_paged(qi, qs, c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                       c.block_table, c.lens, max_len, **kw)
+
+
+def _oracle(qi, qs, c, pairs=None):
+    return oracle.decode_paged(np_(qi), np_(qs), np_(c.k_cache), np_(c.v_cache), np_(c.k_scale),
+                               np_(c.v_scale), np_(c.block_table), np_(c.lens), pairs=pairs)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv", [(12, 2), (4, 4), (16, 2), (24, 4)])
+@pytest.mark.parametrize("segments", [1, 3, 0])
+def test_decode_small(sage, D, Hq, Hkv, segments):
+    B = 3
+    lens = [37, 300, 129]                     # ragged last pages
+    c = W.paged_cache(B, Hkv, D, lens, seed=D + Hq, device="cuda", extra_blocks=5)
+    qi, qs = _quant_query(sage, B, Hq, D, seed=Hq)
+    # short contexts give |O| ~ 0.5: f16 output keeps output rounding well inside tolerance
+    out, lse = _run(sage, qi, qs, c, max(lens), num_segments=segments, return_lse=True,
+                    out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    o_ref, l_ref = _oracle(qi, qs, c)
+    assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
+    st, word = sage.check_device_status()
+    assert st == 0, word
+
+
+def test_decode_raw_scores_bit_exact(sage):
+    B, Hq, Hkv, D = 2, 12, 2, 256
+    lens = [45, 200]
+    c = W.paged_cache(B, Hkv, D, lens, seed=7, device="cuda", extra_blocks=3)
+    qi, qs = _quant_query(sage, B, Hq, D, seed=8)
+    dbg = torch.full((B, Hq, max(lens)), -(2 ** 31), dtype=torch.int32, device="cuda")
+    _run(sage, qi, qs, c, max(lens), num_segments=2, debug_scores=dbg)
+    torch.cuda.synchronize()
+    d = np_(dbg)
+    for b in range(B):
+        for h in range(Hq):
+            g = h // (Hq // Hkv)
+            keys = oracle.gather_paged(np_(c.k_cache), np_(c.block_table)[b], lens[b], g)
+            ref = oracle.qk_int32(np_(qi)[b, h][None], keys)[0]
+            assert np.array_equal(d[b, h, :lens[b]], ref), (b, h)
+            assert np.all(d[b, h, lens[b]:] == -(2 ** 31))
+
+
+def test_decode_adversarial_int32_bound(sage):
+    """All-+-127 codes at D=256: raw scores hit the 256*127*127 bound exactly."""
+    B, Hq, Hkv, D = 1, 6, 1, 256
+    c = W.paged_cache(B, Hkv, D, [32], seed=1, device="cuda")
+    c.k_cache.fill_(127)
+    c.k_cache[:, :, :, 8:, :] = -127          # slots 8..15 negative
+    qi = torch.full((B, Hq, D), 127, dtype=torch.int8, device="cuda")
+    qi[0, 3] = -127
+    qs = torch.full((B, Hq), 0.01, dtype=torch.float32, device="cuda")
+    dbg = torch.zeros((B, Hq, 32), dtype=torch.int32, device="cuda")
+    _run(sage, qi, qs, c, 32, num_segments=1, debug_scores=dbg)
+    torch.cuda.synchronize()
+    d = np_(dbg)
+    bound = 256 * 127 * 127
+    assert d[0, 0, 0] == bound and d[0, 0, 8] == -bound and d[0, 3, 0] == -bound
+
+
+def test_decode_permuted_block_table_bitwise(sage):
+    B, Hq, Hkv, D = 2, 24, 4, 256
+    lens = [1000, 777]
+    c = W.paged_cache(B, Hkv, D, lens, seed=21, device="cuda")
+    qi, qs = _quant_query(sage, B, Hq, D, seed=22)
+    out1 = _run(sage, qi, qs, c, max(lens), num_segments=4)
+    # move every page to a new physical slot and remap the table
+    nblk = c.k_cache.shape[0]
+    perm = torch.randperm(nblk, generator=torch.Generator().manual_seed(3)).to("cuda")
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(nblk, device="cuda")
+    c2 = W.PagedCache(c.k_cache[inv], c.v_cache[inv], c.k_scale[inv], c.v_scale[inv],
+                      perm[c.block_table.long()].to(torch.int32), c.lens)
+    out2 = _run(sage, qi, qs, c2, max(lens), num_segments=4)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)
+
+
+def test_decode_split_invariance(sage):
+    B, Hq, Hkv, D = 2, 24, 4, 128
+    lens = [2048, 1500]
+    c = W.paged_cache(B, Hkv, D, lens, seed=5, device="cuda")
+    qi, qs = _quant_query(sage, B, Hq, D, seed=6)
+    ref, lref = _run(sage, qi, qs, c, max(lens), num_segments=1, return_lse=True,
+                     out_dtype=torch.float16)
+    for S in (2, 7, 32):
+        out, lse = _run(sage, qi, qs, c, max(lens), num_segments=S, return_lse=True,
+                        out_dtype=torch.float16)
+        torch.cuda.synchronize()
+        assert_close(f32(out), f32(ref), "split %d" % S, rel=2e-3, abs_=1e-3)
+        assert_close(np_(lse), np_(lref), "lse split %d" % S, rel=1e-5, abs_=1e-4)
+
+
+def test_decode_empty_context(sage):
+    B, Hq, Hkv, D = 3, 8, 1, 64
+    lens = [0, 20, 0]
+    c = W.paged_cache(B, Hkv, D, [max(x, 1) for x in lens], seed=9, device="cuda")
+    c.lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    qi, qs = _quant_query(sage, B, Hq, D, seed=10)
+    out, lse = _run(sage, qi, qs, c, 20, num_segments=0, return_lse=True,
+                    out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    o_ref, l_ref = _oracle(qi, qs, c)
+    assert np.all(f32(out)[[0, 2]] == 0) and np.all(np.isneginf(np_(lse)[[0, 2]]))
+    assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
+
+
+def test_decode_bad_block_sets_error_word(sage):
+    B, Hq, Hkv, D = 1, 6, 1, 128
+    c = W.paged_cache(B, Hkv, D, [64], seed=2, device="cuda")
+    qi, qs = _quant_query(sage, B, Hq, D, seed=3)
+    sage.check_device_status()
+    bad = c.block_table.clone()
+    bad[0, 1] = c.k_cache.shape[0] + 100       # out of range: must not be read
+    c_bad = W.PagedCache(c.k_cache, c.v_cache, c.k_scale, c.v_scale, bad, c.lens)
+    _run(sage, qi, qs, c_bad, 64, num_segments=1, out_dtype=torch.float16)
+    st, word = sage.check_device_status()
+    assert st == sage.SAGE_ERR_BAD_BLOCK and word & 2
+    # the context is still usable
+    out = _run(sage, qi, qs, c, 64, num_segments=1, out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert_close(f32(out), _oracle(qi, qs, c)[0])
+
+
+def test_bounded_wait_times_out_and_context_survives(sage):
+    sage.check_device_status()
+    sage.debug_timeout_probe(20000)            # 20 ms wait nobody ends
+    st, word = sage.check_device_status()
+    assert st == sage.SAGE_ERR_TIMEOUT and word & 1
+    x = torch.randn(1, 1, 16, 64, device="cuda", dtype=torch.float16)
+    q, s, _, _ = sage.sage_quant_int8(x)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+
+
+def test_decode_launch_record(sage):
+    c = W.paged_cache(2, 4, 256, [4096, 4096], seed=1, device="cuda")
+    qi, qs = _quant_query(sage, 2, 24, 256, seed=1)
+    _run(sage, qi, qs, c, 4096, num_segments=8)
+    info = sage.last_launch_info()
+    assert info["kernel"] == "decode_kernel" and info["num_segments"] == 8
+    assert info["launches"] == 2 and info["grid"] == (8, 4, 2)
+
+
+def test_decode_paged_decode_full_size(sage):
+    """The B8 / 24:4 GQA / D256 / 8192-token workload, every output vs the oracle."""
+    P = W.WORKLOADS["paged_decode"].params
+    c = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["ctx"]] * P["B"], seed=P["seed"],
+                      device="cuda")
+    qi, qs = _quant_query(sage, P["B"], P["Hq"], P["D"], seed=P["seed"])
+    out, lse = _run(sage, qi, qs, c, P["ctx"], return_lse=True)
+    torch.cuda.synchronize()
+    o_ref, l_ref = _oracle(qi, qs, c)
+    assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
+
+
+@pytest.mark.parametrize("L", [8192, 16384, 32768])
+@pytest.mark.parametrize("B", [1, 16, 64])
+def test_decode_sweep(sage, L, B):
+    P = W.WORKLOADS["decode_sweep"].params
+    c = W.paged_cache(B, P["Hkv"], P["D"], [L] * B, seed=P["seed"] + L + B, device="cuda")
+    qi, qs = _quant_query(sage, B, P["Hq"], P["D"], seed=P["seed"])
+    out, lse = _run(sage, qi, qs, c, L, return_lse=True)
+    torch.cuda.synchronize()
+    # all (b, kv head) pairs up to 16 sequences; a seeded sample beyond
+    pairs = [(b, g) for b in range(B) for g in range(P["Hkv"])]
+    if B > 16:
+        rng = np.random.default_rng(L)
+        pairs = [pairs[i] for i in rng.choice(len(pairs), 24, replace=False)]
+    o_ref, l_ref = _oracle(qi, qs, c, pairs=pairs)
+    grp = P["Hq"] // P["Hkv"]
+    rows = [(b, h) for (b, g) in pairs for h in range(g * grp, (g + 1) * grp)]
+    bi, hi = np.array(rows).T
+    assert_close(f32(out)[bi, hi], o_ref[bi, hi])
+    assert_close(np_(lse)[bi, hi], l_ref[bi, hi], "lse")

@@ -1,0 +1,89 @@
+"""GPU parity: sage_quant_int8 against the oracle, bit-exact codes and scales."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import f32, np_
+from int8_quantized_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_quant(sage, x, block, smooth=False, layout="HND"):
+    q, s, mu, _ = sage.sage_quant_int8(x, block_tokens=block, smooth=smooth, layout=layout)
+    torch.cuda.synchronize()
+    xh = f32(x) if layout == "HND" else f32(x).transpose(0, 2, 1, 3)
+    if smooth:
+        mu_ref = oracle.token_mean(xh)
+        # the mean is an exact sum rounded once: bit-exact on these inputs
+        assert np.array_equal(np_(mu), mu_ref)
+    q_ref, s_ref, _ = oracle.quant_int8(xh, block_tokens=block, smooth=smooth,
+                                        mu=np_(mu) if smooth else None)
+    assert np.array_equal(np_(s), s_ref), "scales differ"
+    assert np.array_equal(np_(q), q_ref), "codes differ in %d places" % int((np_(q) != q_ref).sum())
+    return q, s, mu
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+@pytest.mark.parametrize("block", [1, 64, 128])
+def test_quant_small_bit_exact(sage, D, dtype, block):
+    qkv = W.dense_qkv(2, 3, 3, 200, 200, D, seed=D + block, dtype=dtype, device="cuda",
+                      k_offset_std=2.0)
+    _check_quant(sage, qkv.q, block)
+    _check_quant(sage, qkv.k, block, smooth=True)
+
+
+def test_quant_nhd_strided(sage):
+    x = W.dense_qkv(1, 4, 4, 77, 77, 128, seed=5, device="cuda").q     # [B,H,S,D]
+    nhd = x.transpose(1, 2).contiguous()                                  # [B,S,H,D]
+    q1, s1, _ = _check_quant(sage, nhd, 1, layout="NHD")
+    q2, s2, _, _ = sage.sage_quant_int8(x, block_tokens=1)
+    assert torch.equal(q1, q2) and torch.equal(s1, s2)
+
+
+def test_quant_degenerate(sage):
+    x = torch.zeros((1, 2, 130, 64), dtype=torch.float16, device="cuda")
+    x[0, 1, 5:, 3] = 2.5
+    q, s, _ = _check_quant(sage, x, 128)
+    assert np_(s)[0, 0, 0] == 0.0 and np.all(np_(q)[0, 0] == 0)
+    # empty input: nothing to do
+    e = torch.zeros((1, 2, 0, 64), dtype=torch.float16, device="cuda")
+    q, s, _, _ = sage.sage_quant_int8(e)
+    assert q.numel() == 0
+
+
+def test_quant_row_bias(sage):
+    qkv = W.dense_qkv(1, 6, 2, 96, 96, 128, seed=11, device="cuda", k_offset_std=2.0)
+    _, _, mu, _ = sage.sage_quant_int8(qkv.k, smooth=True)
+    q, s, _, bias = sage.sage_quant_int8(qkv.q, mu_in=mu)
+    torch.cuda.synchronize()
+    ref = oracle.row_bias(f32(qkv.q), np_(mu))
+    scale = np.abs(f32(qkv.q)).sum(-1) * np.abs(np_(mu)).max()
+    assert np.all(np.abs(np_(bias) - ref) <= 1e-5 * scale + 1e-6)
+    q_ref, s_ref, _ = oracle.quant_int8(f32(qkv.q))
+    assert np.array_equal(np_(q), q_ref) and np.array_equal(np_(s), s_ref)
+
+
+def test_quant_dense_prefill_full_size(sage):
+    """Full-size dense-prefill inputs: per-block Q (128) and smoothed K (64), every bit."""
+    P = W.WORKLOADS["dense_prefill"].params
+    qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
+                      dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
+    _check_quant(sage, qkv.k, 64, smooth=True)
+    _check_quant(sage, qkv.q, 128)
+
+
+def test_quant_chunked_prefill_full_size(sage):
+    P = W.WORKLOADS["chunked_prefill"].params
+    qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
+                      dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
+    _check_quant(sage, qkv.k, 1, smooth=True)
+    _check_quant(sage, qkv.q, 1)
+
+
+def test_quant_decode_query_full_size(sage):
+    P = W.WORKLOADS["paged_decode"].params
+    q = W.decode_query(P["B"], P["Hq"], P["D"], seed=P["seed"], device="cuda")
+    _check_quant(sage, q[:, :, None, :], 1)
