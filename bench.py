@@ -1,0 +1,398 @@
+"""Benchmark of the INT8-QK attention hot path on GB300.
+
+One step = one pass of the decode hot path over one batch of the paged
+decode workload (batch 8, 24 query / 4 KV heads, head_dim 256, 8192-token
+INT8 paged context): quantise the bf16 query (INT8, per token/head), run
+the split-K paged decode kernel, merge the segments with the LSE combine.
+
+Prints ONE JSON line (rank 0).  `value` is the decode workload's
+algorithmic bytes (INT8 K/V pages + their scales + block table + query
+codes/scales + bf16 query in + bf16 output) per second of device time,
+inputs resident in HBM, L2 flushed between steps.  `e2e` is the same
+metric through the public API with the per-step inputs (query, block
+table, context lengths) copied from pinned host memory and the output
+copied back inside the timed region; the KV cache is device-resident state,
+as in serving.  `roofline` describes the decode kernel.  A dense-prefill
+and chunked-prefill measurement is added under `prefill` when that kernel
+is available.
+
+--impl reference times the CPU oracle (the plain C reference of the
+method) on the host cores on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT8-QK attention prefill TFLOP/s and paged-decode KV GB/s on 1 GB300 (% roofline)"
+WORKLOAD = "paged_decode"
+L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def decode_bytes(B, Hq, Hkv, D, ctx, max_blocks):
+    """Algorithmic bytes of one decode step (what the method must move)."""
+    kv = 2 * B * ctx * Hkv * D            # INT8 K and V pages
+    scales = 2 * B * ctx * Hkv * 4        # fp32 per-token K and V scales
+    table = B * max_blocks * 4 + B * 4    # block table + context lengths
+    q_bf16 = B * Hq * D * 2               # query in
+    q_codes = B * Hq * D + B * Hq * 4     # INT8 query + scale (written once, read once)
+    out = B * Hq * D * 2                  # bf16 output
+    kernel = kv + scales + table + q_codes
+    step = kv + scales + table + q_bf16 + 2 * q_codes + out
+    return kernel, step
+
+
+def run_ours(args):
+    import torch
+
+    from int8_quantized_attention_gb300 import binding as sage
+    from int8_quantized_attention_gb300 import build
+    from int8_quantized_attention_gb300 import workloads as W
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    build.build()
+    P = W.WORKLOADS[WORKLOAD].params
+    B, Hq, Hkv, D, ctx = P["B"], P["Hq"], P["Hkv"], P["D"], P["ctx"]
+    # every rank runs its own replica of the workload (independent batches)
+    cache = W.paged_cache(B, Hkv, D, [ctx] * B, seed=P["seed"] + rank, device="cuda")
+    q = W.decode_query(B, Hq, D, seed=P["seed"] + rank, device="cuda")
+    max_blocks = cache.block_table.shape[1]
+    S = sage.decode_num_segments(B, Hq, Hkv, ctx)
+    kbytes, sbytes = decode_bytes(B, Hq, Hkv, D, ctx, max_blocks)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def step(ev=None):
+        qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
+        qi = qi.view(B, Hq, D)
+        qs = qs.view(B, Hq)
+        if ev is not None:
+            ev[0].record(stream)
+        op, lp = sage.sage_attn_decode_paged_partials(qi, qs, cache.k_cache, cache.v_cache,
+                                                      cache.k_scale, cache.v_scale,
+                                                      cache.block_table, cache.lens, ctx, S)
+        if ev is not None:
+            ev[1].record(stream)
+        return sage.sage_splitk_combine(op, lp, out_dtype=torch.bfloat16)
+
+    for _ in range(args.warmup):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    st, word = sage.check_device_status()
+    if st != 0:
+        raise RuntimeError("device error word %d after warm-up" % word)
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    barrier()
+    with ClockSampler(local) as clk:
+        for i in range(args.steps):
+            flush.zero_()                 # L2 flush outside the timed window
+            starts[i].record(stream)
+            step(kev[i])
+            ends[i].record(stream)
+        barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    kern_ms = [a.elapsed_time(b) for a, b in kev]
+    t_ms = sum(step_ms)
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([t_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_ms = float(t.item())
+    value = sbytes * ws * args.steps / (t_ms * 1e-3) / 1e9
+
+    # ---- end to end through the public API, host buffers
+    e2e = None
+    if rank == 0 or ws > 1:
+        q_host = q.cpu().pin_memory()
+        bt_host = cache.block_table.cpu().pin_memory()
+        lens_host = cache.lens.cpu().pin_memory()
+        out_host = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+        q_dev = torch.empty_like(q)
+        bt_dev = torch.empty_like(cache.block_table)
+        lens_dev = torch.empty_like(cache.lens)
+        ws_buf = torch.empty(sage.decode_workspace_size(B, Hq, D, S), dtype=torch.uint8,
+                             device="cuda")
+
+        def e2e_step():
+            q_dev.copy_(q_host, non_blocking=True)
+            bt_dev.copy_(bt_host, non_blocking=True)
+            lens_dev.copy_(lens_host, non_blocking=True)
+            qi, qs, _, _ = sage.sage_quant_int8(q_dev[:, :, None, :])
+            out = sage.sage_attn_decode_paged(qi.view(B, Hq, D), qs.view(B, Hq), cache.k_cache,
+                                              cache.v_cache, cache.k_scale, cache.v_scale,
+                                              bt_dev, lens_dev, ctx, num_segments=S,
+                                              workspace=ws_buf)
+            out_host.copy_(out, non_blocking=True)
+
+        for _ in range(args.warmup):
+            e2e_step()
+        torch.cuda.synchronize()
+        es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush.zero_()
+            es[i].record(stream)
+            e2e_step()
+            ee[i].record(stream)
+        torch.cuda.synchronize()
+        e_ms = sum(a.elapsed_time(b) for a, b in zip(es, ee))
+        h2d = q.numel() * 2 + bt_host.numel() * 4 + lens_host.numel() * 4
+        d2h = out_host.numel() * 2
+        e2e = {"value": round(sbytes * args.steps / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e_ms / args.steps, 5)}
+    torch.cuda.synchronize()
+    st, word = sage.check_device_status()
+    if st != 0:
+        raise RuntimeError("device error word %d after the timed region" % word)
+
+    peaks, kind = _peaks()
+    k_avg = statistics.mean(kern_ms)
+    achieved = kbytes / (k_avg * 1e-3) / 1e9
+    roof = {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
+            "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "peak_kind": kind, "traffic": _profile_traffic("decode_kernel"),
+            "algorithmic_bytes": kbytes, "avg_launch_ms": round(k_avg, 5)}
+    if rank != 0:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        return None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_ms / args.steps, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8",
+        "data": "synthetic (seeded; uniform INT8 cache, U(0.005,0.02) scales, N(0,1) bf16 query)",
+        "config": {"workload": "paged_decode B8 Hq24 Hkv4 D256 ctx8192 block16",
+                   "segments": S, "l2": "flushed between steps (512 MB write)",
+                   "step": "quant(Q) + split-K paged decode + LSE combine",
+                   "parallelism": "replicas" if ws > 1 else "single"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": 3 * args.steps,
+        "clocks": clk.summary(),
+    }
+    if args.cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_decode(args.cpu_seconds)
+    if args.prefill:
+        line["prefill"] = prefill_measure(args)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return line
+
+
+def _profile_traffic(kernel):
+    """dram bytes per launch from the committed ncu summary of the workload, if any."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    return d.get(kernel)
+
+
+def cpu_baseline_decode(seconds: float):
+    """The oracle timed on the host cores on a bounded sample of the workload."""
+    import numpy as np
+
+    import oracle
+    from int8_quantized_attention_gb300 import workloads as W
+
+    P = W.WORKLOADS[WORKLOAD].params
+    B, Hq, Hkv, D, ctx = P["B"], P["Hq"], P["Hkv"], P["D"], P["ctx"]
+    cache = W.paged_cache(B, Hkv, D, [ctx] * B, seed=P["seed"], device="cpu")
+    q = W.decode_query(B, Hq, D, seed=P["seed"], device="cpu").float().numpy()
+    qi, qs, _ = oracle.quant_int8(q[:, :, None, :])
+    qi, qs = qi[:, :, 0], qs[:, :, 0]
+    args = [cache.k_cache.numpy(), cache.v_cache.numpy(), cache.k_scale.numpy(),
+            cache.v_scale.numpy(), cache.block_table.numpy(), cache.lens.numpy()]
+    threads = oracle.default_threads()
+    _, sbytes = decode_bytes(B, Hq, Hkv, D, ctx, cache.block_table.shape[1])
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        oracle.decode_paged(qi, qs, *args, threads=threads)
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or passes >= 50:
+            break
+    return {"value": round(sbytes * passes / el / 1e9, 4), "unit": "GB/s", "cores": threads,
+            "kind": "oracle",
+            "sample": "%d full pass(es) of the paged_decode workload (all 8x4 sequence/kv-head "
+                      "pairs), %.1f s" % (passes, el)}
+
+
+def prefill_measure(args):
+    """Dense-prefill throughput (FLOP over unmasked pairs), if the kernel is built."""
+    try:
+        from int8_quantized_attention_gb300 import prefill_bench
+    except ImportError:
+        return None
+    return prefill_bench.measure(args.warmup, max(args.steps, 3))
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return None
+    import numpy as np  # noqa: F401
+
+    from int8_quantized_attention_gb300 import workloads as W
+    import oracle
+
+    P = W.WORKLOADS[WORKLOAD].params
+    B, Hq, Hkv, D, ctx = P["B"], P["Hq"], P["Hkv"], P["D"], P["ctx"]
+    cache = W.paged_cache(B, Hkv, D, [ctx] * B, seed=P["seed"], device="cpu")
+    q = W.decode_query(B, Hq, D, seed=P["seed"], device="cpu").float().numpy()
+    threads = oracle.default_threads()
+    _, sbytes = decode_bytes(B, Hq, Hkv, D, ctx, cache.block_table.shape[1])
+    # each step: the whole workload (all 32 (sequence, kv head) pairs), ~0.3 s on 8+ cores
+    pairs = [(b, g) for b in range(B) for g in range(Hkv)]
+    frac = len(pairs) / (B * Hkv)
+    cargs = [cache.k_cache.numpy(), cache.v_cache.numpy(), cache.k_scale.numpy(),
+             cache.v_scale.numpy(), cache.block_table.numpy(), cache.lens.numpy()]
+
+    def one():
+        qi, qs, _ = oracle.quant_int8(q[:, :, None, :])
+        oracle.decode_paged(qi[:, :, 0], qs[:, :, 0], *cargs, threads=threads, pairs=pairs)
+
+    for _ in range(args.warmup):
+        one()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        one()
+        times.append(time.perf_counter() - t0)
+    t = sum(times)
+    value = sbytes * frac * args.steps / t / 1e9
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "i8", "data": "synthetic",
+            "config": {"workload": "paged_decode B8 Hq24 Hkv4 D256 ctx8192 block16",
+                       "step": "quant(Q) + paged decode, CPU oracle"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle",
+                             "sample": "per step: the full paged_decode workload (32 sequence/"
+                                       "kv-head pairs)"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    line = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -147,6 +147,17 @@ size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments);
 sage_status_t sage_attn_decode_paged(const sage_decode_args_t *args, void *workspace,
                                      size_t workspace_bytes, void *stream);
 
+/* Same decode, without the combine: writes each segment's normalised output
+ * o_part [B*Hq, S, D] and natural-log LSE lse_part [B*Hq, S] (fp32, caller
+ * buffers, o_part 16-byte aligned; 0 / -inf for a segment with no keys).
+ * num_segments must be >= 1; segments that would start past the longest
+ * context are dropped, so S = ceil(P / ceil(P / num_segments)) with
+ * P = ceil(max_context_len / 16) (S = 1 when P = 0); S is also returned in
+ * *segments_used (host, optional).  sage_splitk_combine over these
+ * partials gives the sage_attn_decode_paged result. */
+sage_status_t sage_attn_decode_paged_partials(const sage_decode_args_t *args, float *o_part,
+                                              float *lse_part, int *segments_used, void *stream);
+
 /* --------------------------------------------------------------------------
  * Split-K LSE combine  ([P1] section 4 split-K; [P3] LSE returned "for
  * concatenation").  For every row r:

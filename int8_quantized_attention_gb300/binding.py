@@ -90,6 +90,9 @@ def lib():
         L.sage_attn_decode_workspace_size.restype = ctypes.c_size_t
         L.sage_attn_decode_paged.argtypes = [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t, _vp]
         L.sage_attn_decode_paged.restype = _i
+        L.sage_attn_decode_paged_partials.argtypes = [ctypes.POINTER(DecodeArgs), _vp, _vp,
+                                                      ctypes.POINTER(_i), _vp]
+        L.sage_attn_decode_paged_partials.restype = _i
         L.sage_debug_decode_qk_int32.argtypes = [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t,
                                                  _vp, _vp]
         L.sage_debug_decode_qk_int32.restype = _i
@@ -242,6 +245,33 @@ def sage_attn_decode_paged(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, 
         _check(lib().sage_attn_decode_paged(ctypes.byref(a), _ptr(workspace), ws_bytes,
                                             _stream(stream)))
     return (out, lse) if return_lse else out
+
+
+def decode_segments_used(max_context_len: int, num_segments: int) -> int:
+    """Segment count the partials layout uses (see sage_attn_decode_paged_partials)."""
+    pages = (int(max_context_len) + 15) // 16
+    if pages == 0:
+        return 1
+    pps = (pages + num_segments - 1) // num_segments
+    return (pages + pps - 1) // pps
+
+
+def sage_attn_decode_paged_partials(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale,
+                                    block_table, context_lens, max_context_len: int,
+                                    num_segments: int, *, sm_scale=None, stream=None):
+    """Decode without the combine: returns (o_part [B,Hq,S,D], lse_part [B,Hq,S])."""
+    B, Hq, D = q_int8.shape
+    S = decode_segments_used(max_context_len, num_segments)
+    o_part = torch.empty((B, Hq, S, D), dtype=torch.float32, device=q_int8.device)
+    lse_part = torch.empty((B, Hq, S), dtype=torch.float32, device=q_int8.device)
+    dummy = torch.empty((1,), dtype=torch.float16, device=q_int8.device)
+    a = _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
+                     context_lens, max_context_len, sm_scale, num_segments, dummy, None)
+    used = _i(0)
+    _check(lib().sage_attn_decode_paged_partials(ctypes.byref(a), _ptr(o_part), _ptr(lse_part),
+                                                 ctypes.byref(used), _stream(stream)))
+    assert used.value == S, (used.value, S)
+    return o_part, lse_part
 
 
 def sage_splitk_combine(o_part: torch.Tensor, lse_part: torch.Tensor, out_dtype=torch.bfloat16,

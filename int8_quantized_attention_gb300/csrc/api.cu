@@ -94,6 +94,20 @@ __global__ void timeout_probe_kernel(long long limit_ns, int *err) {
 
 }  // namespace
 
+namespace sage {
+int report_error(int status, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_msg = buf;
+    return status;
+}
+int device_error_word(int **out) { return (int)error_word(out); }
+void record_launch(const LaunchLog &log) { g_last = log; }
+}  // namespace sage
+
 // ---------------------------------------------------------------------------
 
 SAGE_API const char *sage_get_last_error_message(void) { return g_msg.c_str(); }
@@ -246,8 +260,12 @@ SAGE_API size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_se
     return o + rows * sizeof(float);
 }
 
+// partials_o / partials_l (optional): write the segment partials there and
+// skip the combine (num_segments must be given).
 static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
-                                size_t workspace_bytes, int32_t *dbg, void *stream) {
+                                size_t workspace_bytes, int32_t *dbg, void *stream,
+                                float *partials_o = nullptr, float *partials_l = nullptr,
+                                int *segments_used = nullptr) {
     if (!a) return fail(SAGE_ERR_INVALID_ARG, "args is NULL");
     if (!head_dim_ok(a->D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", a->D);
     if (a->out_dtype != SAGE_F16 && a->out_dtype != SAGE_BF16)
@@ -297,6 +315,16 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
     p.out = a->out, p.out_bf16 = a->out_dtype == SAGE_BF16, p.lse = a->lse;
     p.dbg = dbg, p.dbg_stride = a->max_context_len;
     p.err = ew;
+    if (segments_used) *segments_used = S;
+    if (partials_o) {
+        if (!aligned(partials_o, 16) || !partials_l)
+            return fail(SAGE_ERR_INVALID_ARG, "o_part (16-byte aligned) and lse_part are required");
+        p.o_part = partials_o;
+        p.lse_part = partials_l;
+        p.force_partials = 1;
+        cudaError_t e = sage::launch_decode(p, static_cast<cudaStream_t>(stream), g_last);
+        return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "decode launch");
+    }
     if (S > 1) {
         const size_t need = sage_attn_decode_workspace_size(a->B, a->Hq, a->D, S);
         if (!workspace || workspace_bytes < need)
@@ -326,6 +354,16 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
 SAGE_API sage_status_t sage_attn_decode_paged(const sage_decode_args_t *args, void *workspace,
                                               size_t workspace_bytes, void *stream) {
     return run_decode(args, workspace, workspace_bytes, nullptr, stream);
+}
+
+SAGE_API sage_status_t sage_attn_decode_paged_partials(const sage_decode_args_t *args,
+                                                       float *o_part, float *lse_part,
+                                                       int *segments_used, void *stream) {
+    if (!args) return fail(SAGE_ERR_INVALID_ARG, "args is NULL");
+    if (args->num_segments < 1)
+        return fail(SAGE_ERR_INVALID_ARG, "num_segments must be given (>= 1) for partials");
+    if (!o_part) return fail(SAGE_ERR_INVALID_ARG, "o_part is NULL");
+    return run_decode(args, nullptr, 0, nullptr, stream, o_part, lse_part, segments_used);
 }
 
 SAGE_API sage_status_t sage_debug_decode_qk_int32(const sage_decode_args_t *args, void *workspace,
@@ -398,6 +436,7 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, int32_t *dbg, voi
     p.qk_scale_log2 = sm * 1.4426950408889634f;
     p.out = a->out, p.out_bf16 = a->out_dtype == SAGE_BF16, p.lse = a->lse;
     p.dbg = dbg;
+    p.dbg_stride = a->max_prefix_len + a->Sk;
     p.err = ew;
     cudaError_t e = sage::launch_prefill(p, static_cast<cudaStream_t>(stream), g_last);
     if (e == cudaErrorNotSupported)

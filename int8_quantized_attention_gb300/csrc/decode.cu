@@ -323,7 +323,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         }
     }
     __syncthreads();
-    const bool direct = p.num_segments == 1;
+    const bool direct = p.num_segments == 1 && !p.force_partials;
     for (int idx = threadIdx.x; idx < nheads * D; idx += kThreads) {
         const int j = idx / D, d = idx - j * D;
         float M = -INFINITY;

@@ -72,6 +72,7 @@ struct DecodeParams {
     float *lse;               // optional [B*Hq] when num_segments == 1
     int32_t *dbg;             // optional raw score dump [B*Hq, dbg_stride]
     int dbg_stride;
+    int force_partials;       // write o_part/lse_part even with one segment
     int *err;
 };
 
@@ -100,12 +101,18 @@ struct PrefillParams {
     void *out;
     int out_bf16;
     float *lse;
-    int32_t *dbg;             // optional [B,Hq,Sq,max_prefix_len+Sk]
+    int32_t *dbg;             // optional [B,Hq,Sq,dbg_stride]
+    int dbg_stride;           // max_prefix_len + Sk
     int *err;
 };
 
 cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
 
 cudaError_t launch_timeout_probe(int timeout_us, int *err, cudaStream_t st, LaunchLog &log);
+
+// Host-layer services shared by entry points defined outside api.cu.
+int report_error(int status, const char *fmt, ...);   // sets the thread's last message
+int device_error_word(int **out);                      // this device's error word
+void record_launch(const LaunchLog &log);              // updates sage_last_launch_info
 
 }  // namespace sage

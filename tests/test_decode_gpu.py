@@ -198,3 +198,30 @@ def test_decode_sweep(sage, L, B):
     bi, hi = np.array(rows).T
     assert_close(f32(out)[bi, hi], o_ref[bi, hi])
     assert_close(np_(lse)[bi, hi], l_ref[bi, hi], "lse")
+
+
+def test_decode_partials_then_combine(sage):
+    B, Hq, Hkv, D = 2, 24, 4, 256
+    lens = [3000, 1234]
+    c = W.paged_cache(B, Hkv, D, lens, seed=31, device="cuda")
+    qi, qs = _quant_query(sage, B, Hq, D, seed=32)
+    op, lp = sage.sage_attn_decode_paged_partials(qi, qs, c.k_cache, c.v_cache, c.k_scale,
+                                                  c.v_scale, c.block_table, c.lens, max(lens), 5)
+    out, lse = sage.sage_splitk_combine(op, lp, out_dtype=torch.float16, return_lse=True)
+    full, lfull = _run(sage, qi, qs, c, max(lens), num_segments=5, return_lse=True,
+                       out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    assert torch.equal(out, full) and torch.equal(lse, lfull)
+    # each segment partial is itself the attention over its own key range
+    pps = ((max(lens) + 15) // 16 + 4) // 5 * 16
+    seg = 1
+    lo, hi = seg * pps, min((seg + 1) * pps, lens[1])
+    keys = oracle.gather_paged(np_(c.k_cache), np_(c.block_table)[1], lens[1], 0)[lo:hi]
+    ks = oracle.gather_paged_scale(np_(c.k_scale), np_(c.block_table)[1], lens[1], 0)[lo:hi]
+    vals = oracle.gather_paged(np_(c.v_cache), np_(c.block_table)[1], lens[1], 0)[lo:hi]
+    vs = oracle.gather_paged_scale(np_(c.v_scale), np_(c.block_table)[1], lens[1], 0)[lo:hi]
+    o1, l1 = oracle.attend(np_(qi)[1, :6], np_(qs)[1, :6], keys, ks,
+                           vals.astype(np.float64) * vs[:, None].astype(np.float64),
+                           sm_scale=1 / 16)
+    assert_close(np_(op)[1, :6, seg], o1, "segment partial")
+    assert_close(np_(lp)[1, :6, seg], l1, "segment lse")
