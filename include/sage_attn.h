@@ -159,6 +159,33 @@ sage_status_t sage_attn_decode_paged_partials(const sage_decode_args_t *args, fl
                                               float *lse_part, int *segments_used, void *stream);
 
 /* --------------------------------------------------------------------------
+ * Allocation-free decode (no counterpart on the source pages: a deployment
+ * convenience of this library).
+ *
+ * Same computation and result as sage_attn_decode_paged, for callers that
+ * cannot hand the library a workspace: code inside a CUDA graph captured
+ * with a fixed memory plan, plugins whose host framework owns every device
+ * allocation, or embedders that must not re-enter their allocator from the
+ * attention call.  The split-K partials live in one device array built into
+ * the library, of sage_attn_decode_noalloc_max_bytes() bytes (8 MiB) per
+ * GPU that loads the library, held until the process exits.  The call
+ * allocates and frees nothing.
+ *   - Requests whose partials exceed that size (B*Hq*S*(D+1)*4 bytes, S the
+ *     segment count actually used) are rejected with SAGE_ERR_INVALID_ARG and
+ *     a message saying how many bytes were needed; with one segment no
+ *     scratch is used at all.
+ *   - The first call on a device looks the array's address up
+ *     (cudaGetSymbolAddress); make that first call outside any stream
+ *     capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; each call overwrites every slot it reads, so nothing needs
+ *     clearing, but calls that overlap on the GPU (different streams, no
+ *     ordering between them) race on the array: serialise them.
+ * ------------------------------------------------------------------------ */
+size_t sage_attn_decode_noalloc_max_bytes(void);
+sage_status_t sage_attn_decode_paged_noalloc(const sage_decode_args_t *args, void *stream);
+
+/* --------------------------------------------------------------------------
  * Split-K LSE combine  ([P1] section 4 split-K; [P3] LSE returned "for
  * concatenation").  For every row r:
  *   M = max_s lse_part[r,s],  L = M + ln sum_s exp(lse_part[r,s] - M)

@@ -93,6 +93,10 @@ def lib():
         L.sage_attn_decode_paged_partials.argtypes = [ctypes.POINTER(DecodeArgs), _vp, _vp,
                                                       ctypes.POINTER(_i), _vp]
         L.sage_attn_decode_paged_partials.restype = _i
+        L.sage_attn_decode_noalloc_max_bytes.argtypes = []
+        L.sage_attn_decode_noalloc_max_bytes.restype = ctypes.c_size_t
+        L.sage_attn_decode_paged_noalloc.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        L.sage_attn_decode_paged_noalloc.restype = _i
         L.sage_debug_decode_qk_int32.argtypes = [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t,
                                                  _vp, _vp]
         L.sage_debug_decode_qk_int32.restype = _i
