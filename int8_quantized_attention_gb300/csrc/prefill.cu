@@ -4,8 +4,10 @@
 // feature matrix; "INT8 QK MMAC on gfx936 DCU", sections 1, 2.1, 3, 5.2):
 //   S = Q_int8 K_int8^T exactly, each score rescaled by
 //   q_scale[row] * k_scale[col] * sm_scale * log2(e) (+ the smooth_k row bias
-//   on smoothed keys) before a base-2 online softmax; P.V in 16-bit with
-//   FP32 accumulation; O / l and LSE in the epilogue.  Keys come from an
+//   on smoothed keys) before a base-2 online softmax; P.V in f16 with FP32
+//   accumulation (bf16 V is rounded to f16 in shared memory first, as the
+//   README's port converts bf16 V to f16 before its kernel); O / l and LSE
+//   in the epilogue.  Keys come from an
 //   optional paged INT8 prefix followed by the contiguous chunk.
 //
 // GB300 design.  sm_103a has no integer tcgen05 MMA, so QK^T runs on
@@ -266,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ============================================================ MMA issuer
         if (lane == 0 && T > 0) {
             const uint32_t idq = tc::idesc_f16(128, BN, false, false);
-            const uint32_t idp = tc::idesc_f16(128, D, p.v_bf16 != 0, true);
+            const uint32_t idp = tc::idesc_f16(128, D, false, true);  // P.V always in f16
             auto issue_qk = [&](int j) -> bool {
                 const int buf = j & 1;
                 if (!wait_ab(bar(B_KV_FULL + buf), (uint32_t)(j >> 1) & 1u, p.err, abort_flag))
@@ -372,16 +374,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                              (c8 >> 1) * 256 + (r & 15) * 16 +
                                                              (c8 & 1) * 8);
                     uint4 h;
-                    if (p.v_bf16) {
-                        i8x4_to_bf16x4(w.x, h.x, h.y);
-                        i8x4_to_bf16x4(w.y, h.z, h.w);
-                    } else {
-                        i8x4_to_f16x4(w.x, h.x, h.y);
-                        i8x4_to_f16x4(w.y, h.z, h.w);
-                    }
+                    i8x4_to_f16x4(w.x, h.x, h.y);
+                    i8x4_to_f16x4(w.y, h.z, h.w);
                     const int o = (c8 >> 3) * (BN * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
                                   (((c8 & 7) ^ (r & 7)) << 4);
                     *reinterpret_cast<uint4 *>(vf + o) = h;
+                }
+            }
+            if (!t.pre && p.v_bf16) {
+                // bf16 chunk V landed by TMA: round it to f16 in place (same
+                // swizzled position), finite-saturating, so P.V runs in f16
+                const bool w = wait_ab(bar(B_V_FULL + buf), (uint32_t)(j >> 1) & 1u, p.err, abort_flag);
+                if (!__all_sync(0xffffffffu, w)) break;
+                uint4 *vf = reinterpret_cast<uint4 *>(sm + C::OFF_VF + buf * C::VF);
+#pragma unroll 4
+                for (int it = ct; it < BN * D / 8; it += 128) {
+                    uint4 x = vf[it];
+                    uint32_t *u = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u[e]));
+                        __half2 h = __floats2half2_rn(fminf(fmaxf(f.x, -65504.0f), 65504.0f),
+                                                      fminf(fmaxf(f.y, -65504.0f), 65504.0f));
+                        u[e] = *reinterpret_cast<uint32_t *>(&h);
+                    }
+                    vf[it] = x;
                 }
             }
             if (ct < BN) {
@@ -415,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             (row_ok && p.q_bias) ? p.q_bias[((int64_t)b * p.Hq + hq) * p.Sq + i] * p.qk_scale_log2
                                  : 0.0f;
         const int lim = i + off;
-        const bool vb = p.v_bf16 != 0;
         float m_run = -INFINITY, l = 0.0f;
         int done = 0;
         for (int j = 0; j < T; ++j) {
@@ -437,9 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (p.dbg && row_ok) {
                 int32_t *dr = p.dbg + (((int64_t)b * p.Hq + hq) * p.Sq + i) * p.dbg_stride;
-                for (int c = 0; c < t.n; ++c) {
+#pragma unroll
+                for (int c = 0; c < BN; ++c) {
                     const int kg = t.kg0 + c;
-                    if (!p.causal || kg <= lim) dr[kg] = __float2int_rn(s[c]);
+                    if (c < t.n && (!p.causal || kg <= lim)) dr[kg] = __float2int_rn(s[c]);
                 }
             }
             const float *ksc = ksc_all + buf * BN;
@@ -498,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         p0 *= vsc[c0];
                         p1 *= vsc[c0 + 1];
                     }
-                    pk[e] = pack2(p0, p1, vb);
+                    pk[e] = pack2(p0, p1, false);
                 }
                 tc::st32(s_t + c * 32, pk);
             }

@@ -1,0 +1,224 @@
+"""GPU parity: the tcgen05 prefill kernel against the oracle.
+
+Raw INT32 scores (through the debug dump of the same tile path) must be
+bit-exact; outputs and LSE within rel-L2 5e-3 / max-abs 2e-3 of the
+oracle's fp64 quantized-math result.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from helpers import assert_close, f32, np_
+from int8_quantized_attention_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _quant(sage, qkv, q_block, k_block, smooth):
+    qi, qs, _, _ = sage.sage_quant_int8(qkv.q, block_tokens=q_block)
+    ki, ks, mu, _ = sage.sage_quant_int8(qkv.k, block_tokens=k_block, smooth=smooth)
+    bias = None
+    if smooth:
+        _, _, _, bias = sage.sage_quant_int8(qkv.q, block_tokens=q_block, mu_in=mu)
+    return qi, qs, ki, ks, mu, bias
+
+
+def _oracle(qi, qs, qb, ki, ks, kb, v, causal, bias=None, prefix=None, rows=None):
+    pre = None
+    if prefix is not None:
+        pre = dict(k_cache=np_(prefix.k_cache), v_cache=np_(prefix.v_cache),
+                   k_scale=np_(prefix.k_scale), v_scale=np_(prefix.v_scale),
+                   block_table=np_(prefix.block_table), lens=np_(prefix.lens))
+    return oracle.prefill(np_(qi), np_(qs), qb, np_(ki), np_(ks), kb, f32(v), causal=causal,
+                          q_bias=None if bias is None else np_(bias).astype(np.float64),
+                          prefix=pre, rows=rows)
+
+
+def _prefix_dict(c, max_len):
+    return dict(k_cache=c.k_cache, v_cache=c.v_cache, k_scale=c.k_scale, v_scale=c.v_scale,
+                block_table=c.block_table, lens=c.lens, max_len=max_len)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_raw_scores_bit_exact(sage, D, causal):
+    B, Hq, Hkv, S = 1, 2, 1, 200
+    qkv = W.dense_qkv(B, Hq, Hkv, S, S, D, seed=D, device="cuda")
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    dbg = torch.full((B, Hq, S, S), -(2 ** 31), dtype=torch.int32, device="cuda")
+    sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=causal, debug_scores=dbg)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    d = np_(dbg)
+    for h in range(Hq):
+        ref = oracle.qk_int32(np_(qi)[0, h], np_(ki)[0, h // 2])
+        if causal:
+            vis = np.tril(np.ones((S, S), bool))
+            assert np.array_equal(d[0, h][vis], ref[vis])
+            assert np.all(d[0, h][~vis] == -(2 ** 31))
+        else:
+            assert np.array_equal(d[0, h], ref)
+
+
+def test_prefill_adversarial_int32_extremes(sage):
+    """+-127 codes at D = 256: every raw score is +-4,129,024 exactly."""
+    B, H, S, D = 1, 1, 128, 256
+    qi = torch.full((B, H, S, D), 127, dtype=torch.int8, device="cuda")
+    qi[:, :, 1::2] = -127
+    ki = torch.full((B, H, S, D), 127, dtype=torch.int8, device="cuda")
+    ki[:, :, 64:] = -127
+    qs = torch.full((B, H, S), 1e-4, dtype=torch.float32, device="cuda")
+    ks = torch.full((B, H, S), 1e-4, dtype=torch.float32, device="cuda")
+    v = torch.randn((B, H, S, D), dtype=torch.float16, device="cuda")
+    dbg = torch.zeros((B, H, S, S), dtype=torch.int32, device="cuda")
+    sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, v, causal=False, debug_scores=dbg)
+    torch.cuda.synchronize()
+    ref = oracle.qk_int32(np_(qi)[0, 0], np_(ki)[0, 0])
+    assert np.abs(ref).max() == 256 * 127 * 127
+    assert np.array_equal(np_(dbg)[0, 0], ref)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("S", [128, 200, 333])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("vdt", ["fp16", "bf16"])
+def test_prefill_small_per_token(sage, D, S, causal, vdt):
+    B, Hq, Hkv = 2, 4, 2
+    qkv = W.dense_qkv(B, Hq, Hkv, S, S, D, seed=S + D, dtype="fp16", device="cuda", v_dtype=vdt)
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    out, lse = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=causal,
+                                      out_dtype=torch.float16, return_lse=True)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    o_ref, l_ref = _oracle(qi, qs, 1, ki, ks, 1, qkv.v, causal)
+    assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_prefill_per_block_smooth_k(sage, D):
+    B, H, S = 1, 3, 700
+    qkv = W.dense_qkv(B, H, H, S, S, D, seed=7, device="cuda", k_offset_std=2.0)
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 128, 64, True)
+    for causal in (False, True):
+        out, lse = sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, qkv.v, causal=causal,
+                                          q_bias=bias, out_dtype=torch.float16, return_lse=True)
+        torch.cuda.synchronize()
+        o_ref, l_ref = _oracle(qi, qs, 128, ki, ks, 64, qkv.v, causal, bias=bias)
+        assert_close(f32(out), o_ref, "causal=%s" % causal)
+        assert_close(np_(lse), l_ref, "lse causal=%s" % causal)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("P", [0, 100, 256])
+def test_prefill_paged_prefix(sage, D, P):
+    B, Hq, Hkv, Sc = 2, 6, 1, 150
+    qkv = W.dense_qkv(B, Hq, Hkv, Sc, Sc, D, seed=P + D, dtype="bf16", device="cuda",
+                      k_offset_std=2.0)
+    lens = [P, max(P - 37, 0)]
+    c = W.paged_cache(B, Hkv, D, [max(x, 1) for x in lens], seed=P + 1, device="cuda",
+                      extra_blocks=3)
+    c.lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 1, 1, True)
+    out, lse = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=True, q_bias=bias,
+                                      prefix=_prefix_dict(c, max(max(lens), 1)),
+                                      out_dtype=torch.float16, return_lse=True)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    o_ref, l_ref = _oracle(qi, qs, 1, ki, ks, 1, qkv.v, True, bias=bias, prefix=c)
+    assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
+
+
+def test_prefill_paged_prefix_raw_scores(sage):
+    B, Hq, Hkv, Sc, D, P = 1, 2, 1, 64, 256, 77
+    qkv = W.dense_qkv(B, Hq, Hkv, Sc, Sc, D, seed=3, dtype="bf16", device="cuda")
+    c = W.paged_cache(B, Hkv, D, [P], seed=4, device="cuda", extra_blocks=2)
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    dbg = torch.full((B, Hq, Sc, P + Sc), -(2 ** 31), dtype=torch.int32, device="cuda")
+    sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=True,
+                           prefix=_prefix_dict(c, P), debug_scores=dbg)
+    torch.cuda.synchronize()
+    keys = np.concatenate([oracle.gather_paged(np_(c.k_cache), np_(c.block_table)[0], P, 0),
+                           np_(ki)[0, 0]], 0)
+    for h in range(Hq):
+        ref = oracle.qk_int32(np_(qi)[0, h], keys)
+        vis = np.arange(P + Sc)[None, :] <= (np.arange(Sc)[:, None] + P)
+        assert np.array_equal(np_(dbg)[0, h][vis], ref[vis])
+
+
+def test_prefill_launch_record(sage):
+    qkv = W.dense_qkv(1, 2, 2, 256, 256, 128, seed=1, device="cuda")
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=True)
+    info = sage.last_launch_info()
+    assert info["kernel"] == "prefill_kernel" and info["grid"] == (2, 2, 1)
+    assert info["block"] == (320, 1, 1)
+
+
+def test_tiny_prefill_full(sage):
+    """The B1 H2 S128 D64 per-token non-causal workload, every output."""
+    P = W.WORKLOADS["tiny_prefill"].params
+    qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
+                      dtype=P["dtype"], device="cuda")
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    out, lse = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=False,
+                                      sm_scale=1 / 8, return_lse=True)
+    torch.cuda.synchronize()
+    o_ref, l_ref = _oracle(qi, qs, 1, ki, ks, 1, qkv.v, False)
+    assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
+
+
+def test_dense_prefill_full_size_sampled(sage):
+    """B2 H32 S16384 D128 causal per-block + smooth_k + LSE: sampled rows vs the oracle."""
+    P = W.WORKLOADS["dense_prefill"].params
+    qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
+                      dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 128, 64, True)
+    out, lse = sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, qkv.v, causal=True, q_bias=bias,
+                                      return_lse=True)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    rng = np.random.default_rng(0)
+    rows = np.sort(np.concatenate([[0, 1, 127, 128, 8191, 16383],
+                                   rng.choice(P["S"], 58, replace=False)]))
+    pairs = [(0, 0), (0, 17), (1, 5), (1, 31)]
+    for b, h in pairs:
+        sub = lambda t, hh=h: t[b:b + 1, hh:hh + 1]
+        o_ref, l_ref = oracle.prefill(np_(sub(qi)), np_(sub(qs)), 128, np_(sub(ki)), np_(sub(ks)),
+                                      64, f32(sub(qkv.v)), causal=True,
+                                      q_bias=np_(sub(bias)).astype(np.float64), rows=rows)
+        assert_close(f32(out)[b, h, rows], o_ref[0, 0], "b%d h%d" % (b, h))
+        assert_close(np_(lse)[b, h, rows], l_ref[0, 0], "lse b%d h%d" % (b, h))
+
+
+def test_chunked_prefill_full_size_sampled(sage):
+    """B1 Hq24 Hkv4 D256: 2048 new tokens over a 16384-token paged INT8 prefix."""
+    P = W.WORKLOADS["chunked_prefill"].params
+    qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
+                      dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
+    c = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["prefix"]], seed=P["seed"], device="cuda")
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 1, 1, True)
+    out, lse = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=True, q_bias=bias,
+                                      prefix=_prefix_dict(c, P["prefix"]), return_lse=True)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    rng = np.random.default_rng(1)
+    rows = np.sort(np.concatenate([[0, 63, 64, 2047], rng.choice(P["S"], 28, replace=False)]))
+    pre = dict(k_cache=np_(c.k_cache), v_cache=np_(c.v_cache), k_scale=np_(c.k_scale),
+               v_scale=np_(c.v_scale), block_table=np_(c.block_table), lens=np_(c.lens))
+    for h in (0, 5, 6, 23):
+        g = h // 6
+        o_ref, l_ref = oracle.prefill(np_(qi)[:, h:h + 1], np_(qs)[:, h:h + 1], 1,
+                                      np_(ki)[:, g:g + 1], np_(ks)[:, g:g + 1], 1,
+                                      f32(qkv.v)[:, g:g + 1], causal=True,
+                                      q_bias=np_(bias)[:, h:h + 1].astype(np.float64),
+                                      prefix=dict(pre, k_cache=pre["k_cache"][:, g:g + 1],
+                                                  v_cache=pre["v_cache"][:, g:g + 1],
+                                                  k_scale=pre["k_scale"][:, g:g + 1],
+                                                  v_scale=pre["v_scale"][:, g:g + 1]),
+                                      rows=rows)
+        assert_close(f32(out)[0, h, rows], o_ref[0, 0], "h%d" % h)
+        assert_close(np_(lse)[0, h, rows], l_ref[0, 0], "lse h%d" % h)
