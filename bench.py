@@ -71,7 +71,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -144,7 +144,7 @@ def run_ours(args):
     cache = W.paged_cache(B, Hkv, D, [ctx] * B, seed=P["seed"] + rank, device="cuda")
     q = W.decode_query(B, Hq, D, seed=P["seed"] + rank, device="cuda")
     max_blocks = cache.block_table.shape[1]
-    S = sage.decode_num_segments(B, Hq, Hkv, ctx)
+    S = sage.decode_num_segments(B, Hq, Hkv, D, ctx)
     kbytes, sbytes = decode_bytes(B, Hq, Hkv, D, ctx, max_blocks)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -162,6 +162,7 @@ def run_ours(args):
             ev[1].record(stream)
         return sage.sage_splitk_combine(op, lp, out_dtype=torch.bfloat16)
 
+    clk = ClockSampler(local).__enter__()   # samples from warm-up through the timed steps
     for _ in range(args.warmup):
         step()
         flush.zero_()
@@ -181,13 +182,13 @@ def run_ours(args):
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     barrier()
-    with ClockSampler(local) as clk:
-        for i in range(args.steps):
-            flush.zero_()                 # L2 flush outside the timed window
-            starts[i].record(stream)
-            step(kev[i])
-            ends[i].record(stream)
-        barrier()
+    for i in range(args.steps):
+        flush.zero_()                 # L2 flush outside the timed window
+        starts[i].record(stream)
+        step(kev[i])
+        ends[i].record(stream)
+    barrier()
+    clk.__exit__(None, None, None)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
     t_ms = sum(step_ms)
@@ -320,13 +321,137 @@ def cpu_baseline_decode(seconds: float):
                       "pairs), %.1f s" % (passes, el)}
 
 
+def prefill_flops(B, Hq, Sq, prefix, Sk, D, causal):
+    """4*D FLOP per unmasked (query, key) pair (QK^T and P.V)."""
+    if not causal:
+        pairs = Sq * (prefix + Sk)
+    else:
+        off = prefix + Sk - Sq
+        pairs = sum(max(0, min(prefix + Sk, i + off + 1)) for i in range(Sq))
+    return 4 * D * B * Hq * pairs
+
+
 def prefill_measure(args):
-    """Dense-prefill throughput (FLOP over unmasked pairs), if the kernel is built."""
-    try:
-        from int8_quantized_attention_gb300 import prefill_bench
-    except ImportError:
-        return None
-    return prefill_bench.measure(args.warmup, max(args.steps, 3))
+    """Prefill kernel throughput on the dense and chunked prefill workloads."""
+    import torch
+
+    from int8_quantized_attention_gb300 import binding as sage
+    from int8_quantized_attention_gb300 import workloads as W
+
+    peaks, kind = _peaks()
+    peak = peaks["bf16_tflops"]   # f16 dense tensor rate = bf16 rate (nominal ratio 1)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for name in ("dense_prefill", "chunked_prefill"):
+        P = W.WORKLOADS[name].params
+        qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
+                          dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
+        prefix, plen = None, 0
+        if name == "chunked_prefill":
+            c = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["prefix"]], seed=P["seed"],
+                              device="cuda")
+            plen = P["prefix"]
+            prefix = dict(k_cache=c.k_cache, v_cache=c.v_cache, k_scale=c.k_scale,
+                          v_scale=c.v_scale, block_table=c.block_table, lens=c.lens,
+                          max_len=plen)
+        qb, kb = P["q_block"], P["k_block"]
+
+        def quant():
+            ki, ks, mu, _ = sage.sage_quant_int8(qkv.k, block_tokens=kb, smooth=True)
+            qi, qs, _, bias = sage.sage_quant_int8(qkv.q, block_tokens=qb, mu_in=mu)
+            return qi, qs, ki, ks, bias
+
+        qi, qs, ki, ks, bias = quant()
+
+        def attn():
+            return sage.sage_attn_prefill(qi, qs, qb, ki, ks, kb, qkv.v, causal=P["causal"],
+                                          q_bias=bias, prefix=prefix,
+                                          return_lse=P.get("return_lse", False))
+
+        for _ in range(args.warmup):
+            attn()
+        torch.cuda.synchronize()
+        n = max(3, min(args.steps, 10))
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in ev:
+            a.record(stream)
+            attn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        k_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        sv = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(n)]
+        for a, b in sv:
+            a.record(stream)
+            qi, qs, ki, ks, bias = quant()
+            attn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        s_ms = statistics.mean(a.elapsed_time(b) for a, b in sv)
+        st, word = sage.check_device_status()
+        if st != 0:
+            raise RuntimeError("device error word %d in %s" % (word, name))
+        fl = prefill_flops(P["B"], P["Hq"], P["S"], plen, P["S"], P["D"], P["causal"])
+        tf = fl / (k_ms * 1e-3) / 1e12
+        res[name] = {"kernel": "prefill_kernel", "tflops": round(tf, 1),
+                     "frac_of_dense_f16_peak": round(tf / peak, 4), "peak_tflops": peak,
+                     "peak_kind": kind, "kernel_ms": round(k_ms, 4),
+                     "step_ms_with_quant": round(s_ms, 4),
+                     "step_tflops_with_quant": round(fl / (s_ms * 1e-3) / 1e12, 1),
+                     "flop": fl, "launches": n}
+        del qkv, qi, qs, ki, ks, bias, prefix
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_profile(args):
+    """Launch one kernel of a named workload a few times (for ncu captures).
+
+    --profile dense_prefill|chunked_prefill|paged_decode, --heads H shrinks
+    the query heads (and KV heads in proportion) to keep a capture small.
+    """
+    import torch
+
+    from int8_quantized_attention_gb300 import binding as sage
+    from int8_quantized_attention_gb300 import build
+    from int8_quantized_attention_gb300 import workloads as W
+
+    build.build()
+    P = dict(W.WORKLOADS[args.profile].params)
+    if args.heads:
+        ratio = P["Hq"] // P["Hkv"]
+        P["Hq"] = args.heads
+        P["Hkv"] = max(1, args.heads // ratio)
+    if args.profile == "paged_decode":
+        c = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["ctx"]] * P["B"], seed=P["seed"],
+                          device="cuda")
+        q = W.decode_query(P["B"], P["Hq"], P["D"], seed=P["seed"], device="cuda")
+        qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
+        run = lambda: sage.sage_attn_decode_paged(qi[:, :, 0].contiguous(), qs[:, :, 0].contiguous(),
+                                                  c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                                  c.block_table, c.lens, P["ctx"])
+    else:
+        qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
+                          dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
+        prefix = None
+        if args.profile == "chunked_prefill":
+            c = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["prefix"]], seed=P["seed"],
+                              device="cuda")
+            prefix = dict(k_cache=c.k_cache, v_cache=c.v_cache, k_scale=c.k_scale,
+                          v_scale=c.v_scale, block_table=c.block_table, lens=c.lens,
+                          max_len=P["prefix"])
+        ki, ks, mu, _ = sage.sage_quant_int8(qkv.k, block_tokens=P["k_block"], smooth=True)
+        qi, qs, _, bias = sage.sage_quant_int8(qkv.q, block_tokens=P["q_block"], mu_in=mu)
+        run = lambda: sage.sage_attn_prefill(qi, qs, P["q_block"], ki, ks, P["k_block"], qkv.v,
+                                             causal=P["causal"], q_bias=bias, prefix=prefix)
+    for _ in range(args.warmup + args.steps):
+        run()
+    torch.cuda.synchronize()
+    st, word = sage.check_device_status()
+    print(json.dumps({"profile": args.profile, "params": P, "launches": args.warmup + args.steps,
+                      "status": st}))
+    return None
 
 
 def run_reference(args):
@@ -380,13 +505,19 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
+    ap.add_argument("--profile", default=None,
+                    choices=["paged_decode", "dense_prefill", "chunked_prefill"])
+    ap.add_argument("--heads", type=int, default=0)
     args = ap.parse_args()
+    if args.profile:
+        run_profile(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     line = run_reference(args) if args.impl == "reference" else run_ours(args)

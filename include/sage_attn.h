@@ -60,7 +60,7 @@ typedef enum sage_dtype {
 const char *sage_get_last_error_message(void);
 
 /* Library ABI version (increments on any signature change). */
-int sage_version(void);
+int sage_version(void);   /* 2 */
 
 /* --------------------------------------------------------------------------
  * Quantisation  ([P1] section 4; [P3] quant kernel table, feature matrix)
@@ -134,8 +134,11 @@ typedef struct sage_decode_args {
     float *lse;                 /* optional [B, Hq] natural-log LSE (-inf for empty context) */
 } sage_decode_args_t;
 
-/* Segment count the library picks for num_segments == 0 (host only). */
-int sage_decode_num_segments(int B, int Hq, int Hkv, int max_context_len);
+/* Segment count the library picks for num_segments == 0 (host only): the
+ * count whose CTAs (B * Hkv * ceil(Hq/Hkv/8) * S) fill the GPU's resident
+ * decode slots in the fewest, fullest waves, with at least 4 pages per
+ * segment. */
+int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len);
 
 /* Bytes of workspace sage_attn_decode_paged needs: fp32 partial outputs
  * [B,Hq,S,D] plus fp32 partial LSEs [B,Hq,S] (0 when S == 1). */

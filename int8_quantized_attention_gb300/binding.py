@@ -84,7 +84,7 @@ def lib():
         L.sage_quant_int8.argtypes = [_vp, _i, _i, _i, _i, _i, _i64, _i64, _i64, _i, _i, _vp, _i,
                                       _vp, _vp, _vp, _vp, _vp]
         L.sage_quant_int8.restype = _i
-        L.sage_decode_num_segments.argtypes = [_i, _i, _i, _i]
+        L.sage_decode_num_segments.argtypes = [_i, _i, _i, _i, _i]
         L.sage_decode_num_segments.restype = _i
         L.sage_attn_decode_workspace_size.argtypes = [_i, _i, _i, _i]
         L.sage_attn_decode_workspace_size.restype = ctypes.c_size_t
@@ -189,8 +189,8 @@ def sage_quant_int8(x: torch.Tensor, block_tokens: int = 1, smooth: bool = False
     return q, scale, mu, bias
 
 
-def decode_num_segments(B: int, Hq: int, Hkv: int, max_context_len: int) -> int:
-    return int(lib().sage_decode_num_segments(B, Hq, Hkv, max_context_len))
+def decode_num_segments(B: int, Hq: int, Hkv: int, D: int, max_context_len: int) -> int:
+    return int(lib().sage_decode_num_segments(B, Hq, Hkv, D, max_context_len))
 
 
 def decode_workspace_size(B: int, Hq: int, D: int, num_segments: int) -> int:
@@ -234,7 +234,7 @@ def sage_attn_decode_paged(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, 
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=q_int8.device)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=q_int8.device) if return_lse else None
-    S = num_segments or decode_num_segments(B, Hq, Hkv, max_context_len)
+    S = num_segments or decode_num_segments(B, Hq, Hkv, D, max_context_len)
     need = decode_workspace_size(B, Hq, D, S)
     if workspace is None and need:
         workspace = torch.empty((need,), dtype=torch.uint8, device=q_int8.device)

@@ -112,7 +112,7 @@ void record_launch(const LaunchLog &log) { g_last = log; }
 
 SAGE_API const char *sage_get_last_error_message(void) { return g_msg.c_str(); }
 
-SAGE_API int sage_version(void) { return 1; }
+SAGE_API int sage_version(void) { return 2; }
 
 SAGE_API sage_status_t sage_last_launch_info(sage_launch_info_t *info) {
     if (!info) return fail(SAGE_ERR_INVALID_ARG, "info is NULL");
@@ -236,20 +236,36 @@ SAGE_API sage_status_t sage_splitk_combine(const float *o_part, const float *lse
 
 // ----------------------------------------------------------------- decode
 
-SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int max_context_len) {
+SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len) {
     if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || max_context_len <= 0) return 1;
     const int group = Hq / Hkv;
     const int64_t units = (int64_t)B * Hkv * ((group + 7) / 8);
-    const int64_t target = 2ll * sm_count();
+    const int64_t slots = (int64_t)sm_count() * sage::decode_ctas_per_sm(D);
     const int pages = (max_context_len + 15) / 16;
-    int64_t S = (target + units - 1) / units;
     // at least one page per consumer warp in every segment
-    const int64_t cap = pages / 4 > 1 ? pages / 4 : 1;
-    if (S > cap) S = cap;
-    if (S > 1024) S = 1024;
-    if (S < 1) S = 1;
-    const int64_t pps = (pages + S - 1) / S;
-    return (int)((pages + pps - 1) / pps);
+    int64_t smax = pages / 4 > 1 ? pages / 4 : 1;
+    if (smax > 64) smax = 64;
+    // One resident wave when the (sequence, kv head) units leave room: the
+    // largest S whose CTAs all fit.  Otherwise the fewest segments whose CTAs
+    // fill at least 90 % of the wave-slots they occupy (no near-empty tail).
+    int64_t best = 1;
+    if (units <= slots) {
+        best = slots / units;
+    } else {
+        for (int64_t S = 1; S <= smax; ++S) {
+            const int64_t ctas = units * S;
+            const int64_t waves = (ctas + slots - 1) / slots;
+            if ((double)ctas >= 0.9 * (double)(waves * slots)) {
+                best = S;
+                break;
+            }
+        }
+    }
+    if (best > smax) best = smax;
+    if (best < 1) best = 1;
+    const int64_t pps = (pages + best - 1) / best;
+    best = (pages + pps - 1) / pps;
+    return (int)best;
 }
 
 SAGE_API size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments) {
@@ -293,7 +309,8 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
     }
     if (!aligned(a->q, 4)) return fail(SAGE_ERR_INVALID_ARG, "q must be 4-byte aligned");
     int S = a->num_segments ? a->num_segments
-                            : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->max_context_len);
+                            : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->D,
+                                                       a->max_context_len);
     const int pages = (a->max_context_len + 15) / 16;
     int pps = pages > 0 ? (pages + S - 1) / S : 1;
     if (pages > 0) S = (pages + pps - 1) / pps;

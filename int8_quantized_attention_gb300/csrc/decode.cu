@@ -387,11 +387,35 @@ cudaError_t launch_d(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {
 }  // namespace
 
 int decode_ctas_per_sm(int D) {
+    int n = 0;
+    cudaError_t e = cudaSuccess;
     switch (D) {
-        case 64: return DecodeCfg<64>::kCtasPerSm;
-        case 128: return DecodeCfg<128>::kCtasPerSm;
-        default: return DecodeCfg<256>::kCtasPerSm;
+        case 64:
+            e = cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     DecodeCfg<64>::kSmem);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64>, kThreads,
+                                                                  DecodeCfg<64>::kSmem);
+            if (e != cudaSuccess || n < 1) n = DecodeCfg<64>::kCtasPerSm;
+            break;
+        case 128:
+            e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     DecodeCfg<128>::kSmem);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128>, kThreads,
+                                                                  DecodeCfg<128>::kSmem);
+            if (e != cudaSuccess || n < 1) n = DecodeCfg<128>::kCtasPerSm;
+            break;
+        default:
+            e = cudaFuncSetAttribute(decode_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     DecodeCfg<256>::kSmem);
+            if (e == cudaSuccess)
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<256>, kThreads,
+                                                                  DecodeCfg<256>::kSmem);
+            if (e != cudaSuccess || n < 1) n = DecodeCfg<256>::kCtasPerSm;
+            break;
     }
+    return n;
 }
 
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {

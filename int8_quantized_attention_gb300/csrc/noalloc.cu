@@ -95,7 +95,8 @@ SAGE_API sage_status_t sage_attn_decode_paged_noalloc(const sage_decode_args_t *
         return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG, "q must be 4-byte aligned");
 
     int S = a->num_segments ? a->num_segments
-                            : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->max_context_len);
+                            : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->D,
+                                                       a->max_context_len);
     const int pages = (a->max_context_len + 15) / 16;
     const int pps = pages > 0 ? (pages + S - 1) / S : 1;
     S = pages > 0 ? (pages + pps - 1) / pps : 1;

@@ -425,9 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int i = i0 + r;
         const bool row_ok = i < p.Sq;
         const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
-        const float rq = row_ok ? p.q_scale[((int64_t)b * p.Hq + hq) * p.q_groups + (i >> p.q_shift)] *
-                                      p.qk_scale_log2
-                                : 0.0f;
+        // kept strictly positive so that a masked (-inf) score stays -inf; an
+        // all-zero Q row (scale 0) then scores ~1e-30 * acc = 0 as it should
+        const float rq = fmaxf(row_ok ? p.q_scale[((int64_t)b * p.Hq + hq) * p.q_groups +
+                                                  (i >> p.q_shift)] * p.qk_scale_log2
+                                      : 0.0f,
+                               1e-30f);
         const float bc =
             (row_ok && p.q_bias) ? p.q_bias[((int64_t)b * p.Hq + hq) * p.Sq + i] * p.qk_scale_log2
                                  : 0.0f;
@@ -442,36 +445,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             tc::fence_after();
             const uint32_t s_t = tmem + lane_base + C::COL_S + buf * BN;
-            float s[BN];
-#pragma unroll
+            const float *ksc = ksc_all + buf * BN;
+            const float *vsc = vsc_all + buf * BN;
+            const bool masked = (t.n < BN) || (p.causal && (t.kg0 + BN - 1 > i0 + off));
+            // ---- pass 1: row max of the scaled scores (S stays in TMEM)
+            float mx = -INFINITY;
+#pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t rr[32];
                 tc::ld32(s_t + c * 32, rr);
                 tc::wait_ld();
+                if (p.dbg && row_ok) {
+                    int32_t *dr = p.dbg + (((int64_t)b * p.Hq + hq) * p.Sq + i) * p.dbg_stride;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(rr[e]);
-            }
-            if (p.dbg && row_ok) {
-                int32_t *dr = p.dbg + (((int64_t)b * p.Hq + hq) * p.Sq + i) * p.dbg_stride;
+                    for (int e = 0; e < 32; ++e) {
+                        const int cc = c * 32 + e, kg = t.kg0 + cc;
+                        if (cc < t.n && (!p.causal || kg <= lim))
+                            dr[kg] = __float2int_rn(__uint_as_float(rr[e]));
+                    }
+                }
+                if (masked) {
 #pragma unroll
-                for (int c = 0; c < BN; ++c) {
-                    const int kg = t.kg0 + c;
-                    if (c < t.n && (!p.causal || kg <= lim)) dr[kg] = __float2int_rn(s[c]);
+                    for (int e = 0; e < 32; ++e) {
+                        const int cc = c * 32 + e;
+                        const float u = (cc >= t.n || (p.causal && t.kg0 + cc > lim))
+                                            ? -INFINITY
+                                            : __uint_as_float(rr[e]) * ksc[cc];
+                        mx = fmaxf(mx, u);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mx = fmaxf(mx, __uint_as_float(rr[e]) * ksc[c * 32 + e]);
                 }
             }
-            const float *ksc = ksc_all + buf * BN;
-            const float *vsc = vsc_all + buf * BN;
-            const bool masked = (t.n < BN) || (p.causal && (t.kg0 + BN - 1 > i0 + off));
-            float mx = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < BN; ++c) {
-                float u = s[c] * ksc[c];
-                if (masked && (c >= t.n || (p.causal && t.kg0 + c > lim))) u = -INFINITY;
-                s[c] = u;
-                mx = fmaxf(mx, u);
-            }
             const float tb = t.pre ? 0.0f : bc;
-            const float tmax = mx == -INFINITY ? -INFINITY : fmaf(mx, rq, tb);
+            const float tmax = fmaf(mx, rq, tb);  // -inf when every key is masked (rq > 0)
             const float cand = fmaxf(m_run, tmax);
             const bool move = cand != -INFINITY && (m_run == -INFINITY || cand > m_run + 8.0f);
             float alpha = 1.0f;
@@ -501,15 +509,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc::wait_st();
             }
             const float nb = tb - (m_run == -INFINITY ? 0.0f : m_run);
+            // ---- pass 2: P = 2^(s*ksc*rq + tb - m) in 32-key chunks; the 16
+            // packed f16x2 words of chunk c overwrite S columns [16c, 16c+16),
+            // which were read in this pass already
             float lsum = 0.0f;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t rr[32];
+                tc::ld32(s_t + c * 32, rr);
+                tc::wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int c0 = c * 64 + 2 * e;
-                    float p0 = s[c0] == -INFINITY ? 0.0f : fast_exp2(fmaf(s[c0], rq, nb));
-                    float p1 = s[c0 + 1] == -INFINITY ? 0.0f : fast_exp2(fmaf(s[c0 + 1], rq, nb));
+                for (int e = 0; e < 16; ++e) {
+                    const int c0 = c * 32 + 2 * e;
+                    float u0 = __uint_as_float(rr[2 * e]) * ksc[c0];
+                    float u1 = __uint_as_float(rr[2 * e + 1]) * ksc[c0 + 1];
+                    if (masked) {
+                        if (c0 >= t.n || (p.causal && t.kg0 + c0 > lim)) u0 = -INFINITY;
+                        if (c0 + 1 >= t.n || (p.causal && t.kg0 + c0 + 1 > lim)) u1 = -INFINITY;
+                    }
+                    float p0 = fast_exp2(fmaf(u0, rq, nb));
+                    float p1 = fast_exp2(fmaf(u1, rq, nb));
                     lsum += p0 + p1;
                     if (t.pre) {
                         p0 *= vsc[c0];
@@ -517,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     pk[e] = pack2(p0, p1, false);
                 }
-                tc::st32(s_t + c * 32, pk);
+                tc::st16(s_t + c * 16, pk);
             }
             l += lsum;
             tc::wait_st();
