@@ -142,6 +142,22 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// 16 int8 channels [16*dc, 16*dc+16) of key r -> exact f16, stored as the
+// two 16-byte chunks 2*dc, 2*dc+1 of row r in a 128-byte-swizzled tile
+// (64-channel atom columns BN*128 bytes apart, chunk c of row r at c ^ (r%8)).
+template <int BN>
+__device__ __forceinline__ void store_piece(uint8_t *tile, int r, int dc, uint4 w) {
+    uint4 h0, h1;
+    i8x4_to_f16x4(w.x, h0.x, h0.y);
+    i8x4_to_f16x4(w.y, h0.z, h0.w);
+    i8x4_to_f16x4(w.z, h1.x, h1.y);
+    i8x4_to_f16x4(w.w, h1.z, h1.w);
+    const int c8 = 2 * dc;
+    uint8_t *row = tile + (c8 >> 3) * (BN * 128) + (r >> 3) * 1024 + (r & 7) * 128;
+    *reinterpret_cast<uint4 *>(row + (((c8 & 7) ^ (r & 7)) << 4)) = h0;
+    *reinterpret_cast<uint4 *>(row + ((((c8 + 1) & 7) ^ (r & 7)) << 4)) = h1;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p,
@@ -344,41 +360,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!__all_sync(0xffffffffu, ok)) break;
             const uint8_t *kr = sm + C::OFF_KR + buf * C::KR;
             uint8_t *kf = sm + C::OFF_KF + buf * C::KF;
-            constexpr int ITEMS = BN * D / 8;  // 16-byte f16 chunks per tile
-#pragma unroll 4
-            for (int it = ct; it < ITEMS; it += 128) {
-                const int r = it / (D / 8), c8 = it % (D / 8);
-                uint2 w = make_uint2(0, 0);
-                if (r < t.n) {
-                    const uint8_t *src = t.pre ? kr + (r >> 4) * (D * 16) + (c8 >> 1) * 256 +
-                                                     (r & 15) * 16 + (c8 & 1) * 8
-                                               : kr + r * D + c8 * 8;
-                    w = *reinterpret_cast<const uint2 *>(src);
-                }
-                uint4 h;
-                i8x4_to_f16x4(w.x, h.x, h.y);
-                i8x4_to_f16x4(w.y, h.z, h.w);
-                const int o = (c8 >> 3) * (BN * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
-                              (((c8 & 7) ^ (r & 7)) << 4);
-                *reinterpret_cast<uint4 *>(kf + o) = h;
-            }
+            // 16-byte pieces (16 channels of one key) -> two swizzled f16
+            // chunks.  Contiguous rows: channel pieces vary fastest across
+            // threads; page slabs ([D/16][16 keys][16]): keys vary fastest.
+            // Both mappings keep the shared-memory reads conflict-free.
+            constexpr int PIECES = BN * D / 16;
             if (t.pre) {
                 const uint8_t *vr = sm + C::OFF_VR + buf * C::VR;
                 uint8_t *vf = sm + C::OFF_VF + buf * C::VF;
 #pragma unroll 4
-                for (int it = ct; it < ITEMS; it += 128) {
-                    const int r = it / (D / 8), c8 = it % (D / 8);
-                    uint2 w = make_uint2(0, 0);
-                    if (r < t.n)
-                        w = *reinterpret_cast<const uint2 *>(vr + (r >> 4) * (D * 16) +
-                                                             (c8 >> 1) * 256 + (r & 15) * 16 +
-                                                             (c8 & 1) * 8);
-                    uint4 h;
-                    i8x4_to_f16x4(w.x, h.x, h.y);
-                    i8x4_to_f16x4(w.y, h.z, h.w);
-                    const int o = (c8 >> 3) * (BN * 128) + (r >> 3) * 1024 + (r & 7) * 128 +
-                                  (((c8 & 7) ^ (r & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(vf + o) = h;
+                for (int it = ct; it < PIECES; it += 128) {
+                    const int r = it % BN, dc = it / BN;
+                    const int src = (r >> 4) * (D * 16) + dc * 256 + (r & 15) * 16;
+                    uint4 wk = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
+                    if (r < t.n) {
+                        wk = *reinterpret_cast<const uint4 *>(kr + src);
+                        wv = *reinterpret_cast<const uint4 *>(vr + src);
+                    }
+                    store_piece<BN>(kf, r, dc, wk);
+                    store_piece<BN>(vf, r, dc, wv);
+                }
+            } else {
+#pragma unroll 4
+                for (int it = ct; it < PIECES; it += 128) {
+                    const int r = it / (D / 16), dc = it % (D / 16);
+                    uint4 w = make_uint4(0, 0, 0, 0);
+                    if (r < t.n) w = *reinterpret_cast<const uint4 *>(kr + r * D + dc * 16);
+                    store_piece<BN>(kf, r, dc, w);
                 }
             }
             if (!t.pre && p.v_bf16) {
