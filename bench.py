@@ -39,6 +39,12 @@ WORKLOAD = "paged_decode"
 L2_FLUSH_BYTES = 512 << 20  # > 2x the 129 MB L2
 
 
+def l2_flush(buf):
+    """Evict L2 by READING a buffer 4x its size (clean lines: no write-back of
+    the flush itself lands inside the next timed region)."""
+    buf.max()
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -147,7 +153,7 @@ def run_ours(args):
     S = sage.decode_num_segments(B, Hq, Hkv, D, ctx)
     kbytes, sbytes = decode_bytes(B, Hq, Hkv, D, ctx, max_blocks)
     stream = torch.cuda.current_stream()
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
 
     def step(ev=None):
         qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
@@ -165,7 +171,7 @@ def run_ours(args):
     clk = ClockSampler(local).__enter__()   # samples from warm-up through the timed steps
     for _ in range(args.warmup):
         step()
-        flush.zero_()
+        l2_flush(flush)
     torch.cuda.synchronize()
     st, word = sage.check_device_status()
     if st != 0:
@@ -183,7 +189,7 @@ def run_ours(args):
            for _ in range(args.steps)]
     barrier()
     for i in range(args.steps):
-        flush.zero_()                 # L2 flush outside the timed window
+        l2_flush(flush)               # L2 flush outside the timed window
         starts[i].record(stream)
         step(kev[i])
         ends[i].record(stream)
@@ -229,7 +235,7 @@ def run_ours(args):
         es = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         ee = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
         for i in range(args.steps):
-            flush.zero_()
+            l2_flush(flush)
             es[i].record(stream)
             e2e_step()
             ee[i].record(stream)
@@ -264,7 +270,7 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "i8",
         "data": "synthetic (seeded; uniform INT8 cache, U(0.005,0.02) scales, N(0,1) bf16 query)",
         "config": {"workload": "paged_decode B8 Hq24 Hkv4 D256 ctx8192 block16",
-                   "segments": S, "l2": "flushed between steps (512 MB write)",
+                   "segments": S, "l2": "flushed between steps (read of a 512 MB buffer)",
                    "step": "quant(Q) + split-K paged decode + LSE combine",
                    "parallelism": "replicas" if ws > 1 else "single"},
         "roofline": roof, "e2e": e2e, "gpu_launches": 3 * args.steps,

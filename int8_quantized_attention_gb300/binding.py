@@ -256,6 +256,9 @@ def decode_segments_used(max_context_len: int, num_segments: int) -> int:
     pages = (int(max_context_len) + 15) // 16
     if pages == 0:
         return 1
+    cap = 1024  # longest segment in pages (decode_max_segment_pages)
+    if num_segments * cap < pages:
+        num_segments = (pages + cap - 1) // cap
     pps = (pages + num_segments - 1) // num_segments
     return (pages + pps - 1) // pps
 

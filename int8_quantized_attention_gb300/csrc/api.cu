@@ -263,6 +263,8 @@ SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_con
     }
     if (best > smax) best = smax;
     if (best < 1) best = 1;
+    const int64_t cap = sage::decode_max_segment_pages();
+    if (best * cap < pages) best = (pages + cap - 1) / cap;
     const int64_t pps = (pages + best - 1) / best;
     best = (pages + pps - 1) / pps;
     return (int)best;
@@ -312,6 +314,10 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
                             : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->D,
                                                        a->max_context_len);
     const int pages = (a->max_context_len + 15) / 16;
+    {   // a segment is at most decode_max_segment_pages() pages long
+        const int cap = sage::decode_max_segment_pages();
+        if ((int64_t)S * cap < pages) S = (pages + cap - 1) / cap;
+    }
     int pps = pages > 0 ? (pages + S - 1) / S : 1;
     if (pages > 0) S = (pages + pps - 1) / pps;
     else S = 1;

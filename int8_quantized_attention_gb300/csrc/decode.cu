@@ -34,6 +34,8 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
+constexpr int kMaxSegPages = 1024;  // block-table entries staged per CTA (segment length cap)
+
 template <int D>
 struct DecodeCfg {
     static constexpr int kSlab = D * 16;                 // bytes of one page slab
@@ -41,8 +43,17 @@ struct DecodeCfg {
     static constexpr int kStages = D == 256 ? 8 : (D == 128 ? 12 : 16);
     static constexpr int kVStage = D * 16 * 2;           // per-warp f16 copy of V
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kSmem = kRingBytes + kConsumerWarps * kVStage + kStages * 16 + 64;
+    static constexpr int kOffBar = kRingBytes + kConsumerWarps * kVStage;
+    static constexpr int kOffBt = kOffBar + kStages * 16 + 64;
+    static constexpr int kSmem = kOffBt + kMaxSegPages * 4;
     static constexpr int kCtasPerSm = 227 * 1024 / (kSmem + 1024);
+    // pages whose K/V slabs are prefetched into L2 ahead of the ring
+    static constexpr int kPrefetchPages = 8;
+    // Page i goes to stage i % kStages and to consumer warp i % kConsumerWarps.
+    // Every stage must always be read by the same warp: mbarrier parity waits
+    // cannot tell phase k from phase k-2, so a stage shared by two warps
+    // would let one of them pass a full-barrier wait a phase early.
+    static_assert(kStages % kConsumerWarps == 0, "each stage belongs to one consumer warp");
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -102,6 +113,7 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
     uint64_t *full = reinterpret_cast<uint64_t *>(vst_all + kConsumerWarps * Cfg::kVStage);
     uint64_t *empty = full + NST;
     int *stage_ok = reinterpret_cast<int *>(empty + NST);
+    int *bt_s = reinterpret_cast<int *>(smem + Cfg::kOffBt);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seg = blockIdx.x;
@@ -117,7 +129,11 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
     }
     const int npages = (ctx + 15) >> 4;
     const int pg0 = seg * p.pages_per_seg;
-    const int np = max(0, min(pg0 + p.pages_per_seg, npages) - pg0);
+    int np = max(0, min(pg0 + p.pages_per_seg, npages) - pg0);
+    if (np > kMaxSegPages) {  // the host never asks for longer segments
+        if (threadIdx.x == 0) atomicOr(p.err, kErrBadBlock);
+        np = kMaxSegPages;
+    }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
@@ -125,6 +141,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
             mbar_init(smem_u32(&empty[s]), 1);
         }
         fence_barrier_init();
+    }
+    {
+        const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks + pg0;
+        for (int i = threadIdx.x; i < np; i += kThreads) bt_s[i] = bt[i];
     }
     __syncthreads();
 
@@ -139,13 +159,12 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         // ------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t pol = l2_policy_evict_first();
-            const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks + pg0;
             int issued = 0;
             for (int i = 0; i < np; ++i) {
                 const int s = i % NST;
                 const uint32_t ph = (uint32_t)(i / NST) & 1u;
                 if (!mbar_wait(smem_u32(&empty[s]), ph ^ 1u, p.err)) break;
-                const int blk = bt[i];
+                const int blk = bt_s[i];
                 const uint32_t fb = smem_u32(&full[s]);
                 if ((unsigned)blk >= (unsigned)p.num_blocks) {
                     atomicOr(p.err, kErrBadBlock);
@@ -195,7 +214,27 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         }
         uint8_t *vst = vst_all + warp * Cfg::kVStage;
         const uint32_t vst_a = smem_u32(vst);
+        // HBM latency under full load is several microseconds, far more than
+        // the ring covers: each warp also prefetches, with plain per-lane L2
+        // prefetches (no shared memory, no registers), the K and V slabs of
+        // the pages kPrefetchPages ahead, so the ring's copies hit in L2.
+        auto prefetch_page = [&](int i) {
+            if (i < np) {
+                const int blk = bt_s[i];
+                if ((unsigned)blk < (unsigned)p.num_blocks) {
+                    const int64_t pg = (int64_t)blk * p.Hkv + kvh;
+                    for (int ln = lane; ln < Cfg::kSlab / 128; ln += 32) {  // 128-byte lines
+                        const int64_t off = pg * Cfg::kSlab + ln * 128;
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_cache + off));
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_cache + off));
+                    }
+                }
+            }
+        };
+        for (int i = warp + NST; i < min(np, Cfg::kPrefetchPages); i += kConsumerWarps)
+            prefetch_page(i);
         for (int i = warp; i < np; i += kConsumerWarps) {
+            prefetch_page(i + Cfg::kPrefetchPages);
             const int s = i % NST;
             const bool got = mbar_wait(smem_u32(&full[s]), (uint32_t)(i / NST) & 1u, p.err);
             if (!__all_sync(0xffffffffu, got)) break;  // keep the warp converged
@@ -385,6 +424,8 @@ cudaError_t launch_d(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {
 }
 
 }  // namespace
+
+int decode_max_segment_pages() { return kMaxSegPages; }
 
 int decode_ctas_per_sm(int D) {
     int n = 0;

@@ -77,6 +77,7 @@ struct DecodeParams {
 };
 
 int decode_ctas_per_sm(int D);
+int decode_max_segment_pages();   // longest segment (in 16-token pages) one CTA takes
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t st, LaunchLog &log);
 
 struct PrefillParams {

@@ -98,6 +98,10 @@ SAGE_API sage_status_t sage_attn_decode_paged_noalloc(const sage_decode_args_t *
                             : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->D,
                                                        a->max_context_len);
     const int pages = (a->max_context_len + 15) / 16;
+    {   // a segment is at most decode_max_segment_pages() pages long
+        const int cap = sage::decode_max_segment_pages();
+        if ((int64_t)S * cap < pages) S = (pages + cap - 1) / cap;
+    }
     const int pps = pages > 0 ? (pages + S - 1) / S : 1;
     S = pages > 0 ? (pages + pps - 1) / pps : 1;
     const size_t rows = (size_t)a->B * a->Hq * S;
