@@ -60,7 +60,7 @@ typedef enum sage_dtype {
 const char *sage_get_last_error_message(void);
 
 /* Library ABI version (increments on any signature change). */
-int sage_version(void);   /* 2 */
+int sage_version(void);   /* 3 */
 
 /* --------------------------------------------------------------------------
  * Quantisation  ([P1] section 4; [P3] quant kernel table, feature matrix)
@@ -244,7 +244,19 @@ typedef struct sage_prefill_args {
     float *lse;                     /* optional [B, Hq, Sq] */
 } sage_prefill_args_t;
 
-sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *stream);
+/* Workspace of sage_attn_prefill (host only): the tensor cores of sm_103a
+ * have no INT8 mode, so each call first expands the INT8 codes it reads --
+ * chunk K, and the paged prefix's K and V gathered through the block table
+ * -- into an exact f16 copy, together with per-key scales; bf16 chunk V is
+ * rounded to f16 there too.  Returns the bytes needed (0 never happens for a
+ * valid request).  The stored representation stays INT8; the copy is scratch
+ * of the call. */
+size_t sage_attn_prefill_workspace_size(const sage_prefill_args_t *args);
+
+/* workspace: device buffer of at least sage_attn_prefill_workspace_size()
+ * bytes, 256-byte aligned; overwritten by the call. */
+sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /* --------------------------------------------------------------------------
  * Test hooks: raw INT32 scores through the same device tile paths
@@ -256,7 +268,8 @@ sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *stream);
  * sage_debug_decode_qk_int32: runs sage_attn_decode_paged and writes
  *   scores[b,h,j] for j < context_lens[b]; scores: int32 [B, Hq, max_context_len].
  * ------------------------------------------------------------------------ */
-sage_status_t sage_debug_prefill_qk_int32(const sage_prefill_args_t *args, int32_t *scores,
+sage_status_t sage_debug_prefill_qk_int32(const sage_prefill_args_t *args, void *workspace,
+                                          size_t workspace_bytes, int32_t *scores,
                                           void *stream);
 sage_status_t sage_debug_decode_qk_int32(const sage_decode_args_t *args, void *workspace,
                                          size_t workspace_bytes, int32_t *scores, void *stream);

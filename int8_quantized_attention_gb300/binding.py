@@ -102,9 +102,12 @@ def lib():
         L.sage_debug_decode_qk_int32.restype = _i
         L.sage_splitk_combine.argtypes = [_vp, _vp, _i, _i, _i, _vp, _i, _vp, _vp]
         L.sage_splitk_combine.restype = _i
-        L.sage_attn_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp]
+        L.sage_attn_prefill_workspace_size.argtypes = [ctypes.POINTER(PrefillArgs)]
+        L.sage_attn_prefill_workspace_size.restype = ctypes.c_size_t
+        L.sage_attn_prefill.argtypes = [ctypes.POINTER(PrefillArgs), _vp, ctypes.c_size_t, _vp]
         L.sage_attn_prefill.restype = _i
-        L.sage_debug_prefill_qk_int32.argtypes = [ctypes.POINTER(PrefillArgs), _vp, _vp]
+        L.sage_debug_prefill_qk_int32.argtypes = [ctypes.POINTER(PrefillArgs), _vp,
+                                                  ctypes.c_size_t, _vp, _vp]
         L.sage_debug_prefill_qk_int32.restype = _i
         L.sage_last_launch_info.argtypes = [ctypes.POINTER(LaunchInfo)]
         L.sage_last_launch_info.restype = _i
@@ -297,7 +300,8 @@ def sage_splitk_combine(o_part: torch.Tensor, lse_part: torch.Tensor, out_dtype=
 
 def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: int, v, *,
                       causal: bool, sm_scale=None, q_bias=None, prefix: Optional[dict] = None,
-                      out_dtype=None, return_lse: bool = False, debug_scores=None, stream=None):
+                      out_dtype=None, return_lse: bool = False, debug_scores=None,
+                      workspace: Optional[torch.Tensor] = None, stream=None):
     """INT8-QK prefill attention over an optional paged INT8 prefix + a chunk.
 
     q_int8 [B,Hq,Sq,D]; q_scale [B,Hq,ceil(Sq/q_block)]; k_int8 [B,Hkv,Sk,D];
@@ -341,12 +345,16 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
     a.causal = int(bool(causal))
     a.sm_scale = float(sm_scale) if sm_scale else 0.0
     a.out, a.out_dtype, a.lse = _ptr(out), _dt(out_dtype), _ptr(lse)
+    need = int(lib().sage_attn_prefill_workspace_size(ctypes.byref(a)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q_int8.device)
+    wsb = workspace.numel() * workspace.element_size()
     if debug_scores is not None:
         _need(debug_scores, torch.int32, "debug_scores")
-        _check(lib().sage_debug_prefill_qk_int32(ctypes.byref(a), _ptr(debug_scores),
-                                                 _stream(stream)))
+        _check(lib().sage_debug_prefill_qk_int32(ctypes.byref(a), _ptr(workspace), wsb,
+                                                 _ptr(debug_scores), _stream(stream)))
     else:
-        _check(lib().sage_attn_prefill(ctypes.byref(a), _stream(stream)))
+        _check(lib().sage_attn_prefill(ctypes.byref(a), _ptr(workspace), wsb, _stream(stream)))
     return (out, lse) if return_lse else out
 
 

@@ -112,7 +112,7 @@ void record_launch(const LaunchLog &log) { g_last = log; }
 
 SAGE_API const char *sage_get_last_error_message(void) { return g_msg.c_str(); }
 
-SAGE_API int sage_version(void) { return 2; }
+SAGE_API int sage_version(void) { return 3; }
 
 SAGE_API sage_status_t sage_last_launch_info(sage_launch_info_t *info) {
     if (!info) return fail(SAGE_ERR_INVALID_ARG, "info is NULL");
@@ -398,7 +398,7 @@ SAGE_API sage_status_t sage_debug_decode_qk_int32(const sage_decode_args_t *args
 
 // ---------------------------------------------------------------- prefill
 
-static sage_status_t run_prefill(const sage_prefill_args_t *a, int32_t *dbg, void *stream) {
+static sage_status_t check_prefill(const sage_prefill_args_t *a, int *qs_out, int *ks_out) {
     if (!a) return fail(SAGE_ERR_INVALID_ARG, "args is NULL");
     if (!head_dim_ok(a->D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", a->D);
     if (a->out_dtype != SAGE_F16 && a->out_dtype != SAGE_BF16)
@@ -414,10 +414,28 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, int32_t *dbg, voi
         return fail(SAGE_ERR_UNSUPPORTED, "q_block must be 1 or a power of two >= 128");
     if (ks < 0 || (a->k_block != 1 && a->k_block < 64))
         return fail(SAGE_ERR_UNSUPPORTED, "k_block must be 1 or a power of two >= 64");
-    const bool has_prefix = a->max_prefix_len > 0;
     if (a->max_prefix_len < 0 ||
-        (has_prefix && (int64_t)a->max_prefix_len > 16ll * a->max_blocks))
+        (a->max_prefix_len > 0 && (int64_t)a->max_prefix_len > 16ll * a->max_blocks))
         return fail(SAGE_ERR_INVALID_ARG, "max_prefix_len exceeds 16 * max_blocks");
+    *qs_out = qs;
+    *ks_out = ks;
+    return SAGE_OK;
+}
+
+SAGE_API size_t sage_attn_prefill_workspace_size(const sage_prefill_args_t *a) {
+    int qs = 0, ks = 0;
+    if (check_prefill(a, &qs, &ks) != SAGE_OK) return 0;
+    return sage::prefill_layout(a->B, a->Hkv, a->Sk, a->D, a->max_prefix_len,
+                                a->v_dtype == SAGE_BF16)
+        .bytes;
+}
+
+static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
+                                 size_t workspace_bytes, int32_t *dbg, void *stream) {
+    int qs = 0, ks = 0;
+    sage_status_t cs = check_prefill(a, &qs, &ks);
+    if (cs != SAGE_OK) return cs;
+    const bool has_prefix = a->max_prefix_len > 0;
     g_last = sage::LaunchLog();
     if ((int64_t)a->B * a->Sq == 0) return SAGE_OK;
     if (!a->q || !a->q_scale || !a->out) return fail(SAGE_ERR_INVALID_ARG, "q, q_scale, out required");
@@ -427,14 +445,18 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, int32_t *dbg, voi
         if (!a->k_cache || !a->v_cache || !a->k_cache_scale || !a->v_cache_scale ||
             !a->block_table || !a->prefix_lens || a->num_blocks < 1)
             return fail(SAGE_ERR_INVALID_ARG, "paged prefix needs caches, scales, table, lens");
-        if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16) ||
-            !aligned(a->k_cache_scale, 16) || !aligned(a->v_cache_scale, 16))
-            return fail(SAGE_ERR_INVALID_ARG, "caches and scales must be 16-byte aligned");
+        if (!aligned(a->k_cache, 16) || !aligned(a->v_cache, 16))
+            return fail(SAGE_ERR_INVALID_ARG, "caches must be 16-byte aligned");
     }
     if (a->Sk + a->max_prefix_len == 0) return fail(SAGE_ERR_INVALID_ARG, "no keys");
     if (!aligned(a->q, 16) || (a->k && !aligned(a->k, 16)) || (a->v && !aligned(a->v, 16)) ||
         !aligned(a->out, 16))
         return fail(SAGE_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    const sage::PrefillLayout L = sage::prefill_layout(a->B, a->Hkv, a->Sk, a->D,
+                                                       a->max_prefix_len, a->v_dtype == SAGE_BF16);
+    if (!workspace || workspace_bytes < L.bytes)
+        return fail(SAGE_ERR_INVALID_ARG, "workspace too small: need %zu bytes", L.bytes);
+    if (!aligned(workspace, 256)) return fail(SAGE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
     int *ew = nullptr;
     sage_status_t st = error_word(&ew);
     if (st != SAGE_OK) return st;
@@ -461,18 +483,31 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, int32_t *dbg, voi
     p.dbg = dbg;
     p.dbg_stride = a->max_prefix_len + a->Sk;
     p.err = ew;
-    cudaError_t e = sage::launch_prefill(p, static_cast<cudaStream_t>(stream), g_last);
+    char *w = static_cast<char *>(workspace);
+    p.BN = L.BN, p.Ppad = L.Ppad, p.Lpad = L.Lpad, p.Vrows = L.Vrows;
+    p.k_ws = reinterpret_cast<__half *>(w + L.off_k);
+    p.v_ws = L.Vrows ? reinterpret_cast<__half *>(w + L.off_v) : nullptr;
+    p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);
+    p.vsc_ws = reinterpret_cast<float *>(w + L.off_vsc);
+    cudaStream_t cst = static_cast<cudaStream_t>(stream);
+    sage::LaunchLog stage_log;
+    cudaError_t e = sage::launch_prefill_stage(p, cst, stage_log);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill staging launch");
+    e = sage::launch_prefill(p, cst, g_last);
+    g_last.count += stage_log.count;
     if (e == cudaErrorNotSupported)
         return fail(SAGE_ERR_UNSUPPORTED, "prefill configuration not supported by this build");
     return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "prefill launch");
 }
 
-SAGE_API sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *stream) {
-    return run_prefill(args, nullptr, stream);
+SAGE_API sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *workspace,
+                                         size_t workspace_bytes, void *stream) {
+    return run_prefill(args, workspace, workspace_bytes, nullptr, stream);
 }
 
 SAGE_API sage_status_t sage_debug_prefill_qk_int32(const sage_prefill_args_t *args,
+                                                   void *workspace, size_t workspace_bytes,
                                                    int32_t *scores, void *stream) {
     if (!scores) return fail(SAGE_ERR_INVALID_ARG, "scores is NULL");
-    return run_prefill(args, scores, stream);
+    return run_prefill(args, workspace, workspace_bytes, scores, stream);
 }

@@ -2,6 +2,7 @@
 // kernel translation units.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 #include <string.h>
@@ -105,8 +106,24 @@ struct PrefillParams {
     int32_t *dbg;             // optional [B,Hq,Sq,dbg_stride]
     int dbg_stride;           // max_prefix_len + Sk
     int *err;
+    // ---- workspace (exact f16 expansion of the keys/values a call reads)
+    int BN;                   // key tile of the kernel (128, or 64 at D = 256)
+    int Ppad;                 // prefix rows per (b, kv head), a multiple of BN
+    int Lpad;                 // Ppad + Sk rounded up to BN
+    int Vrows;                // rows of v_ws: Lpad for bf16 V, else Ppad (f16 chunk V read in place)
+    __half *k_ws;             // [B*Hkv][Lpad][D] exact f16 key codes
+    __half *v_ws;             // [B*Hkv][Vrows][D] f16 prefix value codes (+ bf16 chunk V as f16)
+    float *ksc_ws;            // [B*Hkv][Lpad] per-key K scale (0 on padding rows)
+    float *vsc_ws;            // [B*Hkv][Ppad] per-key V scale of the prefix
 };
 
+struct PrefillLayout {
+    int BN, Ppad, Lpad, Vrows;
+    size_t off_k, off_v, off_ksc, off_vsc, bytes;
+};
+
+PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16);
+cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
 cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
 
 cudaError_t launch_timeout_probe(int timeout_us, int *err, cudaStream_t st, LaunchLog &log);

@@ -1,0 +1,147 @@
+// Staging pass of the prefill: expands, once per call, the INT8 key codes
+// (and the paged prefix's INT8 value codes, and bf16 chunk values) into an
+// exact f16 copy in the caller's workspace, with one per-key scale array, so
+// that the attention kernel's tiles arrive by TMA in the layout the tensor
+// cores read and every query tile re-reads them from L2 without converting.
+//
+// Workspace rows per (batch, kv head), in key order: [0, Ppad) the paged
+// prefix (key r at row r; rows past the batch's prefix length are zero),
+// [Ppad, Ppad + Sk) the contiguous chunk, then zero rows up to Lpad.  The
+// INT8 -> f16 expansion is exact (|code| <= 127), so S = Q K^T computed on
+// the copy equals the INT32 product of the codes ("INT8 QK MMAC on gfx936
+// DCU", sections 2.1 and 5.2: the scores are exact integer dot products,
+// rescaled afterwards by the per-token / per-block scales).
+#include "common.cuh"
+#include "internal.h"
+
+namespace sage {
+
+namespace {
+
+__device__ __forceinline__ void store_f16x16(__half *dst, uint4 w) {
+    uint4 h0, h1;
+    i8x4_to_f16x4(w.x, h0.x, h0.y);
+    i8x4_to_f16x4(w.y, h0.z, h0.w);
+    i8x4_to_f16x4(w.z, h1.x, h1.y);
+    i8x4_to_f16x4(w.w, h1.z, h1.w);
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    d[0] = h0;
+    d[1] = h1;
+}
+
+// 8 bf16 -> 8 f16, round to nearest, saturating to the finite f16 range
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
+    uint32_t *u = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u[e]));
+        __half2 h = __floats2half2_rn(fminf(fmaxf(f.x, -65504.0f), 65504.0f),
+                                      fminf(fmaxf(f.y, -65504.0f), 65504.0f));
+        u[e] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return x;
+}
+
+// One thread per 16-channel piece of a key row; a block of 256 threads
+// covers 256 / D groups of 16 rows.  Prefix groups read page slabs laid out
+// [D/16][16 tokens][16 bytes] with the token index varying fastest across
+// threads (256 contiguous bytes per 16 threads); chunk groups read rows with
+// the channel piece varying fastest.
+__global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constant__ PrefillParams p) {
+    const int D = p.D;
+    const int per_block = 256 / D;
+    const int t = threadIdx.x % D;
+    const int64_t g = (int64_t)blockIdx.x * per_block + threadIdx.x / D;
+    const int gpb = p.Lpad >> 4;
+    const int64_t BH = (int64_t)p.B * p.Hkv;
+    if (g >= BH * gpb) return;
+    const int bh = (int)(g / gpb);
+    const int row0 = (int)(g % gpb) * 16;
+    const int b = bh / p.Hkv, kvh = bh % p.Hkv;
+    const int Vrows = p.Vrows;
+
+    if (row0 < p.Ppad) {
+        int P = p.prefix_lens[b];
+        if (P < 0 || P > p.max_prefix_len) P = P < 0 ? 0 : p.max_prefix_len;
+        const int slot = t & 15, dc = t >> 4;
+        const int row = row0 + slot;
+        uint4 wk = make_uint4(0, 0, 0, 0), wv = make_uint4(0, 0, 0, 0);
+        float ks = 0.0f, vs = 0.0f;
+        if (row < P) {
+            const int blk = p.block_table[(int64_t)b * p.max_blocks + (row >> 4)];
+            if ((unsigned)blk < (unsigned)p.num_blocks) {
+                const int64_t pg = (int64_t)blk * p.Hkv + kvh;
+                wk = *reinterpret_cast<const uint4 *>(p.k_cache + pg * D * 16 + dc * 256 + slot * 16);
+                wv = *reinterpret_cast<const uint4 *>(p.v_cache + pg * D * 16 + dc * 256 + slot * 16);
+                ks = p.k_cache_scale[pg * 16 + slot];
+                vs = p.v_cache_scale[pg * 16 + slot];
+            } else if (t == 0) {
+                atomicOr(p.err, kErrBadBlock);
+            }
+        }
+        store_f16x16(p.k_ws + ((int64_t)bh * p.Lpad + row) * D + dc * 16, wk);
+        store_f16x16(p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16, wv);
+        if (dc == 0) {
+            p.ksc_ws[(int64_t)bh * p.Lpad + row] = ks;
+            p.vsc_ws[(int64_t)bh * p.Ppad + row] = vs;
+        }
+    } else {
+        const int np = D >> 4;
+        const int slot = t / np, dc = t % np;
+        const int row = row0 + slot;
+        const int c = row - p.Ppad;
+        const bool ok = c < p.Sk;
+        uint4 wk = make_uint4(0, 0, 0, 0);
+        float ks = 0.0f;
+        if (ok) {
+            wk = *reinterpret_cast<const uint4 *>(p.k + ((int64_t)bh * p.Sk + c) * D + dc * 16);
+            ks = p.k_scale[(int64_t)bh * p.k_groups + (c >> p.k_shift)];
+        }
+        store_f16x16(p.k_ws + ((int64_t)bh * p.Lpad + row) * D + dc * 16, wk);
+        if (dc == 0) p.ksc_ws[(int64_t)bh * p.Lpad + row] = ks;
+        if (p.v_bf16) {
+            uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+            if (ok) {
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    static_cast<const __nv_bfloat16 *>(p.v) + ((int64_t)bh * p.Sk + c) * D + dc * 16);
+                v0 = bf16x8_to_f16x8(src[0]);
+                v1 = bf16x8_to_f16x8(src[1]);
+            }
+            uint4 *d = reinterpret_cast<uint4 *>(p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16);
+            d[0] = v0;
+            d[1] = v1;
+        }
+    }
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+}  // namespace
+
+PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16) {
+    PrefillLayout L = {};
+    L.BN = D == 256 ? 64 : 128;
+    L.Ppad = (max_prefix_len + L.BN - 1) / L.BN * L.BN;
+    L.Lpad = L.Ppad + (Sk + L.BN - 1) / L.BN * L.BN;
+    L.Vrows = v_bf16 ? L.Lpad : L.Ppad;
+    const size_t BH = (size_t)B * Hkv;
+    L.off_k = 0;
+    L.off_v = align256(L.off_k + BH * L.Lpad * D * 2);
+    L.off_ksc = align256(L.off_v + BH * L.Vrows * D * 2);
+    L.off_vsc = align256(L.off_ksc + BH * L.Lpad * 4);
+    L.bytes = align256(L.off_vsc + BH * L.Ppad * 4);
+    return L;
+}
+
+cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
+    const int64_t groups = (int64_t)p.B * p.Hkv * (p.Lpad >> 4);
+    const int per_block = 256 / p.D;
+    const int64_t blocks = (groups + per_block - 1) / per_block;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+    prefill_stage_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+    log.add("prefill_stage_kernel", dim3((unsigned)blocks), dim3(256), dim3(1, 1, 1), 0);
+    return cudaGetLastError();
+}
+
+}  // namespace sage

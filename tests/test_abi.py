@@ -67,8 +67,9 @@ def test_rejects_bad_arguments_on_host(lib):
     p = binding.PrefillArgs()
     p.B, p.Hq, p.Hkv, p.Sq, p.Sk, p.D = 1, 2, 2, 8, 8, 64
     p.q_block, p.k_block = 100, 1
-    assert lib.sage_attn_prefill(ctypes.byref(p), None) == binding.SAGE_ERR_UNSUPPORTED
-    assert lib.sage_attn_prefill(None, None) == binding.SAGE_ERR_INVALID_ARG
+    assert lib.sage_attn_prefill(ctypes.byref(p), None, 0, None) == binding.SAGE_ERR_UNSUPPORTED
+    assert lib.sage_attn_prefill(None, None, 0, None) == binding.SAGE_ERR_INVALID_ARG
+    assert lib.sage_attn_prefill_workspace_size(None) == 0
 
 
 def test_workspace_arithmetic(lib):

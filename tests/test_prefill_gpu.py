@@ -153,8 +153,10 @@ def test_prefill_launch_record(sage):
     qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
     sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=True)
     info = sage.last_launch_info()
-    assert info["kernel"] == "prefill_kernel" and info["grid"] == (2, 2, 1)
-    assert info["block"] == (320, 1, 1)
+    # two 128-row query tiles per CTA at D = 128: one softmax warpgroup each,
+    # plus a warpgroup holding the producer and MMA warps
+    assert info["kernel"] == "prefill_kernel" and info["grid"] == (1, 2, 1)
+    assert info["block"] == (384, 1, 1)
 
 
 def test_tiny_prefill_full(sage):
