@@ -60,8 +60,10 @@ struct PCfg {
     // softmax warpgroups + one warpgroup holding the producer and MMA warps
     // (and two idle warps, so that register reallocation works per warpgroup)
     static constexpr int THREADS = NQ * 128 + 128;
-    // registers: 2 x 128 x 216 + 128 x 72 = 384 x 168, the launch budget
-    static constexpr int REG_SOFTMAX = 216, REG_OTHER = 72;
+    // registers: 2 x 128 x 208 + 128 x 88 = 384 x 168, the launch budget
+    static constexpr int REG_SOFTMAX = 208, REG_OTHER = 88;
+    static_assert(NQ == 1 || NQ * 128 * REG_SOFTMAX + 128 * REG_OTHER <= THREADS * 168,
+                  "register split exceeds the launch budget");
     static constexpr int QB = 128 * D * 2;     // f16 Q tile, swizzled
     static constexpr int KB = BN * D * 2;      // f16 K (or V) tile, swizzled
     // stage: K tile | V tile | per-key K scales | per-key V scales (prefix)
@@ -87,8 +89,9 @@ enum {
     B_S_FULL = 16,    // [NQ*NS] MMA: S = Q K^T done
     B_P_FULL = 20,    // [NQ*NS] softmax: P written to TMEM (and O rescaled)
     B_O_DONE = 24,    // [NQ] MMA: O_t += P_t V done
-    B_Q_READY = 26,   // softmax: Q in shared memory
-    B_DRAIN = 27      // MMA: every issued MMA retired
+    B_O_FINAL = 26,   // [NQ] MMA: the last O_t += P_t V done (one phase)
+    B_Q_READY = 28,   // softmax: Q in shared memory
+    B_DRAIN = 29      // MMA: every issued MMA retired
 };
 
 struct PrefillMaps {
@@ -117,6 +120,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// three-input maximum (one instruction on sm_100-family parts)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t pack2(float a, float b, bool bf16) {
@@ -200,7 +210,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             mbar_init(bar(B_S_FULL + s), 1);
             mbar_init(bar(B_P_FULL + s), 128);
         }
-        for (int t = 0; t < NQ; ++t) mbar_init(bar(B_O_DONE + t), 1);
+        for (int t = 0; t < NQ; ++t) {
+            mbar_init(bar(B_O_DONE + t), 1);
+            mbar_init(bar(B_O_FINAL + t), 1);
+        }
         mbar_init(bar(B_Q_READY), NQ * 128);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
@@ -300,6 +313,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     tc::mma_ts(tmem + t * D, pt + kk * 8, bd, idp, (jj > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc::commit(bar(B_O_DONE + t));
+                if (jj == T - 1) tc::commit(bar(B_O_FINAL + t));
             };
             auto k_ready = [&](int jj) {
                 const bool ok = wait_ab(bar(B_K_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err,
@@ -384,6 +398,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             (row_ok && p.q_bias) ? p.q_bias[((int64_t)b * p.Hq + hq) * p.Sq + i] * p.qk_scale_log2
                                  : 0.0f;
         const int lim = i + off;
+        // K scales constant over 64-key groups (k_block >= 64, chunk keys):
+        // the max runs on the raw integer scores and the scale folds into
+        // the exponent's FMA, one value per group
+        const bool kuni = p.k_shift >= 6;
         float m_run = -INFINITY, l = 0.0f;
         int done = 0;
         for (int jj = 0; jj < T; ++jj) {
@@ -414,10 +432,29 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     if (c < nvalid && (!p.causal || kg0 + c <= lim))
                         dr[kg0 + c] = __float2int_rn(__uint_as_float(x[c]));
             }
-            // ---- scale recovery in place (x <- s * k_scale) and the row max
+            // ---- the row max of the scaled scores
             const bool tmask = nvalid < BN || (p.causal && kg0 + BN - 1 > i_first + off);
+            const bool uni = kuni && !pre && !tmask;
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            if (!tmask) {
+            float kg[BN / 64];
+            if (uni) {
+                // scale >= 0, so max(s) * k == max(s * k)
+#pragma unroll
+                for (int g = 0; g < BN / 64; ++g) {
+                    kg[g] = ksc4[16 * g].x;
+                    float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const int c = 64 * g + 8 * q;
+                        a0 = fmax3(a0, __uint_as_float(x[c]), __uint_as_float(x[c + 1]));
+                        a1 = fmax3(a1, __uint_as_float(x[c + 2]), __uint_as_float(x[c + 3]));
+                        a2 = fmax3(a2, __uint_as_float(x[c + 4]), __uint_as_float(x[c + 5]));
+                        a3 = fmax3(a3, __uint_as_float(x[c + 6]), __uint_as_float(x[c + 7]));
+                    }
+                    m4[g] = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * kg[g];
+                }
+            } else if (!tmask) {
+                // per-key scales: x <- s * k_scale in place
 #pragma unroll
                 for (int c4 = 0; c4 < BN / 4; ++c4) {
                     const float4 k = ksc4[c4];
@@ -485,6 +522,28 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const float nb = tb - (m_run == -INFINITY ? 0.0f : m_run);
             // ---- P = 2^(z*rq + tb - m), packed f16 pairs over the S columns
             float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (uni) {
+#pragma unroll
+                for (int h = 0; h < BN / 64; ++h) {
+                    const float kr = kg[h] * rq;
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int q4 = 0; q4 < 16; ++q4) {
+                        const int c = 64 * h + 4 * q4;
+                        const float p0 = fast_exp2(fmaf(__uint_as_float(x[c]), kr, nb));
+                        const float p1 = fast_exp2(fmaf(__uint_as_float(x[c + 1]), kr, nb));
+                        const float p2 = fast_exp2(fmaf(__uint_as_float(x[c + 2]), kr, nb));
+                        const float p3 = fast_exp2(fmaf(__uint_as_float(x[c + 3]), kr, nb));
+                        ls4[0] += p0;
+                        ls4[1] += p1;
+                        ls4[2] += p2;
+                        ls4[3] += p3;
+                        pk[2 * q4] = pack2(p0, p1, false);
+                        pk[2 * q4 + 1] = pack2(p2, p3, false);
+                    }
+                    tc::st32(s_t + h * 32, pk);
+                }
+            } else
 #pragma unroll
             for (int h = 0; h < BN / 64; ++h) {
                 // 64 keys -> 32 packed words -> TMEM columns [32h, 32h+32)
@@ -518,9 +577,12 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             done = jj + 1;
         }
         // ------------------------------------------------ epilogue
+        // O_DONE cannot tell the last phase from two phases back when S is
+        // double-buffered (the last two P.V may both be in flight), so the
+        // epilogue waits on a barrier that completes exactly once
         bool have = done == T && T > 0;
         if (have) {
-            const bool w = wait_ab(bar(B_O_DONE + t), (uint32_t)(T - 1) & 1u, p.err, abort_flag);
+            const bool w = wait_ab(bar(B_O_FINAL + t), 0u, p.err, abort_flag);
             have = __all_sync(0xffffffffu, w);
             tc::fence_after();
         }

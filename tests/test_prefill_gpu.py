@@ -131,6 +131,28 @@ def test_prefill_paged_prefix(sage, D, P):
     assert_close(np_(lse), l_ref, "lse")
 
 
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_prefill_repeatable(sage, D):
+    """Repeated calls give bit-identical outputs and LSE: the kernel has no
+    order-dependent reduction, so any difference is a read that raced a
+    tensor-core write (e.g. the epilogue reading O before the last P.V)."""
+    B, Hq, Hkv, Sc, P = 1, 8, 2, 1024, 2048
+    qkv = W.dense_qkv(B, Hq, Hkv, Sc, Sc, D, seed=D, dtype="bf16", device="cuda",
+                      k_offset_std=1.0)
+    c = W.paged_cache(B, Hkv, D, [P], seed=D + 1, device="cuda")
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 128, 64, True)
+    outs = []
+    for _ in range(6):
+        outs.append(sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, qkv.v, causal=True,
+                                           q_bias=bias, prefix=_prefix_dict(c, P),
+                                           return_lse=True))
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    for o, l in outs[1:]:
+        assert torch.equal(o, outs[0][0])
+        assert torch.equal(l, outs[0][1])
+
+
 def test_prefill_paged_prefix_raw_scores(sage):
     B, Hq, Hkv, Sc, D, P = 1, 2, 1, 64, 256, 77
     qkv = W.dense_qkv(B, Hq, Hkv, Sc, Sc, D, seed=3, dtype="bf16", device="cuda")
