@@ -57,6 +57,7 @@ struct PCfg {
     static constexpr int BN = D == 256 ? 64 : 128;
     static constexpr int NQ = D == 256 ? 1 : 2;  // 128-row query tiles per CTA
     static constexpr int NS = D == 256 ? 2 : 1;  // S buffers per query tile
+    static constexpr int NPH = BN / 64;          // P handed to the MMA in 64-key parts
     // softmax warpgroups + one warpgroup holding the producer and MMA warps
     // (and two idle warps, so that register reallocation works per warpgroup)
     static constexpr int THREADS = NQ * 128 + 128;
@@ -87,7 +88,7 @@ enum {
     B_K_EMPTY = 8,    // [NST] MMA: every QK^T reading the K stage retired
     B_V_EMPTY = 12,   // [NST] MMA: every P.V reading the V stage retired
     B_S_FULL = 16,    // [NQ*NS] MMA: S = Q K^T done
-    B_P_FULL = 20,    // [NQ*NS] softmax: P written to TMEM (and O rescaled)
+    B_P_FULL = 20,    // [NQ*NS*NPH] softmax: a 64-key part of P in TMEM (O rescaled)
     B_O_DONE = 24,    // [NQ] MMA: O_t += P_t V done
     B_O_FINAL = 26,   // [NQ] MMA: the last O_t += P_t V done (one phase)
     B_Q_READY = 28,   // softmax: Q in shared memory
@@ -120,6 +121,40 @@ __device__ __forceinline__ float fast_exp2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Packed FP32 pair arithmetic (fma / mul / add .f32x2 on sm_100-family
+// parts): one instruction updates two values, which halves the FP32 issue
+// slots the softmax spends per score.  Same rounding as the scalar forms.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 u2f2(uint32_t a, uint32_t b) {
+    return make_float2(__uint_as_float(a), __uint_as_float(b));
 }
 
 // three-input maximum (one instruction on sm_100-family parts)
@@ -206,10 +241,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             mbar_init(bar(B_K_EMPTY + s), 1);
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
-        for (int s = 0; s < NQ * NS; ++s) {
-            mbar_init(bar(B_S_FULL + s), 1);
-            mbar_init(bar(B_P_FULL + s), 128);
-        }
+        for (int s = 0; s < NQ * NS; ++s) mbar_init(bar(B_S_FULL + s), 1);
+        for (int s = 0; s < NQ * NS * C::NPH; ++s) mbar_init(bar(B_P_FULL + s), 128);
         for (int t = 0; t < NQ; ++t) {
             mbar_init(bar(B_O_DONE + t), 1);
             mbar_init(bar(B_O_FINAL + t), 1);
@@ -288,32 +321,49 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         if (lane == 0 && T > 0) {
             const uint32_t idq = tc::idesc_f16(128, BN, false, false);
             const uint32_t idp = tc::idesc_f16(128, D, false, true);  // P.V in f16
+            // descriptors built once; a k-step adds its byte offset >> 4
+            const uint64_t qd0 = tc::sdesc_sw128(sm_a, 16, 1024);
+            const uint64_t kd0 = tc::sdesc_sw128(sm_a + C::OFF_ST, 16, 1024);
+            const uint64_t vd0 = tc::sdesc_sw128(sm_a + C::OFF_ST + C::KB, BN * 128, 1024);
             auto qk = [&](int jj, int t) {
                 const int slot = t * NS + (NS == 1 ? 0 : (jj & 1));
-                const uint32_t kst = sm_a + C::OFF_ST + (jj % NST) * C::SB;
-                const uint32_t qst = sm_a + t * C::QB;
+                const uint64_t qd = qd0 + (uint64_t)((t * C::QB) >> 4);
+                const uint64_t kd = kd0 + (uint64_t)(((jj % NST) * C::SB) >> 4);
                 const uint32_t d = tmem + C::COL_S + slot * BN;
+                tc::mma_ss(d, qd, kd, idq, 0u);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t ad =
-                        tc::sdesc_sw128(qst + (ks >> 2) * (128 * 128) + (ks & 3) * 32, 16, 1024);
-                    const uint64_t bd =
-                        tc::sdesc_sw128(kst + (ks >> 2) * (BN * 128) + (ks & 3) * 32, 16, 1024);
-                    tc::mma_ss(d, ad, bd, idq, ks > 0 ? 1u : 0u);
-                }
+                for (int ks = 1; ks < D / 16; ++ks)
+                    tc::mma_ss_acc(d, qd + (((ks >> 2) * (128 * 128) + (ks & 3) * 32) >> 4),
+                                   kd + (((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4), idq);
                 tc::commit(bar(B_S_FULL + slot));
             };
-            auto pv = [&](int jj, int t) {
+            // O_t += P_t V_j in 64-key parts, each issued as soon as the
+            // softmax has stored that part of P (the first part also needs V)
+            auto pv = [&](int jj, int t) -> bool {
                 const int slot = t * NS + (NS == 1 ? 0 : (jj & 1));
-                const uint32_t vst = sm_a + C::OFF_ST + (jj % NST) * C::SB + C::KB;
+                const uint32_t sp = NS == 1 ? (uint32_t)jj & 1u : (uint32_t)(jj >> 1) & 1u;
+                const uint64_t vd = vd0 + (uint64_t)(((jj % NST) * C::SB) >> 4);
                 const uint32_t pt = tmem + C::COL_S + slot * BN;
+                const uint32_t o = tmem + t * D;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t bd = tc::sdesc_sw128(vst + kk * 2048, BN * 128, 1024);
-                    tc::mma_ts(tmem + t * D, pt + kk * 8, bd, idp, (jj > 0 || kk > 0) ? 1u : 0u);
+                for (int h = 0; h < C::NPH; ++h) {
+                    bool ok = wait_ab(bar(B_P_FULL + slot * C::NPH + h), sp, p.err, abort_flag);
+                    if (ok && h == 0 && t == 0)
+                        ok = wait_ab(bar(B_V_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err,
+                                     abort_flag);
+                    if (!ok) return false;
+                    tc::fence_after();
+#pragma unroll
+                    for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {
+                        if (kk == 0)
+                            tc::mma_ts(o, pt, vd, idp, jj > 0 ? 1u : 0u);
+                        else
+                            tc::mma_ts_acc(o, pt + kk * 8, vd + ((kk * 2048) >> 4), idp);
+                    }
                 }
                 tc::commit(bar(B_O_DONE + t));
                 if (jj == T - 1) tc::commit(bar(B_O_FINAL + t));
+                return true;
             };
             auto k_ready = [&](int jj) {
                 const bool ok = wait_ab(bar(B_K_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err,
@@ -329,15 +379,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             }
             for (int jj = 0; ok && jj < T; ++jj) {
                 const int s = jj % NST;
-                const uint32_t ph = (uint32_t)(jj / NST) & 1u;
                 if constexpr (NS == 1) {
                     // per query tile: O_t += P_t V_j, then S_t = Q_t K_{j+1}
                     for (int t = 0; t < NQ; ++t) {
-                        ok = wait_ab(bar(B_P_FULL + t), (uint32_t)jj & 1u, p.err, abort_flag);
-                        if (ok && t == 0) ok = wait_ab(bar(B_V_FULL + s), ph, p.err, abort_flag);
-                        if (!ok) break;
-                        tc::fence_after();
-                        pv(jj, t);
+                        if (!(ok = pv(jj, t))) break;
                         if (t == NQ - 1) tc::commit(bar(B_V_EMPTY + s));
                         if (jj + 1 < T) {
                             if (t == 0 && !(ok = k_ready(jj + 1))) break;
@@ -352,12 +397,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                         qk(jj + 1, 0);
                         tc::commit(bar(B_K_EMPTY + (jj + 1) % NST));
                     }
-                    ok = wait_ab(bar(B_P_FULL + (jj & 1)), (uint32_t)(jj >> 1) & 1u, p.err,
-                                 abort_flag) &&
-                         wait_ab(bar(B_V_FULL + s), ph, p.err, abort_flag);
-                    if (!ok) break;
-                    tc::fence_after();
-                    pv(jj, 0);
+                    if (!(ok = pv(jj, 0))) break;
                     tc::commit(bar(B_V_EMPTY + s));
                 }
             }
@@ -458,18 +498,14 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
 #pragma unroll
                 for (int c4 = 0; c4 < BN / 4; ++c4) {
                     const float4 k = ksc4[c4];
-                    const float z0 = __uint_as_float(x[4 * c4]) * k.x;
-                    const float z1 = __uint_as_float(x[4 * c4 + 1]) * k.y;
-                    const float z2 = __uint_as_float(x[4 * c4 + 2]) * k.z;
-                    const float z3 = __uint_as_float(x[4 * c4 + 3]) * k.w;
-                    x[4 * c4] = __float_as_uint(z0);
-                    x[4 * c4 + 1] = __float_as_uint(z1);
-                    x[4 * c4 + 2] = __float_as_uint(z2);
-                    x[4 * c4 + 3] = __float_as_uint(z3);
-                    m4[0] = fmaxf(m4[0], z0);
-                    m4[1] = fmaxf(m4[1], z1);
-                    m4[2] = fmaxf(m4[2], z2);
-                    m4[3] = fmaxf(m4[3], z3);
+                    const float2 z01 = fmul2(u2f2(x[4 * c4], x[4 * c4 + 1]), make_float2(k.x, k.y));
+                    const float2 z23 = fmul2(u2f2(x[4 * c4 + 2], x[4 * c4 + 3]), make_float2(k.z, k.w));
+                    x[4 * c4] = __float_as_uint(z01.x);
+                    x[4 * c4 + 1] = __float_as_uint(z01.y);
+                    x[4 * c4 + 2] = __float_as_uint(z23.x);
+                    x[4 * c4 + 3] = __float_as_uint(z23.y);
+                    m4[c4 & 1] = fmax3(m4[c4 & 1], z01.x, z01.y);
+                    m4[2 + (c4 & 1)] = fmax3(m4[2 + (c4 & 1)], z23.x, z23.y);
                 }
             } else {
                 const int cl = p.causal ? min(nvalid, lim - kg0 + 1) : nvalid;  // keys [0, cl) count
@@ -514,66 +550,72 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     tc::ld32(tmem + lane_base + t * D + c * 32, o);
                     tc::wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * f);
+                    for (int e = 0; e < 32; e += 2) {
+                        const float2 v = fmul2(u2f2(o[e], o[e + 1]), make_float2(f, f));
+                        o[e] = __float_as_uint(v.x);
+                        o[e + 1] = __float_as_uint(v.y);
+                    }
                     tc::st32(tmem + lane_base + t * D + c * 32, o);
                 }
                 tc::wait_st();
             }
             const float nb = tb - (m_run == -INFINITY ? 0.0f : m_run);
             // ---- P = 2^(z*rq + tb - m), packed f16 pairs over the S columns
-            float ls4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            float2 ls01 = make_float2(0.0f, 0.0f), ls23 = make_float2(0.0f, 0.0f);
+            const float2 nb2 = make_float2(nb, nb);
             if (uni) {
 #pragma unroll
                 for (int h = 0; h < BN / 64; ++h) {
-                    const float kr = kg[h] * rq;
+                    const float2 kr2 = make_float2(kg[h] * rq, kg[h] * rq);
                     uint32_t pk[32];
 #pragma unroll
                     for (int q4 = 0; q4 < 16; ++q4) {
                         const int c = 64 * h + 4 * q4;
-                        const float p0 = fast_exp2(fmaf(__uint_as_float(x[c]), kr, nb));
-                        const float p1 = fast_exp2(fmaf(__uint_as_float(x[c + 1]), kr, nb));
-                        const float p2 = fast_exp2(fmaf(__uint_as_float(x[c + 2]), kr, nb));
-                        const float p3 = fast_exp2(fmaf(__uint_as_float(x[c + 3]), kr, nb));
-                        ls4[0] += p0;
-                        ls4[1] += p1;
-                        ls4[2] += p2;
-                        ls4[3] += p3;
-                        pk[2 * q4] = pack2(p0, p1, false);
-                        pk[2 * q4 + 1] = pack2(p2, p3, false);
+                        const float2 a01 = ffma2(u2f2(x[c], x[c + 1]), kr2, nb2);
+                        const float2 a23 = ffma2(u2f2(x[c + 2], x[c + 3]), kr2, nb2);
+                        const float2 p01 = make_float2(fast_exp2(a01.x), fast_exp2(a01.y));
+                        const float2 p23 = make_float2(fast_exp2(a23.x), fast_exp2(a23.y));
+                        ls01 = fadd2(ls01, p01);
+                        ls23 = fadd2(ls23, p23);
+                        pk[2 * q4] = pack2(p01.x, p01.y, false);
+                        pk[2 * q4 + 1] = pack2(p23.x, p23.y, false);
                     }
                     tc::st32(s_t + h * 32, pk);
+                    tc::wait_st();
+                    tc::fence_before();
+                    mbar_arrive(bar(B_P_FULL + slot * C::NPH + h));
                 }
-            } else
+            } else {
+                const float2 rq2 = make_float2(rq, rq);
 #pragma unroll
-            for (int h = 0; h < BN / 64; ++h) {
-                // 64 keys -> 32 packed words -> TMEM columns [32h, 32h+32)
-                uint32_t pk[32];
+                for (int h = 0; h < BN / 64; ++h) {
+                    // 64 keys -> 32 packed words -> TMEM columns [32h, 32h+32)
+                    uint32_t pk[32];
 #pragma unroll
-                for (int q4 = 0; q4 < 16; ++q4) {
-                    const int c4 = 16 * h + q4;
-                    const float p0 = fast_exp2(fmaf(__uint_as_float(x[4 * c4]), rq, nb));
-                    const float p1 = fast_exp2(fmaf(__uint_as_float(x[4 * c4 + 1]), rq, nb));
-                    const float p2 = fast_exp2(fmaf(__uint_as_float(x[4 * c4 + 2]), rq, nb));
-                    const float p3 = fast_exp2(fmaf(__uint_as_float(x[4 * c4 + 3]), rq, nb));
-                    ls4[0] += p0;
-                    ls4[1] += p1;
-                    ls4[2] += p2;
-                    ls4[3] += p3;
-                    if (pre) {
-                        const float4 v = vsc4[c4];
-                        pk[2 * q4] = pack2(p0 * v.x, p1 * v.y, false);
-                        pk[2 * q4 + 1] = pack2(p2 * v.z, p3 * v.w, false);
-                    } else {
-                        pk[2 * q4] = pack2(p0, p1, false);
-                        pk[2 * q4 + 1] = pack2(p2, p3, false);
+                    for (int q4 = 0; q4 < 16; ++q4) {
+                        const int c = 64 * h + 4 * q4;
+                        const float2 a01 = ffma2(u2f2(x[c], x[c + 1]), rq2, nb2);
+                        const float2 a23 = ffma2(u2f2(x[c + 2], x[c + 3]), rq2, nb2);
+                        float2 p01 = make_float2(fast_exp2(a01.x), fast_exp2(a01.y));
+                        float2 p23 = make_float2(fast_exp2(a23.x), fast_exp2(a23.y));
+                        ls01 = fadd2(ls01, p01);
+                        ls23 = fadd2(ls23, p23);
+                        if (pre) {
+                            // prefix keys: fold the per-token V scale into P
+                            const float4 v = vsc4[c / 4];
+                            p01 = fmul2(p01, make_float2(v.x, v.y));
+                            p23 = fmul2(p23, make_float2(v.z, v.w));
+                        }
+                        pk[2 * q4] = pack2(p01.x, p01.y, false);
+                        pk[2 * q4 + 1] = pack2(p23.x, p23.y, false);
                     }
+                    tc::st32(s_t + h * 32, pk);
+                    tc::wait_st();
+                    tc::fence_before();
+                    mbar_arrive(bar(B_P_FULL + slot * C::NPH + h));
                 }
-                tc::st32(s_t + h * 32, pk);
             }
-            l += (ls4[0] + ls4[1]) + (ls4[2] + ls4[3]);
-            tc::wait_st();
-            tc::fence_before();
-            mbar_arrive(bar(B_P_FULL + slot));
+            l += (ls01.x + ls01.y) + (ls23.x + ls23.y);
             done = jj + 1;
         }
         // ------------------------------------------------ epilogue
@@ -601,9 +643,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             if (row_ok) {
                 uint32_t pk[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    pk[e] = pack2(__uint_as_float(o[2 * e]) * inv, __uint_as_float(o[2 * e + 1]) * inv,
-                                  p.out_bf16 != 0);
+                for (int e = 0; e < 16; ++e) {
+                    const float2 v = fmul2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv));
+                    pk[e] = pack2(v.x, v.y, p.out_bf16 != 0);
+                }
                 uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out) +
                                                        orow * D + c * 32);
 #pragma unroll

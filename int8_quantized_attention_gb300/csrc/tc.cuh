@@ -93,6 +93,22 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// Accumulating forms with a constant enable-input-D operand (no predicate
+// set-up per instruction); the descriptors are built once and advanced by
+// adding (byte offset >> 4) to their start-address field.
+__device__ __forceinline__ void mma_ss_acc(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d_tmem),
+                 "l"(a_desc), "l"(b_desc), "r"(idesc)
+                 : "memory");
+}
+__device__ __forceinline__ void mma_ts_acc(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                           uint32_t idesc) {
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d_tmem),
+                 "r"(a_tmem), "l"(b_desc), "r"(idesc)
+                 : "memory");
+}
+
 // ------------------------------------------------------------ TMEM ld/st
 // 32 lanes x 32 bits, 32 consecutive columns: register i <- column col+i of
 // the lane (taddr lane field) + thread index.
