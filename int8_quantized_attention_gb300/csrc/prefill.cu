@@ -465,12 +465,22 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             for (int c = 0; c < BN / 32; ++c)
                 tc::ld32(s_t + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
             tc::wait_ld();
-            if (p.dbg && row_ok) {
+            if (p.dbg) {
+                // debug dump of the raw INT32 scores, re-read from TMEM in
+                // 8-column pieces so that it adds no live registers here
                 int32_t *dr = p.dbg + (((int64_t)b * p.Hq + hq) * p.Sq + i) * p.dbg_stride;
+#pragma unroll 1
+                for (int c8 = 0; c8 < BN / 8; ++c8) {
+                    uint32_t v[8];
+                    tc::ld8(s_t + c8 * 8, v);
+                    tc::wait_ld();
 #pragma unroll
-                for (int c = 0; c < BN; ++c)
-                    if (c < nvalid && (!p.causal || kg0 + c <= lim))
-                        dr[kg0 + c] = __float2int_rn(__uint_as_float(x[c]));
+                    for (int e = 0; e < 8; ++e) {
+                        const int c = c8 * 8 + e;
+                        if (row_ok && c < nvalid && (!p.causal || kg0 + c <= lim))
+                            dr[kg0 + c] = __float2int_rn(__uint_as_float(v[e]));
+                    }
+                }
             }
             // ---- the row max of the scaled scores
             const bool tmask = nvalid < BN || (p.causal && kg0 + BN - 1 > i_first + off);
@@ -544,18 +554,19 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 }
                 tc::fence_after();
                 const float f = fix ? alpha : 1.0f;
+                // 8-column pieces: the S row is live in registers here
 #pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tc::ld32(tmem + lane_base + t * D + c * 32, o);
+                for (int c = 0; c < D / 8; ++c) {
+                    uint32_t o[8];
+                    tc::ld8(tmem + lane_base + t * D + c * 8, o);
                     tc::wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
+                    for (int e = 0; e < 8; e += 2) {
                         const float2 v = fmul2(u2f2(o[e], o[e + 1]), make_float2(f, f));
                         o[e] = __float_as_uint(v.x);
                         o[e + 1] = __float_as_uint(v.y);
                     }
-                    tc::st32(tmem + lane_base + t * D + c * 32, o);
+                    tc::st8(tmem + lane_base + t * D + c * 8, o);
                 }
                 tc::wait_st();
             }
