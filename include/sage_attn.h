@@ -113,7 +113,11 @@ sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B, int H, i
  *   lse   = ln sum_j exp(t_j)
  * The context is cut into num_segments contiguous runs of pages; each is
  * reduced on its own and the partials are merged by the LSE combine
- * (sage_splitk_combine).
+ * (sage_splitk_combine).  With 2..8 segments the segments of one (sequence,
+ * KV head) run as one thread-block cluster and the combine happens in
+ * distributed shared memory inside the same kernel (one launch, no partials
+ * in device memory); with more segments the partials go through the
+ * workspace and the combine kernel.
  * ------------------------------------------------------------------------ */
 typedef struct sage_decode_args {
     const int8_t *q;            /* [B, Hq, D] int8 (sage_quant_int8 output) */
@@ -137,11 +141,14 @@ typedef struct sage_decode_args {
 /* Segment count the library picks for num_segments == 0 (host only): the
  * count whose CTAs (B * Hkv * ceil(Hq/Hkv/8) * S) fill the GPU's resident
  * decode slots in the fewest, fullest waves, with at least 4 pages per
- * segment. */
+ * segment; 8 (in-cluster combine) is preferred over a larger single-wave
+ * count when it still fills 75 % of the slots. */
 int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len);
 
-/* Bytes of workspace sage_attn_decode_paged needs: fp32 partial outputs
- * [B,Hq,S,D] plus fp32 partial LSEs [B,Hq,S] (0 when S == 1). */
+/* Bytes of workspace sage_attn_decode_paged may need: fp32 partial outputs
+ * [B,Hq,S,D] plus fp32 partial LSEs [B,Hq,S] (0 when S == 1).  A call with
+ * 2..8 segments normally combines in-cluster and leaves the workspace
+ * untouched; it uses the workspace only if the cluster launch is refused. */
 size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments);
 
 /* workspace: device buffer of at least sage_attn_decode_workspace_size()

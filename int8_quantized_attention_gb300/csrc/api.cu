@@ -251,6 +251,11 @@ SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_con
     int64_t best = 1;
     if (units <= slots) {
         best = slots / units;
+        // up to kDecodeMaxCluster segments merge inside one thread-block
+        // cluster (no partials in HBM, no combine launch): worth a slightly
+        // emptier wave, down to 75 % of the slots
+        if (best > sage::kDecodeMaxCluster && units * sage::kDecodeMaxCluster * 4 >= slots * 3)
+            best = sage::kDecodeMaxCluster;
     } else {
         for (int64_t S = 1; S <= smax; ++S) {
             const int64_t ctas = units * S;
@@ -348,6 +353,20 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
         cudaError_t e = sage::launch_decode(p, static_cast<cudaStream_t>(stream), g_last);
         return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "decode launch");
     }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (S > 1 && S <= sage::kDecodeMaxCluster) {
+        // the segments of each (sequence, kv head, head tile) form one
+        // cluster and combine in distributed shared memory
+        p.cluster = 1;
+        cudaError_t e = sage::launch_decode(p, cs, g_last);
+        if (e == cudaSuccess) return SAGE_OK;
+        if (e != cudaErrorInvalidClusterSize && e != cudaErrorNotSupported &&
+            e != cudaErrorLaunchOutOfResources)
+            return cuda_fail(e, "decode launch (cluster)");
+        cudaGetLastError();  // clear, then take the partials + combine path below
+        p.cluster = 0;
+        g_last = sage::LaunchLog();
+    }
     if (S > 1) {
         const size_t need = sage_attn_decode_workspace_size(a->B, a->Hq, a->D, S);
         if (!workspace || workspace_bytes < need)
@@ -359,7 +378,6 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
         p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
                                                ((rows * a->D * sizeof(float) + 255) & ~(size_t)255));
     }
-    cudaStream_t cs = static_cast<cudaStream_t>(stream);
     cudaError_t e = sage::launch_decode(p, cs, g_last);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     if (S > 1) {

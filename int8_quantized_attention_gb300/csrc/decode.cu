@@ -23,9 +23,19 @@
 //     FP32 accumulation.
 // At the end the four warps merge (m, l, O) through shared memory and the
 // CTA writes either the segment partial (O normalised, LSE) or, with one
-// segment, the final output.
+// segment, the final output.  When the segments of a (sequence, kv head,
+// head tile) are launched as one thread-block cluster (at most 8), the LSE
+// combine ("INT8 QK MMAC on gfx936 DCU", section 4: split-K) happens here
+// instead: each CTA leaves its normalised segment output and base-2 LSE in
+// its shared memory, and after a cluster barrier every CTA reduces a slice
+// of the outputs by reading all segments through distributed shared memory,
+// so no partial touches HBM and no second kernel is launched.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace sage {
 
@@ -362,6 +372,80 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
         }
     }
     __syncthreads();
+    if (p.cluster) {
+        // ------------------------------------------- in-cluster LSE combine
+        // this CTA's segment result: co[head][D] normalised, cl[head] base-2 LSE
+        float *co = ml + kConsumerWarps * 8;
+        float *cl = co + 8 * D;
+        for (int idx = threadIdx.x; idx < nheads * D; idx += kThreads) {
+            const int j = idx / D, d = idx - j * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + j]);
+            float val = 0.0f;
+            if (M != -INFINITY) {
+                float L = 0.0f, acc = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float f = exp2f(mm[w * 8 + j] - M);
+                    L = fmaf(f, ml[w * 8 + j], L);
+                    acc = fmaf(f, mo[(w * 8 + j) * D + d], acc);
+                }
+                val = acc / L;
+            }
+            co[j * D + d] = val;
+        }
+        if (threadIdx.x < nheads) {
+            const int j = threadIdx.x;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + j]);
+            float lse2 = -INFINITY;
+            if (M != -INFINITY) {
+                float L = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w)
+                    L = fmaf(exp2f(mm[w * 8 + j] - M), ml[w * 8 + j], L);
+                lse2 = M + log2f(L);
+            }
+            cl[j] = lse2;
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int S = p.num_segments;
+        for (int idx = seg * kThreads + threadIdx.x; idx < nheads * D; idx += S * kThreads) {
+            const int j = idx / D, d = idx - j * D;
+            float ls[kDecodeMaxCluster];
+            float M = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < kDecodeMaxCluster; ++r) {
+                ls[r] = r < S ? cluster.map_shared_rank(cl, r)[j] : -INFINITY;
+                M = fmaxf(M, ls[r]);
+            }
+            float val = 0.0f, L = 0.0f;
+            if (M != -INFINITY) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int r = 0; r < kDecodeMaxCluster; ++r) {
+                    if (r < S && ls[r] != -INFINITY) {
+                        const float w = exp2f(ls[r] - M);
+                        L += w;
+                        acc = fmaf(w, cluster.map_shared_rank(co, r)[j * D + d], acc);
+                    }
+                }
+                val = acc / L;
+            }
+            const int64_t row = (int64_t)b * p.Hq + head0 + j;
+            if (p.out_bf16)
+                reinterpret_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(val);
+            else
+                reinterpret_cast<__half *>(p.out)[row * D + d] = __float2half_rn(val);
+            if (d == 0 && p.lse)
+                p.lse[row] = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.69314718055994530942f;
+        }
+        cluster.sync();  // every CTA's shared memory stays alive until all have read it
+        return;
+    }
     const bool direct = p.num_segments == 1 && !p.force_partials;
     for (int idx = threadIdx.x; idx < nheads * D; idx += kThreads) {
         const int j = idx / D, d = idx - j * D;
@@ -417,8 +501,26 @@ cudaError_t launch_d(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {
         cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const dim3 grid(p.num_segments, p.Hkv * p.head_tiles, p.B);
-    decode_kernel<D><<<grid, kThreads, Cfg::kSmem, st>>>(p);
-    log.add("decode_kernel", grid, dim3(kThreads), dim3(1, 1, 1), Cfg::kSmem);
+    if (p.cluster) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = Cfg::kSmem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = p.num_segments;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, p);
+        if (e != cudaSuccess) return e;
+        log.add("decode_kernel", grid, dim3(kThreads), dim3(p.num_segments, 1, 1), Cfg::kSmem);
+    } else {
+        decode_kernel<D><<<grid, kThreads, Cfg::kSmem, st>>>(p);
+        log.add("decode_kernel", grid, dim3(kThreads), dim3(1, 1, 1), Cfg::kSmem);
+    }
     log.segments = p.num_segments;
     return cudaGetLastError();
 }

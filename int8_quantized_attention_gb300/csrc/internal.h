@@ -74,8 +74,13 @@ struct DecodeParams {
     int32_t *dbg;             // optional raw score dump [B*Hq, dbg_stride]
     int dbg_stride;
     int force_partials;       // write o_part/lse_part even with one segment
+    int cluster;              // 1: the segments of a (sequence, kv head, head tile) form one
+                              // thread-block cluster and merge through distributed shared memory
     int *err;
 };
+
+constexpr int kDecodeMaxCluster = 8;   // segments merged in-cluster (portable cluster size;
+                                       // larger, non-portable clusters measured slower)
 
 int decode_ctas_per_sm(int D);
 int decode_max_segment_pages();   // longest segment (in 16-token pages) one CTA takes

@@ -28,7 +28,7 @@ def _oracle(qi, qs, c, pairs=None):
 
 @pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("Hq,Hkv", [(12, 2), (4, 4), (16, 2), (24, 4)])
-@pytest.mark.parametrize("segments", [1, 3, 0])
+@pytest.mark.parametrize("segments", [1, 3, 12, 24, 0])
 def test_decode_small(sage, D, Hq, Hkv, segments):
     B = 3
     lens = [37, 300, 129]                     # ragged last pages
@@ -160,10 +160,17 @@ def test_bounded_wait_times_out_and_context_survives(sage):
 def test_decode_launch_record(sage):
     c = W.paged_cache(2, 4, 256, [4096, 4096], seed=1, device="cuda")
     qi, qs = _quant_query(sage, 2, 24, 256, seed=1)
+    # up to 8 segments: one launch, the segments of a (sequence, kv head)
+    # form a cluster and combine in distributed shared memory
     _run(sage, qi, qs, c, 4096, num_segments=8)
     info = sage.last_launch_info()
     assert info["kernel"] == "decode_kernel" and info["num_segments"] == 8
-    assert info["launches"] == 2 and info["grid"] == (8, 4, 2)
+    assert info["launches"] == 1 and info["grid"] == (8, 4, 2) and info["cluster"] == (8, 1, 1)
+    # more segments: partials in the workspace, then the combine kernel
+    _run(sage, qi, qs, c, 4096, num_segments=32)
+    info = sage.last_launch_info()
+    assert info["kernel"] == "decode_kernel" and info["num_segments"] == 32
+    assert info["launches"] == 2 and info["grid"] == (32, 4, 2) and info["cluster"] == (1, 1, 1)
 
 
 def test_decode_paged_decode_full_size(sage):
@@ -211,7 +218,11 @@ def test_decode_partials_then_combine(sage):
     full, lfull = _run(sage, qi, qs, c, max(lens), num_segments=5, return_lse=True,
                        out_dtype=torch.float16)
     torch.cuda.synchronize()
-    assert torch.equal(out, full) and torch.equal(lse, lfull)
+    # up to 8 segments the full decode combines inside a thread-block cluster
+    # (base-2 arithmetic), the standalone kernel in natural log: equal up to
+    # fp32 rounding order, i.e. within an ulp of the f16 output
+    assert_close(f32(out), f32(full), "combine vs fused", rel=1e-3, abs_=1e-3)
+    assert_close(np_(lse), np_(lfull), "lse combine vs fused", rel=1e-6, abs_=1e-5)
     # each segment partial is itself the attention over its own key range
     pps = ((max(lens) + 15) // 16 + 4) // 5 * 16
     seg = 1
