@@ -138,11 +138,13 @@ typedef struct sage_decode_args {
     float *lse;                 /* optional [B, Hq] natural-log LSE (-inf for empty context) */
 } sage_decode_args_t;
 
-/* Segment count the library picks for num_segments == 0 (host only): the
- * count whose CTAs (B * Hkv * ceil(Hq/Hkv/8) * S) fill the GPU's resident
- * decode slots in the fewest, fullest waves, with at least 4 pages per
- * segment; 8 (in-cluster combine) is preferred over a larger single-wave
- * count when it still fills 75 % of the slots. */
+/* Segment count the library picks for num_segments == 0 (host only).  With
+ * U = B * Hkv * ceil(Hq/Hkv/8) (sequence, KV head, 8-head tile) units and
+ * P = ceil(max_context_len/16) pages it aims at about 1.7 CTAs per SM when
+ * U * P / SMs < 400 pages, else about 5 per SM (S = target / U rounded, at
+ * least 4 pages per segment, at most 64 segments); 8 (in-cluster combine) is
+ * preferred over a larger count that it reaches to within 3/4.  The rule is
+ * empirical, measured on GB300. */
 int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len);
 
 /* Bytes of workspace sage_attn_decode_paged may need: fp32 partial outputs

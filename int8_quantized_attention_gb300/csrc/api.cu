@@ -238,36 +238,29 @@ SAGE_API sage_status_t sage_splitk_combine(const float *o_part, const float *lse
 
 SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len) {
     if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || max_context_len <= 0) return 1;
+    (void)D;
     const int group = Hq / Hkv;
     const int64_t units = (int64_t)B * Hkv * ((group + 7) / 8);
-    const int64_t slots = (int64_t)sm_count() * sage::decode_ctas_per_sm(D);
+    const int64_t sms = sm_count();
     const int pages = (max_context_len + 15) / 16;
-    // at least one page per consumer warp in every segment
+    // at least 4 pages per segment (one per consumer warp), at most 64 segments
     int64_t smax = pages / 4 > 1 ? pages / 4 : 1;
     if (smax > 64) smax = 64;
-    // One resident wave when the (sequence, kv head) units leave room: the
-    // largest S whose CTAs all fit.  Otherwise the fewest segments whose CTAs
-    // fill at least 90 % of the wave-slots they occupy (no near-empty tail).
-    int64_t best = 1;
-    if (units <= slots) {
-        best = slots / units;
-        // up to kDecodeMaxCluster segments merge inside one thread-block
-        // cluster (no partials in HBM, no combine launch): worth a slightly
-        // emptier wave, down to 75 % of the slots
-        if (best > sage::kDecodeMaxCluster && units * sage::kDecodeMaxCluster * 4 >= slots * 3)
-            best = sage::kDecodeMaxCluster;
-    } else {
-        for (int64_t S = 1; S <= smax; ++S) {
-            const int64_t ctas = units * S;
-            const int64_t waves = (ctas + slots - 1) / slots;
-            if ((double)ctas >= 0.9 * (double)(waves * slots)) {
-                best = S;
-                break;
-            }
-        }
-    }
-    if (best > smax) best = smax;
+    // Measured on GB300 (D = 256, 3 CTAs per SM): with little work per SM
+    // (under ~400 pages) about 1.7 CTAs per SM is fastest (longer segments
+    // amortise each CTA's start and merge); with more work about 5 per SM
+    // (shorter CTAs even out the tail).
+    const int64_t pages_per_sm = units * pages / (sms > 0 ? sms : 1);
+    const int64_t target = pages_per_sm < 400 ? (sms * 27 + 8) / 16 : sms * 5;
+    int64_t best = (target + units / 2) / units;
     if (best < 1) best = 1;
+    if (best > smax) best = smax;
+    // up to kDecodeMaxCluster segments combine inside one thread-block
+    // cluster (no partials in device memory, no combine launch): take it
+    // while it keeps at least 3/4 of the target CTA count
+    if (best > sage::kDecodeMaxCluster &&
+        units * sage::kDecodeMaxCluster * 4 >= target * 3 && sage::kDecodeMaxCluster <= smax)
+        best = sage::kDecodeMaxCluster;
     const int64_t cap = sage::decode_max_segment_pages();
     if (best * cap < pages) best = (pages + cap - 1) / cap;
     const int64_t pps = (pages + best - 1) / best;

@@ -117,6 +117,20 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
     hi = *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Same exact conversion, pairing bytes (0, 2) and (1, 3): for a register
+// holding two 16-bit elements of two rows (a transposed ldmatrix of int8 data),
+// `even` gets the low byte of each element and `odd` the high byte.
+__device__ __forceinline__ void i8x4_to_f16x2_even_odd(uint32_t w, uint32_t &even, uint32_t &odd) {
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t a = __byte_perm(u, 0x64646464u, 0x4240);  // halves: 0x64|u0, 0x64|u2
+    uint32_t c = __byte_perm(u, 0x64646464u, 0x4341);  // halves: 0x64|u1, 0x64|u3
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+    __half2 l = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
+    __half2 h = __hsub2(*reinterpret_cast<__half2 *>(&c), bias);
+    even = *reinterpret_cast<uint32_t *>(&l);
+    odd = *reinterpret_cast<uint32_t *>(&h);
+}
+
 // bf16 variant: the fp32 with bits 0x4B000000 | u equals 2^23 + u exactly;
 // subtracting 2^23 + 128 gives b exactly, and every |b| <= 128 is exact in
 // bf16 (8 significand bits), so the final rounding is exact too.

@@ -51,14 +51,14 @@ struct DecodeCfg {
     static constexpr int kSlab = D * 16;                 // bytes of one page slab
     static constexpr int kStageBytes = 2 * kSlab + 128;  // K, V, K scales, V scales
     static constexpr int kStages = D == 256 ? 8 : (D == 128 ? 12 : 16);
-    static constexpr int kVStage = D * 16 * 2;           // per-warp f16 copy of V
     static constexpr int kRingBytes = kStages * kStageBytes;
-    static constexpr int kOffBar = kRingBytes + kConsumerWarps * kVStage;
+    static constexpr int kOffBar = kRingBytes;
+    // after the loop the ring holds the warp merge and the cluster combine
+    static_assert(kRingBytes >= (2 * kConsumerWarps * 8 + kConsumerWarps * 8 * D + 8 * D + 8) * 4,
+                  "merge area fits in the ring");
     static constexpr int kOffBt = kOffBar + kStages * 16 + 64;
     static constexpr int kSmem = kOffBt + kMaxSegPages * 4;
     static constexpr int kCtasPerSm = 227 * 1024 / (kSmem + 1024);
-    // pages whose K/V slabs are prefetched into L2 ahead of the ring
-    static constexpr int kPrefetchPages = 8;
     // Page i goes to stage i % kStages and to consumer warp i % kConsumerWarps.
     // Every stage must always be read by the same warp: mbarrier parity waits
     // cannot tell phase k from phase k-2, so a stage shared by two warps
@@ -114,13 +114,12 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
+__global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
     using Cfg = DecodeCfg<D>;
     constexpr int NST = Cfg::kStages;
     extern __shared__ __align__(128) uint8_t smem[];
     uint8_t *ring = smem;
-    uint8_t *vst_all = smem + Cfg::kRingBytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(vst_all + kConsumerWarps * Cfg::kVStage);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + Cfg::kOffBar);
     uint64_t *empty = full + NST;
     int *stage_ok = reinterpret_cast<int *>(empty + NST);
     int *bt_s = reinterpret_cast<int *>(smem + Cfg::kOffBt);
@@ -222,65 +221,35 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
             colscale[j] = hc < nheads ? p.q_scale[(int64_t)b * p.Hq + head0 + hc] * p.qk_scale_log2
                                       : 0.0f;
         }
-        uint8_t *vst = vst_all + warp * Cfg::kVStage;
-        const uint32_t vst_a = smem_u32(vst);
-        // HBM latency under full load is several microseconds, far more than
-        // the ring covers: each warp also prefetches, with plain per-lane L2
-        // prefetches (no shared memory, no registers), the K and V slabs of
-        // the pages kPrefetchPages ahead, so the ring's copies hit in L2.
-        auto prefetch_page = [&](int i) {
-            if (i < np) {
-                const int blk = bt_s[i];
-                if ((unsigned)blk < (unsigned)p.num_blocks) {
-                    const int64_t pg = (int64_t)blk * p.Hkv + kvh;
-                    for (int ln = lane; ln < Cfg::kSlab / 128; ln += 32) {  // 128-byte lines
-                        const int64_t off = pg * Cfg::kSlab + ln * 128;
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.k_cache + off));
-                        asm volatile("prefetch.global.L2 [%0];" ::"l"(p.v_cache + off));
-                    }
-                }
-            }
-        };
-        for (int i = warp + NST; i < min(np, Cfg::kPrefetchPages); i += kConsumerWarps)
-            prefetch_page(i);
+        // ldmatrix row address of this lane for the transposed V loads:
+        // matrix (lane / 8) = (16-channel block 2*dp + lane/16, keys 0-7 or 8-15)
+        const uint32_t v_off = (lane >> 4) * 256 + ((lane >> 3) & 1) * 128 + (lane & 7) * 16;
         for (int i = warp; i < np; i += kConsumerWarps) {
-            prefetch_page(i + Cfg::kPrefetchPages);
             const int s = i % NST;
             const bool got = mbar_wait(smem_u32(&full[s]), (uint32_t)(i / NST) & 1u, p.err);
             if (!__all_sync(0xffffffffu, got)) break;  // keep the warp converged
             const uint8_t *stg = ring + s * Cfg::kStageBytes;
             const bool ok = stage_ok[s] != 0;
             const uint32_t stg_a = smem_u32(stg);
-            // ---- QK^T: rows = 16 keys of the page, cols = 8 heads
-            int c[4] = {0, 0, 0, 0};
+            // ---- QK^T: rows = 16 keys of the page, cols = 8 heads; two
+            // independent accumulation chains (integer sums, exact)
+            int c[4] = {0, 0, 0, 0}, c2[4] = {0, 0, 0, 0};
 #pragma unroll
-            for (int ks = 0; ks < D / 32; ++ks) {
+            for (int ks = 0; ks < D / 32; ks += 2) {
                 uint32_t a[4];
                 ldsm_x4(stg_a + ks * 512 + lane * 16, a);
                 mma_s8(c, a, qf[ks][0], qf[ks][1]);
+                if (ks + 1 < D / 32) {
+                    ldsm_x4(stg_a + (ks + 1) * 512 + lane * 16, a);
+                    mma_s8(c2, a, qf[ks + 1][0], qf[ks + 1][1]);
+                }
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[e] += c2[e];
             const float *ksc = reinterpret_cast<const float *>(stg + 2 * Cfg::kSlab);
             const float *vsc = ksc + 16;
             const float sk0 = ksc[g], sk1 = ksc[g + 8];
             const float sv0 = vsc[g], sv1 = vsc[g + 8];
-            // ---- V int8 -> f16 into this warp's staging (row = chunk*16 + key)
-#pragma unroll
-            for (int it = 0; it < D / 32; ++it) {
-                const int row = it * 32 + lane;
-                const int dc = row >> 4, key = row & 15;
-                const uint4 w = *reinterpret_cast<const uint4 *>(stg + Cfg::kSlab + row * 16);
-                uint4 h0, h1;
-                i8x4_to_f16x4(w.x, h0.x, h0.y);
-                i8x4_to_f16x4(w.y, h0.z, h0.w);
-                i8x4_to_f16x4(w.z, h1.x, h1.y);
-                i8x4_to_f16x4(w.w, h1.z, h1.w);
-                const int sw = (key >> 2) & 1;
-                uint8_t *dst = vst + dc * 512 + key * 32;
-                *reinterpret_cast<uint4 *>(dst + (sw ? 16 : 0)) = h0;
-                *reinterpret_cast<uint4 *>(dst + (sw ? 0 : 16)) = h1;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // stage fully read
             // ---- scores, mask, online softmax (base 2)
             const int tok0 = (pg0 + i) * 16;
             const bool v0 = ok && (tok0 + g) < ctx, v1 = ok && (tok0 + g + 8) < ctx;
@@ -301,42 +270,59 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
                 t[0][j] = v0 ? (float)c[j] * sk0 * colscale[j] : -INFINITY;
                 t[1][j] = v1 ? (float)c[2 + j] * sk1 * colscale[j] : -INFINITY;
             }
+            // Lazy rescaling: the running max m moves only when a page's max
+            // exceeds it by more than 2^8, so most pages leave O untouched
+            // (P then stays below 2^8; f16 P and fp32 O/l hold that easily).
             float alpha[2], pr[2][2];
+            bool need = false;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 float mx = fmaxf(t[0][j], t[1][j]);
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mn = fmaxf(m[j], mx);
-                const float ms = mn == -INFINITY ? 0.0f : mn;  // all masked so far
-                alpha[j] = fast_exp2(m[j] - ms);
+                alpha[j] = 1.0f;
+                if (mx != -INFINITY && (m[j] == -INFINITY || mx > m[j] + 8.0f)) {
+                    alpha[j] = m[j] == -INFINITY ? 0.0f : fast_exp2(m[j] - mx);
+                    m[j] = mx;
+                    need = true;
+                }
+                const float ms = m[j] == -INFINITY ? 0.0f : m[j];  // all masked so far
                 pr[0][j] = fast_exp2(t[0][j] - ms);
                 pr[1][j] = fast_exp2(t[1][j] - ms);
                 l[j] = l[j] * alpha[j] + pr[0][j] + pr[1][j];
-                m[j] = mn;
             }
+            if (__any_sync(0xffffffffu, need)) {
 #pragma unroll
-            for (int dt = 0; dt < D / 16; ++dt) {
-                o[dt][0] *= alpha[0];
-                o[dt][1] *= alpha[1];
-                o[dt][2] *= alpha[0];
-                o[dt][3] *= alpha[1];
+                for (int dt = 0; dt < D / 16; ++dt) {
+                    o[dt][0] *= alpha[0];
+                    o[dt][1] *= alpha[1];
+                    o[dt][2] *= alpha[0];
+                    o[dt][3] *= alpha[1];
+                }
             }
             // ---- P^T (x v_scale) -> B operand via in-register transpose
             const uint32_t pb0 = movmatrix_trans(pack_f16x2(pr[0][0] * sv0, pr[0][1] * sv0));
             const uint32_t pb1 = movmatrix_trans(pack_f16x2(pr[1][0] * sv1, pr[1][1] * sv1));
-            // ---- O^T += V^T P^T
-            const int mi = lane >> 3, r8 = lane & 7;
-            const int key = (mi >> 1) * 8 + r8;
-            const uint32_t a_off = key * 32 + ((((mi & 1) ^ ((key >> 2) & 1))) * 16);
+            // ---- O^T += V^T P^T.  A = V^T straight from the INT8 slab: a
+            // transposed ldmatrix gives each lane keys (2q4, 2q4+1) of the
+            // channel pair (2g, 2g+1); the even channel fills A row g, the odd
+            // one row g + 8, so accumulator rows g / g+8 hold channels 2g / 2g+1
+            // of the 16-channel block.  Exact int8 -> f16 in registers.
+            const uint32_t vstg = stg_a + Cfg::kSlab + v_off;
 #pragma unroll
-            for (int dt = 0; dt < D / 16; ++dt) {
-                uint32_t a[4];
-                ldsm_x4_trans(vst_a + dt * 512 + a_off, a);
-                mma_f16(o[dt], a, pb0, pb1);
+            for (int dp = 0; dp < D / 32; ++dp) {
+                uint32_t r[4], a[4];
+                ldsm_x4_trans(vstg + dp * 512, r);
+                i8x4_to_f16x2_even_odd(r[0], a[0], a[1]);
+                i8x4_to_f16x2_even_odd(r[1], a[2], a[3]);
+                mma_f16(o[2 * dp], a, pb0, pb1);
+                i8x4_to_f16x2_even_odd(r[2], a[0], a[1]);
+                i8x4_to_f16x2_even_odd(r[3], a[2], a[3]);
+                mma_f16(o[2 * dp + 1], a, pb0, pb1);
             }
-            __syncwarp();  // staging is rewritten by this warp's next page
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // stage fully read
         }
         // ---- per-warp totals of l over the 8 key rows sharing a column
 #pragma unroll
@@ -349,10 +335,10 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
     __syncthreads();  // ring and staging are free from here on
 
     // ------------------------------------------------------- warp merge
-    // merge area: mo[w][head][D] aliases the V staging; mm/ml alias the ring
-    float *mo = reinterpret_cast<float *>(vst_all);
+    // merge area (the ring is free now): mm/ml [w][head], mo [w][head][D]
     float *mm = reinterpret_cast<float *>(ring);
     float *ml = mm + kConsumerWarps * 8;
+    float *mo = ml + kConsumerWarps * 8;
     if (warp < kConsumerWarps) {
         const int g = lane >> 2, q4 = lane & 3;
         if (lane < 4) {
@@ -362,20 +348,21 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(DecodeParams p) {
                 ml[warp * 8 + 2 * q4 + j] = l[j];
             }
         }
+        // accumulator rows g / g + 8 of block dt are channels 2g / 2g + 1
         float *mw = mo + warp * 8 * D;
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
-            mw[(2 * q4) * D + dt * 16 + g] = o[dt][0];
-            mw[(2 * q4 + 1) * D + dt * 16 + g] = o[dt][1];
-            mw[(2 * q4) * D + dt * 16 + g + 8] = o[dt][2];
-            mw[(2 * q4 + 1) * D + dt * 16 + g + 8] = o[dt][3];
+            mw[(2 * q4) * D + dt * 16 + 2 * g] = o[dt][0];
+            mw[(2 * q4 + 1) * D + dt * 16 + 2 * g] = o[dt][1];
+            mw[(2 * q4) * D + dt * 16 + 2 * g + 1] = o[dt][2];
+            mw[(2 * q4 + 1) * D + dt * 16 + 2 * g + 1] = o[dt][3];
         }
     }
     __syncthreads();
     if (p.cluster) {
         // ------------------------------------------- in-cluster LSE combine
         // this CTA's segment result: co[head][D] normalised, cl[head] base-2 LSE
-        float *co = ml + kConsumerWarps * 8;
+        float *co = mo + kConsumerWarps * 8 * D;
         float *cl = co + 8 * D;
         for (int idx = threadIdx.x; idx < nheads * D; idx += kThreads) {
             const int j = idx / D, d = idx - j * D;
