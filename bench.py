@@ -123,11 +123,10 @@ def decode_bytes(B, Hq, Hkv, D, ctx, max_blocks):
     kv = 2 * B * ctx * Hkv * D            # INT8 K and V pages
     scales = 2 * B * ctx * Hkv * 4        # fp32 per-token K and V scales
     table = B * max_blocks * 4 + B * 4    # block table + context lengths
-    q_bf16 = B * Hq * D * 2               # query in
-    q_codes = B * Hq * D + B * Hq * 4     # INT8 query + scale (written once, read once)
+    q_bf16 = B * Hq * D * 2               # query in (quantised inside the decode kernel)
     out = B * Hq * D * 2                  # bf16 output
-    kernel = kv + scales + table + q_codes
-    step = kv + scales + table + q_bf16 + 2 * q_codes + out
+    kernel = kv + scales + table + q_bf16 + out
+    step = kernel                         # the step is that one kernel
     return kernel, step
 
 
@@ -161,17 +160,16 @@ def run_ours(args):
     launches = {"n": 0}
 
     def step(ev=None):
-        qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
-        n = sage.last_launch_info()["launches"]
+        # one launch: per-token query quantisation, split-K paged decode and
+        # (up to 8 segments) the LSE combine all run in the decode kernel
         if ev is not None:
             ev[0].record(stream)
-        out = sage.sage_attn_decode_paged(qi.view(B, Hq, D), qs.view(B, Hq), cache.k_cache,
-                                          cache.v_cache, cache.k_scale, cache.v_scale,
-                                          cache.block_table, cache.lens, ctx, num_segments=S,
-                                          workspace=ws_step, out=out_step)
+        out = sage.sage_attn_decode_paged_q16(q, cache.k_cache, cache.v_cache, cache.k_scale,
+                                              cache.v_scale, cache.block_table, cache.lens, ctx,
+                                              num_segments=S, workspace=ws_step, out=out_step)
         if ev is not None:
             ev[1].record(stream)
-        launches["n"] = n + sage.last_launch_info()["launches"]
+        launches["n"] = sage.last_launch_info()["launches"]
         return out
 
     clk = ClockSampler(local).__enter__()   # samples from warm-up through the timed steps
@@ -242,11 +240,9 @@ def run_ours(args):
             q_dev.copy_(q_host, non_blocking=True)
             bt_dev.copy_(bt_host, non_blocking=True)
             lens_dev.copy_(lens_host, non_blocking=True)
-            qi, qs, _, _ = sage.sage_quant_int8(q_dev[:, :, None, :])
-            out = sage.sage_attn_decode_paged(qi.view(B, Hq, D), qs.view(B, Hq), cache.k_cache,
-                                              cache.v_cache, cache.k_scale, cache.v_scale,
-                                              bt_dev, lens_dev, ctx, num_segments=S,
-                                              workspace=ws_buf)
+            out = sage.sage_attn_decode_paged_q16(q_dev, cache.k_cache, cache.v_cache,
+                                                  cache.k_scale, cache.v_scale, bt_dev, lens_dev,
+                                                  ctx, num_segments=S, workspace=ws_buf)
             out_host.copy_(out, non_blocking=True)
 
         for _ in range(args.warmup):
@@ -291,8 +287,8 @@ def run_ours(args):
         "data": "synthetic (seeded; uniform INT8 cache, U(0.005,0.02) scales, N(0,1) bf16 query)",
         "config": {"workload": "paged_decode B8 Hq24 Hkv4 D256 ctx8192 block16",
                    "segments": S, "l2": "flushed between steps (read of a 512 MB buffer)",
-                   "step": "quant(Q) + split-K paged decode with in-cluster LSE combine"
-                           if 1 < S <= 8 else "quant(Q) + split-K paged decode + LSE combine",
+                   "step": "query quant + split-K paged decode + in-cluster LSE combine, one kernel"
+                           if 1 < S <= 8 else "query quant + split-K paged decode (one kernel) + LSE combine",
                    "launch": "CUDA graph replay per step",
                    "parallelism": "replicas" if ws > 1 else "single"},
         "roofline": roof, "e2e": e2e, "gpu_launches": launches["n"] * args.steps,

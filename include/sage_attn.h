@@ -133,7 +133,7 @@ typedef struct sage_decode_args {
     int max_context_len;        /* host-side bound on context_lens, <= 16 * max_blocks */
     float sm_scale;             /* <= 0 selects 1/sqrt(D) */
     int num_segments;           /* 0 selects sage_decode_num_segments() */
-    void *out;                  /* [B, Hq, D] */
+    void *out;                  /* [B, Hq, D], 8-byte aligned */
     sage_dtype_t out_dtype;
     float *lse;                 /* optional [B, Hq] natural-log LSE (-inf for empty context) */
 } sage_decode_args_t;
@@ -158,6 +158,17 @@ size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments);
  * contents are scratch and are overwritten. */
 sage_status_t sage_attn_decode_paged(const sage_decode_args_t *args, void *workspace,
                                      size_t workspace_bytes, void *stream);
+
+/* Same decode with the query quantisation fused in: q is the f16/bf16 query
+ * [B, Hq, D] (8-byte aligned); args->q and args->q_scale are ignored.  Each
+ * CTA quantises the query rows of its heads per (token, head) with the
+ * arithmetic of sage_quant_int8 ([P1] section 4: s = max|q| / 127, codes
+ * round(q / s)), so the codes and the result equal sage_quant_int8 followed
+ * by sage_attn_decode_paged bit for bit; the split-K segments recompute the
+ * same codes instead of reading them from a separate launch. */
+sage_status_t sage_attn_decode_paged_q16(const sage_decode_args_t *args, const void *q,
+                                         sage_dtype_t q_dtype, void *workspace,
+                                         size_t workspace_bytes, void *stream);
 
 /* Same decode, without the combine: writes each segment's normalised output
  * o_part [B*Hq, S, D] and natural-log LSE lse_part [B*Hq, S] (fp32, caller

@@ -90,6 +90,9 @@ def lib():
         L.sage_attn_decode_workspace_size.restype = ctypes.c_size_t
         L.sage_attn_decode_paged.argtypes = [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t, _vp]
         L.sage_attn_decode_paged.restype = _i
+        L.sage_attn_decode_paged_q16.argtypes = [ctypes.POINTER(DecodeArgs), _vp, _i, _vp,
+                                                 ctypes.c_size_t, _vp]
+        L.sage_attn_decode_paged_q16.restype = _i
         L.sage_attn_decode_paged_partials.argtypes = [ctypes.POINTER(DecodeArgs), _vp, _vp,
                                                       ctypes.POINTER(_i), _vp]
         L.sage_attn_decode_paged_partials.restype = _i
@@ -201,16 +204,17 @@ def decode_workspace_size(B: int, Hq: int, D: int, num_segments: int) -> int:
 
 
 def _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
-                 max_context_len, sm_scale, num_segments, out, lse):
-    _need(q_int8, torch.int8, "q_int8")
-    _need(q_scale, torch.float32, "q_scale")
+                 max_context_len, sm_scale, num_segments, out, lse, shape=None):
+    if shape is None:
+        _need(q_int8, torch.int8, "q_int8")
+        _need(q_scale, torch.float32, "q_scale")
     _need(k_cache, torch.int8, "k_cache")
     _need(v_cache, torch.int8, "v_cache")
     _need(k_scale, torch.float32, "k_scale")
     _need(v_scale, torch.float32, "v_scale")
     _need(block_table, torch.int32, "block_table")
     _need(context_lens, torch.int32, "context_lens")
-    B, Hq, D = q_int8.shape
+    B, Hq, D = q_int8.shape if shape is None else shape
     a = DecodeArgs()
     a.q, a.q_scale = _ptr(q_int8), _ptr(q_scale)
     a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
@@ -251,6 +255,34 @@ def sage_attn_decode_paged(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, 
     else:
         _check(lib().sage_attn_decode_paged(ctypes.byref(a), _ptr(workspace), ws_bytes,
                                             _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+def sage_attn_decode_paged_q16(q, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                               max_context_len: int, *, sm_scale=None, num_segments: int = 0,
+                               out_dtype=torch.bfloat16, return_lse: bool = False,
+                               workspace: Optional[torch.Tensor] = None,
+                               out: Optional[torch.Tensor] = None, stream=None):
+    """Paged decode with the per-token query quantisation fused into the kernel.
+
+    q [B,Hq,D] f16/bf16.  Same result as sage_quant_int8 + sage_attn_decode_paged.
+    """
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[1]
+    if q.dtype not in (torch.float16, torch.bfloat16) or not q.is_contiguous():
+        raise ValueError("q must be a contiguous f16/bf16 tensor")
+    if out is None:
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if return_lse else None
+    S = num_segments or decode_num_segments(B, Hq, Hkv, D, max_context_len)
+    need = decode_workspace_size(B, Hq, D, S)
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    a = _decode_args(None, None, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                     max_context_len, sm_scale, S, out, lse, shape=(B, Hq, D))
+    _check(lib().sage_attn_decode_paged_q16(ctypes.byref(a), _ptr(q), _dt(q.dtype), _ptr(workspace),
+                                            ws_bytes, _stream(stream)))
     return (out, lse) if return_lse else out
 
 

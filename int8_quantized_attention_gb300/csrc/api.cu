@@ -281,7 +281,8 @@ SAGE_API size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_se
 static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
                                 size_t workspace_bytes, int32_t *dbg, void *stream,
                                 float *partials_o = nullptr, float *partials_l = nullptr,
-                                int *segments_used = nullptr) {
+                                int *segments_used = nullptr, const void *q_fp = nullptr,
+                                int q_fp_bf16 = 0) {
     if (!a) return fail(SAGE_ERR_INVALID_ARG, "args is NULL");
     if (!head_dim_ok(a->D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", a->D);
     if (a->out_dtype != SAGE_F16 && a->out_dtype != SAGE_BF16)
@@ -297,8 +298,9 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
         return fail(SAGE_ERR_INVALID_ARG, "num_segments outside [0, 1024]");
     g_last = sage::LaunchLog();
     if (a->B == 0) return SAGE_OK;
-    if (!a->q || !a->q_scale || !a->context_lens || !a->out)
+    if ((!q_fp && (!a->q || !a->q_scale)) || !a->context_lens || !a->out)
         return fail(SAGE_ERR_INVALID_ARG, "q, q_scale, context_lens and out are required");
+    if (q_fp && !aligned(q_fp, 8)) return fail(SAGE_ERR_INVALID_ARG, "q must be 8-byte aligned");
     if (a->max_context_len > 0) {
         if (!a->k_cache || !a->v_cache || !a->k_scale || !a->v_scale || !a->block_table)
             return fail(SAGE_ERR_INVALID_ARG, "cache, scales and block_table are required");
@@ -307,7 +309,8 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
             !aligned(a->v_scale, 16))
             return fail(SAGE_ERR_INVALID_ARG, "caches and scales must be 16-byte aligned");
     }
-    if (!aligned(a->q, 4)) return fail(SAGE_ERR_INVALID_ARG, "q must be 4-byte aligned");
+    if (!q_fp && !aligned(a->q, 4)) return fail(SAGE_ERR_INVALID_ARG, "q must be 4-byte aligned");
+    if (!aligned(a->out, 8)) return fail(SAGE_ERR_INVALID_ARG, "out must be 8-byte aligned");
     int S = a->num_segments ? a->num_segments
                             : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->D,
                                                        a->max_context_len);
@@ -324,6 +327,7 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
     if (st != SAGE_OK) return st;
     sage::DecodeParams p = {};
     p.q = a->q, p.q_scale = a->q_scale;
+    p.q_fp = q_fp, p.q_fp_bf16 = q_fp_bf16;
     p.k_cache = a->k_cache, p.v_cache = a->v_cache, p.k_scale = a->k_scale, p.v_scale = a->v_scale;
     p.block_table = a->block_table, p.context_lens = a->context_lens;
     p.B = a->B, p.Hq = a->Hq, p.Hkv = a->Hkv, p.D = a->D, p.group = a->Hq / a->Hkv;
@@ -388,6 +392,16 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
 SAGE_API sage_status_t sage_attn_decode_paged(const sage_decode_args_t *args, void *workspace,
                                               size_t workspace_bytes, void *stream) {
     return run_decode(args, workspace, workspace_bytes, nullptr, stream);
+}
+
+SAGE_API sage_status_t sage_attn_decode_paged_q16(const sage_decode_args_t *args, const void *q,
+                                                  sage_dtype_t q_dtype, void *workspace,
+                                                  size_t workspace_bytes, void *stream) {
+    if (!q) return fail(SAGE_ERR_INVALID_ARG, "q is NULL");
+    if (q_dtype != SAGE_F16 && q_dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "q dtype must be f16 or bf16");
+    return run_decode(args, workspace, workspace_bytes, nullptr, stream, nullptr, nullptr, nullptr,
+                      q, q_dtype == SAGE_BF16);
 }
 
 SAGE_API sage_status_t sage_attn_decode_paged_partials(const sage_decode_args_t *args,

@@ -117,6 +117,17 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
     hi = *reinterpret_cast<uint32_t *>(&h);
 }
 
+// Symmetric INT8 code of v with scale s = fl32(amax / 127): one correctly
+// rounded fp32 division, round to nearest even, clamped to [-127, 127]; an
+// all-zero row (s == 0) gives code 0.  ("INT8 QK MMAC on gfx936 DCU",
+// section 4: q = round(x / s), s = max|x| / 127.)
+__device__ __forceinline__ int8_t quant_code(float v, float s) {
+    if (s == 0.0f) return 0;
+    int r = __float2int_rn(__fdiv_rn(v, s));
+    r = max(-127, min(127, r));
+    return static_cast<int8_t>(r);
+}
+
 // Same exact conversion, pairing bytes (0, 2) and (1, 3): for a register
 // holding two 16-bit elements of two rows (a transposed ldmatrix of int8 data),
 // `even` gets the low byte of each element and `odd` the high byte.

@@ -54,10 +54,13 @@ struct DecodeCfg {
     static constexpr int kRingBytes = kStages * kStageBytes;
     static constexpr int kOffBar = kRingBytes;
     // after the loop the ring holds the warp merge and the cluster combine
-    static_assert(kRingBytes >= (2 * kConsumerWarps * 8 + kConsumerWarps * 8 * D + 8 * D + 8) * 4,
+    static_assert(kRingBytes >= (3 * kConsumerWarps * 8 + kConsumerWarps * 8 * (D + 4) + 8 + 8 * D +
+                                 kDecodeMaxCluster * 8 + 8) * 4,
                   "merge area fits in the ring");
     static constexpr int kOffBt = kOffBar + kStages * 16 + 64;
-    static constexpr int kSmem = kOffBt + kMaxSegPages * 4;
+    static constexpr int kOffQ = kOffBt + kMaxSegPages * 4;     // int8 query codes [8][D]
+    static constexpr int kOffQs = kOffQ + 8 * D;               // their scales [8]
+    static constexpr int kSmem = kOffQs + 8 * 4;
     static constexpr int kCtasPerSm = 227 * 1024 / (kSmem + 1024);
     // Page i goes to stage i % kStages and to consumer warp i % kConsumerWarps.
     // Every stage must always be read by the same warp: mbarrier parity waits
@@ -123,6 +126,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
     uint64_t *empty = full + NST;
     int *stage_ok = reinterpret_cast<int *>(empty + NST);
     int *bt_s = reinterpret_cast<int *>(smem + Cfg::kOffBt);
+    int8_t *q_s = reinterpret_cast<int8_t *>(smem + Cfg::kOffQ);
+    float *qsc_s = reinterpret_cast<float *>(smem + Cfg::kOffQs);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seg = blockIdx.x;
@@ -203,8 +208,70 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
         const int g = lane >> 2, q4 = lane & 3;
         // B operand (Q^T): column n = head g of this tile, 4 bytes per k-quad.
         uint32_t qf[D / 32][2];
-        {
-            const bool hv = g < nheads;
+        float colscale[2];
+        const bool hv = g < nheads;
+        if (p.q_fp) {
+            // The query quantised here, per (token, head), with the same
+            // arithmetic as the quant kernel (bit-identical codes and scale).
+            // Warp w quantises heads 2w, 2w+1 (16 lanes per head, D/16
+            // channels per lane) into shared memory; the consumer warps then
+            // meet at a named barrier (the producer is already copying).
+            {
+                const int hh = 2 * warp + (lane >> 4);  // head of this half-warp
+                const int cpl = D / 16;                 // channels per lane
+                const int c0 = (lane & 15) * cpl;
+                float f[cpl];
+                if (hh < nheads) {
+                    const uint16_t *src = static_cast<const uint16_t *>(p.q_fp) +
+                                          ((int64_t)b * p.Hq + head0 + hh) * D + c0;
+#pragma unroll
+                    for (int e = 0; e < cpl; e += 4) {
+                        const uint2 u = *reinterpret_cast<const uint2 *>(src + e);
+                        const uint32_t w2[2] = {u.x, u.y};
+#pragma unroll
+                        for (int k = 0; k < 2; ++k) {
+                            float2 t;
+                            if (p.q_fp_bf16)
+                                t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w2[k]));
+                            else
+                                t = __half22float2(*reinterpret_cast<const __half2 *>(&w2[k]));
+                            f[e + 2 * k] = t.x;
+                            f[e + 2 * k + 1] = t.y;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < cpl; ++e) f[e] = 0.0f;
+                }
+                float amax = 0.0f;
+#pragma unroll
+                for (int e = 0; e < cpl; ++e) amax = fmaxf(amax, fabsf(f[e]));
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+                const float sq = __fdiv_rn(amax, 127.0f);
+                if (hh < 8) {
+#pragma unroll
+                    for (int e = 0; e < cpl; e += 4) {
+                        uint32_t w = 0;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            w |= (uint32_t)(uint8_t)quant_code(f[e + k], sq) << (8 * k);
+                        *reinterpret_cast<uint32_t *>(q_s + hh * D + c0 + e) = w;
+                    }
+                    if ((lane & 15) == 0) qsc_s[hh] = sq;
+                }
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+#pragma unroll
+            for (int ks = 0; ks < D / 32; ++ks) {
+                qf[ks][0] = hv ? *reinterpret_cast<const uint32_t *>(q_s + g * D + ks * 32 + 4 * q4) : 0u;
+                qf[ks][1] =
+                    hv ? *reinterpret_cast<const uint32_t *>(q_s + g * D + ks * 32 + 16 + 4 * q4) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                colscale[j] = 2 * q4 + j < nheads ? qsc_s[2 * q4 + j] * p.qk_scale_log2 : 0.0f;
+        } else {
             const int8_t *qrow = p.q + ((int64_t)b * p.Hq + head0 + (hv ? g : 0)) * D;
 #pragma unroll
             for (int ks = 0; ks < D / 32; ++ks) {
@@ -212,14 +279,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
                 qf[ks][1] =
                     hv ? *reinterpret_cast<const uint32_t *>(qrow + ks * 32 + 16 + 4 * q4) : 0u;
             }
-        }
-        // Column heads of the accumulator fragments: 2*q4 and 2*q4+1.
-        float colscale[2];
+            // Column heads of the accumulator fragments: 2*q4 and 2*q4+1.
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int hc = 2 * q4 + j;
-            colscale[j] = hc < nheads ? p.q_scale[(int64_t)b * p.Hq + head0 + hc] * p.qk_scale_log2
-                                      : 0.0f;
+            for (int j = 0; j < 2; ++j) {
+                const int hc = 2 * q4 + j;
+                colscale[j] = hc < nheads
+                                  ? p.q_scale[(int64_t)b * p.Hq + head0 + hc] * p.qk_scale_log2
+                                  : 0.0f;
+            }
         }
         // ldmatrix row address of this lane for the transposed V loads:
         // matrix (lane / 8) = (16-channel block 2*dp + lane/16, keys 0-7 or 8-15)
@@ -231,21 +298,25 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
             const uint8_t *stg = ring + s * Cfg::kStageBytes;
             const bool ok = stage_ok[s] != 0;
             const uint32_t stg_a = smem_u32(stg);
-            // ---- QK^T: rows = 16 keys of the page, cols = 8 heads; two
-            // independent accumulation chains (integer sums, exact)
-            int c[4] = {0, 0, 0, 0}, c2[4] = {0, 0, 0, 0};
+            // ---- QK^T: rows = 16 keys of the page, cols = 8 heads; up to
+            // four independent accumulation chains (integer sums, exact)
+            constexpr int KS = D / 32, NC = KS < 4 ? KS : 4;
+            int cc[NC][4];
 #pragma unroll
-            for (int ks = 0; ks < D / 32; ks += 2) {
+            for (int h = 0; h < NC; ++h) cc[h][0] = cc[h][1] = cc[h][2] = cc[h][3] = 0;
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks) {
                 uint32_t a[4];
                 ldsm_x4(stg_a + ks * 512 + lane * 16, a);
-                mma_s8(c, a, qf[ks][0], qf[ks][1]);
-                if (ks + 1 < D / 32) {
-                    ldsm_x4(stg_a + (ks + 1) * 512 + lane * 16, a);
-                    mma_s8(c2, a, qf[ks + 1][0], qf[ks + 1][1]);
-                }
+                mma_s8(cc[ks % NC], a, qf[ks][0], qf[ks][1]);
             }
+            int c[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) c[e] += c2[e];
+            for (int e = 0; e < 4; ++e) {
+                c[e] = cc[0][e];
+#pragma unroll
+                for (int h = 1; h < NC; ++h) c[e] += cc[h][e];
+            }
             const float *ksc = reinterpret_cast<const float *>(stg + 2 * Cfg::kSlab);
             const float *vsc = ksc + 16;
             const float sk0 = ksc[g], sk1 = ksc[g + 8];
@@ -335,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
     __syncthreads();  // ring and staging are free from here on
 
     // ------------------------------------------------------- warp merge
-    // merge area (the ring is free now): mm/ml [w][head], mo [w][head][D]
+    // merge area (the ring is free now): mm/ml [w][head], mo [w][head][D (+4)]
+    constexpr int kMoStride = D + 4;
     float *mm = reinterpret_cast<float *>(ring);
     float *ml = mm + kConsumerWarps * 8;
     float *mo = ml + kConsumerWarps * 8;
@@ -348,130 +420,143 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
                 ml[warp * 8 + 2 * q4 + j] = l[j];
             }
         }
-        // accumulator rows g / g + 8 of block dt are channels 2g / 2g + 1
-        float *mw = mo + warp * 8 * D;
+        // accumulator rows g / g + 8 of block dt are channels 2g / 2g + 1:
+        // (o0, o2) and (o1, o3) are channel pairs of heads 2q4 and 2q4 + 1.
+        // Rows of kMoStride = D + 4 floats keep these 8-byte stores at the
+        // minimum two wavefronts per warp.
+        float *mw = mo + warp * 8 * kMoStride;
 #pragma unroll
         for (int dt = 0; dt < D / 16; ++dt) {
-            mw[(2 * q4) * D + dt * 16 + 2 * g] = o[dt][0];
-            mw[(2 * q4 + 1) * D + dt * 16 + 2 * g] = o[dt][1];
-            mw[(2 * q4) * D + dt * 16 + 2 * g + 1] = o[dt][2];
-            mw[(2 * q4 + 1) * D + dt * 16 + 2 * g + 1] = o[dt][3];
+            *reinterpret_cast<float2 *>(mw + (2 * q4) * kMoStride + dt * 16 + 2 * g) =
+                make_float2(o[dt][0], o[dt][2]);
+            *reinterpret_cast<float2 *>(mw + (2 * q4 + 1) * kMoStride + dt * 16 + 2 * g) =
+                make_float2(o[dt][1], o[dt][3]);
         }
     }
     __syncthreads();
-    if (p.cluster) {
-        // ------------------------------------------- in-cluster LSE combine
-        // this CTA's segment result: co[head][D] normalised, cl[head] base-2 LSE
-        float *co = mo + kConsumerWarps * 8 * D;
-        float *cl = co + 8 * D;
-        for (int idx = threadIdx.x; idx < nheads * D; idx += kThreads) {
-            const int j = idx / D, d = idx - j * D;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + j]);
-            float val = 0.0f;
-            if (M != -INFINITY) {
-                float L = 0.0f, acc = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) {
-                    const float f = exp2f(mm[w * 8 + j] - M);
-                    L = fmaf(f, ml[w * 8 + j], L);
-                    acc = fmaf(f, mo[(w * 8 + j) * D + d], acc);
-                }
-                val = acc / L;
-            }
-            co[j * D + d] = val;
-        }
-        if (threadIdx.x < nheads) {
-            const int j = threadIdx.x;
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + j]);
-            float lse2 = -INFINITY;
-            if (M != -INFINITY) {
-                float L = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w)
-                    L = fmaf(exp2f(mm[w * 8 + j] - M), ml[w * 8 + j], L);
-                lse2 = M + log2f(L);
-            }
-            cl[j] = lse2;
-        }
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        const int S = p.num_segments;
-        for (int idx = seg * kThreads + threadIdx.x; idx < nheads * D; idx += S * kThreads) {
-            const int j = idx / D, d = idx - j * D;
-            float ls[kDecodeMaxCluster];
-            float M = -INFINITY;
-#pragma unroll
-            for (int r = 0; r < kDecodeMaxCluster; ++r) {
-                ls[r] = r < S ? cluster.map_shared_rank(cl, r)[j] : -INFINITY;
-                M = fmaxf(M, ls[r]);
-            }
-            float val = 0.0f, L = 0.0f;
-            if (M != -INFINITY) {
-                float acc = 0.0f;
-#pragma unroll
-                for (int r = 0; r < kDecodeMaxCluster; ++r) {
-                    if (r < S && ls[r] != -INFINITY) {
-                        const float w = exp2f(ls[r] - M);
-                        L += w;
-                        acc = fmaf(w, cluster.map_shared_rank(co, r)[j * D + d], acc);
-                    }
-                }
-                val = acc / L;
-            }
-            const int64_t row = (int64_t)b * p.Hq + head0 + j;
-            if (p.out_bf16)
-                reinterpret_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(val);
-            else
-                reinterpret_cast<__half *>(p.out)[row * D + d] = __float2half_rn(val);
-            if (d == 0 && p.lse)
-                p.lse[row] = M == -INFINITY ? -INFINITY : (M + log2f(L)) * 0.69314718055994530942f;
-        }
-        cluster.sync();  // every CTA's shared memory stays alive until all have read it
-        return;
-    }
-    const bool direct = p.num_segments == 1 && !p.force_partials;
-    for (int idx = threadIdx.x; idx < nheads * D; idx += kThreads) {
-        const int j = idx / D, d = idx - j * D;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + j]);
-        float val = 0.0f;
-        if (M != -INFINITY) {
-            float L = 0.0f, acc = 0.0f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = exp2f(mm[w * 8 + j] - M);
-                L = fmaf(f, ml[w * 8 + j], L);
-                acc = fmaf(f, mo[(w * 8 + j) * D + d], acc);
-            }
-            val = acc / L;
-        }
-        const int64_t row = (int64_t)b * p.Hq + head0 + j;
-        if (direct) {
-            if (p.out_bf16)
-                reinterpret_cast<__nv_bfloat16 *>(p.out)[row * D + d] = __float2bfloat16_rn(val);
-            else
-                reinterpret_cast<__half *>(p.out)[row * D + d] = __float2half_rn(val);
-        } else {
-            p.o_part[(row * p.num_segments + seg) * D + d] = val;
-        }
-    }
+    // per-head merge weights, once: fw[w][j] = 2^(m_wj - M_j) / L_j and the
+    // segment's base-2 LSE hl[j] = M_j + log2 L_j (-inf with no visible key)
+    float *fw = mo + kConsumerWarps * 8 * kMoStride;
+    float *hl = fw + kConsumerWarps * 8;
     if (threadIdx.x < nheads) {
         const int j = threadIdx.x;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mm[w * 8 + j]);
-        float lse = -INFINITY;
-        if (M != -INFINITY) {
-            float L = 0.0f;
+        if (M == -INFINITY) {
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) L = fmaf(exp2f(mm[w * 8 + j] - M), ml[w * 8 + j], L);
-            lse = (M + log2f(L)) * 0.69314718055994530942f;
+            for (int w = 0; w < kConsumerWarps; ++w) fw[w * 8 + j] = 0.0f;
+            hl[j] = -INFINITY;
+        } else {
+            float f[kConsumerWarps], L = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                f[w] = fast_exp2(mm[w * 8 + j] - M);
+                L = fmaf(f[w], ml[w * 8 + j], L);
+            }
+            const float inv = 1.0f / L;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) fw[w * 8 + j] = f[w] * inv;
+            hl[j] = M + log2f(L);
         }
+    }
+    __syncthreads();
+    // the segment's normalised output, 4 channels per thread
+    auto seg_out = [&](int j, int d) {
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float f = fw[w * 8 + j];
+            const float4 v = *reinterpret_cast<const float4 *>(mo + (w * 8 + j) * kMoStride + d);
+            acc.x = fmaf(f, v.x, acc.x);
+            acc.y = fmaf(f, v.y, acc.y);
+            acc.z = fmaf(f, v.z, acc.z);
+            acc.w = fmaf(f, v.w, acc.w);
+        }
+        return acc;
+    };
+    auto store_out = [&](int64_t row, int d, float4 v) {
+        if (p.out_bf16) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+            uint2 u = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            *reinterpret_cast<uint2 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + row * D + d) = u;
+        } else {
+            __half2 lo = __floats2half2_rn(v.x, v.y), hi = __floats2half2_rn(v.z, v.w);
+            uint2 u = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+            *reinterpret_cast<uint2 *>(reinterpret_cast<__half *>(p.out) + row * D + d) = u;
+        }
+    };
+    constexpr float kLn2 = 0.69314718055994530942f;
+    if (p.cluster) {
+        // ------------------------------------------- in-cluster LSE combine
+        // this CTA's segment result co[head][D]; its base-2 LSE is hl[head]
+        float *co = hl + 8;
+        float *cw = co + 8 * D;                  // [rank][head] combine weights
+        float *gl = cw + kDecodeMaxCluster * 8;  // [head] combined base-2 LSE
+        for (int idx = 4 * threadIdx.x; idx < nheads * D; idx += 4 * kThreads) {
+            const int j = idx / D, d = idx - j * D;
+            *reinterpret_cast<float4 *>(co + j * D + d) = seg_out(j, d);
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        const int S = p.num_segments;
+        if (threadIdx.x < nheads) {
+            const int j = threadIdx.x;
+            float ls[kDecodeMaxCluster];
+            float M = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < kDecodeMaxCluster; ++r) {
+                ls[r] = r < S ? cluster.map_shared_rank(hl, r)[j] : -INFINITY;
+                M = fmaxf(M, ls[r]);
+            }
+            float L = 0.0f;
+            float f[kDecodeMaxCluster];
+#pragma unroll
+            for (int r = 0; r < kDecodeMaxCluster; ++r) {
+                f[r] = (M != -INFINITY && ls[r] != -INFINITY) ? fast_exp2(ls[r] - M) : 0.0f;
+                L += f[r];
+            }
+            const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+#pragma unroll
+            for (int r = 0; r < kDecodeMaxCluster; ++r) cw[r * 8 + j] = f[r] * inv;
+            gl[j] = M == -INFINITY ? -INFINITY : M + log2f(L);
+        }
+        __syncthreads();
+        // this CTA reduces a slice of the outputs, 4 channels per thread
+        for (int idx = 4 * (seg * kThreads + threadIdx.x); idx < nheads * D; idx += 4 * S * kThreads) {
+            const int j = idx / D, d = idx - j * D;
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int r = 0; r < kDecodeMaxCluster; ++r) {
+                if (r < S) {
+                    const float w = cw[r * 8 + j];
+                    const float4 v = *reinterpret_cast<const float4 *>(cluster.map_shared_rank(co, r) + j * D + d);
+                    acc.x = fmaf(w, v.x, acc.x);
+                    acc.y = fmaf(w, v.y, acc.y);
+                    acc.z = fmaf(w, v.z, acc.z);
+                    acc.w = fmaf(w, v.w, acc.w);
+                }
+            }
+            const int64_t row = (int64_t)b * p.Hq + head0 + j;
+            store_out(row, d, acc);
+            if (d == 0 && p.lse) p.lse[row] = gl[j] * kLn2;
+        }
+        cluster.sync();  // every CTA's shared memory stays alive until all have read it
+        return;
+    }
+    const bool direct = p.num_segments == 1 && !p.force_partials;
+    for (int idx = 4 * threadIdx.x; idx < nheads * D; idx += 4 * kThreads) {
+        const int j = idx / D, d = idx - j * D;
+        const float4 v = seg_out(j, d);
+        const int64_t row = (int64_t)b * p.Hq + head0 + j;
+        if (direct)
+            store_out(row, d, v);
+        else
+            *reinterpret_cast<float4 *>(p.o_part + (row * p.num_segments + seg) * D + d) = v;
+    }
+    if (threadIdx.x < nheads) {
+        const int j = threadIdx.x;
+        const float lse = hl[j] * kLn2;  // -inf * ln2 stays -inf
         const int64_t row = (int64_t)b * p.Hq + head0 + j;
         if (direct) {
             if (p.lse) p.lse[row] = lse;

@@ -58,6 +58,8 @@ cudaError_t launch_combine(const CombineParams &p, cudaStream_t st, LaunchLog &l
 struct DecodeParams {
     const int8_t *q;
     const float *q_scale;
+    const void *q_fp;         // optional [B, Hq, D] f16/bf16 query quantised in the kernel
+    int q_fp_bf16;
     const int8_t *k_cache, *v_cache;
     const float *k_scale, *v_scale;
     const int32_t *block_table, *context_lens;

@@ -29,12 +29,7 @@ __device__ __forceinline__ void load8(const T *p, float (&v)[8]) {
     for (int i = 0; i < 8; ++i) v[i] = DT<T>::to_f(e[i]);
 }
 
-__device__ __forceinline__ int8_t quant1(float v, float s) {
-    if (s == 0.0f) return 0;
-    int r = __float2int_rn(__fdiv_rn(v, s));
-    r = max(-127, min(127, r));
-    return static_cast<int8_t>(r);
-}
+__device__ __forceinline__ int8_t quant1(float v, float s) { return quant_code(v, s); }
 
 __device__ __forceinline__ void store8_i8(int8_t *dst, const float (&v)[8], float s) {
     uint32_t w0 = 0, w1 = 0;

@@ -64,6 +64,8 @@ def test_rejects_bad_arguments_on_host(lib):
     assert lib.sage_attn_decode_paged(ctypes.byref(a), None, 0, None) == binding.SAGE_ERR_INVALID_ARG
     a.Hkv, a.D = 2, 96
     assert lib.sage_attn_decode_paged(ctypes.byref(a), None, 0, None) == binding.SAGE_ERR_UNSUPPORTED
+    assert lib.sage_attn_decode_paged_q16(ctypes.byref(a), None, binding.SAGE_BF16, None, 0,
+                                          None) == binding.SAGE_ERR_INVALID_ARG
     p = binding.PrefillArgs()
     p.B, p.Hq, p.Hkv, p.Sq, p.Sk, p.D = 1, 2, 2, 8, 8, 64
     p.q_block, p.k_block = 100, 1

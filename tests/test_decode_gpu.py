@@ -236,3 +236,26 @@ def test_decode_partials_then_combine(sage):
                            sm_scale=1 / 16)
     assert_close(np_(op)[1, :6, seg], o1, "segment partial")
     assert_close(np_(lp)[1, :6, seg], l1, "segment lse")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("Hq,Hkv", [(24, 4), (4, 4), (16, 2)])
+@pytest.mark.parametrize("segments", [1, 3, 12])
+@pytest.mark.parametrize("qdt", [torch.bfloat16, torch.float16])
+def test_decode_fused_query_quant_bitwise(sage, D, Hq, Hkv, segments, qdt):
+    """Quantising the query inside the decode kernel gives the same codes and
+    scales as sage_quant_int8, hence bit-identical outputs and LSE."""
+    B = 3
+    lens = [37, 300, 129]
+    c = W.paged_cache(B, Hkv, D, lens, seed=D + Hq + 7, device="cuda", extra_blocks=5)
+    q = W.decode_query(B, Hq, D, seed=Hq + 3, device="cuda").to(qdt).contiguous()
+    qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
+    ref, lref = _run(sage, qi.view(B, Hq, D), qs.view(B, Hq), c, max(lens), num_segments=segments,
+                     return_lse=True, out_dtype=torch.float16)
+    out, lse = sage.sage_attn_decode_paged_q16(q, c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                               c.block_table, c.lens, max(lens),
+                                               num_segments=segments, return_lse=True,
+                                               out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert torch.equal(out, ref) and torch.equal(lse, lref)
