@@ -478,6 +478,126 @@ def run_profile(args):
     return None
 
 
+def run_configs(args):
+    """Every configuration of the workload table, one JSON line each: GPU time
+    (CUDA events, L2 flushed before each timed call), throughput, fraction of
+    the measured peak, and the CPU oracle's time on the host cores (full for
+    the small configurations, a row/pair sample scaled by work otherwise)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    from int8_quantized_attention_gb300 import binding as sage
+    from int8_quantized_attention_gb300 import workloads as W
+
+    sage.lib()
+    peaks, kind = _peaks()
+    flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    threads = oracle.default_threads()
+
+    def gpu_ms(fn, reps=20):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            l2_flush(flush)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        ts.sort()
+        return statistics.median(ts)
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    # ---- prefill configurations
+    for name in ("tiny_prefill", "chunked_prefill", "dense_prefill"):
+        P = W.WORKLOADS[name].params
+        Sq = P["S"]
+        prefix_len = P.get("prefix", 0)
+        qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], Sq, Sq, P["D"], seed=P["seed"],
+                          dtype=P["dtype"], device="cuda", k_offset_std=P.get("k_offset_std", 0.0))
+        prefix, pc = None, None
+        if prefix_len:
+            pc = W.paged_cache(P["B"], P["Hkv"], P["D"], [prefix_len], seed=P["seed"], device="cuda")
+            prefix = dict(k_cache=pc.k_cache, v_cache=pc.v_cache, k_scale=pc.k_scale,
+                          v_scale=pc.v_scale, block_table=pc.block_table, lens=pc.lens,
+                          max_len=prefix_len)
+        qb, kb = P["q_block"], P["k_block"]
+        ki, ks, mu, _ = sage.sage_quant_int8(qkv.k, block_tokens=kb, smooth=P["smooth_k"])
+        qi, qs, _, bias = sage.sage_quant_int8(qkv.q, block_tokens=qb,
+                                               mu_in=mu if P["smooth_k"] else None)
+        sm = 1.0 / 8.0 if name == "tiny_prefill" else None
+        ws = torch.empty(1, dtype=torch.uint8, device="cuda")
+        out = sage.sage_attn_prefill(qi, qs, qb, ki, ks, kb, qkv.v, causal=P["causal"],
+                                     q_bias=bias, prefix=prefix, sm_scale=sm)
+        fn = lambda: sage.sage_attn_prefill(qi, qs, qb, ki, ks, kb, qkv.v, causal=P["causal"],
+                                            q_bias=bias, prefix=prefix, sm_scale=sm)
+        ms = gpu_ms(fn)
+        flop = prefill_flops(P["B"], P["Hq"], Sq, prefix_len, Sq, P["D"], P["causal"])
+        tf = flop / (ms * 1e-3) / 1e12
+        # oracle: one (batch, head) on a row sample, scaled by visible pairs
+        rows = np.arange(Sq) if Sq <= 128 else np.linspace(0, Sq - 1, 16).astype(np.int64)
+        sub = lambda t: t[0:1, 0:1].cpu().numpy()
+        pre = None
+        if pc is not None:
+            pre = dict(k_cache=pc.k_cache.cpu().numpy(), v_cache=pc.v_cache.cpu().numpy(),
+                       k_scale=pc.k_scale.cpu().numpy(), v_scale=pc.v_scale.cpu().numpy(),
+                       block_table=pc.block_table.cpu().numpy(), lens=pc.lens.cpu().numpy())
+        t0 = time.perf_counter()
+        oracle.prefill(sub(qi), sub(qs), qb, sub(ki), sub(ks), kb, sub(qkv.v.float()),
+                       causal=P["causal"], sm_scale=sm,
+                       q_bias=None if bias is None else sub(bias).astype(np.float64),
+                       prefix=pre, rows=rows, threads=threads)
+        t_or = time.perf_counter() - t0
+        off = prefix_len + Sq - Sq
+        vis = lambda i: (min(prefix_len + Sq, i + off + 1) if P["causal"] else prefix_len + Sq)
+        pairs_s = sum(vis(int(i)) for i in rows)
+        scale = flop / (4 * P["D"]) / pairs_s
+        emit({"config": name, "gpu_ms": round(ms, 4), "tflops": round(tf, 1),
+              "frac_of_measured_f16_peak": round(tf / peaks["bf16_tflops"], 4),
+              "oracle_s": round(t_or * scale, 2), "oracle_cores": threads,
+              "oracle_sample": "full" if scale == 1 else "1 (batch, head), %d rows, scaled x%.0f" % (len(rows), scale)})
+        del qkv, qi, ki, out
+
+    # ---- decode configurations
+    P = W.WORKLOADS["paged_decode"].params
+    shapes = [("paged_decode", P["B"], P["ctx"])]
+    SW = W.WORKLOADS["decode_sweep"].params
+    shapes += [("decode_sweep", b, c) for c in SW["ctx"] for b in SW["batch"]]
+    for name, B, ctx in shapes:
+        Hq, Hkv, D = P["Hq"], P["Hkv"], P["D"]
+        cache = W.paged_cache(B, Hkv, D, [ctx] * B, seed=P["seed"], device="cuda")
+        q = W.decode_query(B, Hq, D, seed=P["seed"], device="cuda")
+        S = sage.decode_num_segments(B, Hq, Hkv, D, ctx)
+        ws = torch.empty(max(1, sage.decode_workspace_size(B, Hq, D, S)), dtype=torch.uint8,
+                         device="cuda")
+        fn = lambda: sage.sage_attn_decode_paged_q16(q, cache.k_cache, cache.v_cache,
+                                                     cache.k_scale, cache.v_scale,
+                                                     cache.block_table, cache.lens, ctx,
+                                                     num_segments=S, workspace=ws)
+        ms = gpu_ms(fn)
+        kbytes, _ = decode_bytes(B, Hq, Hkv, D, ctx, cache.block_table.shape[1])
+        gbs = kbytes / (ms * 1e-3) / 1e9
+        # oracle: one (sequence, kv head) pair, scaled by the pair count
+        cc = [cache.k_cache.cpu().numpy(), cache.v_cache.cpu().numpy(), cache.k_scale.cpu().numpy(),
+              cache.v_scale.cpu().numpy(), cache.block_table.cpu().numpy(), cache.lens.cpu().numpy()]
+        qq = q.float().cpu().numpy()
+        t0 = time.perf_counter()
+        qi, qs, _ = oracle.quant_int8(qq[:, :, None, :])
+        oracle.decode_paged(qi[:, :, 0], qs[:, :, 0], *cc, threads=threads, pairs=[(0, 0)])
+        t_or = (time.perf_counter() - t0) * B * Hkv
+        emit({"config": name, "B": B, "ctx": ctx, "segments": S, "gpu_ms": round(ms, 4),
+              "GBps": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+              "oracle_s": round(t_or, 3), "oracle_cores": threads,
+              "oracle_sample": "1 of %d (sequence, kv head) pairs, scaled" % (B * Hkv)})
+        del cache
+
+
 def run_reference(args):
     ws, rank, _ = _dist()
     if rank != 0:
@@ -538,9 +658,14 @@ def main():
     ap.add_argument("--profile", default=None,
                     choices=["paged_decode", "dense_prefill", "chunked_prefill"])
     ap.add_argument("--heads", type=int, default=0)
+    ap.add_argument("--configs", action="store_true",
+                    help="time every configuration of the workload table (one JSON line each)")
     args = ap.parse_args()
     if args.profile:
         run_profile(args)
+        return
+    if args.configs:
+        run_configs(args)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -142,7 +142,7 @@ typedef struct sage_decode_args {
  * U = B * Hkv * ceil(Hq/Hkv/8) (sequence, KV head, 8-head tile) units and
  * P = ceil(max_context_len/16) pages it aims at about 1.7 CTAs per SM when
  * U * P / SMs < 400 pages, else about 5 per SM (S = target / U rounded, at
- * least 4 pages per segment, at most 64 segments); 8 (in-cluster combine) is
+ * least 16 pages per segment, at most 64 segments); 8 (in-cluster combine) is
  * preferred over a larger count that it reaches to within 3/4.  The rule is
  * empirical, measured on GB300. */
 int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len);

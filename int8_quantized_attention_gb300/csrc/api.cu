@@ -243,8 +243,9 @@ SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_con
     const int64_t units = (int64_t)B * Hkv * ((group + 7) / 8);
     const int64_t sms = sm_count();
     const int pages = (max_context_len + 15) / 16;
-    // at least 4 pages per segment (one per consumer warp), at most 64 segments
-    int64_t smax = pages / 4 > 1 ? pages / 4 : 1;
+    // at least 16 pages per segment (shorter ones cost more in start-up and
+    // combine than they gain in parallelism, measured), at most 64 segments
+    int64_t smax = pages / 16 > 1 ? pages / 16 : 1;
     if (smax > 64) smax = 64;
     // Measured on GB300 (D = 256, 3 CTAs per SM): with little work per SM
     // (under ~400 pages) about 1.7 CTAs per SM is fastest (longer segments

@@ -38,15 +38,23 @@ __global__ void __launch_bounds__(32 * kRowsPerCta) combine_kernel(CombineParams
         sum = warp_sum(sum);
         L = M + logf(sum);
         const float *op = p.o_part + r * (int64_t)p.S * D + lane * V;
-        for (int s = 0; s < p.S; ++s) {
-            const float l = lp[s];
-            if (l == -INFINITY) continue;
-            const float w = expf(l - L);
+        // 32 segments at a time: lane k computes segment k's weight once, the
+        // weights are broadcast by shuffle and the partial loads of the 32
+        // segments are independent (no serial L2 round trip per segment)
+        for (int s0 = 0; s0 < p.S; s0 += 32) {
+            const int sl = s0 + lane;
+            const float l = sl < p.S ? lp[sl] : -INFINITY;
+            const float wl = l == -INFINITY ? 0.0f : expf(l - L);
+            const int n = min(32, p.S - s0);
+#pragma unroll 8
+            for (int k = 0; k < n; ++k) {
+                const float w = __shfl_sync(0xffffffffu, wl, k);
 #pragma unroll
-            for (int i = 0; i < V; i += 2) {
-                const float2 o2 = *reinterpret_cast<const float2 *>(op + (int64_t)s * D + i);
-                acc[i] = fmaf(w, o2.x, acc[i]);
-                acc[i + 1] = fmaf(w, o2.y, acc[i + 1]);
+                for (int i = 0; i < V; i += 2) {
+                    const float2 o2 = *reinterpret_cast<const float2 *>(op + (int64_t)(s0 + k) * D + i);
+                    acc[i] = fmaf(w, o2.x, acc[i]);
+                    acc[i + 1] = fmaf(w, o2.y, acc[i + 1]);
+                }
             }
         }
     }
