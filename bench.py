@@ -337,7 +337,7 @@ def cpu_baseline_decode(seconds: float):
         oracle.decode_paged(qi, qs, *args, threads=threads)
         passes += 1
         el = time.perf_counter() - t0
-        if el >= seconds or passes >= 50:
+        if el >= seconds or passes >= 1000:
             break
     return {"value": round(sbytes * passes / el / 1e9, 4), "unit": "GB/s", "cores": threads,
             "kind": "oracle",
@@ -451,10 +451,8 @@ def run_profile(args):
         c = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["ctx"]] * P["B"], seed=P["seed"],
                           device="cuda")
         q = W.decode_query(P["B"], P["Hq"], P["D"], seed=P["seed"], device="cuda")
-        qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
-        run = lambda: sage.sage_attn_decode_paged(qi[:, :, 0].contiguous(), qs[:, :, 0].contiguous(),
-                                                  c.k_cache, c.v_cache, c.k_scale, c.v_scale,
-                                                  c.block_table, c.lens, P["ctx"])
+        run = lambda: sage.sage_attn_decode_paged_q16(q, c.k_cache, c.v_cache, c.k_scale,
+                                                      c.v_scale, c.block_table, c.lens, P["ctx"])
     else:
         qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
                           dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
