@@ -514,7 +514,6 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
     p.k_ws = reinterpret_cast<__half *>(w + L.off_k);
     p.v_ws = L.Vrows ? reinterpret_cast<__half *>(w + L.off_v) : nullptr;
     p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);
-    p.vsc_ws = reinterpret_cast<float *>(w + L.off_vsc);
     cudaStream_t cst = static_cast<cudaStream_t>(stream);
     sage::LaunchLog stage_log;
     cudaError_t e = sage::launch_prefill_stage(p, cst, stage_log);

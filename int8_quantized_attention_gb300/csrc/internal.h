@@ -119,14 +119,13 @@ struct PrefillParams {
     int Lpad;                 // Ppad + Sk rounded up to BN
     int Vrows;                // rows of v_ws: Lpad for bf16 V, else Ppad (f16 chunk V read in place)
     __half *k_ws;             // [B*Hkv][Lpad][D] exact f16 key codes
-    __half *v_ws;             // [B*Hkv][Vrows][D] f16 prefix value codes (+ bf16 chunk V as f16)
+    __half *v_ws;             // [B*Hkv][Vrows][D] f16 prefix values (code * v_scale; + bf16 chunk V)
     float *ksc_ws;            // [B*Hkv][Lpad] per-key K scale (0 on padding rows)
-    float *vsc_ws;            // [B*Hkv][Ppad] per-key V scale of the prefix
 };
 
 struct PrefillLayout {
     int BN, Ppad, Lpad, Vrows;
-    size_t off_k, off_v, off_ksc, off_vsc, bytes;
+    size_t off_k, off_v, off_ksc, bytes;
 };
 
 PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16);

@@ -58,26 +58,41 @@ struct PCfg {
     static constexpr int NQ = D == 256 ? 1 : 2;  // 128-row query tiles per CTA
     static constexpr int NS = D == 256 ? 2 : 1;  // S buffers per query tile
     static constexpr int NPH = BN / 64;          // P handed to the MMA in 64-key parts
+    // softmax warpgroups per query tile: at D = 256 two, each taking half of
+    // a row's 64 columns (one warpgroup alone is the critical path there)
+    static constexpr int SPLIT = D == 256 ? 2 : 1;
+    static constexpr int CW = BN / SPLIT;        // S columns per softmax thread
+    static constexpr int NSW = NQ * SPLIT;       // softmax warpgroups
     // softmax warpgroups + one warpgroup holding the producer and MMA warps
     // (and two idle warps, so that register reallocation works per warpgroup)
-    static constexpr int THREADS = NQ * 128 + 128;
+    static constexpr int THREADS = NSW * 128 + 128;
     // registers: 2 x 128 x 208 + 128 x 88 = 384 x 168, the launch budget
     static constexpr int REG_SOFTMAX = 208, REG_OTHER = 88;
-    static_assert(NQ == 1 || NQ * 128 * REG_SOFTMAX + 128 * REG_OTHER <= THREADS * 168,
+    static_assert(NSW == 1 || NSW * 128 * REG_SOFTMAX + 128 * REG_OTHER <= THREADS * 168,
                   "register split exceeds the launch budget");
-    static constexpr int QB = 128 * D * 2;     // f16 Q tile, swizzled
+    static_assert(SPLIT == 1 || NPH == 1, "split rows hand P over as one part");
+    // Q as the A operand of QK^T: in TMEM when it fits beside O and S
+    // (one query tile at D = 256: O 256 + S 2x64 + Q 128 columns), which
+    // also frees the shared memory of a Q tile for a third ring stage;
+    // otherwise in shared memory (two query tiles fill TMEM with O and S)
+    static constexpr bool QT = NQ * D + NQ * NS * BN + NQ * D / 2 <= 512;
+    static constexpr int QB = QT ? 0 : 128 * D * 2;     // f16 Q tile, swizzled
     static constexpr int KB = BN * D * 2;      // f16 K (or V) tile, swizzled
-    // stage: K tile | V tile | per-key K scales | per-key V scales (prefix)
-    static constexpr int SB = (2 * KB + 2 * BN * 4 + 1023) / 1024 * 1024;
+    // stage: K tile | V tile | per-key K scales
+    static constexpr int SB = (2 * KB + BN * 4 + 1023) / 1024 * 1024;
     static constexpr int OFF_ST = NQ * QB;
     static constexpr int NST_FIT = (kSmemLimit - 1024 - OFF_ST - 512) / SB;
     static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
     static constexpr int OFF_BAR = OFF_ST + NST * SB;
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
-    static constexpr int SMEM = OFF_MISC + 64 + 1024;
+    // split rows: partial row max / sum of each half, double-buffered
+    static constexpr int OFF_RED = OFF_MISC + 64;
+    static constexpr int SMEM = OFF_RED + (SPLIT > 1 ? 2 * NSW * 128 * 4 : 0) + 1024;
     static constexpr uint32_t COL_S = NQ * D;
+    static constexpr uint32_t COL_Q = NQ * D + NQ * NS * BN;  // when QT
     static_assert(NST >= 2, "the key ring needs two stages");
-    static_assert(NQ * D + NQ * NS * BN <= 512, "tensor memory holds 512 columns");
+    static_assert(NQ * D + NQ * NS * BN + (QT ? NQ * D / 2 : 0) <= 512,
+                  "tensor memory holds 512 columns");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
 };
 
@@ -89,7 +104,6 @@ enum {
     B_V_EMPTY = 12,   // [NST] MMA: every P.V reading the V stage retired
     B_S_FULL = 16,    // [NQ*NS] MMA: S = Q K^T done
     B_P_FULL = 20,    // [NQ*NS*NPH] softmax: a 64-key part of P in TMEM (O rescaled)
-    B_O_DONE = 24,    // [NQ] MMA: O_t += P_t V done
     B_O_FINAL = 26,   // [NQ] MMA: the last O_t += P_t V done (one phase)
     B_Q_READY = 28,   // softmax: Q in shared memory
     B_DRAIN = 29      // MMA: every issued MMA retired
@@ -196,7 +210,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                    const __grid_constant__ PrefillMaps maps) {
     using C = PCfg<D>;
     constexpr int BN = C::BN, NQ = C::NQ, NS = C::NS, NST = C::NST;
-    constexpr int kProducer = NQ * 4, kMma = NQ * 4 + 1;
+    constexpr int kProducer = C::NSW * 4, kMma = C::NSW * 4 + 1;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -242,12 +256,11 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             mbar_init(bar(B_V_EMPTY + s), 1);
         }
         for (int s = 0; s < NQ * NS; ++s) mbar_init(bar(B_S_FULL + s), 1);
-        for (int s = 0; s < NQ * NS * C::NPH; ++s) mbar_init(bar(B_P_FULL + s), 128);
+        for (int s = 0; s < NQ * NS * C::NPH; ++s) mbar_init(bar(B_P_FULL + s), 128 * C::SPLIT);
         for (int t = 0; t < NQ; ++t) {
-            mbar_init(bar(B_O_DONE + t), 1);
             mbar_init(bar(B_O_FINAL + t), 1);
         }
-        mbar_init(bar(B_Q_READY), NQ * 128);
+        mbar_init(bar(B_Q_READY), C::NSW * 128);
         mbar_init(bar(B_DRAIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -261,7 +274,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     tc::fence_after();
     const uint32_t tmem = *tmem_slot;
     if (warp >= kProducer) {
-        if constexpr (NQ == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
+        if constexpr (C::NSW == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
     if (warp == kProducer) {
         // ============================================================ producer
         if (lane == 0 && T > 0) {
@@ -298,7 +311,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 const bool pre = jj < n_pre;
                 const int w = pre ? jj : wpre + (jj - n_pre);
                 const uint32_t st = sm_a + C::OFF_ST + s * C::SB;
-                mbar_arrive_expect_tx(bar(B_V_FULL + s), C::KB + BN * 4 * (pre ? 2 : 1));
+                mbar_arrive_expect_tx(bar(B_V_FULL + s), C::KB + BN * 4);
                 const CUtensorMap *vm = pre ? &maps.v_pre : &maps.v_ch;
                 const int vrow = pre ? w * BN : (w - wpre) * BN + vch_off;
 #pragma unroll
@@ -307,9 +320,6 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                                     bar(B_V_FULL + s));
                 bulk_g2s(st + 2 * C::KB, p.ksc_ws + (int64_t)bh * p.Lpad + w * BN, BN * 4,
                          bar(B_V_FULL + s));
-                if (pre)
-                    bulk_g2s(st + 2 * C::KB + BN * 4, p.vsc_ws + (int64_t)bh * p.Ppad + w * BN,
-                             BN * 4, bar(B_V_FULL + s));
                 ++issued;
             }
             for (int jj = max(0, issued - NST); jj < issued; ++jj)
@@ -330,11 +340,21 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 const uint64_t qd = qd0 + (uint64_t)((t * C::QB) >> 4);
                 const uint64_t kd = kd0 + (uint64_t)(((jj % NST) * C::SB) >> 4);
                 const uint32_t d = tmem + C::COL_S + slot * BN;
-                tc::mma_ss(d, qd, kd, idq, 0u);
+                if constexpr (C::QT) {
+                    // A = Q from TMEM: column c of lane r holds f16 channels 2c, 2c+1
+                    const uint32_t qa = tmem + C::COL_Q + t * (D / 2);
+                    tc::mma_ts(d, qa, kd, idq, 0u);
 #pragma unroll
-                for (int ks = 1; ks < D / 16; ++ks)
-                    tc::mma_ss_acc(d, qd + (((ks >> 2) * (128 * 128) + (ks & 3) * 32) >> 4),
-                                   kd + (((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4), idq);
+                    for (int ks = 1; ks < D / 16; ++ks)
+                        tc::mma_ts_acc(d, qa + ks * 8,
+                                       kd + (((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4), idq);
+                } else {
+                    tc::mma_ss(d, qd, kd, idq, 0u);
+#pragma unroll
+                    for (int ks = 1; ks < D / 16; ++ks)
+                        tc::mma_ss_acc(d, qd + (((ks >> 2) * (128 * 128) + (ks & 3) * 32) >> 4),
+                                       kd + (((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4), idq);
+                }
                 tc::commit(bar(B_S_FULL + slot));
             };
             // O_t += P_t V_j in 64-key parts, each issued as soon as the
@@ -361,7 +381,6 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                             tc::mma_ts_acc(o, pt + kk * 8, vd + ((kk * 2048) >> 4), idp);
                     }
                 }
-                tc::commit(bar(B_O_DONE + t));
                 if (jj == T - 1) tc::commit(bar(B_O_FINAL + t));
                 return true;
             };
@@ -407,25 +426,65 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         __syncwarp();
     }
     } else {
-        if constexpr (NQ == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
+        if constexpr (C::NSW == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
         // ============================================================ softmax
-        const int t = warp >> 2;               // query tile of this warpgroup
+        constexpr int SPLIT = C::SPLIT, CW = C::CW;
+        const int wg = warp >> 2;              // softmax warpgroup
+        const int t = wg / SPLIT;              // query tile of this warpgroup
+        const int hc = wg % SPLIT;             // which part of the row's columns
+        const int c0 = hc * CW;                // first S column of this thread
         const int r = threadIdx.x & 127;       // row within the tile = TMEM lane
         const int i_first = i0 + t * 128;
         const int i = i_first + r;
         const bool row_ok = i < p.Sq;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
-        {
-            // Q row int8 -> f16 in the swizzled K-major layout of the A operand
-            const int8_t *qrow = p.q + (((int64_t)b * p.Hq + hq) * p.Sq + i) * D;
-            uint8_t *qt = sm + t * C::QB;
-#pragma unroll
-            for (int dc = 0; dc < D / 16; ++dc) {
-                uint4 w = make_uint4(0, 0, 0, 0);
-                if (row_ok) w = *reinterpret_cast<const uint4 *>(qrow + dc * 16);
-                store_piece<128>(qt, r, dc, w);
+        // split rows: the two threads of a row swap partial maxima / sums
+        float *red = reinterpret_cast<float *>(sm + C::OFF_RED);
+        auto pair_sync = [&]() {
+            asm volatile("bar.sync %0, %1;" ::"r"(1 + t), "n"(SPLIT * 128) : "memory");
+        };
+        auto pair_max = [&](float v, int ph) {
+            if constexpr (SPLIT == 1) {
+                return v;
+            } else {
+                float *rb = red + ((ph & 1) * C::NSW + wg) * 128;
+                rb[r] = v;
+                pair_sync();
+                return fmaxf(v, red[((ph & 1) * C::NSW + (wg ^ 1)) * 128 + r]);
             }
-            tc::fence_proxy_async();  // st.shared -> visible to the tensor core
+        };
+        {
+            const int8_t *qrow = p.q + (((int64_t)b * p.Hq + hq) * p.Sq + i) * D;
+            if constexpr (C::QT) {
+                // Q row int8 -> exact f16 pairs in this thread's TMEM lane
+                // (each of a row's SPLIT threads writes its share of channels)
+#pragma unroll 1
+                for (int c = hc * (D / 64 / SPLIT); c < (hc + 1) * (D / 64 / SPLIT); ++c) {
+                    uint32_t v[32];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        uint4 w = make_uint4(0, 0, 0, 0);
+                        if (row_ok) w = *reinterpret_cast<const uint4 *>(qrow + c * 64 + u * 16);
+                        i8x4_to_f16x4(w.x, v[u * 8 + 0], v[u * 8 + 1]);
+                        i8x4_to_f16x4(w.y, v[u * 8 + 2], v[u * 8 + 3]);
+                        i8x4_to_f16x4(w.z, v[u * 8 + 4], v[u * 8 + 5]);
+                        i8x4_to_f16x4(w.w, v[u * 8 + 6], v[u * 8 + 7]);
+                    }
+                    tc::st32(tmem + lane_base + C::COL_Q + t * (D / 2) + c * 32, v);
+                }
+                tc::wait_st();
+                tc::fence_before();
+            } else {
+                // Q row int8 -> f16 in the swizzled K-major layout of the A operand
+                uint8_t *qt = sm + t * C::QB;
+#pragma unroll
+                for (int dc = hc * (D / 16 / SPLIT); dc < (hc + 1) * (D / 16 / SPLIT); ++dc) {
+                    uint4 w = make_uint4(0, 0, 0, 0);
+                    if (row_ok) w = *reinterpret_cast<const uint4 *>(qrow + dc * 16);
+                    store_piece<128>(qt, r, dc, w);
+                }
+                tc::fence_proxy_async();  // st.shared -> visible to the tensor core
+            }
             mbar_arrive(bar(B_Q_READY));
         }
         // kept strictly positive so that a masked (-inf) score stays -inf; an
@@ -442,9 +501,19 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         // the max runs on the raw integer scores and the scale folds into
         // the exponent's FMA, one value per group
         const bool kuni = p.k_shift >= 6;
+        constexpr int NG = CW >= 64 ? CW / 64 : 1;   // 64-key groups this thread touches
+        constexpr int GW = CW >= 64 ? 64 : CW;       // its columns per group
         float m_run = -INFINITY, l = 0.0f;
         int done = 0;
+        // After an abort (a bounded wait gave up) a split row's two threads
+        // still pass the same pair barriers, tile by tile, so neither waits
+        // for a partner that left; with whole rows the loop simply ends.
+        bool alive = true;
         for (int jj = 0; jj < T; ++jj) {
+            if (!alive) {
+                pair_max(0.0f, jj);
+                continue;
+            }
             const int s = jj % NST;
             const int slot = t * NS + (NS == 1 ? 0 : (jj & 1));
             const uint32_t sp = NS == 1 ? (uint32_t)jj & 1u : (uint32_t)(jj >> 1) & 1u;
@@ -454,29 +523,35 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const int kg0 = pre ? key0 : P + key0;  // over prefix + chunk
             bool ok = wait_ab(bar(B_S_FULL + slot), sp, p.err, abort_flag);
             ok = ok && wait_ab(bar(B_V_FULL + s), (uint32_t)(jj / NST) & 1u, p.err, abort_flag);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            if (!__all_sync(0xffffffffu, ok)) {
+                if constexpr (SPLIT == 1) break;
+                alive = false;
+                pair_max(0.0f, jj);
+                continue;
+            }
             tc::fence_after();
             const uint32_t s_t = tmem + lane_base + C::COL_S + slot * BN;
             const uint8_t *stg = sm + C::OFF_ST + s * C::SB;
-            const float4 *ksc4 = reinterpret_cast<const float4 *>(stg + 2 * C::KB);
-            const float4 *vsc4 = reinterpret_cast<const float4 *>(stg + 2 * C::KB + BN * 4);
-            uint32_t x[BN];
+            const float4 *ksc4 = reinterpret_cast<const float4 *>(stg + 2 * C::KB) + c0 / 4;
+            uint32_t x[CW];
+            if constexpr (CW >= 32) {
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
-                tc::ld32(s_t + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+                for (int c = 0; c < CW / 32; ++c)
+                    tc::ld32(s_t + c0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&x[c * 32]));
+            }
             tc::wait_ld();
             if (p.dbg) {
                 // debug dump of the raw INT32 scores, re-read from TMEM in
                 // 8-column pieces so that it adds no live registers here
                 int32_t *dr = p.dbg + (((int64_t)b * p.Hq + hq) * p.Sq + i) * p.dbg_stride;
 #pragma unroll 1
-                for (int c8 = 0; c8 < BN / 8; ++c8) {
+                for (int c8 = 0; c8 < CW / 8; ++c8) {
                     uint32_t v[8];
-                    tc::ld8(s_t + c8 * 8, v);
+                    tc::ld8(s_t + c0 + c8 * 8, v);
                     tc::wait_ld();
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int c = c8 * 8 + e;
+                        const int c = c0 + c8 * 8 + e;
                         if (row_ok && c < nvalid && (!p.causal || kg0 + c <= lim))
                             dr[kg0 + c] = __float2int_rn(__uint_as_float(v[e]));
                     }
@@ -486,16 +561,16 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const bool tmask = nvalid < BN || (p.causal && kg0 + BN - 1 > i_first + off);
             const bool uni = kuni && !pre && !tmask;
             float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-            float kg[BN / 64];
+            float kg[NG];
             if (uni) {
                 // scale >= 0, so max(s) * k == max(s * k)
 #pragma unroll
-                for (int g = 0; g < BN / 64; ++g) {
+                for (int g = 0; g < NG; ++g) {
                     kg[g] = ksc4[16 * g].x;
                     float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int c = 64 * g + 8 * q;
+                    for (int q = 0; q < GW / 8; ++q) {
+                        const int c = GW * g + 8 * q;
                         a0 = fmax3(a0, __uint_as_float(x[c]), __uint_as_float(x[c + 1]));
                         a1 = fmax3(a1, __uint_as_float(x[c + 2]), __uint_as_float(x[c + 3]));
                         a2 = fmax3(a2, __uint_as_float(x[c + 4]), __uint_as_float(x[c + 5]));
@@ -506,7 +581,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             } else if (!tmask) {
                 // per-key scales: x <- s * k_scale in place
 #pragma unroll
-                for (int c4 = 0; c4 < BN / 4; ++c4) {
+                for (int c4 = 0; c4 < CW / 4; ++c4) {
                     const float4 k = ksc4[c4];
                     const float2 z01 = fmul2(u2f2(x[4 * c4], x[4 * c4 + 1]), make_float2(k.x, k.y));
                     const float2 z23 = fmul2(u2f2(x[4 * c4 + 2], x[4 * c4 + 3]), make_float2(k.z, k.w));
@@ -518,9 +593,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     m4[2 + (c4 & 1)] = fmax3(m4[2 + (c4 & 1)], z23.x, z23.y);
                 }
             } else {
-                const int cl = p.causal ? min(nvalid, lim - kg0 + 1) : nvalid;  // keys [0, cl) count
+                // keys [0, cl) of the tile count
+                const int cl = (p.causal ? min(nvalid, lim - kg0 + 1) : nvalid) - c0;
 #pragma unroll
-                for (int c4 = 0; c4 < BN / 4; ++c4) {
+                for (int c4 = 0; c4 < CW / 4; ++c4) {
                     const float4 k = ksc4[c4];
                     const float kk[4] = {k.x, k.y, k.z, k.w};
 #pragma unroll
@@ -532,7 +608,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     }
                 }
             }
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            const float mx = pair_max(fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])), jj);
             const float tb = pre ? 0.0f : bc;
             const float tmax = fmaf(mx, rq, tb);  // -inf when every key is masked (rq > 0)
             const float cand = fmaxf(m_run, tmax);
@@ -546,17 +622,24 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const bool fix = move && jj > 0 && alpha != 1.0f;
             if (__any_sync(0xffffffffu, fix)) {
                 // O holds P.V of earlier tiles scaled to the old max: once the
-                // last P.V retired, rescale this warp's rows in TMEM
+                // last P.V retired, rescale this thread's columns of the row
                 if (NS == 2) {
-                    const bool w = wait_ab(bar(B_O_DONE + t), (uint32_t)(jj - 1) & 1u, p.err,
-                                           abort_flag);
-                    if (!__all_sync(0xffffffffu, w)) break;
+                    // with one query tile the V stage of tile jj-1 is released
+                    // exactly when P.V(jj-1) retires; S(jj) alone does not
+                    // imply it (QK(jj) was issued before P.V(jj-1))
+                    const bool w = wait_ab(bar(B_V_EMPTY + (jj - 1) % NST),
+                                           (uint32_t)((jj - 1) / NST) & 1u, p.err, abort_flag);
+                    if (!__all_sync(0xffffffffu, w)) {
+                        if constexpr (SPLIT == 1) break;
+                        alive = false;  // this tile's pair barrier is behind us
+                        continue;
+                    }
                 }
                 tc::fence_after();
                 const float f = fix ? alpha : 1.0f;
                 // 8-column pieces: the S row is live in registers here
 #pragma unroll 1
-                for (int c = 0; c < D / 8; ++c) {
+                for (int c = hc * (D / 8 / SPLIT); c < (hc + 1) * (D / 8 / SPLIT); ++c) {
                     uint32_t o[8];
                     tc::ld8(tmem + lane_base + t * D + c * 8, o);
                     tc::wait_ld();
@@ -571,68 +654,51 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 tc::wait_st();
             }
             const float nb = tb - (m_run == -INFINITY ? 0.0f : m_run);
-            // ---- P = 2^(z*rq + tb - m), packed f16 pairs over the S columns
+            // ---- P = 2^(z*rq + tb - m), packed f16 pairs over the S columns;
+            // a 64-key part goes to the MMA as soon as it is stored
             float2 ls01 = make_float2(0.0f, 0.0f), ls23 = make_float2(0.0f, 0.0f);
             const float2 nb2 = make_float2(nb, nb);
-            if (uni) {
+            const float2 rq2 = make_float2(rq, rq);
 #pragma unroll
-                for (int h = 0; h < BN / 64; ++h) {
-                    const float2 kr2 = make_float2(kg[h] * rq, kg[h] * rq);
-                    uint32_t pk[32];
+            for (int g = 0; g < NG; ++g) {
+                const float2 kr2 = uni ? make_float2(kg[g] * rq, kg[g] * rq) : rq2;
+                uint32_t pk[GW / 2];
 #pragma unroll
-                    for (int q4 = 0; q4 < 16; ++q4) {
-                        const int c = 64 * h + 4 * q4;
-                        const float2 a01 = ffma2(u2f2(x[c], x[c + 1]), kr2, nb2);
-                        const float2 a23 = ffma2(u2f2(x[c + 2], x[c + 3]), kr2, nb2);
-                        const float2 p01 = make_float2(fast_exp2(a01.x), fast_exp2(a01.y));
-                        const float2 p23 = make_float2(fast_exp2(a23.x), fast_exp2(a23.y));
-                        ls01 = fadd2(ls01, p01);
-                        ls23 = fadd2(ls23, p23);
-                        pk[2 * q4] = pack2(p01.x, p01.y, false);
-                        pk[2 * q4 + 1] = pack2(p23.x, p23.y, false);
-                    }
-                    tc::st32(s_t + h * 32, pk);
-                    tc::wait_st();
-                    tc::fence_before();
-                    mbar_arrive(bar(B_P_FULL + slot * C::NPH + h));
+                for (int q4 = 0; q4 < GW / 4; ++q4) {
+                    const int c = GW * g + 4 * q4;
+                    const float2 a01 = ffma2(u2f2(x[c], x[c + 1]), kr2, nb2);
+                    const float2 a23 = ffma2(u2f2(x[c + 2], x[c + 3]), kr2, nb2);
+                    const float2 p01 = make_float2(fast_exp2(a01.x), fast_exp2(a01.y));
+                    const float2 p23 = make_float2(fast_exp2(a23.x), fast_exp2(a23.y));
+                    ls01 = fadd2(ls01, p01);
+                    ls23 = fadd2(ls23, p23);
+                    pk[2 * q4] = pack2(p01.x, p01.y, false);
+                    pk[2 * q4 + 1] = pack2(p23.x, p23.y, false);
                 }
-            } else {
-                const float2 rq2 = make_float2(rq, rq);
-#pragma unroll
-                for (int h = 0; h < BN / 64; ++h) {
-                    // 64 keys -> 32 packed words -> TMEM columns [32h, 32h+32)
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int q4 = 0; q4 < 16; ++q4) {
-                        const int c = 64 * h + 4 * q4;
-                        const float2 a01 = ffma2(u2f2(x[c], x[c + 1]), rq2, nb2);
-                        const float2 a23 = ffma2(u2f2(x[c + 2], x[c + 3]), rq2, nb2);
-                        float2 p01 = make_float2(fast_exp2(a01.x), fast_exp2(a01.y));
-                        float2 p23 = make_float2(fast_exp2(a23.x), fast_exp2(a23.y));
-                        ls01 = fadd2(ls01, p01);
-                        ls23 = fadd2(ls23, p23);
-                        if (pre) {
-                            // prefix keys: fold the per-token V scale into P
-                            const float4 v = vsc4[c / 4];
-                            p01 = fmul2(p01, make_float2(v.x, v.y));
-                            p23 = fmul2(p23, make_float2(v.z, v.w));
-                        }
-                        pk[2 * q4] = pack2(p01.x, p01.y, false);
-                        pk[2 * q4 + 1] = pack2(p23.x, p23.y, false);
-                    }
-                    tc::st32(s_t + h * 32, pk);
-                    tc::wait_st();
-                    tc::fence_before();
-                    mbar_arrive(bar(B_P_FULL + slot * C::NPH + h));
-                }
+                const uint32_t pcol = s_t + (c0 + GW * g) / 2;
+                if constexpr (GW == 64)
+                    tc::st32(pcol, pk);
+                else
+                    tc::st16(pcol, *reinterpret_cast<uint32_t(*)[16]>(pk));
+                tc::wait_st();
+                tc::fence_before();
+                mbar_arrive(bar(B_P_FULL + slot * C::NPH + (c0 + GW * g) / 64));
             }
             l += (ls01.x + ls01.y) + (ls23.x + ls23.y);
             done = jj + 1;
         }
         // ------------------------------------------------ epilogue
-        // O_DONE cannot tell the last phase from two phases back when S is
-        // double-buffered (the last two P.V may both be in flight), so the
-        // epilogue waits on a barrier that completes exactly once
+        if constexpr (SPLIT > 1) {
+            // the row's sum is the two halves' sums (same running max)
+            float *rb = red + ((T & 1) * C::NSW + wg) * 128;
+            rb[r] = l;
+            pair_sync();
+            l += red[((T & 1) * C::NSW + (wg ^ 1)) * 128 + r];
+        }
+        // with S double-buffered the last two P.V may both be in flight, and a
+        // parity wait on a per-tile barrier cannot tell its last phase from
+        // two phases back, so the epilogue waits on a barrier that completes
+        // exactly once
         bool have = done == T && T > 0;
         if (have) {
             const bool w = wait_ab(bar(B_O_FINAL + t), 0u, p.err, abort_flag);
@@ -642,7 +708,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const int64_t orow = ((int64_t)b * p.Hq + hq) * p.Sq + i;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = hc * (D / 32 / SPLIT); c < (hc + 1) * (D / 32 / SPLIT); ++c) {
             uint32_t o[32];
             if (have) {
                 tc::ld32(tmem + lane_base + t * D + c * 32, o);
@@ -665,7 +731,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
             }
         }
-        if (row_ok && p.lse)
+        if (row_ok && p.lse && hc == 0)
             p.lse[orow] = l > 0.0f ? (m_run + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     }
 

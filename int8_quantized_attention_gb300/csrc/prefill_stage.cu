@@ -4,6 +4,8 @@
 // that the attention kernel's tiles arrive by TMA in the layout the tensor
 // cores read and every query tile re-reads them from L2 without converting.
 //
+// Prefix values are stored as f16(code * v_scale) (one rounding, as the P.V
+// operand); K codes stay exact.
 // Workspace rows per (batch, kv head), in key order: [0, Ppad) the paged
 // prefix (key r at row r; rows past the batch's prefix length are zero),
 // [Ppad, Ppad + Sk) the contiguous chunk, then zero rows up to Lpad.  The
@@ -27,6 +29,26 @@ __device__ __forceinline__ void store_f16x16(__half *dst, uint4 w) {
     uint4 *d = reinterpret_cast<uint4 *>(dst);
     d[0] = h0;
     d[1] = h1;
+}
+
+// 16 int8 codes times one scale -> 16 f16 (round to nearest, finite range)
+__device__ __forceinline__ void store_f16x16_scaled(__half *dst, uint4 w, float sc) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+    uint32_t h[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const int8_t *b = reinterpret_cast<const int8_t *>(&u[e]);
+        const float f0 = fminf(fmaxf((float)b[0] * sc, -65504.0f), 65504.0f);
+        const float f1 = fminf(fmaxf((float)b[1] * sc, -65504.0f), 65504.0f);
+        const float f2 = fminf(fmaxf((float)b[2] * sc, -65504.0f), 65504.0f);
+        const float f3 = fminf(fmaxf((float)b[3] * sc, -65504.0f), 65504.0f);
+        __half2 lo = __floats2half2_rn(f0, f1), hi = __floats2half2_rn(f2, f3);
+        h[2 * e] = *reinterpret_cast<uint32_t *>(&lo);
+        h[2 * e + 1] = *reinterpret_cast<uint32_t *>(&hi);
+    }
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    d[1] = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
 // 8 bf16 -> 8 f16, round to nearest, saturating to the finite f16 range
@@ -80,11 +102,10 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
             }
         }
         store_f16x16(p.k_ws + ((int64_t)bh * p.Lpad + row) * D + dc * 16, wk);
-        store_f16x16(p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16, wv);
-        if (dc == 0) {
-            p.ksc_ws[(int64_t)bh * p.Lpad + row] = ks;
-            p.vsc_ws[(int64_t)bh * p.Ppad + row] = vs;
-        }
+        // prefix values: the per-token V scale is applied here, once, so the
+        // attention kernel treats prefix and chunk values alike
+        store_f16x16_scaled(p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16, wv, vs);
+        if (dc == 0) p.ksc_ws[(int64_t)bh * p.Lpad + row] = ks;
     } else {
         const int np = D >> 4;
         const int slot = t / np, dc = t % np;
@@ -128,8 +149,7 @@ PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, 
     L.off_k = 0;
     L.off_v = align256(L.off_k + BH * L.Lpad * D * 2);
     L.off_ksc = align256(L.off_v + BH * L.Vrows * D * 2);
-    L.off_vsc = align256(L.off_ksc + BH * L.Lpad * 4);
-    L.bytes = align256(L.off_vsc + BH * L.Ppad * 4);
+    L.bytes = align256(L.off_ksc + BH * L.Lpad * 4);
     return L;
 }
 
