@@ -20,18 +20,22 @@
 // One CTA owns NQ query tiles of 128 rows (NQ = 2 for D <= 128, 1 for
 // D = 256) of one (batch, head); keys stream in tiles of BN (128, or 64 at
 // D = 256) through an NST-deep ring.
-//   warps 0..4NQ-1  softmax, one warpgroup per query tile, one thread per
-//              query row (TMEM lane): Q int8 -> f16 into shared memory once;
+//   warps 0..4NQ*SPLIT-1  softmax: per query tile one warpgroup (one thread
+//              per query row = TMEM lane), or at D = 256 two warpgroups
+//              sharing each row's columns; Q int8 -> f16 into shared memory
+//              (or TMEM) once;
 //              per key tile one tcgen05.ld of the whole S row into
 //              registers, per-column K-scale recovery, online softmax with
 //              lazy rescaling (O is rescaled only when the row max grows by
 //              more than 2^8), P written back over S in TMEM.
-//   warp 4NQ   producer: lane 0 streams K tiles, lane 1 V tiles and the
+//   next warp  producer: lane 0 streams K tiles, lane 1 V tiles and the
 //              per-key scales (TMA tensor loads + 1-D bulk copies).
-//   warp 4NQ+1 TMEM owner and MMA issuer (one thread): S_t = Q_t K^T from
-//              shared memory, then O_t += P_t V with P from TMEM.  With two
-//              query tiles the two warpgroups ping-pong: the tensor core
-//              works on one tile's MMAs while the other tile's softmax runs.
+//   next warp  TMEM owner and MMA issuer (one thread): S_t = Q_t K^T (Q from
+//              shared memory, or from TMEM where it fits), then O_t += P_t V
+//              with P from TMEM.  With two query tiles the two warpgroups
+//              ping-pong: the tensor core works on one tile's MMAs while the
+//              other tile's softmax runs (one issuer keeps each tile's MMAs
+//              together; two issuers interleaving them measured slower).
 //              With one tile (D = 256) S is double-buffered instead.
 // Tensor memory (512 columns): O_t at [t*D, t*D+D), S slots from NQ*D.
 // Every mbarrier wait is bounded; a timeout raises a CTA-wide abort flag
