@@ -28,8 +28,9 @@
 //              registers, per-column K-scale recovery, online softmax with
 //              lazy rescaling (O is rescaled only when the row max grows by
 //              more than 2^8), P written back over S in TMEM.
-//   next warp  producer: lane 0 streams K tiles, lane 1 V tiles and the
-//              per-key scales (TMA tensor loads + 1-D bulk copies).
+//   next warp  producer (one thread): per key tile the K and V tiles (TMA
+//              tensor loads) and the per-key K scales (1-D bulk copy) into
+//              one stage of an NST-deep ring.
 //   next warp  TMEM owner and MMA issuer (one thread): S_t = Q_t K^T (Q from
 //              shared memory, or from TMEM where it fits), then O_t += P_t V
 //              with P from TMEM.  With two query tiles the two warpgroups
@@ -102,10 +103,8 @@ struct PCfg {
 
 // barrier slots
 enum {
-    B_K_FULL = 0,     // [NST] producer: K tile landed
-    B_V_FULL = 4,     // [NST] producer: V tile and per-key scales landed
-    B_K_EMPTY = 8,    // [NST] MMA: every QK^T reading the K stage retired
-    B_V_EMPTY = 12,   // [NST] MMA: every P.V reading the V stage retired
+    B_KV_FULL = 0,    // [NST] producer: K tile, V tile and per-key scales landed
+    B_KV_EMPTY = 4,   // [NST] MMA: every QK^T and P.V reading the stage retired
     B_S_FULL = 16,    // [NQ*NS] MMA: S = Q K^T done
     B_P_FULL = 20,    // [NQ*NS*NPH] softmax: a 64-key part of P in TMEM (O rescaled)
     B_O_FINAL = 26,   // [NQ] MMA: the last O_t += P_t V done (one phase)
@@ -254,10 +253,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
-            mbar_init(bar(B_K_FULL + s), 1);
-            mbar_init(bar(B_V_FULL + s), 1);
-            mbar_init(bar(B_K_EMPTY + s), 1);
-            mbar_init(bar(B_V_EMPTY + s), 1);
+            mbar_init(bar(B_KV_FULL + s), 1);
+            mbar_init(bar(B_KV_EMPTY + s), 1);
         }
         for (int s = 0; s < NQ * NS; ++s) mbar_init(bar(B_S_FULL + s), 1);
         for (int s = 0; s < NQ * NS * C::NPH; ++s) mbar_init(bar(B_P_FULL + s), 128 * C::SPLIT);
@@ -282,27 +279,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     if (warp == kProducer) {
         // ============================================================ producer
         if (lane == 0 && T > 0) {
-            // K stream: a stage is refilled once every QK^T that read it retired
+            // one stage per key tile (K, V and the per-key K scales on one
+            // barrier), refilled once every QK^T and P.V that read it retired
             tc::prefetch_tmap(&maps.k);
-            int issued = 0;
-            for (int jj = 0; jj < T; ++jj) {
-                const int s = jj % NST;
-                if (jj >= NST &&
-                    !wait_ab(bar(B_K_EMPTY + s), (uint32_t)(jj / NST - 1) & 1u, p.err, abort_flag))
-                    break;
-                const int w = jj < n_pre ? jj : wpre + (jj - n_pre);
-                const uint32_t st = sm_a + C::OFF_ST + s * C::SB;
-                mbar_arrive_expect_tx(bar(B_K_FULL + s), C::KB);
-#pragma unroll
-                for (int a = 0; a < D / 64; ++a)
-                    tc::tma_load_3d(st + a * BN * 128, &maps.k, a * 64, w * BN, bh,
-                                    bar(B_K_FULL + s));
-                ++issued;
-            }
-            for (int jj = max(0, issued - NST); jj < issued; ++jj)
-                mbar_wait(bar(B_K_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err);
-        } else if (lane == 1 && T > 0) {
-            // V stream (+ per-key scales): refilled once every P.V retired
             if (n_pre > 0) tc::prefetch_tmap(&maps.v_pre);
             if (n_ch > 0) tc::prefetch_tmap(&maps.v_ch);
             const int vch_off = p.v_bf16 ? p.Ppad : 0;
@@ -310,24 +289,26 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             for (int jj = 0; jj < T; ++jj) {
                 const int s = jj % NST;
                 if (jj >= NST &&
-                    !wait_ab(bar(B_V_EMPTY + s), (uint32_t)(jj / NST - 1) & 1u, p.err, abort_flag))
+                    !wait_ab(bar(B_KV_EMPTY + s), (uint32_t)(jj / NST - 1) & 1u, p.err, abort_flag))
                     break;
                 const bool pre = jj < n_pre;
                 const int w = pre ? jj : wpre + (jj - n_pre);
                 const uint32_t st = sm_a + C::OFF_ST + s * C::SB;
-                mbar_arrive_expect_tx(bar(B_V_FULL + s), C::KB + BN * 4);
+                const uint32_t fb = bar(B_KV_FULL + s);
+                mbar_arrive_expect_tx(fb, 2 * C::KB + BN * 4);
+#pragma unroll
+                for (int a = 0; a < D / 64; ++a)
+                    tc::tma_load_3d(st + a * BN * 128, &maps.k, a * 64, w * BN, bh, fb);
                 const CUtensorMap *vm = pre ? &maps.v_pre : &maps.v_ch;
                 const int vrow = pre ? w * BN : (w - wpre) * BN + vch_off;
 #pragma unroll
                 for (int a = 0; a < D / 64; ++a)
-                    tc::tma_load_3d(st + C::KB + a * BN * 128, vm, a * 64, vrow, bh,
-                                    bar(B_V_FULL + s));
-                bulk_g2s(st + 2 * C::KB, p.ksc_ws + (int64_t)bh * p.Lpad + w * BN, BN * 4,
-                         bar(B_V_FULL + s));
+                    tc::tma_load_3d(st + C::KB + a * BN * 128, vm, a * 64, vrow, bh, fb);
+                bulk_g2s(st + 2 * C::KB, p.ksc_ws + (int64_t)bh * p.Lpad + w * BN, BN * 4, fb);
                 ++issued;
             }
             for (int jj = max(0, issued - NST); jj < issued; ++jj)
-                mbar_wait(bar(B_V_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err);
+                mbar_wait(bar(B_KV_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err);
         }
         __syncwarp();
     } else if (warp == kMma) {
@@ -371,10 +352,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 const uint32_t o = tmem + t * D;
 #pragma unroll
                 for (int h = 0; h < C::NPH; ++h) {
-                    bool ok = wait_ab(bar(B_P_FULL + slot * C::NPH + h), sp, p.err, abort_flag);
-                    if (ok && h == 0 && t == 0)
-                        ok = wait_ab(bar(B_V_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err,
-                                     abort_flag);
+                    // (the stage's V landed with its K, waited before QK^T)
+                    const bool ok = wait_ab(bar(B_P_FULL + slot * C::NPH + h), sp, p.err, abort_flag);
                     if (!ok) return false;
                     tc::fence_after();
 #pragma unroll
@@ -389,7 +368,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 return true;
             };
             auto k_ready = [&](int jj) {
-                const bool ok = wait_ab(bar(B_K_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err,
+                const bool ok = wait_ab(bar(B_KV_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err,
                                         abort_flag);
                 tc::fence_after();
                 return ok;
@@ -398,7 +377,6 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             if (ok) {
 #pragma unroll
                 for (int t = 0; t < NQ; ++t) qk(0, t);
-                tc::commit(bar(B_K_EMPTY + 0));
             }
             for (int jj = 0; ok && jj < T; ++jj) {
                 const int s = jj % NST;
@@ -406,11 +384,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     // per query tile: O_t += P_t V_j, then S_t = Q_t K_{j+1}
                     for (int t = 0; t < NQ; ++t) {
                         if (!(ok = pv(jj, t))) break;
-                        if (t == NQ - 1) tc::commit(bar(B_V_EMPTY + s));
+                        if (t == NQ - 1) tc::commit(bar(B_KV_EMPTY + s));
                         if (jj + 1 < T) {
                             if (t == 0 && !(ok = k_ready(jj + 1))) break;
                             qk(jj + 1, t);
-                            if (t == NQ - 1) tc::commit(bar(B_K_EMPTY + (jj + 1) % NST));
                         }
                     }
                 } else {
@@ -418,10 +395,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     if (jj + 1 < T) {
                         if (!(ok = k_ready(jj + 1))) break;
                         qk(jj + 1, 0);
-                        tc::commit(bar(B_K_EMPTY + (jj + 1) % NST));
                     }
                     if (!(ok = pv(jj, 0))) break;
-                    tc::commit(bar(B_V_EMPTY + s));
+                    tc::commit(bar(B_KV_EMPTY + s));
                 }
             }
             tc::commit(bar(B_DRAIN));
@@ -526,7 +502,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const int nvalid = min(BN, (pre ? P : p.Sk) - key0);
             const int kg0 = pre ? key0 : P + key0;  // over prefix + chunk
             bool ok = wait_ab(bar(B_S_FULL + slot), sp, p.err, abort_flag);
-            ok = ok && wait_ab(bar(B_V_FULL + s), (uint32_t)(jj / NST) & 1u, p.err, abort_flag);
+            ok = ok && wait_ab(bar(B_KV_FULL + s), (uint32_t)(jj / NST) & 1u, p.err, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
                 if constexpr (SPLIT == 1) break;
                 alive = false;
@@ -631,7 +607,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     // with one query tile the V stage of tile jj-1 is released
                     // exactly when P.V(jj-1) retires; S(jj) alone does not
                     // imply it (QK(jj) was issued before P.V(jj-1))
-                    const bool w = wait_ab(bar(B_V_EMPTY + (jj - 1) % NST),
+                    const bool w = wait_ab(bar(B_KV_EMPTY + (jj - 1) % NST),
                                            (uint32_t)((jj - 1) / NST) & 1u, p.err, abort_flag);
                     if (!__all_sync(0xffffffffu, w)) {
                         if constexpr (SPLIT == 1) break;
