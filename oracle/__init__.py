@@ -47,6 +47,9 @@ def _lib():
         lib.oracle_attend.restype = _i64
         lib.oracle_splitk_combine.argtypes = [_vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp]
         lib.oracle_splitk_combine.restype = None
+        lib.oracle_kv_append.argtypes = [_vp, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _i64,
+                                         _vp, _vp]
+        lib.oracle_kv_append.restype = _i64
         _LIB = lib
     return _LIB
 
@@ -313,3 +316,24 @@ def splitk_combine(o_part, lse_part):
     lse = np.empty((R,), np.float64)
     _lib().oracle_splitk_combine(_p(o_part), _p(lse_part), R, S, D, _p(o), _p(lse))
     return o.reshape(*lead, D), lse.reshape(*lead)
+
+
+def kv_append(x, block_table, positions, cache, scale):
+    """Quantise new rows per (token, KV head) and write them into a paged cache.
+
+    x float32 [B,H,n,D] (exact fp32 copies of the fp16/bf16 rows);
+    block_table int32 [B,max_blocks]; positions int32 [B] (row 0's token
+    index); cache int8 [num_blocks,H,D/16,16,16] and scale float32
+    [num_blocks,H,16] are copied, updated and returned with the count of
+    rows whose page index was out of range (those are left untouched).
+    ([P1] sections 3 and 4.)
+    """
+    x = _c(x, np.float32)
+    B, H, n, D = x.shape
+    bt = _c(block_table, np.int32)
+    pos = _c(positions, np.int32)
+    cache = np.array(cache, dtype=np.int8, copy=True, order="C")
+    scale = np.array(scale, dtype=np.float32, copy=True, order="C")
+    skipped = _lib().oracle_kv_append(_p(x), B, H, n, D, _p(bt), bt.shape[1], _p(pos),
+                                      cache.shape[0], _p(cache), _p(scale))
+    return cache, scale, int(skipped)

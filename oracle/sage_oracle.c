@@ -246,3 +246,48 @@ void oracle_splitk_combine(const double *opart, const double *lpart, int64_t R,
         lse[r] = L;
     }
 }
+
+/* ------------------------------------------------------------------ */
+/* KV producer: quantise new key/value rows and write them into the   */
+/* paged INT8 cache.                                                   */
+/* [P1] section 4: K and V are quantised per token and per KV head     */
+/* (s = max|x| / 127 over the row's D channels, codes round(x / s));   */
+/* [P1] section 3: token t of sequence b lives in page                 */
+/* block_table[b][t / 16], slot t % 16, channel c at                   */
+/* [page][kv_head][c / 16][slot][c % 16]; its scale at                  */
+/* [page][kv_head][slot].                                              */
+/* x: [B][H][n][D] fp32 (the new rows); pos[b]: position of row 0 of   */
+/* sequence b.  Returns the number of rows skipped because their page  */
+/* index was outside [0, num_blocks).                                  */
+/* ------------------------------------------------------------------ */
+
+int64_t oracle_kv_append(const float *x, int64_t B, int64_t H, int64_t n, int D,
+                         const int32_t *block_table, int64_t max_blocks, const int32_t *pos,
+                         int64_t num_blocks, int8_t *cache, float *scale)
+{
+    int64_t skipped = 0;
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < H; ++h)
+            for (int64_t t = 0; t < n; ++t) {
+                const float *row = x + ((b * H + h) * n + t) * D;
+                const int64_t p = (int64_t)pos[b] + t;
+                const int64_t blk = block_table[b * max_blocks + p / 16];
+                const int64_t slot = p % 16;
+                if (blk < 0 || blk >= num_blocks) {
+                    ++skipped;
+                    continue;
+                }
+                float amax = 0.0f;
+                for (int c = 0; c < D; ++c) {
+                    const float a = fabsf(row[c]);
+                    if (a > amax)
+                        amax = a;
+                }
+                const float s = amax / 127.0f;
+                int8_t *page = cache + (blk * H + h) * (int64_t)D * 16;
+                for (int c = 0; c < D; ++c)
+                    page[(c / 16) * 256 + slot * 16 + (c % 16)] = quant_one(row[c], s);
+                scale[(blk * H + h) * 16 + slot] = s;
+            }
+    return skipped;
+}

@@ -389,3 +389,55 @@ def test_prefill_with_paged_prefix_equals_concatenated_keys():
                                           0.3, causal=True, offset=P)
         np.testing.assert_allclose(o[0, h], o_ref, rtol=1e-12, atol=1e-14)
         np.testing.assert_allclose(lse[0, h], l_ref, rtol=1e-12)
+
+
+def test_kv_append_identity_and_page_layout():
+    """Rows of integers with amax exactly 127 quantise to themselves (s = 1);
+    every element must land at [page][head][c/16][slot][c%16] of the page
+    the block table names for its token ([P1] sections 3 and 4).  The
+    expected cache is written here element by element, by hand."""
+    rng = np.random.default_rng(21)
+    B, H, n, D, nblk = 2, 3, 23, 64, 9
+    x = rng.integers(-127, 128, (B, H, n, D)).astype(np.float32)
+    x[..., 5] = np.where(rng.random((B, H, n)) < 0.5, 127.0, -127.0)
+    table = np.stack([rng.permutation(nblk)[:4], rng.permutation(nblk)[:4]]).astype(np.int32)
+    pos = np.array([3, 17], np.int32)
+    cache0 = rng.integers(-127, 128, (nblk, H, D // 16, 16, 16)).astype(np.int8)
+    scale0 = rng.uniform(0.005, 0.02, (nblk, H, 16)).astype(np.float32)
+    cache, scale, skipped = oracle.kv_append(x, table, pos, cache0, scale0)
+    assert skipped == 0
+    want_c, want_s = cache0.copy(), scale0.copy()
+    for b in range(B):
+        for h in range(H):
+            for t in range(n):
+                p = pos[b] + t
+                blk, slot = table[b, p // 16], p % 16
+                want_s[blk, h, slot] = 1.0
+                for c in range(D):
+                    want_c[blk, h, c // 16, slot, c % 16] = x[b, h, t, c]
+    assert np.array_equal(cache, want_c)
+    assert np.array_equal(scale, want_s)
+
+
+def test_kv_append_error_bound_and_bad_pages():
+    """Each stored code times its scale is within half a quantisation step
+    of the input, the scale is the row's amax / 127, and rows whose page
+    index is out of range are skipped and leave the cache untouched."""
+    rng = np.random.default_rng(22)
+    B, H, n, D, nblk = 1, 2, 40, 128, 6
+    x = rng.standard_normal((B, H, n, D)).astype(np.float32) * 3
+    table = np.array([[2, 0, 99, 4]], np.int32)      # page index 99 does not exist
+    pos = np.array([0], np.int32)
+    cache0 = np.zeros((nblk, H, D // 16, 16, 16), np.int8)
+    scale0 = np.zeros((nblk, H, 16), np.float32)
+    cache, scale, skipped = oracle.kv_append(x, table, pos, cache0, scale0)
+    assert skipped == H * 8                          # tokens 32..39 map to page 99
+    for h in range(H):
+        for t in range(32):
+            blk, slot = table[0, t // 16], t % 16
+            s = scale[blk, h, slot]
+            assert s == np.float32(np.abs(x[0, h, t]).max() / np.float32(127))
+            codes = cache[blk, h, :, slot, :].reshape(D).astype(np.float64)
+            assert np.all(np.abs(codes * s - x[0, h, t]) <= s / 2 * (1 + 1e-6))
+    untouched = [b for b in range(nblk) if b not in (2, 0)]
+    assert not cache[untouched].any() and not scale[untouched].any()
