@@ -60,7 +60,7 @@ typedef enum sage_dtype {
 const char *sage_get_last_error_message(void);
 
 /* Library ABI version (increments on any signature change). */
-int sage_version(void);   /* 3 */
+int sage_version(void);   /* 4 */
 
 /* --------------------------------------------------------------------------
  * Quantisation  ([P1] section 4; [P3] quant kernel table, feature matrix)
@@ -101,6 +101,27 @@ sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B, int H, i
  *   k_scale, v_scale : fp32 [num_blocks, Hkv, 16], per token and KV head.
  *   block_table      : int32 [B, max_blocks].
  * ------------------------------------------------------------------------ */
+
+/* --------------------------------------------------------------------------
+ * KV producer: append new tokens to the paged INT8 cache  ([P1] sections 3, 4)
+ *
+ * k_new, v_new: f16/bf16 [B, Hkv, n_new, D] contiguous, 16-byte aligned.
+ * Row t of sequence b is token positions[b] + t: it is quantised per token
+ * and KV head (s = max|x| / 127 in fp32, codes rne(x / s) clamped to
+ * [-127, 127]; an all-zero row gives s = 0 and codes 0, the rule of
+ * sage_quant_int8) and written to page block_table[b][pos / 16], slot
+ * pos % 16, in the cache layout above, with its scale at
+ * k_scale/v_scale[page][kv_head][slot].  positions (int32 [B]) and
+ * block_table are device arrays read on the GPU: a position outside the
+ * table or a page outside [0, num_blocks) skips that row and sets the
+ * bad-block bit of the device error word (sage_check_device_status).
+ * Rows of different sequences must not share a page slot.
+ * ------------------------------------------------------------------------ */
+sage_status_t sage_kv_cache_append(const void *k_new, const void *v_new, sage_dtype_t dtype,
+                                   int B, int Hkv, int n_new, int D,
+                                   const int32_t *block_table, int max_blocks,
+                                   const int32_t *positions, int num_blocks, int8_t *k_cache,
+                                   int8_t *v_cache, float *k_scale, float *v_scale, void *stream);
 
 /* --------------------------------------------------------------------------
  * Split-K paged decode  ([P1] sections 1, 3, 4, 5)

@@ -93,6 +93,9 @@ def lib():
         L.sage_attn_decode_paged_q16.argtypes = [ctypes.POINTER(DecodeArgs), _vp, _i, _vp,
                                                  ctypes.c_size_t, _vp]
         L.sage_attn_decode_paged_q16.restype = _i
+        L.sage_kv_cache_append.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp, _i, _vp,
+                                           _vp, _vp, _vp, _vp]
+        L.sage_kv_cache_append.restype = _i
         L.sage_attn_decode_paged_partials.argtypes = [ctypes.POINTER(DecodeArgs), _vp, _vp,
                                                       ctypes.POINTER(_i), _vp]
         L.sage_attn_decode_paged_partials.restype = _i
@@ -284,6 +287,31 @@ def sage_attn_decode_paged_q16(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     _check(lib().sage_attn_decode_paged_q16(ctypes.byref(a), _ptr(q), _dt(q.dtype), _ptr(workspace),
                                             ws_bytes, _stream(stream)))
     return (out, lse) if return_lse else out
+
+
+def sage_kv_cache_append(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table,
+                         positions, stream=None):
+    """Quantise new K/V rows per (token, KV head) into the paged INT8 cache, in place.
+
+    k_new, v_new [B,Hkv,n,D] f16/bf16; block_table int32 [B,max_blocks];
+    positions int32 [B] (token index of row 0 of each sequence).
+    """
+    for t, name in ((k_new, "k_new"), (v_new, "v_new")):
+        if t.dtype not in (torch.float16, torch.bfloat16) or not t.is_contiguous():
+            raise ValueError(name + " must be a contiguous f16/bf16 tensor")
+    if v_new.dtype != k_new.dtype or v_new.shape != k_new.shape:
+        raise ValueError("k_new and v_new must match in dtype and shape")
+    _need(k_cache, torch.int8, "k_cache")
+    _need(v_cache, torch.int8, "v_cache")
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    _need(block_table, torch.int32, "block_table")
+    _need(positions, torch.int32, "positions")
+    B, H, n, D = k_new.shape
+    _check(lib().sage_kv_cache_append(_ptr(k_new), _ptr(v_new), _dt(k_new.dtype), B, H, n, D,
+                                      _ptr(block_table), block_table.shape[1], _ptr(positions),
+                                      k_cache.shape[0], _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(k_scale), _ptr(v_scale), _stream(stream)))
 
 
 def decode_segments_used(max_context_len: int, num_segments: int) -> int:

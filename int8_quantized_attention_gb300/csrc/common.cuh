@@ -176,11 +176,17 @@ struct DT;
 template <>
 struct DT<__half> {
     static __device__ __forceinline__ float to_f(__half x) { return __half2float(x); }
+    static __device__ __forceinline__ float2 to_f2(uint32_t w) {
+        return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+    }
     static __device__ __forceinline__ __half from_f(float x) { return __float2half_rn(x); }
 };
 template <>
 struct DT<__nv_bfloat16> {
     static __device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+    static __device__ __forceinline__ float2 to_f2(uint32_t w) {
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w));
+    }
     static __device__ __forceinline__ __nv_bfloat16 from_f(float x) {
         return __float2bfloat16_rn(x);
     }

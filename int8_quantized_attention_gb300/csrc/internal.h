@@ -88,6 +88,19 @@ int decode_ctas_per_sm(int D);
 int decode_max_segment_pages();   // longest segment (in 16-token pages) one CTA takes
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t st, LaunchLog &log);
 
+struct KvAppendParams {
+    const void *k, *v;        // [B, H, n, D] f16/bf16 new rows
+    int bf16;
+    int B, H, n, D;
+    const int32_t *block_table, *pos;  // [B, max_blocks], [B]
+    int max_blocks, num_blocks;
+    int8_t *k_cache, *v_cache;         // [num_blocks, H, D/16, 16, 16]
+    float *k_scale, *v_scale;          // [num_blocks, H, 16]
+    int *err;
+};
+
+cudaError_t launch_kv_append(const KvAppendParams &p, cudaStream_t st, LaunchLog &log);
+
 struct PrefillParams {
     int B, Hq, Hkv, Sq, Sk, D, group;
     const int8_t *q;

@@ -1,0 +1,102 @@
+// KV producer step: quantise new key/value rows per (token, KV head) and
+// write them into the paged INT8 cache ("INT8 QK MMAC on gfx936 DCU",
+// section 4: s = max|x| / 127, codes round(x / s); section 3: token t of
+// sequence b sits in page block_table[b][t / 16], slot t % 16, channel c at
+// [page][kv_head][c / 16][slot][c % 16], its scale at [page][kv_head][slot]).
+//
+// One warp per row (K rows and V rows in one launch): each lane loads D/32
+// consecutive channels (one 4-16 byte vector), the row's amax comes from a
+// warp max-reduction, and each lane stores its codes as one vector into the
+// 16-channel group of the page slot.  Pages outside [0, num_blocks) and
+// positions outside the block table set the error word's bad-block bit and
+// the row is skipped.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sage {
+
+namespace {
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) kv_append_kernel(KvAppendParams p) {
+    constexpr int CPL = D / 32;  // channels per lane: 2, 4 or 8
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int64_t rows = (int64_t)p.B * p.H * p.n;
+    if (row >= 2 * rows) return;  // whole warp leaves together
+    const bool is_v = row >= rows;
+    const int64_t r = is_v ? row - rows : row;
+    const int64_t t = r % p.n, bh = r / p.n;
+    const int64_t b = bh / p.H, h = bh % p.H;
+    const int64_t pos = (int64_t)p.pos[b] + t;
+    const int64_t pi = pos >> 4;
+    int blk = -1;
+    if (pos >= 0 && pi < p.max_blocks) blk = p.block_table[b * p.max_blocks + pi];
+    if ((unsigned)blk >= (unsigned)p.num_blocks) {
+        if (lane == 0) atomicOr(p.err, kErrBadBlock);
+        return;
+    }
+    const T *src = static_cast<const T *>(is_v ? p.v : p.k) + r * D + lane * CPL;
+    float f[CPL];
+    if constexpr (CPL == 8) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(src);
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 v = DT<T>::to_f2(w[e]);
+            f[2 * e] = v.x, f[2 * e + 1] = v.y;
+        }
+    } else if constexpr (CPL == 4) {
+        const uint2 u = *reinterpret_cast<const uint2 *>(src);
+        const float2 a = DT<T>::to_f2(u.x), c = DT<T>::to_f2(u.y);
+        f[0] = a.x, f[1] = a.y, f[2] = c.x, f[3] = c.y;
+    } else {
+        const float2 a = DT<T>::to_f2(*reinterpret_cast<const uint32_t *>(src));
+        f[0] = a.x, f[1] = a.y;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) amax = fmaxf(amax, fabsf(f[e]));
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    uint32_t w[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < CPL; ++e)
+        w[e >> 2] |= (uint32_t)(uint8_t)quant_code(f[e], s) << (8 * (e & 3));
+    const int c0 = lane * CPL;
+    const int64_t slot = pos & 15;
+    const int64_t page = (int64_t)blk * p.H + h;
+    int8_t *dst = (is_v ? p.v_cache : p.k_cache) + page * D * 16 + (c0 >> 4) * 256 + slot * 16 +
+                  (c0 & 15);
+    if constexpr (CPL == 8)
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(w[0], w[1]);
+    else if constexpr (CPL == 4)
+        *reinterpret_cast<uint32_t *>(dst) = w[0];
+    else
+        *reinterpret_cast<uint16_t *>(dst) = (uint16_t)w[0];
+    if (lane == 0) (is_v ? p.v_scale : p.k_scale)[page * 16 + slot] = s;
+}
+
+template <typename T>
+cudaError_t launch_t(const KvAppendParams &p, cudaStream_t st, LaunchLog &log) {
+    const int64_t rows = 2 * (int64_t)p.B * p.H * p.n;
+    const int64_t grid = (rows + 7) / 8;
+    if (grid == 0) return cudaSuccess;
+    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    switch (p.D) {
+        case 64: kv_append_kernel<T, 64><<<(unsigned)grid, 256, 0, st>>>(p); break;
+        case 128: kv_append_kernel<T, 128><<<(unsigned)grid, 256, 0, st>>>(p); break;
+        case 256: kv_append_kernel<T, 256><<<(unsigned)grid, 256, 0, st>>>(p); break;
+        default: return cudaErrorInvalidValue;
+    }
+    log.add("kv_append_kernel", dim3((unsigned)grid), dim3(256), dim3(1, 1, 1), 0);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_kv_append(const KvAppendParams &p, cudaStream_t st, LaunchLog &log) {
+    return p.bf16 ? launch_t<__nv_bfloat16>(p, st, log) : launch_t<__half>(p, st, log);
+}
+
+}  // namespace sage
