@@ -52,6 +52,25 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(value: float, device="cpu") -> float:
+    """The largest of every rank's value (the slowest replica's time); the
+    value itself with one process."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, steps: int, max_ms: float) -> float:
+    """Whole-job throughput of N replicas: every rank's units over the
+    slowest rank's time (weak scaling), in units per second."""
+    return units_per_rank * world * steps / (max_ms * 1e-3)
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -215,13 +234,8 @@ def run_ours(args):
     clk.__exit__(None, None, None)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     kern_ms = [a.elapsed_time(b) for a, b in kev]
-    t_ms = sum(step_ms)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([t_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_ms = float(t.item())
-    value = sbytes * ws * args.steps / (t_ms * 1e-3) / 1e9
+    t_ms = max_over_ranks(sum(step_ms), device="cuda")
+    value = whole_job_rate(sbytes, ws, args.steps, t_ms) / 1e9
 
     # ---- end to end through the public API, host buffers
     e2e = None
