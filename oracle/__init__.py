@@ -337,3 +337,98 @@ def kv_append(x, block_table, positions, cache, scale):
     skipped = _lib().oracle_kv_append(_p(x), B, H, n, D, _p(bt), bt.shape[1], _p(pos),
                                       cache.shape[0], _p(cache), _p(scale))
     return cache, scale, int(skipped)
+
+
+# --------------------------------------------------------------------------
+# Variable-length packed batches ([P3] "Varlen per-batch loop" and the
+# batched varlen kernel its roadmap plans): sequence b occupies packed
+# tokens cu_seqlens[b] .. cu_seqlens[b+1]-1; it is sliced out and processed
+# as one single-sequence call, so quantisation groups, the smooth_k mean and
+# the causal alignment are all per sequence.
+# --------------------------------------------------------------------------
+
+def seq_bounds(cu_seqlens):
+    cu = np.asarray(cu_seqlens, np.int64)
+    return [(int(cu[b]), int(cu[b + 1])) for b in range(len(cu) - 1)]
+
+
+def quant_int8_varlen(x, cu_seqlens, block_tokens: int = 1, smooth: bool = False):
+    """Per-sequence INT8 quantisation of a packed batch.
+
+    x: float32 [total, H, D] (token-major, as packed batches are stored).
+    Returns (q int8 [H, total, D], scales: list over sequences of fp32
+    [H, ceil(len_b / block_tokens)], mu fp32 [B, H, D] or None).  An empty
+    sequence has no groups and a zero mean.
+    """
+    x = _c(x, np.float32)
+    total, H, D = x.shape
+    bounds = seq_bounds(cu_seqlens)
+    q = np.zeros((H, total, D), np.int8)
+    scales = []
+    mu = np.zeros((len(bounds), H, D), np.float32) if smooth else None
+    for b, (t0, t1) in enumerate(bounds):
+        if t1 == t0:
+            scales.append(np.zeros((H, 0), np.float32))
+            continue
+        xb = np.ascontiguousarray(x[t0:t1].transpose(1, 0, 2))   # [H, len, D]
+        qb, sb, mb = quant_int8(xb, block_tokens=block_tokens, smooth=smooth)
+        q[:, t0:t1] = qb
+        scales.append(sb)
+        if smooth:
+            mu[b] = mb
+    return q, scales, mu
+
+
+def row_bias_varlen(x, cu_seqlens, mu):
+    """b[h, t] = sum_c x[t, h, c] mu[b(t), h / (H / Hmu), c] in fp64.
+
+    x: [total, H, D]; mu: [B, Hmu, D].  Returns fp64 [H, total].
+    """
+    x = _c(x, np.float32)
+    mu = _c(mu, np.float32)
+    total, H, _ = x.shape
+    out = np.zeros((H, total), np.float64)
+    for b, (t0, t1) in enumerate(seq_bounds(cu_seqlens)):
+        if t1 > t0:
+            xb = np.ascontiguousarray(x[t0:t1].transpose(1, 0, 2))[None]
+            out[:, t0:t1] = row_bias(xb, mu[b:b + 1])[0]
+    return out
+
+
+def prefill_varlen(q_i8, q_scales, q_block, k_i8, k_scales, k_block, v, cu_seqlens_q,
+                   cu_seqlens_k, *, causal, sm_scale=None, q_bias=None, rows=None,
+                   threads=None):
+    """Prefill attention over a packed batch, one single-sequence call each.
+
+    q_i8 int8 [Hq, total_q, D]; q_scales list of fp32 [Hq, ceil(len_q_b / q_block)];
+    k_i8 int8 [Hkv, total_k, D]; k_scales list of fp32 [Hkv, ceil(len_k_b / k_block)];
+    v float [total_k, Hkv, D]; q_bias fp64 [Hq, total_q] or None (the
+    sequence's keys are smoothed); causal alignment bottom-right within
+    each sequence.  rows: optional list over sequences of row indices
+    (within the sequence) to evaluate; other rows stay NaN.
+    Returns (o fp64 [total_q, Hq, D], lse fp64 [Hq, total_q]).
+    """
+    q_i8 = np.asarray(q_i8)
+    Hq, total_q, D = q_i8.shape
+    o = np.full((total_q, Hq, D), np.nan)
+    lse = np.full((Hq, total_q), np.nan)
+    bq, bk = seq_bounds(cu_seqlens_q), seq_bounds(cu_seqlens_k)
+    for b, ((q0, q1), (k0, k1)) in enumerate(zip(bq, bk)):
+        if q1 == q0:
+            continue
+        if k1 == k0:
+            # no keys: nothing to attend to (zero output, empty sum)
+            sel = np.arange(q1 - q0) if rows is None else np.asarray(rows[b], np.int64)
+            o[q0 + sel] = 0.0
+            lse[:, q0 + sel] = -np.inf
+            continue
+        sel = None if rows is None else rows[b]
+        qb = None if q_bias is None else np.asarray(q_bias)[None, :, q0:q1]
+        ob, lb = prefill(q_i8[None, :, q0:q1], np.asarray(q_scales[b])[None], q_block,
+                         np.asarray(k_i8)[None, :, k0:k1], np.asarray(k_scales[b])[None], k_block,
+                         np.asarray(v)[k0:k1].transpose(1, 0, 2)[None], causal=causal,
+                         sm_scale=sm_scale, q_bias=qb, rows=sel, threads=threads)
+        idx = np.arange(q1 - q0) if sel is None else np.asarray(sel, np.int64)
+        o[q0 + idx] = ob[0].transpose(1, 0, 2)
+        lse[:, q0 + idx] = lb[0]
+    return o, lse

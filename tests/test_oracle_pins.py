@@ -27,9 +27,11 @@ def textbook_attention(q, k, v, sm_scale, causal=False, offset=0):
         j = np.arange(k.shape[0])[None, :]
         s = np.where(j <= i + offset, s, -np.inf)
     m = s.max(axis=1, keepdims=True)
-    p = np.exp(s - m)
-    l = p.sum(axis=1, keepdims=True)
-    return (p / l) @ v.astype(np.float64), (m + np.log(l))[:, 0]
+    with np.errstate(invalid="ignore", divide="ignore"):
+        # a row with every key masked has m = -inf: NaN output, -inf LSE
+        p = np.exp(s - m)
+        l = p.sum(axis=1, keepdims=True)
+        return (p / l) @ v.astype(np.float64), (m + np.log(l))[:, 0]
 
 
 def integer_rows(rng, n, d, amax=127):
@@ -441,3 +443,131 @@ def test_kv_append_error_bound_and_bad_pages():
             assert np.all(np.abs(codes * s - x[0, h, t]) <= s / 2 * (1 + 1e-6))
     untouched = [b for b in range(nblk) if b not in (2, 0)]
     assert not cache[untouched].any() and not scale[untouched].any()
+
+
+# --------------------------------------------------------------------------
+# variable-length packed batches: every sequence is its own problem
+# --------------------------------------------------------------------------
+
+def test_varlen_quant_groups_and_mean_are_per_sequence():
+    # two sequences (70 and 50 tokens) packed back to back; per-64-token
+    # groups.  Groups taken over the packed axis would put sequence 0's
+    # tokens 64..69 in one group with sequence 1's first 58 tokens (amax 100).
+    rng = np.random.default_rng(21)
+    H, D = 2, 64
+    cu = np.array([0, 70, 120])
+    x = np.zeros((120, H, D), np.float32)
+    x[0:64] = rng.uniform(-0.5, 0.5, (64, H, D))
+    x[0:64, :, 3] = 1.0
+    x[64:70] = rng.uniform(-0.25, 0.25, (6, H, D))
+    x[64:70, :, 5] = -0.5
+    x[70:120] = rng.uniform(-50, 50, (50, H, D))
+    x[70:120, :, 7] = 100.0
+    q, scales, _ = oracle.quant_int8_varlen(x, cu, block_tokens=64)
+    f = np.float32
+    assert scales[0].shape == (H, 2) and scales[1].shape == (H, 1)
+    assert np.all(scales[0][:, 0] == f(1.0) / f(127.0))
+    assert np.all(scales[0][:, 1] == f(0.5) / f(127.0))
+    assert np.all(scales[1][:, 0] == f(100.0) / f(127.0))
+    assert np.all(q[:, 0:64, 3] == 127) and np.all(q[:, 64:70, 5] == -127)
+    assert np.all(q[:, 70:120, 7] == 127)
+    # smooth: rows constant within a sequence -> the mean is that row, the
+    # smoothed rows are zero, codes and scales are zero
+    rows = np.array([0.25, -1.5, 3.0], np.float32)
+    cu3 = np.array([0, 5, 5, 12])      # the middle sequence is empty
+    x3 = np.zeros((12, 1, D), np.float32)
+    x3[0:5] = rows[0]
+    x3[5:12] = rows[2]
+    q3, s3, mu3 = oracle.quant_int8_varlen(x3, cu3, block_tokens=1, smooth=True)
+    assert np.all(mu3[0] == rows[0]) and np.all(mu3[1] == 0.0) and np.all(mu3[2] == rows[2])
+    assert np.all(q3 == 0) and all(np.all(s == 0) for s in s3)
+    assert s3[1].shape == (1, 0)
+
+
+def _varlen_case(rng, lq, lk, Hq, Hkv, D):
+    cu_q = np.concatenate([[0], np.cumsum(lq)])
+    cu_k = np.concatenate([[0], np.cumsum(lk)])
+    q = np.stack([integer_rows(rng, cu_q[-1], D) for _ in range(Hq)])   # [Hq, tq, D]
+    k = np.stack([integer_rows(rng, cu_k[-1], D) for _ in range(Hkv)])
+    return cu_q, cu_k, q, k
+
+
+def test_varlen_prefill_equals_textbook_per_sequence():
+    # integer Q/K with per-token amax 127: quantisation is the identity, so
+    # every sequence's rows equal exact float64 attention over its own keys
+    rng = np.random.default_rng(22)
+    lq, lk = [5, 0, 9, 3], [7, 4, 9, 1]
+    Hq, Hkv, D = 4, 2, 64
+    cu_q, cu_k, q, k = _varlen_case(rng, lq, lk, Hq, Hkv, D)
+    v = rng.standard_normal((cu_k[-1], Hkv, D))
+    sm = 1.0 / 4096
+    qs = [np.ones((Hq, n), np.float32) for n in lq]
+    ks = [np.ones((Hkv, n), np.float32) for n in lk]
+    for causal in (False, True):
+        o, lse = oracle.prefill_varlen(q.astype(np.int8), qs, 1, k.astype(np.int8), ks, 1, v,
+                                       cu_q, cu_k, causal=causal, sm_scale=sm)
+        for b in range(len(lq)):
+            for h in range(Hq):
+                g = h // (Hq // Hkv)
+                qq = q[h, cu_q[b]:cu_q[b + 1]]
+                if len(qq) == 0:
+                    continue
+                ref_o, ref_l = textbook_attention(qq, k[g, cu_k[b]:cu_k[b + 1]],
+                                                  v[cu_k[b]:cu_k[b + 1], g], sm, causal,
+                                                  lk[b] - lq[b])
+                got_o = o[cu_q[b]:cu_q[b + 1], h]
+                got_l = lse[h, cu_q[b]:cu_q[b + 1]]
+                fin = np.isfinite(ref_l)
+                np.testing.assert_allclose(got_o[fin], ref_o[fin], rtol=1e-9, atol=1e-12)
+                np.testing.assert_allclose(got_l[fin], ref_l[fin], rtol=1e-12)
+                assert np.all(np.isneginf(got_l[~fin])) and np.all(got_o[~fin] == 0)
+
+
+def test_varlen_causal_alignment_closed_form():
+    # K codes 0: every visible key scores 0, so row i of sequence b averages
+    # the visible keys' values v_j = j: o = (n - 1) / 2 and lse = ln n with
+    # n = min(Sk_b, i + Sk_b - Sq_b + 1) (bottom-right alignment per sequence)
+    lq, lk = [6, 4, 8], [3, 10, 8]
+    Hq, Hkv, D = 2, 1, 64
+    cu_q = np.concatenate([[0], np.cumsum(lq)])
+    cu_k = np.concatenate([[0], np.cumsum(lk)])
+    rng = np.random.default_rng(23)
+    q = rng.integers(-127, 128, (Hq, cu_q[-1], D)).astype(np.int8)
+    k = np.zeros((Hkv, cu_k[-1], D), np.int8)
+    v = np.zeros((cu_k[-1], Hkv, D))
+    for b in range(3):
+        v[cu_k[b]:cu_k[b + 1]] = np.arange(lk[b])[:, None, None]
+    qs = [rng.uniform(0.01, 0.02, (Hq, n)).astype(np.float32) for n in lq]
+    ks = [rng.uniform(0.01, 0.02, (Hkv, n)).astype(np.float32) for n in lk]
+    o, lse = oracle.prefill_varlen(q, qs, 1, k, ks, 1, v, cu_q, cu_k, causal=True)
+    for b in range(3):
+        for i in range(lq[b]):
+            n = min(lk[b], i + lk[b] - lq[b] + 1)
+            t = cu_q[b] + i
+            if n <= 0:
+                assert np.all(o[t] == 0) and np.all(np.isneginf(lse[:, t]))
+            else:
+                np.testing.assert_allclose(o[t], (n - 1) / 2.0, rtol=0, atol=1e-12)
+                np.testing.assert_allclose(lse[:, t], math.log(n), rtol=1e-14)
+
+
+def test_varlen_values_never_leak_across_sequences():
+    # V constant per sequence: softmax rows sum to 1, so every output row of
+    # sequence b equals that sequence's constant, whatever the scores
+    rng = np.random.default_rng(24)
+    lq, lk = [33, 17, 50], [40, 17, 64]
+    Hq, Hkv, D = 2, 2, 64
+    cu_q = np.concatenate([[0], np.cumsum(lq)])
+    cu_k = np.concatenate([[0], np.cumsum(lk)])
+    x_q = rng.standard_normal((cu_q[-1], Hq, D)).astype(np.float32)
+    x_k = (rng.standard_normal((cu_k[-1], Hkv, D)) * 3).astype(np.float32)
+    q, qs, _ = oracle.quant_int8_varlen(x_q, cu_q, block_tokens=1)
+    k, ks, _ = oracle.quant_int8_varlen(x_k, cu_k, block_tokens=1)
+    consts = [1.5, -2.0, 0.75]
+    v = np.zeros((cu_k[-1], Hkv, D))
+    for b in range(3):
+        v[cu_k[b]:cu_k[b + 1]] = consts[b]
+    for causal in (False, True):
+        o, _ = oracle.prefill_varlen(q, qs, 1, k, ks, 1, v, cu_q, cu_k, causal=causal)
+        for b in range(3):
+            np.testing.assert_allclose(o[cu_q[b]:cu_q[b + 1]], consts[b], rtol=1e-13)
