@@ -60,7 +60,7 @@ typedef enum sage_dtype {
 const char *sage_get_last_error_message(void);
 
 /* Library ABI version (increments on any signature change). */
-int sage_version(void);   /* 4 */
+int sage_version(void);   /* 5 */
 
 /* --------------------------------------------------------------------------
  * Quantisation  ([P1] section 4; [P3] quant kernel table, feature matrix)
@@ -92,6 +92,44 @@ sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B, int H, i
                               int block_tokens, int smooth, const float *mu_in, int mu_heads,
                               int8_t *x_int8, float *scale, float *mu_out, float *bias_out,
                               void *stream);
+
+/* --------------------------------------------------------------------------
+ * Variable-length packed batches  ([P3] "Varlen per-batch loop": each
+ * sequence of a packed batch is sliced out and processed as one
+ * single-sequence call; the roadmap's batched varlen kernel is what the
+ * calls below provide, one launch for the whole batch)
+ *
+ * Sequence b holds packed tokens cu_seqlens[b] .. cu_seqlens[b+1]-1
+ * (cu_seqlens: int32 [B+1] device array, cu_seqlens[0] >= 0,
+ * non-decreasing, cu_seqlens[B] <= total, each length <= the caller's
+ * max_seqlen).  Packed tokens outside every sequence are not read or
+ * written.  A sequence that breaks these rules sets the bad-block bit of
+ * the device error word and is treated as empty.
+ *
+ * Scale groups: per token (block_tokens == 1) group = packed token; per
+ * block, sequence b's groups start at cu_seqlens[b] / block_tokens + b and
+ * cover its own tokens only (ceil(len / block_tokens) groups; one unused
+ * slot per sequence at most, holding 0).  sage_varlen_scale_groups() gives
+ * the groups per head: total (per token) or total / block_tokens + B.
+ *
+ * sage_quant_int8_varlen: the rule of sage_quant_int8, per sequence.
+ *   x        : f16/bf16 [total, H, D] through element strides (stride_t
+ *              between tokens, stride_h between heads), channels contiguous,
+ *              16-byte aligned, strides multiples of 8.
+ *   x_int8   : int8 [H, total, D].   scale: fp32 [H, groups].
+ *   smooth   : mu_out fp32 [B, H, D] = each sequence's own token mean (0 for
+ *              an empty sequence), subtracted before quantising.
+ *   mu_in    : optional fp32 [B, mu_heads, D]; bias_out fp32 [H, total] =
+ *              sum_c x[t,h,c] * mu_in[b(t), h / (H / mu_heads), c].
+ * ------------------------------------------------------------------------ */
+int64_t sage_varlen_scale_groups(int64_t total, int B, int block_tokens);
+
+sage_status_t sage_quant_int8_varlen(const void *x, sage_dtype_t dtype, int B, int H,
+                                     int64_t total, int D, int64_t stride_h, int64_t stride_t,
+                                     const int32_t *cu_seqlens, int max_seqlen, int block_tokens,
+                                     int smooth, const float *mu_in, int mu_heads,
+                                     int8_t *x_int8, float *scale, float *mu_out,
+                                     float *bias_out, void *stream);
 
 /* --------------------------------------------------------------------------
  * Paged INT8 K/V cache  ([P1] section 3)
@@ -300,6 +338,58 @@ sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *workspace
                                 size_t workspace_bytes, void *stream);
 
 /* --------------------------------------------------------------------------
+ * Varlen prefill  ([P3] "Varlen per-batch loop" and roadmap; the attention
+ * itself is sage_attn_prefill's, per sequence)
+ *
+ * For every sequence b: its queries (cu_seqlens_q) attend to its keys
+ * (cu_seqlens_k) exactly as sage_attn_prefill with B = 1 and no prefix
+ * would, including the per-score scale recovery, the smooth_k bias and the
+ * bottom-right causal alignment j <= i + (Sk_b - Sq_b).  A sequence with
+ * queries and no keys gets out = 0 and lse = -inf.  One staging launch and
+ * one attention launch cover the whole batch.
+ *   q       : int8 [Hq, total_q, D] (sage_quant_int8_varlen),
+ *   q_scale : fp32 [Hq, sage_varlen_scale_groups(total_q, B, q_block)],
+ *   k       : int8 [Hkv, total_k, D], k_scale likewise with k_block,
+ *   v       : f16/bf16 [total_k, Hkv, D] through element strides
+ *             (v_stride_t, v_stride_h; 0 selects the dense packing),
+ *             multiples of 8, 16-byte aligned,
+ *   q_bias  : optional fp32 [Hq, total_q] (the sequences' keys are smoothed),
+ *   out     : [total_q, Hq, D] (16-byte aligned), lse: optional fp32 [Hq, total_q].
+ * B <= 65535.  D, q_block, k_block, dtypes and sm_scale as in sage_attn_prefill.
+ * ------------------------------------------------------------------------ */
+typedef struct sage_prefill_varlen_args {
+    int B, Hq, Hkv, D;
+    int64_t total_q, total_k;       /* packed query / key tokens */
+    int max_seqlen_q, max_seqlen_k; /* host bounds on the sequences' lengths */
+    const int32_t *cu_seqlens_q;    /* [B + 1] device */
+    const int32_t *cu_seqlens_k;    /* [B + 1] device */
+    const int8_t *q;
+    const float *q_scale;
+    int q_block;
+    const int8_t *k;
+    const float *k_scale;
+    int k_block;
+    const void *v;
+    sage_dtype_t v_dtype;
+    int64_t v_stride_t, v_stride_h;
+    const float *q_bias;
+    int causal;
+    float sm_scale;                 /* <= 0 selects 1/sqrt(D) */
+    void *out;
+    sage_dtype_t out_dtype;
+    float *lse;
+} sage_prefill_varlen_args_t;
+
+/* Workspace bytes of sage_attn_prefill_varlen (host only): the f16 copy of
+ * every sequence's keys and values, each padded to whole key tiles. */
+size_t sage_attn_prefill_varlen_workspace_size(const sage_prefill_varlen_args_t *args);
+
+/* workspace: at least sage_attn_prefill_varlen_workspace_size() bytes,
+ * 256-byte aligned; overwritten by the call. */
+sage_status_t sage_attn_prefill_varlen(const sage_prefill_varlen_args_t *args, void *workspace,
+                                       size_t workspace_bytes, void *stream);
+
+/* --------------------------------------------------------------------------
  * Test hooks: raw INT32 scores through the same device tile paths
  * ([P1] section 7, layer 1: check the lane/fragment mapping of the raw
  * accumulators).
@@ -312,6 +402,12 @@ sage_status_t sage_attn_prefill(const sage_prefill_args_t *args, void *workspace
 sage_status_t sage_debug_prefill_qk_int32(const sage_prefill_args_t *args, void *workspace,
                                           size_t workspace_bytes, int32_t *scores,
                                           void *stream);
+/* sage_debug_prefill_varlen_qk_int32: the same for a packed batch;
+ *   scores[h, t, j] (int32 [Hq, total_q, max_seqlen_k]) for query token t
+ *   and key j of t's sequence. */
+sage_status_t sage_debug_prefill_varlen_qk_int32(const sage_prefill_varlen_args_t *args,
+                                                 void *workspace, size_t workspace_bytes,
+                                                 int32_t *scores, void *stream);
 sage_status_t sage_debug_decode_qk_int32(const sage_decode_args_t *args, void *workspace,
                                          size_t workspace_bytes, int32_t *scores, void *stream);
 

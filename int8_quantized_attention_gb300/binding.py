@@ -58,6 +58,17 @@ class PrefillArgs(ctypes.Structure):
                 ("causal", _i), ("sm_scale", _f), ("out", _vp), ("out_dtype", _i), ("lse", _vp)]
 
 
+class PrefillVarlenArgs(ctypes.Structure):
+    _fields_ = [("B", _i), ("Hq", _i), ("Hkv", _i), ("D", _i), ("total_q", _i64), ("total_k", _i64),
+                ("max_seqlen_q", _i), ("max_seqlen_k", _i),
+                ("cu_seqlens_q", _vp), ("cu_seqlens_k", _vp),
+                ("q", _vp), ("q_scale", _vp), ("q_block", _i),
+                ("k", _vp), ("k_scale", _vp), ("k_block", _i),
+                ("v", _vp), ("v_dtype", _i), ("v_stride_t", _i64), ("v_stride_h", _i64),
+                ("q_bias", _vp), ("causal", _i), ("sm_scale", _f), ("out", _vp), ("out_dtype", _i),
+                ("lse", _vp)]
+
+
 class LaunchInfo(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_char * 64), ("grid", _i * 3), ("block", _i * 3),
                 ("cluster", _i * 3), ("smem_bytes", _i), ("num_segments", _i), ("launches", _i)]
@@ -84,6 +95,19 @@ def lib():
         L.sage_quant_int8.argtypes = [_vp, _i, _i, _i, _i, _i, _i64, _i64, _i64, _i, _i, _vp, _i,
                                       _vp, _vp, _vp, _vp, _vp]
         L.sage_quant_int8.restype = _i
+        L.sage_varlen_scale_groups.argtypes = [_i64, _i, _i]
+        L.sage_varlen_scale_groups.restype = _i64
+        L.sage_quant_int8_varlen.argtypes = [_vp, _i, _i, _i, _i64, _i, _i64, _i64, _vp, _i, _i,
+                                             _i, _vp, _i, _vp, _vp, _vp, _vp, _vp]
+        L.sage_quant_int8_varlen.restype = _i
+        L.sage_attn_prefill_varlen_workspace_size.argtypes = [ctypes.POINTER(PrefillVarlenArgs)]
+        L.sage_attn_prefill_varlen_workspace_size.restype = ctypes.c_size_t
+        L.sage_attn_prefill_varlen.argtypes = [ctypes.POINTER(PrefillVarlenArgs), _vp,
+                                               ctypes.c_size_t, _vp]
+        L.sage_attn_prefill_varlen.restype = _i
+        L.sage_debug_prefill_varlen_qk_int32.argtypes = [ctypes.POINTER(PrefillVarlenArgs), _vp,
+                                                         ctypes.c_size_t, _vp, _vp]
+        L.sage_debug_prefill_varlen_qk_int32.restype = _i
         L.sage_decode_num_segments.argtypes = [_i, _i, _i, _i, _i]
         L.sage_decode_num_segments.restype = _i
         L.sage_attn_decode_workspace_size.argtypes = [_i, _i, _i, _i]
@@ -415,6 +439,106 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
                                                  _ptr(debug_scores), _stream(stream)))
     else:
         _check(lib().sage_attn_prefill(ctypes.byref(a), _ptr(workspace), wsb, _stream(stream)))
+    return (out, lse) if return_lse else out
+
+
+# --------------------------------------------------------------------------
+# Variable-length packed batches (sequence b = packed tokens
+# cu_seqlens[b] .. cu_seqlens[b+1]-1)
+# --------------------------------------------------------------------------
+
+def varlen_scale_groups(total: int, B: int, block_tokens: int) -> int:
+    """Scale groups per head of a packed batch (see sage_quant_int8_varlen)."""
+    return int(lib().sage_varlen_scale_groups(int(total), int(B), int(block_tokens)))
+
+
+def sage_quant_int8_varlen(x: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen: int,
+                           block_tokens: int = 1, smooth: bool = False,
+                           mu_in: Optional[torch.Tensor] = None, stream=None):
+    """Per-sequence INT8 quantisation of a packed batch x [total, H, D].
+
+    Returns (x_int8 [H, total, D], scale [H, groups], mu [B, H, D] when
+    smooth, bias [H, total] when mu_in [B, Hmu, D] is given).
+    """
+    total, H, D = x.shape
+    if x.stride(2) != 1:
+        raise ValueError("channel dimension must be contiguous")
+    _need(cu_seqlens, torch.int32, "cu_seqlens")
+    B = cu_seqlens.numel() - 1
+    dev = x.device
+    G = varlen_scale_groups(total, B, block_tokens)
+    q = torch.empty((H, total, D), dtype=torch.int8, device=dev)
+    scale = torch.empty((H, G), dtype=torch.float32, device=dev)
+    mu = torch.empty((B, H, D), dtype=torch.float32, device=dev) if smooth else None
+    bias = None
+    mu_heads = 0
+    if mu_in is not None:
+        _need(mu_in, torch.float32, "mu_in")
+        mu_heads = mu_in.shape[1]
+        bias = torch.empty((H, total), dtype=torch.float32, device=dev)
+    _check(lib().sage_quant_int8_varlen(_ptr(x), _dt(x.dtype), B, H, total, D, x.stride(1),
+                                        x.stride(0), _ptr(cu_seqlens), int(max_seqlen),
+                                        block_tokens, int(bool(smooth)), _ptr(mu_in), mu_heads,
+                                        _ptr(q), _ptr(scale), _ptr(mu), _ptr(bias),
+                                        _stream(stream)))
+    return q, scale, mu, bias
+
+
+def sage_attn_prefill_varlen(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: int, v,
+                             cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, *,
+                             causal: bool, sm_scale=None, q_bias=None, out_dtype=None,
+                             return_lse: bool = False, debug_scores=None,
+                             workspace: Optional[torch.Tensor] = None, stream=None):
+    """INT8-QK prefill attention over a packed variable-length batch.
+
+    q_int8 [Hq, total_q, D]; q_scale [Hq, groups_q]; k_int8 [Hkv, total_k, D];
+    k_scale [Hkv, groups_k] (sage_quant_int8_varlen layouts); v [total_k, Hkv, D]
+    f16/bf16 (channels contiguous); q_bias [Hq, total_q] or None.
+    Returns out [total_q, Hq, D] (and lse [Hq, total_q]).
+    """
+    Hq, total_q, D = q_int8.shape
+    Hkv, total_k = k_int8.shape[0], k_int8.shape[1]
+    _need(q_int8, torch.int8, "q_int8")
+    _need(k_int8, torch.int8, "k_int8")
+    _need(q_scale, torch.float32, "q_scale")
+    _need(k_scale, torch.float32, "k_scale")
+    _need(cu_seqlens_q, torch.int32, "cu_seqlens_q")
+    _need(cu_seqlens_k, torch.int32, "cu_seqlens_k")
+    if v.stride(2) != 1:
+        raise ValueError("v channel dimension must be contiguous")
+    B = cu_seqlens_q.numel() - 1
+    if cu_seqlens_k.numel() != B + 1:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k describe different batch sizes")
+    out_dtype = out_dtype or v.dtype
+    dev = q_int8.device
+    out = torch.empty((total_q, Hq, D), dtype=out_dtype, device=dev)
+    lse = torch.empty((Hq, total_q), dtype=torch.float32, device=dev) if return_lse else None
+    a = PrefillVarlenArgs()
+    a.B, a.Hq, a.Hkv, a.D = B, Hq, Hkv, D
+    a.total_q, a.total_k = total_q, total_k
+    a.max_seqlen_q, a.max_seqlen_k = int(max_seqlen_q), int(max_seqlen_k)
+    a.cu_seqlens_q, a.cu_seqlens_k = _ptr(cu_seqlens_q), _ptr(cu_seqlens_k)
+    a.q, a.q_scale, a.q_block = _ptr(q_int8), _ptr(q_scale), q_block
+    a.k, a.k_scale, a.k_block = _ptr(k_int8), _ptr(k_scale), k_block
+    a.v, a.v_dtype = _ptr(v), _dt(v.dtype)
+    a.v_stride_t, a.v_stride_h = v.stride(0), v.stride(1)
+    if q_bias is not None:
+        _need(q_bias, torch.float32, "q_bias")
+    a.q_bias = _ptr(q_bias)
+    a.causal = int(bool(causal))
+    a.sm_scale = float(sm_scale) if sm_scale else 0.0
+    a.out, a.out_dtype, a.lse = _ptr(out), _dt(out_dtype), _ptr(lse)
+    need = int(lib().sage_attn_prefill_varlen_workspace_size(ctypes.byref(a)))
+    if workspace is None or workspace.numel() * workspace.element_size() < need:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+    wsb = workspace.numel() * workspace.element_size()
+    if debug_scores is not None:
+        _need(debug_scores, torch.int32, "debug_scores")
+        _check(lib().sage_debug_prefill_varlen_qk_int32(ctypes.byref(a), _ptr(workspace), wsb,
+                                                        _ptr(debug_scores), _stream(stream)))
+    else:
+        _check(lib().sage_attn_prefill_varlen(ctypes.byref(a), _ptr(workspace), wsb,
+                                              _stream(stream)))
     return (out, lse) if return_lse else out
 
 

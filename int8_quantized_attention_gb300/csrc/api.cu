@@ -112,7 +112,7 @@ void record_launch(const LaunchLog &log) { g_last = log; }
 
 SAGE_API const char *sage_get_last_error_message(void) { return g_msg.c_str(); }
 
-SAGE_API int sage_version(void) { return 4; }
+SAGE_API int sage_version(void) { return 5; }
 
 SAGE_API sage_status_t sage_last_launch_info(sage_launch_info_t *info) {
     if (!info) return fail(SAGE_ERR_INVALID_ARG, "info is NULL");
@@ -207,6 +207,69 @@ SAGE_API sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B,
     p.bias = mu_in ? bias_out : nullptr;
     cudaError_t e = sage::launch_quant(p, static_cast<cudaStream_t>(stream), g_last);
     return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "quant launch");
+}
+
+SAGE_API int64_t sage_varlen_scale_groups(int64_t total, int B, int block_tokens) {
+    if (total < 0 || B < 0 || block_tokens < 1) return 0;
+    return block_tokens == 1 ? total : total / block_tokens + B;
+}
+
+SAGE_API sage_status_t sage_quant_int8_varlen(const void *x, sage_dtype_t dtype, int B, int H,
+                                              int64_t total, int D, int64_t stride_h,
+                                              int64_t stride_t, const int32_t *cu_seqlens,
+                                              int max_seqlen, int block_tokens, int smooth,
+                                              const float *mu_in, int mu_heads, int8_t *x_int8,
+                                              float *scale, float *mu_out, float *bias_out,
+                                              void *stream) {
+    if (dtype != SAGE_F16 && dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "x dtype must be f16 or bf16");
+    if (!head_dim_ok(D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", D);
+    if (B < 0 || H < 0 || total < 0 || max_seqlen < 0)
+        return fail(SAGE_ERR_INVALID_ARG, "negative shape");
+    if (block_tokens < 1 || block_tokens > 1024)
+        return fail(SAGE_ERR_INVALID_ARG, "block_tokens %d outside [1, 1024]", block_tokens);
+    g_last = sage::LaunchLog();
+    if ((int64_t)B * H == 0 || total == 0) return SAGE_OK;
+    if (!x || !x_int8 || !scale || !cu_seqlens)
+        return fail(SAGE_ERR_INVALID_ARG, "x, x_int8, scale and cu_seqlens are required");
+    if (!aligned(x, 16)) return fail(SAGE_ERR_INVALID_ARG, "x must be 16-byte aligned");
+    if (!aligned(x_int8, 8)) return fail(SAGE_ERR_INVALID_ARG, "x_int8 must be 8-byte aligned");
+    if (stride_h % 8 || stride_t % 8)
+        return fail(SAGE_ERR_INVALID_ARG, "strides must be multiples of 8 elements");
+    if (smooth && !mu_out) return fail(SAGE_ERR_INVALID_ARG, "smooth needs mu_out");
+    if (smooth && (int64_t)B * H > 65535)
+        return fail(SAGE_ERR_UNSUPPORTED, "smooth supports at most 65535 (sequence, head) pairs");
+    if (mu_in) {
+        if (!bias_out) return fail(SAGE_ERR_INVALID_ARG, "mu_in needs bias_out");
+        if (mu_heads < 1 || H % mu_heads)
+            return fail(SAGE_ERR_INVALID_ARG, "H (%d) must be a multiple of mu_heads (%d)", H,
+                        mu_heads);
+    }
+    const int64_t groups = sage_varlen_scale_groups(total, B, block_tokens);
+    if ((int64_t)H * groups > 0x7fffffffll)
+        return fail(SAGE_ERR_UNSUPPORTED, "too many scale groups");
+    int *ew = nullptr;
+    sage_status_t st = error_word(&ew);
+    if (st != SAGE_OK) return st;
+    sage::QuantParams p = {};
+    p.x = x;
+    p.bf16 = dtype == SAGE_BF16;
+    p.B = B, p.H = H, p.S = max_seqlen, p.D = D;
+    p.sb = 0, p.sh = stride_h, p.ss = stride_t;
+    p.block = block_tokens;
+    p.smooth = smooth;
+    p.mu_bias = mu_in;
+    p.mu_heads = mu_in ? mu_heads : 1;
+    p.q = x_int8;
+    p.scale = scale;
+    p.mu_out = mu_out;
+    p.bias = mu_in ? bias_out : nullptr;
+    p.cu = cu_seqlens;
+    p.total = total;
+    p.groups = groups;
+    p.err = ew;
+    cudaError_t e = sage::launch_quant(p, static_cast<cudaStream_t>(stream), g_last);
+    return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "varlen quant launch");
 }
 
 // ---------------------------------------------------------------- combine
@@ -535,6 +598,116 @@ SAGE_API sage_status_t sage_debug_prefill_qk_int32(const sage_prefill_args_t *ar
                                                    int32_t *scores, void *stream) {
     if (!scores) return fail(SAGE_ERR_INVALID_ARG, "scores is NULL");
     return run_prefill(args, workspace, workspace_bytes, scores, stream);
+}
+
+// --------------------------------------------------------- varlen prefill
+
+static sage_status_t check_prefill_varlen(const sage_prefill_varlen_args_t *a, int *qs_out,
+                                          int *ks_out) {
+    if (!a) return fail(SAGE_ERR_INVALID_ARG, "args is NULL");
+    if (!head_dim_ok(a->D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", a->D);
+    if (a->out_dtype != SAGE_F16 && a->out_dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "out dtype must be f16 or bf16");
+    if (a->v_dtype != SAGE_F16 && a->v_dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "v dtype must be f16 or bf16");
+    if (a->B < 0 || a->B > 65535 || a->Hq < 1 || a->Hq > 65535 || a->Hkv < 1 ||
+        a->Hq % a->Hkv || a->total_q < 0 || a->total_k < 0 || a->max_seqlen_q < 0 ||
+        a->max_seqlen_k < 0)
+        return fail(SAGE_ERR_INVALID_ARG, "bad shape (B=%d Hq=%d Hkv=%d total_q=%lld total_k=%lld)",
+                    a->B, a->Hq, a->Hkv, (long long)a->total_q, (long long)a->total_k);
+    const int qs = a->q_block == 1 ? 0 : ilog2_exact(a->q_block);
+    const int ks = a->k_block == 1 ? 0 : ilog2_exact(a->k_block);
+    if (qs < 0 || (a->q_block != 1 && a->q_block < 128))
+        return fail(SAGE_ERR_UNSUPPORTED, "q_block must be 1 or a power of two >= 128");
+    if (ks < 0 || (a->k_block != 1 && a->k_block < 64))
+        return fail(SAGE_ERR_UNSUPPORTED, "k_block must be 1 or a power of two >= 64");
+    const int BN = a->D == 256 ? 64 : 128;
+    if (a->total_k + (int64_t)a->B * (BN + 4) + 16 > 0x7fffffffll ||
+        (int64_t)a->Hkv * a->total_k > 0x7fffffffffffll)
+        return fail(SAGE_ERR_UNSUPPORTED, "packed key count too large");
+    *qs_out = qs;
+    *ks_out = ks;
+    return SAGE_OK;
+}
+
+SAGE_API size_t sage_attn_prefill_varlen_workspace_size(const sage_prefill_varlen_args_t *a) {
+    int qs = 0, ks = 0;
+    if (check_prefill_varlen(a, &qs, &ks) != SAGE_OK) return 0;
+    return sage::prefill_layout_varlen(a->B, a->Hkv, a->total_k, a->D).bytes;
+}
+
+static sage_status_t run_prefill_varlen(const sage_prefill_varlen_args_t *a, void *workspace,
+                                        size_t workspace_bytes, int32_t *dbg, void *stream) {
+    int qs = 0, ks = 0;
+    sage_status_t cs = check_prefill_varlen(a, &qs, &ks);
+    if (cs != SAGE_OK) return cs;
+    g_last = sage::LaunchLog();
+    if ((int64_t)a->B * a->total_q * a->max_seqlen_q == 0) return SAGE_OK;
+    if (!a->cu_seqlens_q || !a->cu_seqlens_k)
+        return fail(SAGE_ERR_INVALID_ARG, "cu_seqlens_q and cu_seqlens_k are required");
+    if (!a->q || !a->q_scale || !a->out) return fail(SAGE_ERR_INVALID_ARG, "q, q_scale, out required");
+    if (a->total_k > 0 && (!a->k || !a->k_scale || !a->v))
+        return fail(SAGE_ERR_INVALID_ARG, "k, k_scale and v are required when total_k > 0");
+    const int64_t vst = a->v_stride_t ? a->v_stride_t : (int64_t)a->Hkv * a->D;
+    const int64_t vsh = a->v_stride_h ? a->v_stride_h : a->D;
+    if (vst % 8 || vsh % 8) return fail(SAGE_ERR_INVALID_ARG, "v strides must be multiples of 8");
+    if (!aligned(a->q, 16) || (a->k && !aligned(a->k, 16)) || (a->v && !aligned(a->v, 16)) ||
+        !aligned(a->out, 16))
+        return fail(SAGE_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    const sage::PrefillLayout L = sage::prefill_layout_varlen(a->B, a->Hkv, a->total_k, a->D);
+    if (!workspace || workspace_bytes < L.bytes)
+        return fail(SAGE_ERR_INVALID_ARG, "workspace too small: need %zu bytes", L.bytes);
+    if (!aligned(workspace, 256)) return fail(SAGE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+    int *ew = nullptr;
+    sage_status_t st = error_word(&ew);
+    if (st != SAGE_OK) return st;
+    sage::PrefillParams p = {};
+    p.B = a->B, p.Hq = a->Hq, p.Hkv = a->Hkv, p.D = a->D;
+    p.Sq = a->max_seqlen_q, p.Sk = a->max_seqlen_k;
+    p.group = a->Hq / a->Hkv;
+    p.q = a->q, p.q_scale = a->q_scale, p.q_shift = qs;
+    p.q_groups = (int)sage_varlen_scale_groups(a->total_q, a->B, a->q_block);
+    p.k = a->k, p.k_scale = a->k_scale, p.k_shift = ks;
+    p.k_groups = (int)sage_varlen_scale_groups(a->total_k, a->B, a->k_block);
+    p.v = a->v, p.v_bf16 = a->v_dtype == SAGE_BF16;
+    p.q_bias = a->q_bias;
+    p.causal = a->causal != 0;
+    const float sm = a->sm_scale > 0.0f ? a->sm_scale : 1.0f / sqrtf((float)a->D);
+    p.qk_scale_log2 = sm * 1.4426950408889634f;
+    p.out = a->out, p.out_bf16 = a->out_dtype == SAGE_BF16, p.lse = a->lse;
+    p.dbg = dbg;
+    p.dbg_stride = a->max_seqlen_k;
+    p.err = ew;
+    p.cu_q = a->cu_seqlens_q, p.cu_k = a->cu_seqlens_k;
+    p.total_q = a->total_q, p.total_k = a->total_k;
+    p.v_st = vst, p.v_sh = vsh;
+    char *w = static_cast<char *>(workspace);
+    p.BN = L.BN, p.Ppad = 0, p.Lpad = L.Lpad, p.Vrows = L.Vrows;
+    p.k_ws = reinterpret_cast<__half *>(w + L.off_k);
+    p.v_ws = reinterpret_cast<__half *>(w + L.off_v);
+    p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);
+    cudaStream_t cst = static_cast<cudaStream_t>(stream);
+    sage::LaunchLog stage_log;
+    cudaError_t e = sage::launch_prefill_stage(p, cst, stage_log);
+    if (e != cudaSuccess) return cuda_fail(e, "varlen prefill staging launch");
+    e = sage::launch_prefill(p, cst, g_last);
+    g_last.count += stage_log.count;
+    if (e == cudaErrorNotSupported)
+        return fail(SAGE_ERR_UNSUPPORTED, "prefill configuration not supported by this build");
+    return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "varlen prefill launch");
+}
+
+SAGE_API sage_status_t sage_attn_prefill_varlen(const sage_prefill_varlen_args_t *args,
+                                                void *workspace, size_t workspace_bytes,
+                                                void *stream) {
+    return run_prefill_varlen(args, workspace, workspace_bytes, nullptr, stream);
+}
+
+SAGE_API sage_status_t sage_debug_prefill_varlen_qk_int32(const sage_prefill_varlen_args_t *args,
+                                                          void *workspace, size_t workspace_bytes,
+                                                          int32_t *scores, void *stream) {
+    if (!scores) return fail(SAGE_ERR_INVALID_ARG, "scores is NULL");
+    return run_prefill_varlen(args, workspace, workspace_bytes, scores, stream);
 }
 
 // ---------------------------------------------------------------- kv append

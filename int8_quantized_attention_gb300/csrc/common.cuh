@@ -13,6 +13,54 @@ namespace sage {
 constexpr int kErrTimeout = 1;
 constexpr int kErrBadBlock = 2;
 
+// ------------------------------------------------ variable-length batches
+// Sequence b of a packed batch holds packed tokens [cu[b], cu[b+1]).  A
+// range outside [0, total], running backwards or longer than the caller's
+// bound max_len sets the bad-block bit of *err (when err is given) and is
+// treated as an empty sequence.
+__device__ __forceinline__ int varlen_seq(const int32_t *cu, int b, int max_len, int64_t total,
+                                          int *err, int64_t *start) {
+    const int64_t a = cu[b], e = cu[b + 1];
+    if (a < 0 || e < a || e > total || e - a > max_len) {
+        if (err) atomicOr(err, kErrBadBlock);
+        *start = 0;
+        return 0;
+    }
+    *start = a;
+    return (int)(e - a);
+}
+
+// First scale group of sequence b: per token (block 1) its first packed
+// token; per block cu[b] / block + b, which leaves every sequence
+// ceil(len / block) groups of its own (at most total / block + B in all).
+__host__ __device__ __forceinline__ int64_t varlen_group0(int64_t cu_b, int b, int block) {
+    return block == 1 ? cu_b : cu_b / block + b;
+}
+
+// First workspace row of sequence b's keys in the prefill's staged copy
+// of a packed batch: its first packed key plus b * (bn + 4) rows, rounded up
+// to a multiple of 4.  Each sequence's tiles of bn rows stay clear of the
+// next sequence, the per-key scale rows stay 16-byte aligned, and all rows
+// fit below total_k + B * (bn + 4).
+__host__ __device__ __forceinline__ int64_t varlen_key_row0(int64_t cu_b, int b, int bn) {
+    return (cu_b + (int64_t)b * (bn + 4) + 3) & ~(int64_t)3;
+}
+
+// Largest b in [0, B) whose key(b) <= x, by bisection (key non-decreasing
+// for a valid packed batch; any input terminates).
+template <typename Key>
+__device__ __forceinline__ int varlen_bisect(int B, int64_t x, Key key) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (key(mid) <= x)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    return lo;
+}
+
 // Upper bound on any single wait inside a kernel (nanoseconds).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

@@ -40,6 +40,14 @@ struct QuantParams {
     float *scale;
     float *mu_out;
     float *bias;
+    // packed variable-length batch (cu == null: the dense [B,H,S,D] form):
+    // sequence b is tokens [cu[b], cu[b+1]) of x [total, H, D] (strides sh,
+    // ss); S is the caller's bound on a sequence's length; codes [H, total, D],
+    // scales [H, groups], mu [B, H, D], bias [H, total]
+    const int32_t *cu;
+    int64_t total;
+    int64_t groups;
+    int *err;
 };
 
 cudaError_t launch_quant(const QuantParams &p, cudaStream_t st, LaunchLog &log);
@@ -134,6 +142,15 @@ struct PrefillParams {
     __half *k_ws;             // [B*Hkv][Lpad][D] exact f16 key codes
     __half *v_ws;             // [B*Hkv][Vrows][D] f16 prefix values (code * v_scale; + bf16 chunk V)
     float *ksc_ws;            // [B*Hkv][Lpad] per-key K scale (0 on padding rows)
+    // ---- packed variable-length batch (cu_q == null: the dense form).
+    // Sq / Sk are then the bounds max_seqlen_q / max_seqlen_k; q [Hq, total_q, D],
+    // q_scale [Hq, q_groups], k [Hkv, total_k, D], k_scale [Hkv, k_groups],
+    // v [total_k, Hkv, D] (strides v_st, v_sh), q_bias / lse [Hq, total_q],
+    // out [total_q, Hq, D]; the workspace holds [Hkv][Lpad] rows with
+    // sequence b's keys from varlen_key_row0(); no paged prefix.
+    const int32_t *cu_q, *cu_k;
+    int64_t total_q, total_k;
+    int64_t v_st, v_sh;
 };
 
 struct PrefillLayout {
@@ -142,6 +159,7 @@ struct PrefillLayout {
 };
 
 PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16);
+PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D);
 cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
 cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
 

@@ -8,7 +8,10 @@
 //   accumulation (bf16 V is rounded to f16 first, as the README's port
 //   converts bf16 V to f16 before its kernel); O / l and LSE in the
 //   epilogue.  Keys come from an optional paged INT8 prefix followed by the
-//   contiguous chunk.
+//   contiguous chunk.  A packed variable-length batch (the README's varlen
+//   path, there one launch per sequence) runs as one launch: every CTA
+//   finds its sequence's query rows and keys through cu_seqlens and the
+//   result is the single-sequence attention of each sequence.
 //
 // GB300 design.  sm_103a has no integer tcgen05 MMA, so QK^T runs on
 // kind::f16 over the INT8 codes expanded EXACTLY to f16 (|q|,|k| <= 127;
@@ -207,7 +210,9 @@ __device__ __forceinline__ void store_piece(uint8_t *tile, int r, int dc, uint4 
     *reinterpret_cast<uint4 *>(row + ((((c8 + 1) & 7) ^ (r & 7)) << 4)) = h1;
 }
 
-template <int D>
+// VL: a packed variable-length batch (rows and keys located through
+// cu_seqlens); the dense instantiation keeps its addressing in closed form.
+template <int D, bool VL>
 __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p,
                    const __grid_constant__ PrefillMaps maps) {
@@ -228,8 +233,49 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     const int ct = nct - 1 - (int)blockIdx.x;  // heaviest (causal) tiles first
     const int hq = blockIdx.y, b = blockIdx.z;
     const int kvh = hq / p.group;
-    const int bh = b * p.Hkv + kvh;
     const int i0 = ct * 128 * NQ;
+
+    // ------------------------------------------------ where this CTA's rows live
+    // Sq(), Sk(): this sequence's query and chunk-key counts (the dense form
+    // reads the kernel parameters at each use, which keeps them out of the
+    // registers); kz, krow0: the staged keys' (head, first row) coordinates.
+    int vsq = 0, vsk = 0;
+    int64_t qs = 0, vq_row0 = 0, vsc0 = 0;
+    int kz = b * p.Hkv + kvh, krow0 = 0;
+    auto Sq = [&]() -> int {
+        if constexpr (VL) return vsq;
+        return p.Sq;
+    };
+    auto Sk = [&]() -> int {
+        if constexpr (VL) return vsk;
+        return p.Sk;
+    };
+    if constexpr (VL) {
+        int *e = (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) ? p.err : nullptr;
+        int64_t ks = 0;
+        vsq = varlen_seq(p.cu_q, b, p.Sq, p.total_q, e, &qs);
+        vsk = varlen_seq(p.cu_k, b, p.Sk, p.total_k, e, &ks);
+        if (i0 >= vsq) return;  // past this sequence's queries (whole CTA)
+        vq_row0 = (int64_t)hq * p.total_q + qs;
+        vsc0 = (int64_t)hq * p.q_groups + varlen_group0(qs, b, 1 << p.q_shift);
+        kz = kvh;
+        krow0 = (int)varlen_key_row0(ks, b, BN);
+    }
+    // row of query i in q, q_bias, lse and the debug dump ([Hq, total_q]
+    // packed, [B, Hq, Sq] dense); its output row (packed output is
+    // token-major [total_q, Hq, D]); its scale group
+    auto q_row = [&](int i) -> int64_t {
+        if constexpr (VL) return vq_row0 + i;
+        return ((int64_t)b * p.Hq + hq) * p.Sq + i;
+    };
+    auto out_row = [&](int i) -> int64_t {
+        if constexpr (VL) return (qs + i) * p.Hq + hq;
+        return ((int64_t)b * p.Hq + hq) * p.Sq + i;
+    };
+    auto q_group = [&](int i) -> int64_t {
+        if constexpr (VL) return vsc0 + (i >> p.q_shift);
+        return ((int64_t)b * p.Hq + hq) * p.q_groups + (i >> p.q_shift);
+    };
 
     // ------------------------------------------------------ tile schedule
     int P = 0;
@@ -240,13 +286,13 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             P = P < 0 ? 0 : p.max_prefix_len;
         }
     }
-    const int off = P + p.Sk - p.Sq;  // key j visible to row i iff j <= i + off (causal)
-    const int row_last = min(i0 + 128 * NQ - 1, p.Sq - 1);
-    const int kmax = p.causal ? row_last + off : P + p.Sk - 1;
+    const int off = P + Sk() - Sq();  // key j visible to row i iff j <= i + off (causal)
+    const int row_last = min(i0 + 128 * NQ - 1, Sq() - 1);
+    const int kmax = p.causal ? row_last + off : P + Sk() - 1;
     int n_pre = 0, n_ch = 0;
     if (kmax >= 0) {
         n_pre = min((P + BN - 1) / BN, kmax / BN + 1);
-        if (kmax >= P) n_ch = min((p.Sk + BN - 1) / BN, (kmax - P) / BN + 1);
+        if (kmax >= P) n_ch = min((Sk() + BN - 1) / BN, (kmax - P) / BN + 1);
     }
     const int T = n_pre + n_ch;
     const int wpre = p.Ppad / BN;  // first chunk tile in the workspace
@@ -298,13 +344,14 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 mbar_arrive_expect_tx(fb, 2 * C::KB + BN * 4);
 #pragma unroll
                 for (int a = 0; a < D / 64; ++a)
-                    tc::tma_load_3d(st + a * BN * 128, &maps.k, a * 64, w * BN, bh, fb);
+                    tc::tma_load_3d(st + a * BN * 128, &maps.k, a * 64, krow0 + w * BN, kz, fb);
                 const CUtensorMap *vm = pre ? &maps.v_pre : &maps.v_ch;
-                const int vrow = pre ? w * BN : (w - wpre) * BN + vch_off;
+                const int vrow = krow0 + (pre ? w * BN : (w - wpre) * BN + vch_off);
 #pragma unroll
                 for (int a = 0; a < D / 64; ++a)
-                    tc::tma_load_3d(st + C::KB + a * BN * 128, vm, a * 64, vrow, bh, fb);
-                bulk_g2s(st + 2 * C::KB, p.ksc_ws + (int64_t)bh * p.Lpad + w * BN, BN * 4, fb);
+                    tc::tma_load_3d(st + C::KB + a * BN * 128, vm, a * 64, vrow, kz, fb);
+                bulk_g2s(st + 2 * C::KB, p.ksc_ws + (int64_t)kz * p.Lpad + krow0 + w * BN, BN * 4,
+                         fb);
                 ++issued;
             }
             for (int jj = max(0, issued - NST); jj < issued; ++jj)
@@ -416,7 +463,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         const int r = threadIdx.x & 127;       // row within the tile = TMEM lane
         const int i_first = i0 + t * 128;
         const int i = i_first + r;
-        const bool row_ok = i < p.Sq;
+        const bool row_ok = i < Sq();
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
         // split rows: the two threads of a row swap partial maxima / sums
         float *red = reinterpret_cast<float *>(sm + C::OFF_RED);
@@ -434,7 +481,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             }
         };
         {
-            const int8_t *qrow = p.q + (((int64_t)b * p.Hq + hq) * p.Sq + i) * D;
+            const int8_t *qrow = p.q + q_row(i) * D;
             if constexpr (C::QT) {
                 // Q row int8 -> exact f16 pairs in this thread's TMEM lane
                 // (each of a row's SPLIT threads writes its share of channels)
@@ -469,13 +516,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         }
         // kept strictly positive so that a masked (-inf) score stays -inf; an
         // all-zero Q row (scale 0) then scores ~1e-30 * acc = 0 as it should
-        const float rq = fmaxf(row_ok ? p.q_scale[((int64_t)b * p.Hq + hq) * p.q_groups +
-                                                  (i >> p.q_shift)] * p.qk_scale_log2
-                                      : 0.0f,
-                               1e-30f);
-        const float bc =
-            (row_ok && p.q_bias) ? p.q_bias[((int64_t)b * p.Hq + hq) * p.Sq + i] * p.qk_scale_log2
-                                 : 0.0f;
+        const float rq = fmaxf(row_ok ? p.q_scale[q_group(i)] * p.qk_scale_log2 : 0.0f, 1e-30f);
+        const float bc = (row_ok && p.q_bias) ? p.q_bias[q_row(i)] * p.qk_scale_log2 : 0.0f;
         const int lim = i + off;
         // K scales constant over 64-key groups (k_block >= 64, chunk keys):
         // the max runs on the raw integer scores and the scale folds into
@@ -499,7 +541,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const uint32_t sp = NS == 1 ? (uint32_t)jj & 1u : (uint32_t)(jj >> 1) & 1u;
             const bool pre = jj < n_pre;
             const int key0 = pre ? jj * BN : (jj - n_pre) * BN;  // within its source
-            const int nvalid = min(BN, (pre ? P : p.Sk) - key0);
+            const int nvalid = min(BN, (pre ? P : Sk()) - key0);
             const int kg0 = pre ? key0 : P + key0;  // over prefix + chunk
             bool ok = wait_ab(bar(B_S_FULL + slot), sp, p.err, abort_flag);
             ok = ok && wait_ab(bar(B_KV_FULL + s), (uint32_t)(jj / NST) & 1u, p.err, abort_flag);
@@ -523,7 +565,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             if (p.dbg) {
                 // debug dump of the raw INT32 scores, re-read from TMEM in
                 // 8-column pieces so that it adds no live registers here
-                int32_t *dr = p.dbg + (((int64_t)b * p.Hq + hq) * p.Sq + i) * p.dbg_stride;
+                int32_t *dr = p.dbg + q_row(i) * p.dbg_stride;
 #pragma unroll 1
                 for (int c8 = 0; c8 < CW / 8; ++c8) {
                     uint32_t v[8];
@@ -686,7 +728,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             tc::fence_after();
         }
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const int64_t orow = ((int64_t)b * p.Hq + hq) * p.Sq + i;
+        const int64_t orow = q_row(i);
 #pragma unroll 1
         for (int c = hc * (D / 32 / SPLIT); c < (hc + 1) * (D / 32 / SPLIT); ++c) {
             uint32_t o[32];
@@ -705,7 +747,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     pk[e] = pack2(v.x, v.y, p.out_bf16 != 0);
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out) +
-                                                       orow * D + c * 32);
+                                                       out_row(i) * D + c * 32);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
@@ -752,29 +794,36 @@ bool make_map(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t bh) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
-cudaError_t launch_d(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
+template <int D, bool VL>
+cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     using C = PCfg<D>;
     if (p.BN != C::BN) return cudaErrorInvalidValue;
     if (!encode_fn()) return cudaErrorNotSupported;
     PrefillMaps m;
     memset(&m, 0, sizeof(m));
-    const uint64_t bh = (uint64_t)p.B * p.Hkv;
+    // staged keys per (batch, kv head), or per kv head for a packed batch
+    const uint64_t bh = p.cu_q ? (uint64_t)p.Hkv : (uint64_t)p.B * p.Hkv;
     if (!make_map<D>(&m.k, p.k_ws, p.Lpad, bh)) return cudaErrorInvalidValue;
     if (p.Vrows > 0 && !make_map<D>(&m.v_pre, p.v_ws, p.Vrows, bh)) return cudaErrorInvalidValue;
     if (p.Sk > 0) {
-        if (p.v_bf16)
+        if (p.v_bf16 || p.cu_q)
             m.v_ch = m.v_pre;
         else if (!make_map<D>(&m.v_ch, p.v, p.Sk, bh))
             return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((p.Sq + 128 * C::NQ - 1) / (128 * C::NQ), p.Hq, p.B);
-    prefill_kernel<D><<<grid, C::THREADS, C::SMEM, st>>>(p, m);
-    log.add("prefill_kernel", grid, dim3(C::THREADS), dim3(1, 1, 1), C::SMEM);
+    prefill_kernel<D, VL><<<grid, C::THREADS, C::SMEM, st>>>(p, m);
+    log.add(VL ? "prefill_varlen_kernel" : "prefill_kernel", grid, dim3(C::THREADS), dim3(1, 1, 1),
+            C::SMEM);
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t launch_d(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
+    return p.cu_q ? launch_dv<D, true>(p, st, log) : launch_dv<D, false>(p, st, log);
 }
 
 }  // namespace

@@ -135,6 +135,56 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
     }
 }
 
+// Packed variable-length batch: sequence b's keys go to workspace rows
+// [r0, r0 + ceil(len / BN) * BN) of each KV head, r0 = varlen_key_row0(),
+// with zero rows after its last key up to the tile boundary.  K codes ->
+// exact f16, V (f16 copied, bf16 rounded) -> f16, one K scale per key.  One
+// thread per 16-channel piece, the piece varying fastest along a row.
+__global__ void __launch_bounds__(256)
+    prefill_stage_varlen_kernel(const __grid_constant__ PrefillParams p) {
+    const int D = p.D;
+    const int per_block = 256 / D;
+    const int t = threadIdx.x % D;
+    const int gps = (p.Sk + p.BN - 1) / p.BN * p.BN / 16;   // 16-row groups per sequence
+    const int64_t g = (int64_t)blockIdx.x * per_block + threadIdx.x / D;
+    if (g >= (int64_t)p.B * p.Hkv * gps) return;
+    const int bh = (int)(g / gps);
+    const int row0 = (int)(g % gps) * 16;
+    const int b = bh / p.Hkv, kvh = bh % p.Hkv;
+    int64_t ks = 0;
+    const int len = varlen_seq(p.cu_k, b, p.Sk, p.total_k, nullptr, &ks);
+    if (row0 >= (len + p.BN - 1) / p.BN * p.BN) return;
+    const int np = D >> 4;
+    const int slot = t / np, dc = t % np;
+    const int row = row0 + slot;
+    const bool ok = row < len;
+    const int64_t wrow = (int64_t)kvh * p.Lpad + varlen_key_row0(ks, b, p.BN) + row;
+    uint4 wk = make_uint4(0, 0, 0, 0), v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+    float ksc = 0.0f;
+    if (ok) {
+        wk = *reinterpret_cast<const uint4 *>(p.k + ((int64_t)kvh * p.total_k + ks + row) * D +
+                                              dc * 16);
+        ksc = p.k_scale[(int64_t)kvh * p.k_groups + varlen_group0(ks, b, 1 << p.k_shift) +
+                        (row >> p.k_shift)];
+        const int64_t vo = (ks + row) * p.v_st + kvh * p.v_sh + dc * 16;
+        if (p.v_bf16) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const __nv_bfloat16 *>(p.v) + vo);
+            v0 = bf16x8_to_f16x8(src[0]);
+            v1 = bf16x8_to_f16x8(src[1]);
+        } else {
+            const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __half *>(p.v) + vo);
+            v0 = src[0];
+            v1 = src[1];
+        }
+    }
+    store_f16x16(p.k_ws + wrow * D + dc * 16, wk);
+    if (dc == 0) p.ksc_ws[wrow] = ksc;
+    uint4 *d = reinterpret_cast<uint4 *>(p.v_ws + wrow * D + dc * 16);
+    d[0] = v0;
+    d[1] = v1;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
@@ -153,7 +203,33 @@ PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, 
     return L;
 }
 
+PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D) {
+    PrefillLayout L = {};
+    L.BN = D == 256 ? 64 : 128;
+    L.Ppad = 0;
+    const int64_t rows = (total_k + (int64_t)B * (L.BN + 4) + 15) / 16 * 16;
+    L.Lpad = (int)rows;
+    L.Vrows = L.Lpad;
+    const size_t H = (size_t)Hkv;
+    L.off_k = 0;
+    L.off_v = align256(L.off_k + H * rows * D * 2);
+    L.off_ksc = align256(L.off_v + H * rows * D * 2);
+    L.bytes = align256(L.off_ksc + H * rows * 4);
+    return L;
+}
+
 cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
+    if (p.cu_q) {
+        const int gps = (p.Sk + p.BN - 1) / p.BN * p.BN / 16;
+        const int64_t groups = (int64_t)p.B * p.Hkv * gps;
+        const int per_block = 256 / p.D;
+        const int64_t blocks = (groups + per_block - 1) / per_block;
+        if (blocks == 0) return cudaSuccess;
+        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
+        prefill_stage_varlen_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+        log.add("prefill_stage_varlen_kernel", dim3((unsigned)blocks), dim3(256), dim3(1, 1, 1), 0);
+        return cudaGetLastError();
+    }
     const int64_t groups = (int64_t)p.B * p.Hkv * (p.Lpad >> 4);
     const int per_block = 256 / p.D;
     const int64_t blocks = (groups + per_block - 1) / per_block;

@@ -9,7 +9,12 @@
 //
 // Memory layout: x is read through (b, h, s) strides with the channel
 // dimension contiguous, 16 bytes (8 elements) per thread per load; the
-// int8 output is dense [B,H,S,D].  These kernels are HBM-bound.
+// int8 output is dense [B,H,S,D].  A packed variable-length batch (the
+// README's varlen path: sequence b is packed tokens cu[b] .. cu[b+1]-1 of
+// x [total, H, D]) is quantised sequence by sequence: groups start at each
+// sequence's first token and smooth_k takes each sequence's own mean; the
+// int8 output is [H, total, D] and the scales [H, groups] with sequence
+// b's groups from varlen_group0().  These kernels are HBM-bound.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -53,32 +58,23 @@ __device__ __forceinline__ float row_sum(float v, int tpr) {
 // ---------------------------------------------------------------------------
 // Per-token quantisation: each row of D elements is handled by D/8 lanes.
 // ---------------------------------------------------------------------------
+// One row: src its first element (this lane's 8 channels), msub / mbias the
+// mean rows (or null), orow its output row (codes, bias), sidx its scale.
 template <typename T>
-__global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
-    const int tpr = p.D / 8;
-    const int rows_per_cta = 256 / tpr;
-    const int64_t nrows = (int64_t)p.B * p.H * p.S;
-    const int64_t r = (int64_t)blockIdx.x * rows_per_cta + threadIdx.x / tpr;
-    const int c0 = (threadIdx.x % tpr) * 8;
-    const bool valid = r < nrows;
+__device__ __forceinline__ void quant_row(const QuantParams &p, bool valid, const T *src,
+                                          const float *msub, const float *mbias, int64_t orow,
+                                          int64_t sidx, int c0, int tpr) {
     float v[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     float amax = 0.0f, dot = 0.0f;
-    int64_t bh = 0;
     if (valid) {
-        const int64_t s = r % p.S;
-        bh = r / p.S;
-        const int64_t b = bh / p.H, h = bh % p.H;
-        const T *src = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh + s * p.ss + c0;
         load8(src, v);
-        if (p.mu_bias) {
-            const float *m = p.mu_bias + (b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0;
+        if (mbias) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) dot = fmaf(v[i], m[i], dot);
+            for (int i = 0; i < 8; ++i) dot = fmaf(v[i], mbias[i], dot);
         }
-        if (p.mu_sub) {
-            const float *m = p.mu_sub + bh * p.D + c0;
+        if (msub) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = v[i] - m[i];
+            for (int i = 0; i < 8; ++i) v[i] = v[i] - msub[i];
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
@@ -87,11 +83,63 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     dot = row_sum(dot, tpr);
     if (!valid) return;
     const float s = __fdiv_rn(amax, 127.0f);
-    store8_i8(p.q + r * p.D + c0, v, s);
+    store8_i8(p.q + orow * p.D + c0, v, s);
     if (threadIdx.x % tpr == 0) {
-        p.scale[r] = s;
-        if (p.bias) p.bias[r] = dot;
+        p.scale[sidx] = s;
+        if (p.bias) p.bias[orow] = dot;
     }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
+    const int tpr = p.D / 8;
+    const int rows_per_cta = 256 / tpr;
+    const int64_t nrows = (int64_t)p.B * p.H * p.S;
+    const int64_t r = (int64_t)blockIdx.x * rows_per_cta + threadIdx.x / tpr;
+    const int c0 = (threadIdx.x % tpr) * 8;
+    const bool valid = r < nrows;
+    const T *src = nullptr;
+    const float *msub = nullptr, *mbias = nullptr;
+    if (valid) {
+        const int64_t s = r % p.S;
+        const int64_t bh = r / p.S;
+        const int64_t b = bh / p.H, h = bh % p.H;
+        src = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh + s * p.ss + c0;
+        if (p.mu_bias) mbias = p.mu_bias + (b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0;
+        if (p.mu_sub) msub = p.mu_sub + bh * p.D + c0;
+    }
+    quant_row<T>(p, valid, src, msub, mbias, r, r, c0, tpr);
+}
+
+// Packed batch: row r = (head h, packed token t); t's sequence by bisection.
+// Tokens outside every valid sequence are left untouched.
+template <typename T>
+__global__ void __launch_bounds__(256) quant_rows_varlen_kernel(QuantParams p) {
+    const int tpr = p.D / 8;
+    const int rows_per_cta = 256 / tpr;
+    const int64_t nrows = (int64_t)p.H * p.total;
+    const int64_t r = (int64_t)blockIdx.x * rows_per_cta + threadIdx.x / tpr;
+    const int c0 = (threadIdx.x % tpr) * 8;
+    bool valid = r < nrows;
+    const T *src = nullptr;
+    const float *msub = nullptr, *mbias = nullptr;
+    if (r < p.B && c0 == 0) {
+        // the first B rows also check one sequence each for the error word
+        int64_t start = 0;
+        varlen_seq(p.cu, (int)r, p.S, p.total, p.err, &start);
+    }
+    if (valid) {
+        const int64_t h = r / p.total, t = r % p.total;
+        const int b = varlen_bisect(p.B, t, [&](int i) { return (int64_t)p.cu[i]; });
+        int64_t start = 0;
+        const int len = varlen_seq(p.cu, b, p.S, p.total, nullptr, &start);
+        valid = t >= start && t < start + len;
+        src = reinterpret_cast<const T *>(p.x) + h * p.sh + t * p.ss + c0;
+        if (p.mu_bias)
+            mbias = p.mu_bias + ((int64_t)b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0;
+        if (p.mu_sub) msub = p.mu_sub + ((int64_t)b * p.H + h) * p.D + c0;
+    }
+    quant_row<T>(p, valid, src, msub, mbias, r, r, c0, tpr);
 }
 
 // ---------------------------------------------------------------------------
@@ -99,23 +147,16 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
 // Pass 1 finds the block's amax (and per-row biases); pass 2 re-reads the
 // block (L1/L2 resident) and writes the codes.
 // ---------------------------------------------------------------------------
+// Tokens [t0, t1) of one (sequence, head): token t at base + t * p.ss (this
+// lane's channels), output row orow0 + t, scale at sidx.
 template <typename T>
-__global__ void __launch_bounds__(256) quant_blocks_kernel(QuantParams p) {
+__device__ __forceinline__ void quant_block(const QuantParams &p, const T *base,
+                                            const float *msub, const float *mbias, int64_t t0,
+                                            int64_t t1, int64_t orow0, int64_t sidx) {
     __shared__ float red[8];
     const int tpr = p.D / 8;
     const int rows_per_pass = 256 / tpr;
-    const int64_t ngroups = (p.S + p.block - 1) / p.block;
-    const int64_t g = blockIdx.x % ngroups;
-    const int64_t bh = blockIdx.x / ngroups;
-    const int64_t b = bh / p.H, h = bh % p.H;
-    const int64_t t0 = g * p.block;
-    const int64_t t1 = (t0 + p.block < (int64_t)p.S) ? t0 + p.block : (int64_t)p.S;
     const int c0 = (threadIdx.x % tpr) * 8;
-    const T *base = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh + c0;
-    const float *msub = p.mu_sub ? p.mu_sub + bh * p.D + c0 : nullptr;
-    const float *mbias =
-        p.mu_bias ? p.mu_bias + (b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0 : nullptr;
-
     float amax = 0.0f;
     for (int64_t t = t0 + threadIdx.x / tpr; t - (threadIdx.x / tpr) < t1; t += rows_per_pass) {
         const bool valid = t < t1;
@@ -136,7 +177,7 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(QuantParams p) {
         }
         if (mbias) {
             dot = row_sum(dot, tpr);
-            if (valid && threadIdx.x % tpr == 0) p.bias[bh * p.S + t] = dot;
+            if (valid && threadIdx.x % tpr == 0) p.bias[orow0 + t] = dot;
         }
     }
     amax = warp_max(amax);
@@ -149,7 +190,7 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(QuantParams p) {
     }
     __syncthreads();
     const float s = __fdiv_rn(red[0], 127.0f);
-    if (threadIdx.x == 0) p.scale[bh * ngroups + g] = s;
+    if (threadIdx.x == 0) p.scale[sidx] = s;
     for (int64_t t = t0 + threadIdx.x / tpr; t < t1; t += rows_per_pass) {
         float v[8];
         load8(base + t * p.ss, v);
@@ -157,8 +198,54 @@ __global__ void __launch_bounds__(256) quant_blocks_kernel(QuantParams p) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) v[i] = v[i] - msub[i];
         }
-        store8_i8(p.q + (bh * p.S + t) * p.D + c0, v, s);
+        store8_i8(p.q + (orow0 + t) * p.D + c0, v, s);
     }
+}
+
+template <typename T>
+__global__ void __launch_bounds__(256) quant_blocks_kernel(QuantParams p) {
+    const int tpr = p.D / 8;
+    const int64_t ngroups = (p.S + p.block - 1) / p.block;
+    const int64_t g = blockIdx.x % ngroups;
+    const int64_t bh = blockIdx.x / ngroups;
+    const int64_t b = bh / p.H, h = bh % p.H;
+    const int64_t t0 = g * p.block;
+    const int64_t t1 = (t0 + p.block < (int64_t)p.S) ? t0 + p.block : (int64_t)p.S;
+    const int c0 = (threadIdx.x % tpr) * 8;
+    const T *base = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh + c0;
+    const float *msub = p.mu_sub ? p.mu_sub + bh * p.D + c0 : nullptr;
+    const float *mbias =
+        p.mu_bias ? p.mu_bias + (b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0 : nullptr;
+    quant_block<T>(p, base, msub, mbias, t0, t1, bh * p.S, bh * ngroups + g);
+}
+
+// Packed batch: one CTA per (head, scale group); the group's sequence by
+// bisection over the sequences' first groups.  A group slot past its
+// sequence's end (the layout reserves up to one per sequence) gets scale 0.
+template <typename T>
+__global__ void __launch_bounds__(256) quant_blocks_varlen_kernel(QuantParams p) {
+    const int tpr = p.D / 8;
+    const int64_t g = blockIdx.x % p.groups;
+    const int64_t h = blockIdx.x / p.groups;
+    const int b = varlen_bisect(p.B, g, [&](int i) {
+        return varlen_group0(p.cu[i] < 0 ? 0 : p.cu[i], i, p.block);
+    });
+    int64_t start = 0;
+    const int len = varlen_seq(p.cu, b, p.S, p.total, threadIdx.x == 0 ? p.err : nullptr, &start);
+    const int64_t j = g - varlen_group0(start, b, p.block);
+    const int64_t t0 = j * p.block;
+    if (len == 0 || j < 0 || t0 >= len) {
+        if (threadIdx.x == 0) p.scale[h * p.groups + g] = 0.0f;
+        return;
+    }
+    const int64_t t1 = (t0 + p.block < (int64_t)len) ? t0 + p.block : (int64_t)len;
+    const int c0 = (threadIdx.x % tpr) * 8;
+    const T *base = reinterpret_cast<const T *>(p.x) + h * p.sh + start * p.ss + c0;
+    const float *msub = p.mu_sub ? p.mu_sub + ((int64_t)b * p.H + h) * p.D + c0 : nullptr;
+    const float *mbias =
+        p.mu_bias ? p.mu_bias + ((int64_t)b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0
+                  : nullptr;
+    quant_block<T>(p, base, msub, mbias, t0, t1, h * p.total + start, h * p.groups + g);
 }
 
 // ---------------------------------------------------------------------------
@@ -199,12 +286,20 @@ __global__ void __launch_bounds__(256) token_mean_kernel(QuantParams p) {
     const int lanes_t = 256 / tpr;
     const int64_t bh = blockIdx.y;
     const int64_t b = bh / p.H, h = bh % p.H;
-    const int64_t chunk = (p.S + kMeanCluster - 1) / kMeanCluster;
+    // tokens of this (sequence, head): dense S rows, or one packed sequence
+    int64_t n = p.S;
+    const T *base = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh;
+    if (p.cu) {
+        int64_t start = 0;
+        n = varlen_seq(p.cu, (int)b, p.S, p.total, nullptr, &start);
+        base = reinterpret_cast<const T *>(p.x) + start * p.ss + h * p.sh;
+    }
+    const int64_t chunk = (n + kMeanCluster - 1) / kMeanCluster;
     const int64_t t0 = rank * chunk;
-    const int64_t t1 = (t0 + chunk < (int64_t)p.S) ? t0 + chunk : (int64_t)p.S;
+    const int64_t t1 = (t0 + chunk < n) ? t0 + chunk : n;
     const int c0 = (threadIdx.x % tpr) * 8;
     const int lt = threadIdx.x / tpr;
-    const T *base = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh + c0;
+    base += c0;
     Acc acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0;
@@ -227,7 +322,8 @@ __global__ void __launch_bounds__(256) token_mean_kernel(QuantParams p) {
     if (rank == 0 && threadIdx.x < p.D) {
         Acc tot = 0;
         for (int r = 0; r < kMeanCluster; ++r) tot += cluster.map_shared_rank(cta_sum, r)[threadIdx.x];
-        const double mean = MeanAcc<T>::finish(tot) / (double)p.S;
+        // an empty sequence has no mean; 0 keeps its (unused) row defined
+        const double mean = n > 0 ? MeanAcc<T>::finish(tot) / (double)n : 0.0;
         p.mu_out[bh * p.D + threadIdx.x] = (float)mean;
     }
     cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
@@ -254,7 +350,23 @@ cudaError_t launch_quant_t(const QuantParams &p, cudaStream_t st, LaunchLog &log
         if (e != cudaSuccess) return e;
         q.mu_sub = p.mu_out;
     }
-    if (p.block == 1) {
+    if (p.cu) {
+        if (p.block == 1) {
+            const int rows_per_cta = 256 / (p.D / 8);
+            const int64_t nrows = (int64_t)p.H * p.total;
+            const unsigned grid = (unsigned)((nrows + rows_per_cta - 1) / rows_per_cta);
+            if (grid > 0) {
+                quant_rows_varlen_kernel<T><<<grid, 256, 0, st>>>(q);
+                log.add("quant_rows_varlen_kernel", dim3(grid), dim3(256), dim3(1, 1, 1), 0);
+            }
+        } else {
+            const unsigned grid = (unsigned)((int64_t)p.H * p.groups);
+            if (grid > 0) {
+                quant_blocks_varlen_kernel<T><<<grid, 256, 0, st>>>(q);
+                log.add("quant_blocks_varlen_kernel", dim3(grid), dim3(256), dim3(1, 1, 1), 0);
+            }
+        }
+    } else if (p.block == 1) {
         const int rows_per_cta = 256 / (p.D / 8);
         const int64_t nrows = (int64_t)p.B * p.H * p.S;
         const unsigned grid = (unsigned)((nrows + rows_per_cta - 1) / rows_per_cta);

@@ -7,6 +7,9 @@ describe:
 
 * dense prefill: Q/K/V ~ N(0, 1) in fp16/bf16, HND layout, with an
   optional per-(head, channel) K offset ~ N(0, 4) that smooth_k removes;
+* packed variable-length batches: the same distributions, token-major
+  [total, H, D] with sequence lengths drawn log-uniformly (many short
+  sequences and a few long ones, the mix a varlen batch serves);
 * paged decode / paged prefix: INT8 cache values uniform in [-127, 127],
   per-token per-KV-head fp32 scales ~ U(0.005, 0.02), cache layout
   [block, kv_head, head_dim/16, 16, 16], block table a random
@@ -99,6 +102,46 @@ def dense_qkv(B: int, Hq: int, Hkv: int, Sq: int, Sk: int, D: int, seed: int, dt
     return DenseQKV(q, k, v)
 
 
+@dataclass
+class VarlenQKV:
+    q: torch.Tensor            # [total_q, Hq, D]
+    k: torch.Tensor            # [total_k, Hkv, D]
+    v: torch.Tensor            # [total_k, Hkv, D]
+    cu_q: torch.Tensor         # int32 [B + 1]
+    cu_k: torch.Tensor         # int32 [B + 1]
+    max_q: int
+    max_k: int
+
+
+def varlen_lengths(n: int, lo: int, hi: int, seed: int):
+    """n sequence lengths, log-uniform in [lo, hi] (seeded, CPU)."""
+    g = _gen(seed, "cpu")
+    u = torch.rand((n,), generator=g, dtype=torch.float64)
+    return [int(round(lo * (hi / lo) ** float(x))) for x in u]
+
+
+def varlen_qkv(lens_q, lens_k, Hq: int, Hkv: int, D: int, seed: int, dtype="fp16", device="cpu",
+               k_offset_std: float = 0.0, v_dtype=None) -> VarlenQKV:
+    """Packed token-major Q/K/V ~ N(0,1); K gets a per-(head, channel) offset
+    ~ N(0, k_offset_std^2) shared by every token of the batch."""
+    g = _gen(seed, device)
+    dt = _DT[dtype]
+    vdt = _DT[v_dtype] if v_dtype else dt
+    tq, tk = int(sum(lens_q)), int(sum(lens_k))
+    q = _normal((tq, Hq, D), g, device, dt)
+    k = _normal((tk, Hkv, D), g, device, dt, offset_shape=(1, Hkv, D), offset_std=k_offset_std)
+    v = _normal((tk, Hkv, D), g, device, vdt)
+
+    def cu(lens):
+        c = [0]
+        for n in lens:
+            c.append(c[-1] + int(n))
+        return torch.tensor(c, dtype=torch.int32, device=device)
+
+    return VarlenQKV(q, k, v, cu(lens_q), cu(lens_k), max(lens_q, default=0),
+                     max(lens_k, default=0))
+
+
 def decode_query(B: int, Hq: int, D: int, seed: int, dtype="bf16", device="cpu") -> torch.Tensor:
     """One new query token per sequence: [B, Hq, D] ~ N(0, 1)."""
     g = _gen(seed, device)
@@ -129,6 +172,10 @@ WORKLOADS = {
                                                     dtype="fp16", seed=3, q_block=128,
                                                     k_block=64, smooth_k=True, causal=True,
                                                     k_offset_std=2.0, return_lse=True)),
+    "varlen_prefill": Workload("varlen_prefill", dict(n=24, lo=256, hi=8192, Hq=32, Hkv=8,
+                                                      D=128, dtype="fp16", seed=5, q_block=128,
+                                                      k_block=64, smooth_k=True, causal=True,
+                                                      k_offset_std=2.0)),
     "decode_sweep": Workload("decode_sweep", dict(Hq=24, Hkv=4, D=256, dtype="bf16", seed=4,
                                                   ctx=(8192, 16384, 32768), batch=(1, 16, 64))),
 }

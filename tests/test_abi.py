@@ -84,3 +84,55 @@ def test_workspace_arithmetic(lib):
 def test_launch_info_struct(lib):
     info = binding.LaunchInfo()
     assert lib.sage_last_launch_info(ctypes.byref(info)) == binding.SAGE_OK
+
+
+def test_varlen_scale_group_layout(lib):
+    # per token: one group per packed token; per block: total / block + B
+    assert lib.sage_varlen_scale_groups(1000, 7, 1) == 1000
+    assert lib.sage_varlen_scale_groups(1000, 7, 64) == 1000 // 64 + 7
+    # the documented first groups (cu[b] / block + b) leave every sequence
+    # ceil(len / block) slots of its own inside that count
+    rng = __import__("numpy").random.default_rng(3)
+    for block in (64, 128, 256):
+        for _ in range(200):
+            lens = rng.integers(0, 700, size=rng.integers(1, 12))
+            cu = [0]
+            for n in lens:
+                cu.append(cu[-1] + int(n))
+            G = lib.sage_varlen_scale_groups(cu[-1], len(lens), block)
+            ends = []
+            for b, n in enumerate(lens):
+                g0 = cu[b] // block + b
+                ends.append((g0, g0 + (int(n) + block - 1) // block))
+            for (a0, a1), (b0, _) in zip(ends, ends[1:]):
+                assert a1 <= b0
+            assert ends[-1][1] <= G
+
+
+def test_varlen_rejects_bad_arguments_on_host(lib):
+    st = lib.sage_quant_int8_varlen(None, 0, 1, 1, 10, 96, 0, 0, None, 10, 1, 0, None, 0, None,
+                                    None, None, None, None)
+    assert st == binding.SAGE_ERR_UNSUPPORTED
+    st = lib.sage_quant_int8_varlen(ctypes.c_void_p(16), 0, 1, 1, 10, 64, 64, 64, None, 10, 1, 0,
+                                    None, 0, ctypes.c_void_p(16), ctypes.c_void_p(16), None,
+                                    None, None)
+    assert st == binding.SAGE_ERR_INVALID_ARG     # cu_seqlens missing
+    a = binding.PrefillVarlenArgs()
+    a.B, a.Hq, a.Hkv, a.D = 2, 6, 4, 128
+    a.total_q = a.total_k = 100
+    a.max_seqlen_q = a.max_seqlen_k = 60
+    a.q_block = a.k_block = 1
+    assert lib.sage_attn_prefill_varlen(ctypes.byref(a), None, 0, None) == \
+        binding.SAGE_ERR_INVALID_ARG              # Hq % Hkv != 0
+    a.Hkv = 2
+    a.q_block = 96
+    assert lib.sage_attn_prefill_varlen(ctypes.byref(a), None, 0, None) == \
+        binding.SAGE_ERR_UNSUPPORTED
+    a.q_block = 1
+    assert lib.sage_attn_prefill_varlen(ctypes.byref(a), None, 0, None) == \
+        binding.SAGE_ERR_INVALID_ARG              # no cu_seqlens
+    assert lib.sage_attn_prefill_varlen_workspace_size(None) == 0
+    # workspace: K and V f16 copies plus scales over total_k + B * (BN + 4) rows
+    need = lib.sage_attn_prefill_varlen_workspace_size(ctypes.byref(a))
+    rows = 100 + 2 * (128 + 4)
+    assert need >= 2 * (2 * rows * 128 * 2) + 2 * rows * 4
