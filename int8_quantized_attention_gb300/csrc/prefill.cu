@@ -229,11 +229,25 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nct = (p.Sq + 128 * NQ - 1) / (128 * NQ);
-    const int ct = nct - 1 - (int)blockIdx.x;  // heaviest (causal) tiles first
-    const int hq = blockIdx.y, b = blockIdx.z;
+    constexpr int QR = 128 * NQ;  // query rows per CTA
+    const int hq = blockIdx.y;
     const int kvh = hq / p.group;
-    const int i0 = ct * 128 * NQ;
+    int b, ct;
+    if constexpr (VL) {
+        // compact tile index: sequence b owns tiles [cu_q[b] / QR + b, ...),
+        // ceil(len_b / QR) of them (at most one spare slot per sequence)
+        const int g = blockIdx.x;
+        b = varlen_bisect(p.B, g, [&](int k) {
+            const int c = p.cu_q[k];
+            return varlen_group0(c < 0 ? 0 : c, k, QR);
+        });
+        const int c = p.cu_q[b];
+        ct = g - (int)varlen_group0(c < 0 ? 0 : c, b, QR);  // reversed below
+    } else {
+        const int nct = (p.Sq + QR - 1) / QR;
+        ct = nct - 1 - (int)blockIdx.x;  // heaviest (causal) tiles first
+        b = blockIdx.z;
+    }
 
     // ------------------------------------------------ where this CTA's rows live
     // Sq(), Sk(): this sequence's query and chunk-key counts (the dense form
@@ -251,11 +265,15 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         return p.Sk;
     };
     if constexpr (VL) {
-        int *e = (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.y == 0) ? p.err : nullptr;
+        int *e = threadIdx.x == 0 ? p.err : nullptr;  // each CTA checks its sequence
         int64_t ks = 0;
         vsq = varlen_seq(p.cu_q, b, p.Sq, p.total_q, e, &qs);
         vsk = varlen_seq(p.cu_k, b, p.Sk, p.total_k, e, &ks);
-        if (i0 >= vsq) return;  // past this sequence's queries (whole CTA)
+        const int ntile = (vsq + QR - 1) / QR;
+        // a spare slot, a slot before the first sequence, or an empty or
+        // invalid sequence: nothing to do (the whole CTA returns)
+        if (ct < 0 || ct >= ntile) return;
+        ct = ntile - 1 - ct;      // heaviest (causal) tiles of the sequence first
         vq_row0 = (int64_t)hq * p.total_q + qs;
         vsc0 = (int64_t)hq * p.q_groups + varlen_group0(qs, b, 1 << p.q_shift);
         kz = kvh;
@@ -276,6 +294,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         if constexpr (VL) return vsc0 + (i >> p.q_shift);
         return ((int64_t)b * p.Hq + hq) * p.q_groups + (i >> p.q_shift);
     };
+    const int i0 = ct * QR;
 
     // ------------------------------------------------------ tile schedule
     int P = 0;
@@ -814,7 +833,11 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    const dim3 grid((p.Sq + 128 * C::NQ - 1) / (128 * C::NQ), p.Hq, p.B);
+    // packed batches: one CTA per compact tile slot (ceil(len_b / QR) per
+    // sequence, at most total_q / QR + B slots), heads in y
+    constexpr int QR = 128 * C::NQ;
+    const dim3 grid = VL ? dim3((unsigned)(p.total_q / QR + p.B), p.Hq, 1)
+                         : dim3((p.Sq + QR - 1) / QR, p.Hq, p.B);
     prefill_kernel<D, VL><<<grid, C::THREADS, C::SMEM, st>>>(p, m);
     log.add(VL ? "prefill_varlen_kernel" : "prefill_kernel", grid, dim3(C::THREADS), dim3(1, 1, 1),
             C::SMEM);
