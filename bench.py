@@ -446,8 +446,9 @@ def prefill_measure(args):
 def run_profile(args):
     """Launch one kernel of a named workload a few times (for ncu captures).
 
-    --profile dense_prefill|chunked_prefill|paged_decode, --heads H shrinks
-    the query heads (and KV heads in proportion) to keep a capture small.
+    --profile dense_prefill|chunked_prefill|varlen_prefill|paged_decode,
+    --heads H shrinks the query heads (and KV heads in proportion) to keep a
+    capture small.
     """
     import torch
 
@@ -467,6 +468,18 @@ def run_profile(args):
         q = W.decode_query(P["B"], P["Hq"], P["D"], seed=P["seed"], device="cuda")
         run = lambda: sage.sage_attn_decode_paged_q16(q, c.k_cache, c.v_cache, c.k_scale,
                                                       c.v_scale, c.block_table, c.lens, P["ctx"])
+    elif args.profile == "varlen_prefill":
+        lens = W.varlen_lengths(P["n"], P["lo"], P["hi"], P["seed"])
+        x = W.varlen_qkv(lens, lens, P["Hq"], P["Hkv"], P["D"], seed=P["seed"], dtype=P["dtype"],
+                         device="cuda", k_offset_std=P["k_offset_std"])
+        ki, ks, mu, _ = sage.sage_quant_int8_varlen(x.k, x.cu_k, x.max_k,
+                                                    block_tokens=P["k_block"], smooth=True)
+        qi, qs, _, bias = sage.sage_quant_int8_varlen(x.q, x.cu_q, x.max_q,
+                                                      block_tokens=P["q_block"], mu_in=mu)
+        run = lambda: sage.sage_attn_prefill_varlen(qi, qs, P["q_block"], ki, ks, P["k_block"],
+                                                    x.v, x.cu_q, x.cu_k, x.max_q, x.max_k,
+                                                    causal=P["causal"], q_bias=bias,
+                                                    return_lse=True)
     else:
         qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
                           dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
@@ -576,6 +589,49 @@ def run_configs(args):
               "oracle_sample": "full" if scale == 1 else "1 (batch, head), %d rows, scaled x%.0f" % (len(rows), scale)})
         del qkv, qi, ki, out
 
+    # ---- packed variable-length prefill (one launch over every sequence)
+    P = W.WORKLOADS["varlen_prefill"].params
+    lens = W.varlen_lengths(P["n"], P["lo"], P["hi"], P["seed"])
+    x = W.varlen_qkv(lens, lens, P["Hq"], P["Hkv"], P["D"], seed=P["seed"], dtype=P["dtype"],
+                     device="cuda", k_offset_std=P["k_offset_std"])
+    qb, kb = P["q_block"], P["k_block"]
+    ki, ks, mu, _ = sage.sage_quant_int8_varlen(x.k, x.cu_k, x.max_k, block_tokens=kb, smooth=True)
+    qi, qs, _, bias = sage.sage_quant_int8_varlen(x.q, x.cu_q, x.max_q, block_tokens=qb, mu_in=mu)
+    vws = torch.empty(sage.prefill_varlen_workspace_size(len(lens), P["Hq"], P["Hkv"], P["D"],
+                                                        x.q.shape[0], x.k.shape[0], x.max_q,
+                                                        x.max_k),
+                      dtype=torch.uint8, device="cuda")
+    fn = lambda: sage.sage_attn_prefill_varlen(qi, qs, qb, ki, ks, kb, x.v, x.cu_q, x.cu_k,
+                                               x.max_q, x.max_k, causal=P["causal"], q_bias=bias,
+                                               return_lse=True, workspace=vws)
+    ms = gpu_ms(fn)
+    flop = sum(4 * P["D"] * P["Hq"] * (n * (n + 1) // 2 if P["causal"] else n * n) for n in lens)
+    tf = flop / (ms * 1e-3) / 1e12
+    # oracle: the longest sequence, one head, 16 rows, scaled by visible pairs
+    bl = int(np.argmax(lens))
+    cq = x.cu_q.cpu().numpy()
+    n = lens[bl]
+    t0s, t1s = int(cq[bl]), int(cq[bl + 1])
+    g0q, g0k = t0s // qb + bl, t0s // kb + bl
+    rows = np.linspace(0, n - 1, 16).astype(np.int64)
+    t0 = time.perf_counter()
+    oracle.prefill(qi[0:1, t0s:t1s][None].cpu().numpy(),
+                   qs[0:1, g0q:g0q + (n + qb - 1) // qb][None].cpu().numpy(), qb,
+                   ki[0:1, t0s:t1s][None].cpu().numpy(),
+                   ks[0:1, g0k:g0k + (n + kb - 1) // kb][None].cpu().numpy(), kb,
+                   x.v[t0s:t1s, 0:1].float().transpose(0, 1)[None].cpu().numpy(),
+                   causal=P["causal"], q_bias=bias[0:1, t0s:t1s][None].cpu().numpy().astype(np.float64),
+                   rows=rows, threads=threads)
+    t_or = time.perf_counter() - t0
+    pairs_s = sum(int(i) + 1 for i in rows) if P["causal"] else len(rows) * n
+    scale = flop / (4 * P["D"]) / pairs_s
+    emit({"config": "varlen_prefill", "sequences": len(lens), "tokens": int(sum(lens)),
+          "gpu_ms": round(ms, 4), "tflops": round(tf, 1),
+          "frac_of_measured_f16_peak": round(tf / peaks["bf16_tflops"], 4),
+          "oracle_s": round(t_or * scale, 2), "oracle_cores": threads,
+          "oracle_sample": "1 sequence x 1 head, %d rows, scaled x%.0f" % (len(rows), scale)})
+    del x, qi, ki
+
     # ---- decode configurations
     P = W.WORKLOADS["paged_decode"].params
     shapes = [("paged_decode", P["B"], P["ctx"])]
@@ -668,7 +724,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--profile", default=None,
-                    choices=["paged_decode", "dense_prefill", "chunked_prefill"])
+                    choices=["paged_decode", "dense_prefill", "chunked_prefill",
+                             "varlen_prefill"])
     ap.add_argument("--heads", type=int, default=0)
     ap.add_argument("--configs", action="store_true",
                     help="time every configuration of the workload table (one JSON line each)")

@@ -385,7 +385,8 @@ def sage_splitk_combine(o_part: torch.Tensor, lse_part: torch.Tensor, out_dtype=
 def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: int, v, *,
                       causal: bool, sm_scale=None, q_bias=None, prefix: Optional[dict] = None,
                       out_dtype=None, return_lse: bool = False, debug_scores=None,
-                      workspace: Optional[torch.Tensor] = None, stream=None):
+                      workspace: Optional[torch.Tensor] = None, out=None, lse=None,
+                      stream=None):
     """INT8-QK prefill attention over an optional paged INT8 prefix + a chunk.
 
     q_int8 [B,Hq,Sq,D]; q_scale [B,Hq,ceil(Sq/q_block)]; k_int8 [B,Hkv,Sk,D];
@@ -401,10 +402,16 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
     _need(k_scale, torch.float32, "k_scale")
     if not v.is_contiguous():
         raise ValueError("v must be contiguous")
-    out_dtype = out_dtype or v.dtype
-    out = torch.empty((B, Hq, Sq, D), dtype=out_dtype, device=q_int8.device)
-    lse = (torch.empty((B, Hq, Sq), dtype=torch.float32, device=q_int8.device)
-           if return_lse else None)
+    out_dtype = out.dtype if out is not None else (out_dtype or v.dtype)
+    if out is None:
+        out = torch.empty((B, Hq, Sq, D), dtype=out_dtype, device=q_int8.device)
+    elif tuple(out.shape) != (B, Hq, Sq, D) or not out.is_contiguous():
+        raise ValueError("out must be a contiguous [B, Hq, Sq, D] tensor")
+    if lse is not None:
+        _need(lse, torch.float32, "lse")
+        return_lse = True
+    elif return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q_int8.device)
     a = PrefillArgs()
     a.B, a.Hq, a.Hkv, a.Sq, a.Sk, a.D = B, Hq, Hkv, Sq, Sk, D
     a.q, a.q_scale, a.q_block = _ptr(q_int8), _ptr(q_scale), q_block
@@ -482,6 +489,18 @@ def sage_quant_int8_varlen(x: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen
                                         _ptr(q), _ptr(scale), _ptr(mu), _ptr(bias),
                                         _stream(stream)))
     return q, scale, mu, bias
+
+
+def prefill_varlen_workspace_size(B: int, Hq: int, Hkv: int, D: int, total_q: int, total_k: int,
+                                  max_seqlen_q: int, max_seqlen_k: int) -> int:
+    """Workspace bytes sage_attn_prefill_varlen needs for these sizes."""
+    a = PrefillVarlenArgs()
+    a.B, a.Hq, a.Hkv, a.D = B, Hq, Hkv, D
+    a.total_q, a.total_k = total_q, total_k
+    a.max_seqlen_q, a.max_seqlen_k = max_seqlen_q, max_seqlen_k
+    a.q_block = a.k_block = 1
+    a.v_dtype = a.out_dtype = SAGE_F16
+    return int(lib().sage_attn_prefill_varlen_workspace_size(ctypes.byref(a)))
 
 
 def sage_attn_prefill_varlen(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: int, v,

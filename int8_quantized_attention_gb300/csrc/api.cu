@@ -574,6 +574,7 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
     p.err = ew;
     char *w = static_cast<char *>(workspace);
     p.BN = L.BN, p.Ppad = L.Ppad, p.Lpad = L.Lpad, p.Vrows = L.Vrows;
+    p.bundle = sage::prefill_bundle(a->B, a->Hq, p.group, L.Lpad, a->D);
     p.k_ws = reinterpret_cast<__half *>(w + L.off_k);
     p.v_ws = L.Vrows ? reinterpret_cast<__half *>(w + L.off_v) : nullptr;
     p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);

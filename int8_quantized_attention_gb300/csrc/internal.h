@@ -151,7 +151,14 @@ struct PrefillParams {
     const int32_t *cu_q, *cu_k;
     int64_t total_q, total_k;
     int64_t v_st, v_sh;
+    // dense form: (batch, head) pairs per scheduling bundle (1 .. B * Hq)
+    int bundle;
 };
+
+// Pairs per bundle of the dense prefill's CTA order: as many KV heads'
+// staged keys and values (f16, rows each) as fit in a share of L2, times
+// the GQA group, so that the heads of one KV head stay together.
+int prefill_bundle(int B, int Hq, int group, int rows, int D);
 
 struct PrefillLayout {
     int BN, Ppad, Lpad, Vrows;

@@ -230,10 +230,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int QR = 128 * NQ;  // query rows per CTA
-    const int hq = blockIdx.y;
-    const int kvh = hq / p.group;
-    int b, ct;
+    int b, hq, ct;
     if constexpr (VL) {
+        hq = blockIdx.y;
         // compact tile index: sequence b owns tiles [cu_q[b] / QR + b, ...),
         // ceil(len_b / QR) of them (at most one spare slot per sequence)
         const int g = blockIdx.x;
@@ -244,10 +243,22 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         const int c = p.cu_q[b];
         ct = g - (int)varlen_group0(c < 0 ? 0 : c, b, QR);  // reversed below
     } else {
+        // one linear CTA index over (batch, head) pairs taken in bundles of
+        // p.bundle (whose staged keys fit in L2 together): within a bundle
+        // the heaviest (causal) query tiles of all its pairs come first, so
+        // that no heavy tile is left to run alone at the end of the grid
         const int nct = (p.Sq + QR - 1) / QR;
-        ct = nct - 1 - (int)blockIdx.x;  // heaviest (causal) tiles first
-        b = blockIdx.z;
+        const int L = blockIdx.x;
+        const int per = nct * p.bundle;
+        const int bun = L / per;
+        const int nb = min(p.bundle, p.B * p.Hq - bun * p.bundle);
+        const int r = L - bun * per;
+        ct = nct - 1 - r / nb;
+        const int u = bun * p.bundle + r % nb;
+        b = u / p.Hq;
+        hq = u % p.Hq;
     }
+    const int kvh = hq / p.group;
 
     // ------------------------------------------------ where this CTA's rows live
     // Sq(), Sk(): this sequence's query and chunk-key counts (the dense form
@@ -837,7 +848,8 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     // sequence, at most total_q / QR + B slots), heads in y
     constexpr int QR = 128 * C::NQ;
     const dim3 grid = VL ? dim3((unsigned)(p.total_q / QR + p.B), p.Hq, 1)
-                         : dim3((p.Sq + QR - 1) / QR, p.Hq, p.B);
+                         : dim3((unsigned)((p.Sq + QR - 1) / QR * p.Hq * p.B), 1, 1);
+    if (!VL && (p.bundle < 1 || p.bundle > p.B * p.Hq)) return cudaErrorInvalidValue;
     prefill_kernel<D, VL><<<grid, C::THREADS, C::SMEM, st>>>(p, m);
     log.add(VL ? "prefill_varlen_kernel" : "prefill_kernel", grid, dim3(C::THREADS), dim3(1, 1, 1),
             C::SMEM);
@@ -850,6 +862,16 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
 }
 
 }  // namespace
+
+int prefill_bundle(int B, int Hq, int group, int rows, int D) {
+    constexpr double kL2Share = 48.0 * 1024 * 1024;  // of the 126 MB L2
+    const double kv = (double)rows * D * 2 * 2;       // f16 K and V of one KV head
+    int kvh = kv > 0 ? (int)(kL2Share / kv) : 1;
+    kvh = kvh < 1 ? 1 : kvh;
+    const long long n = (long long)kvh * group;
+    const long long pairs = (long long)B * Hq;
+    return (int)(n < pairs ? n : pairs);
+}
 
 cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     switch (p.D) {

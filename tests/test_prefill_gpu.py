@@ -177,7 +177,8 @@ def test_prefill_launch_record(sage):
     info = sage.last_launch_info()
     # two 128-row query tiles per CTA at D = 128: one softmax warpgroup each,
     # plus a warpgroup holding the producer and MMA warps
-    assert info["kernel"] == "prefill_kernel" and info["grid"] == (1, 2, 1)
+    # (one linear index over query tiles x heads x batches)
+    assert info["kernel"] == "prefill_kernel" and info["grid"] == (2, 1, 1)
     assert info["block"] == (384, 1, 1)
 
 
@@ -244,5 +245,28 @@ def test_chunked_prefill_full_size_sampled(sage):
                                                   k_scale=pre["k_scale"][:, g:g + 1],
                                                   v_scale=pre["v_scale"][:, g:g + 1]),
                                       rows=rows)
+        assert_close(f32(out)[0, h, rows], o_ref[0, 0], "h%d" % h)
+        assert_close(np_(lse)[0, h, rows], l_ref[0, 0], "lse h%d" % h)
+
+
+def test_prefill_bundled_order_covers_every_tile(sage):
+    """Eight (batch, head) pairs of 16384 keys at D = 256 run in L2-sized
+    bundles of three (3 + 3 + 2): every output row is written exactly by
+    its own tile (rows pre-filled with NaN) and sampled rows of every pair
+    match the oracle."""
+    B, H, S, D = 1, 8, 16384, 256
+    qkv = W.dense_qkv(B, H, H, S, S, D, seed=41, device="cuda")
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    out = torch.full((B, H, S, D), float("nan"), dtype=torch.float16, device="cuda")
+    lse = torch.full((B, H, S), float("nan"), dtype=torch.float32, device="cuda")
+    sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=True, out=out, lse=lse)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert torch.isfinite(out).all() and torch.isfinite(lse).all()
+    rows = np.array([0, 127, 128, 5000, 16383])
+    for h in range(H):
+        o_ref, l_ref = oracle.prefill(np_(qi)[:, h:h + 1], np_(qs)[:, h:h + 1], 1,
+                                      np_(ki)[:, h:h + 1], np_(ks)[:, h:h + 1], 1,
+                                      f32(qkv.v)[:, h:h + 1], causal=True, rows=rows)
         assert_close(f32(out)[0, h, rows], o_ref[0, 0], "h%d" % h)
         assert_close(np_(lse)[0, h, rows], l_ref[0, 0], "lse h%d" % h)
