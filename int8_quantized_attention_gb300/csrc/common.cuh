@@ -169,11 +169,102 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t &lo, uint32_t
 // rounded fp32 division, round to nearest even, clamped to [-127, 127]; an
 // all-zero row (s == 0) gives code 0.  ("INT8 QK MMAC on gfx936 DCU",
 // section 4: q = round(x / s), s = max|x| / 127.)
-__device__ __forceinline__ int8_t quant_code(float v, float s) {
+// Packed FP32 pair arithmetic (fma / mul / add .f32x2 on sm_100-family
+// parts): one instruction updates two values, which halves the FP32 issue
+// slots the softmax spends per score.  Same rounding as the scalar forms.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float2 u2f2(uint32_t a, uint32_t b) {
+    return make_float2(__uint_as_float(a), __uint_as_float(b));
+}
+
+// three-input maximum (one instruction on sm_100-family parts)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Reciprocal of a group scale for quant_code (0 for s = 0).
+__device__ __forceinline__ float quant_recip(float s) { return s != 0.0f ? __frcp_rn(s) : 0.0f; }
+
+// rne(fl32(v / s)) clamped to [-127, 127], with r = quant_recip(s).  The
+// correctly rounded quotient is only needed near a rounding boundary:
+// y = fl32(v * r) differs from fl32(v / s) by at most 3 * 2^-24 * |v / s|,
+// and |v / s| <= 127.00001 because |v| <= amax and s = fl32(amax / 127), so
+// y is within 2.3e-5 of it.  When y lies farther than kTieBand from every
+// k + 0.5, both round to the same integer; otherwise (and for a non-finite
+// or out-of-range y) the division is taken.
+constexpr float kTieBand = 3.0e-5f;
+__device__ __forceinline__ int8_t quant_code(float v, float s, float r) {
     if (s == 0.0f) return 0;
-    int r = __float2int_rn(__fdiv_rn(v, s));
-    r = max(-127, min(127, r));
-    return static_cast<int8_t>(r);
+    const float y = v * r;
+    const float yr = rintf(y);
+    int q;
+    if (fabsf(y) < 128.0f && fabsf(y - yr) < 0.5f - kTieBand)
+        q = (int)yr;
+    else
+        q = __float2int_rn(__fdiv_rn(v, s));
+    q = max(-127, min(127, q));
+    return static_cast<int8_t>(q);
+}
+
+// Eight values at once, the same codes as quant_code, as two little-endian
+// words of int8.  With |y| < 2^22, t = y + 1.5 * 2^23 holds rne(y) in the
+// low bits of its mantissa, so the low byte of t's bits is the two's
+// complement code itself and t - 1.5 * 2^23 is rne(y) as a float; if any of
+// the eight y lies within kTieBand of a rounding boundary (or is not
+// finite) the group is redone through the division.
+__device__ __forceinline__ void quant8(const float (&v)[8], float s, float r, uint32_t &w0,
+                                       uint32_t &w1) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    uint32_t tb[8];
+    float dmax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const float2 y = fmul2(make_float2(v[i], v[i + 1]), make_float2(r, r));
+        const float2 t = fadd2(y, make_float2(kMagic, kMagic));
+        const float2 yr = fadd2(t, make_float2(-kMagic, -kMagic));
+        const float2 d = fadd2(y, make_float2(-yr.x, -yr.y));
+        dmax = fmax3(dmax, fabsf(d.x), fabsf(d.y));
+        tb[i] = __float_as_uint(t.x);
+        tb[i + 1] = __float_as_uint(t.y);
+    }
+    if (dmax < 0.5f - kTieBand) {  // false for NaN
+        w0 = __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
+        w1 = __byte_perm(__byte_perm(tb[4], tb[5], 0x0040), __byte_perm(tb[6], tb[7], 0x0040), 0x5410);
+        return;
+    }
+    w0 = w1 = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w0 |= (uint32_t)(uint8_t)quant_code(v[i], s, r) << (8 * i);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w1 |= (uint32_t)(uint8_t)quant_code(v[i + 4], s, r) << (8 * i);
 }
 
 // Same exact conversion, pairing bytes (0, 2) and (1, 3): for a register

@@ -249,13 +249,14 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
 #pragma unroll
                 for (int o = 1; o < 16; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
                 const float sq = __fdiv_rn(amax, 127.0f);
+                const float rq = quant_recip(sq);
                 if (hh < 8) {
 #pragma unroll
                     for (int e = 0; e < cpl; e += 4) {
                         uint32_t w = 0;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            w |= (uint32_t)(uint8_t)quant_code(f[e + k], sq) << (8 * k);
+                            w |= (uint32_t)(uint8_t)quant_code(f[e + k], sq, rq) << (8 * k);
                         *reinterpret_cast<uint32_t *>(q_s + hh * D + c0 + e) = w;
                     }
                     if ((lane & 15) == 0) qsc_s[hh] = sq;

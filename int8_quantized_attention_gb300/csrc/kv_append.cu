@@ -59,10 +59,11 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendParams p) {
     for (int e = 0; e < CPL; ++e) amax = fmaxf(amax, fabsf(f[e]));
     amax = warp_max(amax);
     const float s = __fdiv_rn(amax, 127.0f);
+    const float rs = quant_recip(s);
     uint32_t w[2] = {0u, 0u};
 #pragma unroll
     for (int e = 0; e < CPL; ++e)
-        w[e >> 2] |= (uint32_t)(uint8_t)quant_code(f[e], s) << (8 * (e & 3));
+        w[e >> 2] |= (uint32_t)(uint8_t)quant_code(f[e], s, rs) << (8 * (e & 3));
     const int c0 = lane * CPL;
     const int64_t slot = pos & 15;
     const int64_t page = (int64_t)blk * p.H + h;

@@ -87,3 +87,29 @@ def test_quant_decode_query_full_size(sage):
     P = W.WORKLOADS["paged_decode"].params
     q = W.decode_query(P["B"], P["Hq"], P["D"], seed=P["seed"], device="cuda")
     _check_quant(sage, q[:, :, None, :], 1)
+
+
+def test_quant_exact_ties_with_non_power_of_two_scales(sage):
+    """amax = 127 m gives s = m exactly; x = m (k + 1/2) makes x / s an exact
+    tie, where x * fl32(1/m) lands a hair above or below it.  The codes must
+    follow the correctly rounded quotient (ties to even), and so must values
+    one f16 step either side of each tie."""
+    D = 64
+    rows = []
+    # scales where x * fl32(1/s) misrounds up to 78 of the 254 ties
+    for m in (0.4375, 0.9375, 1.625, 3.5, 7.0, 15.0):
+        ties = np.array([m * (k + 0.5) for k in range(-127, 127)], np.float32)
+        ties = ties[np.abs(ties) < 127 * m]
+        vals = np.concatenate([ties, np.nextafter(ties.astype(np.float16), np.float16(np.inf)).astype(np.float32),
+                               np.nextafter(ties.astype(np.float16), np.float16(-np.inf)).astype(np.float32)])
+        vals = vals[np.abs(vals) < 127 * m]
+        vals = vals[(vals.astype(np.float16).astype(np.float32) == vals)]
+        for i in range(0, len(vals), D - 1):
+            row = np.zeros(D, np.float32)
+            chunk = vals[i:i + D - 1]
+            row[0] = 127 * m
+            row[1:1 + len(chunk)] = chunk
+            rows.append(row)
+    x = torch.tensor(np.stack(rows)[None, None], dtype=torch.float16, device="cuda")
+    _check_quant(sage, x, 1)
+    _check_quant(sage, x, 64)
