@@ -264,6 +264,25 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         if constexpr (VL) return vsc0 + (i >> p.q_shift);
         return ((int64_t)b * p.Hq + hq) * p.q_groups + (i >> p.q_shift);
     };
+    // The same rows for use after the key loop.  Dense: (b, hq) come from
+    // the linear CTA index, so the pair index b * Hq + hq is recomputed from
+    // a fresh read of it rather than kept live through the softmax loop.
+    auto late_pair = [&]() -> int64_t {
+        int L;
+        asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(L));
+        const int per = (p.Sq + QR - 1) / QR * p.bundle;
+        const int bun = L / per;
+        const int nb = min(p.bundle, p.B * p.Hq - bun * p.bundle);
+        return (int64_t)bun * p.bundle + (L - bun * per) % nb;
+    };
+    auto q_row_late = [&](int i) -> int64_t {
+        if constexpr (VL) return vq_row0 + i;
+        return late_pair() * p.Sq + i;
+    };
+    auto out_row_late = [&](int i) -> int64_t {
+        if constexpr (VL) return (qs + i) * p.Hq + hq;
+        return late_pair() * p.Sq + i;
+    };
     const int i0 = ct * QR;
 
     // ------------------------------------------------------ tile schedule
@@ -554,7 +573,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             if (p.dbg) {
                 // debug dump of the raw INT32 scores, re-read from TMEM in
                 // 8-column pieces so that it adds no live registers here
-                int32_t *dr = p.dbg + q_row(i) * p.dbg_stride;
+                int32_t *dr = p.dbg + q_row_late(i) * p.dbg_stride;
 #pragma unroll 1
                 for (int c8 = 0; c8 < CW / 8; ++c8) {
                     uint32_t v[8];
@@ -717,7 +736,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             tc::fence_after();
         }
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const int64_t orow = q_row(i);
+        const int64_t orow = q_row_late(i);
+        uint16_t *obase = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i) * D;
 #pragma unroll 1
         for (int c = hc * (D / 32 / SPLIT); c < (hc + 1) * (D / 32 / SPLIT); ++c) {
             uint32_t o[32];
@@ -735,8 +755,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     const float2 v = fmul2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv));
                     pk[e] = pack2(v.x, v.y, p.out_bf16 != 0);
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out) +
-                                                       out_row(i) * D + c * 32);
+                uint4 *dst = reinterpret_cast<uint4 *>(obase + c * 32);
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
