@@ -205,7 +205,7 @@ def _run(jobs, threads):
 
 
 def prefill(q_i8, q_scale, q_block, k_i8, k_scale, k_block, v, *, causal, sm_scale=None,
-            q_bias=None, prefix=None, rows=None, threads=None):
+            q_bias=None, prefix=None, rows=None, threads=None, smooth_v=False):
     """Prefill attention, optionally over a paged INT8 prefix.
 
     q_i8 [B,Hq,Sq,D] int8, q_scale [B,Hq,ceil(Sq/q_block)] fp32;
@@ -219,6 +219,11 @@ def prefill(q_i8, q_scale, q_block, k_i8, k_scale, k_block, v, *, causal, sm_sca
     Causal alignment is bottom-right: key j is visible to query i iff
     j <= i + (Sk - Sq), Sk = prefix + chunk length.
     rows: optional query-row indices to evaluate (same for every b, h).
+    smooth_v ([P3] "V mean fusion"): mu = the chunk's per-(b, kv head,
+    channel) mean of V (token_mean, rounded to fp32) is subtracted from every
+    value the rows attend to (prefix included) and added back to the output;
+    a row that sees no key keeps o = 0.  In exact arithmetic the result is
+    unchanged (each softmax row sums to 1); the kernels gain precision.
     Returns (o fp64 [B,Hq,R,D], lse fp64 [B,Hq,R]).
     """
     q_i8 = np.asarray(q_i8)
@@ -234,6 +239,7 @@ def prefill(q_i8, q_scale, q_block, k_i8, k_scale, k_block, v, *, causal, sm_sca
     v = np.asarray(v, np.float64)
     sq_full = expand_scale(q_scale, Sq, q_block)
     sk_full = expand_scale(k_scale, Sc, k_block)
+    mu_v = token_mean(np.asarray(v, np.float32)).astype(np.float64) if smooth_v else None
     jobs = []
     for b in range(B):
         P = 0 if prefix is None else int(prefix["lens"][b])
@@ -253,13 +259,19 @@ def prefill(q_i8, q_scale, q_block, k_i8, k_scale, k_block, v, *, causal, sm_sca
             smoothed = None
             if q_bias is not None:
                 smoothed = np.concatenate([np.zeros(P, np.uint8), np.ones(Sc, np.uint8)])
+            mu = None if mu_v is None else mu_v[b, g]
+            if mu is not None:
+                vals = vals - mu[None, :]
             for h in range(g * group, (g + 1) * group):
-                def job(b=b, h=h, keys=keys, sks=sks, vals=vals, smoothed=smoothed, P=P):
+                def job(b=b, h=h, keys=keys, sks=sks, vals=vals, smoothed=smoothed, P=P, mu=mu):
                     qb = None if q_bias is None else np.asarray(q_bias)[b, h, rows]
                     ob, lb = attend(q_i8[b, h, rows], sq_full[b, h, rows], keys, sks, vals,
                                     sm_scale=sm_scale, causal=causal,
                                     causal_offset=P + Sc - Sq, qpos=rows, qbias=qb,
                                     smoothed=smoothed)
+                    if mu is not None:
+                        seen = np.isfinite(lb)
+                        ob = np.where(seen[:, None], ob + mu[None, :], 0.0)
                     o[b, h] = ob
                     lse[b, h] = lb
                 jobs.append(job)
@@ -397,7 +409,7 @@ def row_bias_varlen(x, cu_seqlens, mu):
 
 def prefill_varlen(q_i8, q_scales, q_block, k_i8, k_scales, k_block, v, cu_seqlens_q,
                    cu_seqlens_k, *, causal, sm_scale=None, q_bias=None, rows=None,
-                   threads=None):
+                   threads=None, smooth_v=False):
     """Prefill attention over a packed batch, one single-sequence call each.
 
     q_i8 int8 [Hq, total_q, D]; q_scales list of fp32 [Hq, ceil(len_q_b / q_block)];
@@ -427,7 +439,8 @@ def prefill_varlen(q_i8, q_scales, q_block, k_i8, k_scales, k_block, v, cu_seqle
         ob, lb = prefill(q_i8[None, :, q0:q1], np.asarray(q_scales[b])[None], q_block,
                          np.asarray(k_i8)[None, :, k0:k1], np.asarray(k_scales[b])[None], k_block,
                          np.asarray(v)[k0:k1].transpose(1, 0, 2)[None], causal=causal,
-                         sm_scale=sm_scale, q_bias=qb, rows=sel, threads=threads)
+                         sm_scale=sm_scale, q_bias=qb, rows=sel, threads=threads,
+                         smooth_v=smooth_v)
         idx = np.arange(q1 - q0) if sel is None else np.asarray(sel, np.int64)
         o[q0 + idx] = ob[0].transpose(1, 0, 2)
         lse[:, q0 + idx] = lb[0]

@@ -571,3 +571,52 @@ def test_varlen_values_never_leak_across_sequences():
         o, _ = oracle.prefill_varlen(q, qs, 1, k, ks, 1, v, cu_q, cu_k, causal=causal)
         for b in range(3):
             np.testing.assert_allclose(o[cu_q[b]:cu_q[b + 1]], consts[b], rtol=1e-13)
+
+
+# --------------------------------------------------------------------------
+# smooth_v: subtract the chunk's V mean from every value, add it back
+# --------------------------------------------------------------------------
+
+def test_smooth_v_is_exact_identity_with_prefix_and_empty_rows():
+    # softmax rows sum to 1, so P (V - mu) + mu = P V: smoothing changes no
+    # output in exact arithmetic, with or without a paged prefix, and a row
+    # that sees no key stays 0 (a forgotten add-back, a wrong sign or a mean
+    # taken off the chunk only would all show here: V has a large offset)
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, Sq, Sk, D = 1, 4, 2, 40, 24, 64
+    q = rng.integers(-127, 128, (B, Hq, Sq, D)).astype(np.int8)
+    k = rng.integers(-127, 128, (B, Hkv, Sk, D)).astype(np.int8)
+    qs = rng.uniform(0.001, 0.002, (B, Hq, Sq)).astype(np.float32)
+    ks = rng.uniform(0.001, 0.002, (B, Hkv, Sk)).astype(np.float32)
+    v = (rng.standard_normal((B, Hkv, Sk, D)) + 50.0).astype(np.float32)
+    P = 32
+    pre = dict(k_cache=rng.integers(-127, 128, (4, Hkv, D // 16, 16, 16)).astype(np.int8),
+               v_cache=rng.integers(-127, 128, (4, Hkv, D // 16, 16, 16)).astype(np.int8),
+               k_scale=rng.uniform(0.001, 0.002, (4, Hkv, 16)).astype(np.float32),
+               v_scale=rng.uniform(0.005, 0.02, (4, Hkv, 16)).astype(np.float32),
+               block_table=np.array([[2, 0, 3, 1]], np.int32), lens=np.array([P]))
+    for prefix in (None, pre):
+        # Sq > Sk + P: the first causal rows see no key at all
+        o0, l0 = oracle.prefill(q, qs, 1, k, ks, 1, v, causal=True, prefix=prefix)
+        o1, l1 = oracle.prefill(q, qs, 1, k, ks, 1, v, causal=True, prefix=prefix, smooth_v=True)
+        assert np.array_equal(l0, l1)
+        np.testing.assert_allclose(o1, o0, rtol=0, atol=1e-11)
+        empty = ~np.isfinite(l0)
+        assert np.all(o1[empty] == 0)
+        if prefix is None:
+            assert empty.any()   # Sq > Sk: the first 16 rows see nothing
+
+
+def test_smooth_v_mean_is_the_chunk_token_mean():
+    # the subtracted mean is token_mean of the chunk values: with V constant
+    # along tokens every smoothed value is 0, so only the add-back remains
+    rng = np.random.default_rng(32)
+    D = 64
+    v = np.broadcast_to(rng.uniform(-3, 3, (1, 1, 1, D)), (1, 1, 20, D)).astype(np.float32)
+    mu = oracle.token_mean(v)
+    assert np.array_equal(mu[0, 0], v[0, 0, 0])
+    q = rng.integers(-127, 128, (1, 1, 20, D)).astype(np.int8)
+    k = rng.integers(-127, 128, (1, 1, 20, D)).astype(np.int8)
+    s = np.full((1, 1, 20), 0.01, np.float32)
+    o, _ = oracle.prefill(q, s, 1, k, s, 1, v, causal=False, smooth_v=True)
+    np.testing.assert_allclose(o[0, 0], np.broadcast_to(v[0, 0, 0], (20, D)), rtol=0, atol=1e-15)
