@@ -60,7 +60,7 @@ typedef enum sage_dtype {
 const char *sage_get_last_error_message(void);
 
 /* Library ABI version (increments on any signature change). */
-int sage_version(void);   /* 5 */
+int sage_version(void);   /* 6 */
 
 /* --------------------------------------------------------------------------
  * Quantisation  ([P1] section 4; [P3] quant kernel table, feature matrix)
@@ -298,6 +298,14 @@ sage_status_t sage_splitk_combine(const float *o_part, const float *lse_part, in
  * q_bias (from sage_quant_int8's bias_out with the K mean) restores the
  * scores of smoothed chunk keys; with no prefix it only shifts the LSE
  * ([P3]'s LSE correction).
+ * smooth_v ([P3] feature matrix "V mean fusion", SubMean kernel, output
+ * stage "V mean added back"): mu[b,kvh,c] = mean over the chunk's Sk
+ * tokens of v[b,kvh,:,c] (exact sum rounded once to fp32, as smooth_k's
+ * mean) is subtracted from every value the rows attend to (prefix included,
+ * rounded to f16 after an fp32 subtraction) and added to o_i; a row that
+ * sees no key keeps o_i = 0.  The result equals the unsmoothed one in exact
+ * arithmetic; the f16 P.V operand carries (v - mu) instead of v.  v_mean
+ * (optional, [B, Hkv, D] fp32) receives mu.
  * ------------------------------------------------------------------------ */
 typedef struct sage_prefill_args {
     int B, Hq, Hkv, Sq, Sk, D;      /* D = 64, 128 or 256; Sk may be 0 with a prefix */
@@ -321,6 +329,8 @@ typedef struct sage_prefill_args {
     void *out;                      /* [B, Hq, Sq, D] */
     sage_dtype_t out_dtype;
     float *lse;                     /* optional [B, Hq, Sq] */
+    int smooth_v;                   /* subtract the chunk's V mean, add it back to o */
+    float *v_mean;                  /* optional out [B, Hkv, D] fp32 (smooth_v) */
 } sage_prefill_args_t;
 
 /* Workspace of sage_attn_prefill (host only): the tensor cores of sm_103a
@@ -378,6 +388,8 @@ typedef struct sage_prefill_varlen_args {
     void *out;
     sage_dtype_t out_dtype;
     float *lse;
+    int smooth_v;                   /* per-sequence V mean, as sage_attn_prefill's */
+    float *v_mean;                  /* optional out [B, Hkv, D] fp32 (smooth_v) */
 } sage_prefill_varlen_args_t;
 
 /* Workspace bytes of sage_attn_prefill_varlen (host only): the f16 copy of

@@ -55,7 +55,8 @@ class PrefillArgs(ctypes.Structure):
                 ("k_cache", _vp), ("v_cache", _vp), ("k_cache_scale", _vp), ("v_cache_scale", _vp),
                 ("block_table", _vp), ("prefix_lens", _vp),
                 ("num_blocks", _i), ("max_blocks", _i), ("max_prefix_len", _i),
-                ("causal", _i), ("sm_scale", _f), ("out", _vp), ("out_dtype", _i), ("lse", _vp)]
+                ("causal", _i), ("sm_scale", _f), ("out", _vp), ("out_dtype", _i), ("lse", _vp),
+                ("smooth_v", _i), ("v_mean", _vp)]
 
 
 class PrefillVarlenArgs(ctypes.Structure):
@@ -66,7 +67,7 @@ class PrefillVarlenArgs(ctypes.Structure):
                 ("k", _vp), ("k_scale", _vp), ("k_block", _i),
                 ("v", _vp), ("v_dtype", _i), ("v_stride_t", _i64), ("v_stride_h", _i64),
                 ("q_bias", _vp), ("causal", _i), ("sm_scale", _f), ("out", _vp), ("out_dtype", _i),
-                ("lse", _vp)]
+                ("lse", _vp), ("smooth_v", _i), ("v_mean", _vp)]
 
 
 class LaunchInfo(ctypes.Structure):
@@ -386,13 +387,16 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
                       causal: bool, sm_scale=None, q_bias=None, prefix: Optional[dict] = None,
                       out_dtype=None, return_lse: bool = False, debug_scores=None,
                       workspace: Optional[torch.Tensor] = None, out=None, lse=None,
+                      smooth_v: bool = False, v_mean: Optional[torch.Tensor] = None,
                       stream=None):
     """INT8-QK prefill attention over an optional paged INT8 prefix + a chunk.
 
     q_int8 [B,Hq,Sq,D]; q_scale [B,Hq,ceil(Sq/q_block)]; k_int8 [B,Hkv,Sk,D];
     k_scale [B,Hkv,ceil(Sk/k_block)]; v [B,Hkv,Sk,D] f16/bf16; q_bias [B,Hq,Sq]
     (smooth_k correction) or None; prefix = dict(k_cache, v_cache, k_scale,
-    v_scale, block_table, lens, max_len) or None.
+    v_scale, block_table, lens, max_len) or None.  smooth_v subtracts the
+    chunk's V mean from every value and adds it back to the output; v_mean
+    ([B, Hkv, D] fp32, optional) receives that mean.
     """
     B, Hq, Sq, D = q_int8.shape
     Hkv, Sk = k_int8.shape[1], k_int8.shape[2]
@@ -436,6 +440,9 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
     a.causal = int(bool(causal))
     a.sm_scale = float(sm_scale) if sm_scale else 0.0
     a.out, a.out_dtype, a.lse = _ptr(out), _dt(out_dtype), _ptr(lse)
+    if v_mean is not None:
+        _need(v_mean, torch.float32, "v_mean")
+    a.smooth_v, a.v_mean = int(bool(smooth_v)), _ptr(v_mean)
     need = int(lib().sage_attn_prefill_workspace_size(ctypes.byref(a)))
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q_int8.device)
@@ -492,9 +499,11 @@ def sage_quant_int8_varlen(x: torch.Tensor, cu_seqlens: torch.Tensor, max_seqlen
 
 
 def prefill_varlen_workspace_size(B: int, Hq: int, Hkv: int, D: int, total_q: int, total_k: int,
-                                  max_seqlen_q: int, max_seqlen_k: int) -> int:
+                                  max_seqlen_q: int, max_seqlen_k: int,
+                                  smooth_v: bool = False) -> int:
     """Workspace bytes sage_attn_prefill_varlen needs for these sizes."""
     a = PrefillVarlenArgs()
+    a.smooth_v = int(bool(smooth_v))
     a.B, a.Hq, a.Hkv, a.D = B, Hq, Hkv, D
     a.total_q, a.total_k = total_q, total_k
     a.max_seqlen_q, a.max_seqlen_k = max_seqlen_q, max_seqlen_k
@@ -507,7 +516,8 @@ def sage_attn_prefill_varlen(q_int8, q_scale, q_block: int, k_int8, k_scale, k_b
                              cu_seqlens_q, cu_seqlens_k, max_seqlen_q: int, max_seqlen_k: int, *,
                              causal: bool, sm_scale=None, q_bias=None, out_dtype=None,
                              return_lse: bool = False, debug_scores=None,
-                             workspace: Optional[torch.Tensor] = None, stream=None):
+                             workspace: Optional[torch.Tensor] = None, smooth_v: bool = False,
+                             v_mean: Optional[torch.Tensor] = None, stream=None):
     """INT8-QK prefill attention over a packed variable-length batch.
 
     q_int8 [Hq, total_q, D]; q_scale [Hq, groups_q]; k_int8 [Hkv, total_k, D];
@@ -547,6 +557,9 @@ def sage_attn_prefill_varlen(q_int8, q_scale, q_block: int, k_int8, k_scale, k_b
     a.causal = int(bool(causal))
     a.sm_scale = float(sm_scale) if sm_scale else 0.0
     a.out, a.out_dtype, a.lse = _ptr(out), _dt(out_dtype), _ptr(lse)
+    if v_mean is not None:
+        _need(v_mean, torch.float32, "v_mean")
+    a.smooth_v, a.v_mean = int(bool(smooth_v)), _ptr(v_mean)
     need = int(lib().sage_attn_prefill_varlen_workspace_size(ctypes.byref(a)))
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)

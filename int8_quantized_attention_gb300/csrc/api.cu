@@ -112,7 +112,7 @@ void record_launch(const LaunchLog &log) { g_last = log; }
 
 SAGE_API const char *sage_get_last_error_message(void) { return g_msg.c_str(); }
 
-SAGE_API int sage_version(void) { return 5; }
+SAGE_API int sage_version(void) { return 6; }
 
 SAGE_API sage_status_t sage_last_launch_info(sage_launch_info_t *info) {
     if (!info) return fail(SAGE_ERR_INVALID_ARG, "info is NULL");
@@ -515,7 +515,7 @@ SAGE_API size_t sage_attn_prefill_workspace_size(const sage_prefill_args_t *a) {
     int qs = 0, ks = 0;
     if (check_prefill(a, &qs, &ks) != SAGE_OK) return 0;
     return sage::prefill_layout(a->B, a->Hkv, a->Sk, a->D, a->max_prefix_len,
-                                a->v_dtype == SAGE_BF16)
+                                a->v_dtype == SAGE_BF16, a->smooth_v != 0)
         .bytes;
 }
 
@@ -541,8 +541,13 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
     if (!aligned(a->q, 16) || (a->k && !aligned(a->k, 16)) || (a->v && !aligned(a->v, 16)) ||
         !aligned(a->out, 16))
         return fail(SAGE_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
+    if (a->smooth_v && (int64_t)a->B * a->Hkv > 65535)
+        return fail(SAGE_ERR_UNSUPPORTED, "smooth_v supports at most 65535 (batch, kv head) pairs");
+    if (a->v_mean && !aligned(a->v_mean, 16))
+        return fail(SAGE_ERR_INVALID_ARG, "v_mean must be 16-byte aligned");
     const sage::PrefillLayout L = sage::prefill_layout(a->B, a->Hkv, a->Sk, a->D,
-                                                       a->max_prefix_len, a->v_dtype == SAGE_BF16);
+                                                       a->max_prefix_len, a->v_dtype == SAGE_BF16,
+                                                       a->smooth_v != 0);
     if (!workspace || workspace_bytes < L.bytes)
         return fail(SAGE_ERR_INVALID_ARG, "workspace too small: need %zu bytes", L.bytes);
     if (!aligned(workspace, 256)) return fail(SAGE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -580,7 +585,22 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
     p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);
     cudaStream_t cst = static_cast<cudaStream_t>(stream);
     sage::LaunchLog stage_log;
-    cudaError_t e = sage::launch_prefill_stage(p, cst, stage_log);
+    cudaError_t e = cudaSuccess;
+    if (a->smooth_v) {
+        // the chunk's V mean per (batch, kv head), the smooth_k mean kernel's
+        float *mu = a->v_mean ? a->v_mean : reinterpret_cast<float *>(w + L.off_vmean);
+        sage::QuantParams mp = {};
+        mp.x = a->v;
+        mp.bf16 = a->v_dtype == SAGE_BF16;
+        mp.B = a->B, mp.H = a->Hkv, mp.S = a->Sk, mp.D = a->D;
+        mp.sb = (int64_t)a->Hkv * a->Sk * a->D, mp.sh = (int64_t)a->Sk * a->D, mp.ss = a->D;
+        mp.smooth = 1;
+        mp.mu_out = mu;
+        e = sage::launch_token_mean(mp, cst, stage_log);
+        if (e != cudaSuccess) return cuda_fail(e, "V mean launch");
+        p.v_mean = mu;
+    }
+    e = sage::launch_prefill_stage(p, cst, stage_log);
     if (e != cudaSuccess) return cuda_fail(e, "prefill staging launch");
     e = sage::launch_prefill(p, cst, g_last);
     g_last.count += stage_log.count;
@@ -634,7 +654,7 @@ static sage_status_t check_prefill_varlen(const sage_prefill_varlen_args_t *a, i
 SAGE_API size_t sage_attn_prefill_varlen_workspace_size(const sage_prefill_varlen_args_t *a) {
     int qs = 0, ks = 0;
     if (check_prefill_varlen(a, &qs, &ks) != SAGE_OK) return 0;
-    return sage::prefill_layout_varlen(a->B, a->Hkv, a->total_k, a->D).bytes;
+    return sage::prefill_layout_varlen(a->B, a->Hkv, a->total_k, a->D, a->smooth_v != 0).bytes;
 }
 
 static sage_status_t run_prefill_varlen(const sage_prefill_varlen_args_t *a, void *workspace,
@@ -655,7 +675,12 @@ static sage_status_t run_prefill_varlen(const sage_prefill_varlen_args_t *a, voi
     if (!aligned(a->q, 16) || (a->k && !aligned(a->k, 16)) || (a->v && !aligned(a->v, 16)) ||
         !aligned(a->out, 16))
         return fail(SAGE_ERR_INVALID_ARG, "q, k, v and out must be 16-byte aligned");
-    const sage::PrefillLayout L = sage::prefill_layout_varlen(a->B, a->Hkv, a->total_k, a->D);
+    if (a->smooth_v && (int64_t)a->B * a->Hkv > 65535)
+        return fail(SAGE_ERR_UNSUPPORTED, "smooth_v supports at most 65535 (sequence, kv head) pairs");
+    if (a->v_mean && !aligned(a->v_mean, 16))
+        return fail(SAGE_ERR_INVALID_ARG, "v_mean must be 16-byte aligned");
+    const sage::PrefillLayout L =
+        sage::prefill_layout_varlen(a->B, a->Hkv, a->total_k, a->D, a->smooth_v != 0);
     if (!workspace || workspace_bytes < L.bytes)
         return fail(SAGE_ERR_INVALID_ARG, "workspace too small: need %zu bytes", L.bytes);
     if (!aligned(workspace, 256)) return fail(SAGE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -689,7 +714,23 @@ static sage_status_t run_prefill_varlen(const sage_prefill_varlen_args_t *a, voi
     p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);
     cudaStream_t cst = static_cast<cudaStream_t>(stream);
     sage::LaunchLog stage_log;
-    cudaError_t e = sage::launch_prefill_stage(p, cst, stage_log);
+    cudaError_t e = cudaSuccess;
+    if (a->smooth_v) {
+        // each sequence's V mean per kv head
+        float *mu = a->v_mean ? a->v_mean : reinterpret_cast<float *>(w + L.off_vmean);
+        sage::QuantParams mp = {};
+        mp.x = a->v;
+        mp.bf16 = a->v_dtype == SAGE_BF16;
+        mp.B = a->B, mp.H = a->Hkv, mp.S = a->max_seqlen_k, mp.D = a->D;
+        mp.sh = vsh, mp.ss = vst;
+        mp.smooth = 1;
+        mp.mu_out = mu;
+        mp.cu = a->cu_seqlens_k, mp.total = a->total_k, mp.err = ew;
+        e = sage::launch_token_mean(mp, cst, stage_log);
+        if (e != cudaSuccess) return cuda_fail(e, "varlen V mean launch");
+        p.v_mean = mu;
+    }
+    e = sage::launch_prefill_stage(p, cst, stage_log);
     if (e != cudaSuccess) return cuda_fail(e, "varlen prefill staging launch");
     e = sage::launch_prefill(p, cst, g_last);
     g_last.count += stage_log.count;

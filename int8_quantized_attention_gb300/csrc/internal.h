@@ -51,6 +51,8 @@ struct QuantParams {
 };
 
 cudaError_t launch_quant(const QuantParams &p, cudaStream_t st, LaunchLog &log);
+// The smooth_k mean pass alone: mu_out[b, h, :] over x's tokens.
+cudaError_t launch_token_mean(const QuantParams &p, cudaStream_t st, LaunchLog &log);
 
 struct CombineParams {
     const float *o_part;      // [R, S, D]
@@ -153,6 +155,9 @@ struct PrefillParams {
     int64_t v_st, v_sh;
     // dense form: (batch, head) pairs per scheduling bundle (1 .. B * Hq)
     int bundle;
+    // smooth_v: per (batch or sequence, kv head) V mean [B * Hkv][D], subtracted
+    // from the staged values and added back to the output; null when off
+    const float *v_mean;
 };
 
 // Pairs per bundle of the dense prefill's CTA order: as many KV heads'
@@ -162,11 +167,12 @@ int prefill_bundle(int B, int Hq, int group, int rows, int D);
 
 struct PrefillLayout {
     int BN, Ppad, Lpad, Vrows;
-    size_t off_k, off_v, off_ksc, bytes;
+    size_t off_k, off_v, off_ksc, off_vmean, bytes;  // off_vmean: smooth_v's mean [B*Hkv][D]
 };
 
-PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16);
-PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D);
+PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16,
+                             bool smooth_v);
+PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D, bool smooth_v);
 cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
 cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
 

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     // reads the kernel parameters at each use, which keeps them out of the
     // registers); kz, krow0: the staged keys' (head, first row) coordinates.
     int vsq = 0, vsk = 0;
-    int64_t qs = 0, vq_row0 = 0, vsc0 = 0;
+    int64_t qs = 0, vq_row0 = 0, vsc0 = 0, vmu_vl = 0;
     int kz = b * p.Hkv + kvh, krow0 = 0;
     auto Sq = [&]() -> int {
         if constexpr (VL) return vsq;
@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         vsc0 = (int64_t)hq * p.q_groups + varlen_group0(qs, b, 1 << p.q_shift);
         kz = kvh;
         krow0 = (int)varlen_key_row0(ks, b, BN);
+        vmu_vl = ((int64_t)b * p.Hkv + kvh) * D;
     }
     // row of query i in q, q_bias, lse and the debug dump ([Hq, total_q]
     // packed, [B, Hq, Sq] dense); its output row (packed output is
@@ -282,6 +283,13 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     auto out_row_late = [&](int i) -> int64_t {
         if constexpr (VL) return (qs + i) * p.Hq + hq;
         return late_pair() * p.Sq + i;
+    };
+    // smooth_v: this (batch or sequence, kv head)'s V mean row
+    auto v_mean_late = [&]() -> const float * {
+        if constexpr (VL) return p.v_mean + vmu_vl;
+        const int64_t u = late_pair();
+        const int64_t bb = u / p.Hq, kv = (u % p.Hq) / p.group;
+        return p.v_mean + (bb * p.Hkv + kv) * D;
     };
     const int i0 = ct * QR;
 
@@ -338,7 +346,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             tc::prefetch_tmap(&maps.k);
             if (n_pre > 0) tc::prefetch_tmap(&maps.v_pre);
             if (n_ch > 0) tc::prefetch_tmap(&maps.v_ch);
-            const int vch_off = p.v_bf16 ? p.Ppad : 0;
+            // chunk values staged after the prefix (bf16 or smoothed V), or
+            // read in place from the caller's f16 V
+            const int vch_off = (p.v_bf16 || p.v_mean) ? p.Ppad : 0;
             int issued = 0;
             for (int jj = 0; jj < T; ++jj) {
                 const int s = jj % NST;
@@ -738,6 +748,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const int64_t orow = q_row_late(i);
         uint16_t *obase = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i) * D;
+        // smooth_v: the V mean goes back onto rows that saw a key
+        const float *vmu = (p.v_mean && l > 0.0f) ? v_mean_late() : nullptr;
 #pragma unroll 1
         for (int c = hc * (D / 32 / SPLIT); c < (hc + 1) * (D / 32 / SPLIT); ++c) {
             uint32_t o[32];
@@ -750,10 +762,24 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             }
             if (row_ok) {
                 uint32_t pk[16];
+                if (vmu) {
+                    const float4 *m4 = reinterpret_cast<const float4 *>(vmu + c * 32);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float2 v = fmul2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv));
-                    pk[e] = pack2(v.x, v.y, p.out_bf16 != 0);
+                    for (int e = 0; e < 16; e += 2) {
+                        const float4 m = m4[e / 2];
+                        const float2 v0 = ffma2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv),
+                                                make_float2(m.x, m.y));
+                        const float2 v1 = ffma2(u2f2(o[2 * e + 2], o[2 * e + 3]),
+                                                make_float2(inv, inv), make_float2(m.z, m.w));
+                        pk[e] = pack2(v0.x, v0.y, p.out_bf16 != 0);
+                        pk[e + 1] = pack2(v1.x, v1.y, p.out_bf16 != 0);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float2 v = fmul2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv));
+                        pk[e] = pack2(v.x, v.y, p.out_bf16 != 0);
+                    }
                 }
                 uint4 *dst = reinterpret_cast<uint4 *>(obase + c * 32);
 #pragma unroll
@@ -814,7 +840,7 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     if (!make_map<D>(&m.k, p.k_ws, p.Lpad, bh)) return cudaErrorInvalidValue;
     if (p.Vrows > 0 && !make_map<D>(&m.v_pre, p.v_ws, p.Vrows, bh)) return cudaErrorInvalidValue;
     if (p.Sk > 0) {
-        if (p.v_bf16 || p.cu_q)
+        if (p.v_bf16 || p.cu_q || p.v_mean)
             m.v_ch = m.v_pre;
         else if (!make_map<D>(&m.v_ch, p.v, p.Sk, bh))
             return cudaErrorInvalidValue;

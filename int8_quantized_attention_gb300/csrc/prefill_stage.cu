@@ -8,7 +8,9 @@
 // operand); K codes stay exact.
 // Workspace rows per (batch, kv head), in key order: [0, Ppad) the paged
 // prefix (key r at row r; rows past the batch's prefix length are zero),
-// [Ppad, Ppad + Sk) the contiguous chunk, then zero rows up to Lpad.  The
+// [Ppad, Ppad + Sk) the contiguous chunk, then zero rows up to Lpad.  With
+// smooth_v every staged value is f16(value - V mean of its channel), the
+// chunk's f16 values included.  The
 // INT8 -> f16 expansion is exact (|code| <= 127), so S = Q K^T computed on
 // the copy equals the INT32 product of the codes ("INT8 QK MMAC on gfx936
 // DCU", sections 2.1 and 5.2: the scores are exact integer dot products,
@@ -49,6 +51,40 @@ __device__ __forceinline__ void store_f16x16_scaled(__half *dst, uint4 w, float 
     uint4 *d = reinterpret_cast<uint4 *>(dst);
     d[0] = make_uint4(h[0], h[1], h[2], h[3]);
     d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// 16 values minus the V mean of their channels -> f16 (round to nearest,
+// saturating); mu points at the 16 channels' means
+__device__ __forceinline__ void store_f16x16_minus(__half *dst, const float (&v)[16],
+                                                   const float *mu) {
+    uint32_t h[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float a = fminf(fmaxf(v[2 * e] - mu[2 * e], -65504.0f), 65504.0f);
+        const float b = fminf(fmaxf(v[2 * e + 1] - mu[2 * e + 1], -65504.0f), 65504.0f);
+        __half2 x = __floats2half2_rn(a, b);
+        h[e] = *reinterpret_cast<uint32_t *>(&x);
+    }
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+}
+
+// 16 consecutive f16 or bf16 values as floats
+__device__ __forceinline__ void load16f(const void *src, bool bf16, float (&v)[16]) {
+    const uint4 *s = reinterpret_cast<const uint4 *>(src);
+    const uint4 w[2] = {s[0], s[1]};
+    const uint32_t *u = reinterpret_cast<const uint32_t *>(w);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        float2 f;
+        if (bf16)
+            f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&u[e]));
+        else
+            f = __half22float2(*reinterpret_cast<const __half2 *>(&u[e]));
+        v[2 * e] = f.x;
+        v[2 * e + 1] = f.y;
+    }
 }
 
 // 8 bf16 -> 8 f16, round to nearest, saturating to the finite f16 range
@@ -104,7 +140,16 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
         store_f16x16(p.k_ws + ((int64_t)bh * p.Lpad + row) * D + dc * 16, wk);
         // prefix values: the per-token V scale is applied here, once, so the
         // attention kernel treats prefix and chunk values alike
-        store_f16x16_scaled(p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16, wv, vs);
+        __half *vd = p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16;
+        if (p.v_mean && row < P) {
+            const int8_t *c = reinterpret_cast<const int8_t *>(&wv);
+            float v[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) v[e] = (float)c[e] * vs;
+            store_f16x16_minus(vd, v, p.v_mean + (int64_t)bh * D + dc * 16);
+        } else {
+            store_f16x16_scaled(vd, wv, vs);
+        }
         if (dc == 0) p.ksc_ws[(int64_t)bh * p.Lpad + row] = ks;
     } else {
         const int np = D >> 4;
@@ -120,7 +165,18 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
         }
         store_f16x16(p.k_ws + ((int64_t)bh * p.Lpad + row) * D + dc * 16, wk);
         if (dc == 0) p.ksc_ws[(int64_t)bh * p.Lpad + row] = ks;
-        if (p.v_bf16) {
+        __half *vd = p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16;
+        if (p.v_mean) {
+            const int64_t vo = ((int64_t)bh * p.Sk + c) * D + dc * 16;
+            if (ok) {
+                float v[16];
+                load16f(static_cast<const char *>(p.v) + vo * 2, p.v_bf16 != 0, v);
+                store_f16x16_minus(vd, v, p.v_mean + (int64_t)bh * D + dc * 16);
+            } else {
+                uint4 *d = reinterpret_cast<uint4 *>(vd);
+                d[0] = d[1] = make_uint4(0, 0, 0, 0);
+            }
+        } else if (p.v_bf16) {
             uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
             if (ok) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(
@@ -128,7 +184,7 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
                 v0 = bf16x8_to_f16x8(src[0]);
                 v1 = bf16x8_to_f16x8(src[1]);
             }
-            uint4 *d = reinterpret_cast<uint4 *>(p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16);
+            uint4 *d = reinterpret_cast<uint4 *>(vd);
             d[0] = v0;
             d[1] = v1;
         }
@@ -159,7 +215,8 @@ __global__ void __launch_bounds__(256)
     const int row = row0 + slot;
     const bool ok = row < len;
     const int64_t wrow = (int64_t)kvh * p.Lpad + varlen_key_row0(ks, b, p.BN) + row;
-    uint4 wk = make_uint4(0, 0, 0, 0), v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+    uint4 wk = make_uint4(0, 0, 0, 0);
+    uint4 vv[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
     float ksc = 0.0f;
     if (ok) {
         wk = *reinterpret_cast<const uint4 *>(p.k + ((int64_t)kvh * p.total_k + ks + row) * D +
@@ -167,43 +224,50 @@ __global__ void __launch_bounds__(256)
         ksc = p.k_scale[(int64_t)kvh * p.k_groups + varlen_group0(ks, b, 1 << p.k_shift) +
                         (row >> p.k_shift)];
         const int64_t vo = (ks + row) * p.v_st + kvh * p.v_sh + dc * 16;
-        if (p.v_bf16) {
+        if (p.v_mean) {
+            float v[16];
+            load16f(static_cast<const char *>(p.v) + vo * 2, p.v_bf16 != 0, v);
+            store_f16x16_minus(reinterpret_cast<__half *>(vv), v,
+                               p.v_mean + ((int64_t)b * p.Hkv + kvh) * D + dc * 16);
+        } else if (p.v_bf16) {
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 static_cast<const __nv_bfloat16 *>(p.v) + vo);
-            v0 = bf16x8_to_f16x8(src[0]);
-            v1 = bf16x8_to_f16x8(src[1]);
+            vv[0] = bf16x8_to_f16x8(src[0]);
+            vv[1] = bf16x8_to_f16x8(src[1]);
         } else {
             const uint4 *src = reinterpret_cast<const uint4 *>(static_cast<const __half *>(p.v) + vo);
-            v0 = src[0];
-            v1 = src[1];
+            vv[0] = src[0];
+            vv[1] = src[1];
         }
     }
     store_f16x16(p.k_ws + wrow * D + dc * 16, wk);
     if (dc == 0) p.ksc_ws[wrow] = ksc;
     uint4 *d = reinterpret_cast<uint4 *>(p.v_ws + wrow * D + dc * 16);
-    d[0] = v0;
-    d[1] = v1;
+    d[0] = vv[0];
+    d[1] = vv[1];
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
-PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16) {
+PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16,
+                             bool smooth_v) {
     PrefillLayout L = {};
     L.BN = D == 256 ? 64 : 128;
     L.Ppad = (max_prefix_len + L.BN - 1) / L.BN * L.BN;
     L.Lpad = L.Ppad + (Sk + L.BN - 1) / L.BN * L.BN;
-    L.Vrows = v_bf16 ? L.Lpad : L.Ppad;
+    L.Vrows = (v_bf16 || smooth_v) ? L.Lpad : L.Ppad;
     const size_t BH = (size_t)B * Hkv;
     L.off_k = 0;
     L.off_v = align256(L.off_k + BH * L.Lpad * D * 2);
     L.off_ksc = align256(L.off_v + BH * L.Vrows * D * 2);
-    L.bytes = align256(L.off_ksc + BH * L.Lpad * 4);
+    L.off_vmean = align256(L.off_ksc + BH * L.Lpad * 4);
+    L.bytes = align256(L.off_vmean + (smooth_v ? BH * D * 4 : 0));
     return L;
 }
 
-PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D) {
+PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D, bool smooth_v) {
     PrefillLayout L = {};
     L.BN = D == 256 ? 64 : 128;
     L.Ppad = 0;
@@ -214,7 +278,8 @@ PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D) {
     L.off_k = 0;
     L.off_v = align256(L.off_k + H * rows * D * 2);
     L.off_ksc = align256(L.off_v + H * rows * D * 2);
-    L.bytes = align256(L.off_ksc + H * rows * 4);
+    L.off_vmean = align256(L.off_ksc + H * rows * 4);
+    L.bytes = align256(L.off_vmean + (smooth_v ? (size_t)B * Hkv * D * 4 : 0));
     return L;
 }
 

@@ -549,23 +549,29 @@ unsigned launch_blocks(const QuantParams &q, unsigned grid, cudaStream_t st, boo
 }
 
 template <typename T>
+cudaError_t launch_mean_t(const QuantParams &p, cudaStream_t st, LaunchLog &log) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(kMeanCluster, (unsigned)(p.B * p.H), 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kMeanCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, token_mean_kernel<T>, p);
+    log.add("token_mean_kernel", cfg.gridDim, cfg.blockDim, dim3(kMeanCluster, 1, 1), 0);
+    return e;
+}
+
+template <typename T>
 cudaError_t launch_quant_t(const QuantParams &p, cudaStream_t st, LaunchLog &log) {
     cudaError_t e = cudaSuccess;
     QuantParams q = p;
     if (p.smooth) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(kMeanCluster, (unsigned)(p.B * p.H), 1);
-        cfg.blockDim = dim3(256, 1, 1);
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = kMeanCluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, token_mean_kernel<T>, q);
-        log.add("token_mean_kernel", cfg.gridDim, cfg.blockDim, dim3(kMeanCluster, 1, 1), 0);
+        e = launch_mean_t<T>(q, st, log);
         if (e != cudaSuccess) return e;
         q.mu_sub = p.mu_out;
     }
@@ -611,6 +617,12 @@ cudaError_t launch_quant_t(const QuantParams &p, cudaStream_t st, LaunchLog &log
 cudaError_t launch_quant(const QuantParams &p, cudaStream_t st, LaunchLog &log) {
     if (p.bf16) return launch_quant_t<__nv_bfloat16>(p, st, log);
     return launch_quant_t<__half>(p, st, log);
+}
+
+cudaError_t launch_token_mean(const QuantParams &p, cudaStream_t st, LaunchLog &log) {
+    if ((int64_t)p.B * p.H == 0) return cudaSuccess;
+    if (p.bf16) return launch_mean_t<__nv_bfloat16>(p, st, log);
+    return launch_mean_t<__half>(p, st, log);
 }
 
 }  // namespace sage

@@ -270,3 +270,48 @@ def test_prefill_bundled_order_covers_every_tile(sage):
                                       f32(qkv.v)[:, h:h + 1], causal=True, rows=rows)
         assert_close(f32(out)[0, h, rows], o_ref[0, 0], "h%d" % h)
         assert_close(np_(lse)[0, h, rows], l_ref[0, 0], "lse h%d" % h)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("vdt", ["fp16", "bf16"])
+def test_prefill_smooth_v(sage, D, vdt):
+    """smooth_v: the V mean (bit-exact against the oracle's token mean) is
+    subtracted before P.V and added back; outputs against the oracle's
+    smooth_v result.  V carries a common offset (outputs stay below 2, so f16
+    output rounding stays inside the tolerance)."""
+    B, Hq, Hkv, S = 2, 4, 2, 333
+    qkv = W.dense_qkv(B, Hq, Hkv, S, S, D, seed=D + 61, device="cuda", v_dtype=vdt)
+    v = (qkv.v.float() * 0.25 + 1.25).to(qkv.v.dtype)
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    mu = torch.empty((B, Hkv, D), dtype=torch.float32, device="cuda")
+    for causal in (False, True):
+        out, lse = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, v, causal=causal,
+                                          out_dtype=torch.float16, return_lse=True,
+                                          smooth_v=True, v_mean=mu)
+        torch.cuda.synchronize()
+        assert sage.check_device_status()[0] == 0
+        assert np.array_equal(np_(mu), oracle.token_mean(f32(v)))
+        o_ref, l_ref = oracle.prefill(np_(qi), np_(qs), 1, np_(ki), np_(ks), 1, f32(v),
+                                      causal=causal, smooth_v=True)
+        assert_close(f32(out), o_ref, "causal=%s" % causal)
+        assert_close(np_(lse), l_ref, "lse causal=%s" % causal)
+
+
+def test_prefill_smooth_v_paged_prefix(sage):
+    """smooth_v over a paged INT8 prefix: the chunk's V mean comes off the
+    prefix values too, so the identity P (V - mu) + mu = P V still holds."""
+    B, Hq, Hkv, Sc, D, P = 1, 6, 1, 150, 256, 200
+    qkv = W.dense_qkv(B, Hq, Hkv, Sc, Sc, D, seed=71, dtype="bf16", device="cuda")
+    v = (qkv.v.float() * 0.25 + 0.75).to(qkv.v.dtype)
+    c = W.paged_cache(B, Hkv, D, [P], seed=72, device="cuda")
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    out = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, v, causal=True,
+                                 prefix=_prefix_dict(c, P), out_dtype=torch.float16,
+                                 smooth_v=True)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    pre = dict(k_cache=np_(c.k_cache), v_cache=np_(c.v_cache), k_scale=np_(c.k_scale),
+               v_scale=np_(c.v_scale), block_table=np_(c.block_table), lens=np_(c.lens))
+    o_ref, _ = oracle.prefill(np_(qi), np_(qs), 1, np_(ki), np_(ks), 1, f32(v), causal=True,
+                              prefix=pre, smooth_v=True)
+    assert_close(f32(out), o_ref)

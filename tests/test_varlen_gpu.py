@@ -246,3 +246,29 @@ def test_varlen_bad_lengths_flag_and_skip(sage):
     assert sage.check_device_status()[0] == 0
     assert torch.equal(out[:64], good[:64])
     assert torch.all(out[64:] == 0)
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_varlen_smooth_v(sage, D):
+    """smooth_v per sequence: each sequence's own V mean (bit-exact), and the
+    same outputs as the per-sequence oracle with smooth_v."""
+    x = W.varlen_qkv(LQ, LK, 4, 2, D, seed=D + 81, device="cuda", v_dtype="bf16")
+    x.v = (x.v.float() * 0.25 + 1.25).to(x.v.dtype)
+    qi, qs, ki, ks, _ = _quant_all(sage, x, 1, 1, False)
+    mu = torch.empty((len(LQ), 2, D), dtype=torch.float32, device="cuda")
+    out, lse = sage.sage_attn_prefill_varlen(qi, qs, 1, ki, ks, 1, x.v, x.cu_q, x.cu_k, x.max_q,
+                                             x.max_k, causal=True, out_dtype=torch.float16,
+                                             return_lse=True, smooth_v=True, v_mean=mu)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    ck = np_(x.cu_k)
+    for b, (t0, t1) in enumerate(oracle.seq_bounds(ck)):
+        ref = oracle.token_mean(np.ascontiguousarray(f32(x.v)[t0:t1].transpose(1, 0, 2))) \
+            if t1 > t0 else np.zeros((2, D), np.float32)
+        assert np.array_equal(np_(mu)[b], ref), "mean of sequence %d" % b
+    cq = np_(x.cu_q)
+    o_ref, l_ref = oracle.prefill_varlen(np_(qi), _seq_scales(qs, cq, 1), 1, np_(ki),
+                                         _seq_scales(ks, ck, 1), 1, f32(x.v), cq, ck,
+                                         causal=True, smooth_v=True)
+    assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
