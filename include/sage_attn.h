@@ -177,6 +177,13 @@ sage_status_t sage_kv_cache_append(const void *k_new, const void *v_new, sage_dt
  * distributed shared memory inside the same kernel (one launch, no partials
  * in device memory); with more segments the partials go through the
  * workspace and the combine kernel.
+ * Per-step inputs and outputs -- q (or the f16/bf16 query of the _q16 form),
+ * q_scale, block_table, context_lens, out and lse -- may be device memory
+ * or pinned host memory that the GPU addresses at the same pointer (as on
+ * GB300, whose kernels then read and write it over NVLink-C2C with no
+ * copy-engine transfer); any other pointer is rejected with
+ * SAGE_ERR_INVALID_ARG.  The caches, scales and workspace must be device
+ * memory.
  * ------------------------------------------------------------------------ */
 typedef struct sage_decode_args {
     const int8_t *q;            /* [B, Hq, D] int8 (sage_quant_int8 output) */

@@ -163,6 +163,16 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _ptr_io(t: Optional[torch.Tensor]):
+    """A per-step decode input/output: a CUDA tensor or a pinned host tensor
+    (which the kernels reach directly; the library checks the mapping)."""
+    if t is None:
+        return None
+    if not (t.is_cuda or t.is_pinned()):
+        raise ValueError("tensor must be on a CUDA device or in pinned host memory")
+    return ctypes.c_void_p(t.data_ptr())
+
+
 def _stream(stream=None):
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
@@ -244,17 +254,17 @@ def _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_tabl
     _need(context_lens, torch.int32, "context_lens")
     B, Hq, D = q_int8.shape if shape is None else shape
     a = DecodeArgs()
-    a.q, a.q_scale = _ptr(q_int8), _ptr(q_scale)
+    a.q, a.q_scale = _ptr_io(q_int8), _ptr_io(q_scale)
     a.k_cache, a.v_cache = _ptr(k_cache), _ptr(v_cache)
     a.k_scale, a.v_scale = _ptr(k_scale), _ptr(v_scale)
-    a.block_table, a.context_lens = _ptr(block_table), _ptr(context_lens)
+    a.block_table, a.context_lens = _ptr_io(block_table), _ptr_io(context_lens)
     a.B, a.Hq, a.Hkv, a.D = B, Hq, k_cache.shape[1], D
     a.num_blocks, a.max_blocks = k_cache.shape[0], block_table.shape[1]
     a.max_context_len = int(max_context_len)
     a.sm_scale = float(sm_scale) if sm_scale else 0.0
     a.num_segments = int(num_segments)
-    a.out, a.out_dtype = _ptr(out), _dt(out.dtype)
-    a.lse = _ptr(lse)
+    a.out, a.out_dtype = _ptr_io(out), _dt(out.dtype)
+    a.lse = _ptr_io(lse)
     return a
 
 
@@ -267,12 +277,12 @@ def sage_attn_decode_paged(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, 
     B, Hq, D = q_int8.shape
     Hkv = k_cache.shape[1]
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q_int8.device)
-    lse = torch.empty((B, Hq), dtype=torch.float32, device=q_int8.device) if return_lse else None
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=k_cache.device)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=k_cache.device) if return_lse else None
     S = num_segments or decode_num_segments(B, Hq, Hkv, D, max_context_len)
     need = decode_workspace_size(B, Hq, D, S)
     if workspace is None and need:
-        workspace = torch.empty((need,), dtype=torch.uint8, device=q_int8.device)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a = _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
                      context_lens, max_context_len, sm_scale, S, out, lse)
@@ -294,22 +304,24 @@ def sage_attn_decode_paged_q16(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     """Paged decode with the per-token query quantisation fused into the kernel.
 
     q [B,Hq,D] f16/bf16.  Same result as sage_quant_int8 + sage_attn_decode_paged.
+    q, block_table, context_lens and out may be pinned host tensors: the
+    kernel reads and writes them in place (NVLink-C2C on GB300).
     """
     B, Hq, D = q.shape
     Hkv = k_cache.shape[1]
     if q.dtype not in (torch.float16, torch.bfloat16) or not q.is_contiguous():
         raise ValueError("q must be a contiguous f16/bf16 tensor")
     if out is None:
-        out = torch.empty((B, Hq, D), dtype=out_dtype, device=q.device)
-    lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device) if return_lse else None
+        out = torch.empty((B, Hq, D), dtype=out_dtype, device=k_cache.device)
+    lse = torch.empty((B, Hq), dtype=torch.float32, device=k_cache.device) if return_lse else None
     S = num_segments or decode_num_segments(B, Hq, Hkv, D, max_context_len)
     need = decode_workspace_size(B, Hq, D, S)
     if workspace is None and need:
-        workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+        workspace = torch.empty((need,), dtype=torch.uint8, device=k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     a = _decode_args(None, None, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
                      max_context_len, sm_scale, S, out, lse, shape=(B, Hq, D))
-    _check(lib().sage_attn_decode_paged_q16(ctypes.byref(a), _ptr(q), _dt(q.dtype), _ptr(workspace),
+    _check(lib().sage_attn_decode_paged_q16(ctypes.byref(a), _ptr_io(q), _dt(q.dtype), _ptr(workspace),
                                             ws_bytes, _stream(stream)))
     return (out, lse) if return_lse else out
 
@@ -357,9 +369,9 @@ def sage_attn_decode_paged_partials(q_int8, q_scale, k_cache, v_cache, k_scale, 
     """Decode without the combine: returns (o_part [B,Hq,S,D], lse_part [B,Hq,S])."""
     B, Hq, D = q_int8.shape
     S = decode_segments_used(max_context_len, num_segments)
-    o_part = torch.empty((B, Hq, S, D), dtype=torch.float32, device=q_int8.device)
-    lse_part = torch.empty((B, Hq, S), dtype=torch.float32, device=q_int8.device)
-    dummy = torch.empty((1,), dtype=torch.float16, device=q_int8.device)
+    o_part = torch.empty((B, Hq, S, D), dtype=torch.float32, device=k_cache.device)
+    lse_part = torch.empty((B, Hq, S), dtype=torch.float32, device=k_cache.device)
+    dummy = torch.empty((1,), dtype=torch.float16, device=k_cache.device)
     a = _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
                      context_lens, max_context_len, sm_scale, num_segments, dummy, None)
     used = _i(0)

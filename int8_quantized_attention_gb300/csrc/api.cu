@@ -58,6 +58,26 @@ sage_status_t error_word(int **out) {
 }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// A per-step input or output of decode may live in device memory or in
+// pinned host memory that the GPU reaches at the same address (GB300: the
+// kernels read and write it over NVLink-C2C, no copy-engine transfer).
+// Anything else (pageable host memory, a foreign pointer) is rejected here
+// rather than faulting on the device.
+sage_status_t check_reachable(const void *ptr, const char *name) {
+    if (!ptr) return SAGE_OK;
+    cudaPointerAttributes at = {};
+    const cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(SAGE_ERR_INVALID_ARG, "%s: not memory the GPU can reach (%s)", name,
+                    cudaGetErrorString(e));
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return SAGE_OK;
+    if (at.type == cudaMemoryTypeHost && at.devicePointer == ptr) return SAGE_OK;
+    return fail(SAGE_ERR_INVALID_ARG, "%s: must be device memory or mapped pinned host memory",
+                name);
+}
 bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
 
 int sm_count() {
@@ -375,6 +395,16 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
     }
     if (!q_fp && !aligned(a->q, 4)) return fail(SAGE_ERR_INVALID_ARG, "q must be 4-byte aligned");
     if (!aligned(a->out, 8)) return fail(SAGE_ERR_INVALID_ARG, "out must be 8-byte aligned");
+    {   // the per-step inputs and outputs: device or mapped pinned host memory
+        const struct { const void *p; const char *n; } io[] = {
+            {q_fp ? q_fp : (const void *)a->q, "q"}, {q_fp ? nullptr : (const void *)a->q_scale, "q_scale"},
+            {a->max_context_len > 0 ? a->block_table : nullptr, "block_table"},
+            {a->context_lens, "context_lens"}, {a->out, "out"}, {a->lse, "lse"}};
+        for (const auto &x : io) {
+            const sage_status_t r = check_reachable(x.p, x.n);
+            if (r != SAGE_OK) return r;
+        }
+    }
     int S = a->num_segments ? a->num_segments
                             : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->D,
                                                        a->max_context_len);

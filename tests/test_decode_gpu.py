@@ -1,4 +1,6 @@
 """GPU parity: split-K paged decode + LSE combine against the oracle."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -259,3 +261,41 @@ def test_decode_fused_query_quant_bitwise(sage, D, Hq, Hkv, segments, qdt):
     torch.cuda.synchronize()
     assert sage.check_device_status()[0] == 0
     assert torch.equal(out, ref) and torch.equal(lse, lref)
+
+
+def test_decode_pinned_host_io_bitwise(sage):
+    """Per-step inputs and outputs in pinned host memory (read and written by
+    the kernel in place) give exactly the device-memory result; pageable
+    host memory is refused before anything is launched."""
+    B, Hq, Hkv, D, ctx = 4, 12, 2, 128, 700
+    c = W.paged_cache(B, Hkv, D, [ctx, 5, 333, 0], seed=91, device="cuda")
+    q = W.decode_query(B, Hq, D, seed=91, device="cuda")
+    ref, ref_lse = sage.sage_attn_decode_paged_q16(q, c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                                   c.block_table, c.lens, ctx, return_lse=True)
+    out_h = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    got = sage.sage_attn_decode_paged_q16(q.cpu().pin_memory(), c.k_cache, c.v_cache, c.k_scale,
+                                          c.v_scale, c.block_table.cpu().pin_memory(),
+                                          c.lens.cpu().pin_memory(), ctx, out=out_h)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert got.data_ptr() == out_h.data_ptr()
+    assert torch.equal(out_h, ref.cpu())
+    # the INT8 entry point with pinned query codes and scales
+    qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
+    r2 = sage.sage_attn_decode_paged(qi[:, :, 0], qs[:, :, 0], c.k_cache, c.v_cache, c.k_scale,
+                                     c.v_scale, c.block_table, c.lens, ctx)
+    o2 = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    sage.sage_attn_decode_paged(qi[:, :, 0].cpu().pin_memory(), qs[:, :, 0].cpu().pin_memory(),
+                                c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                c.block_table.cpu().pin_memory(), c.lens.cpu().pin_memory(), ctx,
+                                out=o2)
+    torch.cuda.synchronize()
+    assert torch.equal(o2, r2.cpu())
+    # pageable host memory: rejected on the host, nothing launched
+    a = sage._decode_args(None, None, c.k_cache, c.v_cache, c.k_scale, c.v_scale, c.block_table,
+                          c.lens, ctx, None, 0, ref, None, shape=(B, Hq, D))
+    pageable = np.zeros(B * Hq * D, np.float32)
+    st = sage.lib().sage_attn_decode_paged_q16(ctypes.byref(a), pageable.ctypes.data_as(ctypes.c_void_p),
+                                               sage.SAGE_BF16, None, 0, None)
+    assert st == sage.SAGE_ERR_INVALID_ARG
+    assert b"pinned host memory" in sage.lib().sage_get_last_error_message()
