@@ -168,7 +168,7 @@ def run_ours(args):
     cache = W.paged_cache(B, Hkv, D, [ctx] * B, seed=P["seed"] + rank, device="cuda")
     q = W.decode_query(B, Hq, D, seed=P["seed"] + rank, device="cuda")
     max_blocks = cache.block_table.shape[1]
-    S = sage.decode_num_segments(B, Hq, Hkv, D, ctx)
+    S = args.segments or sage.decode_num_segments(B, Hq, Hkv, D, ctx)
     kbytes, sbytes = decode_bytes(B, Hq, Hkv, D, ctx, max_blocks)
     stream = torch.cuda.current_stream()
     flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
@@ -252,10 +252,15 @@ def run_ours(args):
         ws_buf = torch.empty(sage.decode_workspace_size(B, Hq, D, S), dtype=torch.uint8,
                              device="cuda")
 
+        # segment count: the library's own choice for host-resident I/O
+        S_e2e = args.segments
+        ws_buf = torch.empty(max(1, sage.decode_workspace_size(B, Hq, D, 64)), dtype=torch.uint8,
+                             device="cuda")
+
         def e2e_step():
             sage.sage_attn_decode_paged_q16(q_host, cache.k_cache, cache.v_cache, cache.k_scale,
                                             cache.v_scale, bt_host, lens_host, ctx,
-                                            num_segments=S, workspace=ws_buf, out=out_host)
+                                            num_segments=S_e2e, workspace=ws_buf, out=out_host)
 
         for _ in range(args.warmup):
             e2e_step()
@@ -729,6 +734,8 @@ def main():
                     choices=["paged_decode", "dense_prefill", "chunked_prefill",
                              "varlen_prefill"])
     ap.add_argument("--heads", type=int, default=0)
+    ap.add_argument("--segments", type=int, default=0,
+                    help="decode segment count (0: the library's choice)")
     ap.add_argument("--configs", action="store_true",
                     help="time every configuration of the workload table (one JSON line each)")
     args = ap.parse_args()

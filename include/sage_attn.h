@@ -206,12 +206,20 @@ typedef struct sage_decode_args {
 
 /* Segment count the library picks for num_segments == 0 (host only).  With
  * U = B * Hkv * ceil(Hq/Hkv/8) (sequence, KV head, 8-head tile) units and
- * P = ceil(max_context_len/16) pages it aims at about 1.7 CTAs per SM when
- * U * P / SMs < 400 pages, else about 5 per SM (S = target / U rounded, at
- * least 16 pages per segment, at most 64 segments); 8 (in-cluster combine) is
- * preferred over a larger count that it reaches to within 3/4.  The rule is
- * empirical, measured on GB300. */
+ * P = ceil(max_context_len/16) pages: S = 2.5 SMs / U rounded (one wave of
+ * about 2.5 CTAs per SM), or, when that is below 2, S = 5 SMs / U rounded
+ * (several waves of shorter CTAs); at least 8 pages per segment, at most 64
+ * segments.  This is the choice for device-resident per-step inputs; a call
+ * with num_segments == 0 whose query, block table or output is pinned host
+ * memory aims at about 1.7 CTAs per SM instead (each segment's CTA reads its
+ * inputs across the CPU-GPU link).  The rule is empirical, measured on GB300. */
 int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len);
+
+/* The segment count a decode call with args->num_segments == 0 will use,
+ * taking into account where its per-step inputs and output live (q: the
+ * f16/bf16 query of the _q16 form, or NULL for args->q).  Host only; use it
+ * to size the workspace. */
+int sage_decode_auto_segments(const sage_decode_args_t *args, const void *q);
 
 /* Bytes of workspace sage_attn_decode_paged may need: fp32 partial outputs
  * [B,Hq,S,D] plus fp32 partial LSEs [B,Hq,S] (0 when S == 1).  A call with

@@ -111,6 +111,8 @@ def lib():
         L.sage_debug_prefill_varlen_qk_int32.restype = _i
         L.sage_decode_num_segments.argtypes = [_i, _i, _i, _i, _i]
         L.sage_decode_num_segments.restype = _i
+        L.sage_decode_auto_segments.argtypes = [ctypes.POINTER(DecodeArgs), _vp]
+        L.sage_decode_auto_segments.restype = _i
         L.sage_attn_decode_workspace_size.argtypes = [_i, _i, _i, _i]
         L.sage_attn_decode_workspace_size.restype = ctypes.c_size_t
         L.sage_attn_decode_paged.argtypes = [ctypes.POINTER(DecodeArgs), _vp, ctypes.c_size_t, _vp]
@@ -279,13 +281,15 @@ def sage_attn_decode_paged(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, 
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=k_cache.device)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=k_cache.device) if return_lse else None
-    S = num_segments or decode_num_segments(B, Hq, Hkv, D, max_context_len)
+    a = _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
+                     context_lens, max_context_len, sm_scale, num_segments, out, lse)
+    # the library's choice for these buffers (it depends on where they live)
+    S = num_segments or int(lib().sage_decode_auto_segments(ctypes.byref(a), None))
+    a.num_segments = S
     need = decode_workspace_size(B, Hq, D, S)
-    if workspace is None and need:
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty((need,), dtype=torch.uint8, device=k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    a = _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
-                     context_lens, max_context_len, sm_scale, S, out, lse)
     if debug_scores is not None:
         _need(debug_scores, torch.int32, "debug_scores")
         _check(lib().sage_debug_decode_qk_int32(ctypes.byref(a), _ptr(workspace), ws_bytes,
@@ -314,13 +318,15 @@ def sage_attn_decode_paged_q16(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=k_cache.device)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=k_cache.device) if return_lse else None
-    S = num_segments or decode_num_segments(B, Hq, Hkv, D, max_context_len)
+    a = _decode_args(None, None, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
+                     max_context_len, sm_scale, num_segments, out, lse, shape=(B, Hq, D))
+    # the library's choice for these buffers (it depends on where they live)
+    S = num_segments or int(lib().sage_decode_auto_segments(ctypes.byref(a), _ptr_io(q)))
+    a.num_segments = S
     need = decode_workspace_size(B, Hq, D, S)
-    if workspace is None and need:
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
         workspace = torch.empty((need,), dtype=torch.uint8, device=k_cache.device)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    a = _decode_args(None, None, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
-                     max_context_len, sm_scale, S, out, lse, shape=(B, Hq, D))
     _check(lib().sage_attn_decode_paged_q16(ctypes.byref(a), _ptr_io(q), _dt(q.dtype), _ptr(workspace),
                                             ws_bytes, _stream(stream)))
     return (out, lse) if return_lse else out

@@ -2,6 +2,8 @@
 // configuration, the per-device error word and the launch record.
 // Every entry point is declared (and documented) in include/sage_attn.h.
 #include <math.h>
+
+#include <cmath>
 #include <stdarg.h>
 #include <stdio.h>
 
@@ -78,6 +80,17 @@ sage_status_t check_reachable(const void *ptr, const char *name) {
     return fail(SAGE_ERR_INVALID_ARG, "%s: must be device memory or mapped pinned host memory",
                 name);
 }
+// True when `ptr` is pinned host memory (checked reachable beforehand).
+bool is_host_memory(const void *ptr) {
+    if (!ptr) return false;
+    cudaPointerAttributes at = {};
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return at.type == cudaMemoryTypeHost;
+}
+
 bool head_dim_ok(int D) { return D == 64 || D == 128 || D == 256; }
 
 int sm_count() {
@@ -319,37 +332,48 @@ SAGE_API sage_status_t sage_splitk_combine(const float *o_part, const float *lse
 
 // ----------------------------------------------------------------- decode
 
-SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len) {
+// Segment count for a decode call.  `per_sm_x16` is 16 times the CTAs per
+// SM the single-wave choice aims at: 40 (2.5 per SM) when the per-step
+// inputs and outputs are in device memory, 27 (about 1.7) when they are in
+// pinned host memory -- there every segment's CTA reads its query and table
+// slice across NVLink-C2C at start-up, and fewer CTAs measured faster.
+static int decode_segments(int B, int Hq, int Hkv, int max_context_len, int per_sm_x16) {
     if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || max_context_len <= 0) return 1;
-    (void)D;
     const int group = Hq / Hkv;
     const int64_t units = (int64_t)B * Hkv * ((group + 7) / 8);
     const int64_t sms = sm_count();
     const int pages = (max_context_len + 15) / 16;
-    // at least 16 pages per segment (shorter ones cost more in start-up and
+    // at least 8 pages per segment (shorter ones cost more in start-up and
     // combine than they gain in parallelism, measured), at most 64 segments
-    int64_t smax = pages / 16 > 1 ? pages / 16 : 1;
+    int64_t smax = pages / 8 > 1 ? pages / 8 : 1;
     if (smax > 64) smax = 64;
-    // Measured on GB300 (D = 256, 3 CTAs per SM): with little work per SM
-    // (under ~400 pages) about 1.7 CTAs per SM is fastest (longer segments
-    // amortise each CTA's start and merge); with more work about 5 per SM
-    // (shorter CTAs even out the tail).
-    const int64_t pages_per_sm = units * pages / (sms > 0 ? sms : 1);
-    const int64_t target = pages_per_sm < 400 ? (sms * 27 + 8) / 16 : sms * 5;
-    int64_t best = (target + units / 2) / units;
+    // Measured on GB300 (D = 256; every segment count 2..16, 20..64 on the
+    // batch 1 / 8 / 16 / 64 shapes): when the units are few, the fastest grid
+    // is one wave of about 2.5 CTAs per SM with device-resident inputs (a
+    // fuller wave of ~3 per SM measured slower, clusters of 7 much slower);
+    // when even two segments per unit would overfill that, about 5 CTAs per
+    // SM in several waves (shorter CTAs even out the tail).
+    int64_t best = (sms * per_sm_x16 / 16 + units / 2) / units;
+    if (best < 2) best = (sms * 5 + units / 2) / units;
     if (best < 1) best = 1;
     if (best > smax) best = smax;
-    // up to kDecodeMaxCluster segments combine inside one thread-block
-    // cluster (no partials in device memory, no combine launch): take it
-    // while it keeps at least 3/4 of the target CTA count
-    if (best > sage::kDecodeMaxCluster &&
-        units * sage::kDecodeMaxCluster * 4 >= target * 3 && sage::kDecodeMaxCluster <= smax)
-        best = sage::kDecodeMaxCluster;
     const int64_t cap = sage::decode_max_segment_pages();
     if (best * cap < pages) best = (pages + cap - 1) / cap;
     const int64_t pps = (pages + best - 1) / best;
     best = (pages + pps - 1) / pps;
     return (int)best;
+}
+
+SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len) {
+    (void)D;
+    return decode_segments(B, Hq, Hkv, max_context_len, 40);
+}
+
+SAGE_API int sage_decode_auto_segments(const sage_decode_args_t *a, const void *q) {
+    if (!a) return 1;
+    const bool host_io = is_host_memory(q ? q : (const void *)a->q) ||
+                         is_host_memory(a->block_table) || is_host_memory(a->out);
+    return decode_segments(a->B, a->Hq, a->Hkv, a->max_context_len, host_io ? 27 : 40);
 }
 
 SAGE_API size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments) {
@@ -405,9 +429,7 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
             if (r != SAGE_OK) return r;
         }
     }
-    int S = a->num_segments ? a->num_segments
-                            : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->D,
-                                                       a->max_context_len);
+    int S = a->num_segments ? a->num_segments : sage_decode_auto_segments(a, q_fp);
     const int pages = (a->max_context_len + 15) / 16;
     {   // a segment is at most decode_max_segment_pages() pages long
         const int cap = sage::decode_max_segment_pages();
@@ -474,7 +496,7 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
     if (S > 1) {
         sage::LaunchLog tmp = g_last;
         sage::CombineParams c = {p.o_part, p.lse_part, a->B * a->Hq, S, a->D, a->out,
-                                 p.out_bf16, a->lse};
+                                 p.out_bf16, a->lse, 1};
         e = sage::launch_combine(c, cs, tmp);
         if (e != cudaSuccess) return cuda_fail(e, "combine launch");
         // keep the decode kernel as the recorded kernel; count both launches

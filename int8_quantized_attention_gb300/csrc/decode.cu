@@ -129,6 +129,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
     int8_t *q_s = reinterpret_cast<int8_t *>(smem + Cfg::kOffQ);
     float *qsc_s = reinterpret_cast<float *>(smem + Cfg::kOffQs);
 
+    // a combine kernel launched behind this grid may be scheduled once every
+    // CTA has started; it waits on the device for this grid to complete
+    asm volatile("griddepcontrol.launch_dependents;");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int seg = blockIdx.x;
     const int kvh = blockIdx.y / p.head_tiles;

@@ -61,6 +61,10 @@ struct CombineParams {
     void *out;
     int out_bf16;
     float *lse_out;
+    // launched right behind the decode kernel that writes the partials: the
+    // combine may start while that grid runs (programmatic dependent launch)
+    // and waits on the device for its completion before reading them
+    int after_decode;
 };
 
 cudaError_t launch_combine(const CombineParams &p, cudaStream_t st, LaunchLog &log);

@@ -149,7 +149,7 @@ SAGE_API sage_status_t sage_attn_decode_paged_noalloc(const sage_decode_args_t *
     if (S > 1) {
         sage::LaunchLog tmp = log;
         sage::CombineParams c = {p.o_part, p.lse_part, a->B * a->Hq, S, a->D, a->out, p.out_bf16,
-                                 a->lse};
+                                 a->lse, 1};
         e = sage::launch_combine(c, cs, tmp);
         if (e != cudaSuccess)
             return (sage_status_t)report_error(SAGE_ERR_CUDA, "combine launch: %s",
