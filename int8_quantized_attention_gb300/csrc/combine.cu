@@ -4,12 +4,14 @@
 // returns the LSE "for concatenation"):
 //   M = max_s lse_s,  L = M + ln sum_s exp(lse_s - M),
 //   out = sum_s exp(lse_s - L) * o_s.
-// One CTA per output row; its W warps (up to 8, about one per 8 segments)
-// each take every W-th segment and accumulate all D channels (D/32 per
-// lane, coalesced float4 loads, independent across segments), then the W
-// partial rows add up in shared memory.  With few rows (batch-1 decode has
-// a handful of (sequence, head) rows and up to 64 segments) the segments,
-// not the rows, carry the parallelism.  HBM/L2-bound.
+// One CTA per output row; its W warps (one per segment, at most 8) take
+// every W-th segment.  Each warp first issues the loads of its segments'
+// partial outputs and LSEs (up to kSegChunk per round, all independent),
+// then scans the row's S LSEs itself for M and L (no barrier), weights and
+// adds its segments, and the W partial rows add up in shared memory: one
+// memory round trip and one barrier per row.  With few rows (batch-1 decode
+// has a handful of (sequence, head) rows and up to 64 segments) the
+// segments, not the rows, carry the parallelism.  HBM/L2-bound.
 #include "common.cuh"
 #include "internal.h"
 
@@ -18,52 +20,60 @@ namespace sage {
 namespace {
 
 constexpr int kMaxCombineWarps = 8;
+constexpr int kSegChunk = 8;  // segments a warp holds in registers per round
 
 template <int D, typename TO>
 __global__ void __launch_bounds__(32 * kMaxCombineWarps) combine_kernel(CombineParams p) {
     constexpr int V = D / 32;  // channels per lane: 2, 4 or 8
     __shared__ float part[kMaxCombineWarps][D];
-    __shared__ float sh_L;
     const int W = (int)blockDim.x >> 5;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t r = blockIdx.x;
     const float *lp = p.lse_part + r * p.S;
+    const float *op = p.o_part + r * (int64_t)p.S * D + lane * V;
     // launched behind the decode kernel: wait here (not at the launch) until
     // that grid has completed and its partials are visible; a no-op otherwise
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    if (warp == 0) {
-        float M = -INFINITY;
-        for (int s = lane; s < p.S; s += 32) M = fmaxf(M, lp[s]);
-        M = warp_max(M);
-        float L = -INFINITY;
-        if (M != -INFINITY) {
-            float sum = 0.0f;
-            for (int s = lane; s < p.S; s += 32) {
-                const float l = lp[s];
-                if (l != -INFINITY) sum += expf(l - M);
-            }
-            sum = warp_sum(sum);
-            L = M + logf(sum);
-        }
-        if (lane == 0) sh_L = L;
-    }
-    __syncthreads();
-    const float L = sh_L;
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.0f;
-    if (L != -INFINITY) {
-        const float *op = p.o_part + r * (int64_t)p.S * D + lane * V;
-#pragma unroll 4
-        for (int s = warp; s < p.S; s += W) {
-            const float l = lp[s];
-            const float w = l == -INFINITY ? 0.0f : expf(l - L);
+    float L = -INFINITY;
+    for (int s0 = warp; s0 < p.S; s0 += W * kSegChunk) {
+        // this round's segments: loads first, all independent of M and L
+        float lv[kSegChunk], ov[kSegChunk][V];
+#pragma unroll
+        for (int k = 0; k < kSegChunk; ++k) {
+            const int s = s0 + k * W;
+            lv[k] = s < p.S ? lp[s] : -INFINITY;
 #pragma unroll
             for (int i = 0; i < V; i += 2) {
-                const float2 o2 = *reinterpret_cast<const float2 *>(op + (int64_t)s * D + i);
-                acc[i] = fmaf(w, o2.x, acc[i]);
-                acc[i + 1] = fmaf(w, o2.y, acc[i + 1]);
+                float2 o2 = make_float2(0.0f, 0.0f);
+                if (s < p.S) o2 = *reinterpret_cast<const float2 *>(op + (int64_t)s * D + i);
+                ov[k][i] = o2.x;
+                ov[k][i + 1] = o2.y;
             }
+        }
+        if (s0 == warp) {
+            // the row's M and L, scanned by every warp (no barrier)
+            float M = -INFINITY;
+            for (int s = lane; s < p.S; s += 32) M = fmaxf(M, lp[s]);
+            M = warp_max(M);
+            if (M != -INFINITY) {
+                float sum = 0.0f;
+                for (int s = lane; s < p.S; s += 32) {
+                    const float l = lp[s];
+                    if (l != -INFINITY) sum += expf(l - M);
+                }
+                sum = warp_sum(sum);
+                L = M + logf(sum);
+            }
+        }
+        if (L == -INFINITY) break;  // no segment saw a key: the row stays 0
+#pragma unroll
+        for (int k = 0; k < kSegChunk; ++k) {
+            const float w = lv[k] == -INFINITY ? 0.0f : expf(lv[k] - L);
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] = fmaf(w, ov[k][i], acc[i]);
         }
     }
 #pragma unroll
@@ -77,6 +87,7 @@ __global__ void __launch_bounds__(32 * kMaxCombineWarps) combine_kernel(CombineP
             for (int k = 1; k < W; ++k) v += part[k][lane * V + i];
             out[i] = DT<TO>::from_f(v);
         }
+        // every warp, warp 0 included, found L in its first round (W <= S)
         if (p.lse_out && lane == 0) p.lse_out[r] = L;
     }
 }
@@ -85,7 +96,7 @@ template <int D>
 cudaError_t launch_d(const CombineParams &p, cudaStream_t st, LaunchLog &log) {
     const unsigned grid = (unsigned)p.R;
     if (grid == 0) return cudaSuccess;
-    int W = (p.S + 7) / 8;
+    int W = p.S;  // one warp per segment, at most kMaxCombineWarps
     W = W < 1 ? 1 : (W > kMaxCombineWarps ? kMaxCombineWarps : W);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
