@@ -84,7 +84,8 @@ int sage_version(void);   /* 6 */
  * D        : 64, 128 or 256.   block_tokens: 1..1024.
  * x_int8   : int8 [B,H,S,D] dense (HND).
  * scale    : fp32 [B,H,ceil(S/block_tokens)].
- * mu_out   : fp32 [B,H,D], required iff smooth.
+ * mu_out   : fp32 [B,H,D], required iff smooth; 16-byte aligned.
+ * mu_in    : fp32 [B,mu_heads,D], 16-byte aligned.
  * bias_out : fp32 [B,H,S], required iff mu_in.
  * ------------------------------------------------------------------------ */
 sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B, int H, int S, int D,
@@ -118,8 +119,9 @@ sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B, int H, i
  *              16-byte aligned, strides multiples of 8.
  *   x_int8   : int8 [H, total, D].   scale: fp32 [H, groups].
  *   smooth   : mu_out fp32 [B, H, D] = each sequence's own token mean (0 for
- *              an empty sequence), subtracted before quantising.
- *   mu_in    : optional fp32 [B, mu_heads, D]; bias_out fp32 [H, total] =
+ *              an empty sequence), subtracted before quantising; 16-byte
+ *              aligned.
+ *   mu_in    : optional fp32 [B, mu_heads, D], 16-byte aligned; bias_out fp32 [H, total] =
  *              sum_c x[t,h,c] * mu_in[b(t), h / (H / mu_heads), c].
  * ------------------------------------------------------------------------ */
 int64_t sage_varlen_scale_groups(int64_t total, int B, int block_tokens);

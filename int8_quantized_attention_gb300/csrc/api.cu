@@ -217,6 +217,8 @@ SAGE_API sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B,
     if (stride_b % 8 || stride_h % 8 || stride_s % 8)
         return fail(SAGE_ERR_INVALID_ARG, "strides must be multiples of 8 elements");
     if (smooth && !mu_out) return fail(SAGE_ERR_INVALID_ARG, "smooth needs mu_out");
+    if ((smooth && !aligned(mu_out, 16)) || (mu_in && !aligned(mu_in, 16)))
+        return fail(SAGE_ERR_INVALID_ARG, "mu_out and mu_in must be 16-byte aligned");
     if (smooth && (int64_t)B * H > 65535)
         return fail(SAGE_ERR_UNSUPPORTED, "smooth supports at most 65535 (batch, head) pairs");
     if (mu_in) {
@@ -270,6 +272,8 @@ SAGE_API sage_status_t sage_quant_int8_varlen(const void *x, sage_dtype_t dtype,
     if (stride_h % 8 || stride_t % 8)
         return fail(SAGE_ERR_INVALID_ARG, "strides must be multiples of 8 elements");
     if (smooth && !mu_out) return fail(SAGE_ERR_INVALID_ARG, "smooth needs mu_out");
+    if ((smooth && !aligned(mu_out, 16)) || (mu_in && !aligned(mu_in, 16)))
+        return fail(SAGE_ERR_INVALID_ARG, "mu_out and mu_in must be 16-byte aligned");
     if (smooth && (int64_t)B * H > 65535)
         return fail(SAGE_ERR_UNSUPPORTED, "smooth supports at most 65535 (sequence, head) pairs");
     if (mu_in) {

@@ -26,6 +26,25 @@ struct LaunchLog {
     }
 };
 
+// Division of 32-bit n < 2^31 by an invariant divisor d (1 <= d < 2^31)
+// as a multiply-high and a shift (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994, section 4): with
+// l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (mulhi(n, m) + n) >> l; mulhi(n, m) <= n keeps the sum in 32 bits.
+struct FastDiv {
+    uint32_t d = 1, m = 1;
+    int l = 0;
+    FastDiv() = default;
+    explicit FastDiv(uint32_t div) : d(div) {
+        l = 0;
+        while ((1ull << l) < d) ++l;
+        m = (uint32_t)((((1ull << l) - d) << 32) / d + 1);
+    }
+#ifdef __CUDACC__
+    __device__ __forceinline__ uint32_t div(uint32_t n) const { return (__umulhi(n, m) + n) >> l; }
+#endif
+};
+
 struct QuantParams {
     const void *x;
     int bf16;
@@ -48,6 +67,12 @@ struct QuantParams {
     int64_t total;
     int64_t groups;
     int *err;
+    // per-token kernels: rows are (outer, inner) pairs, outer = b * H + h and
+    // inner = s (dense) or outer = h and inner = t (packed); one launch takes
+    // outers [outer0, outer0 + n_outer) with n_outer * inner < 2^31
+    int64_t outer0;
+    uint32_t n_outer;
+    FastDiv div_inner, div_h, div_grp;
 };
 
 cudaError_t launch_quant(const QuantParams &p, cudaStream_t st, LaunchLog &log);

@@ -17,6 +17,8 @@
 // b's groups from varlen_group0().  These kernels are HBM-bound.
 #include <cooperative_groups.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -60,15 +62,19 @@ __device__ __forceinline__ float row_sum(float v, int tpr) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-token quantisation: each row of D elements is handled by D/8 lanes.
+// Per-token quantisation: each row of D elements is handled by
+// D / (8 * kRowChunks) lanes, each holding kRowChunks 16-byte chunks of it,
+// interleaved so that one load instruction of a row's lanes reads
+// contiguous bytes.  The per-row work (the lane reductions, the scale's
+// division and reciprocal, the row's addresses) is shared by 32 channels of
+// a lane (with 8 per lane it was most of the instructions).  Each thread
+// takes kRowsPerThread rows, issuing all their loads before any arithmetic.
 // ---------------------------------------------------------------------------
-// Each thread takes kRowsPerThread rows (its 8 channels of each), issuing
-// all their loads before any arithmetic so that several 16-byte loads per
-// thread are in flight (one at a time left the kernel latency-bound).
-constexpr int kRowsPerThread = 4;
+constexpr int kRowChunks = 4;
+constexpr int kRowsPerThread = 1;
 
-// One row of a thread: src its 8 channels, msub / mbias the mean rows (or
-// null), orow its output row (codes, bias; also its scale index).
+// One row of a thread: src its first chunk, msub / mbias the mean rows at
+// that chunk (or null), orow its output row (codes, bias; also its scale).
 template <typename T>
 struct RowJob {
     const T *src;
@@ -77,36 +83,65 @@ struct RowJob {
     bool valid;
 };
 
+__device__ __forceinline__ void sub8(float (&v)[8], const float *m) {
+    const float4 a = *reinterpret_cast<const float4 *>(m);
+    const float4 b = *reinterpret_cast<const float4 *>(m + 4);
+    v[0] -= a.x, v[1] -= a.y, v[2] -= a.z, v[3] -= a.w;
+    v[4] -= b.x, v[5] -= b.y, v[6] -= b.z, v[7] -= b.w;
+}
+
+__device__ __forceinline__ float dot8(const float (&v)[8], const float *m, float acc) {
+    const float4 a = *reinterpret_cast<const float4 *>(m);
+    const float4 b = *reinterpret_cast<const float4 *>(m + 4);
+    acc = fmaf(v[0], a.x, acc), acc = fmaf(v[1], a.y, acc);
+    acc = fmaf(v[2], a.z, acc), acc = fmaf(v[3], a.w, acc);
+    acc = fmaf(v[4], b.x, acc), acc = fmaf(v[5], b.y, acc);
+    acc = fmaf(v[6], b.z, acc), acc = fmaf(v[7], b.w, acc);
+    return acc;
+}
+
+// cs: elements between a lane's chunks (tpr * 8); c0: this lane's first
+// channel.  Lanes of one row are consecutive and `valid` is uniform over them.
 template <typename T>
 __device__ __forceinline__ void quant_rows(const QuantParams &p, const RowJob<T> (&job)[kRowsPerThread],
                                            int c0, int tpr) {
-    uint4 raw[kRowsPerThread];
+    const int cs = tpr * 8;
+    uint4 raw[kRowsPerThread][kRowChunks];
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k)
-        raw[k] = job[k].valid ? ldg16(job[k].src) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int c = 0; c < kRowChunks; ++c)
+            raw[k][c] = job[k].valid ? ldg16(job[k].src + c * cs) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) {
-        float v[8];
-        cvt8<T>(raw[k], v);
         float amax = 0.0f, dot = 0.0f;
         if (job[k].valid) {
-            if (job[k].mbias) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) dot = fmaf(v[i], job[k].mbias[i], dot);
+            for (int c = 0; c < kRowChunks; ++c) {
+                float v[8];
+                cvt8<T>(raw[k][c], v);
+                if (job[k].mbias) dot = dot8(v, job[k].mbias + c * cs, dot);
+                if (job[k].msub) sub8(v, job[k].msub + c * cs);
+                amax = fmax3(amax, fmax3(fabsf(v[0]), fabsf(v[1]), fabsf(v[2])),
+                             fmax3(fabsf(v[3]), fabsf(v[4]), fmaxf(fabsf(v[5]),
+                                   fmaxf(fabsf(v[6]), fabsf(v[7])))));
             }
-            if (job[k].msub) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = v[i] - job[k].msub[i];
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
         }
-        // every lane of the row takes part (valid is uniform over a row)
         amax = row_max(amax, tpr);
         dot = row_sum(dot, tpr);
         if (!job[k].valid) continue;
         const float sc = __fdiv_rn(amax, 127.0f);
-        store8_i8(p.q + job[k].orow * p.D + c0, v, sc);
+        const float rc = quant_recip(sc);
+        int8_t *dst = p.q + job[k].orow * p.D + c0;
+#pragma unroll
+        for (int c = 0; c < kRowChunks; ++c) {
+            float v[8];
+            cvt8<T>(raw[k][c], v);
+            if (job[k].msub) sub8(v, job[k].msub + c * cs);
+            uint32_t w0, w1;
+            quant8(v, sc, rc, w0, w1);
+            *reinterpret_cast<uint2 *>(dst + c * cs) = make_uint2(w0, w1);
+        }
         if (threadIdx.x % tpr == 0) {
             p.scale[job[k].orow] = sc;
             if (p.bias) p.bias[job[k].orow] = dot;
@@ -114,25 +149,32 @@ __device__ __forceinline__ void quant_rows(const QuantParams &p, const RowJob<T>
     }
 }
 
+// Row r of a launch (r < n_outer * inner) is (outer0 + r / inner, r % inner);
+// the divisions are multiplications by invariant-divisor constants (64-bit
+// division per row left these kernels instruction-bound).
 template <typename T>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
-    const int tpr = p.D / 8;
+    const int tpr = p.D / (8 * kRowChunks);
     const int rows_per_slab = 256 / tpr;
-    const int64_t nrows = (int64_t)p.B * p.H * p.S;
+    const uint32_t nrows = p.n_outer * (uint32_t)p.S;
     const int c0 = (threadIdx.x % tpr) * 8;
     RowJob<T> job[kRowsPerThread];
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) {
-        const int64_t r =
-            ((int64_t)blockIdx.x * kRowsPerThread + k) * rows_per_slab + threadIdx.x / tpr;
-        job[k] = RowJob<T>{nullptr, nullptr, nullptr, r, r < nrows};
+        const uint32_t r =
+            (blockIdx.x * kRowsPerThread + k) * rows_per_slab + threadIdx.x / tpr;
+        job[k] = RowJob<T>{nullptr, nullptr, nullptr, 0, r < nrows};
         if (r < nrows) {
-            const int64_t s = r % p.S;
-            const int64_t bh = r / p.S;
-            const int64_t b = bh / p.H, h = bh % p.H;
+            const uint32_t ol = p.div_inner.div(r);
+            const uint32_t s = r - ol * (uint32_t)p.S;
+            const int64_t bh = p.outer0 + ol;
+            const uint32_t b = p.div_h.div((uint32_t)bh);
+            const uint32_t h = (uint32_t)bh - b * (uint32_t)p.H;
+            job[k].orow = bh * p.S + s;
             job[k].src = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh + s * p.ss + c0;
             if (p.mu_bias)
-                job[k].mbias = p.mu_bias + (b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0;
+                job[k].mbias =
+                    p.mu_bias + ((int64_t)b * p.mu_heads + p.div_grp.div(h)) * p.D + c0;
             if (p.mu_sub) job[k].msub = p.mu_sub + bh * p.D + c0;
         }
     }
@@ -143,13 +185,13 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
 // Tokens outside every valid sequence are left untouched.
 template <typename T>
 __global__ void __launch_bounds__(256) quant_rows_varlen_kernel(QuantParams p) {
-    const int tpr = p.D / 8;
+    const int tpr = p.D / (8 * kRowChunks);
     const int rows_per_slab = 256 / tpr;
-    const int64_t nrows = (int64_t)p.H * p.total;
+    const uint32_t nrows = p.n_outer * (uint32_t)p.total;
     const int c0 = (threadIdx.x % tpr) * 8;
-    {
-        // the first B threads of the grid also check one sequence each for
-        // the error word
+    if (p.outer0 == 0) {
+        // the first B threads of the first launch also check one sequence
+        // each for the error word
         const int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
         if (g < p.B) {
             int64_t start = 0;
@@ -159,19 +201,22 @@ __global__ void __launch_bounds__(256) quant_rows_varlen_kernel(QuantParams p) {
     RowJob<T> job[kRowsPerThread];
 #pragma unroll
     for (int k = 0; k < kRowsPerThread; ++k) {
-        const int64_t r =
-            ((int64_t)blockIdx.x * kRowsPerThread + k) * rows_per_slab + threadIdx.x / tpr;
-        job[k] = RowJob<T>{nullptr, nullptr, nullptr, r, false};
+        const uint32_t r =
+            (blockIdx.x * kRowsPerThread + k) * rows_per_slab + threadIdx.x / tpr;
+        job[k] = RowJob<T>{nullptr, nullptr, nullptr, 0, false};
         if (r < nrows) {
-            const int64_t h = r / p.total, t = r % p.total;
+            const uint32_t hl = p.div_inner.div(r);
+            const int64_t t = r - hl * (uint32_t)p.total;
+            const int64_t h = p.outer0 + hl;
             const int b = varlen_bisect(p.B, t, [&](int i) { return (int64_t)p.cu[i]; });
             int64_t start = 0;
             const int len = varlen_seq(p.cu, b, p.S, p.total, nullptr, &start);
+            job[k].orow = h * p.total + t;
             job[k].valid = t >= start && t < start + len;
             job[k].src = reinterpret_cast<const T *>(p.x) + h * p.sh + t * p.ss + c0;
             if (p.mu_bias)
-                job[k].mbias =
-                    p.mu_bias + ((int64_t)b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0;
+                job[k].mbias = p.mu_bias +
+                               ((int64_t)b * p.mu_heads + p.div_grp.div((uint32_t)h)) * p.D + c0;
             if (p.mu_sub) job[k].msub = p.mu_sub + ((int64_t)b * p.H + h) * p.D + c0;
         }
     }
@@ -219,12 +264,7 @@ __device__ __forceinline__ void quant_block_regs(const QuantParams &p, const T *
         const int64_t t = t0 + lt + (int64_t)it * rpp;
         raw[it] = t < t1 ? ldg16(base + t * p.ss) : make_uint4(0, 0, 0, 0);
     }
-    float ms[8], mb[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        ms[i] = msub ? msub[i] : 0.0f;
-        mb[i] = mbias ? mbias[i] : 0.0f;
-    }
+    // the mean rows are read per use (L1 hits), not held in registers
     float amax = 0.0f;
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
@@ -232,18 +272,19 @@ __device__ __forceinline__ void quant_block_regs(const QuantParams &p, const T *
         float v[8];
         cvt8<T>(raw[it], v);
         if (mbias) {
-            float dot = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) dot = fmaf(v[i], mb[i], dot);
+            float dot = dot8(v, mbias, 0.0f);
             dot = row_sum(dot, tpr);
             if (t < t1 && threadIdx.x % tpr == 0) p.bias[orow0 + t] = dot;
         }
         if (t < t1) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(msub ? v[i] - ms[i] : v[i]));
+            if (msub) sub8(v, msub);
+            amax = fmax3(amax, fmax3(fabsf(v[0]), fabsf(v[1]), fabsf(v[2])),
+                         fmax3(fabsf(v[3]), fabsf(v[4]), fmaxf(fabsf(v[5]),
+                               fmaxf(fabsf(v[6]), fabsf(v[7])))));
         }
     }
     const float s = __fdiv_rn(block_max(amax), 127.0f);
+    const float rc = quant_recip(s);
     if (threadIdx.x == 0) p.scale[sidx] = s;
 #pragma unroll
     for (int it = 0; it < IT; ++it) {
@@ -251,11 +292,10 @@ __device__ __forceinline__ void quant_block_regs(const QuantParams &p, const T *
         if (t < t1) {
             float v[8];
             cvt8<T>(raw[it], v);
-            if (msub) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = v[i] - ms[i];
-            }
-            store8_i8(p.q + (orow0 + t) * p.D + c0, v, s);
+            if (msub) sub8(v, msub);
+            uint32_t w0, w1;
+            quant8(v, s, rc, w0, w1);
+            *reinterpret_cast<uint2 *>(p.q + (orow0 + t) * p.D + c0) = make_uint2(w0, w1);
         }
     }
 }
@@ -317,18 +357,21 @@ __device__ __forceinline__ void quant_block_any(const QuantParams &p, const T *b
 template <typename T, int IT>
 __global__ void __launch_bounds__(1024) quant_blocks_kernel(QuantParams p) {
     const int tpr = p.D / 8;
-    const int64_t ngroups = (p.S + p.block - 1) / p.block;
-    const int64_t g = blockIdx.x % ngroups;
-    const int64_t bh = blockIdx.x / ngroups;
-    const int64_t b = bh / p.H, h = bh % p.H;
-    const int64_t t0 = g * p.block;
+    // CTA = (b * H + h) * ngroups + g, split by invariant-divisor constants
+    const uint32_t ngroups = p.div_inner.d;
+    const uint32_t bh = p.div_inner.div(blockIdx.x);
+    const uint32_t g = blockIdx.x - bh * ngroups;
+    const uint32_t b = p.div_h.div(bh);
+    const uint32_t h = bh - b * (uint32_t)p.H;
+    const int64_t t0 = (int64_t)g * p.block;
     const int64_t t1 = (t0 + p.block < (int64_t)p.S) ? t0 + p.block : (int64_t)p.S;
     const int c0 = (threadIdx.x % tpr) * 8;
     const T *base = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh + c0;
-    const float *msub = p.mu_sub ? p.mu_sub + bh * p.D + c0 : nullptr;
+    const float *msub = p.mu_sub ? p.mu_sub + (int64_t)bh * p.D + c0 : nullptr;
     const float *mbias =
-        p.mu_bias ? p.mu_bias + (b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0 : nullptr;
-    quant_block_any<T, IT>(p, base, msub, mbias, t0, t1, bh * p.S, bh * ngroups + g);
+        p.mu_bias ? p.mu_bias + ((int64_t)b * p.mu_heads + p.div_grp.div(h)) * p.D + c0 : nullptr;
+    quant_block_any<T, IT>(p, base, msub, mbias, t0, t1, (int64_t)bh * p.S,
+                           (int64_t)bh * ngroups + g);
 }
 
 // Packed batch: one CTA per (head, scale group); the group's sequence by
@@ -337,8 +380,9 @@ __global__ void __launch_bounds__(1024) quant_blocks_kernel(QuantParams p) {
 template <typename T, int IT>
 __global__ void __launch_bounds__(1024) quant_blocks_varlen_kernel(QuantParams p) {
     const int tpr = p.D / 8;
-    const int64_t g = blockIdx.x % p.groups;
-    const int64_t h = blockIdx.x / p.groups;
+    const uint32_t hh = p.div_inner.div(blockIdx.x);  // CTA = h * groups + g
+    const int64_t g = blockIdx.x - hh * (uint32_t)p.groups;
+    const int64_t h = hh;
     const int b = varlen_bisect(p.B, g, [&](int i) {
         return varlen_group0(p.cu[i] < 0 ? 0 : p.cu[i], i, p.block);
     });
@@ -355,105 +399,113 @@ __global__ void __launch_bounds__(1024) quant_blocks_varlen_kernel(QuantParams p
     const T *base = reinterpret_cast<const T *>(p.x) + h * p.sh + start * p.ss + c0;
     const float *msub = p.mu_sub ? p.mu_sub + ((int64_t)b * p.H + h) * p.D + c0 : nullptr;
     const float *mbias =
-        p.mu_bias ? p.mu_bias + ((int64_t)b * p.mu_heads + h / (p.H / p.mu_heads)) * p.D + c0
+        p.mu_bias ? p.mu_bias + ((int64_t)b * p.mu_heads + p.div_grp.div(hh)) * p.D + c0
                   : nullptr;
     quant_block_any<T, IT>(p, base, msub, mbias, t0, t1, h * p.total + start, h * p.groups + g);
 }
 
 // ---------------------------------------------------------------------------
 // smooth_k mean: mu[b,h,c] = (sum_t x[b,h,t,c]) / S rounded once to fp32.
-// A cluster of kMeanCluster CTAs shares one (b, h): each CTA sums a slice
-// of tokens, rank 0 adds the slices through distributed shared memory.
-// f16: every f16 value is an integer multiple of 2^-24 below 2^16, so the
-// sum is kept EXACTLY as an integer count of 2^-24 units.  Without a
-// 64-bit float-to-integer conversion per element (that unit saturated
-// first): x * 2^24 = hi * 2^20 + lo with integers |hi| <= 2^20 and
-// |lo| <= 2^19, both obtained on the FMA pipe from the bits of
-// t = x * 2^4 + 1.5 * 2^23 (rounded once to the integer hi, held in the
+// A cluster of kMeanCluster CTAs shares one (b, h) and kMeanSlice channels:
+// each CTA sums a slice of tokens, rank 0 adds the slices through
+// distributed shared memory (channel slices keep few (b, h) pairs from
+// leaving most SMs idle).
+// A value |x| < 2^16 that is an integer multiple of 2^-24 (every f16 value;
+// a bf16 value of exponent -17 .. 15) is summed EXACTLY as an integer count
+// of 2^-24 units.  Without a 64-bit float-to-integer conversion per element
+// (that unit saturated first): x * 2^24 = hi * 2^20 + lo with integers
+// |hi| <= 2^20 and |lo| <= 2^19, both obtained on the FMA pipe from the bits
+// of t = x * 2^4 + 1.5 * 2^23 (rounded once to the integer hi, held in the
 // low mantissa bits of t) and of lo + 1.5 * 2^23; the raw bit patterns are
 // summed in 32 bits (their constant 1.5 * 2^23 part is taken off once per
-// count) and folded into 64 bits every kMeanFold tokens.  bf16 sums in
-// fp64 (exact whenever the fp64 sum is).
+// count) and folded into 64 bits every kMeanFold tokens.  Other bf16 values
+// (tiny, large or not finite) are summed in fp64 on a rarely taken branch
+// (the fp64 pipe is narrow: summing every bf16 value there was the
+// bottleneck).  The total, count * 2^-24 plus the fp64 part, is exact
+// whenever the values' binary span fits fp64's 53 bits.
 // ---------------------------------------------------------------------------
 constexpr int kMeanCluster = 8;
+constexpr int kMeanSlice = 64;   // channels per CTA (8 lanes of 8)
 constexpr int kMeanUnroll = 8;
 constexpr int kMeanFold = 1024;  // tokens per thread between 64-bit folds
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
 
-template <typename T>
-struct MeanAcc {  // bf16: fp64 sums
-    struct Part {
-        double s[8];
-        __device__ __forceinline__ void zero() {
+// One thread's running sums over its 8 channels; kCheck: values may fall
+// outside the exact range (bf16).
+template <bool kCheck>
+struct MeanPart {
+    uint32_t hi[8], lo[8];
+    double fb[8];  // values outside the exact range (kCheck only)
+    __device__ __forceinline__ void zero() {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) s[i] = 0.0;
+        for (int i = 0; i < 8; ++i) {
+            hi[i] = lo[i] = 0u;
+            fb[i] = 0.0;
         }
-        __device__ __forceinline__ void add(const float (&v)[8]) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) s[i] += (double)v[i];
-        }
-    };
-    using type = double;
-    static __device__ __forceinline__ void fold(Part &p, type (&acc)[8], int) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] += p.s[i];
-        p.zero();
     }
-    static __device__ __forceinline__ double finish(double s) { return s; }
-};
-
-template <>
-struct MeanAcc<__half> {
-    static constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
-    struct Part {
-        uint32_t hi[8], lo[8];
-        __device__ __forceinline__ void zero() {
-#pragma unroll
-            for (int i = 0; i < 8; ++i) hi[i] = lo[i] = 0u;
+    // the split of x (one pair of channels); ok: x lies in the exact range
+    static __device__ __forceinline__ void split(float2 x, float2 &t, float2 &tl, bool &ok0,
+                                                 bool &ok1) {
+        // t = rne(x * 2^4) + 1.5 * 2^23 (|x * 2^4| < 2^20: one rounding)
+        t = ffma2(x, make_float2(16.0f, 16.0f), make_float2(kMagic, kMagic));
+        const float2 h = fadd2(t, make_float2(-kMagic, -kMagic));  // hi, exact
+        // lo = x * 2^24 - hi * 2^20: an integer of magnitude <= 2^19 when x
+        // is a multiple of 2^-24 (exact), else a fraction that tl rounds
+        const float2 xl = fmul2(x, make_float2(16777216.0f, 16777216.0f));
+        const float2 l = ffma2(h, make_float2(-1048576.0f, -1048576.0f), xl);
+        tl = fadd2(l, make_float2(kMagic, kMagic));
+        ok0 = ok1 = true;
+        if (kCheck) {
+            const float2 back = fadd2(tl, make_float2(-kMagic, -kMagic));
+            ok0 = fabsf(x.x) < 65536.0f && back.x == l.x;
+            ok1 = fabsf(x.y) < 65536.0f && back.y == l.y;
         }
-        __device__ __forceinline__ void add(const float (&v)[8]) {
+    }
+    __device__ __forceinline__ void add(const float (&v)[8]) {
+        uint32_t bad = 0;  // bit i: channel i's value lies outside the range
 #pragma unroll
-            for (int i = 0; i < 8; i += 2) {
-                const float2 x = make_float2(v[i], v[i + 1]);
-                // t = rne(x * 2^4) + 1.5 * 2^23 (|x * 2^4| < 2^20: one rounding)
-                const float2 t = ffma2(x, make_float2(16.0f, 16.0f), make_float2(kMagic, kMagic));
-                const float2 h = fadd2(t, make_float2(-kMagic, -kMagic));  // hi, exact
-                // lo = x * 2^24 - hi * 2^20: an integer of magnitude <= 2^19, exact
-                const float2 xl = fmul2(x, make_float2(16777216.0f, 16777216.0f));
-                const float2 l = ffma2(h, make_float2(-1048576.0f, -1048576.0f), xl);
-                const float2 tl = fadd2(l, make_float2(kMagic, kMagic));
-                hi[i] += __float_as_uint(t.x);
-                hi[i + 1] += __float_as_uint(t.y);
-                lo[i] += __float_as_uint(tl.x);
-                lo[i + 1] += __float_as_uint(tl.y);
-            }
+        for (int i = 0; i < 8; i += 2) {
+            float2 t, tl;
+            bool ok0, ok1;
+            split(make_float2(v[i], v[i + 1]), t, tl, ok0, ok1);
+            // a value outside the range adds the magic alone (integer 0)
+            hi[i] += ok0 ? __float_as_uint(t.x) : __float_as_uint(kMagic);
+            hi[i + 1] += ok1 ? __float_as_uint(t.y) : __float_as_uint(kMagic);
+            lo[i] += ok0 ? __float_as_uint(tl.x) : __float_as_uint(kMagic);
+            lo[i + 1] += ok1 ? __float_as_uint(tl.y) : __float_as_uint(kMagic);
+            bad |= (ok0 ? 0u : 1u << i) | (ok1 ? 0u : 2u << i);
         }
-    };
-    using type = long long;
+        if (kCheck && bad) add_outside(fb, v, bad);
+    }
+    // out of line: the rare fp64 path keeps its sums in local memory, off
+    // the registers of the streaming loop
+    static __device__ __noinline__ void add_outside(double *fb, const float (&v)[8], uint32_t bad) {
+        for (int i = 0; i < 8; ++i)
+            if (bad >> i & 1u) fb[i] += (double)v[i];
+    }
     // n: values added since the last fold (each carried 1.5 * 2^23 in its bits)
-    static __device__ __forceinline__ void fold(Part &p, type (&acc)[8], int n) {
+    __device__ __forceinline__ void fold(long long (&acc)[8], int n) {
         const uint32_t off = (uint32_t)n * (uint32_t)__float_as_uint(kMagic);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const long long h = (int32_t)(p.hi[i] - off), l = (int32_t)(p.lo[i] - off);
+            const long long h = (int32_t)(hi[i] - off), l = (int32_t)(lo[i] - off);
             acc[i] += h * 1048576ll + l;
+            hi[i] = lo[i] = 0u;
         }
-        p.zero();
-    }
-    static __device__ __forceinline__ double finish(long long s) {
-        return (double)s * (1.0 / 16777216.0);
     }
 };
 
 template <typename T>
 __global__ void __launch_bounds__(256) token_mean_kernel(QuantParams p) {
-    using M = MeanAcc<T>;
-    using Acc = typename M::type;
-    __shared__ Acc part[2048];     // [token lanes][D]: (256 / (D/8)) * D = 2048
-    __shared__ Acc cta_sum[256];
+    constexpr bool kCheck = !std::is_same<T, __half>::value;
+    constexpr int kTpr = kMeanSlice / 8;   // lanes per token row
+    constexpr int kLanesT = 256 / kTpr;    // token lanes
+    __shared__ long long part[kLanesT * kMeanSlice];
+    __shared__ long long cta_sum[kMeanSlice];
+    __shared__ double fpart[kCheck ? kLanesT * kMeanSlice : 1];
+    __shared__ double fcta[kCheck ? kMeanSlice : 1];
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = (int)cluster.block_rank();
-    const int tpr = p.D / 8;
-    const int lanes_t = 256 / tpr;
     const int64_t bh = blockIdx.y;
     const int64_t b = bh / p.H, h = bh % p.H;
     // tokens of this (sequence, head): dense S rows, or one packed sequence
@@ -467,22 +519,23 @@ __global__ void __launch_bounds__(256) token_mean_kernel(QuantParams p) {
     const int64_t chunk = (n + kMeanCluster - 1) / kMeanCluster;
     const int64_t t0 = rank * chunk;
     const int64_t t1 = (t0 + chunk < n) ? t0 + chunk : n;
-    const int c0 = (threadIdx.x % tpr) * 8;
-    const int lt = threadIdx.x / tpr;
-    base += c0;
-    Acc acc[8];
+    const int cl = (threadIdx.x % kTpr) * 8;      // channel within the slice
+    const int ch0 = blockIdx.z * kMeanSlice;      // the slice's first channel
+    const int lt = threadIdx.x / kTpr;
+    base += ch0 + cl;
+    long long acc[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) acc[i] = 0;
-    typename M::Part part32;
+    MeanPart<kCheck> part32;
     part32.zero();
     int since_fold = 0;
     // kMeanUnroll loads in flight per thread; rows past the slice load as
     // zeros, which add nothing (and are counted like the rest)
-    for (int64_t t = t0 + lt; t < t1; t += (int64_t)lanes_t * kMeanUnroll) {
+    for (int64_t t = t0 + lt; t < t1; t += (int64_t)kLanesT * kMeanUnroll) {
         uint4 raw[kMeanUnroll];
 #pragma unroll
         for (int u = 0; u < kMeanUnroll; ++u) {
-            const int64_t tt = t + (int64_t)u * lanes_t;
+            const int64_t tt = t + (int64_t)u * kLanesT;
             raw[u] = tt < t1 ? ldg16(base + tt * p.ss) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
@@ -493,27 +546,39 @@ __global__ void __launch_bounds__(256) token_mean_kernel(QuantParams p) {
         }
         since_fold += kMeanUnroll;
         if (since_fold >= kMeanFold) {
-            M::fold(part32, acc, since_fold);
+            part32.fold(acc, since_fold);
             since_fold = 0;
         }
     }
-    M::fold(part32, acc, since_fold);
+    part32.fold(acc, since_fold);
     // reduce over the token lanes
 #pragma unroll
-    for (int i = 0; i < 8; ++i) part[lt * p.D + c0 + i] = acc[i];
+    for (int i = 0; i < 8; ++i) {
+        part[lt * kMeanSlice + cl + i] = acc[i];
+        if (kCheck) fpart[lt * kMeanSlice + cl + i] = part32.fb[i];
+    }
     __syncthreads();
-    if (threadIdx.x < p.D) {
-        Acc sum = 0;
-        for (int l = 0; l < lanes_t; ++l) sum += part[l * p.D + threadIdx.x];
+    if (threadIdx.x < kMeanSlice) {
+        long long sum = 0;
+        double fsum = 0.0;
+        for (int l = 0; l < kLanesT; ++l) {
+            sum += part[l * kMeanSlice + threadIdx.x];
+            if (kCheck) fsum += fpart[l * kMeanSlice + threadIdx.x];
+        }
         cta_sum[threadIdx.x] = sum;
+        if (kCheck) fcta[threadIdx.x] = fsum;
     }
     cluster.sync();
-    if (rank == 0 && threadIdx.x < p.D) {
-        Acc tot = 0;
-        for (int r = 0; r < kMeanCluster; ++r) tot += cluster.map_shared_rank(cta_sum, r)[threadIdx.x];
+    if (rank == 0 && threadIdx.x < kMeanSlice) {
+        long long tot = 0;
+        double ftot = 0.0;
+        for (int r = 0; r < kMeanCluster; ++r) {
+            tot += cluster.map_shared_rank(cta_sum, r)[threadIdx.x];
+            if (kCheck) ftot += cluster.map_shared_rank(fcta, r)[threadIdx.x];
+        }
         // an empty sequence has no mean; 0 keeps its (unused) row defined
-        const double mean = n > 0 ? MeanAcc<T>::finish(tot) / (double)n : 0.0;
-        p.mu_out[bh * p.D + threadIdx.x] = (float)mean;
+        const double mean = n > 0 ? ((double)tot * (1.0 / 16777216.0) + ftot) / (double)n : 0.0;
+        p.mu_out[bh * p.D + ch0 + threadIdx.x] = (float)mean;
     }
     cluster.sync();  // keep every CTA's shared memory alive until rank 0 has read it
 }
@@ -551,7 +616,7 @@ unsigned launch_blocks(const QuantParams &q, unsigned grid, cudaStream_t st, boo
 template <typename T>
 cudaError_t launch_mean_t(const QuantParams &p, cudaStream_t st, LaunchLog &log) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kMeanCluster, (unsigned)(p.B * p.H), 1);
+    cfg.gridDim = dim3(kMeanCluster, (unsigned)(p.B * p.H), (unsigned)(p.D / kMeanSlice));
     cfg.blockDim = dim3(256, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -575,35 +640,52 @@ cudaError_t launch_quant_t(const QuantParams &p, cudaStream_t st, LaunchLog &log
         if (e != cudaSuccess) return e;
         q.mu_sub = p.mu_out;
     }
-    if (p.cu) {
-        if (p.block == 1) {
-            const int rows_per_cta = 256 / (p.D / 8) * kRowsPerThread;
-            const int64_t nrows = (int64_t)p.H * p.total;
-            const int64_t checks = ((int64_t)p.B + 255) / 256;   // error-word checks
-            int64_t g = (nrows + rows_per_cta - 1) / rows_per_cta;
-            const unsigned grid = (unsigned)(g > checks ? g : checks);
-            if (grid > 0) {
-                quant_rows_varlen_kernel<T><<<grid, 256, 0, st>>>(q);
-                log.add("quant_rows_varlen_kernel", dim3(grid), dim3(256), dim3(1, 1, 1), 0);
+    q.div_h = FastDiv((uint32_t)(p.H > 0 ? p.H : 1));
+    q.div_grp = FastDiv((uint32_t)(p.H / p.mu_heads > 0 ? p.H / p.mu_heads : 1));
+    if (p.block == 1) {
+        // per-token rows, in launches of whole outers below 2^31 rows each
+        const int64_t inner = p.cu ? p.total : (int64_t)p.S;
+        const int64_t outers = p.cu ? (int64_t)p.H : (int64_t)p.B * p.H;
+        const int rows_per_cta = 256 / (p.D / (8 * kRowChunks)) * kRowsPerThread;
+        const int64_t limit = (1ll << 31) - 1 - rows_per_cta;
+        const int64_t per = inner > 0 ? limit / inner : outers;  // outers per launch
+        if ((inner > 0 && per < 1) || outers >= (1ll << 31))
+            return cudaErrorInvalidValue;  // one outer of 2^31 rows, or 2^31 outers
+        const int64_t chunk = per < outers ? per : outers;
+        q.div_inner = FastDiv((uint32_t)(inner > 0 ? inner : 1));
+        const int64_t checks = p.cu ? ((int64_t)p.B + 255) / 256 : 0;  // error-word checks
+        int64_t o0 = 0, n = 0;
+        do {
+            n = outers - o0 < chunk ? outers - o0 : chunk;
+            q.outer0 = o0;
+            q.n_outer = (uint32_t)n;
+            int64_t g = (n * inner + rows_per_cta - 1) / rows_per_cta;
+            if (o0 == 0 && g < checks) g = checks;
+            if (g > 0) {
+                if (p.cu) {
+                    quant_rows_varlen_kernel<T><<<(unsigned)g, 256, 0, st>>>(q);
+                    log.add("quant_rows_varlen_kernel", dim3((unsigned)g), dim3(256),
+                            dim3(1, 1, 1), 0);
+                } else {
+                    quant_rows_kernel<T><<<(unsigned)g, 256, 0, st>>>(q);
+                    log.add("quant_rows_kernel", dim3((unsigned)g), dim3(256), dim3(1, 1, 1), 0);
+                }
             }
-        } else {
-            const unsigned grid = (unsigned)((int64_t)p.H * p.groups);
-            if (grid > 0) {
-                const unsigned th = launch_blocks<T>(q, grid, st, true);
-                log.add("quant_blocks_varlen_kernel", dim3(grid), dim3(th), dim3(1, 1, 1), 0);
-            }
-        }
-    } else if (p.block == 1) {
-        const int rows_per_cta = 256 / (p.D / 8) * kRowsPerThread;
-        const int64_t nrows = (int64_t)p.B * p.H * p.S;
-        const unsigned grid = (unsigned)((nrows + rows_per_cta - 1) / rows_per_cta);
+            o0 += n;
+        } while (o0 < outers && n > 0);
+    } else if (p.cu) {
+        const unsigned grid = (unsigned)((int64_t)p.H * p.groups);
+        q.div_inner = FastDiv((uint32_t)(p.groups > 0 ? p.groups : 1));
         if (grid > 0) {
-            quant_rows_kernel<T><<<grid, 256, 0, st>>>(q);
-            log.add("quant_rows_kernel", dim3(grid), dim3(256), dim3(1, 1, 1), 0);
+            const unsigned th = launch_blocks<T>(q, grid, st, true);
+            log.add("quant_blocks_varlen_kernel", dim3(grid), dim3(th), dim3(1, 1, 1), 0);
         }
     } else {
         const int64_t ngroups = (p.S + p.block - 1) / p.block;
-        const unsigned grid = (unsigned)((int64_t)p.B * p.H * ngroups);
+        const int64_t cta = (int64_t)p.B * p.H * ngroups;
+        if (cta >= (1ll << 31)) return cudaErrorInvalidValue;  // 2^31 groups or more
+        const unsigned grid = (unsigned)cta;
+        q.div_inner = FastDiv((uint32_t)(ngroups > 0 ? ngroups : 1));
         if (grid > 0) {
             const unsigned th = launch_blocks<T>(q, grid, st, false);
             log.add("quant_blocks_kernel", dim3(grid), dim3(th), dim3(1, 1, 1), 0);

@@ -113,3 +113,49 @@ def test_quant_exact_ties_with_non_power_of_two_scales(sage):
     x = torch.tensor(np.stack(rows)[None, None], dtype=torch.float16, device="cuda")
     _check_quant(sage, x, 1)
     _check_quant(sage, x, 64)
+
+
+@pytest.mark.parametrize("B,H,Hmu,S,D", [(7, 5, 5, 1, 64), (3, 6, 2, 3, 128), (2, 24, 4, 33, 256),
+                                         (1, 9, 3, 2049, 64)])
+def test_quant_rows_odd_shapes(sage, B, H, Hmu, S, D):
+    """Per-token rows over (b, h, s) with sizes that are not powers of two:
+    every row's sequence, head, token and GQA mean group lands in place."""
+    x = W.dense_qkv(B, H, H, S, S, D, seed=S + H, device="cuda").q
+    mu = torch.randn((B, Hmu, D), dtype=torch.float32, device="cuda",
+                     generator=torch.Generator("cuda").manual_seed(B * H))
+    q, s, _, bias = sage.sage_quant_int8(x, mu_in=mu)
+    torch.cuda.synchronize()
+    q_ref, s_ref, _ = oracle.quant_int8(f32(x))
+    assert np.array_equal(np_(q), q_ref) and np.array_equal(np_(s), s_ref)
+    ref = oracle.row_bias(f32(x), np_(mu))
+    scale = np.abs(f32(x)).sum(-1) * np.abs(np_(mu)).max()
+    assert np.all(np.abs(np_(bias) - ref) <= 1e-5 * scale + 1e-6)
+    # the strided [B,S,H,D] view of the same tensor gives the same rows
+    q2, s2, _, _ = sage.sage_quant_int8(x.transpose(1, 2).contiguous(), layout="NHD")
+    assert torch.equal(q, q2) and torch.equal(s, s2)
+
+
+def test_quant_bf16_mean_outside_exact_range(sage):
+    """bf16 values the integer path cannot hold (finer than 2^-24, or of
+    magnitude 2^16 and up) take the fp64 path; every value here is a
+    multiple of 2^-26 and the sums stay below 2^25, so the mean is an exact
+    sum rounded once on both sides, bit for bit."""
+    g = np.random.default_rng(17)
+    B, H, S, D = 1, 2, 256, 64
+    x = g.standard_normal((B, H, S, D)).astype(np.float32)
+    x = torch.tensor(x).to(torch.bfloat16).float().numpy()
+    x[np.abs(x) < 2.0 ** -18] = 0.0                          # keep every unit >= 2^-26
+    mant = 1.0 + g.integers(0, 128, size=(B, H, S, D)) / 128.0
+    sign = np.where(g.random((B, H, S, D)) < 0.5, -1.0, 1.0)
+    tiny = (sign * mant * 2.0 ** -19).astype(np.float32)      # unit 2^-26
+    big = (sign * mant * 2.0 ** 16).astype(np.float32)        # 2^16 <= |x| < 2^17
+    pick = g.random((B, H, S, D))
+    x[..., 0:8] = np.where(pick[..., 0:8] < 0.1, tiny[..., 0:8], x[..., 0:8])
+    x[..., 8:16] = np.where(pick[..., 8:16] < 0.1, big[..., 8:16], x[..., 8:16])
+    x[..., 16] = tiny[..., 16]
+    x[..., 17] = big[..., 17]
+    x[..., 18] = np.where(pick[..., 18] < 0.5, tiny[..., 18], big[..., 18])
+    xt = torch.tensor(x, dtype=torch.bfloat16, device="cuda")
+    assert np.array_equal(f32(xt), x)                          # representable in bf16
+    _check_quant(sage, xt, 1, smooth=True)
+    _check_quant(sage, xt, 64, smooth=True)
