@@ -210,7 +210,10 @@ typedef struct sage_decode_args {
  * U = B * Hkv * ceil(Hq/Hkv/8) (sequence, KV head, 8-head tile) units and
  * P = ceil(max_context_len/16) pages: S = 2.5 SMs / U rounded (one wave of
  * about 2.5 CTAs per SM), or, when that is below 2, S = 5 SMs / U rounded
- * (several waves of shorter CTAs); at least 8 pages per segment, at most 64
+ * (several waves of shorter CTAs); when floor(R SMs / U) is above 8 (R the
+ * decode kernel's CTAs per SM for this D, the segments then merged by the
+ * combine kernel rather than in a cluster) and not below that choice, S is
+ * that one full wave instead; at least 8 pages per segment, at most 64
  * segments.  This is the choice for device-resident per-step inputs; a call
  * with num_segments == 0 whose query, block table or output is pinned host
  * memory aims at about 1.7 CTAs per SM instead (each segment's CTA reads its

@@ -341,7 +341,7 @@ SAGE_API sage_status_t sage_splitk_combine(const float *o_part, const float *lse
 // inputs and outputs are in device memory, 27 (about 1.7) when they are in
 // pinned host memory -- there every segment's CTA reads its query and table
 // slice across NVLink-C2C at start-up, and fewer CTAs measured faster.
-static int decode_segments(int B, int Hq, int Hkv, int max_context_len, int per_sm_x16) {
+static int decode_segments(int B, int Hq, int Hkv, int D, int max_context_len, int per_sm_x16) {
     if (B <= 0 || Hkv <= 0 || Hq <= 0 || Hq % Hkv || max_context_len <= 0) return 1;
     const int group = Hq / Hkv;
     const int64_t units = (int64_t)B * Hkv * ((group + 7) / 8);
@@ -360,6 +360,15 @@ static int decode_segments(int B, int Hq, int Hkv, int max_context_len, int per_
     int64_t best = (sms * per_sm_x16 / 16 + units / 2) / units;
     if (best < 2) best = (sms * 5 + units / 2) / units;
     if (best < 1) best = 1;
+    // With device-resident I/O and more segments than one cluster takes
+    // (the partials then merge in the combine kernel), one wave that fills
+    // every SM to the kernel's residency beats it: CTAs on an SM that holds
+    // fewer of them finish early and leave HBM idle at the end (batch 8:
+    // 448 CTAs at 3 per SM, 33.4 us; 384 at the 2.5-per-SM choice, 36.5).
+    if (per_sm_x16 >= 40) {
+        const int64_t full = sms * sage::decode_ctas_per_sm(D) / units;
+        if (full > sage::kDecodeMaxCluster && full >= best) best = full;
+    }
     if (best > smax) best = smax;
     const int64_t cap = sage::decode_max_segment_pages();
     if (best * cap < pages) best = (pages + cap - 1) / cap;
@@ -369,15 +378,14 @@ static int decode_segments(int B, int Hq, int Hkv, int max_context_len, int per_
 }
 
 SAGE_API int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len) {
-    (void)D;
-    return decode_segments(B, Hq, Hkv, max_context_len, 40);
+    return decode_segments(B, Hq, Hkv, D, max_context_len, 40);
 }
 
 SAGE_API int sage_decode_auto_segments(const sage_decode_args_t *a, const void *q) {
     if (!a) return 1;
     const bool host_io = is_host_memory(q ? q : (const void *)a->q) ||
                          is_host_memory(a->block_table) || is_host_memory(a->out);
-    return decode_segments(a->B, a->Hq, a->Hkv, a->max_context_len, host_io ? 27 : 40);
+    return decode_segments(a->B, a->Hq, a->Hkv, a->D, a->max_context_len, host_io ? 27 : 40);
 }
 
 SAGE_API size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments) {
