@@ -8,8 +8,9 @@
 // every W-th segment.  Each warp first issues the loads of its segments'
 // partial outputs and LSEs (up to kSegChunk per round, all independent),
 // then scans the row's S LSEs itself for M and L (no barrier), weights and
-// adds its segments, and the W partial rows add up in shared memory: one
-// memory round trip and one barrier per row.  With few rows (batch-1 decode
+// adds its segments, and the W partial rows add up in shared memory, each
+// thread summing and storing its own channels: one memory round trip and
+// one barrier per row.  With few rows (batch-1 decode
 // has a handful of (sequence, head) rows and up to 64 segments) the
 // segments, not the rows, carry the parallelism.  HBM/L2-bound.
 #include "common.cuh"
@@ -79,17 +80,15 @@ __global__ void __launch_bounds__(32 * kMaxCombineWarps) combine_kernel(CombineP
 #pragma unroll
     for (int i = 0; i < V; ++i) part[warp][lane * V + i] = acc[i];
     __syncthreads();
-    if (warp == 0) {
-        TO *out = reinterpret_cast<TO *>(p.out) + r * D + lane * V;
-#pragma unroll
-        for (int i = 0; i < V; ++i) {
-            float v = part[0][lane * V + i];
-            for (int k = 1; k < W; ++k) v += part[k][lane * V + i];
-            out[i] = DT<TO>::from_f(v);
-        }
-        // every warp, warp 0 included, found L in its first round (W <= S)
-        if (p.lse_out && lane == 0) p.lse_out[r] = L;
+    // every thread adds the W warp rows of its channels and stores them
+    TO *out = reinterpret_cast<TO *>(p.out) + r * D;
+    for (int c = threadIdx.x; c < D; c += blockDim.x) {
+        float v = part[0][c];
+        for (int k = 1; k < W; ++k) v += part[k][c];
+        out[c] = DT<TO>::from_f(v);
     }
+    // every warp, warp 0 included, found L in its first round (W <= S)
+    if (p.lse_out && threadIdx.x == 0) p.lse_out[r] = L;
 }
 
 template <int D>
