@@ -426,7 +426,7 @@ __global__ void __launch_bounds__(1024) quant_blocks_varlen_kernel(QuantParams p
 // ---------------------------------------------------------------------------
 constexpr int kMeanCluster = 8;
 constexpr int kMeanSlice = 64;   // channels per CTA (8 lanes of 8)
-constexpr int kMeanUnroll = 8;
+constexpr int kMeanUnroll = 4;   // rows per thread per batch (two batches in flight)
 constexpr int kMeanFold = 1024;  // tokens per thread between 64-bit folds
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
 
@@ -529,19 +529,28 @@ __global__ void __launch_bounds__(256) token_mean_kernel(QuantParams p) {
     MeanPart<kCheck> part32;
     part32.zero();
     int since_fold = 0;
-    // kMeanUnroll loads in flight per thread; rows past the slice load as
-    // zeros, which add nothing (and are counted like the rest)
-    for (int64_t t = t0 + lt; t < t1; t += (int64_t)kLanesT * kMeanUnroll) {
-        uint4 raw[kMeanUnroll];
+    // Software pipelined: the next batch of kMeanUnroll rows is loaded
+    // before the current one is summed, so a thread always has loads in
+    // flight (loading, then summing, left HBM idle during the sums); rows
+    // past the slice load as zeros, which add nothing (and are counted like
+    // the rest).
+    const int64_t step = (int64_t)kLanesT * kMeanUnroll;
+    auto load_batch = [&](int64_t t, uint4 (&raw)[kMeanUnroll]) {
 #pragma unroll
         for (int u = 0; u < kMeanUnroll; ++u) {
             const int64_t tt = t + (int64_t)u * kLanesT;
             raw[u] = tt < t1 ? ldg16(base + tt * p.ss) : make_uint4(0, 0, 0, 0);
         }
+    };
+    uint4 cur[kMeanUnroll];
+    load_batch(t0 + lt, cur);
+    for (int64_t t = t0 + lt; t < t1; t += step) {
+        uint4 nxt[kMeanUnroll];
+        load_batch(t + step, nxt);
 #pragma unroll
         for (int u = 0; u < kMeanUnroll; ++u) {
             float v[8];
-            cvt8<T>(raw[u], v);
+            cvt8<T>(cur[u], v);
             part32.add(v);
         }
         since_fold += kMeanUnroll;
@@ -549,6 +558,8 @@ __global__ void __launch_bounds__(256) token_mean_kernel(QuantParams p) {
             part32.fold(acc, since_fold);
             since_fold = 0;
         }
+#pragma unroll
+        for (int u = 0; u < kMeanUnroll; ++u) cur[u] = nxt[u];
     }
     part32.fold(acc, since_fold);
     // reduce over the token lanes
