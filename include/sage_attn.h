@@ -216,8 +216,9 @@ typedef struct sage_decode_args {
  * that one full wave instead; at least 8 pages per segment, at most 64
  * segments.  This is the choice for device-resident per-step inputs; a call
  * with num_segments == 0 whose query, block table or output is pinned host
- * memory aims at about 1.7 CTAs per SM instead (each segment's CTA reads its
- * inputs across the CPU-GPU link).  The rule is empirical, measured on GB300. */
+ * memory starts from about 1.7 CTAs per SM instead of 2.5 (each segment's
+ * CTA reads its inputs across the CPU-GPU link), the full-wave clause
+ * alike.  The rule is empirical, measured on GB300. */
 int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len);
 
 /* The segment count a decode call with args->num_segments == 0 will use,

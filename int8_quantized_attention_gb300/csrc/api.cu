@@ -360,12 +360,13 @@ static int decode_segments(int B, int Hq, int Hkv, int D, int max_context_len, i
     int64_t best = (sms * per_sm_x16 / 16 + units / 2) / units;
     if (best < 2) best = (sms * 5 + units / 2) / units;
     if (best < 1) best = 1;
-    // With device-resident I/O and more segments than one cluster takes
-    // (the partials then merge in the combine kernel), one wave that fills
-    // every SM to the kernel's residency beats it: CTAs on an SM that holds
-    // fewer of them finish early and leave HBM idle at the end (batch 8:
-    // 448 CTAs at 3 per SM, 33.4 us; 384 at the 2.5-per-SM choice, 36.5).
-    if (per_sm_x16 >= 40) {
+    // With more segments than one cluster takes (the partials then merge in
+    // the combine kernel), one wave that fills every SM to the kernel's
+    // residency beats it: CTAs on an SM that holds fewer of them finish
+    // early and leave HBM idle at the end (batch 8: 448 CTAs at 3 per SM,
+    // 33.4 us per call; 384 at the 2.5-per-SM choice, 36.5; with pinned host
+    // I/O 38.3 us against 40.1 for 8 segments in one cluster).
+    {
         const int64_t full = sms * sage::decode_ctas_per_sm(D) / units;
         if (full > sage::kDecodeMaxCluster && full >= best) best = full;
     }

@@ -299,3 +299,29 @@ def test_decode_pinned_host_io_bitwise(sage):
                                                sage.SAGE_BF16, None, 0, None)
     assert st == sage.SAGE_ERR_INVALID_ARG
     assert b"pinned host memory" in sage.lib().sage_get_last_error_message()
+
+
+def test_auto_segments_fill_one_wave(sage):
+    """Past one cluster's 8 segments the library's choice is one full wave:
+    decode_kernel<256> holds 3 CTAs per SM (160 threads x 128 registers,
+    ~71 KB of shared memory), and the (sequence, KV head) units times the
+    segments fill the SMs to that without a second wave.  Pinned host I/O
+    takes the same choice for this shape."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    B, Hq, Hkv, D, ctx = 8, 24, 4, 256, 8192
+    S = sage.decode_num_segments(B, Hq, Hkv, D, ctx)
+    units = B * Hkv
+    assert S > 8 and S * units <= 3 * sms < (S + 1) * units, (S, sms)
+    c = W.paged_cache(B, Hkv, D, [ctx] * B, seed=7, device="cuda")
+    q = W.decode_query(B, Hq, D, seed=7, device="cuda")
+    dev = sage.sage_attn_decode_paged_q16(q, c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                          c.block_table, c.lens, ctx)
+    torch.cuda.synchronize()
+    assert sage.last_launch_info()["num_segments"] == S
+    qh, bth, lh = q.cpu().pin_memory(), c.block_table.cpu().pin_memory(), c.lens.cpu().pin_memory()
+    out_h = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
+    sage.sage_attn_decode_paged_q16(qh, c.k_cache, c.v_cache, c.k_scale, c.v_scale, bth, lh, ctx,
+                                    out=out_h)
+    torch.cuda.synchronize()
+    assert sage.last_launch_info()["num_segments"] == S
+    assert torch.equal(out_h, dev.cpu())
