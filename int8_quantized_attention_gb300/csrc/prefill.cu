@@ -313,6 +313,22 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     const int T = n_pre + n_ch;
     const int wpre = p.Ppad / BN;  // first chunk tile in the workspace
 
+    // The softmax threads issue the loads of their query row's channels now:
+    // they land while the barriers and tensor memory are set up (issued
+    // after that, each 16-byte piece between shared-memory stores, the query
+    // took ~3 us of every CTA's start-up).
+    constexpr int QLD = D / (16 * C::SPLIT);  // 16-byte pieces of a thread's channels
+    uint4 qw[QLD];
+    {
+        const int wq = warp >> 2;
+        const int iq = i0 + (wq / C::SPLIT) * 128 + (threadIdx.x & 127);
+        const bool ok = warp < kProducer && iq < Sq();
+        const int8_t *src = p.q + (ok ? q_row(iq) * D : 0) + (wq % C::SPLIT) * (D / C::SPLIT);
+#pragma unroll
+        for (int k = 0; k < QLD; ++k)
+            qw[k] = ok ? __ldg(reinterpret_cast<const uint4 *>(src) + k) : make_uint4(0, 0, 0, 0);
+    }
+
     if (threadIdx.x == 0) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(bar(B_KV_FULL + s), 1);
@@ -499,17 +515,16 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             }
         };
         {
-            const int8_t *qrow = p.q + q_row(i) * D;
             if constexpr (C::QT) {
                 // Q row int8 -> exact f16 pairs in this thread's TMEM lane
                 // (each of a row's SPLIT threads writes its share of channels)
-#pragma unroll 1
-                for (int c = hc * (D / 64 / SPLIT); c < (hc + 1) * (D / 64 / SPLIT); ++c) {
+#pragma unroll
+                for (int cc = 0; cc < D / 64 / SPLIT; ++cc) {
+                    const int c = hc * (D / 64 / SPLIT) + cc;
                     uint32_t v[32];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
-                        uint4 w = make_uint4(0, 0, 0, 0);
-                        if (row_ok) w = *reinterpret_cast<const uint4 *>(qrow + c * 64 + u * 16);
+                        const uint4 w = qw[cc * 4 + u];
                         i8x4_to_f16x4(w.x, v[u * 8 + 0], v[u * 8 + 1]);
                         i8x4_to_f16x4(w.y, v[u * 8 + 2], v[u * 8 + 3]);
                         i8x4_to_f16x4(w.z, v[u * 8 + 4], v[u * 8 + 5]);
@@ -523,11 +538,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 // Q row int8 -> f16 in the swizzled K-major layout of the A operand
                 uint8_t *qt = sm + t * C::QB;
 #pragma unroll
-                for (int dc = hc * (D / 16 / SPLIT); dc < (hc + 1) * (D / 16 / SPLIT); ++dc) {
-                    uint4 w = make_uint4(0, 0, 0, 0);
-                    if (row_ok) w = *reinterpret_cast<const uint4 *>(qrow + dc * 16);
-                    store_piece<128>(qt, r, dc, w);
-                }
+                for (int k = 0; k < QLD; ++k) store_piece<128>(qt, r, hc * QLD + k, qw[k]);
                 tc::fence_proxy_async();  // st.shared -> visible to the tensor core
             }
             mbar_arrive(bar(B_Q_READY));
@@ -750,16 +761,24 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         uint16_t *obase = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i) * D;
         // smooth_v: the V mean goes back onto rows that saw a key
         const float *vmu = (p.v_mean && l > 0.0f) ? v_mean_late() : nullptr;
+        // two 32-column pieces of O per tensor-memory round trip
+        constexpr int NCH = D / 32 / SPLIT;
+        static_assert(NCH % 2 == 0, "O pieces go in pairs");
 #pragma unroll 1
-        for (int c = hc * (D / 32 / SPLIT); c < (hc + 1) * (D / 32 / SPLIT); ++c) {
-            uint32_t o[32];
+        for (int c2 = 0; c2 < NCH; c2 += 2) {
+            uint32_t oo[2][32];
             if (have) {
-                tc::ld32(tmem + lane_base + t * D + c * 32, o);
+                tc::ld32(tmem + lane_base + t * D + (hc * NCH + c2) * 32, oo[0]);
+                tc::ld32(tmem + lane_base + t * D + (hc * NCH + c2 + 1) * 32, oo[1]);
                 tc::wait_ld();
             } else {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) o[e] = 0u;
+                for (int e = 0; e < 32; ++e) oo[0][e] = oo[1][e] = 0u;
             }
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+            const int c = hc * NCH + c2 + h2;
+            const uint32_t (&o)[32] = oo[h2];
             if (row_ok) {
                 uint32_t pk[16];
                 if (vmu) {
@@ -785,6 +804,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            }
             }
         }
         if (row_ok && p.lse && hc == 0)
