@@ -102,6 +102,10 @@ struct PCfg {
     static_assert(NQ * D + NQ * NS * BN + (QT ? NQ * D / 2 : 0) <= 512,
                   "tensor memory holds 512 columns");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
+    // epilogue staging: 4 KB per softmax warp, in its tile's Q tile or, with
+    // one query tile, in the key ring
+    static_assert(QB == 0 ? NST * SB >= NSW * 4 * 4096 : (QB >= 4 * 4096 && NQ > 1),
+                  "epilogue staging fits");
 };
 
 // barrier slots
@@ -758,9 +762,20 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         }
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
         const int64_t orow = q_row_late(i);
-        uint16_t *obase = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i) * D;
         // smooth_v: the V mean goes back onto rows that saw a key
         const float *vmu = (p.v_mean && l > 0.0f) ? v_mean_late() : nullptr;
+        // The O rows go out through shared memory: each warp stages its 32
+        // rows, 64 channels at a time, then stores 4 rows' 128-byte pieces
+        // per instruction (one row per thread made every store instruction
+        // touch 32 rows, most of the epilogue's time).  The staging space is
+        // this tile's Q tile (not read since its last QK^T, which retired
+        // before the last P.V) or, with one query tile, the key ring (every
+        // MMA has retired by now); 16-byte pieces XOR-swizzled by row.
+        const int i_w0 = i - lane;  // this warp's first row (rows are consecutive)
+        const int64_t ostride = VL ? (int64_t)p.Hq * D : (int64_t)D;  // elements between rows
+        uint16_t *obase0 = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i_w0) * D;
+        uint8_t *ost = (C::QB > 0 ? sm + t * C::QB + (warp & 3) * 4096 : sm + C::OFF_ST + warp * 4096);
+        const int nrow_w = min(32, Sq() - i_w0);  // rows of this warp inside the sequence
         // two 32-column pieces of O per tensor-memory round trip
         constexpr int NCH = D / 32 / SPLIT;
         static_assert(NCH % 2 == 0, "O pieces go in pairs");
@@ -775,14 +790,12 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) oo[0][e] = oo[1][e] = 0u;
             }
+            uint32_t pk[32];  // this row's 64 channels, f16 / bf16 pairs
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
-            const int c = hc * NCH + c2 + h2;
-            const uint32_t (&o)[32] = oo[h2];
-            if (row_ok) {
-                uint32_t pk[16];
+                const uint32_t(&o)[32] = oo[h2];
                 if (vmu) {
-                    const float4 *m4 = reinterpret_cast<const float4 *>(vmu + c * 32);
+                    const float4 *m4 = reinterpret_cast<const float4 *>(vmu + (hc * NCH + c2 + h2) * 32);
 #pragma unroll
                     for (int e = 0; e < 16; e += 2) {
                         const float4 m = m4[e / 2];
@@ -790,21 +803,31 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                                                 make_float2(m.x, m.y));
                         const float2 v1 = ffma2(u2f2(o[2 * e + 2], o[2 * e + 3]),
                                                 make_float2(inv, inv), make_float2(m.z, m.w));
-                        pk[e] = pack2(v0.x, v0.y, p.out_bf16 != 0);
-                        pk[e + 1] = pack2(v1.x, v1.y, p.out_bf16 != 0);
+                        pk[h2 * 16 + e] = pack2(v0.x, v0.y, p.out_bf16 != 0);
+                        pk[h2 * 16 + e + 1] = pack2(v1.x, v1.y, p.out_bf16 != 0);
                     }
                 } else {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) {
                         const float2 v = fmul2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv));
-                        pk[e] = pack2(v.x, v.y, p.out_bf16 != 0);
+                        pk[h2 * 16 + e] = pack2(v.x, v.y, p.out_bf16 != 0);
                     }
                 }
-                uint4 *dst = reinterpret_cast<uint4 *>(obase + c * 32);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    dst[e] = make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
             }
+            __syncwarp();  // the previous pair's staged rows have been read
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4 *>(ost + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            __syncwarp();
+            const int j = lane & 7;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int rr = (lane >> 3) + 4 * k;
+                if (rr < nrow_w) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(ost + rr * 128 + ((j ^ (rr & 7)) << 4));
+                    *reinterpret_cast<uint4 *>(obase0 + rr * ostride + (hc * NCH + c2) * 32 + j * 8) = v;
+                }
             }
         }
         if (row_ok && p.lse && hc == 0)
