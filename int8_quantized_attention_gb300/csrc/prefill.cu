@@ -317,23 +317,47 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     const int T = n_pre + n_ch;
     const int wpre = p.Ppad / BN;  // first chunk tile in the workspace
 
-    // The softmax threads issue the loads of their query row's channels now:
-    // they land while the barriers and tensor memory are set up (issued
-    // after that, each 16-byte piece between shared-memory stores, the query
-    // took ~3 us of every CTA's start-up).
-    constexpr int QLD = D / (16 * C::SPLIT);  // 16-byte pieces of a thread's channels
+    // The softmax threads issue their query loads now: they land while the
+    // barriers and tensor memory are set up (issued after that, each
+    // 16-byte piece between shared-memory stores, the query took ~3 us of
+    // every CTA's start-up).  A query tile's rows are consecutive in memory,
+    // so with Q headed for shared memory each warpgroup reads its tile
+    // coalesced, piece u = thread + 128 m (row u / (D / 16)); reading one
+    // row per thread made every load instruction gather 32 rows, and the
+    // CTA's ~2000 scattered misses held up its tensor-memory allocation by
+    // a microsecond.  With Q headed for tensor memory each thread needs its
+    // own row's channels (its TMEM lane).
+    constexpr int QLD = D / (16 * C::SPLIT);  // 16-byte pieces per thread
     uint4 qw[QLD];
     {
         const int wq = warp >> 2;
-        const int iq = i0 + (wq / C::SPLIT) * 128 + (threadIdx.x & 127);
-        const bool ok = warp < kProducer && iq < Sq();
-        const int8_t *src = p.q + (ok ? q_row(iq) * D : 0) + (wq % C::SPLIT) * (D / C::SPLIT);
+        const int ti = threadIdx.x & 127;
+        if constexpr (C::QT) {
+            const int iq = i0 + (wq / C::SPLIT) * 128 + ti;
+            const bool ok = warp < kProducer && iq < Sq();
+            const int8_t *src = p.q + (ok ? q_row(iq) * D : 0) + (wq % C::SPLIT) * (D / C::SPLIT);
 #pragma unroll
-        for (int k = 0; k < QLD; ++k)
-            qw[k] = ok ? __ldg(reinterpret_cast<const uint4 *>(src) + k) : make_uint4(0, 0, 0, 0);
+            for (int k = 0; k < QLD; ++k)
+                qw[k] = ok ? __ldg(reinterpret_cast<const uint4 *>(src) + k) : make_uint4(0, 0, 0, 0);
+        } else {
+            static_assert(C::QT || C::SPLIT == 1, "a shared-memory Q tile belongs to one warpgroup");
+            const int row0 = i0 + wq * 128;
+            const bool sm_thread = warp < kProducer;
+            const int8_t *src = p.q + (sm_thread && row0 < Sq() ? q_row(row0) * D : 0);
+#pragma unroll
+            for (int m = 0; m < QLD; ++m) {
+                const int u = ti + 128 * m;
+                const bool ok = sm_thread && row0 + u / (D / 16) < Sq();
+                qw[m] = ok ? __ldg(reinterpret_cast<const uint4 *>(src) + u) : make_uint4(0, 0, 0, 0);
+            }
+        }
     }
 
-    if (threadIdx.x == 0) {
+    // barriers set up by the producer warp's first thread, which holds no
+    // query loads: the initialising thread's fence waits for its own
+    // outstanding loads, and with those in flight it held the whole CTA
+    // (and the first key copies) back by about a microsecond
+    if (threadIdx.x == kProducer * 32) {
         for (int s = 0; s < NST; ++s) {
             mbar_init(bar(B_KV_FULL + s), 1);
             mbar_init(bar(B_KV_EMPTY + s), 1);
@@ -542,7 +566,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 // Q row int8 -> f16 in the swizzled K-major layout of the A operand
                 uint8_t *qt = sm + t * C::QB;
 #pragma unroll
-                for (int k = 0; k < QLD; ++k) store_piece<128>(qt, r, hc * QLD + k, qw[k]);
+                for (int m = 0; m < QLD; ++m) {
+                    const int u = r + 128 * m;
+                    store_piece<128>(qt, u / (D / 16), u % (D / 16), qw[m]);
+                }
                 tc::fence_proxy_async();  // st.shared -> visible to the tensor core
             }
             mbar_arrive(bar(B_Q_READY));
