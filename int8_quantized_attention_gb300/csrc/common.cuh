@@ -46,6 +46,29 @@ __host__ __device__ __forceinline__ int64_t varlen_key_row0(int64_t cu_b, int b,
     return (cu_b + (int64_t)b * (bn + 4) + 3) & ~(int64_t)3;
 }
 
+// The same answer found by a whole warp at once (every lane passes the
+// same B and x): each step the 32 lanes test 32 evenly spaced candidates
+// of the remaining range -- one round of independent loads -- and keep the
+// stretch after the last one that passes, so B <= 32 takes one step and
+// B <= 1024 two, where a bisection makes log2(B) dependent loads (each an
+// L2 round trip once streaming data has pushed the offsets out of L1).
+// For keys that are not non-decreasing it still returns some b in [0, B).
+template <typename Key>
+__device__ __forceinline__ int varlen_find_warp(int B, int64_t x, Key key) {
+    const int lane = threadIdx.x & 31;
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int step = (hi - lo + 32) / 32;  // ceil((hi - lo + 1) / 32) >= 1
+        const int c = lo + lane * step;
+        const unsigned m = __ballot_sync(0xffffffffu, c <= hi && key(c) <= x);
+        if (m == 0u) return lo;  // only at the first step: no key <= x, as the bisection
+        const int nlo = lo + (31 - __clz(m)) * step;
+        hi = min(hi, nlo + step - 1);
+        lo = nlo;
+    }
+    return lo;
+}
+
 // Largest b in [0, B) whose key(b) <= x, by bisection (key non-decreasing
 // for a valid packed batch; any input terminates).
 template <typename Key>

@@ -199,7 +199,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         // compact tile index: sequence b owns tiles [cu_q[b] / QR + b, ...),
         // ceil(len_b / QR) of them (at most one spare slot per sequence)
         const int g = blockIdx.x;
-        b = varlen_bisect(p.B, g, [&](int k) {
+        b = varlen_find_warp(p.B, g, [&](int k) {
             const int c = p.cu_q[k];
             return varlen_group0(c < 0 ? 0 : c, k, QR);
         });

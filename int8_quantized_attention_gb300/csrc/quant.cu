@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(1024) quant_blocks_varlen_kernel(QuantParams p
     const uint32_t hh = p.div_inner.div(blockIdx.x);  // CTA = h * groups + g
     const int64_t g = blockIdx.x - hh * (uint32_t)p.groups;
     const int64_t h = hh;
-    const int b = varlen_bisect(p.B, g, [&](int i) {
+    const int b = varlen_find_warp(p.B, g, [&](int i) {
         return varlen_group0(p.cu[i] < 0 ? 0 : p.cu[i], i, p.block);
     });
     int64_t start = 0;
