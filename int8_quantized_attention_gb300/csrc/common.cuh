@@ -18,9 +18,9 @@ constexpr int kErrBadBlock = 2;
 // range outside [0, total], running backwards or longer than the caller's
 // bound max_len sets the bad-block bit of *err (when err is given) and is
 // treated as an empty sequence.
-__device__ __forceinline__ int varlen_seq(const int32_t *cu, int b, int max_len, int64_t total,
-                                          int *err, int64_t *start) {
-    const int64_t a = cu[b], e = cu[b + 1];
+// The same from the two offsets a = cu[b], e = cu[b+1] already loaded.
+__device__ __forceinline__ int varlen_seq_of(int64_t a, int64_t e, int max_len, int64_t total,
+                                             int *err, int64_t *start) {
     if (a < 0 || e < a || e > total || e - a > max_len) {
         if (err) atomicOr(err, kErrBadBlock);
         *start = 0;
@@ -28,6 +28,11 @@ __device__ __forceinline__ int varlen_seq(const int32_t *cu, int b, int max_len,
     }
     *start = a;
     return (int)(e - a);
+}
+
+__device__ __forceinline__ int varlen_seq(const int32_t *cu, int b, int max_len, int64_t total,
+                                          int *err, int64_t *start) {
+    return varlen_seq_of(cu[b], cu[b + 1], max_len, total, err, start);
 }
 
 // First scale group of sequence b: per token (block 1) its first packed

@@ -194,6 +194,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int QR = 128 * NQ;  // query rows per CTA
     int b, hq, ct;
+    int cq0 = 0, cq1 = 0, ck0 = 0, ck1 = 0;  // packed batch: this sequence's offsets
     if constexpr (VL) {
         hq = blockIdx.y;
         // compact tile index: sequence b owns tiles [cu_q[b] / QR + b, ...),
@@ -203,8 +204,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const int c = p.cu_q[k];
             return varlen_group0(c < 0 ? 0 : c, k, QR);
         });
-        const int c = p.cu_q[b];
-        ct = g - (int)varlen_group0(c < 0 ? 0 : c, b, QR);  // reversed below
+        // the sequence's query and key bounds, loaded together
+        cq0 = p.cu_q[b], cq1 = p.cu_q[b + 1], ck0 = p.cu_k[b], ck1 = p.cu_k[b + 1];
+        ct = g - (int)varlen_group0(cq0 < 0 ? 0 : cq0, b, QR);  // reversed below
     } else {
         // one linear CTA index over (batch, head) pairs taken in bundles of
         // p.bundle (whose staged keys fit in L2 together): within a bundle
@@ -241,8 +243,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     if constexpr (VL) {
         int *e = threadIdx.x == 0 ? p.err : nullptr;  // each CTA checks its sequence
         int64_t ks = 0;
-        vsq = varlen_seq(p.cu_q, b, p.Sq, p.total_q, e, &qs);
-        vsk = varlen_seq(p.cu_k, b, p.Sk, p.total_k, e, &ks);
+        vsq = varlen_seq_of(cq0, cq1, p.Sq, p.total_q, e, &qs);
+        vsk = varlen_seq_of(ck0, ck1, p.Sk, p.total_k, e, &ks);
         const int ntile = (vsq + QR - 1) / QR;
         // a spare slot, a slot before the first sequence, or an empty or
         // invalid sequence: nothing to do (the whole CTA returns)
