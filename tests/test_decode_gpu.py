@@ -325,3 +325,18 @@ def test_auto_segments_fill_one_wave(sage):
     torch.cuda.synchronize()
     assert sage.last_launch_info()["num_segments"] == S
     assert torch.equal(out_h, dev.cpu())
+
+
+def test_decode_output_only_8_byte_aligned(sage):
+    """An output that is only 8-byte aligned (what the interface requires)
+    gets the same bits as a 16-byte aligned one."""
+    B, Hq, Hkv, D = 2, 24, 4, 256
+    c = W.paged_cache(B, Hkv, D, [4096, 3000], seed=51, device="cuda")
+    qi, qs = _quant_query(sage, B, Hq, D, seed=52)
+    ref = _run(sage, qi, qs, c, 4096, num_segments=20)
+    buf = torch.zeros(B * Hq * D + 4, dtype=torch.bfloat16, device="cuda")
+    out = buf[4:].view(B, Hq, D)                      # 8 bytes past a 16-byte boundary
+    assert out.data_ptr() % 16 == 8
+    _run(sage, qi, qs, c, 4096, num_segments=20, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
