@@ -100,6 +100,21 @@ def test_quant_zero_group():
     assert s[0, 1] == np.float32(1) / np.float32(127) and np.all(q[0, 2:] == 127)
 
 
+def test_quant_per_block_tail_group_closed_form():
+    """S = 130 in 64-token groups: rows 0-127 hold even integers with amax
+    254 (scale exactly 2, codes x / 2), the 2-row tail group integers with
+    amax 127 (scale 1, codes x): a group boundary or tail taken wrong moves
+    a scale or a code."""
+    rng = np.random.default_rng(7)
+    head = 2.0 * integer_rows(rng, 128, 32)            # every row reaches +-254
+    tail = integer_rows(rng, 2, 32)                    # every row reaches +-127
+    x = np.concatenate([head, tail])[None].astype(np.float32)
+    q, s, _ = oracle.quant_int8(x, block_tokens=64)
+    assert s.shape == (1, 3) and s[0].tolist() == [2.0, 2.0, 1.0]
+    assert np.array_equal(q[0, :128].astype(np.float32), head / 2.0)
+    assert np.array_equal(q[0, 128:].astype(np.float32), tail)
+
+
 def test_quant_integer_identity():
     rng = np.random.default_rng(2)
     x = integer_rows(rng, 50, 128)
