@@ -135,6 +135,17 @@ def test_token_mean_closed_forms():
     assert np.all(oracle.token_mean(const) == 3.25)
 
 
+def test_token_mean_wide_range_is_exact():
+    """The mean is an exact sum rounded once: values 40 binades apart
+    cancel exactly (a float32 running sum would lose the small terms and
+    give 0), and a large offset plus a tiny mean comes back exactly."""
+    x = np.array([2.0 ** 20, 2.0 ** -20, -(2.0 ** 20), 2.0 ** -20], np.float32)
+    mu = oracle.token_mean(x[None, :, None])
+    assert mu[0, 0] == np.float32(2.0 ** -21)
+    big = np.array([3.0e4, 2.0 ** -18, -3.0e4, 0.0, 2.0 ** -18, 0.0, 0.0, 0.0], np.float32)
+    assert oracle.token_mean(big[None, :, None])[0, 0] == np.float32(2.0 ** -20)
+
+
 def test_smooth_subtracts_mean_before_quant():
     # K rows = mu + I with I integer (amax 127) and symmetric (+I, -I pairs)
     # so that the token mean is exactly mu and K - mu = I exactly.
