@@ -227,10 +227,13 @@ int sage_decode_num_segments(int B, int Hq, int Hkv, int D, int max_context_len)
  * to size the workspace. */
 int sage_decode_auto_segments(const sage_decode_args_t *args, const void *q);
 
-/* Bytes of workspace sage_attn_decode_paged may need: fp32 partial outputs
- * [B,Hq,S,D] plus fp32 partial LSEs [B,Hq,S] (0 when S == 1).  A call with
- * 2..8 segments normally combines in-cluster and leaves the workspace
- * untouched; it uses the workspace only if the cluster launch is refused. */
+/* Bytes of workspace sage_attn_decode_paged may need (0 when S == 1): fp32
+ * partial outputs [B,Hq,S,D], fp32 partial LSEs [B,Hq,S], then int8 query
+ * codes [B,Hq,D] and fp32 scales [B,Hq], each region 256-byte aligned.  A
+ * call with 2..8 segments normally combines in-cluster and leaves the
+ * partials untouched (it uses them only if the cluster launch is refused);
+ * the query regions serve sage_attn_decode_paged_q16 with a query in pinned
+ * host memory. */
 size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments);
 
 /* workspace: device buffer of at least sage_attn_decode_workspace_size()
@@ -245,7 +248,11 @@ sage_status_t sage_attn_decode_paged(const sage_decode_args_t *args, void *works
  * arithmetic of sage_quant_int8 ([P1] section 4: s = max|q| / 127, codes
  * round(q / s)), so the codes and the result equal sage_quant_int8 followed
  * by sage_attn_decode_paged bit for bit; the split-K segments recompute the
- * same codes instead of reading them from a separate launch. */
+ * same codes instead of reading them from a separate launch.  Exception:
+ * with a query in pinned host memory and more than one segment, the query
+ * is quantised once into the workspace (by the sage_quant_int8 kernel, one
+ * extra launch) and the decode, launched behind it, reads the codes -- every
+ * segment reading the query across the CPU-GPU link cost more. */
 sage_status_t sage_attn_decode_paged_q16(const sage_decode_args_t *args, const void *q,
                                          sage_dtype_t q_dtype, void *workspace,
                                          size_t workspace_bytes, void *stream);

@@ -389,12 +389,27 @@ SAGE_API int sage_decode_auto_segments(const sage_decode_args_t *a, const void *
     return decode_segments(a->B, a->Hq, a->Hkv, a->D, a->max_context_len, host_io ? 27 : 40);
 }
 
+// Decode workspace (S > 1): fp32 partial outputs [B*Hq, S, D], fp32 partial
+// LSEs [B*Hq, S], then the int8 query codes [B*Hq, D] and their scales
+// [B*Hq] of a query that sits in pinned host memory, each region 256-byte
+// aligned.
+struct DecodeWorkspace {
+    size_t l_off, qc_off, qs_off, bytes;
+};
+static DecodeWorkspace decode_workspace(int B, int Hq, int D, int S) {
+    DecodeWorkspace w = {0, 0, 0, 0};
+    if (S <= 1 || B <= 0 || Hq <= 0 || D <= 0) return w;
+    const size_t rows = (size_t)B * Hq * S, qrows = (size_t)B * Hq;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    w.l_off = up(rows * D * sizeof(float));
+    w.qc_off = w.l_off + up(rows * sizeof(float));
+    w.qs_off = w.qc_off + up(qrows * D);
+    w.bytes = w.qs_off + qrows * sizeof(float);
+    return w;
+}
+
 SAGE_API size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_segments) {
-    if (num_segments <= 1 || B <= 0 || Hq <= 0 || D <= 0) return 0;
-    const size_t rows = (size_t)B * Hq * num_segments;
-    size_t o = rows * D * sizeof(float);
-    o = (o + 255) & ~(size_t)255;
-    return o + rows * sizeof(float);
+    return decode_workspace(B, Hq, D, num_segments).bytes;
 }
 
 // partials_o / partials_l (optional): write the segment partials there and
@@ -480,6 +495,38 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
         return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "decode launch");
     }
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    const DecodeWorkspace w = decode_workspace(a->B, a->Hq, a->D, S);
+    if (S > 1) {
+        if (!workspace || workspace_bytes < w.bytes)
+            return fail(SAGE_ERR_INVALID_ARG, "workspace too small: need %zu bytes for %d segments",
+                        w.bytes, S);
+        if (!aligned(workspace, 16)) return fail(SAGE_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
+    }
+    if (q_fp && S > 1 && !dbg && is_host_memory(q_fp)) {
+        // A query in pinned host memory is quantised once, by the per-token
+        // kernel reading it across NVLink-C2C, into the workspace (the same
+        // codes and scales, bit for bit); every segment's CTA then reads the
+        // codes from device memory instead of the query from the host (14
+        // segments per (sequence, kv head) read it 14 times).  The decode is
+        // launched right behind it and overlaps its start-up with it.
+        char *ws = static_cast<char *>(workspace);
+        sage::QuantParams qp = {};
+        qp.x = q_fp;
+        qp.bf16 = q_fp_bf16;
+        qp.B = a->B, qp.H = a->Hq, qp.S = 1, qp.D = a->D;
+        qp.sb = (int64_t)a->Hq * a->D, qp.sh = a->D, qp.ss = a->D;
+        qp.block = 1;
+        qp.mu_heads = 1;
+        qp.q = reinterpret_cast<int8_t *>(ws + w.qc_off);
+        qp.scale = reinterpret_cast<float *>(ws + w.qs_off);
+        sage::LaunchLog qlog;
+        cudaError_t e = sage::launch_quant(qp, cs, qlog);
+        if (e != cudaSuccess) return cuda_fail(e, "query quantisation launch");
+        p.q = qp.q, p.q_scale = qp.scale;
+        p.q_fp = nullptr;
+        p.after_quant = 1;
+        g_last.count = qlog.count;
+    }
     if (S > 1 && S <= sage::kDecodeMaxCluster) {
         // the segments of each (sequence, kv head, head tile) form one
         // cluster and combine in distributed shared memory
@@ -491,18 +538,13 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
             return cuda_fail(e, "decode launch (cluster)");
         cudaGetLastError();  // clear, then take the partials + combine path below
         p.cluster = 0;
+        const int n = g_last.count;
         g_last = sage::LaunchLog();
+        g_last.count = n > 0 ? n - 1 : 0;  // the query's quantisation, when it ran
     }
     if (S > 1) {
-        const size_t need = sage_attn_decode_workspace_size(a->B, a->Hq, a->D, S);
-        if (!workspace || workspace_bytes < need)
-            return fail(SAGE_ERR_INVALID_ARG, "workspace too small: need %zu bytes for %d segments",
-                        need, S);
-        if (!aligned(workspace, 16)) return fail(SAGE_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
-        const size_t rows = (size_t)a->B * a->Hq * S;
         p.o_part = static_cast<float *>(workspace);
-        p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                               ((rows * a->D * sizeof(float) + 255) & ~(size_t)255));
+        p.lse_part = reinterpret_cast<float *>(static_cast<char *>(workspace) + w.l_off);
     }
     cudaError_t e = sage::launch_decode(p, cs, g_last);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");

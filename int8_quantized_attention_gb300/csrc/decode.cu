@@ -139,6 +139,22 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
     const int b = blockIdx.z;
     const int head0 = kvh * p.group + ht * 8;
     const int nheads = min(8, p.group - ht * 8);
+    // The consumers of the fused-query form load their query channels first
+    // thing: the loads land during the barrier set-up and the block-table
+    // round trip.  Issued after those, a query in pinned host memory (read
+    // over NVLink-C2C by every segment's CTA) delayed the first page by ~4 us.
+    constexpr int kQPieces = D / 64;  // 8-byte pieces (4 channels) per lane
+    uint2 qraw[kQPieces];
+    {
+        const int hh = 2 * warp + (lane >> 4);
+        const bool ld = p.q_fp && warp < kConsumerWarps && hh < nheads;
+        const uint16_t *src = ld ? static_cast<const uint16_t *>(p.q_fp) +
+                                       ((int64_t)b * p.Hq + head0 + hh) * D + (lane & 15) * (D / 16)
+                                 : nullptr;
+#pragma unroll
+        for (int k = 0; k < kQPieces; ++k)
+            qraw[k] = ld ? *reinterpret_cast<const uint2 *>(src + 4 * k) : make_uint2(0u, 0u);
+    }
     int ctx = p.context_lens[b];
     if (ctx < 0 || ctx > p.max_ctx) {  // never read past the table row
         if (threadIdx.x == 0) atomicOr(p.err, kErrBadBlock);
@@ -225,11 +241,9 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
                 const int c0 = (lane & 15) * cpl;
                 float f[cpl];
                 if (hh < nheads) {
-                    const uint16_t *src = static_cast<const uint16_t *>(p.q_fp) +
-                                          ((int64_t)b * p.Hq + head0 + hh) * D + c0;
 #pragma unroll
                     for (int e = 0; e < cpl; e += 4) {
-                        const uint2 u = *reinterpret_cast<const uint2 *>(src + e);
+                        const uint2 u = qraw[e / 4];  // loaded at kernel start
                         const uint32_t w2[2] = {u.x, u.y};
 #pragma unroll
                         for (int k = 0; k < 2; ++k) {
@@ -276,6 +290,10 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
             for (int j = 0; j < 2; ++j)
                 colscale[j] = 2 * q4 + j < nheads ? qsc_s[2 * q4 + j] * p.qk_scale_log2 : 0.0f;
         } else {
+            // launched behind the kernel that quantises the query: wait here
+            // (the producer is already copying pages) until its codes are
+            // visible; a no-op otherwise
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             const int8_t *qrow = p.q + ((int64_t)b * p.Hq + head0 + (hv ? g : 0)) * D;
 #pragma unroll
             for (int ks = 0; ks < D / 32; ++ks) {
@@ -577,26 +595,33 @@ cudaError_t launch_d(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {
         cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const dim3 grid(p.num_segments, p.Hkv * p.head_tiles, p.B);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = Cfg::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
     if (p.cluster) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(kThreads);
-        cfg.dynamicSmemBytes = Cfg::kSmem;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = p.num_segments;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, p);
-        if (e != cudaSuccess) return e;
-        log.add("decode_kernel", grid, dim3(kThreads), dim3(p.num_segments, 1, 1), Cfg::kSmem);
-    } else {
-        decode_kernel<D><<<grid, kThreads, Cfg::kSmem, st>>>(p);
-        log.add("decode_kernel", grid, dim3(kThreads), dim3(1, 1, 1), Cfg::kSmem);
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = p.num_segments;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    if (p.after_quant) {
+        // may start while the query's quantisation runs (programmatic
+        // dependent launch); the consumers wait for it on the device
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, p);
+    if (e != cudaSuccess) return e;
+    log.add("decode_kernel", grid, dim3(kThreads), dim3(p.cluster ? p.num_segments : 1, 1, 1),
+            Cfg::kSmem);
     log.segments = p.num_segments;
     return cudaGetLastError();
 }

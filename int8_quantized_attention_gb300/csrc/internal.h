@@ -117,6 +117,8 @@ struct DecodeParams {
     int force_partials;       // write o_part/lse_part even with one segment
     int cluster;              // 1: the segments of a (sequence, kv head, head tile) form one
                               // thread-block cluster and merge through distributed shared memory
+    int after_quant;          // 1: launched right behind the kernel that writes q / q_scale
+                              // (programmatic dependent launch; consumers wait on the device)
     int *err;
 };
 

@@ -154,6 +154,9 @@ __device__ __forceinline__ void quant_rows(const QuantParams &p, const RowJob<T>
 // division per row left these kernels instruction-bound).
 template <typename T>
 __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
+    // a decode launched behind this kernel may start now; it waits on the
+    // device before reading the codes
+    asm volatile("griddepcontrol.launch_dependents;");
     const int tpr = p.D / (8 * kRowChunks);
     const int rows_per_slab = 256 / tpr;
     const uint32_t nrows = p.n_outer * (uint32_t)p.S;

@@ -340,3 +340,27 @@ def test_decode_output_only_8_byte_aligned(sage):
     _run(sage, qi, qs, c, 4096, num_segments=20, out=out)
     torch.cuda.synchronize()
     assert torch.equal(out, ref)
+
+
+def test_decode_host_query_quantised_once(sage):
+    """A query in pinned host memory is quantised once into the workspace
+    by the per-token kernel, and the decode launched behind it reads the
+    codes: the same bits as the fused path on a device query, with one more
+    launch (quantisation, decode, combine at 14 segments)."""
+    B, Hq, Hkv, D, ctx = 8, 24, 4, 256, 8192
+    c = W.paged_cache(B, Hkv, D, [ctx, 8000, 4097, 16, 8192, 3000, 1, 7777], seed=93,
+                      device="cuda")
+    q = W.decode_query(B, Hq, D, seed=93, device="cuda")
+    ref, ref_lse = sage.sage_attn_decode_paged_q16(q, c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                                   c.block_table, c.lens, ctx, num_segments=14,
+                                                   return_lse=True)
+    torch.cuda.synchronize()
+    assert sage.last_launch_info()["launches"] == 2
+    got, lse = sage.sage_attn_decode_paged_q16(q.cpu().pin_memory(), c.k_cache, c.v_cache,
+                                               c.k_scale, c.v_scale, c.block_table, c.lens, ctx,
+                                               num_segments=14, return_lse=True)
+    torch.cuda.synchronize()
+    info = sage.last_launch_info()
+    assert info["kernel"] == "decode_kernel" and info["launches"] == 3
+    assert sage.check_device_status()[0] == 0
+    assert torch.equal(got, ref) and torch.equal(lse, ref_lse)
