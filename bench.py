@@ -281,8 +281,9 @@ def run_ours(args):
                "ms_per_step": round(e_ms / args.steps, 5),
                "method": "per step: sage_attn_decode_paged_q16 called on pinned host "
                          "buffers (query, block table, context lengths in; bf16 output out), "
-                         "which the kernel reads and writes over NVLink-C2C; eager call, "
-                         "no graph"}
+                         "read and written over NVLink-C2C (the query quantised once by the "
+                         "library's quantisation kernel, the decode launched behind it); "
+                         "eager call, no graph"}
     torch.cuda.synchronize()
     st, word = sage.check_device_status()
     if st != 0:
