@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
     // device before reading the codes
     asm volatile("griddepcontrol.launch_dependents;");
     const int tpr = p.D / (8 * kRowChunks);
-    const int rows_per_slab = 256 / tpr;
+    const int rows_per_slab = (int)blockDim.x / tpr;
     const uint32_t nrows = p.n_outer * (uint32_t)p.S;
     const int c0 = (threadIdx.x % tpr) * 8;
     RowJob<T> job[kRowsPerThread];
@@ -189,7 +189,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(QuantParams p) {
 template <typename T>
 __global__ void __launch_bounds__(256) quant_rows_varlen_kernel(QuantParams p) {
     const int tpr = p.D / (8 * kRowChunks);
-    const int rows_per_slab = 256 / tpr;
+    const int rows_per_slab = (int)blockDim.x / tpr;
     const uint32_t nrows = p.n_outer * (uint32_t)p.total;
     const int c0 = (threadIdx.x % tpr) * 8;
     if (p.outer0 == 0) {
@@ -660,14 +660,18 @@ cudaError_t launch_quant_t(const QuantParams &p, cudaStream_t st, LaunchLog &log
         // per-token rows, in launches of whole outers below 2^31 rows each
         const int64_t inner = p.cu ? p.total : (int64_t)p.S;
         const int64_t outers = p.cu ? (int64_t)p.H : (int64_t)p.B * p.H;
-        const int rows_per_cta = 256 / (p.D / (8 * kRowChunks)) * kRowsPerThread;
+        // few rows (a decode step's query): 64-thread CTAs spread the loads
+        // over 4x the SMs (the rows' latency, not bandwidth, is the cost there)
+        const int64_t all_rows = inner * outers;
+        const int threads = all_rows <= 4096 ? 64 : 256;
+        const int rows_per_cta = threads / (p.D / (8 * kRowChunks)) * kRowsPerThread;
         const int64_t limit = (1ll << 31) - 1 - rows_per_cta;
         const int64_t per = inner > 0 ? limit / inner : outers;  // outers per launch
         if ((inner > 0 && per < 1) || outers >= (1ll << 31))
             return cudaErrorInvalidValue;  // one outer of 2^31 rows, or 2^31 outers
         const int64_t chunk = per < outers ? per : outers;
         q.div_inner = FastDiv((uint32_t)(inner > 0 ? inner : 1));
-        const int64_t checks = p.cu ? ((int64_t)p.B + 255) / 256 : 0;  // error-word checks
+        const int64_t checks = p.cu ? ((int64_t)p.B + threads - 1) / threads : 0;  // error-word checks
         int64_t o0 = 0, n = 0;
         do {
             n = outers - o0 < chunk ? outers - o0 : chunk;
@@ -677,12 +681,12 @@ cudaError_t launch_quant_t(const QuantParams &p, cudaStream_t st, LaunchLog &log
             if (o0 == 0 && g < checks) g = checks;
             if (g > 0) {
                 if (p.cu) {
-                    quant_rows_varlen_kernel<T><<<(unsigned)g, 256, 0, st>>>(q);
-                    log.add("quant_rows_varlen_kernel", dim3((unsigned)g), dim3(256),
+                    quant_rows_varlen_kernel<T><<<(unsigned)g, threads, 0, st>>>(q);
+                    log.add("quant_rows_varlen_kernel", dim3((unsigned)g), dim3(threads),
                             dim3(1, 1, 1), 0);
                 } else {
-                    quant_rows_kernel<T><<<(unsigned)g, 256, 0, st>>>(q);
-                    log.add("quant_rows_kernel", dim3((unsigned)g), dim3(256), dim3(1, 1, 1), 0);
+                    quant_rows_kernel<T><<<(unsigned)g, threads, 0, st>>>(q);
+                    log.add("quant_rows_kernel", dim3((unsigned)g), dim3(threads), dim3(1, 1, 1), 0);
                 }
             }
             o0 += n;
