@@ -646,3 +646,174 @@ def test_smooth_v_mean_is_the_chunk_token_mean():
     s = np.full((1, 1, 20), 0.01, np.float32)
     o, _ = oracle.prefill(q, s, 1, k, s, 1, v, causal=False, smooth_v=True)
     np.testing.assert_allclose(o[0, 0], np.broadcast_to(v[0, 0, 0], (20, D)), rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
+# per-block scales, the mixed smoothed/unsmoothed key set, row sampling and
+# the per-sequence row bias: the glue around the C functions
+# --------------------------------------------------------------------------
+
+def _grouped_rows(rng, n, d, block, exps):
+    """Integer rows whose 'block'-token group g has amax exactly 127 * 2^exps[g]
+    (every element a multiple of 2^exps[g]), so a per-block quantisation with
+    that block has scale 2^exps[g] and is exact."""
+    x = integer_rows(rng, n, d).astype(np.float64)
+    for g in range((n + block - 1) // block):
+        x[g * block:(g + 1) * block] *= 2.0 ** exps[g]
+    return x.astype(np.float32)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_per_block_scales_against_textbook(causal):
+    """Q in 128-token groups and K in 64-token groups with a different
+    power-of-two scale per group (ragged last groups): per-block quantisation
+    is then exact, so the method equals float64 attention on the original
+    values.  Swapping the two block sizes, or mapping rows to groups with
+    anything but row // block, scales some scores by the wrong group and
+    fails here."""
+    rng = np.random.default_rng(41)
+    Sq, Sk, D = 200, 300, 32                       # Q groups 128 + 72; K 4 x 64 + 44
+    q = _grouped_rows(rng, Sq, D, 128, [-3, 2])
+    k = _grouped_rows(rng, Sk, D, 64, [1, -2, 3, 0, -1])
+    v = rng.standard_normal((Sk, D))
+    qi, qs, _ = oracle.quant_int8(q[None, None], block_tokens=128)
+    ki, ks, _ = oracle.quant_int8(k[None, None], block_tokens=64)
+    assert qs[0, 0].tolist() == [2.0 ** -3, 2.0 ** 2]
+    assert ks[0, 0].tolist() == [2.0, 2.0 ** -2, 2.0 ** 3, 1.0, 0.5]
+    sm = 1.0 / (D * 127.0 * 127.0 * 8.0)
+    o, lse = oracle.prefill(qi, qs, 128, ki, ks, 64, v[None, None], causal=causal, sm_scale=sm,
+                            threads=1)
+    o_ref, lse_ref = textbook_attention(q, k, v, sm, causal, Sk - Sq)
+    np.testing.assert_allclose(o[0, 0], o_ref, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lse[0, 0], lse_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_bias_applies_to_the_chunk_not_the_prefix():
+    """Chunked prefill with smooth_k over an unsmoothed paged prefix: the
+    chunk keys are K_new = mu + I exactly (I integer, in +-pairs so the token
+    mean is mu), the prefix keys are stored codes with power-of-two scales,
+    Q is integer with amax 127.  With the row bias q.mu given, the result
+    must equal float64 attention over [prefix keys as stored || chunk keys
+    before smoothing]; the bias added to the prefix scores instead, or left
+    off the chunk, fails."""
+    rng = np.random.default_rng(42)
+    Hq, Hkv, D, P, Sc, nblk = 2, 1, 32, 40, 24, 6
+    half = integer_rows(rng, Sc // 2, D)
+    I = np.concatenate([half, -half], 0)
+    mu = (rng.integers(-200, 200, size=D) * 0.25).astype(np.float32)
+    k_new = (I + mu[None, :]).astype(np.float32)
+    q = np.stack([integer_rows(rng, Sc, D) for _ in range(Hq)])          # [Hq, Sc, D]
+    v_new = rng.standard_normal((Sc, D))
+    table = rng.permutation(nblk)[:3].astype(np.int32)
+    kl = rng.integers(-127, 128, (Hkv, P, D)).astype(np.int8)
+    vl = rng.integers(-127, 128, (Hkv, P, D)).astype(np.int8)
+    ksl = (2.0 ** -rng.integers(-1, 3, (Hkv, P))).astype(np.float32)
+    vsl = rng.uniform(0.005, 0.02, (Hkv, P)).astype(np.float32)
+    kc, ks = _scatter_to_pages(kl, ksl, table, nblk)
+    vc, vs = _scatter_to_pages(vl, vsl, table, nblk)
+    prefix = dict(k_cache=kc, v_cache=vc, k_scale=ks, v_scale=vs, block_table=table[None],
+                  lens=[P])
+    ki, ksn, mu_o = oracle.quant_int8(k_new[None, None], smooth=True)
+    assert np.array_equal(mu_o[0, 0], mu) and np.all(ksn == 1.0)
+    qi, qsc, _ = oracle.quant_int8(q[None])
+    bias = oracle.row_bias(q[None], mu_o)
+    sm = 1.0 / (D * 127.0 * 127.0 * 2.0)
+    o, lse = oracle.prefill(qi, qsc, 1, ki, ksn, 1, v_new[None, None], causal=True, sm_scale=sm,
+                            q_bias=bias, prefix=prefix, threads=1)
+    keys = np.concatenate([kl[0] * ksl[0][:, None].astype(np.float64), k_new], 0)
+    vals = np.concatenate([vl[0] * vsl[0][:, None].astype(np.float64), v_new], 0)
+    for h in range(Hq):
+        o_ref, l_ref = textbook_attention(q[h], keys, vals, sm, causal=True, offset=P)
+        np.testing.assert_allclose(o[0, h], o_ref, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[0, h], l_ref, rtol=1e-12, atol=1e-12)
+
+
+def test_prefill_row_sample_equals_full_rows():
+    """Evaluating a subset of query rows (causal, over a paged prefix, per
+    block Q and K) gives exactly those rows of the full evaluation: the row
+    positions, not their order in the sample, decide what each row sees."""
+    rng = np.random.default_rng(43)
+    Hq, Hkv, D, P, Sq = 2, 1, 32, 37, 150
+    table = rng.permutation(4)[:3].astype(np.int32)
+    kc = rng.integers(-127, 128, (4, Hkv, D // 16, 16, 16)).astype(np.int8)
+    vc = rng.integers(-127, 128, (4, Hkv, D // 16, 16, 16)).astype(np.int8)
+    sc = rng.uniform(0.005, 0.02, (4, Hkv, 16)).astype(np.float32)
+    prefix = dict(k_cache=kc, v_cache=vc, k_scale=sc, v_scale=sc[::-1].copy(),
+                  block_table=table[None], lens=[P])
+    x = rng.standard_normal((1, Hq, Sq, D)).astype(np.float32)
+    kx = rng.standard_normal((1, Hkv, Sq, D)).astype(np.float32)
+    qi, qs, _ = oracle.quant_int8(x, block_tokens=128)
+    ki, ks, _ = oracle.quant_int8(kx, block_tokens=64)
+    v = rng.standard_normal((1, Hkv, Sq, D))
+    o, lse = oracle.prefill(qi, qs, 128, ki, ks, 64, v, causal=True, prefix=prefix, threads=1)
+    rows = np.array([149, 0, 77, 128, 127, 5])
+    o2, l2 = oracle.prefill(qi, qs, 128, ki, ks, 64, v, causal=True, prefix=prefix, rows=rows,
+                            threads=1)
+    assert np.array_equal(o2, o[:, :, rows]) and np.array_equal(l2, lse[:, :, rows])
+
+
+def test_row_bias_varlen_hand_computed():
+    """b[h, t] = sum_c x[t, h, c] mu[seq(t), h // (H / Hmu), c], written out
+    with explicit loops over sequences, tokens, heads and channels; integer
+    values make every sum exact, and each sequence's mean differs so a wrong
+    sequence or GQA group changes the result."""
+    rng = np.random.default_rng(44)
+    H, Hmu, D = 4, 2, 8
+    cu = np.array([0, 3, 3, 8, 9])                    # includes an empty sequence
+    x = rng.integers(-5, 6, (cu[-1], H, D)).astype(np.float32)
+    mu = rng.integers(-3, 4, (len(cu) - 1, Hmu, D)).astype(np.float32)
+    got = oracle.row_bias_varlen(x, cu, mu)
+    want = np.zeros((H, cu[-1]))
+    for b in range(len(cu) - 1):
+        for t in range(cu[b], cu[b + 1]):
+            for h in range(H):
+                acc = 0.0
+                for c in range(D):
+                    acc += float(x[t, h, c]) * float(mu[b, h // (H // Hmu), c])
+                want[h, t] = acc
+    assert np.array_equal(got, want)
+
+
+def test_decode_pairs_and_varlen_rows_sample_the_full_result():
+    """The sampled forms the full-size parity tests use: decode over a list
+    of (sequence, KV head) pairs gives exactly those heads of the full
+    decode (the others stay zero / -inf), and varlen prefill over per-
+    sequence row lists gives exactly those rows (the others stay NaN)."""
+    rng = np.random.default_rng(45)
+    B, Hq, Hkv, D, nblk = 3, 4, 2, 32, 12
+    lens = [40, 17, 64]
+    table = rng.permutation(nblk).reshape(B, 4).astype(np.int32)
+    kc = rng.integers(-127, 128, (nblk, Hkv, D // 16, 16, 16)).astype(np.int8)
+    vc = rng.integers(-127, 128, (nblk, Hkv, D // 16, 16, 16)).astype(np.int8)
+    ks = rng.uniform(0.005, 0.02, (nblk, Hkv, 16)).astype(np.float32)
+    vs = rng.uniform(0.005, 0.02, (nblk, Hkv, 16)).astype(np.float32)
+    qi = rng.integers(-127, 128, (B, Hq, D)).astype(np.int8)
+    qs = rng.uniform(0.005, 0.02, (B, Hq)).astype(np.float32)
+    o, lse = oracle.decode_paged(qi, qs, kc, vc, ks, vs, table, lens, threads=1)
+    pairs = [(2, 0), (0, 1)]
+    o2, l2 = oracle.decode_paged(qi, qs, kc, vc, ks, vs, table, lens, threads=1, pairs=pairs)
+    for b in range(B):
+        for g in range(Hkv):
+            hs = slice(2 * g, 2 * g + 2)
+            if (b, g) in pairs:
+                assert np.array_equal(o2[b, hs], o[b, hs]) and np.array_equal(l2[b, hs], lse[b, hs])
+            else:
+                assert np.all(o2[b, hs] == 0) and np.all(np.isneginf(l2[b, hs]))
+    lq, lk = [9, 30, 4], [12, 30, 20]
+    cu_q = np.concatenate([[0], np.cumsum(lq)])
+    cu_k = np.concatenate([[0], np.cumsum(lk)])
+    xq = rng.standard_normal((cu_q[-1], Hq, D)).astype(np.float32)
+    xk = rng.standard_normal((cu_k[-1], Hkv, D)).astype(np.float32)
+    q8, qsc, _ = oracle.quant_int8_varlen(xq, cu_q, block_tokens=1)
+    k8, ksc, _ = oracle.quant_int8_varlen(xk, cu_k, block_tokens=1)
+    v = rng.standard_normal((cu_k[-1], Hkv, D))
+    of, lf = oracle.prefill_varlen(q8, qsc, 1, k8, ksc, 1, v, cu_q, cu_k, causal=True)
+    rows = [np.array([8, 0]), np.array([29, 3, 17]), np.array([1])]
+    os_, ls_ = oracle.prefill_varlen(q8, qsc, 1, k8, ksc, 1, v, cu_q, cu_k, causal=True,
+                                     rows=rows)
+    picked = np.zeros(cu_q[-1], bool)
+    for b in range(3):
+        t = cu_q[b] + rows[b]
+        picked[t] = True
+        assert np.array_equal(os_[t], of[t]) and np.array_equal(ls_[:, t], lf[:, t])
+    assert np.all(np.isnan(os_[~picked])) and np.all(np.isnan(ls_[:, ~picked]))
