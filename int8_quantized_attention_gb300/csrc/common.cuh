@@ -262,15 +262,28 @@ __device__ __forceinline__ int8_t quant_code(float v, float s, float r) {
     return static_cast<int8_t>(q);
 }
 
+// Three-input maximum that returns NaN when any input is NaN.
+__device__ __forceinline__ float fmax3_nan(float a, float b, float c) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // Eight values at once, the same codes as quant_code, as two little-endian
 // words of int8.  With |y| < 2^22, t = y + 1.5 * 2^23 holds rne(y) in the
 // low bits of its mantissa, so the low byte of t's bits is the two's
-// complement code itself and t - 1.5 * 2^23 is rne(y) as a float; if any of
-// the eight y lies within kTieBand of a rounding boundary (or is not
-// finite) the group is redone through the division.
+// complement code itself and t - 1.5 * 2^23 is rne(y) as a float.  That
+// shortcut is taken only when s is a normal float (then r = 1/s is finite
+// and |y| <= 127.00002, so no code needs the clamp) or s = 0 (every y is
+// 0), and every y lies farther than kTieBand from a rounding boundary.
+// Otherwise the group is redone through quant_code: a subnormal s (a bf16
+// group with amax below about 1.5e-36) can make r infinite -- y then is
+// +-inf or NaN -- or, with its few significand bits, put |v / s| above
+// 127.5, where the code is the clamp's 127.
 __device__ __forceinline__ void quant8(const float (&v)[8], float s, float r, uint32_t &w0,
                                        uint32_t &w1) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+    constexpr float kMinNormal = 1.17549435e-38f;
     uint32_t tb[8];
     float dmax = 0.0f;
 #pragma unroll
@@ -279,11 +292,12 @@ __device__ __forceinline__ void quant8(const float (&v)[8], float s, float r, ui
         const float2 t = fadd2(y, make_float2(kMagic, kMagic));
         const float2 yr = fadd2(t, make_float2(-kMagic, -kMagic));
         const float2 d = fadd2(y, make_float2(-yr.x, -yr.y));
-        dmax = fmax3(dmax, fabsf(d.x), fabsf(d.y));
+        dmax = fmax3_nan(dmax, fabsf(d.x), fabsf(d.y));  // a NaN d makes dmax NaN
         tb[i] = __float_as_uint(t.x);
         tb[i + 1] = __float_as_uint(t.y);
     }
-    if (dmax < 0.5f - kTieBand) {  // false for NaN
+    // the comparison is false when dmax is NaN
+    if (dmax < 0.5f - kTieBand && (s >= kMinNormal || s == 0.0f)) {
         w0 = __byte_perm(__byte_perm(tb[0], tb[1], 0x0040), __byte_perm(tb[2], tb[3], 0x0040), 0x5410);
         w1 = __byte_perm(__byte_perm(tb[4], tb[5], 0x0040), __byte_perm(tb[6], tb[7], 0x0040), 0x5410);
         return;

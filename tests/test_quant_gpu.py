@@ -159,3 +159,100 @@ def test_quant_bf16_mean_outside_exact_range(sage):
     assert np.array_equal(f32(xt), x)                          # representable in bf16
     _check_quant(sage, xt, 1, smooth=True)
     _check_quant(sage, xt, 64, smooth=True)
+
+
+def _tiny_bf16(rng, shape, group_axis_len, block, tiny_groups):
+    """bf16 values, N(0,1), whose quantisation groups listed in tiny_groups
+    (group index along the token axis, blocks of `block` tokens) are scaled
+    so that the group's amax lies in [1e-40, 3.7e-37]: the scale amax / 127
+    is then a subnormal float, whose reciprocal can overflow to infinity and
+    whose few significand bits can put |x / s| above 127.5 (code 127 by the
+    clamp).  Returns an fp32 array of values exactly representable in bf16."""
+    x = rng.standard_normal(shape).astype(np.float32)
+    for g in tiny_groups:
+        t0, t1 = g * block, min((g + 1) * block, group_axis_len)
+        sl = x[..., t0:t1, :]
+        amax = np.abs(sl).max(axis=(-2, -1), keepdims=True)
+        target = 10.0 ** rng.uniform(-40.0, np.log10(3.7e-37), size=amax.shape)
+        x[..., t0:t1, :] = sl / amax * target
+    return torch.tensor(x).to(torch.bfloat16).float().numpy()
+
+
+@pytest.mark.parametrize("block", [1, 64, 128])
+def test_quant_bf16_subnormal_scales(sage, block):
+    """Groups whose bf16 amax is below 3.7e-37 (subnormal scale): every code
+    and scale bit-exact against the oracle, next to ordinary groups in the
+    same tensor, per token and per block."""
+    rng = np.random.default_rng(100 + block)
+    B, H, S, D = 2, 3, 300, 128
+    ngroups = (S + block - 1) // block
+    tiny = [g for g in range(ngroups) if g % 3 != 1]          # some groups stay ordinary
+    x = _tiny_bf16(rng, (B, H, S, D), S, block, tiny)
+    xt = torch.tensor(x, dtype=torch.bfloat16, device="cuda")
+    assert np.array_equal(f32(xt), x)
+    q, s, _ = _check_quant(sage, xt, block)
+    sub = np_(s)[np_(s) != 0]
+    assert (sub < 1.17549435e-38).any() and (sub > 1e-3).any()
+
+
+def test_quant_bf16_subnormal_scales_decode_query(sage):
+    """A decode step's query (few rows: the small-CTA per-token path) with
+    tiny bf16 heads, bit-exact; and the same query handed to the fused
+    decode from pinned host memory, where the library quantises it once
+    into the workspace (codes at the offsets the header declares)."""
+    rng = np.random.default_rng(7)
+    B, Hq, Hkv, D, ctx = 2, 24, 4, 256, 512
+    x = _tiny_bf16(rng, (B, Hq, 1, D), 1, 1, [0])
+    x[:, ::5] = rng.standard_normal((B, x[:, ::5].shape[1], 1, D))   # a few ordinary heads
+    x = torch.tensor(x).to(torch.bfloat16).float().numpy()
+    qd = torch.tensor(x, dtype=torch.bfloat16, device="cuda")
+    _check_quant(sage, qd, 1)
+    q_ref, s_ref, _ = oracle.quant_int8(x, block_tokens=1)
+    cache = W.paged_cache(B, Hkv, D, [ctx] * B, seed=3, device="cuda")
+    q_host = qd[:, :, 0].cpu().pin_memory()
+    S = sage.decode_segments_used(ctx, 14)
+    assert S > 8                                              # partials + combine
+    # sized for the 14 segments asked for (the binding's check); the library
+    # lays the workspace out for the S segments it actually uses
+    ws = torch.zeros(sage.decode_workspace_size(B, Hq, D, 14), dtype=torch.uint8, device="cuda")
+    sage.sage_attn_decode_paged_q16(q_host, cache.k_cache, cache.v_cache, cache.k_scale,
+                                    cache.v_scale, cache.block_table, cache.lens, ctx,
+                                    num_segments=14, workspace=ws)
+    assert sage.last_launch_info()["launches"] == 3       # quant, decode, combine
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    up = lambda n: (n + 255) // 256 * 256
+    rows = B * Hq * S
+    qc_off = up(rows * D * 4) + up(rows * 4)
+    qs_off = qc_off + up(B * Hq * D)
+    w = np_(ws)
+    codes = w[qc_off:qc_off + B * Hq * D].view(np.int8).reshape(B, Hq, D)
+    scales = w[qs_off:qs_off + B * Hq * 4].view(np.float32).reshape(B, Hq)
+    assert np.array_equal(codes, q_ref[:, :, 0]) and np.array_equal(scales, s_ref[:, :, 0])
+
+
+def test_quant_varlen_bf16_subnormal_scales(sage):
+    """The packed-batch kernels with tiny bf16 groups: per-sequence codes and
+    scales bit-exact, per token and per 64-token block."""
+    rng = np.random.default_rng(9)
+    lens = [70, 130, 1, 64]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    H, D = 2, 128
+    x = rng.standard_normal((cu[-1], H, D)).astype(np.float32)
+    for b in range(len(lens)):            # in each sequence, the second half tiny
+        t0, t1 = cu[b] + lens[b] // 2, cu[b + 1]
+        if t1 > t0:
+            sl = x[t0:t1]
+            x[t0:t1] = sl / np.abs(sl).max() * 10.0 ** rng.uniform(-40, -36.5)
+    x = torch.tensor(x).to(torch.bfloat16).float().numpy()
+    xt = torch.tensor(x, dtype=torch.bfloat16, device="cuda")
+    cu_t = torch.tensor(cu, device="cuda")
+    for block in (1, 64):
+        q, s, _, _ = sage.sage_quant_int8_varlen(xt, cu_t, max(lens), block_tokens=block)
+        torch.cuda.synchronize()
+        q_ref, s_ref, _ = oracle.quant_int8_varlen(x, cu, block_tokens=block)
+        assert np.array_equal(np_(q), q_ref)
+        sc = np_(s)
+        for b in range(len(lens)):
+            g0 = cu[b] if block == 1 else cu[b] // block + b
+            assert np.array_equal(sc[:, g0:g0 + s_ref[b].shape[1]], s_ref[b])
