@@ -280,10 +280,16 @@ sage_status_t sage_attn_decode_paged_partials(const sage_decode_args_t *args, fl
  * the library, of sage_attn_decode_noalloc_max_bytes() bytes (8 MiB) per
  * GPU that loads the library, held until the process exits.  The call
  * allocates and frees nothing.
- *   - Requests whose partials exceed that size (B*Hq*S*(D+1)*4 bytes, S the
- *     segment count actually used) are rejected with SAGE_ERR_INVALID_ARG and
+ *   - Arguments are checked exactly as by sage_attn_decode_paged (shapes,
+ *     alignment, per-step buffers in device or mapped pinned host memory)
+ *     before anything is launched.
+ *   - num_segments 0: the library's own choice (sage_decode_auto_segments),
+ *     lowered to the largest count whose partials fit the array.  An
+ *     explicit count whose partials exceed it (B*Hq*S*(D+1)*4 bytes, S the
+ *     segment count actually used) is rejected with SAGE_ERR_INVALID_ARG and
  *     a message saying how many bytes were needed; with one segment no
- *     scratch is used at all.
+ *     scratch is used at all.  The segments always merge in the combine
+ *     kernel (two launches), never in a thread-block cluster.
  *   - The first call on a device looks the array's address up
  *     (cudaGetSymbolAddress); make that first call outside any stream
  *     capture.

@@ -412,13 +412,9 @@ SAGE_API size_t sage_attn_decode_workspace_size(int B, int Hq, int D, int num_se
     return decode_workspace(B, Hq, D, num_segments).bytes;
 }
 
-// partials_o / partials_l (optional): write the segment partials there and
-// skip the combine (num_segments must be given).
-static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
-                                size_t workspace_bytes, int32_t *dbg, void *stream,
-                                float *partials_o = nullptr, float *partials_l = nullptr,
-                                int *segments_used = nullptr, const void *q_fp = nullptr,
-                                int q_fp_bf16 = 0) {
+namespace sage {
+
+int check_decode_args(const sage_decode_args_t *a, const void *q_fp) {
     if (!a) return fail(SAGE_ERR_INVALID_ARG, "args is NULL");
     if (!head_dim_ok(a->D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", a->D);
     if (a->out_dtype != SAGE_F16 && a->out_dtype != SAGE_BF16)
@@ -432,7 +428,6 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
                     a->max_context_len, a->max_blocks);
     if (a->num_segments < 0 || a->num_segments > 1024)
         return fail(SAGE_ERR_INVALID_ARG, "num_segments outside [0, 1024]");
-    g_last = sage::LaunchLog();
     if (a->B == 0) return SAGE_OK;
     if ((!q_fp && (!a->q || !a->q_scale)) || !a->context_lens || !a->out)
         return fail(SAGE_ERR_INVALID_ARG, "q, q_scale, context_lens and out are required");
@@ -457,6 +452,21 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
             if (r != SAGE_OK) return r;
         }
     }
+    return SAGE_OK;
+}
+
+}  // namespace sage
+
+// partials_o / partials_l (optional): write the segment partials there and
+// skip the combine (num_segments must be given).
+static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
+                                size_t workspace_bytes, int32_t *dbg, void *stream,
+                                float *partials_o = nullptr, float *partials_l = nullptr,
+                                int *segments_used = nullptr, const void *q_fp = nullptr,
+                                int q_fp_bf16 = 0) {
+    g_last = sage::LaunchLog();
+    const sage_status_t chk = (sage_status_t)sage::check_decode_args(a, q_fp);
+    if (chk != SAGE_OK || a->B == 0) return chk;
     int S = a->num_segments ? a->num_segments : sage_decode_auto_segments(a, q_fp);
     const int pages = (a->max_context_len + 15) / 16;
     {   // a segment is at most decode_max_segment_pages() pages long

@@ -7,6 +7,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include "sage_attn.h"
+
 namespace sage {
 
 // Record of the kernels one API call enqueued (runtime-path evidence).
@@ -213,5 +215,14 @@ cudaError_t launch_timeout_probe(int timeout_us, int *err, cudaStream_t st, Laun
 int report_error(int status, const char *fmt, ...);   // sets the thread's last message
 int device_error_word(int **out);                      // this device's error word
 void record_launch(const LaunchLog &log);              // updates sage_last_launch_info
+
+// Argument checks every decode entry point makes before it launches
+// anything: head_dim and output dtype supported, Hq a multiple of Hkv,
+// max_context_len within the block table, pointers present and aligned
+// (q 4 bytes, or 8 for the f16/bf16 query q_fp of the fused form; out 8;
+// caches and scales 16), and the per-step inputs and outputs in device
+// memory or mapped pinned host memory.  Returns 0 (SAGE_OK) or the status
+// with the thread's last message set; with B == 0 only the shape checks run.
+int check_decode_args(const sage_decode_args_t *args, const void *q_fp);
 
 }  // namespace sage

@@ -57,56 +57,39 @@ sage_status_t scratch_address(void **out) {
 
 SAGE_API size_t sage_attn_decode_noalloc_max_bytes(void) { return kNoallocScratchBytes; }
 
+// Bytes of built-in scratch a call with S segments uses: the fp32 partial
+// outputs [B*Hq, S, D] (256-byte aligned end) and partial LSEs [B*Hq, S].
+static size_t scratch_bytes(const sage_decode_args_t *a, int S) {
+    if (S <= 1) return 0;
+    const size_t rows = (size_t)a->B * a->Hq * S;
+    return ((rows * a->D * sizeof(float) + 255) & ~(size_t)255) + rows * sizeof(float);
+}
+
 SAGE_API sage_status_t sage_attn_decode_paged_noalloc(const sage_decode_args_t *a, void *stream) {
     using sage::report_error;
-    if (!a) return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG, "args is NULL");
-    if (a->D != 64 && a->D != 128 && a->D != 256)
-        return (sage_status_t)report_error(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}",
-                                           a->D);
-    if (a->out_dtype != SAGE_F16 && a->out_dtype != SAGE_BF16)
-        return (sage_status_t)report_error(SAGE_ERR_UNSUPPORTED, "out dtype must be f16 or bf16");
-    if (a->B < 0 || a->Hq < 1 || a->Hkv < 1 || a->Hq % a->Hkv)
-        return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG,
-                                           "need Hq a positive multiple of Hkv (Hq=%d Hkv=%d)",
-                                           a->Hq, a->Hkv);
-    if (a->max_context_len < 0 || a->max_blocks < 0 ||
-        (int64_t)a->max_context_len > 16ll * a->max_blocks)
-        return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG,
-                                           "max_context_len %d exceeds 16 * max_blocks (%d)",
-                                           a->max_context_len, a->max_blocks);
-    if (a->num_segments < 0 || a->num_segments > 1024)
-        return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG, "num_segments outside [0, 1024]");
-    if (a->B == 0) return SAGE_OK;
-    if (!a->q || !a->q_scale || !a->context_lens || !a->out)
-        return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG,
-                                           "q, q_scale, context_lens and out are required");
-    if (a->max_context_len > 0) {
-        if (!a->k_cache || !a->v_cache || !a->k_scale || !a->v_scale || !a->block_table)
-            return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG,
-                                               "cache, scales and block_table are required");
-        if (a->num_blocks < 1)
-            return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG, "num_blocks must be >= 1");
-        if ((reinterpret_cast<uintptr_t>(a->k_cache) | reinterpret_cast<uintptr_t>(a->v_cache) |
-             reinterpret_cast<uintptr_t>(a->k_scale) | reinterpret_cast<uintptr_t>(a->v_scale)) & 15)
-            return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG,
-                                               "caches and scales must be 16-byte aligned");
-    }
-    if (reinterpret_cast<uintptr_t>(a->q) & 3)
-        return (sage_status_t)report_error(SAGE_ERR_INVALID_ARG, "q must be 4-byte aligned");
+    sage::record_launch(sage::LaunchLog());  // nothing launched by this call yet
+    // the same checks as the workspace entry point (shapes, alignment, and
+    // q / q_scale / block_table / context_lens / out / lse reachable by the GPU)
+    const sage_status_t chk = (sage_status_t)sage::check_decode_args(a, nullptr);
+    if (chk != SAGE_OK || a->B == 0) return chk;
 
-    int S = a->num_segments ? a->num_segments
-                            : sage_decode_num_segments(a->B, a->Hq, a->Hkv, a->D,
-                                                       a->max_context_len);
     const int pages = (a->max_context_len + 15) / 16;
-    {   // a segment is at most decode_max_segment_pages() pages long
-        const int cap = sage::decode_max_segment_pages();
-        if ((int64_t)S * cap < pages) S = (pages + cap - 1) / cap;
+    const int cap = sage::decode_max_segment_pages();
+    const int s_min = pages > cap ? (pages + cap - 1) / cap : 1;  // segments of <= cap pages
+    int S = a->num_segments;
+    if (S == 0) {
+        // the library's choice for these buffers, lowered to the largest
+        // count whose partials fit the scratch (never below s_min)
+        S = sage_decode_auto_segments(a, nullptr);
+        while (S > s_min && scratch_bytes(a, S) > kNoallocScratchBytes) --S;
     }
+    if (S < s_min) S = s_min;
     const int pps = pages > 0 ? (pages + S - 1) / S : 1;
     S = pages > 0 ? (pages + pps - 1) / pps : 1;
-    const size_t rows = (size_t)a->B * a->Hq * S;
-    const size_t o_bytes = (rows * a->D * sizeof(float) + 255) & ~(size_t)255;
-    const size_t need = S > 1 ? o_bytes + rows * sizeof(float) : 0;
+    const size_t need = scratch_bytes(a, S);
+    const size_t o_bytes = S > 1 ? ((size_t)a->B * a->Hq * S * a->D * sizeof(float) + 255) &
+                                       ~(size_t)255
+                                 : 0;
     if (need > kNoallocScratchBytes)
         return (sage_status_t)report_error(
             SAGE_ERR_INVALID_ARG,

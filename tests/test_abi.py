@@ -136,3 +136,21 @@ def test_varlen_rejects_bad_arguments_on_host(lib):
     need = lib.sage_attn_prefill_varlen_workspace_size(ctypes.byref(a))
     rows = 100 + 2 * (128 + 4)
     assert need >= 2 * (2 * rows * 128 * 2) + 2 * rows * 4
+
+
+@pytest.mark.parametrize("entry", ["sage_attn_decode_paged", "sage_attn_decode_paged_noalloc"])
+def test_decode_rejects_unaligned_out_before_any_launch(lib, entry):
+    """An output two bytes off an 8-byte boundary (the single-segment decode
+    writes it 8 bytes at a time) is refused by the host checks, which run
+    before any CUDA call: the fake pointers here are never dereferenced."""
+    a = binding.DecodeArgs()
+    a.B, a.Hq, a.Hkv, a.D = 1, 4, 4, 128
+    a.max_context_len, a.max_blocks, a.num_blocks = 0, 1, 1
+    a.q, a.q_scale = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20000)
+    a.context_lens = ctypes.c_void_p(0x30000)
+    a.out, a.out_dtype = ctypes.c_void_p(0x40002), binding.SAGE_BF16
+    fn = getattr(lib, entry)
+    st = fn(ctypes.byref(a), None, 0, None) if entry == "sage_attn_decode_paged" else \
+        fn(ctypes.byref(a), None)
+    assert st == binding.SAGE_ERR_INVALID_ARG
+    assert b"out must be 8-byte aligned" in lib.sage_get_last_error_message()

@@ -29,7 +29,12 @@ def _query(sage, B, Hq, D, seed):
     return qi[:, :, 0].contiguous(), qs[:, :, 0].contiguous()
 
 
-def test_noalloc_decode_matches_workspace_decode_twice(sage):
+@pytest.mark.parametrize("segments", [0, 5])
+def test_noalloc_decode_matches_workspace_decode_twice(sage, segments):
+    """segments 0: the library's choice (more than 8 here, partials + combine
+    on both paths); 5: the workspace entry point merges the 5 segments inside
+    a thread-block cluster, this one through its scratch and the combine
+    kernel, so the two merge paths are compared."""
     L = sage.lib()
     B, Hq, Hkv, D = 4, 24, 4, 256
     lens = [8192, 5000, 333, 4096]
@@ -39,10 +44,13 @@ def test_noalloc_decode_matches_workspace_decode_twice(sage):
         qi, qs = _query(sage, B, Hq, D, seed)
         ref, lref = sage.sage_attn_decode_paged(qi, qs, c.k_cache, c.v_cache, c.k_scale,
                                                 c.v_scale, c.block_table, c.lens, max(lens),
-                                                out_dtype=torch.float16, return_lse=True)
+                                                out_dtype=torch.float16, return_lse=True,
+                                                num_segments=segments)
+        if segments:
+            assert sage.last_launch_info()["launches"] == 1      # in-cluster combine
         out = torch.empty((B, Hq, D), dtype=torch.float16, device="cuda")
         lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
-        a = _args(sage, qi, qs, c, max(lens), out, lse)
+        a = _args(sage, qi, qs, c, max(lens), out, lse, segments=segments)
         assert L.sage_attn_decode_paged_noalloc(ctypes.byref(a), stream) == 0, \
             L.sage_get_last_error_message()
         torch.cuda.synchronize()
@@ -66,3 +74,20 @@ def test_noalloc_rejects_requests_beyond_its_scratch(sage):
     st = L.sage_attn_decode_paged_noalloc(ctypes.byref(a), None)
     assert st == sage.SAGE_ERR_INVALID_ARG
     assert b"scratch" in L.sage_get_last_error_message()
+
+
+def test_noalloc_rejects_pageable_output_before_launch(sage):
+    """An output in ordinary (pageable) host memory is not memory the GPU
+    can write: the call refuses it, as the workspace entry point does,
+    instead of launching a kernel that would fault."""
+    L = sage.lib()
+    B, Hq, Hkv, D = 2, 8, 2, 128
+    c = W.paged_cache(B, Hkv, D, [64, 64], seed=7, device="cuda")
+    qi, qs = _query(sage, B, Hq, D, 8)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16)        # pageable, not pinned
+    a = _args(sage, qi, qs, c, 64, torch.empty(1, dtype=torch.bfloat16, device="cuda"), None)
+    a.out = ctypes.c_void_p(out.data_ptr())
+    st = L.sage_attn_decode_paged_noalloc(ctypes.byref(a), None)
+    assert st == sage.SAGE_ERR_INVALID_ARG
+    assert b"out" in L.sage_get_last_error_message()
+    assert sage.last_launch_info()["launches"] == 0
