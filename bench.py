@@ -249,9 +249,6 @@ def run_ours(args):
         bt_host = cache.block_table.cpu().pin_memory()
         lens_host = cache.lens.cpu().pin_memory()
         out_host = torch.empty((B, Hq, D), dtype=torch.bfloat16).pin_memory()
-        ws_buf = torch.empty(sage.decode_workspace_size(B, Hq, D, S), dtype=torch.uint8,
-                             device="cuda")
-
         # segment count: the library's own choice for host-resident I/O
         S_e2e = args.segments
         ws_buf = torch.empty(max(1, sage.decode_workspace_size(B, Hq, D, 64)), dtype=torch.uint8,

@@ -155,14 +155,29 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
         for (int k = 0; k < kQPieces; ++k)
             qraw[k] = ld ? *reinterpret_cast<const uint2 *>(src + 4 * k) : make_uint2(0u, 0u);
     }
+    // Segment seg covers pages [seg * P / S, (seg + 1) * P / S) of the
+    // longest context (P pages): the segments differ by one page at most.
+    const int pg0 = (int)((int64_t)seg * p.max_pages / p.num_segments);
+    const int pg1 = (int)((int64_t)(seg + 1) * p.max_pages / p.num_segments);
+    // The segment's block-table entries are loaded together with the context
+    // length (one DRAM round trip for both, not two in a row); pg1 <=
+    // max_pages <= max_blocks keeps them inside the table row, and entries
+    // past the context are never used.
+    constexpr int kBtRegs = 2;
+    const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks + pg0;
+    int btr[kBtRegs];
+#pragma unroll
+    for (int k = 0; k < kBtRegs; ++k) {
+        const int i = threadIdx.x + k * kThreads;
+        btr[k] = i < pg1 - pg0 ? bt[i] : 0;
+    }
     int ctx = p.context_lens[b];
     if (ctx < 0 || ctx > p.max_ctx) {  // never read past the table row
         if (threadIdx.x == 0) atomicOr(p.err, kErrBadBlock);
         ctx = ctx < 0 ? 0 : p.max_ctx;
     }
     const int npages = (ctx + 15) >> 4;
-    const int pg0 = seg * p.pages_per_seg;
-    int np = max(0, min(pg0 + p.pages_per_seg, npages) - pg0);
+    int np = max(0, min(pg1, npages) - pg0);
     if (np > kMaxSegPages) {  // the host never asks for longer segments
         if (threadIdx.x == 0) atomicOr(p.err, kErrBadBlock);
         np = kMaxSegPages;
@@ -175,10 +190,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
         }
         fence_barrier_init();
     }
-    {
-        const int32_t *bt = p.block_table + (int64_t)b * p.max_blocks + pg0;
-        for (int i = threadIdx.x; i < np; i += kThreads) bt_s[i] = bt[i];
+#pragma unroll
+    for (int k = 0; k < kBtRegs; ++k) {
+        const int i = threadIdx.x + k * kThreads;
+        if (i < np) bt_s[i] = btr[k];
     }
+    for (int i = threadIdx.x + kBtRegs * kThreads; i < np; i += kThreads) bt_s[i] = bt[i];
     __syncthreads();
 
     // online-softmax state of a consumer thread: columns (heads) 2*q4, 2*q4+1

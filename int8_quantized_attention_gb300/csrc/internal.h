@@ -107,6 +107,8 @@ struct DecodeParams {
     int B, Hq, Hkv, D, group, head_tiles;
     int num_blocks, max_blocks;
     int num_segments, pages_per_seg;
+    int max_pages;            // ceil(max_ctx / 16): segment s covers pages
+                              // [s * max_pages / S, (s + 1) * max_pages / S)
     int max_ctx;              // host bound on context_lens (<= 16 * max_blocks)
     float qk_scale_log2;      // sm_scale * log2(e)
     float *o_part;            // [B*Hq, S, D] when num_segments > 1

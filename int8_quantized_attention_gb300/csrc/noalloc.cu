@@ -113,6 +113,7 @@ SAGE_API sage_status_t sage_attn_decode_paged_noalloc(const sage_decode_args_t *
     p.head_tiles = (p.group + 7) / 8;
     p.num_blocks = a->num_blocks, p.max_blocks = a->max_blocks;
     p.num_segments = S, p.pages_per_seg = pps;
+    p.max_pages = pages;
     p.max_ctx = a->max_context_len;
     const float sm = a->sm_scale > 0.0f ? a->sm_scale : 1.0f / sqrtf((float)a->D);
     p.qk_scale_log2 = sm * 1.4426950408889634f;

@@ -225,10 +225,12 @@ def test_decode_partials_then_combine(sage):
     # fp32 rounding order, i.e. within an ulp of the f16 output
     assert_close(f32(out), f32(full), "combine vs fused", rel=1e-3, abs_=1e-3)
     assert_close(np_(lse), np_(lfull), "lse combine vs fused", rel=1e-6, abs_=1e-5)
-    # each segment partial is itself the attention over its own key range
-    pps = ((max(lens) + 15) // 16 + 4) // 5 * 16
+    # each segment partial is itself the attention over its own key range:
+    # segment s covers pages [s * P / S, (s + 1) * P / S) of the longest
+    # context (P pages), so the segments differ by one page at most
+    P = (max(lens) + 15) // 16
     seg = 1
-    lo, hi = seg * pps, min((seg + 1) * pps, lens[1])
+    lo, hi = seg * P // 5 * 16, min((seg + 1) * P // 5 * 16, lens[1])
     keys = oracle.gather_paged(np_(c.k_cache), np_(c.block_table)[1], lens[1], 0)[lo:hi]
     ks = oracle.gather_paged_scale(np_(c.k_scale), np_(c.block_table)[1], lens[1], 0)[lo:hi]
     vals = oracle.gather_paged(np_(c.v_cache), np_(c.block_table)[1], lens[1], 0)[lo:hi]
@@ -364,3 +366,24 @@ def test_decode_host_query_quantised_once(sage):
     assert info["kernel"] == "decode_kernel" and info["launches"] == 3
     assert sage.check_device_status()[0] == 0
     assert torch.equal(got, ref) and torch.equal(lse, ref_lse)
+
+
+def test_decode_permuted_pages_bitwise_partials_path(sage):
+    """Past one cluster (14 segments: partials in the workspace, then the
+    combine kernel) the same logical cache on permuted physical pages still
+    gives the same bits, with contexts of different lengths."""
+    B, Hq, Hkv, D = 4, 24, 4, 256
+    lens = [8192, 8000, 5000, 8192]
+    c = W.paged_cache(B, Hkv, D, lens, seed=61, device="cuda")
+    qi, qs = _quant_query(sage, B, Hq, D, seed=62)
+    out1 = _run(sage, qi, qs, c, max(lens), num_segments=14)
+    assert sage.last_launch_info()["launches"] == 2
+    nblk = c.k_cache.shape[0]
+    perm = torch.randperm(nblk, generator=torch.Generator().manual_seed(5)).to("cuda")
+    inv = torch.empty_like(perm)
+    inv[perm] = torch.arange(nblk, device="cuda")
+    c2 = W.PagedCache(c.k_cache[inv], c.v_cache[inv], c.k_scale[inv], c.v_scale[inv],
+                      perm[c.block_table.long()].to(torch.int32), c.lens)
+    out2 = _run(sage, qi, qs, c2, max(lens), num_segments=14)
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out2)

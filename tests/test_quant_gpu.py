@@ -223,7 +223,7 @@ def test_quant_bf16_subnormal_scales_decode_query(sage):
     assert sage.check_device_status()[0] == 0
     up = lambda n: (n + 255) // 256 * 256
     rows = B * Hq * S
-    qc_off = up(rows * D * 4) + up(rows * 4)
+    qc_off = up(rows * D * 4) + up(rows * 4)                     # after partials and LSEs
     qs_off = qc_off + up(B * Hq * D)
     w = np_(ws)
     codes = w[qc_off:qc_off + B * Hq * D].view(np.int8).reshape(B, Hq, D)
