@@ -6,15 +6,18 @@ INT8 paged context): quantise the bf16 query (INT8, per token/head), run
 the split-K paged decode kernel, merge the segments with the LSE combine.
 
 Prints ONE JSON line (rank 0).  `value` is the decode workload's
-algorithmic bytes (INT8 K/V pages + their scales + block table + query
-codes/scales + bf16 query in + bf16 output) per second of device time,
-inputs resident in HBM, L2 flushed between steps.  `e2e` is the same
-metric through the public API with the per-step inputs (query, block
-table, context lengths) copied from pinned host memory and the output
-copied back inside the timed region; the KV cache is device-resident state,
-as in serving.  `roofline` describes the decode kernel.  A dense-prefill
-and chunked-prefill measurement is added under `prefill` when that kernel
-is available.
+algorithmic bytes (INT8 K/V pages + their scales + block table + context
+lengths + bf16 query in + bf16 output) per second of device time, inputs
+resident in HBM, L2 flushed between steps.  `e2e` is the same metric
+through the public API with the per-step inputs (query, block table,
+context lengths) and the output in pinned host memory: the kernels read
+and write them in place across NVLink-C2C inside every timed step (no
+copy-engine transfer); the KV cache is device-resident state, as in
+serving.  `roofline` describes the decode kernel launched on its own
+(events around that one launch).  The dense and chunked prefill workloads
+are measured under `prefill`, each with its own `roofline` (the prefill
+kernel against the tensor peak) and `cpu_baseline` (the oracle on a row
+sample, scaled by work).
 
 --impl reference times the CPU oracle (the plain C reference of the
 method) on the host cores on a bounded sample of the same workload.
@@ -138,14 +141,17 @@ class ClockSampler:
 
 
 def decode_bytes(B, Hq, Hkv, D, ctx, max_blocks):
-    """Algorithmic bytes of one decode step (what the method must move)."""
+    """Algorithmic bytes of one decode step (what the method must move) and
+    of the decode kernel launched alone in the partials form (INT8 query
+    codes and scales in; the split-K partials it writes are not algorithmic
+    bytes)."""
     kv = 2 * B * ctx * Hkv * D            # INT8 K and V pages
     scales = 2 * B * ctx * Hkv * 4        # fp32 per-token K and V scales
     table = B * max_blocks * 4 + B * 4    # block table + context lengths
     q_bf16 = B * Hq * D * 2               # query in (quantised inside the decode kernel)
     out = B * Hq * D * 2                  # bf16 output
-    kernel = kv + scales + table + q_bf16 + out
-    step = kernel                         # the step is that one kernel
+    step = kv + scales + table + q_bf16 + out
+    kernel = kv + scales + table + B * Hq * (D + 4)
     return kernel, step
 
 
@@ -226,10 +232,18 @@ def run_ours(args):
         graph.replay()
         ends[i].record(stream)
     barrier()
-    # the decode kernel alone (events around its launch, same flushed state)
+    # The decode kernel on its own: the partials form launches the same
+    # decode_kernel<256> grid (same segments, same pages) without the
+    # combine behind it, with the query codes quantised beforehand; events
+    # bracket that one launch, L2 flushed before each.
+    qi, qs, _, _ = sage.sage_quant_int8(q[:, :, None, :])
+    qi, qs = qi[:, :, 0].contiguous(), qs[:, :, 0].contiguous()
     for i in range(args.steps):
         l2_flush(flush)
-        step(kev[i])
+        kev[i][0].record(stream)
+        sage.sage_attn_decode_paged_partials(qi, qs, cache.k_cache, cache.v_cache, cache.k_scale,
+                                             cache.v_scale, cache.block_table, cache.lens, ctx, S)
+        kev[i][1].record(stream)
     torch.cuda.synchronize()
     clk.__exit__(None, None, None)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
@@ -292,7 +306,10 @@ def run_ours(args):
     roof = {"bound": "hbm", "kernel": "decode_kernel", "achieved": round(achieved, 1),
             "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
             "peak_kind": kind, "traffic": _profile_traffic("decode_kernel"),
-            "algorithmic_bytes": kbytes, "avg_launch_ms": round(k_avg, 5)}
+            "algorithmic_bytes": kbytes, "avg_launch_ms": round(k_avg, 5),
+            "launch": "decode_kernel alone (partials form: %d segments, no combine), CUDA events "
+                      "around the launch, L2 flushed before each" % S,
+            "step_frac": round(value / peaks["hbm_gbs"], 4)}
     if rank != 0:
         if ws > 1:
             import torch.distributed as dist
@@ -374,28 +391,60 @@ def prefill_flops(B, Hq, Sq, prefix, Sk, D, causal):
     return 4 * D * B * Hq * pairs
 
 
+def _oracle_prefill_sample(name, qi, qs, ki, ks, v, bias, prefix_cache, plen, P, threads):
+    """The oracle on one (batch, head) and 16 evenly spaced query rows of a
+    prefill workload; returns (seconds, FLOP of that sample)."""
+    import numpy as np
+
+    import oracle
+
+    Sq, D = P["S"], P["D"]
+    rows = np.arange(Sq) if Sq <= 128 else np.linspace(0, Sq - 1, 16).astype(np.int64)
+    sub = lambda t: t[0:1, 0:1].cpu().numpy()
+    pre = None
+    if prefix_cache is not None:
+        c = prefix_cache
+        pre = dict(k_cache=c.k_cache.cpu().numpy(), v_cache=c.v_cache.cpu().numpy(),
+                   k_scale=c.k_scale.cpu().numpy(), v_scale=c.v_scale.cpu().numpy(),
+                   block_table=c.block_table.cpu().numpy(), lens=c.lens.cpu().numpy())
+    t0 = time.perf_counter()
+    oracle.prefill(sub(qi), sub(qs), P["q_block"], sub(ki), sub(ks), P["k_block"],
+                   sub(v.float()), causal=P["causal"],
+                   q_bias=None if bias is None else sub(bias).astype(np.float64), prefix=pre,
+                   rows=rows, threads=threads)
+    el = time.perf_counter() - t0
+    vis = lambda i: min(plen + Sq, int(i) + plen + 1) if P["causal"] else plen + Sq
+    return el, 4 * D * sum(vis(i) for i in rows)
+
+
 def prefill_measure(args):
-    """Prefill kernel throughput on the dense and chunked prefill workloads."""
+    """Prefill throughput on the dense and chunked prefill workloads: the
+    prefill call (staging pass + prefill_kernel) timed with CUDA events, its
+    roofline against the measured dense tensor peak, the call with the Q/K
+    quantisation in front of it, and the oracle on a row sample as the CPU
+    baseline (scaled by FLOP, marked extrapolated)."""
     import torch
 
+    import oracle
     from int8_quantized_attention_gb300 import binding as sage
     from int8_quantized_attention_gb300 import workloads as W
 
     peaks, kind = _peaks()
     peak = peaks["bf16_tflops"]   # f16 dense tensor rate = bf16 rate (nominal ratio 1)
     stream = torch.cuda.current_stream()
+    threads = oracle.default_threads()
     res = {}
     for name in ("dense_prefill", "chunked_prefill"):
         P = W.WORKLOADS[name].params
         qkv = W.dense_qkv(P["B"], P["Hq"], P["Hkv"], P["S"], P["S"], P["D"], seed=P["seed"],
                           dtype=P["dtype"], device="cuda", k_offset_std=P["k_offset_std"])
-        prefix, plen = None, 0
+        prefix, plen, pc = None, 0, None
         if name == "chunked_prefill":
-            c = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["prefix"]], seed=P["seed"],
-                              device="cuda")
+            pc = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["prefix"]], seed=P["seed"],
+                               device="cuda")
             plen = P["prefix"]
-            prefix = dict(k_cache=c.k_cache, v_cache=c.v_cache, k_scale=c.k_scale,
-                          v_scale=c.v_scale, block_table=c.block_table, lens=c.lens,
+            prefix = dict(k_cache=pc.k_cache, v_cache=pc.v_cache, k_scale=pc.k_scale,
+                          v_scale=pc.v_scale, block_table=pc.block_table, lens=pc.lens,
                           max_len=plen)
         qb, kb = P["q_block"], P["k_block"]
 
@@ -423,6 +472,7 @@ def prefill_measure(args):
             b.record(stream)
         torch.cuda.synchronize()
         k_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        launches = sage.last_launch_info()["launches"]
         sv = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(n)]
         for a, b in sv:
@@ -437,13 +487,28 @@ def prefill_measure(args):
             raise RuntimeError("device error word %d in %s" % (word, name))
         fl = prefill_flops(P["B"], P["Hq"], P["S"], plen, P["S"], P["D"], P["causal"])
         tf = fl / (k_ms * 1e-3) / 1e12
-        res[name] = {"kernel": "prefill_kernel", "tflops": round(tf, 1),
-                     "frac_of_dense_f16_peak": round(tf / peak, 4), "peak_tflops": peak,
-                     "peak_kind": kind, "kernel_ms": round(k_ms, 4),
-                     "step_ms_with_quant": round(s_ms, 4),
-                     "step_tflops_with_quant": round(fl / (s_ms * 1e-3) / 1e12, 1),
-                     "flop": fl, "launches": n}
-        del qkv, qi, qs, ki, ks, bias, prefix
+        cpu = None
+        if args.cpu_baseline:
+            el, fl_s = _oracle_prefill_sample(name, qi, qs, ki, ks, qkv.v, bias, pc, plen, P,
+                                              threads)
+            cpu = {"value": round(fl_s / el / 1e12, 8), "unit": "TFLOP/s", "cores": threads,
+                   "kind": "oracle",
+                   "sample": "1 (batch, head) x 16 evenly spaced query rows (%.2f s, %.3g FLOP); "
+                             "extrapolated: the full workload would take %.0f s" %
+                             (el, fl_s, el * fl / fl_s)}
+        res[name] = {
+            "tflops": round(tf, 1), "kernel_ms": round(k_ms, 4), "launches_per_call": launches,
+            "step_ms_with_quant": round(s_ms, 4),
+            "step_tflops_with_quant": round(fl / (s_ms * 1e-3) / 1e12, 1), "flop": fl,
+            "roofline": {"bound": "tensor", "kernel": "prefill_kernel", "achieved": round(tf, 1),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(tf / peak, 4),
+                         "peak_kind": kind + " bf16 dense (f16 runs at the same nominal rate)",
+                         "traffic": _profile_traffic("prefill_kernel:" + name),
+                         "algorithmic_flop": fl, "avg_launch_ms": round(k_ms, 4),
+                         "launch": "the prefill call (staging pass + prefill_kernel), CUDA "
+                                   "events around it, %d calls" % n},
+            "cpu_baseline": cpu}
+        del qkv, qi, qs, ki, ks, bias, prefix, pc
         torch.cuda.empty_cache()
     return res
 
@@ -654,8 +719,8 @@ def run_configs(args):
                                                      cache.block_table, cache.lens, ctx,
                                                      num_segments=S, workspace=ws)
         ms = gpu_ms(fn)
-        kbytes, _ = decode_bytes(B, Hq, Hkv, D, ctx, cache.block_table.shape[1])
-        gbs = kbytes / (ms * 1e-3) / 1e9
+        _, sbytes = decode_bytes(B, Hq, Hkv, D, ctx, cache.block_table.shape[1])
+        gbs = sbytes / (ms * 1e-3) / 1e9
         # oracle: one (sequence, kv head) pair, scaled by the pair count
         cc = [cache.k_cache.cpu().numpy(), cache.v_cache.cpu().numpy(), cache.k_scale.cpu().numpy(),
               cache.v_scale.cpu().numpy(), cache.block_table.cpu().numpy(), cache.lens.cpu().numpy()]
@@ -669,6 +734,38 @@ def run_configs(args):
               "oracle_s": round(t_or, 3), "oracle_cores": threads,
               "oracle_sample": "1 of %d (sequence, kv head) pairs, scaled" % (B * Hkv)})
         del cache
+
+    _configs_kv_append(emit, gpu_ms, peaks)
+
+
+def _configs_kv_append(emit, gpu_ms, peaks):
+    """The KV producer (sage_kv_cache_append): a decode step's new token for
+    every sequence of the paged-decode workload, and a 2048-token chunk of
+    the chunked-prefill workload, quantised and scattered into the cache."""
+    import torch
+
+    from int8_quantized_attention_gb300 import binding as sage
+    from int8_quantized_attention_gb300 import workloads as W
+
+    P = W.WORKLOADS["paged_decode"].params
+    for label, B, n, ctx in (("decode step", P["B"], 1, P["ctx"]), ("prefill chunk", 1, 2048, 16384)):
+        Hkv, D = P["Hkv"], P["D"]
+        c = W.paged_cache(B, Hkv, D, [ctx + n] * B, seed=9, device="cuda")
+        g = torch.Generator("cuda").manual_seed(10)
+        k = torch.randn((B, Hkv, n, D), generator=g, device="cuda").to(torch.bfloat16)
+        v = torch.randn((B, Hkv, n, D), generator=g, device="cuda").to(torch.bfloat16)
+        pos = torch.full((B,), ctx, dtype=torch.int32, device="cuda")
+        fn = lambda: sage.sage_kv_cache_append(k, v, c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                               c.block_table, pos)
+        ms = gpu_ms(fn)
+        rows = 2 * B * Hkv * n
+        nbytes = rows * (2 * D + D + 4) + B * (c.block_table.shape[1] + 1) * 4
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        emit({"config": "kv_append", "case": label, "B": B, "new_tokens": n, "Hkv": Hkv, "D": D,
+              "gpu_ms": round(ms, 4), "GBps": round(gbs, 1),
+              "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
+              "bytes": nbytes})
+        del c
 
 
 def run_reference(args):
