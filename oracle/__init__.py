@@ -45,6 +45,9 @@ def _lib():
         lib.oracle_attend.argtypes = [_i64, ctypes.c_int, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp,
                                       _vp, ctypes.c_int, _i64, ctypes.c_double, _vp, _vp]
         lib.oracle_attend.restype = _i64
+        lib.oracle_attend_pv_int8.argtypes = [_i64, ctypes.c_int, _vp, _vp, _i64, _vp, _vp, _vp,
+                                              _vp, ctypes.c_int, ctypes.c_double, _vp, _vp]
+        lib.oracle_attend_pv_int8.restype = _i64
         lib.oracle_splitk_combine.argtypes = [_vp, _vp, _i64, _i64, ctypes.c_int, _vp, _vp]
         lib.oracle_splitk_combine.restype = None
         lib.oracle_kv_append.argtypes = [_vp, _i64, _i64, _i64, ctypes.c_int, _vp, _i64, _vp, _i64,
@@ -196,6 +199,28 @@ def attend(q, sq, k, sk, v, *, sm_scale, causal=False, causal_offset=0, qpos=Non
     return o, lse
 
 
+def attend_pv_int8(q, sq, k, sk, v, sv, *, sm_scale, block=PAGE):
+    """One query-row batch against one key set with INT8 P.V ([P1] sections
+    6 and 8): v int8 [nk, D] codes and sv fp32 [nk] their per-token scales;
+    the V-scaled probabilities are quantised per group of `block` keys.
+    Returns (o fp64, lse fp64)."""
+    q = _c(q, np.int8)
+    sq = _c(sq, np.float32)
+    k = _c(k, np.int8)
+    sk = _c(sk, np.float32)
+    v = _c(v, np.int8)
+    sv = _c(sv, np.float32)
+    nq, D = q.shape
+    nk = k.shape[0]
+    o = np.empty((nq, D), np.float64)
+    lse = np.empty((nq,), np.float64)
+    bad = _lib().oracle_attend_pv_int8(nq, D, _p(q), _p(sq), nk, _p(k), _p(sk), _p(v), _p(sv),
+                                       int(block), float(sm_scale), _p(o), _p(lse))
+    if bad:
+        raise ValueError("raw score outside the INT32 bound D*127^2")
+    return o, lse
+
+
 def _run(jobs, threads):
     threads = threads or default_threads()
     if threads <= 1 or len(jobs) <= 1:
@@ -280,13 +305,14 @@ def prefill(q_i8, q_scale, q_block, k_i8, k_scale, k_block, v, *, causal, sm_sca
 
 
 def decode_paged(q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
-                 context_lens, *, sm_scale=None, threads=None, pairs=None):
+                 context_lens, *, sm_scale=None, threads=None, pairs=None, pv_int8=False):
     """Single-token decode over a paged INT8 K/V cache ([P1] sections 3-5).
 
     q_i8 [B,Hq,D] int8, q_scale [B,Hq] fp32; caches [nblk,Hkv,D/16,16,16]
     int8; scales [nblk,Hkv,16] fp32; block_table [B,maxblk] int32;
     context_lens [B].  Query head h reads kv head h // (Hq/Hkv).
     pairs: optional list of (b, kv_head) to evaluate (others stay zero).
+    pv_int8: INT8 P.V (attend_pv_int8), quantisation groups = cache pages.
     Returns (o fp64 [B,Hq,D], lse fp64 [B,Hq]).
     """
     q_i8 = np.asarray(q_i8)
@@ -306,11 +332,16 @@ def decode_paged(q_i8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
             bt = block_table[b]
             keys = gather_paged(k_cache, bt, n, g)
             sk = gather_paged_scale(k_scale, bt, n, g)
-            vals = gather_paged(v_cache, bt, n, g).astype(np.float64)
-            vals *= gather_paged_scale(v_scale, bt, n, g).astype(np.float64)[:, None]
             hs = slice(g * group, (g + 1) * group)
-            ob, lb = attend(q_i8[b, hs], np.asarray(q_scale)[b, hs], keys, sk, vals,
-                            sm_scale=sm_scale)
+            if pv_int8:
+                ob, lb = attend_pv_int8(q_i8[b, hs], np.asarray(q_scale)[b, hs], keys, sk,
+                                        gather_paged(v_cache, bt, n, g),
+                                        gather_paged_scale(v_scale, bt, n, g), sm_scale=sm_scale)
+            else:
+                vals = gather_paged(v_cache, bt, n, g).astype(np.float64)
+                vals *= gather_paged_scale(v_scale, bt, n, g).astype(np.float64)[:, None]
+                ob, lb = attend(q_i8[b, hs], np.asarray(q_scale)[b, hs], keys, sk, vals,
+                                sm_scale=sm_scale)
             o[b, hs] = ob
             lse[b, hs] = lb
         jobs.append(job)

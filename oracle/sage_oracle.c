@@ -210,6 +210,76 @@ int64_t oracle_attend(int64_t nq, int D, const int8_t *q, const float *sq,
 }
 
 /*
+ * Attention with INT8 P.V (decode over INT8 values; [P1] sections 6 and 8
+ * name INT8 P.V with "V scale fusion" and "probability quantization").
+ * The V scale is folded into the probabilities, the product is quantised
+ * symmetrically per group of `block` consecutive keys (one 16-token cache
+ * page; the last group may be short), and the INT8 codes multiply the INT8
+ * values exactly:
+ *   z_j  = sm_scale * acc_j * sq_i * sk_j,  M = max_j z_j
+ *   p_j  = exp(z_j - M),  l = sum_j p_j   (unquantised: the denominator)
+ *   w_j  = p_j * sv_j
+ *   s_g  = max_{j in g} w_j / 127,  code_j = rne(w_j / s_g)  (0 if s_g = 0)
+ *   o    = (sum_g s_g * sum_{j in g} code_j * v_j) / l,  lse = M + ln l
+ * Readings (the algorithm's own text is not on the pages): one scale per
+ * (query row, key group) -- a common factor of a group's w cancels in its
+ * codes, so the codes do not depend on which row maximum the softmax uses --
+ * codes in [0, 127] (w >= 0), ties to even as for Q and K.  The code
+ * decision is taken here in fp64 from the exact probabilities.
+ * v: int8 [nk][D] codes, sv: fp32 [nk] per-token scales.
+ */
+int64_t oracle_attend_pv_int8(int64_t nq, int D, const int8_t *q, const float *sq, int64_t nk,
+                              const int8_t *k, const float *sk, const int8_t *v, const float *sv,
+                              int block, double sm_scale, double *o, double *lse)
+{
+    int64_t bound = (int64_t)D * 127 * 127, bad = 0;
+    double *z = (double *)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    double *w = (double *)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    for (int64_t i = 0; i < nq; ++i) {
+        double *oi = o + i * D;
+        for (int c = 0; c < D; ++c) oi[c] = 0.0;
+        if (nk == 0) {
+            lse[i] = -INFINITY;
+            continue;
+        }
+        double m = -INFINITY;
+        for (int64_t j = 0; j < nk; ++j) {
+            int64_t a = 0;
+            for (int c = 0; c < D; ++c)
+                a += (int64_t)q[i * D + c] * (int64_t)k[j * D + c];
+            if (a > bound || a < -bound) ++bad;
+            z[j] = sm_scale * ((double)a * (double)sq[i] * (double)sk[j]);
+            if (z[j] > m) m = z[j];
+        }
+        double l = 0.0;
+        for (int64_t j = 0; j < nk; ++j) {
+            double p = exp(z[j] - m);
+            l += p;
+            w[j] = p * (double)sv[j];
+        }
+        for (int64_t g0 = 0; g0 < nk; g0 += block) {
+            int64_t g1 = g0 + block < nk ? g0 + block : nk;
+            double wmax = 0.0;
+            for (int64_t j = g0; j < g1; ++j)
+                if (w[j] > wmax) wmax = w[j];
+            if (wmax == 0.0) continue;
+            double s = wmax / 127.0;
+            for (int64_t j = g0; j < g1; ++j) {
+                double code = nearbyint(w[j] / s);   /* ties to even */
+                if (code > 127.0) code = 127.0;
+                const int8_t *vj = v + j * D;
+                for (int c = 0; c < D; ++c) oi[c] += s * code * (double)vj[c];
+            }
+        }
+        for (int c = 0; c < D; ++c) oi[c] /= l;
+        lse[i] = m + log(l);
+    }
+    free(z);
+    free(w);
+    return bad;
+}
+
+/*
  * Split-K combine of segment partials (segments are the split-K pieces
  * of [P1] section 4; the pages return the LSE "for concatenation" in
  * [P3] advanced config).  For each row r with S segments:

@@ -817,3 +817,115 @@ def test_decode_pairs_and_varlen_rows_sample_the_full_result():
         picked[t] = True
         assert np.array_equal(os_[t], of[t]) and np.array_equal(ls_[:, t], lf[:, t])
     assert np.all(np.isnan(os_[~picked])) and np.all(np.isnan(ls_[:, ~picked]))
+
+
+# --------------------------------------------------------------------------
+# INT8 P.V: V-scaled probabilities quantised per 16-key group
+# --------------------------------------------------------------------------
+
+def test_pv_int8_exact_when_codes_are_integers():
+    """K = 0 makes every probability equal (p = 1 before normalising), so a
+    group's w_j = sv_j; with sv_j = k_j 2^-10 (k_j integer) and one k_j = 127
+    in every 16-key group (the last one short), the group scale is 2^-10 and
+    the codes are the k_j themselves: INT8 P.V then equals float64 attention
+    on v_j * sv_j exactly.  Groups not aligned at multiples of 16, a scale
+    taken from p instead of p * sv, or a dropped group scale all fail."""
+    rng = np.random.default_rng(51)
+    nk, D = 45, 32
+    kk = rng.integers(1, 127, nk)
+    for g0 in range(0, nk, 16):
+        kk[g0 + rng.integers(0, min(16, nk - g0))] = 127
+    sv = (kk * 2.0 ** -10).astype(np.float32)
+    v = rng.integers(-127, 128, (nk, D)).astype(np.int8)
+    qi = rng.integers(-127, 128, (3, D)).astype(np.int8)
+    sq = np.full(3, 0.01, np.float32)
+    k = np.zeros((nk, D), np.int8)
+    sk = np.full(nk, 0.02, np.float32)
+    o, lse = oracle.attend_pv_int8(qi, sq, k, sk, v, sv, sm_scale=0.1)
+    vhat = v.astype(np.float64) * sv.astype(np.float64)[:, None]
+    o_ref, lse_ref = textbook_attention(np.zeros((3, D)), np.zeros((nk, D)), vhat, 0.1)
+    np.testing.assert_allclose(o, o_ref, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(lse, lse_ref, rtol=1e-14)
+    # the same values with the group boundaries moved by 8 keys change codes
+    o8, _ = oracle.attend_pv_int8(qi, sq, k, sk, v[8:], sv[8:], sm_scale=0.1)
+    o_ref8, _ = textbook_attention(np.zeros((3, D)), np.zeros((nk - 8, D)), vhat[8:], 0.1)
+    assert np.abs(o8 - o_ref8).max() > 1e-6
+
+
+def test_pv_int8_within_half_a_step_of_exact_attention():
+    """Each code is within half a step of w_j / s_g, so INT8 P.V differs from
+    exact attention (same scores, values v_j sv_j) by at most
+    sum_j s_g(j) |v_j| / 2 / l per channel -- and it does differ."""
+    rng = np.random.default_rng(52)
+    nq, nk, D = 4, 70, 64
+    qi = rng.integers(-127, 128, (nq, D)).astype(np.int8)
+    ki = rng.integers(-127, 128, (nk, D)).astype(np.int8)
+    sq = rng.uniform(0.005, 0.02, nq).astype(np.float32)
+    sk = rng.uniform(0.005, 0.02, nk).astype(np.float32)
+    v = rng.integers(-127, 128, (nk, D)).astype(np.int8)
+    sv = rng.uniform(0.005, 0.02, nk).astype(np.float32)
+    sm = 0.5
+    o, lse = oracle.attend_pv_int8(qi, sq, ki, sk, v, sv, sm_scale=sm)
+    vhat = v.astype(np.float64) * sv.astype(np.float64)[:, None]
+    o_ex, lse_ex = oracle.attend(qi, sq, ki, sk, vhat, sm_scale=sm)
+    np.testing.assert_allclose(lse, lse_ex, rtol=1e-14)
+    z = (qi.astype(np.float64) @ ki.astype(np.float64).T) * sq[:, None] * sk[None, :] * sm
+    p = np.exp(z - z.max(1, keepdims=True))
+    w = p * sv[None, :]
+    bound = np.zeros((nq, D))
+    for g0 in range(0, nk, 16):
+        s = w[:, g0:g0 + 16].max(1) / 127.0
+        bound += (s[:, None, None] * 0.5 * np.abs(v[g0:g0 + 16].astype(np.float64))[None]).sum(1)
+    bound /= p.sum(1)[:, None]
+    err = np.abs(o - o_ex)
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-15)
+    assert err.max() > 0
+
+
+def test_pv_int8_single_dominant_key():
+    """One key whose score dwarfs the rest (their probabilities underflow to
+    0): its group's scale is its own w / 127, its code 127, every other code
+    0, so the output is that key's value times its scale."""
+    D = 16
+    k = np.zeros((20, D), np.int8)
+    k[13] = 127
+    q = np.full((1, D), 127, np.int8)
+    v = np.arange(20 * D).reshape(20, D).astype(np.int64) % 255 - 127
+    v = v.astype(np.int8)
+    sv = np.linspace(0.005, 0.02, 20).astype(np.float32)
+    o, lse = oracle.attend_pv_int8(q, np.ones(1, np.float32), k, np.ones(20, np.float32), v, sv,
+                                   sm_scale=1.0)
+    np.testing.assert_allclose(o[0], v[13].astype(np.float64) * np.float64(sv[13]), rtol=1e-14)
+    assert lse[0] == 16 * 127 * 127
+
+
+def test_pv_int8_group_scales_and_rounding_by_hand():
+    """Equal probabilities (K = 0) and hand-chosen v scales: group g of 16
+    keys has its largest w at exactly 127 * 2^-(10+g), so its scale is
+    2^-(10+g); inside a group w_j / s = x_j with x_j listed below (quarter
+    and half steps), whose codes -- nearest integer, ties to even -- are
+    written out by hand.  The output must equal the mean of code_j * s_g(j)
+    * v_j.  Merged groups (a scale shared across 32 keys), truncation or
+    ties away from zero all change it."""
+    xs = [127.0, 3.25, 3.75, 4.5, 5.5, 0.5, 1.5, 0.25, 126.5, 2.0, 7.75, 10.5, 11.5, 0.0, 64.25,
+          99.5]
+    codes = [127, 3, 4, 4, 6, 0, 2, 0, 126, 2, 8, 10, 12, 0, 64, 100]
+    D, G = 8, 3
+    nk = 16 * G
+    rng = np.random.default_rng(53)
+    sv, code_all, scale_all = [], [], []
+    for g in range(G):
+        perm = rng.permutation(16)
+        for t in perm:
+            sv.append(xs[t] * 2.0 ** -(10 + g))
+            code_all.append(codes[t])
+            scale_all.append(2.0 ** -(10 + g))
+    sv = np.array(sv, np.float32)
+    assert np.array_equal(sv.astype(np.float64), np.array(sv, np.float64))
+    v = rng.integers(-127, 128, (nk, D)).astype(np.int8)
+    o, _ = oracle.attend_pv_int8(np.ones((1, D), np.int8), np.ones(1, np.float32),
+                                 np.zeros((nk, D), np.int8), np.ones(nk, np.float32), v, sv,
+                                 sm_scale=1.0)
+    want = (np.array(code_all, np.float64)[:, None] * np.array(scale_all)[:, None]
+            * v.astype(np.float64)).sum(0) / nk
+    np.testing.assert_allclose(o[0], want, rtol=1e-14, atol=1e-18)
