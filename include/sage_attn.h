@@ -204,7 +204,29 @@ typedef struct sage_decode_args {
     void *out;                  /* [B, Hq, D], 8-byte aligned */
     sage_dtype_t out_dtype;
     float *lse;                 /* optional [B, Hq] natural-log LSE (-inf for empty context) */
+    int pv_mode;                /* SAGE_PV_* below; 0 = SAGE_PV_F32 */
 } sage_decode_args_t;
+
+/* P.V of the decode ([P3] advanced configuration, pv_accum_dtype "fp32" /
+ * "fp16" / "fp16+fp16"; [P1] sections 6 and 8: INT8 P.V with the V scale
+ * fused into P).  The INT8 values of a page enter the product exactly in
+ * every mode; P' = p_j * v_scale_j (p = 2^(t_j - m), m a running row max).
+ *   SAGE_PV_F32      P' rounded to f16, fp32 accumulation (default)
+ *   SAGE_PV_F16      P' rounded to f16, f16 accumulation throughout
+ *   SAGE_PV_F16_F32  each 16-key page's product accumulated in f16, then
+ *                    added into fp32 accumulators (two-level accumulation)
+ *   SAGE_PV_INT8     P' quantised per (query head, 16-key page):
+ *                    s = max_j P' / 127, codes rne(P' / s) in [0, 127]
+ *                    (the rounding of sage_quant_int8); the page adds
+ *                    s * sum_j code_j * v_j, the sum exact, to fp32
+ *                    accumulators; the softmax denominator uses unquantised p.
+ * On this GPU the four run at the same tensor rate; F32 is the most precise. */
+enum {
+    SAGE_PV_F32 = 0,
+    SAGE_PV_F16 = 1,
+    SAGE_PV_F16_F32 = 2,
+    SAGE_PV_INT8 = 3
+};
 
 /* Segment count the library picks for num_segments == 0 (host only).  With
  * U = B * Hkv * ceil(Hq/Hkv/8) (sequence, KV head, 8-head tile) units and

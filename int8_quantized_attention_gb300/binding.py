@@ -44,7 +44,8 @@ class DecodeArgs(ctypes.Structure):
                 ("k_scale", _vp), ("v_scale", _vp), ("block_table", _vp), ("context_lens", _vp),
                 ("B", _i), ("Hq", _i), ("Hkv", _i), ("D", _i), ("num_blocks", _i),
                 ("max_blocks", _i), ("max_context_len", _i), ("sm_scale", _f),
-                ("num_segments", _i), ("out", _vp), ("out_dtype", _i), ("lse", _vp)]
+                ("num_segments", _i), ("out", _vp), ("out_dtype", _i), ("lse", _vp),
+                ("pv_mode", _i)]
 
 
 class PrefillArgs(ctypes.Structure):
@@ -243,8 +244,17 @@ def decode_workspace_size(B: int, Hq: int, D: int, num_segments: int) -> int:
     return int(lib().sage_attn_decode_workspace_size(B, Hq, D, num_segments))
 
 
+PV_MODES = {"fp32": 0, "fp16": 1, "fp16+fp32": 2, "int8": 3}
+
+
+def _pv(pv_mode) -> int:
+    if pv_mode not in PV_MODES:
+        raise ValueError("pv_mode must be one of %s" % sorted(PV_MODES))
+    return PV_MODES[pv_mode]
+
+
 def _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
-                 max_context_len, sm_scale, num_segments, out, lse, shape=None):
+                 max_context_len, sm_scale, num_segments, out, lse, shape=None, pv_mode="fp32"):
     if shape is None:
         _need(q_int8, torch.int8, "q_int8")
         _need(q_scale, torch.float32, "q_scale")
@@ -267,6 +277,7 @@ def _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_tabl
     a.num_segments = int(num_segments)
     a.out, a.out_dtype = _ptr_io(out), _dt(out.dtype)
     a.lse = _ptr_io(lse)
+    a.pv_mode = _pv(pv_mode)
     return a
 
 
@@ -274,15 +285,21 @@ def sage_attn_decode_paged(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, 
                            context_lens, max_context_len: int, *, sm_scale=None,
                            num_segments: int = 0, out_dtype=torch.bfloat16,
                            return_lse: bool = False, workspace: Optional[torch.Tensor] = None,
-                           out: Optional[torch.Tensor] = None, debug_scores=None, stream=None):
-    """Split-K paged INT8 decode + LSE combine.  Returns out [B,Hq,D] (and lse)."""
+                           out: Optional[torch.Tensor] = None, debug_scores=None,
+                           pv_mode: str = "fp32", stream=None):
+    """Split-K paged INT8 decode + LSE combine.  Returns out [B,Hq,D] (and lse).
+
+    pv_mode: "fp32" (default), "fp16", "fp16+fp32" or "int8" -- the P.V
+    operands and accumulation (SAGE_PV_* in the header).
+    """
     B, Hq, D = q_int8.shape
     Hkv = k_cache.shape[1]
     if out is None:
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=k_cache.device)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=k_cache.device) if return_lse else None
     a = _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
-                     context_lens, max_context_len, sm_scale, num_segments, out, lse)
+                     context_lens, max_context_len, sm_scale, num_segments, out, lse,
+                     pv_mode=pv_mode)
     # the library's choice for these buffers (it depends on where they live)
     S = num_segments or int(lib().sage_decode_auto_segments(ctypes.byref(a), None))
     a.num_segments = S
@@ -304,7 +321,8 @@ def sage_attn_decode_paged_q16(q, k_cache, v_cache, k_scale, v_scale, block_tabl
                                max_context_len: int, *, sm_scale=None, num_segments: int = 0,
                                out_dtype=torch.bfloat16, return_lse: bool = False,
                                workspace: Optional[torch.Tensor] = None,
-                               out: Optional[torch.Tensor] = None, stream=None):
+                               out: Optional[torch.Tensor] = None, pv_mode: str = "fp32",
+                               stream=None):
     """Paged decode with the per-token query quantisation fused into the kernel.
 
     q [B,Hq,D] f16/bf16.  Same result as sage_quant_int8 + sage_attn_decode_paged.
@@ -319,7 +337,8 @@ def sage_attn_decode_paged_q16(q, k_cache, v_cache, k_scale, v_scale, block_tabl
         out = torch.empty((B, Hq, D), dtype=out_dtype, device=k_cache.device)
     lse = torch.empty((B, Hq), dtype=torch.float32, device=k_cache.device) if return_lse else None
     a = _decode_args(None, None, k_cache, v_cache, k_scale, v_scale, block_table, context_lens,
-                     max_context_len, sm_scale, num_segments, out, lse, shape=(B, Hq, D))
+                     max_context_len, sm_scale, num_segments, out, lse, shape=(B, Hq, D),
+                     pv_mode=pv_mode)
     # the library's choice for these buffers (it depends on where they live)
     S = num_segments or int(lib().sage_decode_auto_segments(ctypes.byref(a), _ptr_io(q)))
     a.num_segments = S
@@ -371,7 +390,8 @@ def decode_segments_used(max_context_len: int, num_segments: int) -> int:
 
 def sage_attn_decode_paged_partials(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale,
                                     block_table, context_lens, max_context_len: int,
-                                    num_segments: int, *, sm_scale=None, stream=None):
+                                    num_segments: int, *, sm_scale=None, pv_mode: str = "fp32",
+                                    stream=None):
     """Decode without the combine: returns (o_part [B,Hq,S,D], lse_part [B,Hq,S])."""
     B, Hq, D = q_int8.shape
     S = decode_segments_used(max_context_len, num_segments)
@@ -379,7 +399,8 @@ def sage_attn_decode_paged_partials(q_int8, q_scale, k_cache, v_cache, k_scale, 
     lse_part = torch.empty((B, Hq, S), dtype=torch.float32, device=k_cache.device)
     dummy = torch.empty((1,), dtype=torch.float16, device=k_cache.device)
     a = _decode_args(q_int8, q_scale, k_cache, v_cache, k_scale, v_scale, block_table,
-                     context_lens, max_context_len, sm_scale, num_segments, dummy, None)
+                     context_lens, max_context_len, sm_scale, num_segments, dummy, None,
+                     pv_mode=pv_mode)
     used = _i(0)
     _check(lib().sage_attn_decode_paged_partials(ctypes.byref(a), _ptr(o_part), _ptr(lse_part),
                                                  ctypes.byref(used), _stream(stream)))

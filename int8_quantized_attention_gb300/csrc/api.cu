@@ -145,7 +145,7 @@ void record_launch(const LaunchLog &log) { g_last = log; }
 
 SAGE_API const char *sage_get_last_error_message(void) { return g_msg.c_str(); }
 
-SAGE_API int sage_version(void) { return 6; }
+SAGE_API int sage_version(void) { return 7; }
 
 SAGE_API sage_status_t sage_last_launch_info(sage_launch_info_t *info) {
     if (!info) return fail(SAGE_ERR_INVALID_ARG, "info is NULL");
@@ -428,6 +428,8 @@ int check_decode_args(const sage_decode_args_t *a, const void *q_fp) {
                     a->max_context_len, a->max_blocks);
     if (a->num_segments < 0 || a->num_segments > 1024)
         return fail(SAGE_ERR_INVALID_ARG, "num_segments outside [0, 1024]");
+    if (a->pv_mode < SAGE_PV_F32 || a->pv_mode > SAGE_PV_INT8)
+        return fail(SAGE_ERR_UNSUPPORTED, "pv_mode %d is not one of SAGE_PV_*", a->pv_mode);
     if (a->B == 0) return SAGE_OK;
     if ((!q_fp && (!a->q || !a->q_scale)) || !a->context_lens || !a->out)
         return fail(SAGE_ERR_INVALID_ARG, "q, q_scale, context_lens and out are required");
@@ -490,6 +492,7 @@ static sage_status_t run_decode(const sage_decode_args_t *a, void *workspace,
     p.num_segments = S, p.pages_per_seg = pps;
     p.max_pages = pages;
     p.max_ctx = a->max_context_len;
+    p.pv_mode = a->pv_mode;
     const float sm = a->sm_scale > 0.0f ? a->sm_scale : 1.0f / sqrtf((float)a->D);
     p.qk_scale_log2 = sm * 1.4426950408889634f;
     p.out = a->out, p.out_bf16 = a->out_dtype == SAGE_BF16, p.lse = a->lse;

@@ -42,6 +42,7 @@ namespace sage {
 namespace {
 
 constexpr int kConsumerWarps = 4;
+constexpr int kPvF32 = 0, kPvF16 = 1, kPvF16F32 = 2, kPvInt8 = 3;  // sage_decode_args_t::pv_mode
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
 constexpr int kMaxSegPages = 1024;  // block-table entries staged per CTA (segment length cap)
@@ -105,6 +106,21 @@ __device__ __forceinline__ void mma_f16(float (&c)[4], const uint32_t (&a)[4], u
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// Same MMA with f16 accumulators: d/c = {row g, row g + 8} x columns
+// (2 q4, 2 q4 + 1), each an f16x2 word.
+__device__ __forceinline__ void mma_f16_f16acc(uint32_t (&c)[2], const uint32_t (&a)[4], uint32_t b0,
+                                               uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f16.f16.f16.f16 {%0,%1}, {%2,%3,%4,%5}, {%6,%7}, "
+        "{%0,%1};"
+        : "+r"(c[0]), "+r"(c[1])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t w) {
+    return __half22float2(*reinterpret_cast<const __half2 *>(&w));
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -116,7 +132,17 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-template <int D>
+// P.V variants (SageAttention MXMACA README, advanced configuration:
+// pv_accum_dtype; "INT8 QK MMAC on gfx936 DCU", sections 6 and 8: INT8 P.V
+// with the V scale fused into P).
+//   kPvF32     f16 P x V, fp32 accumulators (the default)
+//   kPvF16     f16 P x V, f16 accumulators throughout
+//   kPvF16F32  each page's product in f16 accumulators, added to fp32 ones
+//              (the README's two-level "InstBuf" accumulation)
+//   kPvInt8    P' = p * v_scale quantised to INT8 per head over the page's 16
+//              keys (s = max P' / 127, codes rne(P' / s)); codes times INT8
+//              values summed exactly, then scaled by s into fp32
+template <int D, int PV>
 __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
     using Cfg = DecodeCfg<D>;
     constexpr int NST = Cfg::kStages;
@@ -204,6 +230,12 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
     float o[D / 16][4];  // O^T fragments: rows = channels, cols = heads
 #pragma unroll
     for (int t = 0; t < D / 16; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.0f;
+    uint32_t oh[PV == kPvF16 ? D / 16 : 1][2];  // the same fragments in f16 (kPvF16)
+#pragma unroll
+    for (int t = 0; t < (PV == kPvF16 ? D / 16 : 1); ++t) oh[t][0] = oh[t][1] = 0u;
+    // With f16 accumulators the running max moves with every larger page
+    // max, so p <= 1 and the accumulated P'.V stays far inside the f16 range.
+    constexpr float kLazy = PV == kPvF16 ? 0.0f : 8.0f;
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer
@@ -392,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 alpha[j] = 1.0f;
-                if (mx != -INFINITY && (m[j] == -INFINITY || mx > m[j] + 8.0f)) {
+                if (mx != -INFINITY && (m[j] == -INFINITY || mx > m[j] + kLazy)) {
                     alpha[j] = m[j] == -INFINITY ? 0.0f : fast_exp2(m[j] - mx);
                     m[j] = mx;
                     need = true;
@@ -403,17 +435,50 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
                 l[j] = l[j] * alpha[j] + pr[0][j] + pr[1][j];
             }
             if (__any_sync(0xffffffffu, need)) {
+                if constexpr (PV == kPvF16) {
+                    const uint32_t al = pack_f16x2(alpha[0], alpha[1]);
 #pragma unroll
-                for (int dt = 0; dt < D / 16; ++dt) {
-                    o[dt][0] *= alpha[0];
-                    o[dt][1] *= alpha[1];
-                    o[dt][2] *= alpha[0];
-                    o[dt][3] *= alpha[1];
+                    for (int dt = 0; dt < D / 16; ++dt) {
+                        __half2 *h = reinterpret_cast<__half2 *>(oh[dt]);
+                        h[0] = __hmul2(h[0], *reinterpret_cast<const __half2 *>(&al));
+                        h[1] = __hmul2(h[1], *reinterpret_cast<const __half2 *>(&al));
+                    }
+                } else {
+#pragma unroll
+                    for (int dt = 0; dt < D / 16; ++dt) {
+                        o[dt][0] *= alpha[0];
+                        o[dt][1] *= alpha[1];
+                        o[dt][2] *= alpha[0];
+                        o[dt][3] *= alpha[1];
+                    }
                 }
             }
-            // ---- P^T (x v_scale) -> B operand via in-register transpose
-            const uint32_t pb0 = movmatrix_trans(pack_f16x2(pr[0][0] * sv0, pr[0][1] * sv0));
-            const uint32_t pb1 = movmatrix_trans(pack_f16x2(pr[1][0] * sv1, pr[1][1] * sv1));
+            // ---- P^T (x v_scale) -> B operand via in-register transpose;
+            // for INT8 P the operand holds the page's codes and sp the
+            // per-head scale that multiplies the page's exact product
+            float sp[2] = {1.0f, 1.0f};
+            uint32_t pb0, pb1;
+            if constexpr (PV == kPvInt8) {
+                float w[2][2], cd[2][2];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    w[0][j] = pr[0][j] * sv0;
+                    w[1][j] = pr[1][j] * sv1;
+                    float mx = fmaxf(w[0][j], w[1][j]);  // over the page's 16 keys
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                    sp[j] = __fdiv_rn(mx, 127.0f);
+                    const float rp = quant_recip(sp[j]);
+                    cd[0][j] = (float)quant_code(w[0][j], sp[j], rp);
+                    cd[1][j] = (float)quant_code(w[1][j], sp[j], rp);
+                }
+                pb0 = movmatrix_trans(pack_f16x2(cd[0][0], cd[0][1]));  // integers: exact in f16
+                pb1 = movmatrix_trans(pack_f16x2(cd[1][0], cd[1][1]));
+            } else {
+                pb0 = movmatrix_trans(pack_f16x2(pr[0][0] * sv0, pr[0][1] * sv0));
+                pb1 = movmatrix_trans(pack_f16x2(pr[1][0] * sv1, pr[1][1] * sv1));
+            }
             // ---- O^T += V^T P^T.  A = V^T straight from the INT8 slab: a
             // transposed ldmatrix gives each lane keys (2q4, 2q4+1) of the
             // channel pair (2g, 2g+1); the even channel fills A row g, the odd
@@ -424,15 +489,47 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
             for (int dp = 0; dp < D / 32; ++dp) {
                 uint32_t r[4], a[4];
                 ldsm_x4_trans(vstg + dp * 512, r);
-                i8x4_to_f16x2_even_odd(r[0], a[0], a[1]);
-                i8x4_to_f16x2_even_odd(r[1], a[2], a[3]);
-                mma_f16(o[2 * dp], a, pb0, pb1);
-                i8x4_to_f16x2_even_odd(r[2], a[0], a[1]);
-                i8x4_to_f16x2_even_odd(r[3], a[2], a[3]);
-                mma_f16(o[2 * dp + 1], a, pb0, pb1);
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int dt = 2 * dp + hf;
+                    i8x4_to_f16x2_even_odd(r[2 * hf], a[0], a[1]);
+                    i8x4_to_f16x2_even_odd(r[2 * hf + 1], a[2], a[3]);
+                    if constexpr (PV == kPvF32) {
+                        mma_f16(o[dt], a, pb0, pb1);
+                    } else if constexpr (PV == kPvF16) {
+                        mma_f16_f16acc(oh[dt], a, pb0, pb1);
+                    } else if constexpr (PV == kPvF16F32) {
+                        uint32_t h[2] = {0u, 0u};  // this page's product, f16
+                        mma_f16_f16acc(h, a, pb0, pb1);
+                        const float2 lo = unpack_f16x2(h[0]), hi = unpack_f16x2(h[1]);
+                        o[dt][0] += lo.x;
+                        o[dt][1] += lo.y;
+                        o[dt][2] += hi.x;
+                        o[dt][3] += hi.y;
+                    } else {
+                        // codes x values: products <= 127 * 128, sums over 16
+                        // keys below 2^24 -- exact in the fp32 accumulator
+                        float t[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                        mma_f16(t, a, pb0, pb1);
+                        o[dt][0] = fmaf(sp[0], t[0], o[dt][0]);
+                        o[dt][1] = fmaf(sp[1], t[1], o[dt][1]);
+                        o[dt][2] = fmaf(sp[0], t[2], o[dt][2]);
+                        o[dt][3] = fmaf(sp[1], t[3], o[dt][3]);
+                    }
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&empty[s]));  // stage fully read
+        }
+        if constexpr (PV == kPvF16) {
+#pragma unroll
+            for (int dt = 0; dt < D / 16; ++dt) {
+                const float2 lo = unpack_f16x2(oh[dt][0]), hi = unpack_f16x2(oh[dt][1]);
+                o[dt][0] = lo.x;
+                o[dt][1] = lo.y;
+                o[dt][2] = hi.x;
+                o[dt][3] = hi.y;
+            }
         }
         // ---- per-warp totals of l over the 8 key rows sharing a column
 #pragma unroll
@@ -605,11 +702,11 @@ __global__ void __launch_bounds__(kThreads, 3) decode_kernel(DecodeParams p) {
     }
 }
 
-template <int D>
+template <int D, int PV>
 cudaError_t launch_d(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {
     using Cfg = DecodeCfg<D>;
     cudaError_t e =
-        cudaFuncSetAttribute(decode_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+        cudaFuncSetAttribute(decode_kernel<D, PV>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
     if (e != cudaSuccess) return e;
     const dim3 grid(p.num_segments, p.Hkv * p.head_tiles, p.B);
     cudaLaunchConfig_t cfg = {};
@@ -635,7 +732,7 @@ cudaError_t launch_d(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {
     }
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    e = cudaLaunchKernelEx(&cfg, decode_kernel<D>, p);
+    e = cudaLaunchKernelEx(&cfg, decode_kernel<D, PV>, p);
     if (e != cudaSuccess) return e;
     log.add("decode_kernel", grid, dim3(kThreads), dim3(p.cluster ? p.num_segments : 1, 1, 1),
             Cfg::kSmem);
@@ -652,26 +749,26 @@ int decode_ctas_per_sm(int D) {
     cudaError_t e = cudaSuccess;
     switch (D) {
         case 64:
-            e = cudaFuncSetAttribute(decode_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(decode_kernel<64, kPvF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      DecodeCfg<64>::kSmem);
             if (e == cudaSuccess)
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64>, kThreads,
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<64, kPvF32>, kThreads,
                                                                   DecodeCfg<64>::kSmem);
             if (e != cudaSuccess || n < 1) n = DecodeCfg<64>::kCtasPerSm;
             break;
         case 128:
-            e = cudaFuncSetAttribute(decode_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(decode_kernel<128, kPvF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      DecodeCfg<128>::kSmem);
             if (e == cudaSuccess)
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128>, kThreads,
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<128, kPvF32>, kThreads,
                                                                   DecodeCfg<128>::kSmem);
             if (e != cudaSuccess || n < 1) n = DecodeCfg<128>::kCtasPerSm;
             break;
         default:
-            e = cudaFuncSetAttribute(decode_kernel<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            e = cudaFuncSetAttribute(decode_kernel<256, kPvF32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      DecodeCfg<256>::kSmem);
             if (e == cudaSuccess)
-                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<256>, kThreads,
+                e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<256, kPvF32>, kThreads,
                                                                   DecodeCfg<256>::kSmem);
             if (e != cudaSuccess || n < 1) n = DecodeCfg<256>::kCtasPerSm;
             break;
@@ -679,11 +776,22 @@ int decode_ctas_per_sm(int D) {
     return n;
 }
 
+template <int D>
+cudaError_t launch_pv(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {
+    switch (p.pv_mode) {
+        case kPvF32: return launch_d<D, kPvF32>(p, st, log);
+        case kPvF16: return launch_d<D, kPvF16>(p, st, log);
+        case kPvF16F32: return launch_d<D, kPvF16F32>(p, st, log);
+        case kPvInt8: return launch_d<D, kPvInt8>(p, st, log);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 cudaError_t launch_decode(const DecodeParams &p, cudaStream_t st, LaunchLog &log) {
     switch (p.D) {
-        case 64: return launch_d<64>(p, st, log);
-        case 128: return launch_d<128>(p, st, log);
-        case 256: return launch_d<256>(p, st, log);
+        case 64: return launch_pv<64>(p, st, log);
+        case 128: return launch_pv<128>(p, st, log);
+        case 256: return launch_pv<256>(p, st, log);
         default: return cudaErrorInvalidValue;
     }
 }

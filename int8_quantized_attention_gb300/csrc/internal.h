@@ -123,6 +123,7 @@ struct DecodeParams {
                               // thread-block cluster and merge through distributed shared memory
     int after_quant;          // 1: launched right behind the kernel that writes q / q_scale
                               // (programmatic dependent launch; consumers wait on the device)
+    int pv_mode;              // SAGE_PV_* (P.V operands and accumulation)
     int *err;
 };
 

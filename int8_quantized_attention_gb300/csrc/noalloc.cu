@@ -115,6 +115,7 @@ SAGE_API sage_status_t sage_attn_decode_paged_noalloc(const sage_decode_args_t *
     p.num_segments = S, p.pages_per_seg = pps;
     p.max_pages = pages;
     p.max_ctx = a->max_context_len;
+    p.pv_mode = a->pv_mode;
     const float sm = a->sm_scale > 0.0f ? a->sm_scale : 1.0f / sqrtf((float)a->D);
     p.qk_scale_log2 = sm * 1.4426950408889634f;
     p.out = a->out, p.out_bf16 = a->out_dtype == SAGE_BF16, p.lse = a->lse;

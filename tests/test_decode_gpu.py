@@ -387,3 +387,44 @@ def test_decode_permuted_pages_bitwise_partials_path(sage):
     out2 = _run(sage, qi, qs, c2, max(lens), num_segments=14)
     torch.cuda.synchronize()
     assert torch.equal(out1, out2)
+
+
+@pytest.mark.parametrize("pv", ["int8", "fp16+fp32", "fp16"])
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("segments", [1, 5, 12])
+def test_decode_pv_modes(sage, pv, D, segments):
+    """The P.V variants against the oracle: INT8 P.V against the oracle's
+    INT8 P.V (V-scaled probabilities quantised per 16-key page), the f16
+    accumulators against exact attention; ragged contexts, GQA 6:1, one
+    segment, an in-cluster merge and the combine kernel."""
+    B, Hq, Hkv = 3, 24, 4
+    lens = [37, 300, 1029]
+    c = W.paged_cache(B, Hkv, D, lens, seed=D + segments, device="cuda", extra_blocks=3)
+    qi, qs = _quant_query(sage, B, Hq, D, seed=segments)
+    out, lse = _run(sage, qi, qs, c, max(lens), num_segments=segments, return_lse=True,
+                    out_dtype=torch.float16, pv_mode=pv)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    o_ref, l_ref = oracle.decode_paged(np_(qi), np_(qs), np_(c.k_cache), np_(c.v_cache),
+                                       np_(c.k_scale), np_(c.v_scale), np_(c.block_table),
+                                       np_(c.lens), pv_int8=pv == "int8")
+    assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
+
+
+@pytest.mark.parametrize("pv", ["int8", "fp16+fp32", "fp16"])
+def test_decode_pv_modes_full_size(sage, pv):
+    """The paged-decode workload (B8, 24:4, D256, 8192 tokens, 14 segments,
+    bf16 output) in each P.V variant, every output against the oracle."""
+    P = W.WORKLOADS["paged_decode"].params
+    c = W.paged_cache(P["B"], P["Hkv"], P["D"], [P["ctx"]] * P["B"], seed=P["seed"],
+                      device="cuda")
+    qi, qs = _quant_query(sage, P["B"], P["Hq"], P["D"], seed=P["seed"])
+    out, lse = _run(sage, qi, qs, c, P["ctx"], return_lse=True, pv_mode=pv)
+    torch.cuda.synchronize()
+    o_ref, l_ref = oracle.decode_paged(np_(qi), np_(qs), np_(c.k_cache), np_(c.v_cache),
+                                       np_(c.k_scale), np_(c.v_scale), np_(c.block_table),
+                                       np_(c.lens), pv_int8=pv == "int8")
+    r, m = assert_close(f32(out), o_ref)
+    assert_close(np_(lse), l_ref, "lse")
+    print("pv %s: rel-L2 %.3g max-abs %.3g" % (pv, r, m))
