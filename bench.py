@@ -765,6 +765,18 @@ def _configs_kv_append(emit, gpu_ms, peaks):
               "gpu_ms": round(ms, 4), "GBps": round(gbs, 1),
               "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4),
               "bytes": nbytes})
+        # the producer form: the same append plus the step's query quantised
+        # (Hq rows per token) in one launch
+        Hq = P["Hq"]
+        q = torch.randn((B, Hq, n, D), generator=g, device="cuda").to(torch.bfloat16)
+        fp = lambda: sage.sage_kv_producer(q, k, v, c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                           c.block_table, pos)
+        ms = gpu_ms(fp)
+        pbytes = nbytes + B * Hq * n * (2 * D + D + 4)
+        gbs = pbytes / (ms * 1e-3) / 1e9
+        emit({"config": "kv_producer", "case": label, "B": B, "new_tokens": n, "Hq": Hq,
+              "Hkv": Hkv, "D": D, "gpu_ms": round(ms, 4), "GBps": round(gbs, 1),
+              "frac_of_measured_hbm": round(gbs / peaks["hbm_gbs"], 4), "bytes": pbytes})
         del c
 
 

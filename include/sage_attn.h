@@ -163,6 +163,23 @@ sage_status_t sage_kv_cache_append(const void *k_new, const void *v_new, sage_dt
                                    const int32_t *positions, int num_blocks, int8_t *k_cache,
                                    int8_t *v_cache, float *k_scale, float *v_scale, void *stream);
 
+/* The KV producer of a decode or prefill step ([P1] section 4: the query
+ * is quantised once, in the producer that writes the step's K/V, and every
+ * split-K segment reuses its codes): sage_kv_cache_append's K/V rows plus
+ * the step's query rows in ONE launch.  q_new f16/bf16 [B, Hq, n_new, D]
+ * (same dtype as k_new/v_new, 16-byte aligned) is quantised per (token,
+ * head) with the rule of sage_quant_int8 into q_int8 [B, Hq, n_new, D]
+ * (8-byte aligned) and q_scale [B, Hq, n_new] fp32 -- for a decode step
+ * (n_new = 1) exactly the q / q_scale that sage_attn_decode_paged reads.
+ * Errors and bad pages as sage_kv_cache_append; query rows never touch
+ * the cache.  All pointers are device memory. */
+sage_status_t sage_kv_producer(const void *q_new, const void *k_new, const void *v_new,
+                               sage_dtype_t dtype, int B, int Hq, int Hkv, int n_new, int D,
+                               const int32_t *block_table, int max_blocks,
+                               const int32_t *positions, int num_blocks, int8_t *k_cache,
+                               int8_t *v_cache, float *k_scale, float *v_scale, int8_t *q_int8,
+                               float *q_scale, void *stream);
+
 /* --------------------------------------------------------------------------
  * Split-K paged decode  ([P1] sections 1, 3, 4, 5)
  *

@@ -124,6 +124,9 @@ def lib():
         L.sage_kv_cache_append.argtypes = [_vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp, _i, _vp,
                                            _vp, _vp, _vp, _vp]
         L.sage_kv_cache_append.restype = _i
+        L.sage_kv_producer.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _i, _vp, _i,
+                                       _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+        L.sage_kv_producer.restype = _i
         L.sage_attn_decode_paged_partials.argtypes = [ctypes.POINTER(DecodeArgs), _vp, _vp,
                                                       ctypes.POINTER(_i), _vp]
         L.sage_attn_decode_paged_partials.restype = _i
@@ -374,6 +377,36 @@ def sage_kv_cache_append(k_new, v_new, k_cache, v_cache, k_scale, v_scale, block
                                       _ptr(block_table), block_table.shape[1], _ptr(positions),
                                       k_cache.shape[0], _ptr(k_cache), _ptr(v_cache),
                                       _ptr(k_scale), _ptr(v_scale), _stream(stream)))
+
+
+def sage_kv_producer(q_new, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_table,
+                     positions, stream=None):
+    """The step's KV producer in one launch: append k_new/v_new [B,Hkv,n,D] to
+    the paged cache (as sage_kv_cache_append) and quantise q_new [B,Hq,n,D]
+    per (token, head).  Returns (q_int8 [B,Hq,n,D], q_scale [B,Hq,n])."""
+    for t, name in ((q_new, "q_new"), (k_new, "k_new"), (v_new, "v_new")):
+        if t.dtype not in (torch.float16, torch.bfloat16) or not t.is_contiguous():
+            raise ValueError(name + " must be a contiguous f16/bf16 tensor")
+    if len({q_new.dtype, k_new.dtype, v_new.dtype}) != 1 or v_new.shape != k_new.shape:
+        raise ValueError("q_new, k_new and v_new must share a dtype; k_new and v_new a shape")
+    _need(k_cache, torch.int8, "k_cache")
+    _need(v_cache, torch.int8, "v_cache")
+    _need(k_scale, torch.float32, "k_scale")
+    _need(v_scale, torch.float32, "v_scale")
+    _need(block_table, torch.int32, "block_table")
+    _need(positions, torch.int32, "positions")
+    B, Hkv, n, D = k_new.shape
+    Hq = q_new.shape[1]
+    if q_new.shape != (B, Hq, n, D):
+        raise ValueError("q_new must be [B, Hq, n, D] with k_new's B, n and D")
+    q_int8 = torch.empty((B, Hq, n, D), dtype=torch.int8, device=q_new.device)
+    q_scale = torch.empty((B, Hq, n), dtype=torch.float32, device=q_new.device)
+    _check(lib().sage_kv_producer(_ptr(q_new), _ptr(k_new), _ptr(v_new), _dt(k_new.dtype), B, Hq,
+                                  Hkv, n, D, _ptr(block_table), block_table.shape[1],
+                                  _ptr(positions), k_cache.shape[0], _ptr(k_cache), _ptr(v_cache),
+                                  _ptr(k_scale), _ptr(v_scale), _ptr(q_int8), _ptr(q_scale),
+                                  _stream(stream)))
+    return q_int8, q_scale
 
 
 def decode_segments_used(max_context_len: int, num_segments: int) -> int:

@@ -908,3 +908,40 @@ SAGE_API sage_status_t sage_kv_cache_append(const void *k_new, const void *v_new
     cudaError_t e = sage::launch_kv_append(p, static_cast<cudaStream_t>(stream), g_last);
     return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "kv append launch");
 }
+
+SAGE_API sage_status_t sage_kv_producer(const void *q_new, const void *k_new, const void *v_new,
+                                        sage_dtype_t dtype, int B, int Hq, int Hkv, int n_new,
+                                        int D, const int32_t *block_table, int max_blocks,
+                                        const int32_t *positions, int num_blocks, int8_t *k_cache,
+                                        int8_t *v_cache, float *k_scale, float *v_scale,
+                                        int8_t *q_int8, float *q_scale, void *stream) {
+    if (!head_dim_ok(D)) return fail(SAGE_ERR_UNSUPPORTED, "head_dim %d not in {64,128,256}", D);
+    if (dtype != SAGE_F16 && dtype != SAGE_BF16)
+        return fail(SAGE_ERR_UNSUPPORTED, "q/k/v dtype must be f16 or bf16");
+    if (B < 0 || Hq < 1 || Hkv < 1 || n_new < 0 || max_blocks < 1 || num_blocks < 1)
+        return fail(SAGE_ERR_INVALID_ARG,
+                    "bad shape (B=%d Hq=%d Hkv=%d n=%d max_blocks=%d num_blocks=%d)", B, Hq, Hkv,
+                    n_new, max_blocks, num_blocks);
+    g_last = sage::LaunchLog();
+    if ((int64_t)B * n_new == 0) return SAGE_OK;
+    if (!q_new || !k_new || !v_new || !block_table || !positions || !k_cache || !v_cache ||
+        !k_scale || !v_scale || !q_int8 || !q_scale)
+        return fail(SAGE_ERR_INVALID_ARG, "null pointer argument");
+    if (!aligned(q_new, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+        !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(q_int8, 8))
+        return fail(SAGE_ERR_INVALID_ARG,
+                    "q_new, k_new, v_new and the caches must be 16-byte aligned, q_int8 8-byte");
+    int *ew = nullptr;
+    sage_status_t st = error_word(&ew);
+    if (st != SAGE_OK) return st;
+    sage::KvAppendParams p = {};
+    p.k = k_new, p.v = v_new, p.bf16 = dtype == SAGE_BF16;
+    p.B = B, p.H = Hkv, p.n = n_new, p.D = D;
+    p.block_table = block_table, p.pos = positions;
+    p.max_blocks = max_blocks, p.num_blocks = num_blocks;
+    p.k_cache = k_cache, p.v_cache = v_cache, p.k_scale = k_scale, p.v_scale = v_scale;
+    p.q = q_new, p.Hq = Hq, p.q_int8 = q_int8, p.q_scale = q_scale;
+    p.err = ew;
+    cudaError_t e = sage::launch_kv_append(p, static_cast<cudaStream_t>(stream), g_last);
+    return e == cudaSuccess ? SAGE_OK : cuda_fail(e, "kv producer launch");
+}

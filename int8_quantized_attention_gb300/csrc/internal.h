@@ -142,6 +142,12 @@ struct KvAppendParams {
     int max_blocks, num_blocks;
     int8_t *k_cache, *v_cache;         // [num_blocks, H, D/16, 16, 16]
     float *k_scale, *v_scale;          // [num_blocks, H, 16]
+    // optional query rows quantised in the same launch (the KV producer
+    // form): q [B, Hq, n, D] f16/bf16 -> q_int8 [B, Hq, n, D], q_scale [B, Hq, n]
+    const void *q;
+    int Hq;
+    int8_t *q_int8;
+    float *q_scale;
     int *err;
 };
 

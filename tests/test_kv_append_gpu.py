@@ -85,3 +85,63 @@ def test_decode_after_append_matches_oracle(sage):
                                        np_(c.block_table), np_(c.lens))
     assert_close(f32(out), o_ref)
     assert_close(np_(lse), l_ref, "lse")
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("n", [1, 19])
+def test_kv_producer_bit_exact(sage, D, dtype, n):
+    """One launch appends the step's K/V rows to the cache and quantises its
+    query rows ([P1] section 4): cache bytes and scales equal the oracle's
+    append, query codes and scales the oracle's per-token quantisation."""
+    B, Hq, Hkv, nblk = 3, 12, 4, 40
+    g = torch.Generator().manual_seed(D + n + 1)
+    q_new = torch.randn((B, Hq, n, D), generator=g).to(dtype).cuda()
+    k_new = (torch.randn((B, Hkv, n, D), generator=g) * 2).to(dtype).cuda()
+    v_new = torch.randn((B, Hkv, n, D), generator=g).to(dtype).cuda()
+    q_new[1, 3, 0] = 0                                   # an all-zero query row
+    perm = torch.randperm(nblk, generator=g)[: B * 10].view(B, 10).to(torch.int32).cuda()
+    pos = torch.tensor([0, 15, 100], dtype=torch.int32).cuda()
+    kc, vc, ks, vs = _fresh_cache(nblk, Hkv, D, seed=D + 1)
+    want_k = oracle.kv_append(f32(k_new), np_(perm), np_(pos), np_(kc), np_(ks))
+    want_v = oracle.kv_append(f32(v_new), np_(perm), np_(pos), np_(vc), np_(vs))
+    want_q, want_qs, _ = oracle.quant_int8(f32(q_new), block_tokens=1)
+    qi, qs = sage.sage_kv_producer(q_new, k_new, v_new, kc, vc, ks, vs, perm, pos)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    info = sage.last_launch_info()
+    assert info["kernel"] == "kv_producer_kernel" and info["launches"] == 1
+    assert np.array_equal(np_(kc), want_k[0]) and np.array_equal(np_(ks), want_k[1])
+    assert np.array_equal(np_(vc), want_v[0]) and np.array_equal(np_(vs), want_v[1])
+    assert np.array_equal(np_(qi), want_q) and np.array_equal(np_(qs), want_qs)
+
+
+def test_kv_producer_then_decode(sage):
+    """A decode step the way [P1] section 4 runs it: the producer appends the
+    new token and quantises the query once, then the split-K decode reads
+    those codes -- bit for bit the decode with the query quantised inside
+    the kernel, and within tolerance of the oracle."""
+    B, Hq, Hkv, D = 4, 24, 4, 256
+    lens = [700, 4095, 31, 2000]
+    c = W.paged_cache(B, Hkv, D, [n + 1 for n in lens], seed=71, device="cuda")
+    g = torch.Generator().manual_seed(72)
+    q = torch.randn((B, Hq, 1, D), generator=g).to(torch.bfloat16).cuda()
+    k_new = torch.randn((B, Hkv, 1, D), generator=g).to(torch.bfloat16).cuda()
+    v_new = torch.randn((B, Hkv, 1, D), generator=g).to(torch.bfloat16).cuda()
+    pos = torch.tensor(lens, dtype=torch.int32).cuda()
+    qi, qs = sage.sage_kv_producer(q, k_new, v_new, c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                   c.block_table, pos)
+    L = max(lens) + 1
+    out = sage.sage_attn_decode_paged(qi[:, :, 0].contiguous(), qs[:, :, 0].contiguous(),
+                                      c.k_cache, c.v_cache, c.k_scale, c.v_scale, c.block_table,
+                                      c.lens, L, num_segments=12, out_dtype=torch.float16)
+    ref = sage.sage_attn_decode_paged_q16(q[:, :, 0].contiguous(), c.k_cache, c.v_cache,
+                                          c.k_scale, c.v_scale, c.block_table, c.lens, L,
+                                          num_segments=12, out_dtype=torch.float16)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert torch.equal(out, ref)
+    o_ref, _ = oracle.decode_paged(np_(qi)[:, :, 0], np_(qs)[:, :, 0], np_(c.k_cache),
+                                   np_(c.v_cache), np_(c.k_scale), np_(c.v_scale),
+                                   np_(c.block_table), np_(c.lens))
+    assert_close(f32(out), o_ref)
