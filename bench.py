@@ -527,7 +527,7 @@ def run_profile(args):
     from int8_quantized_attention_gb300 import workloads as W
 
     build.build()
-    P = dict(W.WORKLOADS[args.profile].params)
+    P = dict(W.WORKLOADS["paged_decode" if args.profile == "kv_producer" else args.profile].params)
     if args.heads:
         ratio = P["Hq"] // P["Hkv"]
         P["Hq"] = args.heads
@@ -537,7 +537,20 @@ def run_profile(args):
                           device="cuda")
         q = W.decode_query(P["B"], P["Hq"], P["D"], seed=P["seed"], device="cuda")
         run = lambda: sage.sage_attn_decode_paged_q16(q, c.k_cache, c.v_cache, c.k_scale,
-                                                      c.v_scale, c.block_table, c.lens, P["ctx"])
+                                                      c.v_scale, c.block_table, c.lens, P["ctx"],
+                                                      pv_mode=args.pv_mode)
+    elif args.profile == "kv_producer":
+        # the KV producer of a 2048-token chunk of the chunked-prefill shape
+        # (24 query / 4 KV heads, D 256) appended after a 16384-token context
+        n, ctx = 2048, 16384
+        c = W.paged_cache(1, P["Hkv"], P["D"], [ctx + n], seed=9, device="cuda")
+        g = torch.Generator("cuda").manual_seed(10)
+        kn = torch.randn((1, P["Hkv"], n, P["D"]), generator=g, device="cuda").to(torch.bfloat16)
+        vn = torch.randn((1, P["Hkv"], n, P["D"]), generator=g, device="cuda").to(torch.bfloat16)
+        qn = torch.randn((1, P["Hq"], n, P["D"]), generator=g, device="cuda").to(torch.bfloat16)
+        pos = torch.full((1,), ctx, dtype=torch.int32, device="cuda")
+        run = lambda: sage.sage_kv_producer(qn, kn, vn, c.k_cache, c.v_cache, c.k_scale,
+                                            c.v_scale, c.block_table, pos)
     elif args.profile == "varlen_prefill":
         lens = W.varlen_lengths(P["n"], P["lo"], P["hi"], P["seed"])
         x = W.varlen_qkv(lens, lens, P["Hq"], P["Hkv"], P["D"], seed=P["seed"], dtype=P["dtype"],
@@ -839,7 +852,9 @@ def main():
     ap.add_argument("--no-prefill", dest="prefill", action="store_false")
     ap.add_argument("--profile", default=None,
                     choices=["paged_decode", "dense_prefill", "chunked_prefill",
-                             "varlen_prefill"])
+                             "varlen_prefill", "kv_producer"])
+    ap.add_argument("--pv-mode", default="fp32", choices=["fp32", "fp16", "fp16+fp32", "int8"],
+                    help="decode P.V variant for --profile paged_decode")
     ap.add_argument("--heads", type=int, default=0)
     ap.add_argument("--segments", type=int, default=0,
                     help="decode segment count (0: the library's choice)")

@@ -73,9 +73,13 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendParams p) {
     const float s = __fdiv_rn(amax, 127.0f);
     const float rs = quant_recip(s);
     uint32_t w[2] = {0u, 0u};
+    if constexpr (CPL == 8) {
+        quant8(f, s, rs, w[0], w[1]);  // the same codes, eight at a time
+    } else {
 #pragma unroll
-    for (int e = 0; e < CPL; ++e)
-        w[e >> 2] |= (uint32_t)(uint8_t)quant_code(f[e], s, rs) << (8 * (e & 3));
+        for (int e = 0; e < CPL; ++e)
+            w[e >> 2] |= (uint32_t)(uint8_t)quant_code(f[e], s, rs) << (8 * (e & 3));
+    }
     const int c0 = lane * CPL;
     int8_t *dst;
     if (is_q) {
