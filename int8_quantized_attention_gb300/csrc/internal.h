@@ -148,6 +148,7 @@ struct KvAppendParams {
     int Hq;
     int8_t *q_int8;
     float *q_scale;
+    FastDiv div_n, div_h;     // set by the launcher
     int *err;
 };
 

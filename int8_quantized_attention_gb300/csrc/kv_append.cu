@@ -53,12 +53,16 @@ __global__ void __launch_bounds__(256) kv_append_kernel(KvAppendParams p) {
     }
     int64_t page = 0, slot = 0;
     if (!is_q) {
-        const int64_t t = r % p.n, bh = r / p.n;
-        const int64_t b = bh / p.H, h = bh % p.H;
+        // row r = (b * H + h) * n + t: divisions by invariant-divisor
+        // constants (r < 2^31, checked on the host)
+        const uint32_t bh = p.div_n.div((uint32_t)r);
+        const uint32_t t = (uint32_t)r - bh * (uint32_t)p.n;
+        const uint32_t b = p.div_h.div(bh);
+        const uint32_t h = bh - b * (uint32_t)p.H;
         const int64_t pos = (int64_t)p.pos[b] + t;
         const int64_t pi = pos >> 4;
         int blk = -1;
-        if (pos >= 0 && pi < p.max_blocks) blk = p.block_table[b * p.max_blocks + pi];
+        if (pos >= 0 && pi < p.max_blocks) blk = p.block_table[(int64_t)b * p.max_blocks + pi];
         if ((unsigned)blk >= (unsigned)p.num_blocks) {
             if (lane == 0) atomicOr(p.err, kErrBadBlock);
             return;
@@ -102,11 +106,14 @@ cudaError_t launch_t(const KvAppendParams &p, cudaStream_t st, LaunchLog &log) {
     const int64_t rows = 2 * (int64_t)p.B * p.H * p.n + (p.q ? (int64_t)p.B * p.Hq * p.n : 0);
     const int64_t grid = (rows + 7) / 8;
     if (grid == 0) return cudaSuccess;
-    if (grid > 0x7fffffff) return cudaErrorInvalidValue;
+    if (rows >= 0x7fffffff) return cudaErrorInvalidValue;  // row indices are 32-bit
+    KvAppendParams q = p;
+    q.div_n = FastDiv((uint32_t)p.n);
+    q.div_h = FastDiv((uint32_t)p.H);
     switch (p.D) {
-        case 64: kv_append_kernel<T, 64><<<(unsigned)grid, 256, 0, st>>>(p); break;
-        case 128: kv_append_kernel<T, 128><<<(unsigned)grid, 256, 0, st>>>(p); break;
-        case 256: kv_append_kernel<T, 256><<<(unsigned)grid, 256, 0, st>>>(p); break;
+        case 64: kv_append_kernel<T, 64><<<(unsigned)grid, 256, 0, st>>>(q); break;
+        case 128: kv_append_kernel<T, 128><<<(unsigned)grid, 256, 0, st>>>(q); break;
+        case 256: kv_append_kernel<T, 256><<<(unsigned)grid, 256, 0, st>>>(q); break;
         default: return cudaErrorInvalidValue;
     }
     log.add(p.q ? "kv_producer_kernel" : "kv_append_kernel", dim3((unsigned)grid), dim3(256),
