@@ -196,10 +196,13 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     int b, hq, ct;
     int cq0 = 0, cq1 = 0, ck0 = 0, ck1 = 0;  // packed batch: this sequence's offsets
     if constexpr (VL) {
-        hq = blockIdx.y;
+        // one linear index, heads fastest: the CTAs of a tile slot for every
+        // head start together, and the grid ends on the light (first) tiles
+        // of the last sequence instead of on one head's heaviest tiles
+        const int g = (int)(blockIdx.x / (unsigned)p.Hq);
+        hq = (int)(blockIdx.x - (unsigned)g * (unsigned)p.Hq);
         // compact tile index: sequence b owns tiles [cu_q[b] / QR + b, ...),
         // ceil(len_b / QR) of them (at most one spare slot per sequence)
-        const int g = blockIdx.x;
         b = varlen_find_warp(p.B, g, [&](int k) {
             const int c = p.cu_q[k];
             return varlen_group0(c < 0 ? 0 : c, k, QR);
@@ -920,10 +923,12 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    // packed batches: one CTA per compact tile slot (ceil(len_b / QR) per
-    // sequence, at most total_q / QR + B slots), heads in y
+    // packed batches: one CTA per (compact tile slot, head) -- ceil(len_b /
+    // QR) slots per sequence, at most total_q / QR + B -- heads fastest
     constexpr int QR = 128 * C::NQ;
-    const dim3 grid = VL ? dim3((unsigned)(p.total_q / QR + p.B), p.Hq, 1)
+    const int64_t vl_ctas = VL ? (p.total_q / QR + p.B) * (int64_t)p.Hq : 0;
+    if (vl_ctas > 0x7fffffff) return cudaErrorInvalidValue;
+    const dim3 grid = VL ? dim3((unsigned)vl_ctas, 1, 1)
                          : dim3((unsigned)((p.Sq + QR - 1) / QR * p.Hq * p.B), 1, 1);
     if (!VL && (p.bundle < 1 || p.bundle > p.B * p.Hq)) return cudaErrorInvalidValue;
     prefill_kernel<D, VL><<<grid, C::THREADS, C::SMEM, st>>>(p, m);
