@@ -145,3 +145,24 @@ def test_kv_producer_then_decode(sage):
                                    np_(c.v_cache), np_(c.k_scale), np_(c.v_scale),
                                    np_(c.block_table), np_(c.lens))
     assert_close(f32(out), o_ref)
+
+
+def test_kv_producer_bad_page_skips_cache_rows_not_query_rows(sage):
+    """A page outside the cache skips only the K/V rows that would land there
+    (error word's bad-block bit set, the rest of the cache as the oracle's
+    append leaves it); the query rows, which never touch the cache, are
+    quantised all the same."""
+    B, Hq, Hkv, n, D, nblk = 1, 4, 2, 20, 128, 8
+    q_new = torch.randn((B, Hq, n, D), dtype=torch.bfloat16).cuda()
+    k_new = torch.randn((B, Hkv, n, D), dtype=torch.bfloat16).cuda()
+    v_new = torch.randn((B, Hkv, n, D), dtype=torch.bfloat16).cuda()
+    table = torch.tensor([[3, 77]], dtype=torch.int32).cuda()   # page 77 does not exist
+    pos = torch.tensor([4], dtype=torch.int32).cuda()            # tokens 4..23 -> pages 3, 77
+    kc, vc, ks, vs = _fresh_cache(nblk, Hkv, D, seed=6)
+    want_k = oracle.kv_append(f32(k_new), np_(table), np_(pos), np_(kc), np_(ks))
+    want_q, want_qs, _ = oracle.quant_int8(f32(q_new), block_tokens=1)
+    qi, qs = sage.sage_kv_producer(q_new, k_new, v_new, kc, vc, ks, vs, table, pos)
+    st, word = sage.check_device_status()
+    assert st != 0 and word & 2                                  # bad-block bit
+    assert np.array_equal(np_(kc), want_k[0]) and np.array_equal(np_(ks), want_k[1])
+    assert np.array_equal(np_(qi), want_q) and np.array_equal(np_(qs), want_qs)
