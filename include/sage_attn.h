@@ -404,7 +404,14 @@ typedef struct sage_prefill_args {
     float *lse;                     /* optional [B, Hq, Sq] */
     int smooth_v;                   /* subtract the chunk's V mean, add it back to o */
     float *v_mean;                  /* optional out [B, Hkv, D] fp32 (smooth_v) */
+    int layout;                     /* SAGE_LAYOUT_HND (0) or SAGE_LAYOUT_NHD (1), below */
 } sage_prefill_args_t;
+
+/* Layout of the prefill's f16/bf16 tensors ([P3] tensor_layout): HND keeps
+ * v [B, Hkv, Sk, D] and out [B, Hq, Sq, D]; NHD takes v [B, Sk, Hkv, D] and
+ * writes out [B, Sq, Hq, D].  The INT8 codes, scales, q_bias and lse are
+ * head-major in both (the layout sage_quant_int8 writes). */
+enum { SAGE_LAYOUT_HND = 0, SAGE_LAYOUT_NHD = 1 };
 
 /* Workspace of sage_attn_prefill (host only): the tensor cores of sm_103a
  * have no INT8 mode, so each call first expands the INT8 codes it reads --

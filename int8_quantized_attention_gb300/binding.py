@@ -57,7 +57,7 @@ class PrefillArgs(ctypes.Structure):
                 ("block_table", _vp), ("prefix_lens", _vp),
                 ("num_blocks", _i), ("max_blocks", _i), ("max_prefix_len", _i),
                 ("causal", _i), ("sm_scale", _f), ("out", _vp), ("out_dtype", _i), ("lse", _vp),
-                ("smooth_v", _i), ("v_mean", _vp)]
+                ("smooth_v", _i), ("v_mean", _vp), ("layout", _i)]
 
 
 class PrefillVarlenArgs(ctypes.Structure):
@@ -460,7 +460,7 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
                       out_dtype=None, return_lse: bool = False, debug_scores=None,
                       workspace: Optional[torch.Tensor] = None, out=None, lse=None,
                       smooth_v: bool = False, v_mean: Optional[torch.Tensor] = None,
-                      stream=None):
+                      layout: str = "HND", stream=None):
     """INT8-QK prefill attention over an optional paged INT8 prefix + a chunk.
 
     q_int8 [B,Hq,Sq,D]; q_scale [B,Hq,ceil(Sq/q_block)]; k_int8 [B,Hkv,Sk,D];
@@ -468,10 +468,19 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
     (smooth_k correction) or None; prefix = dict(k_cache, v_cache, k_scale,
     v_scale, block_table, lens, max_len) or None.  smooth_v subtracts the
     chunk's V mean from every value and adds it back to the output; v_mean
-    ([B, Hkv, D] fp32, optional) receives that mean.
+    ([B, Hkv, D] fp32, optional) receives that mean.  layout "NHD" takes v
+    as [B,Sk,Hkv,D] and returns out as [B,Sq,Hq,D] (the INT8 codes, scales,
+    q_bias and lse stay head-major).
     """
     B, Hq, Sq, D = q_int8.shape
     Hkv, Sk = k_int8.shape[1], k_int8.shape[2]
+    if layout not in ("HND", "NHD"):
+        raise ValueError("layout must be HND or NHD")
+    nhd = layout == "NHD"
+    vshape = (B, Sk, Hkv, D) if nhd else (B, Hkv, Sk, D)
+    oshape = (B, Sq, Hq, D) if nhd else (B, Hq, Sq, D)
+    if tuple(v.shape) != vshape:
+        raise ValueError("v must be %s for layout %s, got %s" % (vshape, layout, tuple(v.shape)))
     _need(q_int8, torch.int8, "q_int8")
     _need(k_int8, torch.int8, "k_int8")
     _need(q_scale, torch.float32, "q_scale")
@@ -480,9 +489,9 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
         raise ValueError("v must be contiguous")
     out_dtype = out.dtype if out is not None else (out_dtype or v.dtype)
     if out is None:
-        out = torch.empty((B, Hq, Sq, D), dtype=out_dtype, device=q_int8.device)
-    elif tuple(out.shape) != (B, Hq, Sq, D) or not out.is_contiguous():
-        raise ValueError("out must be a contiguous [B, Hq, Sq, D] tensor")
+        out = torch.empty(oshape, dtype=out_dtype, device=q_int8.device)
+    elif tuple(out.shape) != oshape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous %s tensor" % (oshape,))
     if lse is not None:
         _need(lse, torch.float32, "lse")
         return_lse = True
@@ -515,6 +524,7 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
     if v_mean is not None:
         _need(v_mean, torch.float32, "v_mean")
     a.smooth_v, a.v_mean = int(bool(smooth_v)), _ptr(v_mean)
+    a.layout = 1 if nhd else 0
     need = int(lib().sage_attn_prefill_workspace_size(ctypes.byref(a)))
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q_int8.device)

@@ -627,6 +627,9 @@ static sage_status_t check_prefill(const sage_prefill_args_t *a, int *qs_out, in
     if (a->max_prefix_len < 0 ||
         (a->max_prefix_len > 0 && (int64_t)a->max_prefix_len > 16ll * a->max_blocks))
         return fail(SAGE_ERR_INVALID_ARG, "max_prefix_len exceeds 16 * max_blocks");
+    if (a->layout != SAGE_LAYOUT_HND && a->layout != SAGE_LAYOUT_NHD)
+        return fail(SAGE_ERR_UNSUPPORTED, "layout %d is not SAGE_LAYOUT_HND or SAGE_LAYOUT_NHD",
+                    a->layout);
     *qs_out = qs;
     *ks_out = ks;
     return SAGE_OK;
@@ -683,6 +686,11 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
     p.k = a->k, p.k_scale = a->k_scale, p.k_shift = ks;
     p.k_groups = (a->Sk + a->k_block - 1) / a->k_block;
     p.v = a->v, p.v_bf16 = a->v_dtype == SAGE_BF16;
+    p.nhd = a->layout == SAGE_LAYOUT_NHD;
+    // element strides of the chunk's V per batch, kv head and token
+    p.v_sb = (int64_t)a->Hkv * a->Sk * a->D;
+    p.v_sh = p.nhd ? (int64_t)a->D : (int64_t)a->Sk * a->D;
+    p.v_st = p.nhd ? (int64_t)a->Hkv * a->D : (int64_t)a->D;
     p.q_bias = a->q_bias;
     if (has_prefix) {
         p.k_cache = a->k_cache, p.v_cache = a->v_cache;
@@ -714,7 +722,7 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
         mp.x = a->v;
         mp.bf16 = a->v_dtype == SAGE_BF16;
         mp.B = a->B, mp.H = a->Hkv, mp.S = a->Sk, mp.D = a->D;
-        mp.sb = (int64_t)a->Hkv * a->Sk * a->D, mp.sh = (int64_t)a->Sk * a->D, mp.ss = a->D;
+        mp.sb = p.v_sb, mp.sh = p.v_sh, mp.ss = p.v_st;
         mp.smooth = 1;
         mp.mu_out = mu;
         e = sage::launch_token_mean(mp, cst, stage_log);

@@ -196,6 +196,11 @@ struct PrefillParams {
     const int32_t *cu_q, *cu_k;
     int64_t total_q, total_k;
     int64_t v_st, v_sh;
+    // dense form, [P3] tensor_layout NHD: v is [B, Sk, Hkv, D] (element
+    // strides v_sb, v_sh, v_st per batch, head, token; HND otherwise) and out
+    // is [B, Sq, Hq, D]
+    int nhd;
+    int64_t v_sb;
     // dense form: (batch, head) pairs per scheduling bundle (1 .. B * Hq)
     int bundle;
     // smooth_v: per (batch or sequence, kv head) V mean [B * Hkv][D], subtracted

@@ -122,7 +122,9 @@ enum {
 struct PrefillMaps {
     CUtensorMap k;      // f16 key codes [B*Hkv][Lpad][D]
     CUtensorMap v_pre;  // f16 value codes of the prefix [B*Hkv][Vrows][D]
-    CUtensorMap v_ch;   // chunk values: the caller's f16 V [B*Hkv][Sk][D] or v_pre
+    CUtensorMap v_ch;   // chunk values: the caller's f16 V [B*Hkv][Sk][D] or v_pre; with the
+                        // caller's NHD V [B][Sk][Hkv][D] a 4-D map (channel, head, token, batch)
+    int v_ch_4d;        // 1: v_ch is that 4-D map
 };
 
 // Bounded wait that also gives up as soon as another role raised `abort`.
@@ -291,7 +293,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     };
     auto out_row_late = [&](int i) -> int64_t {
         if constexpr (VL) return (qs + i) * p.Hq + hq;
-        return late_pair() * p.Sq + i;
+        const int64_t u = late_pair();
+        if (p.nhd) return ((u / p.Hq) * p.Sq + i) * p.Hq + u % p.Hq;  // [B, Sq, Hq, D]
+        return u * p.Sq + i;
     };
     // smooth_v: this (batch or sequence, kv head)'s V mean row
     auto v_mean_late = [&]() -> const float * {
@@ -414,9 +418,15 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     tc::tma_load_3d(st + a * BN * 128, &maps.k, a * 64, krow0 + w * BN, kz, fb);
                 const CUtensorMap *vm = pre ? &maps.v_pre : &maps.v_ch;
                 const int vrow = krow0 + (pre ? w * BN : (w - wpre) * BN + vch_off);
+                if (!pre && maps.v_ch_4d) {
 #pragma unroll
-                for (int a = 0; a < D / 64; ++a)
-                    tc::tma_load_3d(st + C::KB + a * BN * 128, vm, a * 64, vrow, kz, fb);
+                    for (int a = 0; a < D / 64; ++a)
+                        tc::tma_load_4d(st + C::KB + a * BN * 128, vm, a * 64, kvh, vrow, b, fb);
+                } else {
+#pragma unroll
+                    for (int a = 0; a < D / 64; ++a)
+                        tc::tma_load_3d(st + C::KB + a * BN * 128, vm, a * 64, vrow, kz, fb);
+                }
                 bulk_g2s(st + 2 * C::KB, p.ksc_ws + (int64_t)kz * p.Lpad + krow0 + w * BN, BN * 4,
                          fb);
                 ++issued;
@@ -804,7 +814,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         // before the last P.V) or, with one query tile, the key ring (every
         // MMA has retired by now); 16-byte pieces XOR-swizzled by row.
         const int i_w0 = i - lane;  // this warp's first row (rows are consecutive)
-        const int64_t ostride = VL ? (int64_t)p.Hq * D : (int64_t)D;  // elements between rows
+        const int64_t ostride = (VL || p.nhd) ? (int64_t)p.Hq * D : (int64_t)D;  // between rows
         uint16_t *obase0 = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i_w0) * D;
         uint8_t *ost = (C::QB > 0 ? sm + t * C::QB + (warp & 3) * 4096 : sm + C::OFF_ST + warp * 4096);
         const int nrow_w = min(32, Sq() - i_w0);  // rows of this warp inside the sequence
@@ -888,6 +898,24 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// [B][Sk][Hkv][D] f16 (NHD) as dims (channel, kv head, token, batch) with
+// increasing strides, boxes of 64 channels x 1 head x BN tokens (the same
+// shared-memory tile as the 3-D map's), 128-byte swizzle; tokens past Sk
+// read as zero.
+template <int D>
+bool make_map_nhd(CUtensorMap *tm, const void *base, uint64_t sk, uint64_t hkv, uint64_t batch) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)hkv, (cuuint64_t)sk, (cuuint64_t)batch};
+    cuuint64_t strides[3] = {(cuuint64_t)D * 2, (cuuint64_t)hkv * D * 2,
+                             (cuuint64_t)sk * hkv * D * 2};
+    cuuint32_t box[4] = {64, 1, (cuuint32_t)PCfg<D>::BN, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void *>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // [B*Hkv][rows][D] f16, boxes of 64 channels x BN rows, 128-byte swizzle;
 // rows past `rows` read as zero.
 template <int D>
@@ -915,10 +943,14 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     if (!make_map<D>(&m.k, p.k_ws, p.Lpad, bh)) return cudaErrorInvalidValue;
     if (p.Vrows > 0 && !make_map<D>(&m.v_pre, p.v_ws, p.Vrows, bh)) return cudaErrorInvalidValue;
     if (p.Sk > 0) {
-        if (p.v_bf16 || p.cu_q || p.v_mean)
+        if (p.v_bf16 || p.cu_q || p.v_mean) {
             m.v_ch = m.v_pre;
-        else if (!make_map<D>(&m.v_ch, p.v, p.Sk, bh))
+        } else if (p.nhd) {
+            if (!make_map_nhd<D>(&m.v_ch, p.v, p.Sk, p.Hkv, p.B)) return cudaErrorInvalidValue;
+            m.v_ch_4d = 1;
+        } else if (!make_map<D>(&m.v_ch, p.v, p.Sk, bh)) {
             return cudaErrorInvalidValue;
+        }
     }
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);

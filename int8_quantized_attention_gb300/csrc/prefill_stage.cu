@@ -166,8 +166,10 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
         store_f16x16(p.k_ws + ((int64_t)bh * p.Lpad + row) * D + dc * 16, wk);
         if (dc == 0) p.ksc_ws[(int64_t)bh * p.Lpad + row] = ks;
         __half *vd = p.v_ws + ((int64_t)bh * Vrows + row) * D + dc * 16;
+        // element (b, kv head, token c, channel) of the chunk's V (HND or NHD)
+        const int64_t vo = (int64_t)(bh / p.Hkv) * p.v_sb + (int64_t)(bh % p.Hkv) * p.v_sh +
+                           (int64_t)c * p.v_st + dc * 16;
         if (p.v_mean) {
-            const int64_t vo = ((int64_t)bh * p.Sk + c) * D + dc * 16;
             if (ok) {
                 float v[16];
                 load16f(static_cast<const char *>(p.v) + vo * 2, p.v_bf16 != 0, v);
@@ -180,7 +182,7 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
             uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
             if (ok) {
                 const uint4 *src = reinterpret_cast<const uint4 *>(
-                    static_cast<const __nv_bfloat16 *>(p.v) + ((int64_t)bh * p.Sk + c) * D + dc * 16);
+                    static_cast<const __nv_bfloat16 *>(p.v) + vo);
                 v0 = bf16x8_to_f16x8(src[0]);
                 v1 = bf16x8_to_f16x8(src[1]);
             }

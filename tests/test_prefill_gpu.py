@@ -315,3 +315,50 @@ def test_prefill_smooth_v_paged_prefix(sage):
     o_ref, _ = oracle.prefill(np_(qi), np_(qs), 1, np_(ki), np_(ks), 1, f32(v), causal=True,
                               prefix=pre, smooth_v=True)
     assert_close(f32(out), o_ref)
+
+
+@pytest.mark.parametrize("D", [64, 128, 256])
+@pytest.mark.parametrize("vdt", ["fp16", "bf16"])
+@pytest.mark.parametrize("smooth_v", [False, True])
+@pytest.mark.parametrize("with_prefix", [False, True])
+def test_prefill_nhd_layout_equals_hnd(sage, D, vdt, smooth_v, with_prefix):
+    """[P3]'s tensor_layout: V given as [B, Sk, Hkv, D] and the output written
+    as [B, Sq, Hq, D] give, bit for bit, the HND result transposed -- f16 V
+    read in place (a 4-D tensor map), bf16 V and smooth_v through the
+    staging pass, with and without a paged prefix."""
+    B, Hq, Hkv, S = 2, 4, 2, 300
+    qkv = W.dense_qkv(B, Hq, Hkv, S, S, D, seed=D + 7, dtype=vdt, device="cuda", k_offset_std=2.0)
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 1, 64, True)
+    prefix = None
+    if with_prefix:
+        c = W.paged_cache(B, Hkv, D, [100, 37], seed=D, device="cuda", extra_blocks=3)
+        prefix = _prefix_dict(c, 100)
+    v_nhd = qkv.v.transpose(1, 2).contiguous()
+    out_h, lse_h = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 64, qkv.v, causal=True, q_bias=bias,
+                                          prefix=prefix, return_lse=True, smooth_v=smooth_v)
+    out_n, lse_n = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 64, v_nhd, causal=True, q_bias=bias,
+                                          prefix=prefix, return_lse=True, smooth_v=smooth_v,
+                                          layout="NHD")
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert tuple(out_n.shape) == (B, S, Hq, D)
+    assert torch.equal(out_n, out_h.transpose(1, 2)) and torch.equal(lse_n, lse_h)
+
+
+def test_prefill_nhd_dense_workload_shape_sampled(sage):
+    """NHD at the dense-prefill shape class (f16 V read in place through the
+    4-D map, per-block Q/K, smooth_k, causal, LSE): sampled rows against
+    the oracle, and equal to the HND call."""
+    B, Hq, Hkv, S, D = 1, 8, 8, 4096, 128
+    qkv = W.dense_qkv(B, Hq, Hkv, S, S, D, seed=91, device="cuda", k_offset_std=2.0)
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 128, 64, True)
+    v_nhd = qkv.v.transpose(1, 2).contiguous()
+    out_n, lse_n = sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, v_nhd, causal=True,
+                                          q_bias=bias, return_lse=True, layout="NHD")
+    out_h = sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, qkv.v, causal=True, q_bias=bias)
+    torch.cuda.synchronize()
+    assert torch.equal(out_n.transpose(1, 2), out_h)
+    rows = np.array([0, 1, 127, 128, 2047, 4095])
+    o_ref, l_ref = _oracle(qi, qs, 128, ki, ks, 64, qkv.v, True, bias=bias, rows=rows)
+    assert_close(f32(out_n)[:, rows].transpose(0, 2, 1, 3), o_ref)
+    assert_close(np_(lse_n)[:, :, rows], l_ref, "lse")
