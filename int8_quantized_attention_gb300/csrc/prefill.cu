@@ -30,17 +30,22 @@
 //              per key tile one tcgen05.ld of the whole S row into
 //              registers, per-column K-scale recovery, online softmax with
 //              lazy rescaling (O is rescaled only when the row max grows by
-//              more than 2^8), P written back over S in TMEM.
+//              more than 2^8), P written back over S in TMEM (D <= 128) or
+//              into shared memory (D = 256).
 //   next warp  producer (one thread): per key tile the K and V tiles (TMA
 //              tensor loads) and the per-key K scales (1-D bulk copy) into
-//              one stage of an NST-deep ring.
+//              one stage of an NST-deep ring (D = 256: the K tiles only).
 //   next warp  TMEM owner and MMA issuer (one thread): S_t = Q_t K^T (Q from
 //              shared memory, or from TMEM where it fits), then O_t += P_t V
 //              with P from TMEM.  With two query tiles the two warpgroups
 //              ping-pong: the tensor core works on one tile's MMAs while the
 //              other tile's softmax runs (one issuer keeps each tile's MMAs
 //              together; two issuers interleaving them measured slower).
-//              With one tile (D = 256) S is double-buffered instead.
+//              With one tile (D = 256) S is double-buffered instead, this
+//              warp issues only O += P V (P from shared memory) and
+//   next warp  issues S = Q K^T, and
+//   next warp  streams the V tiles with the per-key K scales through a ring
+//              of their own.
 // Tensor memory (512 columns): O_t at [t*D, t*D+D), S slots from NQ*D.
 // Every mbarrier wait is bounded; a timeout raises a CTA-wide abort flag
 // that makes every other wait give up at once, in-flight copies and MMAs
@@ -64,7 +69,16 @@ template <int D>
 struct PCfg {
     static constexpr int BN = D == 256 ? 64 : 128;
     static constexpr int NQ = D == 256 ? 1 : 2;  // 128-row query tiles per CTA
-    static constexpr int NS = D == 256 ? 2 : 1;  // S buffers per query tile
+    // Wide heads (D = 256): one query tile and three S slots in TMEM (P
+    // written back over S), Q split between TMEM (channels 0-127) and
+    // shared memory (128-255), K and V streamed through separate rings (a K
+    // stage is released when its QK^T retires, a V stage -- V tile and the
+    // per-key K scales -- when its P.V retires) and QK^T and P.V issued by
+    // two threads.  With two S slots (all of Q in TMEM) QK^T(j) had to wait
+    // for P.V(j-2) to retire, a chain of two MMAs and three hand-offs
+    // longer than a key tile's softmax; with three it waits for P.V(j-3).
+    static constexpr bool WIDE = D == 256;
+    static constexpr int NS = WIDE ? 3 : 1;      // S slots per query tile
     static constexpr int NPH = BN / 64;          // P handed to the MMA in 64-key parts
     // softmax warpgroups per query tile: at D = 256 two, each taking half of
     // a row's 64 columns (one warpgroup alone is the critical path there)
@@ -72,50 +86,56 @@ struct PCfg {
     static constexpr int CW = BN / SPLIT;        // S columns per softmax thread
     static constexpr int NSW = NQ * SPLIT;       // softmax warpgroups
     // softmax warpgroups + one warpgroup holding the producer and MMA warps
-    // (and two idle warps, so that register reallocation works per warpgroup)
+    // (and, unless WIDE, two idle warps, so that register reallocation works
+    // per warpgroup)
     static constexpr int THREADS = NSW * 128 + 128;
     // registers: 2 x 128 x 208 + 128 x 88 = 384 x 168, the launch budget
     static constexpr int REG_SOFTMAX = 208, REG_OTHER = 88;
     static_assert(NSW == 1 || NSW * 128 * REG_SOFTMAX + 128 * REG_OTHER <= THREADS * 168,
                   "register split exceeds the launch budget");
     static_assert(SPLIT == 1 || NPH == 1, "split rows hand P over as one part");
-    // Q as the A operand of QK^T: in TMEM when it fits beside O and S
-    // (one query tile at D = 256: O 256 + S 2x64 + Q 128 columns), which
-    // also frees the shared memory of a Q tile for a third ring stage;
-    // otherwise in shared memory (two query tiles fill TMEM with O and S)
-    static constexpr bool QT = NQ * D + NQ * NS * BN + NQ * D / 2 <= 512;
-    static constexpr int QB = QT ? 0 : 128 * D * 2;     // f16 Q tile, swizzled
+    // Q as the A operand of QK^T: in shared memory (two query tiles fill
+    // TMEM with O and S), or (WIDE) channels 0-127 in TMEM and the rest in
+    // shared memory
+    static constexpr int QB = WIDE ? 128 * 128 * 2 : 128 * D * 2;  // f16 Q (part) in smem, swizzled
     static constexpr int KB = BN * D * 2;      // f16 K (or V) tile, swizzled
-    // stage: K tile | V tile | per-key K scales
+    static constexpr int NSV = 2;                                   // V ring depth (WIDE)
+    static constexpr int VSB = (KB + BN * 4 + 1023) / 1024 * 1024;  // V stage (WIDE)
+    // stage: K tile | V tile | per-key K scales (or, WIDE, the K tile alone)
     static constexpr int SB = (2 * KB + BN * 4 + 1023) / 1024 * 1024;
+    static constexpr int KSB = WIDE ? KB : SB;   // ring stride of the K stages
     static constexpr int OFF_ST = NQ * QB;
     static constexpr int NST_FIT = (kSmemLimit - 1024 - OFF_ST - 512) / SB;
-    static constexpr int NST = NST_FIT > 4 ? 4 : NST_FIT;
-    static constexpr int OFF_BAR = OFF_ST + NST * SB;
+    static constexpr int NST = WIDE ? 3 : (NST_FIT > 4 ? 4 : NST_FIT);
+    static constexpr int OFF_V = OFF_ST + NST * KSB;                // WIDE: V ring
+    static constexpr int OFF_BAR = OFF_V + (WIDE ? NSV * VSB : 0);
     static constexpr int OFF_MISC = OFF_BAR + 32 * 8;
     // split rows: partial row max / sum of each half, double-buffered
     static constexpr int OFF_RED = OFF_MISC + 64;
     static constexpr int SMEM = OFF_RED + (SPLIT > 1 ? 2 * NSW * 128 * 4 : 0) + 1024;
     static constexpr uint32_t COL_S = NQ * D;
-    static constexpr uint32_t COL_Q = NQ * D + NQ * NS * BN;  // when QT
+    static constexpr uint32_t COL_Q = NQ * D + NQ * NS * BN;  // WIDE: Q channels 0-127
     static_assert(NST >= 2, "the key ring needs two stages");
-    static_assert(NQ * D + NQ * NS * BN + (QT ? NQ * D / 2 : 0) <= 512,
-                  "tensor memory holds 512 columns");
+    static_assert(NQ * D + NQ * NS * BN + (WIDE ? 64 : 0) <= 512, "tensor memory holds 512 columns");
     static_assert(SMEM <= kSmemLimit, "shared memory budget");
     // epilogue staging: 4 KB per softmax warp, in its tile's Q tile or, with
     // one query tile, in the key ring
-    static_assert(QB == 0 ? NST * SB >= NSW * 4 * 4096 : (QB >= 4 * 4096 && NQ > 1),
-                  "epilogue staging fits");
+    static_assert(NQ == 1 ? NST * KSB >= NSW * 4 * 4096 : QB >= 4 * 4096, "epilogue staging fits");
+    static_assert(!WIDE || (NQ == 1 && SPLIT == 2 && NPH == 1), "wide-head layout");
 };
 
 // barrier slots
 enum {
-    B_KV_FULL = 0,    // [NST] producer: K tile, V tile and per-key scales landed
-    B_KV_EMPTY = 4,   // [NST] MMA: every QK^T and P.V reading the stage retired
+    B_KV_FULL = 0,    // [NST] producer: K tile, V tile and per-key scales landed (WIDE: K tile)
+    B_KV_EMPTY = 4,   // [NST] MMA: every QK^T and P.V reading the stage retired (WIDE: its QK^T)
+    B_S_FREE = 8,     // [NS] WIDE, P.V issuer: the P.V reading an S slot retired
+    B_V_FULL = 11,    // [NSV] WIDE, V producer: V tile and per-key scales landed
+    B_V_EMPTY = 13,   // [NSV] WIDE, P.V issuer: the P.V reading the V stage retired
+    B_DRAIN_QK = 15,  // WIDE, QK^T issuer: every QK^T it issued retired
     B_S_FULL = 16,    // [NQ*NS] MMA: S = Q K^T done
-    B_P_FULL = 20,    // [NQ*NS*NPH] softmax: a 64-key part of P in TMEM (O rescaled)
+    B_P_FULL = 20,    // [NQ*NS*NPH] softmax warps: a 64-key part of P in TMEM (O rescaled)
     B_O_FINAL = 26,   // [NQ] MMA: the last O_t += P_t V done (one phase)
-    B_Q_READY = 28,   // softmax: Q in shared memory
+    B_Q_READY = 28,   // softmax: Q in shared memory / TMEM
     B_DRAIN = 29      // MMA: every issued MMA retired
 };
 
@@ -341,7 +361,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     {
         const int wq = warp >> 2;
         const int ti = threadIdx.x & 127;
-        if constexpr (C::QT) {
+        if constexpr (C::WIDE) {
             const int iq = i0 + (wq / C::SPLIT) * 128 + ti;
             const bool ok = warp < kProducer && iq < Sq();
             const int8_t *src = p.q + (ok ? q_row(iq) * D : 0) + (wq % C::SPLIT) * (D / C::SPLIT);
@@ -349,7 +369,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             for (int k = 0; k < QLD; ++k)
                 qw[k] = ok ? __ldg(reinterpret_cast<const uint4 *>(src) + k) : make_uint4(0, 0, 0, 0);
         } else {
-            static_assert(C::QT || C::SPLIT == 1, "a shared-memory Q tile belongs to one warpgroup");
+            static_assert(C::WIDE || C::SPLIT == 1, "a shared-memory Q tile belongs to one warpgroup");
             const int row0 = i0 + wq * 128;
             const bool sm_thread = warp < kProducer;
             const int8_t *src = p.q + (sm_thread && row0 < Sq() ? q_row(row0) * D : 0);
@@ -372,12 +392,23 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             mbar_init(bar(B_KV_EMPTY + s), 1);
         }
         for (int s = 0; s < NQ * NS; ++s) mbar_init(bar(B_S_FULL + s), 1);
-        for (int s = 0; s < NQ * NS * C::NPH; ++s) mbar_init(bar(B_P_FULL + s), 128 * C::SPLIT);
+        // one arrival per softmax warp (its lanes' stores ordered by the
+        // warp's own synchronisation): 8 arrivals instead of 256 measured
+        // 3 % faster on the dense-prefill workload
+        for (int s = 0; s < NQ * NS * C::NPH; ++s) mbar_init(bar(B_P_FULL + s), 4 * C::SPLIT);
         for (int t = 0; t < NQ; ++t) {
             mbar_init(bar(B_O_FINAL + t), 1);
         }
         mbar_init(bar(B_Q_READY), C::NSW * 128);
         mbar_init(bar(B_DRAIN), 1);
+        if constexpr (C::WIDE) {
+            for (int s = 0; s < NS; ++s) mbar_init(bar(B_S_FREE + s), 1);
+            for (int s = 0; s < C::NSV; ++s) {
+                mbar_init(bar(B_V_FULL + s), 1);
+                mbar_init(bar(B_V_EMPTY + s), 1);
+            }
+            mbar_init(bar(B_DRAIN_QK), 1);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -391,71 +422,96 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     if (warp >= kProducer) {
         if constexpr (C::NSW == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::REG_OTHER));
-    if (warp == kProducer) {
-        // ============================================================ producer
+    if (warp == kProducer || (C::WIDE && warp == kMma + 2)) {
+        // ============================================================ producers
         if (lane == 0 && T > 0) {
-            // one stage per key tile (K, V and the per-key K scales on one
-            // barrier), refilled once every QK^T and P.V that read it retired
-            tc::prefetch_tmap(&maps.k);
-            if (n_pre > 0) tc::prefetch_tmap(&maps.v_pre);
-            if (n_ch > 0) tc::prefetch_tmap(&maps.v_ch);
+            // one stage per key tile, refilled once the MMAs reading it
+            // retired: K, V and the per-key K scales on one barrier, or (WIDE)
+            // the K tile from this warp and V with the scales from warp
+            // kMma + 2, each through its own ring
+            const bool load_k = warp == kProducer;
+            const bool load_v = !C::WIDE || !load_k;
+            if (load_k) tc::prefetch_tmap(&maps.k);
+            if (load_v && n_pre > 0) tc::prefetch_tmap(&maps.v_pre);
+            if (load_v && n_ch > 0) tc::prefetch_tmap(&maps.v_ch);
             // chunk values staged after the prefix (bf16 or smoothed V), or
             // read in place from the caller's f16 V
             const int vch_off = (p.v_bf16 || p.v_mean) ? p.Ppad : 0;
+            const int ns = load_k ? NST : C::NSV;
+            const int full0 = C::WIDE && !load_k ? B_V_FULL : B_KV_FULL;
+            const int empty0 = C::WIDE && !load_k ? B_V_EMPTY : B_KV_EMPTY;
             int issued = 0;
             for (int jj = 0; jj < T; ++jj) {
-                const int s = jj % NST;
-                if (jj >= NST &&
-                    !wait_ab(bar(B_KV_EMPTY + s), (uint32_t)(jj / NST - 1) & 1u, p.err, abort_flag))
+                const int s = jj % ns;
+                if (jj >= ns &&
+                    !wait_ab(bar(empty0 + s), (uint32_t)(jj / ns - 1) & 1u, p.err, abort_flag))
                     break;
                 const bool pre = jj < n_pre;
                 const int w = pre ? jj : wpre + (jj - n_pre);
-                const uint32_t st = sm_a + C::OFF_ST + s * C::SB;
-                const uint32_t fb = bar(B_KV_FULL + s);
-                mbar_arrive_expect_tx(fb, 2 * C::KB + BN * 4);
-#pragma unroll
-                for (int a = 0; a < D / 64; ++a)
-                    tc::tma_load_3d(st + a * BN * 128, &maps.k, a * 64, krow0 + w * BN, kz, fb);
-                const CUtensorMap *vm = pre ? &maps.v_pre : &maps.v_ch;
-                const int vrow = krow0 + (pre ? w * BN : (w - wpre) * BN + vch_off);
-                if (!pre && maps.v_ch_4d) {
+                const uint32_t fb = bar(full0 + s);
+                // K tile at kst; V tile at vst, its per-key scales after it
+                const uint32_t kst = sm_a + C::OFF_ST + s * C::KSB;
+                const uint32_t vst = C::WIDE ? sm_a + C::OFF_V + s * C::VSB : kst + C::KB;
+                mbar_arrive_expect_tx(fb, (load_k ? C::KB : 0) + (load_v ? C::KB + BN * 4 : 0));
+                if (load_k) {
 #pragma unroll
                     for (int a = 0; a < D / 64; ++a)
-                        tc::tma_load_4d(st + C::KB + a * BN * 128, vm, a * 64, kvh, vrow, b, fb);
-                } else {
-#pragma unroll
-                    for (int a = 0; a < D / 64; ++a)
-                        tc::tma_load_3d(st + C::KB + a * BN * 128, vm, a * 64, vrow, kz, fb);
+                        tc::tma_load_3d(kst + a * BN * 128, &maps.k, a * 64, krow0 + w * BN, kz, fb);
                 }
-                bulk_g2s(st + 2 * C::KB, p.ksc_ws + (int64_t)kz * p.Lpad + krow0 + w * BN, BN * 4,
-                         fb);
+                if (load_v) {
+                    const CUtensorMap *vm = pre ? &maps.v_pre : &maps.v_ch;
+                    const int vrow = krow0 + (pre ? w * BN : (w - wpre) * BN + vch_off);
+                    if (!pre && maps.v_ch_4d) {
+#pragma unroll
+                        for (int a = 0; a < D / 64; ++a)
+                            tc::tma_load_4d(vst + a * BN * 128, vm, a * 64, kvh, vrow, b, fb);
+                    } else {
+#pragma unroll
+                        for (int a = 0; a < D / 64; ++a)
+                            tc::tma_load_3d(vst + a * BN * 128, vm, a * 64, vrow, kz, fb);
+                    }
+                    bulk_g2s(vst + C::KB, p.ksc_ws + (int64_t)kz * p.Lpad + krow0 + w * BN, BN * 4,
+                             fb);
+                }
                 ++issued;
             }
-            for (int jj = max(0, issued - NST); jj < issued; ++jj)
-                mbar_wait(bar(B_KV_FULL + jj % NST), (uint32_t)(jj / NST) & 1u, p.err);
+            // wait for the copies still in flight before the CTA may exit
+            for (int jj = max(0, issued - ns); jj < issued; ++jj)
+                mbar_wait(bar(full0 + jj % ns), (uint32_t)(jj / ns) & 1u, p.err);
         }
         __syncwarp();
-    } else if (warp == kMma) {
-        // ============================================================ MMA issuer
+    } else if (warp == kMma || (C::WIDE && warp == kMma + 1)) {
+        // ============================================================ MMA issuers
+        // WIDE: two threads issue, warp kMma + 1 the QK^T of each key tile and
+        // warp kMma the P.V.  The tensor core takes only a couple of MMAs
+        // ahead of execution, so every barrier wait of a single issuer (a few
+        // hundred cycles per key tile) left it idle; with two issuers one
+        // thread's waits overlap the other's MMAs.
         if (lane == 0 && T > 0) {
             const uint32_t idq = tc::idesc_f16(128, BN, false, false);
             const uint32_t idp = tc::idesc_f16(128, D, false, true);  // P.V in f16
             // descriptors built once; a k-step adds its byte offset >> 4
             const uint64_t qd0 = tc::sdesc_sw128(sm_a, 16, 1024);
             const uint64_t kd0 = tc::sdesc_sw128(sm_a + C::OFF_ST, 16, 1024);
-            const uint64_t vd0 = tc::sdesc_sw128(sm_a + C::OFF_ST + C::KB, BN * 128, 1024);
+            const uint64_t vd0 = tc::sdesc_sw128(sm_a + (C::WIDE ? C::OFF_V : C::OFF_ST + C::KB),
+                                                 BN * 128, 1024);
             auto qk = [&](int jj, int t) {
-                const int slot = t * NS + (NS == 1 ? 0 : (jj & 1));
+                const int slot = t * NS + jj % NS;
                 const uint64_t qd = qd0 + (uint64_t)((t * C::QB) >> 4);
-                const uint64_t kd = kd0 + (uint64_t)(((jj % NST) * C::SB) >> 4);
+                const uint64_t kd = kd0 + (uint64_t)(((jj % NST) * C::KSB) >> 4);
                 const uint32_t d = tmem + C::COL_S + slot * BN;
-                if constexpr (C::QT) {
-                    // A = Q from TMEM: column c of lane r holds f16 channels 2c, 2c+1
-                    const uint32_t qa = tmem + C::COL_Q + t * (D / 2);
+                if constexpr (C::WIDE) {
+                    // channels 0-127: A = Q from TMEM (column c of lane r holds
+                    // f16 channels 2c, 2c+1); 128-255: A = Q from shared memory
+                    const uint32_t qa = tmem + C::COL_Q;
                     tc::mma_ts(d, qa, kd, idq, 0u);
 #pragma unroll
-                    for (int ks = 1; ks < D / 16; ++ks)
+                    for (int ks = 1; ks < 8; ++ks)
                         tc::mma_ts_acc(d, qa + ks * 8,
+                                       kd + (((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4), idq);
+#pragma unroll
+                    for (int ks = 8; ks < D / 16; ++ks)
+                        tc::mma_ss_acc(d, qd + ((((ks - 8) >> 2) * (128 * 128) + (ks & 3) * 32) >> 4),
                                        kd + (((ks >> 2) * (BN * 128) + (ks & 3) * 32) >> 4), idq);
                 } else {
                     tc::mma_ss(d, qd, kd, idq, 0u);
@@ -469,9 +525,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             // O_t += P_t V_j in 64-key parts, each issued as soon as the
             // softmax has stored that part of P (the first part also needs V)
             auto pv = [&](int jj, int t) -> bool {
-                const int slot = t * NS + (NS == 1 ? 0 : (jj & 1));
-                const uint32_t sp = NS == 1 ? (uint32_t)jj & 1u : (uint32_t)(jj >> 1) & 1u;
-                const uint64_t vd = vd0 + (uint64_t)(((jj % NST) * C::SB) >> 4);
+                const int slot = t * NS + jj % NS;
+                const uint32_t sp = (uint32_t)(jj / NS) & 1u;
+                const uint64_t vd = C::WIDE ? vd0 + (uint64_t)(((jj % C::NSV) * C::VSB) >> 4)
+                                            : vd0 + (uint64_t)(((jj % NST) * C::SB) >> 4);
                 const uint32_t pt = tmem + C::COL_S + slot * BN;
                 const uint32_t o = tmem + t * D;
 #pragma unroll
@@ -497,35 +554,58 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 tc::fence_after();
                 return ok;
             };
-            bool ok = wait_ab(bar(B_Q_READY), 0, p.err, abort_flag) && k_ready(0);
-            if (ok) {
+            if constexpr (C::WIDE) {
+                if (warp == kMma + 1) {
+                    // S_j = Q K_j^T into slot j % 3 once K_j landed and the
+                    // P.V of key tile j - 3 (the slot's last reader) retired;
+                    // the K stage is free when this QK^T retires
+                    bool ok = wait_ab(bar(B_Q_READY), 0, p.err, abort_flag);
+                    for (int jj = 0; ok && jj < T; ++jj) {
+                        if (!(ok = k_ready(jj))) break;
+                        if (jj >= NS && !(ok = wait_ab(bar(B_S_FREE + jj % NS),
+                                                       (uint32_t)(jj / NS - 1) & 1u, p.err, abort_flag)))
+                            break;
+                        tc::fence_after();
+                        qk(jj, 0);
+                        tc::commit(bar(B_KV_EMPTY + jj % NST));
+                    }
+                    tc::commit(bar(B_DRAIN_QK));
+                    mbar_wait(bar(B_DRAIN_QK), 0, p.err);
+                } else {
+                    // O += P_j V_j once V_j landed and P_j is in TMEM; then V
+                    // stage j and S slot j % 3 are free
+                    bool ok = true;
+                    for (int jj = 0; ok && jj < T; ++jj) {
+                        if (!(ok = wait_ab(bar(B_V_FULL + jj % C::NSV), (uint32_t)(jj / C::NSV) & 1u,
+                                           p.err, abort_flag)))
+                            break;
+                        if (!(ok = pv(jj, 0))) break;
+                        tc::commit(bar(B_V_EMPTY + jj % C::NSV));
+                        tc::commit(bar(B_S_FREE + jj % NS));
+                    }
+                    tc::commit(bar(B_DRAIN));
+                    mbar_wait(bar(B_DRAIN), 0, p.err);
+                }
+            } else {
+                // one issuer; per query tile: O_t += P_t V_j, then S_t = Q_t K_{j+1}
+                bool ok = wait_ab(bar(B_Q_READY), 0, p.err, abort_flag) && k_ready(0);
+                if (ok) {
 #pragma unroll
-                for (int t = 0; t < NQ; ++t) qk(0, t);
-            }
-            for (int jj = 0; ok && jj < T; ++jj) {
-                const int s = jj % NST;
-                if constexpr (NS == 1) {
-                    // per query tile: O_t += P_t V_j, then S_t = Q_t K_{j+1}
+                    for (int t = 0; t < NQ; ++t) qk(0, t);
+                }
+                for (int jj = 0; ok && jj < T; ++jj) {
                     for (int t = 0; t < NQ; ++t) {
                         if (!(ok = pv(jj, t))) break;
-                        if (t == NQ - 1) tc::commit(bar(B_KV_EMPTY + s));
+                        if (t == NQ - 1) tc::commit(bar(B_KV_EMPTY + jj % NST));
                         if (jj + 1 < T) {
                             if (t == 0 && !(ok = k_ready(jj + 1))) break;
                             qk(jj + 1, t);
                         }
                     }
-                } else {
-                    // one query tile, S double-buffered: S(j+1) runs under softmax(j)
-                    if (jj + 1 < T) {
-                        if (!(ok = k_ready(jj + 1))) break;
-                        qk(jj + 1, 0);
-                    }
-                    if (!(ok = pv(jj, 0))) break;
-                    tc::commit(bar(B_KV_EMPTY + s));
                 }
+                tc::commit(bar(B_DRAIN));
+                mbar_wait(bar(B_DRAIN), 0, p.err);  // every issued MMA has retired
             }
-            tc::commit(bar(B_DRAIN));
-            mbar_wait(bar(B_DRAIN), 0, p.err);  // every issued MMA has retired
         }
         __syncwarp();
     }
@@ -558,25 +638,31 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             }
         };
         {
-            if constexpr (C::QT) {
-                // Q row int8 -> exact f16 pairs in this thread's TMEM lane
-                // (each of a row's SPLIT threads writes its share of channels)
+            if constexpr (C::WIDE) {
+                if (hc == 0) {
+                    // channels 0-127 -> exact f16 pairs in this thread's TMEM lane
 #pragma unroll
-                for (int cc = 0; cc < D / 64 / SPLIT; ++cc) {
-                    const int c = hc * (D / 64 / SPLIT) + cc;
-                    uint32_t v[32];
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t v[32];
 #pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const uint4 w = qw[cc * 4 + u];
-                        i8x4_to_f16x4(w.x, v[u * 8 + 0], v[u * 8 + 1]);
-                        i8x4_to_f16x4(w.y, v[u * 8 + 2], v[u * 8 + 3]);
-                        i8x4_to_f16x4(w.z, v[u * 8 + 4], v[u * 8 + 5]);
-                        i8x4_to_f16x4(w.w, v[u * 8 + 6], v[u * 8 + 7]);
+                        for (int u = 0; u < 4; ++u) {
+                            const uint4 w = qw[c * 4 + u];
+                            i8x4_to_f16x4(w.x, v[u * 8 + 0], v[u * 8 + 1]);
+                            i8x4_to_f16x4(w.y, v[u * 8 + 2], v[u * 8 + 3]);
+                            i8x4_to_f16x4(w.z, v[u * 8 + 4], v[u * 8 + 5]);
+                            i8x4_to_f16x4(w.w, v[u * 8 + 6], v[u * 8 + 7]);
+                        }
+                        tc::st32(tmem + lane_base + C::COL_Q + c * 32, v);
                     }
-                    tc::st32(tmem + lane_base + C::COL_Q + t * (D / 2) + c * 32, v);
+                    tc::wait_st();
+                    tc::fence_before();
+                } else {
+                    // channels 128-255 -> f16 in the swizzled K-major
+                    // shared-memory tile (two 64-channel atom columns)
+#pragma unroll
+                    for (int m = 0; m < QLD; ++m) store_piece<128>(sm, r, m, qw[m]);
+                    tc::fence_proxy_async();  // st.shared -> visible to the tensor core
                 }
-                tc::wait_st();
-                tc::fence_before();
             } else {
                 // Q row int8 -> f16 in the swizzled K-major layout of the A operand
                 uint8_t *qt = sm + t * C::QB;
@@ -612,14 +698,19 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 continue;
             }
             const int s = jj % NST;
-            const int slot = t * NS + (NS == 1 ? 0 : (jj & 1));
-            const uint32_t sp = NS == 1 ? (uint32_t)jj & 1u : (uint32_t)(jj >> 1) & 1u;
+            const int slot = t * NS + jj % NS;
+            const uint32_t sp = (uint32_t)(jj / NS) & 1u;
             const bool pre = jj < n_pre;
             const int key0 = pre ? jj * BN : (jj - n_pre) * BN;  // within its source
             const int nvalid = min(BN, (pre ? P : Sk()) - key0);
             const int kg0 = pre ? key0 : P + key0;  // over prefix + chunk
             bool ok = wait_ab(bar(B_S_FULL + slot), sp, p.err, abort_flag);
-            ok = ok && wait_ab(bar(B_KV_FULL + s), (uint32_t)(jj / NST) & 1u, p.err, abort_flag);
+            // the stage holding this tile's per-key K scales
+            if constexpr (C::WIDE)
+                ok = ok && wait_ab(bar(B_V_FULL + jj % C::NSV), (uint32_t)(jj / C::NSV) & 1u, p.err,
+                                   abort_flag);
+            else
+                ok = ok && wait_ab(bar(B_KV_FULL + s), (uint32_t)(jj / NST) & 1u, p.err, abort_flag);
             if (!__all_sync(0xffffffffu, ok)) {
                 if constexpr (SPLIT == 1) break;
                 alive = false;
@@ -628,8 +719,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             }
             tc::fence_after();
             const uint32_t s_t = tmem + lane_base + C::COL_S + slot * BN;
-            const uint8_t *stg = sm + C::OFF_ST + s * C::SB;
-            const float4 *ksc4 = reinterpret_cast<const float4 *>(stg + 2 * C::KB) + c0 / 4;
+            const uint8_t *ksc = C::WIDE ? sm + C::OFF_V + (jj % C::NSV) * C::VSB + C::KB
+                                         : sm + C::OFF_ST + s * C::SB + 2 * C::KB;
+            const float4 *ksc4 = reinterpret_cast<const float4 *>(ksc) + c0 / 4;
             uint32_t x[CW];
             if constexpr (CW >= 32) {
 #pragma unroll
@@ -720,12 +812,11 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             if (__any_sync(0xffffffffu, fix)) {
                 // O holds P.V of earlier tiles scaled to the old max: once the
                 // last P.V retired, rescale this thread's columns of the row
-                if (NS == 2) {
-                    // with one query tile the V stage of tile jj-1 is released
-                    // exactly when P.V(jj-1) retires; S(jj) alone does not
-                    // imply it (QK(jj) was issued before P.V(jj-1))
-                    const bool w = wait_ab(bar(B_KV_EMPTY + (jj - 1) % NST),
-                                           (uint32_t)((jj - 1) / NST) & 1u, p.err, abort_flag);
+                if constexpr (C::WIDE) {
+                    // P.V(jj-1) frees its S slot when it retires; S(jj) alone
+                    // does not imply it (QK(jj) did not wait for P.V(jj-1))
+                    const bool w = wait_ab(bar(B_S_FREE + (jj - 1) % NS),
+                                           (uint32_t)((jj - 1) / NS) & 1u, p.err, abort_flag);
                     if (!__all_sync(0xffffffffu, w)) {
                         if constexpr (SPLIT == 1) break;
                         alive = false;  // this tile's pair barrier is behind us
@@ -779,7 +870,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     tc::st16(pcol, *reinterpret_cast<uint32_t(*)[16]>(pk));
                 tc::wait_st();
                 tc::fence_before();
-                mbar_arrive(bar(B_P_FULL + slot * C::NPH + (c0 + GW * g) / 64));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(B_P_FULL + slot * C::NPH + (c0 + GW * g) / 64));
             }
             l += (ls01.x + ls01.y) + (ls23.x + ls23.y);
             done = jj + 1;
@@ -816,7 +908,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         const int i_w0 = i - lane;  // this warp's first row (rows are consecutive)
         const int64_t ostride = (VL || p.nhd) ? (int64_t)p.Hq * D : (int64_t)D;  // between rows
         uint16_t *obase0 = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i_w0) * D;
-        uint8_t *ost = (C::QB > 0 ? sm + t * C::QB + (warp & 3) * 4096 : sm + C::OFF_ST + warp * 4096);
+        uint8_t *ost = (NQ > 1 ? sm + t * C::QB + (warp & 3) * 4096 : sm + C::OFF_ST + warp * 4096);
         const int nrow_w = min(32, Sq() - i_w0);  // rows of this warp inside the sequence
         // two 32-column pieces of O per tensor-memory round trip
         constexpr int NCH = D / 32 / SPLIT;
