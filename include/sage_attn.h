@@ -405,6 +405,7 @@ typedef struct sage_prefill_args {
     int smooth_v;                   /* subtract the chunk's V mean, add it back to o */
     float *v_mean;                  /* optional out [B, Hkv, D] fp32 (smooth_v) */
     int layout;                     /* SAGE_LAYOUT_HND (0) or SAGE_LAYOUT_NHD (1), below */
+    int tail_split;                 /* SAGE_TAIL_SPLIT_AUTO (0) or SAGE_TAIL_SPLIT_OFF (1), below */
 } sage_prefill_args_t;
 
 /* Layout of the prefill's f16/bf16 tensors ([P3] tensor_layout): HND keeps
@@ -413,13 +414,28 @@ typedef struct sage_prefill_args {
  * head-major in both (the layout sage_quant_int8 writes). */
 enum { SAGE_LAYOUT_HND = 0, SAGE_LAYOUT_NHD = 1 };
 
-/* Workspace of sage_attn_prefill (host only): the tensor cores of sm_103a
- * have no INT8 mode, so each call first expands the INT8 codes it reads --
- * chunk K, and the paged prefix's K and V gathered through the block table
- * -- into an exact f16 copy, together with per-key scales; bf16 chunk V is
- * rounded to f16 there too.  Returns the bytes needed (0 never happens for a
- * valid request).  The stored representation stays INT8; the copy is scratch
- * of the call. */
+/* Split of the last wave (head_dim 256).  A CTA there takes one 128-row query
+ * tile.  When the tiles leave the last wave of CTAs partly empty and carry
+ * about equal work (no causal mask, or a chunk over much longer history),
+ * AUTO splits that wave's tiles by key range into up to 8 parts of at least
+ * 16 key tiles.  Each part is one CTA.
+ * A second kernel merges the parts with the split-K combine ("INT8 QK MMAC
+ * on gfx936 DCU", section 4).  The parts' results are normalised outputs and
+ * their base-2 LSEs, kept in the workspace.  The result is the same attention
+ * to within rounding, but not bit-for-bit the unsplit computation.  OFF never
+ * splits.  The choice changes the workspace size, so pass the same args to
+ * sage_attn_prefill_workspace_size. */
+enum { SAGE_TAIL_SPLIT_AUTO = 0, SAGE_TAIL_SPLIT_OFF = 1 };
+
+/* Workspace of sage_attn_prefill (host only).  The tensor cores of sm_103a
+ * have no INT8 mode, so each call first expands the INT8 codes it reads
+ * into an exact f16 copy, together with per-key scales.  Those codes are
+ * chunk K, and the paged prefix's K and V gathered through the block table.
+ * bf16 chunk V is rounded to f16 there too.  With a tail split (above) the
+ * workspace also holds the split tiles' partial results.  Returns the bytes
+ * needed; 0 only for an invalid request.  The stored representation stays
+ * INT8; the copy is scratch of the call.  The size depends on the current
+ * device's SM count through the tail split. */
 size_t sage_attn_prefill_workspace_size(const sage_prefill_args_t *args);
 
 /* workspace: device buffer of at least sage_attn_prefill_workspace_size()

@@ -57,7 +57,7 @@ class PrefillArgs(ctypes.Structure):
                 ("block_table", _vp), ("prefix_lens", _vp),
                 ("num_blocks", _i), ("max_blocks", _i), ("max_prefix_len", _i),
                 ("causal", _i), ("sm_scale", _f), ("out", _vp), ("out_dtype", _i), ("lse", _vp),
-                ("smooth_v", _i), ("v_mean", _vp), ("layout", _i)]
+                ("smooth_v", _i), ("v_mean", _vp), ("layout", _i), ("tail_split", _i)]
 
 
 class PrefillVarlenArgs(ctypes.Structure):
@@ -460,7 +460,7 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
                       out_dtype=None, return_lse: bool = False, debug_scores=None,
                       workspace: Optional[torch.Tensor] = None, out=None, lse=None,
                       smooth_v: bool = False, v_mean: Optional[torch.Tensor] = None,
-                      layout: str = "HND", stream=None):
+                      layout: str = "HND", tail_split: bool = True, stream=None):
     """INT8-QK prefill attention over an optional paged INT8 prefix + a chunk.
 
     q_int8 [B,Hq,Sq,D]; q_scale [B,Hq,ceil(Sq/q_block)]; k_int8 [B,Hkv,Sk,D];
@@ -470,7 +470,9 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
     chunk's V mean from every value and adds it back to the output; v_mean
     ([B, Hkv, D] fp32, optional) receives that mean.  layout "NHD" takes v
     as [B,Sk,Hkv,D] and returns out as [B,Sq,Hq,D] (the INT8 codes, scales,
-    q_bias and lse stay head-major).
+    q_bias and lse stay head-major).  tail_split=False keeps every query tile
+    in one CTA (SAGE_TAIL_SPLIT_OFF); by default the library may split the
+    last wave's tiles by key range (head_dim 256), equal to within rounding.
     """
     B, Hq, Sq, D = q_int8.shape
     Hkv, Sk = k_int8.shape[1], k_int8.shape[2]
@@ -525,6 +527,7 @@ def sage_attn_prefill(q_int8, q_scale, q_block: int, k_int8, k_scale, k_block: i
         _need(v_mean, torch.float32, "v_mean")
     a.smooth_v, a.v_mean = int(bool(smooth_v)), _ptr(v_mean)
     a.layout = 1 if nhd else 0
+    a.tail_split = 0 if tail_split else 1
     need = int(lib().sage_attn_prefill_workspace_size(ctypes.byref(a)))
     if workspace is None or workspace.numel() * workspace.element_size() < need:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q_int8.device)

@@ -630,16 +630,26 @@ static sage_status_t check_prefill(const sage_prefill_args_t *a, int *qs_out, in
     if (a->layout != SAGE_LAYOUT_HND && a->layout != SAGE_LAYOUT_NHD)
         return fail(SAGE_ERR_UNSUPPORTED, "layout %d is not SAGE_LAYOUT_HND or SAGE_LAYOUT_NHD",
                     a->layout);
+    if (a->tail_split != SAGE_TAIL_SPLIT_AUTO && a->tail_split != SAGE_TAIL_SPLIT_OFF)
+        return fail(SAGE_ERR_INVALID_ARG, "tail_split %d is not SAGE_TAIL_SPLIT_AUTO or _OFF",
+                    a->tail_split);
     *qs_out = qs;
     *ks_out = ks;
     return SAGE_OK;
+}
+
+// The tail split of a (checked) request on the current device.
+static sage::PrefillSplit prefill_split_of(const sage_prefill_args_t *a) {
+    if (a->tail_split == SAGE_TAIL_SPLIT_OFF) return sage::PrefillSplit{0, 0, 0};
+    return sage::prefill_split(a->B, a->Hq, a->Sq, a->D, a->max_prefix_len + a->Sk,
+                               a->causal != 0, sm_count());
 }
 
 SAGE_API size_t sage_attn_prefill_workspace_size(const sage_prefill_args_t *a) {
     int qs = 0, ks = 0;
     if (check_prefill(a, &qs, &ks) != SAGE_OK) return 0;
     return sage::prefill_layout(a->B, a->Hkv, a->Sk, a->D, a->max_prefix_len,
-                                a->v_dtype == SAGE_BF16, a->smooth_v != 0)
+                                a->v_dtype == SAGE_BF16, a->smooth_v != 0, prefill_split_of(a))
         .bytes;
 }
 
@@ -669,9 +679,10 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
         return fail(SAGE_ERR_UNSUPPORTED, "smooth_v supports at most 65535 (batch, kv head) pairs");
     if (a->v_mean && !aligned(a->v_mean, 16))
         return fail(SAGE_ERR_INVALID_ARG, "v_mean must be 16-byte aligned");
+    const sage::PrefillSplit split = prefill_split_of(a);
     const sage::PrefillLayout L = sage::prefill_layout(a->B, a->Hkv, a->Sk, a->D,
                                                        a->max_prefix_len, a->v_dtype == SAGE_BF16,
-                                                       a->smooth_v != 0);
+                                                       a->smooth_v != 0, split);
     if (!workspace || workspace_bytes < L.bytes)
         return fail(SAGE_ERR_INVALID_ARG, "workspace too small: need %zu bytes", L.bytes);
     if (!aligned(workspace, 256)) return fail(SAGE_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
@@ -712,6 +723,11 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
     p.k_ws = reinterpret_cast<__half *>(w + L.off_k);
     p.v_ws = L.Vrows ? reinterpret_cast<__half *>(w + L.off_v) : nullptr;
     p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);
+    if (split.parts > 0) {
+        p.split_f = split.full, p.split_k = split.parts, p.split_tail = split.tail;
+        p.part_o = reinterpret_cast<float *>(w + L.off_part_o);
+        p.part_lse = reinterpret_cast<float *>(w + L.off_part_lse);
+    }
     cudaStream_t cst = static_cast<cudaStream_t>(stream);
     sage::LaunchLog stage_log;
     cudaError_t e = cudaSuccess;

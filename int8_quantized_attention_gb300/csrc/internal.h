@@ -206,7 +206,23 @@ struct PrefillParams {
     // smooth_v: per (batch or sequence, kv head) V mean [B * Hkv][D], subtracted
     // from the staged values and added back to the output; null when off
     const float *v_mean;
+    // dense form, D = 256: the last, partly filled wave's query tiles split by
+    // key range (split_k parts each; 0 = no split).  CTAs [0, split_f) take
+    // whole query tiles; CTA split_f + u * split_k + j takes part j of tile
+    // split_f + u (u < split_tail) and writes its normalised O and base-2 LSE
+    // to part_o [slot][128][D] / part_lse [slot][128] (slot = u * split_k + j),
+    // which the merge kernel combines into out and lse.
+    int split_f, split_k, split_tail;
+    float *part_o, *part_lse;
 };
+
+// How the dense prefill splits its last wave: `full` whole query tiles, then
+// `tail` tiles split into `parts` key ranges each (parts == 0: no split).
+struct PrefillSplit {
+    int full, tail, parts;
+};
+// keys: a query tile's largest key count (prefix + chunk); sms: the device's SMs
+PrefillSplit prefill_split(int B, int Hq, int Sq, int D, int keys, bool causal, int sms);
 
 // Pairs per bundle of the dense prefill's CTA order: as many KV heads'
 // staged keys and values (f16, rows each) as fit in a share of L2, times
@@ -215,11 +231,13 @@ int prefill_bundle(int B, int Hq, int group, int rows, int D);
 
 struct PrefillLayout {
     int BN, Ppad, Lpad, Vrows;
-    size_t off_k, off_v, off_ksc, off_vmean, bytes;  // off_vmean: smooth_v's mean [B*Hkv][D]
+    // off_vmean: smooth_v's mean [B*Hkv][D]; off_part_o / off_part_lse: the
+    // split tail's partial results
+    size_t off_k, off_v, off_ksc, off_vmean, off_part_o, off_part_lse, bytes;
 };
 
 PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16,
-                             bool smooth_v);
+                             bool smooth_v, const PrefillSplit &split);
 PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D, bool smooth_v);
 cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, LaunchLog &log);
 cudaError_t launch_prefill(const PrefillParams &p, cudaStream_t st, LaunchLog &log);

@@ -195,6 +195,33 @@ __device__ __forceinline__ void store_piece(uint8_t *tile, int r, int dc, uint4 
     *reinterpret_cast<uint4 *>(row + ((((c8 + 1) & 7) ^ (r & 7)) << 4)) = h1;
 }
 
+// Dense form: query tile index -> (batch, head, query tile).  One linear
+// index over (batch, head) pairs taken in bundles of p.bundle (whose staged
+// keys fit in L2 together); within a bundle the heaviest (causal) query
+// tiles of all its pairs come first, so that no heavy tile is left to run
+// alone at the end of the grid.  Returns the pair index b * Hq + hq.
+__device__ __forceinline__ int dense_tile(const PrefillParams &p, int QR, int item, int &ct) {
+    const int nct = (p.Sq + QR - 1) / QR;
+    const int per = nct * p.bundle;
+    const int bun = item / per;
+    const int nb = min(p.bundle, p.B * p.Hq - bun * p.bundle);
+    const int r = item - bun * per;
+    ct = nct - 1 - r / nb;
+    return bun * p.bundle + r % nb;
+}
+
+// Dense form: CTA index -> query tile index; part = the CTA's key range of a
+// split tail tile, or -1 for a whole tile.
+__device__ __forceinline__ int split_item(const PrefillParams &p, int L, int &part) {
+    part = -1;
+    if (p.split_k > 0 && L >= p.split_f) {
+        const int v = L - p.split_f;
+        part = v % p.split_k;
+        return p.split_f + v / p.split_k;
+    }
+    return L;
+}
+
 // VL: a packed variable-length batch (rows and keys located through
 // cu_seqlens); the dense instantiation keeps its addressing in closed form.
 template <int D, bool VL>
@@ -216,6 +243,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     constexpr int QR = 128 * NQ;  // query rows per CTA
     int b, hq, ct;
+    int part = -1;  // dense form, D = 256: this CTA's part of a split query tile
     int cq0 = 0, cq1 = 0, ck0 = 0, ck1 = 0;  // packed batch: this sequence's offsets
     if constexpr (VL) {
         // one linear index, heads fastest: the CTAs of a tile slot for every
@@ -233,18 +261,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         cq0 = p.cu_q[b], cq1 = p.cu_q[b + 1], ck0 = p.cu_k[b], ck1 = p.cu_k[b + 1];
         ct = g - (int)varlen_group0(cq0 < 0 ? 0 : cq0, b, QR);  // reversed below
     } else {
-        // one linear CTA index over (batch, head) pairs taken in bundles of
-        // p.bundle (whose staged keys fit in L2 together): within a bundle
-        // the heaviest (causal) query tiles of all its pairs come first, so
-        // that no heavy tile is left to run alone at the end of the grid
-        const int nct = (p.Sq + QR - 1) / QR;
-        const int L = blockIdx.x;
-        const int per = nct * p.bundle;
-        const int bun = L / per;
-        const int nb = min(p.bundle, p.B * p.Hq - bun * p.bundle);
-        const int r = L - bun * per;
-        ct = nct - 1 - r / nb;
-        const int u = bun * p.bundle + r % nb;
+        int item = blockIdx.x;
+        if constexpr (C::WIDE) item = split_item(p, item, part);
+        const int u = dense_tile(p, QR, item, ct);
         b = u / p.Hq;
         hq = u % p.Hq;
     }
@@ -302,10 +321,12 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     auto late_pair = [&]() -> int64_t {
         int L;
         asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(L));
-        const int per = (p.Sq + QR - 1) / QR * p.bundle;
-        const int bun = L / per;
-        const int nb = min(p.bundle, p.B * p.Hq - bun * p.bundle);
-        return (int64_t)bun * p.bundle + (L - bun * per) % nb;
+        if constexpr (C::WIDE) {
+            int pt;
+            L = split_item(p, L, pt);
+        }
+        int c;
+        return dense_tile(p, QR, L, c);
     };
     auto q_row_late = [&](int i) -> int64_t {
         if constexpr (VL) return vq_row0 + i;
@@ -343,7 +364,15 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         n_pre = min((P + BN - 1) / BN, kmax / BN + 1);
         if (kmax >= P) n_ch = min((Sk() + BN - 1) / BN, (kmax - P) / BN + 1);
     }
-    const int T = n_pre + n_ch;
+    int T = n_pre + n_ch;
+    // a part of a split query tile takes key tiles [j0, j0 + T) of it
+    int j0 = 0;
+    if constexpr (C::WIDE && !VL) {
+        if (part >= 0) {
+            j0 = (int)((int64_t)part * T / p.split_k);
+            T = (int)((int64_t)(part + 1) * T / p.split_k) - j0;
+        }
+    }
     const int wpre = p.Ppad / BN;  // first chunk tile in the workspace
 
     // The softmax threads issue their query loads now: they land while the
@@ -446,8 +475,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 if (jj >= ns &&
                     !wait_ab(bar(empty0 + s), (uint32_t)(jj / ns - 1) & 1u, p.err, abort_flag))
                     break;
-                const bool pre = jj < n_pre;
-                const int w = pre ? jj : wpre + (jj - n_pre);
+                const int kt = j0 + jj;  // key tile
+                const bool pre = kt < n_pre;
+                const int w = pre ? kt : wpre + (kt - n_pre);
                 const uint32_t fb = bar(full0 + s);
                 // K tile at kst; V tile at vst, its per-key scales after it
                 const uint32_t kst = sm_a + C::OFF_ST + s * C::KSB;
@@ -700,8 +730,9 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const int s = jj % NST;
             const int slot = t * NS + jj % NS;
             const uint32_t sp = (uint32_t)(jj / NS) & 1u;
-            const bool pre = jj < n_pre;
-            const int key0 = pre ? jj * BN : (jj - n_pre) * BN;  // within its source
+            const int kt = j0 + jj;  // key tile
+            const bool pre = kt < n_pre;
+            const int key0 = pre ? kt * BN : (kt - n_pre) * BN;  // within its source
             const int nvalid = min(BN, (pre ? P : Sk()) - key0);
             const int kg0 = pre ? key0 : P + key0;  // over prefix + chunk
             bool ok = wait_ab(bar(B_S_FULL + slot), sp, p.err, abort_flag);
@@ -895,77 +926,104 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             tc::fence_after();
         }
         const float inv = l > 0.0f ? 1.0f / l : 0.0f;
-        const int64_t orow = q_row_late(i);
-        // smooth_v: the V mean goes back onto rows that saw a key
-        const float *vmu = (p.v_mean && l > 0.0f) ? v_mean_late() : nullptr;
-        // The O rows go out through shared memory: each warp stages its 32
-        // rows, 64 channels at a time, then stores 4 rows' 128-byte pieces
-        // per instruction (one row per thread made every store instruction
-        // touch 32 rows, most of the epilogue's time).  The staging space is
-        // this tile's Q tile (not read since its last QK^T, which retired
-        // before the last P.V) or, with one query tile, the key ring (every
-        // MMA has retired by now); 16-byte pieces XOR-swizzled by row.
-        const int i_w0 = i - lane;  // this warp's first row (rows are consecutive)
-        const int64_t ostride = (VL || p.nhd) ? (int64_t)p.Hq * D : (int64_t)D;  // between rows
-        uint16_t *obase0 = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i_w0) * D;
-        uint8_t *ost = (NQ > 1 ? sm + t * C::QB + (warp & 3) * 4096 : sm + C::OFF_ST + warp * 4096);
-        const int nrow_w = min(32, Sq() - i_w0);  // rows of this warp inside the sequence
-        // two 32-column pieces of O per tensor-memory round trip
-        constexpr int NCH = D / 32 / SPLIT;
-        static_assert(NCH % 2 == 0, "O pieces go in pairs");
+        if (part >= 0) {
+            // a part of a split query tile: its normalised O (f32, without
+            // the smooth_v mean) and base-2 LSE, for the merge kernel; each
+            // thread writes its row's channels straight from TMEM
+            const int64_t slot = (int64_t)blockIdx.x - p.split_f;
+            constexpr int NPC = D / 32 / SPLIT;  // 32-channel pieces of this thread
+            float *po = p.part_o + (slot * 128 + r) * D + hc * NPC * 32;
 #pragma unroll 1
-        for (int c2 = 0; c2 < NCH; c2 += 2) {
-            uint32_t oo[2][32];
-            if (have) {
-                tc::ld32(tmem + lane_base + t * D + (hc * NCH + c2) * 32, oo[0]);
-                tc::ld32(tmem + lane_base + t * D + (hc * NCH + c2 + 1) * 32, oo[1]);
-                tc::wait_ld();
-            } else {
-#pragma unroll
-                for (int e = 0; e < 32; ++e) oo[0][e] = oo[1][e] = 0u;
-            }
-            uint32_t pk[32];  // this row's 64 channels, f16 / bf16 pairs
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const uint32_t(&o)[32] = oo[h2];
-                if (vmu) {
-                    const float4 *m4 = reinterpret_cast<const float4 *>(vmu + (hc * NCH + c2 + h2) * 32);
-#pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        const float4 m = m4[e / 2];
-                        const float2 v0 = ffma2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv),
-                                                make_float2(m.x, m.y));
-                        const float2 v1 = ffma2(u2f2(o[2 * e + 2], o[2 * e + 3]),
-                                                make_float2(inv, inv), make_float2(m.z, m.w));
-                        pk[h2 * 16 + e] = pack2(v0.x, v0.y, p.out_bf16 != 0);
-                        pk[h2 * 16 + e + 1] = pack2(v1.x, v1.y, p.out_bf16 != 0);
-                    }
+            for (int c = 0; c < NPC; ++c) {
+                uint32_t o[32];
+                if (have) {
+                    tc::ld32(tmem + lane_base + t * D + (hc * NPC + c) * 32, o);
+                    tc::wait_ld();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float2 v = fmul2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv));
-                        pk[h2 * 16 + e] = pack2(v.x, v.y, p.out_bf16 != 0);
+                    for (int e = 0; e < 32; ++e) o[e] = 0u;
+                }
+                float4 *d4 = reinterpret_cast<float4 *>(po + c * 32);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    d4[q] = make_float4(__uint_as_float(o[4 * q]) * inv, __uint_as_float(o[4 * q + 1]) * inv,
+                                        __uint_as_float(o[4 * q + 2]) * inv,
+                                        __uint_as_float(o[4 * q + 3]) * inv);
+            }
+            if (hc == 0) p.part_lse[slot * 128 + r] = l > 0.0f ? m_run + log2f(l) : -INFINITY;
+        } else {
+            const int64_t orow = q_row_late(i);
+            // smooth_v: the V mean goes back onto rows that saw a key
+            const float *vmu = (p.v_mean && l > 0.0f) ? v_mean_late() : nullptr;
+            // The O rows go out through shared memory: each warp stages its 32
+            // rows, 64 channels at a time, then stores 4 rows' 128-byte pieces
+            // per instruction (one row per thread made every store instruction
+            // touch 32 rows, most of the epilogue's time).  The staging space is
+            // this tile's Q tile (not read since its last QK^T, which retired
+            // before the last P.V) or, with one query tile, the key ring (every
+            // MMA has retired by now); 16-byte pieces XOR-swizzled by row.
+            const int i_w0 = i - lane;  // this warp's first row (rows are consecutive)
+            const int64_t ostride = (VL || p.nhd) ? (int64_t)p.Hq * D : (int64_t)D;  // between rows
+            uint16_t *obase0 = reinterpret_cast<uint16_t *>(p.out) + out_row_late(i_w0) * D;
+            uint8_t *ost = (NQ > 1 ? sm + t * C::QB + (warp & 3) * 4096 : sm + C::OFF_ST + warp * 4096);
+            const int nrow_w = min(32, Sq() - i_w0);  // rows of this warp inside the sequence
+            // two 32-column pieces of O per tensor-memory round trip
+            constexpr int NCH = D / 32 / SPLIT;
+            static_assert(NCH % 2 == 0, "O pieces go in pairs");
+#pragma unroll 1
+            for (int c2 = 0; c2 < NCH; c2 += 2) {
+                uint32_t oo[2][32];
+                if (have) {
+                    tc::ld32(tmem + lane_base + t * D + (hc * NCH + c2) * 32, oo[0]);
+                    tc::ld32(tmem + lane_base + t * D + (hc * NCH + c2 + 1) * 32, oo[1]);
+                    tc::wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) oo[0][e] = oo[1][e] = 0u;
+                }
+                uint32_t pk[32];  // this row's 64 channels, f16 / bf16 pairs
+#pragma unroll
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    const uint32_t(&o)[32] = oo[h2];
+                    if (vmu) {
+                        const float4 *m4 = reinterpret_cast<const float4 *>(vmu + (hc * NCH + c2 + h2) * 32);
+#pragma unroll
+                        for (int e = 0; e < 16; e += 2) {
+                            const float4 m = m4[e / 2];
+                            const float2 v0 = ffma2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv),
+                                                    make_float2(m.x, m.y));
+                            const float2 v1 = ffma2(u2f2(o[2 * e + 2], o[2 * e + 3]),
+                                                    make_float2(inv, inv), make_float2(m.z, m.w));
+                            pk[h2 * 16 + e] = pack2(v0.x, v0.y, p.out_bf16 != 0);
+                            pk[h2 * 16 + e + 1] = pack2(v1.x, v1.y, p.out_bf16 != 0);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float2 v = fmul2(u2f2(o[2 * e], o[2 * e + 1]), make_float2(inv, inv));
+                            pk[h2 * 16 + e] = pack2(v.x, v.y, p.out_bf16 != 0);
+                        }
+                    }
+                }
+                __syncwarp();  // the previous pair's staged rows have been read
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4 *>(ost + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+                __syncwarp();
+                const int j = lane & 7;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int rr = (lane >> 3) + 4 * k;
+                    if (rr < nrow_w) {
+                        const uint4 v = *reinterpret_cast<const uint4 *>(ost + rr * 128 + ((j ^ (rr & 7)) << 4));
+                        *reinterpret_cast<uint4 *>(obase0 + rr * ostride + (hc * NCH + c2) * 32 + j * 8) = v;
                     }
                 }
             }
-            __syncwarp();  // the previous pair's staged rows have been read
-#pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4 *>(ost + lane * 128 + ((j ^ (lane & 7)) << 4)) =
-                    make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-            __syncwarp();
-            const int j = lane & 7;
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int rr = (lane >> 3) + 4 * k;
-                if (rr < nrow_w) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(ost + rr * 128 + ((j ^ (rr & 7)) << 4));
-                    *reinterpret_cast<uint4 *>(obase0 + rr * ostride + (hc * NCH + c2) * 32 + j * 8) = v;
-                }
-            }
+            if (row_ok && p.lse && hc == 0)
+                p.lse[orow] = l > 0.0f ? (m_run + log2f(l)) * 0.69314718055994530942f : -INFINITY;
         }
-        if (row_ok && p.lse && hc == 0)
-            p.lse[orow] = l > 0.0f ? (m_run + log2f(l)) * 0.69314718055994530942f : -INFINITY;
     }
 
     tc::fence_before();
@@ -974,6 +1032,68 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         tc::fence_after();
         tc::dealloc(tmem, 512);
     }
+}
+
+// Merge of a split query tile's parts (dense form, D = 256): one warp per
+// row, CPL channels per lane.  With lse_j the parts' base-2 LSEs and M their
+// maximum, o = sum_j 2^(lse_j - M) o_j / sum_j 2^(lse_j - M) (the parts' O
+// are normalised by their own sums), plus the smooth_v mean on rows that saw
+// a key, and lse = (M + log2 sum_j 2^(lse_j - M)) ln 2: the attention over
+// the union of the parts' keys (the split-K combine of "INT8 QK MMAC on
+// gfx936 DCU", section 4, over key ranges of a prefill tile).
+template <int D>
+__global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constant__ PrefillParams p) {
+    constexpr int CPL = D / 32;
+    static_assert(CPL == 8, "one 16-byte output store per lane");
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t g = (int64_t)blockIdx.x * 8 + warp;  // (split tile, row)
+    if (g >= (int64_t)p.split_tail * 128) return;
+    const int u = (int)(g >> 7), r = (int)(g & 127);
+    int ct;
+    const int pair = dense_tile(p, 128, p.split_f + u, ct);
+    const int i = ct * 128 + r;
+    if (i >= p.Sq) return;
+    const int64_t slot0 = (int64_t)u * p.split_k;
+    float M = -INFINITY;
+    for (int j = 0; j < p.split_k; ++j) M = fmaxf(M, p.part_lse[(slot0 + j) * 128 + r]);
+    float acc[CPL];
+#pragma unroll
+    for (int e = 0; e < CPL; ++e) acc[e] = 0.0f;
+    float W = 0.0f;
+    if (M != -INFINITY) {
+        for (int j = 0; j < p.split_k; ++j) {
+            const float lj = p.part_lse[(slot0 + j) * 128 + r];
+            if (lj == -INFINITY) continue;  // no key of this part visible to the row
+            const float w = exp2f(lj - M);
+            W += w;
+            const float4 *src =
+                reinterpret_cast<const float4 *>(p.part_o + ((slot0 + j) * 128 + r) * D + lane * CPL);
+#pragma unroll
+            for (int q = 0; q < CPL / 4; ++q) {
+                const float4 v = src[q];
+                acc[4 * q] = fmaf(w, v.x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(w, v.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(w, v.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(w, v.w, acc[4 * q + 3]);
+            }
+        }
+    }
+    const float inv = W > 0.0f ? 1.0f / W : 0.0f;
+    const int b = pair / p.Hq, hq = pair - b * p.Hq;
+    const float *vmu = (p.v_mean && W > 0.0f)
+                           ? p.v_mean + ((int64_t)b * p.Hkv + hq / p.group) * D + lane * CPL
+                           : nullptr;
+    uint32_t pk[CPL / 2];
+#pragma unroll
+    for (int e = 0; e < CPL / 2; ++e) {
+        const float m0 = vmu ? vmu[2 * e] : 0.0f, m1 = vmu ? vmu[2 * e + 1] : 0.0f;
+        pk[e] = pack2(fmaf(acc[2 * e], inv, m0), fmaf(acc[2 * e + 1], inv, m1), p.out_bf16 != 0);
+    }
+    const int64_t orow = p.nhd ? ((int64_t)b * p.Sq + i) * p.Hq + hq : (int64_t)pair * p.Sq + i;
+    *reinterpret_cast<uint4 *>(reinterpret_cast<uint16_t *>(p.out) + orow * D + lane * CPL) =
+        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+    if (p.lse && lane == 0)
+        p.lse[(int64_t)pair * p.Sq + i] = W > 0.0f ? (M + log2f(W)) * 0.69314718055994530942f : -INFINITY;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -1052,13 +1172,30 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     constexpr int QR = 128 * C::NQ;
     const int64_t vl_ctas = VL ? (p.total_q / QR + p.B) * (int64_t)p.Hq : 0;
     if (vl_ctas > 0x7fffffff) return cudaErrorInvalidValue;
-    const dim3 grid = VL ? dim3((unsigned)vl_ctas, 1, 1)
-                         : dim3((unsigned)((p.Sq + QR - 1) / QR * p.Hq * p.B), 1, 1);
+    // dense form at D = 256: CTAs of whole query tiles, then the split tail's parts
+    const int64_t dense_ctas = (int64_t)(p.Sq + QR - 1) / QR * p.Hq * p.B;
+    const bool split = !VL && C::WIDE && p.split_k > 0;
+    if (!split && p.split_k != 0) return cudaErrorInvalidValue;
+    if (split && (p.split_k > 64 || p.split_tail < 1 ||
+                  (int64_t)p.split_f + p.split_tail != dense_ctas || !p.part_o || !p.part_lse))
+        return cudaErrorInvalidValue;
+    const int64_t ctas = VL ? vl_ctas : split ? p.split_f + (int64_t)p.split_tail * p.split_k : dense_ctas;
+    if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)ctas, 1, 1);
     if (!VL && (p.bundle < 1 || p.bundle > p.B * p.Hq)) return cudaErrorInvalidValue;
     prefill_kernel<D, VL><<<grid, C::THREADS, C::SMEM, st>>>(p, m);
     log.add(VL ? "prefill_varlen_kernel" : "prefill_kernel", grid, dim3(C::THREADS), dim3(1, 1, 1),
             C::SMEM);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if constexpr (!VL && C::WIDE) {
+        if (split && e == cudaSuccess) {
+            const unsigned mg = (unsigned)(((int64_t)p.split_tail * 128 + 7) / 8);
+            prefill_merge_kernel<D><<<mg, 256, 0, st>>>(p);
+            ++log.count;  // the attention kernel stays the recorded launch
+            e = cudaGetLastError();
+        }
+    }
+    return e;
 }
 
 template <int D>
@@ -1067,6 +1204,33 @@ cudaError_t launch_d(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
 }
 
 }  // namespace
+
+PrefillSplit prefill_split(int B, int Hq, int Sq, int D, int keys, bool causal, int sms) {
+    PrefillSplit s = {0, 0, 0};
+    if (D != 256 || sms < 1 || keys < 1 || Sq < 1) return s;
+    const int64_t tiles = (int64_t)((Sq + 127) / 128) * B * Hq;  // one 128-row query tile per CTA
+    const int64_t tail = tiles % sms;                             // CTAs of the last, partial wave
+    if (tail == 0 || tiles > 0x3fffffff) return s;
+    // key tiles of a query tile: at most T; causal rows see fewer, the first
+    // query tile at least Tmin.  The model below assumes tiles of about
+    // equal work (a chunk over a long prefix, or no mask).
+    const int T = (keys + 63) / 64;
+    const int Tmin = causal ? (keys - Sq + 128 > 0 ? (keys - Sq + 128) / 64 : 0) : T;
+    if (4 * Tmin < 3 * T) return s;
+    // In units of one query tile's time: k parts of a tail tile run in
+    // ceil(tail * k / sms) rounds, each costing 1/k of a tile plus a fixed
+    // start-up and drain of about 8 key tiles' time; parts of at least 16
+    // key tiles; a split must save 5 %.
+    const double fixed = 8.0 / Tmin;
+    double best = 1.0 + fixed;
+    int bk = 1;
+    for (int k = 2; k <= 8 && Tmin / k >= 16; ++k) {
+        const double c = (double)((tail * k + sms - 1) / sms) * (1.0 / k + fixed);
+        if (c < 0.95 * best) best = c, bk = k;
+    }
+    if (bk > 1) s = {(int)(tiles - tail), (int)tail, bk};
+    return s;
+}
 
 int prefill_bundle(int B, int Hq, int group, int rows, int D) {
     constexpr double kL2Share = 48.0 * 1024 * 1024;  // of the 126 MB L2

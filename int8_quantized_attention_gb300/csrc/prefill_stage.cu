@@ -254,7 +254,7 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 }  // namespace
 
 PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, bool v_bf16,
-                             bool smooth_v) {
+                             bool smooth_v, const PrefillSplit &split) {
     PrefillLayout L = {};
     L.BN = D == 256 ? 64 : 128;
     L.Ppad = (max_prefix_len + L.BN - 1) / L.BN * L.BN;
@@ -265,7 +265,10 @@ PrefillLayout prefill_layout(int B, int Hkv, int Sk, int D, int max_prefix_len, 
     L.off_v = align256(L.off_k + BH * L.Lpad * D * 2);
     L.off_ksc = align256(L.off_v + BH * L.Vrows * D * 2);
     L.off_vmean = align256(L.off_ksc + BH * L.Lpad * 4);
-    L.bytes = align256(L.off_vmean + (smooth_v ? BH * D * 4 : 0));
+    const size_t slots = split.parts > 0 ? (size_t)split.tail * split.parts : 0;
+    L.off_part_o = align256(L.off_vmean + (smooth_v ? BH * D * 4 : 0));
+    L.off_part_lse = align256(L.off_part_o + slots * 128 * D * 4);
+    L.bytes = align256(L.off_part_lse + slots * 128 * 4);
     return L;
 }
 
@@ -281,7 +284,8 @@ PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D, bool
     L.off_v = align256(L.off_k + H * rows * D * 2);
     L.off_ksc = align256(L.off_v + H * rows * D * 2);
     L.off_vmean = align256(L.off_ksc + H * rows * 4);
-    L.bytes = align256(L.off_vmean + (smooth_v ? (size_t)B * Hkv * D * 4 : 0));
+    L.off_part_o = L.off_part_lse = L.bytes =
+        align256(L.off_vmean + (smooth_v ? (size_t)B * Hkv * D * 4 : 0));
     return L;
 }
 

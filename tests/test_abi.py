@@ -154,3 +154,22 @@ def test_decode_rejects_unaligned_out_before_any_launch(lib, entry):
         fn(ctypes.byref(a), None)
     assert st == binding.SAGE_ERR_INVALID_ARG
     assert b"out must be 8-byte aligned" in lib.sage_get_last_error_message()
+
+
+def test_prefill_tail_split_workspace_and_check(lib):
+    """The tail split's partial results are part of the prefill workspace
+    (D = 256, 32 query tiles over 4096 keys: one partial wave), OFF drops
+    them, and an unknown tail_split value is rejected before any launch."""
+    a = binding.PrefillArgs()
+    a.B, a.Hq, a.Hkv, a.Sq, a.Sk, a.D = 1, 8, 2, 512, 4096, 256
+    a.q_block, a.k_block, a.v_dtype, a.out_dtype = 128, 64, 0, 0
+    a.causal = 0
+    with_split = lib.sage_attn_prefill_workspace_size(ctypes.byref(a))
+    a.tail_split = 1
+    without = lib.sage_attn_prefill_workspace_size(ctypes.byref(a))
+    # 32 tiles x 4 parts x 128 rows x (256 + 1) fp32
+    assert with_split >= without + 32 * 4 * 128 * 257 * 4
+    a.tail_split = 2
+    assert lib.sage_attn_prefill_workspace_size(ctypes.byref(a)) == 0
+    ws = ctypes.c_void_p(0)
+    assert lib.sage_attn_prefill(ctypes.byref(a), ws, 0, None) == binding.SAGE_ERR_INVALID_ARG

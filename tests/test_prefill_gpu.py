@@ -362,3 +362,68 @@ def test_prefill_nhd_dense_workload_shape_sampled(sage):
     o_ref, l_ref = _oracle(qi, qs, 128, ki, ks, 64, qkv.v, True, bias=bias, rows=rows)
     assert_close(f32(out_n)[:, rows].transpose(0, 2, 1, 3), o_ref)
     assert_close(np_(lse_n)[:, :, rows], l_ref, "lse")
+
+
+def _split_case(seed, causal, dtype="f16"):
+    # 32 query tiles of 128 rows (1 x 8 heads x 512 rows) over 4096 keys at
+    # D = 256: the whole grid is one partial wave on 152 SMs, so every tile
+    # is split by key range (3 parts with the causal mask, 4 without) and
+    # merged by the merge kernel
+    return W.dense_qkv(1, 8, 2, 512, 4096, 256, seed=seed, dtype=dtype, device="cuda",
+                       k_offset_std=2.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_tail_split_matches_oracle(sage, causal):
+    """The last wave's query tiles split by key range ("INT8 QK MMAC on gfx936
+    DCU", section 4: split-K with an LSE combine) give the oracle's result on
+    sampled rows of every head, stay within rounding of the unsplit launch,
+    and dump the same raw INT32 scores."""
+    qkv = _split_case(61, causal)
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 128, 64, True)
+    kw = dict(causal=causal, q_bias=bias, out_dtype=torch.float16, return_lse=True)
+    S, Sk = 512, 4096
+    dbg_s = torch.full((1, 8, S, Sk), -(2 ** 31), dtype=torch.int32, device="cuda")
+    out, lse = sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, qkv.v, debug_scores=dbg_s, **kw)
+    info = sage.last_launch_info()
+    k = 3 if causal else 4
+    assert info["kernel"] == "prefill_kernel" and info["grid"] == (32 * k, 1, 1)
+    assert info["launches"] == 3  # staging, attention, merge
+    dbg_u = torch.full_like(dbg_s, -(2 ** 31))
+    out_u, lse_u = sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, qkv.v, debug_scores=dbg_u,
+                                          tail_split=False, **kw)
+    assert sage.last_launch_info()["grid"] == (32, 1, 1)
+    assert sage.last_launch_info()["launches"] == 2
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert torch.equal(dbg_s, dbg_u)
+    assert_close(f32(out), f32(out_u), "split vs unsplit", rel=1e-3, abs_=1e-3)
+    assert_close(np_(lse), np_(lse_u), "lse split vs unsplit", rel=1e-5, abs_=1e-4)
+    rows = np.array([0, 1, 127, 128, 255, 256, 383, 384, 511])
+    o_ref, l_ref = _oracle(qi, qs, 128, ki, ks, 64, qkv.v, causal, bias=bias, rows=rows)
+    assert_close(f32(out)[:, :, rows], o_ref)
+    assert_close(np_(lse)[:, :, rows], l_ref, "lse")
+
+
+@pytest.mark.parametrize("smooth_v", [False, True])
+def test_prefill_tail_split_nhd_prefix_smooth_v(sage, smooth_v):
+    """The merge kernel's other output paths: NHD output rows, bf16 output,
+    the smooth_v mean added back, rows of a causal chunk over a paged
+    prefix; equal within rounding to the unsplit launch."""
+    B, Hq, Hkv, Sc, D, Pn = 1, 8, 2, 256, 256, 3840
+    qkv = W.dense_qkv(B, Hq, Hkv, Sc, Sc, D, seed=63, dtype="bf16", device="cuda",
+                      k_offset_std=2.0)
+    c = W.paged_cache(B, Hkv, D, [Pn], seed=64, device="cuda")
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 1, 1, True)
+    v_nhd = qkv.v.transpose(1, 2).contiguous()
+    kw = dict(causal=True, q_bias=bias, prefix=_prefix_dict(c, Pn), return_lse=True,
+              smooth_v=smooth_v, layout="NHD")
+    out, lse = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, v_nhd, **kw)
+    split_grid = sage.last_launch_info()["grid"][0]
+    out_u, lse_u = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, v_nhd, tail_split=False, **kw)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert split_grid > 16  # 16 query tiles, each split
+    assert out.dtype == torch.bfloat16 and tuple(out.shape) == (B, Sc, Hq, D)
+    assert_close(f32(out), f32(out_u), "split vs unsplit", rel=2e-3, abs_=2e-3)
+    assert_close(np_(lse), np_(lse_u), "lse split vs unsplit", rel=1e-5, abs_=1e-4)

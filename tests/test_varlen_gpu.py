@@ -202,7 +202,7 @@ def test_varlen_equals_dense_per_sequence(sage, D, vdt):
             128, ki[:, k0:k1].unsqueeze(0).contiguous(),
             ks[:, gk0:gk0 + nk].unsqueeze(0).contiguous(), 64,
             x.v[k0:k1].transpose(0, 1).unsqueeze(0).contiguous(), causal=True,
-            q_bias=bias[:, q0:q1].unsqueeze(0).contiguous(), return_lse=True)
+            q_bias=bias[:, q0:q1].unsqueeze(0).contiguous(), return_lse=True, tail_split=False)
         torch.cuda.synchronize()
         assert torch.equal(out[q0:q1], o_b[0].transpose(0, 1)), "output of sequence %d" % b
         assert torch.equal(lse[:, q0:q1], l_b[0]), "lse of sequence %d" % b
