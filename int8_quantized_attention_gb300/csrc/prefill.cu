@@ -199,7 +199,8 @@ __device__ __forceinline__ void store_piece(uint8_t *tile, int r, int dc, uint4 
 // index over (batch, head) pairs taken in bundles of p.bundle (whose staged
 // keys fit in L2 together); within a bundle the heaviest (causal) query
 // tiles of all its pairs come first, so that no heavy tile is left to run
-// alone at the end of the grid.  Returns the pair index b * Hq + hq.
+// alone at the end of the grid.  Returns the pair index b * Hq + hq.  (The
+// attention kernel writes the same decode out in place.)
 __device__ __forceinline__ int dense_tile(const PrefillParams &p, int QR, int item, int &ct) {
     const int nct = (p.Sq + QR - 1) / QR;
     const int per = nct * p.bundle;
@@ -261,9 +262,17 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         cq0 = p.cu_q[b], cq1 = p.cu_q[b + 1], ck0 = p.cu_k[b], ck1 = p.cu_k[b + 1];
         ct = g - (int)varlen_group0(cq0 < 0 ? 0 : cq0, b, QR);  // reversed below
     } else {
+        // (the tile decode is written out here and in late_pair(): through
+        // the shared helper the D = 128 kernel spilled more)
         int item = blockIdx.x;
         if constexpr (C::WIDE) item = split_item(p, item, part);
-        const int u = dense_tile(p, QR, item, ct);
+        const int nct = (p.Sq + QR - 1) / QR;
+        const int per = nct * p.bundle;
+        const int bun = item / per;
+        const int nb = min(p.bundle, p.B * p.Hq - bun * p.bundle);
+        const int rr = item - bun * per;
+        ct = nct - 1 - rr / nb;
+        const int u = bun * p.bundle + rr % nb;
         b = u / p.Hq;
         hq = u % p.Hq;
     }
@@ -325,8 +334,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             int pt;
             L = split_item(p, L, pt);
         }
-        int c;
-        return dense_tile(p, QR, L, c);
+        const int per = (p.Sq + QR - 1) / QR * p.bundle;
+        const int bun = L / per;
+        const int nb = min(p.bundle, p.B * p.Hq - bun * p.bundle);
+        return (int64_t)bun * p.bundle + (L - bun * per) % nb;
     };
     auto q_row_late = [&](int i) -> int64_t {
         if constexpr (VL) return vq_row0 + i;
@@ -421,10 +432,12 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             mbar_init(bar(B_KV_EMPTY + s), 1);
         }
         for (int s = 0; s < NQ * NS; ++s) mbar_init(bar(B_S_FULL + s), 1);
-        // one arrival per softmax warp (its lanes' stores ordered by the
-        // warp's own synchronisation): 8 arrivals instead of 256 measured
-        // 3 % faster on the dense-prefill workload
-        for (int s = 0; s < NQ * NS * C::NPH; ++s) mbar_init(bar(B_P_FULL + s), 4 * C::SPLIT);
+        // WIDE: one arrival per softmax warp (its lanes' stores ordered by
+        // the warp's own synchronisation), 0.3 % faster on the chunked
+        // workload; per thread at D <= 128, where per warp measured 0.5 %
+        // slower on the dense workload
+        for (int s = 0; s < NQ * NS * C::NPH; ++s)
+            mbar_init(bar(B_P_FULL + s), C::WIDE ? 4 * C::SPLIT : 128 * C::SPLIT);
         for (int t = 0; t < NQ; ++t) {
             mbar_init(bar(B_O_FINAL + t), 1);
         }
@@ -458,8 +471,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             // retired: K, V and the per-key K scales on one barrier, or (WIDE)
             // the K tile from this warp and V with the scales from warp
             // kMma + 2, each through its own ring
-            const bool load_k = warp == kProducer;
-            const bool load_v = !C::WIDE || !load_k;
+            const bool load_k = !C::WIDE || warp == kProducer;
+            const bool load_v = !C::WIDE || warp != kProducer;
             if (load_k) tc::prefetch_tmap(&maps.k);
             if (load_v && n_pre > 0) tc::prefetch_tmap(&maps.v_pre);
             if (load_v && n_ch > 0) tc::prefetch_tmap(&maps.v_ch);
@@ -901,8 +914,12 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                     tc::st16(pcol, *reinterpret_cast<uint32_t(*)[16]>(pk));
                 tc::wait_st();
                 tc::fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(B_P_FULL + slot * C::NPH + (c0 + GW * g) / 64));
+                if constexpr (C::WIDE) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(B_P_FULL + slot * C::NPH + (c0 + GW * g) / 64));
+                } else {
+                    mbar_arrive(bar(B_P_FULL + slot * C::NPH + (c0 + GW * g) / 64));
+                }
             }
             l += (ls01.x + ls01.y) + (ls23.x + ls23.y);
             done = jj + 1;
