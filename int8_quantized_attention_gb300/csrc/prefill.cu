@@ -25,24 +25,22 @@
 // D = 256) through an NST-deep ring.
 //   warps 0..4NQ*SPLIT-1  softmax: per query tile one warpgroup (one thread
 //              per query row = TMEM lane), or at D = 256 two warpgroups
-//              sharing each row's columns; Q int8 -> f16 into shared memory
-//              (or TMEM) once;
+//              sharing each row's columns; Q int8 -> f16 once, into shared
+//              memory (at D = 256 channels 0-127 into TMEM);
 //              per key tile one tcgen05.ld of the whole S row into
 //              registers, per-column K-scale recovery, online softmax with
 //              lazy rescaling (O is rescaled only when the row max grows by
-//              more than 2^8), P written back over S in TMEM (D <= 128) or
-//              into shared memory (D = 256).
+//              more than 2^8), P written back over S in TMEM.
 //   next warp  producer (one thread): per key tile the K and V tiles (TMA
 //              tensor loads) and the per-key K scales (1-D bulk copy) into
 //              one stage of an NST-deep ring (D = 256: the K tiles only).
-//   next warp  TMEM owner and MMA issuer (one thread): S_t = Q_t K^T (Q from
-//              shared memory, or from TMEM where it fits), then O_t += P_t V
-//              with P from TMEM.  With two query tiles the two warpgroups
-//              ping-pong: the tensor core works on one tile's MMAs while the
-//              other tile's softmax runs (one issuer keeps each tile's MMAs
-//              together; two issuers interleaving them measured slower).
-//              With one tile (D = 256) S is double-buffered instead, this
-//              warp issues only O += P V (P from shared memory) and
+//   next warp  TMEM owner and MMA issuer (one thread): S_t = Q_t K^T, then
+//              O_t += P_t V with P from TMEM.  With two query tiles the two
+//              warpgroups ping-pong: the tensor core works on one tile's
+//              MMAs while the other tile's softmax runs (one issuer keeps
+//              each tile's MMAs together; two issuers interleaving them
+//              measured slower).  With one tile (D = 256) S has three slots
+//              instead, this warp issues only O += P V, and
 //   next warp  issues S = Q K^T, and
 //   next warp  streams the V tiles with the per-key K scales through a ring
 //              of their own.
@@ -932,10 +930,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             pair_sync();
             l += red[((T & 1) * C::NSW + (wg ^ 1)) * 128 + r];
         }
-        // with S double-buffered the last two P.V may both be in flight, and a
-        // parity wait on a per-tile barrier cannot tell its last phase from
-        // two phases back, so the epilogue waits on a barrier that completes
-        // exactly once
+        // with several S slots the last P.V may be in flight together with
+        // earlier ones, and a parity wait on a per-tile barrier cannot tell
+        // its last phase from two phases back, so the epilogue waits on a
+        // barrier that completes exactly once
         bool have = done == T && T > 0;
         if (have) {
             const bool w = wait_ab(bar(B_O_FINAL + t), 0u, p.err, abort_flag);
