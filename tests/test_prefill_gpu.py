@@ -427,3 +427,30 @@ def test_prefill_tail_split_nhd_prefix_smooth_v(sage, smooth_v):
     assert out.dtype == torch.bfloat16 and tuple(out.shape) == (B, Sc, Hq, D)
     assert_close(f32(out), f32(out_u), "split vs unsplit", rel=2e-3, abs_=2e-3)
     assert_close(np_(lse), np_(lse_u), "lse split vs unsplit", rel=1e-5, abs_=1e-4)
+
+
+def test_prefill_tail_split_ragged_prefix(sage):
+    """Two sequences whose paged prefixes differ in length (3840 and 2200
+    tokens): their query tiles have different key counts, so the split
+    parts cover different key ranges; both sequences match the oracle on
+    sampled rows and the unsplit launch within rounding."""
+    B, Hq, Hkv, Sc, D = 2, 4, 1, 256, 256
+    lens = [3840, 2200]
+    qkv = W.dense_qkv(B, Hq, Hkv, Sc, Sc, D, seed=71, dtype="bf16", device="cuda",
+                      k_offset_std=2.0)
+    c = W.paged_cache(B, Hkv, D, lens, seed=72, device="cuda", extra_blocks=3)
+    qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 1, 1, True)
+    kw = dict(causal=True, q_bias=bias, prefix=_prefix_dict(c, max(lens)), return_lse=True,
+              out_dtype=torch.float16)
+    out, lse = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, **kw)
+    grid = sage.last_launch_info()["grid"][0]
+    out_u, lse_u = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, tail_split=False, **kw)
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert grid > 16  # 16 query tiles, each split
+    assert_close(f32(out), f32(out_u), "split vs unsplit", rel=1e-3, abs_=1e-3)
+    assert_close(np_(lse), np_(lse_u), "lse split vs unsplit", rel=1e-5, abs_=1e-4)
+    rows = np.array([0, 1, 127, 128, 200, 255])
+    o_ref, l_ref = _oracle(qi, qs, 1, ki, ks, 1, qkv.v, True, bias=bias, prefix=c, rows=rows)
+    assert_close(f32(out)[:, :, rows], o_ref)
+    assert_close(np_(lse)[:, :, rows], l_ref, "lse")
