@@ -454,3 +454,31 @@ def test_prefill_tail_split_ragged_prefix(sage):
     o_ref, l_ref = _oracle(qi, qs, 1, ki, ks, 1, qkv.v, True, bias=bias, prefix=c, rows=rows)
     assert_close(f32(out)[:, :, rows], o_ref)
     assert_close(np_(lse)[:, :, rows], l_ref, "lse")
+
+
+@pytest.mark.parametrize("D", [128, 256])
+def test_prefill_bad_prefix_page_sets_error_word(sage, D):
+    """A block-table entry out of range inside a sequence's prefix is never
+    read: the staging pass sets the error word's bad-block bit and stages
+    zero rows for that page; the other sequence, whose table is valid,
+    still matches the oracle."""
+    B, Hq, Hkv, Sc = 2, 2, 1, 64
+    lens = [200, 150]
+    qkv = W.dense_qkv(B, Hq, Hkv, Sc, Sc, D, seed=D + 3, device="cuda")
+    c = W.paged_cache(B, Hkv, D, lens, seed=D + 4, device="cuda", extra_blocks=2)
+    c.lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    qi, qs, ki, ks, _, _ = _quant(sage, qkv, 1, 1, False)
+    bad = c.block_table.clone()
+    bad[0, 3] = c.k_cache.shape[0] + 100
+    c_bad = W.PagedCache(c.k_cache, c.v_cache, c.k_scale, c.v_scale, bad, c.lens)
+    assert sage.check_device_status()[0] == 0
+    out, lse = sage.sage_attn_prefill(qi, qs, 1, ki, ks, 1, qkv.v, causal=True,
+                                      prefix=_prefix_dict(c_bad, max(lens)),
+                                      out_dtype=torch.float16, return_lse=True)
+    st, word = sage.check_device_status()
+    assert st == sage.SAGE_ERR_BAD_BLOCK and word & 2
+    o_ref, l_ref = _oracle(qi[1:], qs[1:], 1, ki[1:], ks[1:], 1, qkv.v[1:], True,
+                           prefix=W.PagedCache(c.k_cache, c.v_cache, c.k_scale, c.v_scale,
+                                               c.block_table[1:], c.lens[1:]))
+    assert_close(f32(out)[1:], o_ref)
+    assert_close(np_(lse)[1:], l_ref, "lse")
