@@ -431,7 +431,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         }
         for (int s = 0; s < NQ * NS; ++s) mbar_init(bar(B_S_FULL + s), 1);
         // WIDE: one arrival per softmax warp (its lanes' stores ordered by
-        // the warp's own synchronisation), 0.3 % faster on the chunked
+        // the warp's own synchronisation), 0.2 % faster on the chunked
         // workload; per thread at D <= 128, where per warp measured 0.5 %
         // slower on the dense workload
         for (int s = 0; s < NQ * NS * C::NPH; ++s)
@@ -574,7 +574,8 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 const uint32_t o = tmem + t * D;
 #pragma unroll
                 for (int h = 0; h < C::NPH; ++h) {
-                    // (the stage's V landed with its K, waited before QK^T)
+                    // (the stage's V landed with its K, waited before QK^T;
+                    // WIDE: the P.V issuer waited for the V stage)
                     const bool ok = wait_ab(bar(B_P_FULL + slot * C::NPH + h), sp, p.err, abort_flag);
                     if (!ok) return false;
                     tc::fence_after();
