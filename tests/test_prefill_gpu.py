@@ -482,3 +482,72 @@ def test_prefill_bad_prefix_page_sets_error_word(sage, D):
                                                c.block_table[1:], c.lens[1:]))
     assert_close(f32(out)[1:], o_ref)
     assert_close(np_(lse)[1:], l_ref, "lse")
+
+
+def _fuzz_case(i):
+    """Seeded random prefill configuration i (shapes, head dim, GQA group,
+    masks, scale granularity, smooth_k / smooth_v, layout, V dtype, paged
+    prefix and ragged prefix lengths)."""
+    rng = np.random.default_rng(1000 + i)
+    D = int(rng.choice([64, 128, 256]))
+    Hkv = int(rng.choice([1, 2]))
+    Hq = Hkv * int(rng.choice([1, 2, 3]))
+    B = int(rng.integers(1, 3))
+    Sq = int(rng.integers(1, 300))
+    P = int(rng.choice([0, int(rng.integers(1, 400))]))
+    Sc = int(rng.integers(0 if P > 0 else 1, 300))
+    if i % 8 == 4:  # keys from the paged prefix only (Sk = 0)
+        P, Sc = max(P, 100), 0
+    return dict(D=D, Hkv=Hkv, Hq=Hq, B=B, Sq=Sq, Sc=Sc, P=P,
+                causal=bool(rng.integers(0, 2)), qb=int(rng.choice([1, 128])),
+                kb=int(rng.choice([1, 64])), smooth_k=bool(rng.integers(0, 2)) and Sc > 0,
+                smooth_v=bool(rng.integers(0, 2)) and Sc > 0, nhd=bool(rng.integers(0, 2)),
+                vdt=str(rng.choice(["fp16", "bf16"])), seed=2000 + i)
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_prefill_random_configurations(sage, i):
+    """Seeded random configurations against the oracle on every row:
+    outputs and LSE within tolerance (empty rows: o = 0, lse = -inf)."""
+    c = _fuzz_case(i)
+    B, Hq, Hkv, Sq, Sc, D, P = c["B"], c["Hq"], c["Hkv"], c["Sq"], c["Sc"], c["D"], c["P"]
+    qkv = W.dense_qkv(B, Hq, Hkv, Sq, max(Sc, 1), D, seed=c["seed"], dtype=c["vdt"],
+                      device="cuda", k_offset_std=2.0)
+    qi, qs, _, _ = sage.sage_quant_int8(qkv.q, block_tokens=c["qb"])
+    bias = None
+    if Sc > 0:
+        k = qkv.k[:, :, :Sc].contiguous()
+        v = qkv.v[:, :, :Sc].contiguous()
+        ki, ks, mu, _ = sage.sage_quant_int8(k, block_tokens=c["kb"], smooth=c["smooth_k"])
+        if c["smooth_k"]:
+            _, _, _, bias = sage.sage_quant_int8(qkv.q, block_tokens=c["qb"], mu_in=mu)
+    else:
+        ki = torch.empty((B, Hkv, 0, D), dtype=torch.int8, device="cuda")
+        ks = torch.empty((B, Hkv, 0), dtype=torch.float32, device="cuda")
+        v = torch.empty((B, Hkv, 0, D), dtype=qkv.v.dtype, device="cuda")
+    prefix, pc = None, None
+    if P > 0:
+        lens = [P] + [int(x) for x in np.random.default_rng(c["seed"]).integers(0, P + 1, B - 1)]
+        pc = W.paged_cache(B, Hkv, D, [max(x, 1) for x in lens], seed=c["seed"] + 1,
+                           device="cuda", extra_blocks=2)
+        pc.lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+        prefix = _prefix_dict(pc, P)
+    v_in = v.transpose(1, 2).contiguous() if c["nhd"] else v
+    out, lse = sage.sage_attn_prefill(qi, qs, c["qb"], ki, ks, c["kb"], v_in, causal=c["causal"],
+                                      q_bias=bias, prefix=prefix, out_dtype=torch.float16,
+                                      return_lse=True, smooth_v=c["smooth_v"],
+                                      layout="NHD" if c["nhd"] else "HND")
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    if c["nhd"]:
+        out = out.transpose(1, 2)
+    pre = None
+    if pc is not None:
+        pre = dict(k_cache=np_(pc.k_cache), v_cache=np_(pc.v_cache), k_scale=np_(pc.k_scale),
+                   v_scale=np_(pc.v_scale), block_table=np_(pc.block_table), lens=np_(pc.lens))
+    o_ref, l_ref = oracle.prefill(np_(qi), np_(qs), c["qb"], np_(ki), np_(ks), c["kb"], f32(v),
+                                  causal=c["causal"],
+                                  q_bias=None if bias is None else np_(bias).astype(np.float64),
+                                  prefix=pre, smooth_v=c["smooth_v"])
+    assert_close(f32(out), o_ref, "case %d %s" % (i, c))
+    assert_close(np_(lse), l_ref, "lse case %d" % i)
