@@ -747,13 +747,20 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             const int key0 = pre ? kt * BN : (kt - n_pre) * BN;  // within its source
             const int nvalid = min(BN, (pre ? P : Sk()) - key0);
             const int kg0 = pre ? key0 : P + key0;  // over prefix + chunk
-            bool ok = wait_ab(bar(B_S_FULL + slot), sp, p.err, abort_flag);
-            // the stage holding this tile's per-key K scales
-            if constexpr (C::WIDE)
+            // S, and the stage holding this tile's per-key K scales.  At D <= 128
+            // that stage (with K) landed before its QK^T could run, so it is
+            // waited first, while S is still being computed: a wait on a
+            // completed barrier still costs ~100 cycles, kept off the path
+            // from S to the softmax.
+            bool ok;
+            if constexpr (C::WIDE) {
+                ok = wait_ab(bar(B_S_FULL + slot), sp, p.err, abort_flag);
                 ok = ok && wait_ab(bar(B_V_FULL + jj % C::NSV), (uint32_t)(jj / C::NSV) & 1u, p.err,
                                    abort_flag);
-            else
-                ok = ok && wait_ab(bar(B_KV_FULL + s), (uint32_t)(jj / NST) & 1u, p.err, abort_flag);
+            } else {
+                ok = wait_ab(bar(B_KV_FULL + s), (uint32_t)(jj / NST) & 1u, p.err, abort_flag);
+                ok = ok && wait_ab(bar(B_S_FULL + slot), sp, p.err, abort_flag);
+            }
             if (!__all_sync(0xffffffffu, ok)) {
                 if constexpr (SPLIT == 1) break;
                 alive = false;
