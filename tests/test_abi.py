@@ -173,3 +173,38 @@ def test_prefill_tail_split_workspace_and_check(lib):
     assert lib.sage_attn_prefill_workspace_size(ctypes.byref(a)) == 0
     ws = ctypes.c_void_p(0)
     assert lib.sage_attn_prefill(ctypes.byref(a), ws, 0, None) == binding.SAGE_ERR_INVALID_ARG
+
+
+def _prefill_ws(lib, **kw):
+    a = binding.PrefillArgs()
+    a.B, a.Hq, a.Hkv, a.D = kw.get("B", 1), kw["Hq"], kw.get("Hkv", 1), kw["D"]
+    a.Sq, a.Sk = kw["Sq"], kw["Sk"]
+    a.q_block, a.k_block, a.v_dtype, a.out_dtype = 1, 1, 0, 0
+    a.causal = int(kw.get("causal", 0))
+    if kw.get("prefix", 0):
+        a.max_prefix_len, a.max_blocks = kw["prefix"], (kw["prefix"] + 15) // 16
+    a.tail_split = 0
+    auto = lib.sage_attn_prefill_workspace_size(ctypes.byref(a))
+    a.tail_split = 1
+    off = lib.sage_attn_prefill_workspace_size(ctypes.byref(a))
+    return auto, off
+
+
+def test_prefill_tail_split_plan(lib):
+    """Host side of the tail split (152 SMs without a GPU): a causal chunk
+    over a long prefix at D = 256 with a partial last wave splits (its
+    workspace grows by the parts' partial results); causal self-attention,
+    a grid of whole waves and D <= 128 do not."""
+    # 2048 new tokens over a 16384-token prefix, 24 heads: 384 tiles, 80 in
+    # the last wave, split into 3 parts each
+    auto, off = _prefill_ws(lib, Hq=24, Hkv=4, D=256, Sq=2048, Sk=2048, prefix=16384, causal=1)
+    assert auto - off >= 80 * 3 * 128 * 257 * 4
+    # causal self-attention: the tiles' work differs too much
+    auto, off = _prefill_ws(lib, Hq=24, D=256, Sq=16384, Sk=16384, causal=1)
+    assert auto == off
+    # 152 tiles (one full wave): nothing to balance
+    auto, off = _prefill_ws(lib, Hq=19, D=256, Sq=1024, Sk=8192)
+    assert auto == off
+    # head dim 128: never split
+    auto, off = _prefill_ws(lib, Hq=24, D=128, Sq=2048, Sk=2048, prefix=16384, causal=1)
+    assert auto == off
