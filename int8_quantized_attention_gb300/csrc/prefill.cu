@@ -471,6 +471,12 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             // kMma + 2, each through its own ring
             const bool load_k = !C::WIDE || warp == kProducer;
             const bool load_v = !C::WIDE || warp != kProducer;
+            // this grid is launched behind the staging pass and may start
+            // before it ends: the staged keys, values and per-key scales are
+            // read only after that grid has completed (no-op otherwise).
+            // Everything else this kernel reads was written before the
+            // staging pass began.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             if (load_k) tc::prefetch_tmap(&maps.k);
             if (load_v && n_pre > 0) tc::prefetch_tmap(&maps.v_pre);
             if (load_v && n_ch > 0) tc::prefetch_tmap(&maps.v_ch);
@@ -1068,6 +1074,9 @@ template <int D>
 __global__ void __launch_bounds__(256) prefill_merge_kernel(const __grid_constant__ PrefillParams p) {
     constexpr int CPL = D / 32;
     static_assert(CPL == 8, "one 16-byte output store per lane");
+    // launched behind the attention kernel: its partial results are read
+    // only after that grid has completed
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t g = (int64_t)blockIdx.x * 8 + warp;  // (split tile, row)
     if (g >= (int64_t)p.split_tail * 128) return;
@@ -1206,16 +1215,33 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     if (ctas > 0x7fffffff) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)ctas, 1, 1);
     if (!VL && (p.bundle < 1 || p.bundle > p.B * p.Hq)) return cudaErrorInvalidValue;
-    prefill_kernel<D, VL><<<grid, C::THREADS, C::SMEM, st>>>(p, m);
+    // programmatic dependent launches: the attention kernel behind the
+    // staging pass, the merge behind the attention kernel; each waits on the
+    // device before reading what the grid ahead of it wrote.  The staging
+    // pass lets its dependent start once every staging CTA has started; the
+    // attention kernel does not signal early (a trigger at CTA start made
+    // the dense launch 0.7 % slower), so the merge is released when the
+    // attention grid completes and only its launch overlaps.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(C::THREADS, 1, 1);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D, VL>, p, m);
     log.add(VL ? "prefill_varlen_kernel" : "prefill_kernel", grid, dim3(C::THREADS), dim3(1, 1, 1),
             C::SMEM);
-    e = cudaGetLastError();
     if constexpr (!VL && C::WIDE) {
         if (split && e == cudaSuccess) {
-            const unsigned mg = (unsigned)(((int64_t)p.split_tail * 128 + 7) / 8);
-            prefill_merge_kernel<D><<<mg, 256, 0, st>>>(p);
+            cfg.gridDim = dim3((unsigned)(((int64_t)p.split_tail * 128 + 7) / 8), 1, 1);
+            cfg.blockDim = dim3(256, 1, 1);
+            cfg.dynamicSmemBytes = 0;
+            e = cudaLaunchKernelEx(&cfg, prefill_merge_kernel<D>, p);
             ++log.count;  // the attention kernel stays the recorded launch
-            e = cudaGetLastError();
         }
     }
     return e;

@@ -106,6 +106,9 @@ __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x) {
 // threads (256 contiguous bytes per 16 threads); chunk groups read rows with
 // the channel piece varying fastest.
 __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constant__ PrefillParams p) {
+    // the attention kernel launched behind this pass may be scheduled once
+    // every CTA has started; it waits on the device before reading the copy
+    asm volatile("griddepcontrol.launch_dependents;");
     const int D = p.D;
     const int per_block = 256 / D;
     const int t = threadIdx.x % D;
@@ -193,6 +196,51 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
     }
 }
 
+// K codes alone with no paged prefix (f16 V read in place, no smooth_v):
+// every workspace row is a chunk row, and each thread takes kStageG 16-row
+// groups, the block's 256 / D groups apart, issuing all of their loads
+// before the first conversion and store (48 registers, five CTAs per SM).
+// One group per thread left this pass latency-bound; the other forms keep
+// it, because their registers (the paged prefix's table and page loads, or
+// V as well) would cost more CTAs per SM than the batching gains.
+constexpr int kStageG = 4;
+
+__global__ void __launch_bounds__(256) prefill_stage_keys_kernel(const __grid_constant__ PrefillParams p) {
+    // the attention kernel launched behind this pass may be scheduled once
+    // every CTA has started; it waits on the device before reading the copy
+    asm volatile("griddepcontrol.launch_dependents;");
+    const int D = p.D;
+    const int per_block = 256 / D;
+    const int np = D >> 4;
+    const int t = threadIdx.x % D;
+    const int slot = t / np, dc = t % np;
+    const uint32_t gpb = (uint32_t)p.Lpad >> 4;   // 16-row groups per (b, kv head)
+    const uint32_t groups = (uint32_t)(p.B * p.Hkv) * gpb;
+    const uint32_t g0 = blockIdx.x * (uint32_t)(kStageG * per_block) + threadIdx.x / D;
+    uint4 wk[kStageG];
+    float ks[kStageG];
+#pragma unroll
+    for (int u = 0; u < kStageG; ++u) {
+        wk[u] = make_uint4(0, 0, 0, 0);
+        ks[u] = 0.0f;
+        const uint32_t g = g0 + u * per_block;
+        if (g >= groups) continue;
+        const int bh = (int)(g / gpb);
+        const int c = (int)(g % gpb) * 16 + slot;   // key row = token of the chunk
+        if (c >= p.Sk) continue;
+        wk[u] = *reinterpret_cast<const uint4 *>(p.k + ((int64_t)bh * p.Sk + c) * D + dc * 16);
+        ks[u] = p.k_scale[(int64_t)bh * p.k_groups + (c >> p.k_shift)];
+    }
+#pragma unroll
+    for (int u = 0; u < kStageG; ++u) {
+        const uint32_t g = g0 + u * per_block;
+        if (g >= groups) break;
+        const int64_t row = (int64_t)(g / gpb) * p.Lpad + (g % gpb) * 16 + slot;
+        store_f16x16(p.k_ws + row * D + dc * 16, wk[u]);
+        if (dc == 0) p.ksc_ws[row] = ks[u];
+    }
+}
+
 // Packed variable-length batch: sequence b's keys go to workspace rows
 // [r0, r0 + ceil(len / BN) * BN) of each KV head, r0 = varlen_key_row0(),
 // with zero rows after its last key up to the tile boundary.  K codes ->
@@ -200,6 +248,9 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
 // thread per 16-channel piece, the piece varying fastest along a row.
 __global__ void __launch_bounds__(256)
     prefill_stage_varlen_kernel(const __grid_constant__ PrefillParams p) {
+    // the attention kernel launched behind this pass may be scheduled once
+    // every CTA has started; it waits on the device before reading the copy
+    asm volatile("griddepcontrol.launch_dependents;");
     const int D = p.D;
     const int per_block = 256 / D;
     const int t = threadIdx.x % D;
@@ -303,6 +354,16 @@ cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, Launch
     }
     const int64_t groups = (int64_t)p.B * p.Hkv * (p.Lpad >> 4);
     const int per_block = 256 / p.D;
+    if (p.Ppad == 0 && !p.v_mean && !p.v_bf16) {
+        // group indices are 32-bit there (2^31 groups of 16 f16 rows would
+        // exceed any device's memory many times over)
+        if (groups > 0x7fffffff) return cudaErrorInvalidValue;
+        const int64_t blocks = (groups + kStageG * per_block - 1) / (kStageG * per_block);
+        if (blocks == 0) return cudaSuccess;
+        prefill_stage_keys_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+        log.add("prefill_stage_keys_kernel", dim3((unsigned)blocks), dim3(256), dim3(1, 1, 1), 0);
+        return cudaGetLastError();
+    }
     const int64_t blocks = (groups + per_block - 1) / per_block;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffff) return cudaErrorInvalidValue;

@@ -551,3 +551,43 @@ def test_prefill_random_configurations(sage, i):
                                   prefix=pre, smooth_v=c["smooth_v"])
     assert_close(f32(out), o_ref, "case %d %s" % (i, c))
     assert_close(np_(lse), l_ref, "lse case %d" % i)
+
+
+@pytest.mark.parametrize("form", ["keys_only", "prefix_bf16", "tail_split"])
+def test_prefill_back_to_back_calls_share_workspace(sage, form):
+    """Two calls on one workspace, queued with no synchronisation between
+    them: the second call's attention kernel starts while its staging pass
+    may still run, and its merge while the attention kernel may still run.
+    Each reads only after the grid ahead of it has completed, so the second
+    call gives, bit for bit, what it gives alone on a fresh workspace."""
+    D, S, Sk, Hq, Hkv, dt = {"keys_only": (128, 2048, 2048, 8, 8, "fp16"),
+                             "prefix_bf16": (128, 1024, 1024, 8, 2, "bf16"),
+                             "tail_split": (256, 512, 4096, 8, 2, "fp16")}[form]
+    P = 3000 if form == "prefix_bf16" else 0
+    calls = []
+    for seed in (71, 72):
+        qkv = W.dense_qkv(1, Hq, Hkv, S, Sk, D, seed=seed, dtype=dt, device="cuda",
+                          k_offset_std=2.0)
+        qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 128, 64, True)
+        kw = dict(causal=True, q_bias=bias, return_lse=True)
+        if P:
+            c = W.paged_cache(1, Hkv, D, [P], seed=seed + 10, device="cuda")
+            kw["prefix"] = _prefix_dict(c, P)
+        calls.append((qi, qs, ki, ks, qkv.v, kw))
+    torch.cuda.synchronize()
+    ws = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+
+    def run(i, workspace):
+        qi, qs, ki, ks, v, kw = calls[i]
+        return sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, v, workspace=workspace, **kw)
+
+    run(0, ws)
+    out, lse = run(1, ws)
+    if form == "tail_split":
+        assert sage.last_launch_info()["launches"] == 3  # staging, attention, merge
+    torch.cuda.synchronize()
+    ref, ref_lse = run(1, torch.empty(1 << 30, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert torch.equal(out, ref)
+    assert torch.equal(lse, ref_lse)

@@ -303,3 +303,33 @@ def test_varlen_many_sequences(sage, nseq):
         sel = np.concatenate([int(np_(x.cu_q)[b]) + r for b, r in enumerate(rows) if len(r)])
         assert_close(f32(out)[sel], o_ref[sel])
         assert_close(np_(lse)[:, sel], l_ref[:, sel], "lse")
+
+
+def test_varlen_back_to_back_calls_share_workspace(sage):
+    """Two packed calls on one workspace with no synchronisation between
+    them: the second call's attention kernel, launched behind its staging
+    pass, reads the staged copy only after that pass completed, so it gives
+    what it gives alone on a fresh workspace, bit for bit."""
+    lens = [1500, 300, 2600, 64, 900]
+    calls = []
+    for seed in (81, 82):
+        x = W.varlen_qkv(lens, lens, 8, 2, 128, seed=seed, device="cuda", k_offset_std=2.0)
+        qi, qs, ki, ks, bias = _quant_all(sage, x, 128, 64, True)
+        calls.append((x, qi, qs, ki, ks, bias))
+    torch.cuda.synchronize()
+    ws = torch.empty(1 << 29, dtype=torch.uint8, device="cuda")
+
+    def run(i, workspace):
+        x, qi, qs, ki, ks, bias = calls[i]
+        return sage.sage_attn_prefill_varlen(qi, qs, 128, ki, ks, 64, x.v, x.cu_q, x.cu_k,
+                                             x.max_q, x.max_k, causal=True, q_bias=bias,
+                                             return_lse=True, workspace=workspace)
+
+    run(0, ws)
+    out, lse = run(1, ws)
+    torch.cuda.synchronize()
+    ref, ref_lse = run(1, torch.empty(1 << 29, dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert torch.equal(out, ref)
+    assert torch.equal(lse, ref_lse)
