@@ -720,6 +720,7 @@ static sage_status_t run_prefill(const sage_prefill_args_t *a, void *workspace,
     char *w = static_cast<char *>(workspace);
     p.BN = L.BN, p.Ppad = L.Ppad, p.Lpad = L.Lpad, p.Vrows = L.Vrows;
     p.bundle = sage::prefill_bundle(a->B, a->Hq, p.group, L.Lpad, a->D);
+    p.q_ahead = sm_count();
     p.k_ws = reinterpret_cast<__half *>(w + L.off_k);
     p.v_ws = L.Vrows ? reinterpret_cast<__half *>(w + L.off_v) : nullptr;
     p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);
@@ -854,6 +855,7 @@ static sage_status_t run_prefill_varlen(const sage_prefill_varlen_args_t *a, voi
     p.v_st = vst, p.v_sh = vsh;
     char *w = static_cast<char *>(workspace);
     p.BN = L.BN, p.Ppad = 0, p.Lpad = L.Lpad, p.Vrows = L.Vrows;
+    p.q_ahead = sm_count();
     p.k_ws = reinterpret_cast<__half *>(w + L.off_k);
     p.v_ws = reinterpret_cast<__half *>(w + L.off_v);
     p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);

@@ -214,6 +214,9 @@ struct PrefillParams {
     // which the merge kernel combines into out and lse.
     int split_f, split_k, split_tail;
     float *part_o, *part_lse;
+    // D <= 128: CTA x prefetches into L2 the query tile of CTA x + q_ahead
+    // (one wave of one-CTA-per-SM launches ahead; 0 = no prefetch)
+    int q_ahead;
 };
 
 // How the dense prefill splits its last wave: `full` whole query tiles, then

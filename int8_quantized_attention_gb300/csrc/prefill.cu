@@ -656,6 +656,53 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             }
         }
         __syncwarp();
+    } else if (!C::WIDE && warp == kMma + 1 && p.q_ahead > 0) {
+        // ============================================================ query prefetch
+        // An otherwise idle warp asks L2 for the query tile of the CTA one
+        // wave ahead, so that CTA's query loads at its start hit L2.
+        const unsigned x = blockIdx.x + (unsigned)p.q_ahead;
+        if (x < gridDim.x) {
+            int pb, ph, pct, r0 = 0, nr = 0;
+            int64_t prow = 0;
+            if constexpr (VL) {
+                const int g = (int)(x / (unsigned)p.Hq);
+                ph = (int)(x - (unsigned)g * (unsigned)p.Hq);
+                pb = varlen_find_warp(p.B, g, [&](int k) {
+                    const int c = p.cu_q[k];
+                    return varlen_group0(c < 0 ? 0 : c, k, QR);
+                });
+                int64_t pqs = 0;
+                const int len = varlen_seq_of(p.cu_q[pb], p.cu_q[pb + 1], p.Sq, p.total_q, nullptr, &pqs);
+                const int ntile = (len + QR - 1) / QR;
+                pct = g - (int)varlen_group0(pqs, pb, QR);
+                if (pct >= 0 && pct < ntile) {
+                    r0 = (ntile - 1 - pct) * QR;
+                    nr = min(QR, len - r0);
+                    prow = (int64_t)ph * p.total_q + pqs + r0;
+                }
+            } else {
+                const int nct = (p.Sq + QR - 1) / QR;
+                const int per = nct * p.bundle;
+                const int bun = (int)x / per;
+                const int nb = min(p.bundle, p.B * p.Hq - bun * p.bundle);
+                const int rr = (int)x - bun * per;
+                pct = nct - 1 - rr / nb;
+                const int u = bun * p.bundle + rr % nb;
+                pb = u / p.Hq;
+                ph = u % p.Hq;
+                r0 = pct * QR;
+                nr = min(QR, p.Sq - r0);
+                prow = ((int64_t)pb * p.Hq + ph) * p.Sq + r0;
+            }
+            if (lane == 0 && nr > 0) {
+                // rows of a query tile are consecutive: one bulk prefetch
+                // (16-byte aligned, a multiple of 16 bytes: D is)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.q + prow * D),
+                             "r"((uint32_t)(nr * D))
+                             : "memory");
+            }
+        }
+        __syncwarp();
     }
     } else {
         if constexpr (C::NSW == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::REG_SOFTMAX));
