@@ -396,9 +396,20 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     // own row's channels (its TMEM lane).
     constexpr int QLD = D / (16 * C::SPLIT);  // 16-byte pieces per thread
     uint4 qw[QLD];
+    // dense form: the softmax thread's query scale and row bias, loaded
+    // with the query (after the query staging they held up the first key
+    // tile's softmax; the packed form loads them there, which spills less)
+    float q_sc0 = 0.0f, q_b0 = 0.0f;
     {
         const int wq = warp >> 2;
         const int ti = threadIdx.x & 127;
+        if constexpr (!VL) {
+            const int irow = i0 + (wq / C::SPLIT) * 128 + ti;
+            if (warp < kProducer && irow < Sq()) {
+                q_sc0 = __ldg(p.q_scale + q_group(irow));
+                if (p.q_bias) q_b0 = __ldg(p.q_bias + q_row(irow));
+            }
+        }
         if constexpr (C::WIDE) {
             const int iq = i0 + (wq / C::SPLIT) * 128 + ti;
             const bool ok = warp < kProducer && iq < Sq();
@@ -772,8 +783,14 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         }
         // kept strictly positive so that a masked (-inf) score stays -inf; an
         // all-zero Q row (scale 0) then scores ~1e-30 * acc = 0 as it should
-        const float rq = fmaxf(row_ok ? p.q_scale[q_group(i)] * p.qk_scale_log2 : 0.0f, 1e-30f);
-        const float bc = (row_ok && p.q_bias) ? p.q_bias[q_row(i)] * p.qk_scale_log2 : 0.0f;
+        if constexpr (VL) {
+            if (row_ok) {
+                q_sc0 = p.q_scale[q_group(i)];
+                if (p.q_bias) q_b0 = p.q_bias[q_row(i)];
+            }
+        }
+        const float rq = fmaxf(row_ok ? q_sc0 * p.qk_scale_log2 : 0.0f, 1e-30f);
+        const float bc = (row_ok && p.q_bias) ? q_b0 * p.qk_scale_log2 : 0.0f;
         const int lim = i + off;
         // K scales constant over 64-key groups (k_block >= 64, chunk keys):
         // the max runs on the raw integer scores and the scale folds into
