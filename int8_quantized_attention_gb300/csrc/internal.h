@@ -75,6 +75,9 @@ struct QuantParams {
     int64_t outer0;
     uint32_t n_outer;
     FastDiv div_inner, div_h, div_grp;
+    // dense per-block kernel: CTA x prefetches into L2 the group of CTA
+    // x + ahead (half the CTAs resident at once; 0 = no prefetch)
+    uint32_t ahead;
 };
 
 cudaError_t launch_quant(const QuantParams &p, cudaStream_t st, LaunchLog &log);

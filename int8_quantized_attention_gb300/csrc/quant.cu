@@ -357,8 +357,30 @@ __device__ __forceinline__ void quant_block_any(const QuantParams &p, const T *b
         quant_block<T>(p, base, msub, mbias, t0, t1, orow0, sidx);
 }
 
+// Group of CTA x of the dense per-block launch into L2 (rows contiguous:
+// one bulk request; strided rows are not prefetched).  Each CTA loads its
+// group at its start; asking L2 for the group of the CTA half a wave of
+// resident CTAs ahead turns those later loads from DRAM misses into L2
+// hits (half a wave measured best: Q 109 to 101 us, K mean + quantisation
+// 178 to 175 us on 268 MB tensors; one and two waves gained less).
+template <typename T>
+__device__ __forceinline__ void prefetch_group(const QuantParams &p, uint32_t x) {
+    if (x >= gridDim.x || p.ss != p.D) return;
+    const uint32_t bh = p.div_inner.div(x);
+    const uint32_t g = x - bh * p.div_inner.d;
+    const uint32_t b = p.div_h.div(bh);
+    const uint32_t h = bh - b * (uint32_t)p.H;
+    const int64_t t0 = (int64_t)g * p.block;
+    const int64_t t1 = (t0 + p.block < (int64_t)p.S) ? t0 + p.block : (int64_t)p.S;
+    const T *src = reinterpret_cast<const T *>(p.x) + b * p.sb + h * p.sh + t0 * p.D;
+    const uint32_t bytes = (uint32_t)((t1 - t0) * p.D * (int64_t)sizeof(T));
+    if (t1 > t0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 template <typename T, int IT>
 __global__ void __launch_bounds__(1024) quant_blocks_kernel(QuantParams p) {
+    if (threadIdx.x == 0 && p.ahead > 0) prefetch_group<T>(p, blockIdx.x + p.ahead);
     const int tpr = p.D / 8;
     // CTA = (b * H + h) * ngroups + g, split by invariant-divisor constants
     const uint32_t ngroups = p.div_inner.d;
@@ -617,13 +639,31 @@ inline unsigned block_threads(int block, int D) {
     return t <= 1024 ? (unsigned)(t < 32 ? 32 : t) : 0u;
 }
 
+// CTAs of `kernel` resident on the whole device at `threads` per CTA (0 if
+// the query fails)
+template <typename K>
+uint32_t resident_ctas(K kernel, unsigned threads) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, (int)threads, 0) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return (uint32_t)(sms * per_sm);
+}
+
 template <typename T>
-unsigned launch_blocks(const QuantParams &q, unsigned grid, cudaStream_t st, bool varlen) {
+unsigned launch_blocks(const QuantParams &p, unsigned grid, cudaStream_t st, bool varlen) {
+    QuantParams q = p;
     const unsigned threads = block_threads(q.block, q.D);
-    if (threads)
+    if (threads) {
+        if (!varlen) q.ahead = resident_ctas(quant_blocks_kernel<T, kBlockRows>, threads) / 2;
         launch_blocks_it<T, kBlockRows>(q, grid, threads, st, varlen);
-    else
+    } else {
+        if (!varlen) q.ahead = resident_ctas(quant_blocks_kernel<T, 0>, 256) / 2;
         launch_blocks_it<T, 0>(q, grid, 256, st, varlen);
+    }
     return threads ? threads : 256;
 }
 
