@@ -199,13 +199,17 @@ __global__ void __launch_bounds__(256) prefill_stage_kernel(const __grid_constan
 // K codes alone with no paged prefix (f16 V read in place, no smooth_v):
 // every workspace row is a chunk row, and each thread takes kStageG 16-row
 // groups, the block's 256 / D groups apart, issuing all of their loads
-// before the first conversion and store (48 registers, five CTAs per SM).
+// before the first conversion and store (46 registers, five CTAs per SM),
+// and asks L2 for the key codes of the CTA half a wave of resident CTAs
+// ahead (capping the registers for a sixth CTA per SM spilled and gained
+// less).
 // One group per thread left this pass latency-bound; the other forms keep
 // it, because their registers (the paged prefix's table and page loads, or
 // V as well) would cost more CTAs per SM than the batching gains.
 constexpr int kStageG = 4;
 
-__global__ void __launch_bounds__(256) prefill_stage_keys_kernel(const __grid_constant__ PrefillParams p) {
+__global__ void __launch_bounds__(256) prefill_stage_keys_kernel(const __grid_constant__ PrefillParams p,
+                                                                 uint32_t ahead) {
     // the attention kernel launched behind this pass may be scheduled once
     // every CTA has started; it waits on the device before reading the copy
     asm volatile("griddepcontrol.launch_dependents;");
@@ -217,6 +221,22 @@ __global__ void __launch_bounds__(256) prefill_stage_keys_kernel(const __grid_co
     const uint32_t gpb = (uint32_t)p.Lpad >> 4;   // 16-row groups per (b, kv head)
     const uint32_t groups = (uint32_t)(p.B * p.Hkv) * gpb;
     const uint32_t g0 = blockIdx.x * (uint32_t)(kStageG * per_block) + threadIdx.x / D;
+    if (threadIdx.x == 0 && ahead > 0) {
+        // the key codes of the CTA `ahead` CTAs on (within its first
+        // (b, kv head)) into L2, so that its loads at its start hit L2
+        const uint32_t x = blockIdx.x + ahead;
+        const uint32_t gx = x * (uint32_t)(kStageG * per_block);
+        if (x < gridDim.x && gx < groups) {
+            const uint32_t bh = gx / gpb;
+            const int c0 = (int)(gx % gpb) * 16;
+            const int c1 = min(c0 + kStageG * 256 / (D >> 4), p.Sk);
+            if (c1 > c0)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                 p.k + ((int64_t)bh * p.Sk + c0) * D),
+                             "r"((uint32_t)((c1 - c0) * D))
+                             : "memory");
+        }
+    }
     uint4 wk[kStageG];
     float ks[kStageG];
 #pragma unroll
@@ -360,7 +380,17 @@ cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, Launch
         if (groups > 0x7fffffff) return cudaErrorInvalidValue;
         const int64_t blocks = (groups + kStageG * per_block - 1) / (kStageG * per_block);
         if (blocks == 0) return cudaSuccess;
-        prefill_stage_keys_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+        // prefetch distance: half the CTAs resident at once
+        int dev = 0, sms = 0, per_sm = 0;
+        uint32_t ahead = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess &&
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, prefill_stage_keys_kernel, 256, 0) ==
+                cudaSuccess)
+            ahead = (uint32_t)(sms * per_sm / 2);
+        else
+            cudaGetLastError();
+        prefill_stage_keys_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, ahead);
         log.add("prefill_stage_keys_kernel", dim3((unsigned)blocks), dim3(256), dim3(1, 1, 1), 0);
         return cudaGetLastError();
     }
