@@ -105,7 +105,10 @@ sage_status_t sage_quant_int8(const void *x, sage_dtype_t dtype, int B, int H, i
  * non-decreasing, cu_seqlens[B] <= total, each length <= the caller's
  * max_seqlen).  Packed tokens outside every sequence are not read or
  * written.  A sequence that breaks these rules sets the bad-block bit of
- * the device error word and is treated as empty.
+ * the device error word and is treated as empty; where cu_seqlens
+ * decreases, the kernels' searches over it may misplace the other
+ * sequences' tiles too, so their results are then unspecified (nothing is
+ * read or written outside the tensors).
  *
  * Scale groups: per token (block_tokens == 1) group = packed token; per
  * block, sequence b's groups start at cu_seqlens[b] / block_tokens + b and

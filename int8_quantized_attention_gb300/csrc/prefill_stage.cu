@@ -267,22 +267,32 @@ __global__ void __launch_bounds__(256) prefill_stage_keys_kernel(const __grid_co
 // exact f16, V (f16 copied, bf16 rounded) -> f16, one K scale per key.  One
 // thread per 16-channel piece, the piece varying fastest along a row.
 __global__ void __launch_bounds__(256)
-    prefill_stage_varlen_kernel(const __grid_constant__ PrefillParams p) {
+    prefill_stage_varlen_kernel(const __grid_constant__ PrefillParams p, uint32_t nslot) {
     // the attention kernel launched behind this pass may be scheduled once
     // every CTA has started; it waits on the device before reading the copy
     asm volatile("griddepcontrol.launch_dependents;");
     const int D = p.D;
     const int per_block = 256 / D;
     const int t = threadIdx.x % D;
-    const int gps = (p.Sk + p.BN - 1) / p.BN * p.BN / 16;   // 16-row groups per sequence
-    const int64_t g = (int64_t)blockIdx.x * per_block + threadIdx.x / D;
-    if (g >= (int64_t)p.B * p.Hkv * gps) return;
-    const int bh = (int)(g / gps);
-    const int row0 = (int)(g % gps) * 16;
-    const int b = bh / p.Hkv, kvh = bh % p.Hkv;
+    // compact 16-row group slots per kv head: sequence b owns the slots from
+    // cu_k[b] / 16 + b * (BN / 16 + 1) on, at least ceil(len_b / BN) * BN / 16
+    // of them (a grid of B x the longest sequence's groups left most CTAs
+    // empty).  A warp lies inside one group (D >= 64 threads per group), so
+    // its lanes find the group's sequence together.
+    const uint32_t g = blockIdx.x * (uint32_t)per_block + threadIdx.x / D;
+    if (g >= (uint32_t)p.Hkv * nslot) return;
+    const int kvh = (int)(g / nslot);
+    const int64_t gs = g - (uint32_t)kvh * nslot;   // the group's slot
+    const int spare = p.BN / 16 + 1;
+    const int b = varlen_find_warp(p.B, gs, [&](int k) {
+        const int c = p.cu_k[k];
+        return (int64_t)(c < 0 ? 0 : c) / 16 + (int64_t)k * spare;
+    });
     int64_t ks = 0;
     const int len = varlen_seq(p.cu_k, b, p.Sk, p.total_k, nullptr, &ks);
-    if (row0 >= (len + p.BN - 1) / p.BN * p.BN) return;
+    const int64_t j = gs - (ks / 16 + (int64_t)b * spare);
+    if (len == 0 || j < 0 || j * 16 >= (len + p.BN - 1) / p.BN * p.BN) return;
+    const int row0 = (int)j * 16;
     const int np = D >> 4;
     const int slot = t / np, dc = t % np;
     const int row = row0 + slot;
@@ -362,13 +372,14 @@ PrefillLayout prefill_layout_varlen(int B, int Hkv, int64_t total_k, int D, bool
 
 cudaError_t launch_prefill_stage(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     if (p.cu_q) {
-        const int gps = (p.Sk + p.BN - 1) / p.BN * p.BN / 16;
-        const int64_t groups = (int64_t)p.B * p.Hkv * gps;
+        // group slots per kv head: total_k / 16, plus BN / 16 + 1 per sequence
+        const int64_t nslot = p.total_k / 16 + (int64_t)p.B * (p.BN / 16 + 1);
+        const int64_t groups = (int64_t)p.Hkv * nslot;
         const int per_block = 256 / p.D;
         const int64_t blocks = (groups + per_block - 1) / per_block;
         if (blocks == 0) return cudaSuccess;
-        if (blocks > 0x7fffffff) return cudaErrorInvalidValue;
-        prefill_stage_varlen_kernel<<<(unsigned)blocks, 256, 0, st>>>(p);
+        if (groups > 0x7fffffff) return cudaErrorInvalidValue;
+        prefill_stage_varlen_kernel<<<(unsigned)blocks, 256, 0, st>>>(p, (uint32_t)nslot);
         log.add("prefill_stage_varlen_kernel", dim3((unsigned)blocks), dim3(256), dim3(1, 1, 1), 0);
         return cudaGetLastError();
     }
