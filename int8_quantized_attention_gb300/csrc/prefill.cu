@@ -712,6 +712,23 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                              "r"((uint32_t)(nr * D))
                              : "memory");
             }
+            // dense form: the tile's row biases and scales too, one 128-byte
+            // line per lane, every address inside the rows' range (in the
+            // packed form the extra code made the softmax spill more and
+            // the varlen launch 2.6 % slower)
+            if constexpr (!VL) {
+                auto lines = [&](const float *a, int n) {
+                    if (n > 0 && lane <= (n + 31) / 32) {
+                        const float *x = a + min(32 * lane, n - 1);
+                        asm volatile("prefetch.global.L2 [%0];" ::"l"(x) : "memory");
+                    }
+                };
+                if (nr > 0) {
+                    if (p.q_bias) lines(p.q_bias + prow, nr);
+                    const int g0 = r0 >> p.q_shift, g1 = (r0 + nr - 1) >> p.q_shift;
+                    lines(p.q_scale + ((int64_t)pb * p.Hq + ph) * p.q_groups + g0, g1 - g0 + 1);
+                }
+            }
         }
         __syncwarp();
     }
