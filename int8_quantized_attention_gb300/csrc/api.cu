@@ -856,6 +856,7 @@ static sage_status_t run_prefill_varlen(const sage_prefill_varlen_args_t *a, voi
     char *w = static_cast<char *>(workspace);
     p.BN = L.BN, p.Ppad = 0, p.Lpad = L.Lpad, p.Vrows = L.Vrows;
     p.q_ahead = sm_count();
+    p.vl_pairs = a->D <= 128 && p.group % 2 == 0;
     p.k_ws = reinterpret_cast<__half *>(w + L.off_k);
     p.v_ws = reinterpret_cast<__half *>(w + L.off_v);
     p.ksc_ws = reinterpret_cast<float *>(w + L.off_ksc);

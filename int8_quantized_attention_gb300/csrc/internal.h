@@ -220,6 +220,10 @@ struct PrefillParams {
     // D <= 128: CTA x prefetches into L2 the query tile of CTA x + q_ahead
     // (one wave of one-CTA-per-SM launches ahead; 0 = no prefetch)
     int q_ahead;
+    // packed form, D <= 128, even GQA group: a CTA takes 128 query rows of
+    // two heads sharing a KV head (query tile t = head 2u + t) instead of
+    // 256 rows of one head; the grid has (total_q / 128 + B) * Hq / 2 CTAs
+    int vl_pairs;
 };
 
 // How the dense prefill splits its last wave: `full` whole query tiles, then

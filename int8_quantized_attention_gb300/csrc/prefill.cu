@@ -223,7 +223,7 @@ __device__ __forceinline__ int split_item(const PrefillParams &p, int L, int &pa
 
 // VL: a packed variable-length batch (rows and keys located through
 // cu_seqlens); the dense instantiation keeps its addressing in closed form.
-template <int D, bool VL>
+template <int D, bool VL, bool PR = false>
 __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     prefill_kernel(const __grid_constant__ PrefillParams p,
                    const __grid_constant__ PrefillMaps maps) {
@@ -244,7 +244,22 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
     int b, hq, ct;
     int part = -1;  // dense form, D = 256: this CTA's part of a split query tile
     int cq0 = 0, cq1 = 0, ck0 = 0, ck1 = 0;  // packed batch: this sequence's offsets
-    if constexpr (VL) {
+    // PR (packed form, even GQA group): a CTA takes 128 query rows of two
+    // heads that share a KV head -- query tile t is head hq + t -- instead
+    // of 256 rows of one head, so a sequence's last CTA is not half empty
+    // and the first tile does not sweep the second tile's diagonal key tile
+    // fully masked.  Every other instantiation keeps the code below as is.
+    static_assert(!PR || (VL && NQ == 2), "head pairs: packed form, two query tiles");
+    if constexpr (PR) {
+        const int g = (int)(blockIdx.x / (unsigned)(p.Hq / 2));
+        hq = 2 * (int)(blockIdx.x - (unsigned)g * (unsigned)(p.Hq / 2));
+        b = varlen_find_warp(p.B, g, [&](int k) {
+            const int c = p.cu_q[k];
+            return varlen_group0(c < 0 ? 0 : c, k, 128);
+        });
+        cq0 = p.cu_q[b], cq1 = p.cu_q[b + 1], ck0 = p.cu_k[b], ck1 = p.cu_k[b + 1];
+        ct = g - (int)varlen_group0(cq0 < 0 ? 0 : cq0, b, 128);  // reversed below
+    } else if constexpr (VL) {
         // one linear index, heads fastest: the CTAs of a tile slot for every
         // head start together, and the grid ends on the light (first) tiles
         // of the last sequence instead of on one head's heaviest tiles
@@ -296,7 +311,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         int64_t ks = 0;
         vsq = varlen_seq_of(cq0, cq1, p.Sq, p.total_q, e, &qs);
         vsk = varlen_seq_of(ck0, ck1, p.Sk, p.total_k, e, &ks);
-        const int ntile = (vsq + QR - 1) / QR;
+        const int ntile = (vsq + (PR ? 128 : QR) - 1) / (PR ? 128 : QR);
         // a spare slot, a slot before the first sequence, or an empty or
         // invalid sequence: nothing to do (the whole CTA returns)
         if (ct < 0 || ct >= ntile) return;
@@ -354,7 +369,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         const int64_t bb = u / p.Hq, kv = (u % p.Hq) / p.group;
         return p.v_mean + (bb * p.Hkv + kv) * D;
     };
-    const int i0 = ct * QR;
+    const int i0 = ct * (PR ? 128 : QR);
 
     // ------------------------------------------------------ tile schedule
     int P = 0;
@@ -366,7 +381,7 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         }
     }
     const int off = P + Sk() - Sq();  // key j visible to row i iff j <= i + off (causal)
-    const int row_last = min(i0 + 128 * NQ - 1, Sq() - 1);
+    const int row_last = min(i0 + (PR ? 128 : 128 * NQ) - 1, Sq() - 1);
     const int kmax = p.causal ? row_last + off : P + Sk() - 1;
     int n_pre = 0, n_ch = 0;
     if (kmax >= 0) {
@@ -419,9 +434,10 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 qw[k] = ok ? __ldg(reinterpret_cast<const uint4 *>(src) + k) : make_uint4(0, 0, 0, 0);
         } else {
             static_assert(C::WIDE || C::SPLIT == 1, "a shared-memory Q tile belongs to one warpgroup");
-            const int row0 = i0 + wq * 128;
+            const int row0 = i0 + (PR ? 0 : wq * 128);
             const bool sm_thread = warp < kProducer;
-            const int8_t *src = p.q + (sm_thread && row0 < Sq() ? q_row(row0) * D : 0);
+            const int64_t qoff = PR ? (int64_t)wq * p.total_q : 0;  // PR: tile wq is head hq + wq
+            const int8_t *src = p.q + (sm_thread && row0 < Sq() ? (q_row(row0) + qoff) * D : 0);
 #pragma unroll
             for (int m = 0; m < QLD; ++m) {
                 const int u = ti + 128 * m;
@@ -676,19 +692,21 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
             int pb, ph, pct, r0 = 0, nr = 0;
             int64_t prow = 0;
             if constexpr (VL) {
-                const int g = (int)(x / (unsigned)p.Hq);
-                ph = (int)(x - (unsigned)g * (unsigned)p.Hq);
+                constexpr int QV = PR ? 128 : QR;    // rows per CTA
+                constexpr unsigned HC = PR ? 2 : 1;  // heads per CTA
+                const int g = (int)(x / ((unsigned)p.Hq / HC));
+                ph = (int)(x - (unsigned)g * ((unsigned)p.Hq / HC)) * HC;
                 pb = varlen_find_warp(p.B, g, [&](int k) {
                     const int c = p.cu_q[k];
-                    return varlen_group0(c < 0 ? 0 : c, k, QR);
+                    return varlen_group0(c < 0 ? 0 : c, k, QV);
                 });
                 int64_t pqs = 0;
                 const int len = varlen_seq_of(p.cu_q[pb], p.cu_q[pb + 1], p.Sq, p.total_q, nullptr, &pqs);
-                const int ntile = (len + QR - 1) / QR;
-                pct = g - (int)varlen_group0(pqs, pb, QR);
+                const int ntile = (len + QV - 1) / QV;
+                pct = g - (int)varlen_group0(pqs, pb, QV);
                 if (pct >= 0 && pct < ntile) {
-                    r0 = (ntile - 1 - pct) * QR;
-                    nr = min(QR, len - r0);
+                    r0 = (ntile - 1 - pct) * QV;
+                    nr = min(QV, len - r0);
                     prow = (int64_t)ph * p.total_q + pqs + r0;
                 }
             } else {
@@ -711,6 +729,14 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
                 asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.q + prow * D),
                              "r"((uint32_t)(nr * D))
                              : "memory");
+            }
+            if constexpr (PR) {
+                // the pair's second head
+                if (lane == 1 && nr > 0)
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                     p.q + (prow + p.total_q) * D),
+                                 "r"((uint32_t)(nr * D))
+                                 : "memory");
             }
             // dense form: the tile's row biases and scales too, one 128-byte
             // line per lane, every address inside the rows' range (in the
@@ -741,7 +767,13 @@ __global__ void __launch_bounds__(PCfg<D>::THREADS, 1)
         const int hc = wg % SPLIT;             // which part of the row's columns
         const int c0 = hc * CW;                // first S column of this thread
         const int r = threadIdx.x & 127;       // row within the tile = TMEM lane
-        const int i_first = i0 + t * 128;
+        const int i_first = i0 + (PR ? 0 : t * 128);
+        if constexpr (PR) {
+            // this warpgroup's head: every row address below follows it
+            hq += t;
+            vq_row0 += (int64_t)t * p.total_q;
+            vsc0 += (int64_t)t * p.q_groups;
+        }
         const int i = i_first + r;
         const bool row_ok = i < Sq();
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -1256,7 +1288,7 @@ bool make_map(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t bh) {
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D, bool VL>
+template <int D, bool VL, bool PR = false>
 cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     using C = PCfg<D>;
     if (p.BN != C::BN) return cudaErrorInvalidValue;
@@ -1277,13 +1309,16 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
             return cudaErrorInvalidValue;
         }
     }
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VL>,
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, VL, PR>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     // packed batches: one CTA per (compact tile slot, head) -- ceil(len_b /
     // QR) slots per sequence, at most total_q / QR + B -- heads fastest
     constexpr int QR = 128 * C::NQ;
-    const int64_t vl_ctas = VL ? (p.total_q / QR + p.B) * (int64_t)p.Hq : 0;
+    // PR: 128 rows of two heads (sharing a KV head) per CTA
+    if (PR && (p.group % 2 != 0 || p.Hq % 2 != 0)) return cudaErrorInvalidValue;
+    const int64_t vl_ctas =
+        VL ? (p.total_q / (PR ? 128 : QR) + p.B) * (int64_t)(PR ? p.Hq / 2 : p.Hq) : 0;
     if (vl_ctas > 0x7fffffff) return cudaErrorInvalidValue;
     // dense form at D = 256: CTAs of whole query tiles, then the split tail's parts
     const int64_t dense_ctas = (int64_t)(p.Sq + QR - 1) / QR * p.Hq * p.B;
@@ -1313,7 +1348,7 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
     cfg.stream = st;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D, VL>, p, m);
+    e = cudaLaunchKernelEx(&cfg, prefill_kernel<D, VL, PR>, p, m);
     log.add(VL ? "prefill_varlen_kernel" : "prefill_kernel", grid, dim3(C::THREADS), dim3(1, 1, 1),
             C::SMEM);
     if constexpr (!VL && C::WIDE) {
@@ -1330,7 +1365,11 @@ cudaError_t launch_dv(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
 
 template <int D>
 cudaError_t launch_d(const PrefillParams &p, cudaStream_t st, LaunchLog &log) {
-    return p.cu_q ? launch_dv<D, true>(p, st, log) : launch_dv<D, false>(p, st, log);
+    if (!p.cu_q) return launch_dv<D, false>(p, st, log);
+    if constexpr (PCfg<D>::NQ == 2) {
+        if (p.vl_pairs) return launch_dv<D, true, true>(p, st, log);
+    }
+    return p.vl_pairs ? cudaErrorInvalidValue : launch_dv<D, true>(p, st, log);
 }
 
 }  // namespace

@@ -183,11 +183,15 @@ def test_varlen_raw_scores_bit_exact(sage, D):
 
 @pytest.mark.parametrize("D", [128, 256])
 @pytest.mark.parametrize("vdt", ["fp16", "bf16"])
-def test_varlen_equals_dense_per_sequence(sage, D, vdt):
+@pytest.mark.parametrize("heads", [(4, 2), (3, 3)])
+def test_varlen_equals_dense_per_sequence(sage, D, vdt, heads):
     """One packed launch gives, bit for bit, what the dense kernel gives on
-    each sequence alone (the README's per-batch loop)."""
+    each sequence alone (the README's per-batch loop).  With an even GQA
+    group a D <= 128 launch takes 128 rows of two heads per CTA, otherwise
+    256 rows of one head: both layouts are covered."""
     lq, lk = [300, 77, 129], [300, 200, 129]
-    x = W.varlen_qkv(lq, lk, 4, 2, D, seed=D + 17, device="cuda", v_dtype=vdt, k_offset_std=2.0)
+    x = W.varlen_qkv(lq, lk, heads[0], heads[1], D, seed=D + 17, device="cuda", v_dtype=vdt,
+                     k_offset_std=2.0)
     qi, qs, ki, ks, bias = _quant_all(sage, x, 128, 64, True)
     out, lse = sage.sage_attn_prefill_varlen(qi, qs, 128, ki, ks, 64, x.v, x.cu_q, x.cu_k,
                                              x.max_q, x.max_k, causal=True, q_bias=bias,
