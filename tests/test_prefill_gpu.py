@@ -591,3 +591,50 @@ def test_prefill_back_to_back_calls_share_workspace(sage, form):
     assert sage.check_device_status()[0] == 0
     assert torch.equal(out, ref)
     assert torch.equal(lse, ref_lse)
+
+
+@pytest.mark.parametrize("form", ["dense", "tail_split", "varlen_pairs"])
+def test_prefill_captured_in_a_cuda_graph(sage, form):
+    """A prefill call captured into a CUDA graph and replayed gives, bit for
+    bit, the eager call's output and LSE: the staging pass, the attention
+    kernel launched as its programmatic dependent, and (tail split) the
+    merge launched behind that, all inside one graph."""
+    stream = torch.cuda.Stream()
+    ws = torch.empty(1 << 29, dtype=torch.uint8, device="cuda")
+    if form == "varlen_pairs":
+        lens = [700, 130, 1500]
+        x = W.varlen_qkv(lens, lens, 8, 2, 128, seed=91, device="cuda", k_offset_std=2.0)
+        qi, qs, _, _ = sage.sage_quant_int8_varlen(x.q, x.cu_q, x.max_q, block_tokens=128)
+        ki, ks, mu, _ = sage.sage_quant_int8_varlen(x.k, x.cu_k, x.max_k, block_tokens=64,
+                                                    smooth=True)
+        _, _, _, bias = sage.sage_quant_int8_varlen(x.q, x.cu_q, x.max_q, block_tokens=128,
+                                                    mu_in=mu)
+
+        def call():
+            return sage.sage_attn_prefill_varlen(qi, qs, 128, ki, ks, 64, x.v, x.cu_q, x.cu_k,
+                                                 x.max_q, x.max_k, causal=True, q_bias=bias,
+                                                 return_lse=True, workspace=ws, stream=stream)
+    else:
+        D, S, Sk = (128, 1024, 1024) if form == "dense" else (256, 512, 4096)
+        qkv = W.dense_qkv(1, 8, 2, S, Sk, D, seed=92, device="cuda", k_offset_std=2.0)
+        qi, qs, ki, ks, mu, bias = _quant(sage, qkv, 128, 64, True)
+
+        def call():
+            return sage.sage_attn_prefill(qi, qs, 128, ki, ks, 64, qkv.v, causal=True,
+                                          q_bias=bias, return_lse=True, workspace=ws,
+                                          stream=stream)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        ref, ref_lse = call()
+        ref, ref_lse = ref.clone(), ref_lse.clone()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        out, lse = call()
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    assert torch.equal(out, ref)
+    assert torch.equal(lse, ref_lse)
