@@ -1402,7 +1402,7 @@ PrefillSplit prefill_split(int B, int Hq, int Sq, int D, int keys, bool causal, 
 }
 
 int prefill_bundle(int B, int Hq, int group, int rows, int D) {
-    constexpr double kL2Share = 48.0 * 1024 * 1024;  // of the 126 MB L2
+    constexpr double kL2Share = 32.0 * 1024 * 1024;  // of the 126 MB L2 (16-96 MB swept)
     const double kv = (double)rows * D * 2 * 2;       // f16 K and V of one KV head
     int kvh = kv > 0 ? (int)(kL2Share / kv) : 1;
     kvh = kvh < 1 ? 1 : kvh;
