@@ -337,3 +337,25 @@ def test_varlen_back_to_back_calls_share_workspace(sage):
     assert sage.check_device_status()[0] == 0
     assert torch.equal(out, ref)
     assert torch.equal(lse, ref_lse)
+
+
+@pytest.mark.parametrize("heads", [(8, 2), (6, 6), (3, 1)])
+def test_varlen_launch_layout(sage, heads):
+    """D = 128 packed launches: with an even GQA group a CTA takes 128 query
+    rows of two heads sharing a KV head, (total_q / 128 + B) * Hq / 2 CTAs;
+    otherwise 256 rows of one head, (total_q / 256 + B) * Hq CTAs.  Both
+    give the per-sequence dense result (tested above); this pins which one
+    runs."""
+    Hq, Hkv = heads
+    lens = [300, 1000, 77]
+    x = W.varlen_qkv(lens, lens, Hq, Hkv, 128, seed=Hq + 7 * Hkv, device="cuda")
+    qi, qs, ki, ks, _ = _quant_all(sage, x, 128, 64, False)
+    sage.sage_attn_prefill_varlen(qi, qs, 128, ki, ks, 64, x.v, x.cu_q, x.cu_k, x.max_q, x.max_k,
+                                  causal=True)
+    info = sage.last_launch_info()
+    torch.cuda.synchronize()
+    assert sage.check_device_status()[0] == 0
+    total, B = sum(lens), len(lens)
+    want = (total // 128 + B) * (Hq // 2) if (Hq // Hkv) % 2 == 0 else (total // 256 + B) * Hq
+    assert info["kernel"] == "prefill_varlen_kernel"
+    assert info["grid"] == (want, 1, 1)
